@@ -1,0 +1,383 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA backward pass on GB300.
+
+One step = one full backward (kda_bwd with the chunk states recomputed inside:
+forward-state scan + reverse dS scan, per-chunk gradients, dA_log reduction)
+over one batch of the main workload, B=4 T=8192 H=32 K=V=128 bf16, inputs
+already resident in HBM.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs as one process per GPU under torchrun: every rank processes its
+own batch (independent problems, no collective on the data path), the
+reported time is the max over ranks and the value counts the tokens of all
+ranks ("weak" scaling).  `--impl reference` times the fp64 CPU oracle (the
+only reference there is for this path) on a bounded sample of the same
+workload, on the host cores, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA backward tokens/s on 1×GB300 and % of bf16-TC/HBM roofline; vs CPU oracle"
+WORKLOAD = "main_bf16"
+
+# Algorithmic HBM bytes per (token, head) for K = V = 128, bf16:
+#   gradient kernel: reads q, k, v, dO, g (5 x 256 B), beta (2 B), the chunk
+#   state S_n and state gradient dS_{n+1} (2 x 32 KiB per 64 tokens = 1024 B);
+#   writes dq, dk, dv, dg (4 x 256 B) and dbeta (2 B)            -> 3332 B
+#   scan kernel: forward role reads k, v, g, beta (770 B) and writes S_n
+#   (512 B); reverse role reads q, k, g, beta, dO (1026 B) and writes
+#   dS_{n+1} (512 B)                                              -> 2820 B
+ALG_BYTES = {"grads": 3332, "scan": 2820}
+# Dense-equivalent FLOP per (token, head), K = V = 128 (chunk 64).
+ALG_FLOP = {"grads": 22.0e6 / 64, "scan": 17.0e6 / 64}
+KERNEL_NAMES = {"scan": "kda_scan_kernel", "grads": "kda_grads_kernel",
+                "reduce": "kda_dalog_reduce_kernel"}
+
+# DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum)
+# on the main workload, keyed by the hash of the kernel sources it was taken
+# from; a changed kernel reports null until it is measured again.
+NCU_TRAFFIC = {}
+
+KERNEL_SOURCES = {
+    "grads": ["kda_grads.cu", "kda_chunk.cuh", "kda_device.cuh"],
+    "scan": ["kda_scan.cu", "kda_chunk.cuh", "kda_device.cuh"],
+}
+
+
+def src_hash(kernel):
+    h = hashlib.sha256()
+    for fn in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "linear_attention_backward_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_sample(x, n_units, t_sample, nthreads):
+    """Run the fp64 oracle on n_units (sequence, head) units, each the first
+    t_sample tokens of its sequence; returns seconds."""
+    import numpy as np
+    import oracle
+    B, T, H, K = x["q"].shape
+    units = [(u % B, (u * 7) % H) for u in range(n_units)]
+    t_sample = min(t_sample, T)
+    pick = lambda t, b, h: t[b, :t_sample, h:h + 1].double().numpy()
+    cat = lambda name: np.concatenate([pick(x[name], b, h) for b, h in units], 0)
+    q, k, v, g, dO = (cat(n) for n in ("q", "k", "v", "g", "dO"))
+    beta = np.concatenate([x["beta"][b, :t_sample, h:h + 1].double().numpy()
+                           for b, h in units], 0)
+    # per-unit A_log differs; a one-head batch shares A_log, so take the mean
+    # head's value: the oracle's cost does not depend on it
+    A_log = x["A_log"][:1].double().numpy()
+    cu = [i * t_sample for i in range(n_units + 1)]
+    h0 = x["h0"][:1, :1].double().numpy().repeat(n_units, 0)
+    dhT = x["dhT"][:1, :1].double().numpy().repeat(n_units, 0)
+    t0 = time.perf_counter()
+    oracle.backward(q, k, v, g, beta, A_log, h0, dO, dhT, cu_seqlens=cu, nthreads=nthreads)
+    return time.perf_counter() - t0, n_units * t_sample
+
+
+def cpu_baseline(x, steps=1):
+    cores = os.cpu_count() or 1
+    n_units = cores
+    t_sample = 2048
+    H = x["q"].shape[2]
+    times = []
+    head_tokens = 0
+    for _ in range(steps):
+        dt, head_tokens = oracle_sample(x, n_units, t_sample, cores)
+        times.append(dt)
+    sec = statistics.median(times)
+    return {"value": (head_tokens / H) / sec, "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n_units} (sequence, head) units x first {t_sample} tokens of the "
+                      f"{WORKLOAD} workload (= {head_tokens} head-tokens), fp64, "
+                      f"{cores} OpenMP threads; tokens = head-tokens / H",
+            "seconds": sec}
+
+
+def run_reference(args, ws, rank):
+    import oracle
+    from linear_attention_backward_gb300 import workloads as wl
+    if rank != 0:
+        return 0
+    oracle.build()
+    x = wl.make_inputs(wl.WORKLOADS[WORKLOAD], seed=0)
+    w = wl.WORKLOADS[WORKLOAD]
+    for _ in range(args.warmup):
+        oracle_sample(x, 1, 256, 1)
+    cores = os.cpu_count() or 1
+    t_sample = 1024
+    t_all = 0.0
+    ht = 0
+    for _ in range(args.steps):
+        dt, n = oracle_sample(x, cores, t_sample, cores)
+        t_all += dt
+        ht += n
+    value = (ht / w.H) / t_all
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_all / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {cores} (sequence, head) units x first "
+                                   f"{t_sample} tokens, fp64, {cores} threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: KDA chunked backward, B={w.B} T={w.T} H={w.H} "
+                        f"K={w.K} V={w.V} chunk={w.chunk}, states recomputed in the call",
+            "global_batch": w.B, "seq_len": w.T, "heads": w.H, "head_dim": w.K,
+            "parallelism": "replicas (one independent batch per GPU)",
+            "l2": "inputs larger than L2 (268 MB per input tensor), no flush"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import linear_attention_backward_gb300 as kda
+    from linear_attention_backward_gb300 import workloads as wl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    w = wl.WORKLOADS[WORKLOAD]
+    xh = wl.make_inputs(w, seed=rank)
+    names_in = ["q", "k", "v", "g", "beta", "dO", "A_log"]
+    if w.with_h0:
+        names_in.append("h0")
+    if w.with_dhT:
+        names_in.append("dhT")
+    d = {n: xh[n].to(dev) for n in names_in}
+    h0 = d.get("h0")
+    dhT = d.get("dhT")
+    shape = kda.make_shape(d["q"], d["v"])
+    wsb = torch.empty((kda.workspace_bytes(shape),), dtype=torch.uint8, device=dev)
+    out = {n: torch.empty_like(d[m]) for n, m in
+           (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
+    out["dA_log"] = torch.empty((w.H,), dtype=torch.float32, device=dev)
+    out["dh0"] = torch.empty((w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+
+    def step(events=None):
+        kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], h0, d["dO"], dhT,
+                out=out, workspace=wsb, events=events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert kda.get_device_status() == 0
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e4 in evs:  # materialise the events (created lazily by torch)
+        for e in e4:
+            e.record()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local])
+    sampler.start()
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(K):
+        step(evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if pg:
+        pg.barrier()
+    ms = start.elapsed_time(end)
+    phase = {"scan": [], "grads": [], "reduce": []}
+    for e4 in evs:
+        phase["scan"].append(e4[0].elapsed_time(e4[1]))
+        phase["grads"].append(e4[1].elapsed_time(e4[2]))
+        phase["reduce"].append(e4[2].elapsed_time(e4[3]))
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / K
+    tokens = w.B * w.T
+    value = tokens * ws / (ms_step * 1e-3)
+    assert kda.get_device_status() == 0
+
+    # ---- end to end through the public API with host buffers ----
+    pin = {n: xh[n].pin_memory() for n in names_in}
+    host_out = {n: torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for n, o in out.items()}
+    bi = sum(t.numel() * t.element_size() for t in pin.values())
+    bo = sum(t.numel() * t.element_size() for t in host_out.values())
+    E = max(1, args.e2e_steps)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    s0.record()
+    for _ in range(E):
+        for n in names_in:
+            d[n].copy_(pin[n], non_blocking=True)
+        step()
+        for n, o in out.items():
+            host_out[n].copy_(o, non_blocking=True)
+    s1.record()
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / E
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": tokens * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
+           "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
+
+    # ---- roofline of the dominant kernel ----
+    hbm, tflops, src = load_peaks()
+    kern_ms = {k: statistics.mean(v) for k, v in phase.items()}
+    dom = max(("scan", "grads"), key=lambda k: kern_ms[k])
+    head_tokens = tokens * w.H
+    alg = ALG_BYTES[dom] * head_tokens
+    achieved = alg / (kern_ms[dom] * 1e-3) / 1e9
+    tr = NCU_TRAFFIC.get(KERNEL_NAMES[dom])
+    traffic = tr["bytes_per_launch"] if tr and tr.get("sha") == src_hash(dom) else None
+    roofline = {"kernel": KERNEL_NAMES[dom], "bound": "hbm", "achieved": achieved,
+                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                "alg_bytes_per_launch": alg, "peak_source": f"{src} (MEASURED_PEAKS hbm_gbs)",
+                "tensor_frac": (ALG_FLOP[dom] * head_tokens / (kern_ms[dom] * 1e-3) / 1e12)
+                / tflops}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w), "clocks": clocks, "e2e": e2e,
+        "gpu_launches": 3 * K, "roofline": roofline,
+        "kernels_ms": kern_ms,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = {k: v for k, v in cpu_baseline(xh).items() if k != "seconds"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

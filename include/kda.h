@@ -1,0 +1,164 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi-Delta-Attention backward library.
+ *
+ * The operation.  Per sequence and head, with t the token index,
+ *   q^_t = q_t / sqrt(|q_t|^2 + l2_eps), k^_t likewise      (in-library L2 norm)
+ *   gk_t = -exp(A_log[h]) * softplus(g_t)                     (per-channel log-decay)
+ *   S_t  = (I - beta_t k^_t k^_t^T) Diag(exp(gk_t)) S_{t-1} + beta_t k^_t v_t^T
+ *   o_t  = scale * S_t^T q^_t,     S_0 = h0
+ * and kda_bwd returns the gradients of  sum_t <dO_t, o_t> + <dh_T, S_T>  with
+ * respect to q, k, v, g, beta, A_log and h0.
+ * The work is the chunked backward described on the pages
+ * "bwd-kernelB-beginner-guide-full" (Part 1: the per-chunk gradient kernel
+ * B1/B2/B0/B3 and its outputs dq, dk, dv, dbeta, dg, dA_log; Part 2, B3:
+ * the L2-norm backward and the reverse cumulative sum of the gate gradient)
+ * and "bwd-ncu-and-optimization-playbook" (A/B table: Kernel A, the serial
+ * reverse scan of the per-chunk state gradient dS, grid (N, H, VSplit)).
+ * Chunk size is 64 tokens.
+ *
+ * Conventions for every entry point.
+ *  - Tensors are DEVICE pointers, contiguous, token-major ("native [T,H,D]"
+ *    layout of the kernel-B guide, Part 2, B3 optimisation 8):
+ *      q, k, g, dq, dk, dg : [B, T, H, K]
+ *      v, dO, dv           : [B, T, H, V]
+ *      beta, dbeta         : [B, T, H]
+ *      A_log, dA_log       : [H] fp32
+ *      h0, hT, dh_T, dh0   : [N, H, K, V] fp32, N = B (fixed length) or
+ *                            num_seqs (varlen)
+ *    q, k, v, g, beta, dO and the gradients dq, dk, dv, dg, dbeta all have the
+ *    dtype given in kda_shape (fp32 or bf16).
+ *  - Varlen: cu_seqlens (DEVICE int32 [num_seqs + 1], cu_seqlens[0] == 0,
+ *    non-decreasing, cu_seqlens[num_seqs] == T) packs num_seqs sequences
+ *    back to back in one batch row (B must be 1).  cu_seqlens == NULL means
+ *    B fixed-length sequences of length T.  The library never reads
+ *    cu_seqlens on the host; kernels check it and report a bad table through
+ *    the device status word (kda_get_device_status).
+ *  - Chunk slots.  Per-chunk buffers (the states and the workspace) are
+ *    indexed by a chunk slot, not a dense chunk count, so that no host-side
+ *    scan of cu_seqlens is needed:
+ *      fixed length: slot(b, j) = b * ceil(T / 64) + j
+ *      varlen:       slot(s, j) = floor(cu_seqlens[s] / 64) + s + j
+ *    for chunk j of sequence b / s.  kda_num_chunk_slots() gives the number
+ *    of slots (varlen: floor(T / 64) + num_seqs; a few slots stay unused).
+ *  - Ownership: the caller owns every buffer, including the workspace.  The
+ *    library never allocates or frees memory and never synchronises the
+ *    stream, except kda_get_device_status which synchronises its stream.
+ *  - Errors: argument errors are returned before anything is launched.  A
+ *    failed launch returns KDA_ERR_CUDA.  Errors found on the device (a bad
+ *    cu_seqlens table) are recorded in a device status word read by
+ *    kda_get_device_status.
+ *  - Streams: all work of one call is queued on `stream` in order.  Calls
+ *    on different streams that share output or workspace buffers race.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kda_stream_t; /* == cudaStream_t; NULL = default stream */
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misaligned pointer */
+  KDA_ERR_UNSUPPORTED = 2, /* valid but not built: K, V not in {64, 128}, K != V */
+  KDA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than kda_workspace_bytes */
+  KDA_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
+  KDA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
+  KDA_ERR_DEVICE_ARG = 6   /* the device found a bad cu_seqlens table */
+} kda_status;
+
+typedef enum { KDA_FP32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+typedef struct {
+  int B, T, H, K, V;          /* K == V, both 64 or 128 */
+  int chunk;                  /* must be 64 */
+  int num_seqs;               /* varlen: number of packed sequences; else 0 */
+  const int32_t *cu_seqlens;  /* varlen: DEVICE pointer [num_seqs + 1]; else NULL */
+  float scale;                /* read-out scale; <= 0 selects K^-1/2 */
+  float l2_eps;               /* added to |x|^2 in the L2 norm; < 0 selects 1e-6 */
+  kda_dtype dtype;            /* dtype of q, k, v, g, beta, dO and gradients */
+} kda_shape;
+
+/* Number of chunk slots (see "Chunk slots" above); 0 on a bad shape. */
+int64_t kda_num_chunk_slots(const kda_shape *shape);
+
+/* Bytes of workspace kda_bwd needs: the per-chunk states (dtype of the
+ * shape, [slots, H, K, V]) unless the caller passes them, the per-chunk
+ * state gradients dS (same size) and per-chunk dA_log partials.  Returns 0
+ * on a bad shape. */
+size_t kda_workspace_bytes(const kda_shape *shape);
+
+/* Byte offset inside the workspace of the per-chunk state gradients
+ * dS_{n+1} (the adjoint of the state at the END of chunk n), layout
+ * [slots, H, K, V] in the shape's dtype.  Exposed so that tests can check
+ * the reverse scan on its own. */
+size_t kda_workspace_dstates_offset(const kda_shape *shape);
+
+/* Forward chunk-state recompute (the "all_states" operand of kernel B2 in
+ * "bwd-kernelB-beginner-guide-full", Part 2, B2 optimisation 4).
+ *   states : OUT [slots, H, K, V], dtype of the shape: S at the start of
+ *            every chunk (S_0 = h0), bf16 rounded to nearest even.
+ *   h0     : nullable (zero initial state), fp32 [N, H, K, V].
+ *   hT     : nullable OUT fp32 [N, H, K, V]: the final state of each sequence.
+ * No workspace is needed. */
+kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v,
+                          const void *g, const void *beta,
+                          const float *A_log, const float *h0, void *states,
+                          float *hT, kda_stream_t stream);
+
+/* Backward pass.
+ *   dh_T   : nullable (zero), fp32 [N, H, K, V].
+ *   dq, dk, dv, dg, dbeta : OUT, overwritten, dtype of the shape.
+ *   dA_log : OUT fp32 [H], overwritten (summed over sequences and tokens).
+ *   dh0    : nullable OUT fp32 [N, H, K, V].
+ *   states : nullable; the output of kda_fwd_states for the same inputs.
+ *            NULL recomputes them inside the workspace.
+ *   ws     : DEVICE workspace of at least kda_workspace_bytes(shape) bytes,
+ *            256-byte aligned.  Its content on entry is ignored.
+ * q, k, v, g, beta, A_log and dO are required. */
+kda_status kda_bwd(const kda_shape *shape, const void *q, const void *k,
+                   const void *v, const void *g, const void *beta,
+                   const float *A_log, const float *h0, const void *dO,
+                   const float *dh_T, void *dq, void *dk, void *dv, void *dg,
+                   void *dbeta, float *dA_log, float *dh0, const void *states,
+                   void *ws, size_t ws_bytes, kda_stream_t stream);
+
+/* kda_bwd with phase timing: `events` (nullable) points at 4 cudaEvent_t
+ * created by the caller (timing enabled).  They are recorded on `stream`
+ * at the start of the call, after the chunk scans (forward-state recompute
+ * and reverse dS scan), after the per-chunk gradient kernel and at the end
+ * (after the dA_log reduction).  Otherwise identical to kda_bwd. */
+kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k,
+                         const void *v, const void *g, const void *beta,
+                         const float *A_log, const float *h0, const void *dO,
+                         const float *dh_T, void *dq, void *dk, void *dv, void *dg,
+                         void *dbeta, float *dA_log, float *dh0, const void *states,
+                         void *ws, size_t ws_bytes, kda_stream_t stream,
+                         void *const *events);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device (KDA_OK, KDA_ERR_DEVICE_ARG or KDA_ERR_TIMEOUT), or
+ * KDA_ERR_CUDA if the synchronisation itself reported an error. */
+kda_status kda_get_device_status(kda_stream_t stream);
+
+/* Host-side check of a cu_seqlens table the caller holds on the host:
+ * KDA_OK or KDA_ERR_INVALID_ARG. */
+kda_status kda_check_cu_seqlens_host(const int32_t *cu_seqlens, int num_seqs,
+                                     int total_T);
+
+/* Static description of a status code. */
+const char *kda_status_str(kda_status status);
+
+/* Version of this ABI (increments on any signature change). */
+int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

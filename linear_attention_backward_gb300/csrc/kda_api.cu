@@ -1,0 +1,234 @@
+// kda_api.cu -- host side of the C ABI declared in include/kda.h: argument
+// validation, workspace layout, launch sequencing and the device status word.
+#include <cuda_runtime.h>
+
+#include <stdint.h>
+#include <math.h>
+#include <string.h>
+
+#include "kda.h"
+#include "kda_params.h"
+
+namespace {
+
+constexpr int kChunk = 64;
+constexpr size_t kAlign = 256;
+constexpr int kTargetCtas = 152;  // one wave of the scan kernels fills the SMs
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_seqs_of(const kda_shape *s) { return s->cu_seqlens ? s->num_seqs : s->B; }
+
+// Structural validation of a shape (no pointers other than cu_seqlens' presence).
+kda_status check_shape(const kda_shape *s) {
+  if (s == nullptr) return KDA_ERR_INVALID_ARG;
+  if (s->B < 1 || s->T < 0 || s->H < 1 || s->K < 1 || s->V < 1) return KDA_ERR_INVALID_ARG;
+  if (s->dtype != KDA_FP32 && s->dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (s->chunk != kChunk) return KDA_ERR_UNSUPPORTED;
+  if (s->cu_seqlens != nullptr) {
+    if (s->B != 1 || s->num_seqs < 1) return KDA_ERR_INVALID_ARG;
+  } else if (s->num_seqs != 0) {
+    return KDA_ERR_INVALID_ARG;
+  }
+  if (s->K != s->V) return KDA_ERR_UNSUPPORTED;
+  if (s->K != 64 && s->K != 128) return KDA_ERR_UNSUPPORTED;
+  if (s->dtype == KDA_FP32 && s->K != 64) return KDA_ERR_UNSUPPORTED;
+  // sizes must stay inside 32-bit element offsets per row and 64-bit overall
+  if ((int64_t)s->B * s->T > (int64_t)1 << 31) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+int64_t slots_of(const kda_shape *s) {
+  if (s->cu_seqlens) return (int64_t)(s->T / kChunk) + s->num_seqs;
+  return (int64_t)s->B * ((s->T + kChunk - 1) / kChunk);
+}
+
+size_t elem_size(const kda_shape *s) { return s->dtype == KDA_BF16 ? 2 : 4; }
+
+size_t states_bytes(const kda_shape *s) {
+  return round_up((size_t)slots_of(s) * s->H * (size_t)s->K * s->V * elem_size(s));
+}
+
+void fill_params(const kda_shape *s, kda::KdaParams &p) {
+  memset(&p, 0, sizeof(p));
+  p.B = s->B;
+  p.T = s->T;
+  p.H = s->H;
+  p.num_seqs = num_seqs_of(s);
+  p.cu = s->cu_seqlens;
+  p.nps = (s->T + kChunk - 1) / kChunk;
+  p.nslots = slots_of(s);
+  p.scale = s->scale > 0.f ? s->scale : 1.0f / sqrtf((float)s->K);
+  p.eps = s->l2_eps >= 0.f ? s->l2_eps : 1e-6f;
+  p.nb = 1;
+}
+
+// V band width of the scan kernels: wide bands unless the (sequence, head,
+// role) units alone leave most SMs idle.
+int pick_band(const kda_shape *s, int nroles) {
+  const int units = num_seqs_of(s) * s->H * nroles;
+  int bv = s->V;
+  while (bv > 32 && units * (s->V / bv) * 2 <= kTargetCtas) bv /= 2;
+  return bv;
+}
+
+kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int kda_abi_version(void) { return 1; }
+
+const char *kda_status_str(kda_status st) {
+  switch (st) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+    case KDA_ERR_CUDA: return "CUDA error";
+    case KDA_ERR_TIMEOUT: return "device-side wait timed out";
+    case KDA_ERR_DEVICE_ARG: return "device found a malformed cu_seqlens table";
+  }
+  return "unknown status";
+}
+
+int64_t kda_num_chunk_slots(const kda_shape *shape) {
+  if (check_shape(shape) != KDA_OK) return 0;
+  return slots_of(shape);
+}
+
+size_t kda_workspace_dstates_offset(const kda_shape *shape) {
+  if (check_shape(shape) != KDA_OK) return 0;
+  return states_bytes(shape);
+}
+
+size_t kda_workspace_bytes(const kda_shape *shape) {
+  if (check_shape(shape) != KDA_OK) return 0;
+  const size_t part = round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
+  return 2 * states_bytes(shape) + part;
+}
+
+kda_status kda_check_cu_seqlens_host(const int32_t *cu, int num_seqs, int total_T) {
+  if (cu == nullptr || num_seqs < 1 || total_T < 0) return KDA_ERR_INVALID_ARG;
+  if (cu[0] != 0 || cu[num_seqs] != total_T) return KDA_ERR_INVALID_ARG;
+  for (int i = 0; i < num_seqs; ++i)
+    if (cu[i + 1] < cu[i]) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v, const void *g,
+                          const void *beta, const float *A_log, const float *h0, void *states,
+                          float *hT, kda_stream_t stream) {
+  kda_status st = check_shape(shape);
+  if (st != KDA_OK) return st;
+  const bool tokens = (int64_t)shape->B * shape->T > 0;
+  if (!A_log) return KDA_ERR_INVALID_ARG;
+  if (tokens && (!k || !v || !g || !beta || !states)) return KDA_ERR_INVALID_ARG;
+  const void *ptrs[] = {k, v, g, beta, A_log, h0, states, hT};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  kda::KdaParams p;
+  fill_params(shape, p);
+  p.k = k;
+  p.v = v;
+  p.g = g;
+  p.beta = beta;
+  p.A_log = A_log;
+  p.h0 = h0;
+  p.states = states;
+  p.hT = hT;
+  p.role_base = 0;
+  const int bv = pick_band(shape, 1);
+  p.nb = shape->V / bv;
+  return from_cuda(kda::scan_dispatch(p, shape->K, shape->dtype == KDA_BF16, bv, 1,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_bwd(const kda_shape *shape, const void *q, const void *k, const void *v,
+                   const void *g, const void *beta, const float *A_log, const float *h0,
+                   const void *dO, const float *dh_T, void *dq, void *dk, void *dv, void *dg,
+                   void *dbeta, float *dA_log, float *dh0, const void *states, void *ws,
+                   size_t ws_bytes, kda_stream_t stream) {
+  return kda_bwd_timed(shape, q, k, v, g, beta, A_log, h0, dO, dh_T, dq, dk, dv, dg, dbeta,
+                       dA_log, dh0, states, ws, ws_bytes, stream, nullptr);
+}
+
+kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, const void *v,
+                         const void *g, const void *beta, const float *A_log, const float *h0,
+                         const void *dO, const float *dh_T, void *dq, void *dk, void *dv,
+                         void *dg, void *dbeta, float *dA_log, float *dh0, const void *states,
+                         void *ws, size_t ws_bytes, kda_stream_t stream, void *const *events) {
+  kda_status st = check_shape(shape);
+  if (st != KDA_OK) return st;
+  // per-token tensors may be NULL only when there are no tokens
+  const bool tokens = (int64_t)shape->B * shape->T > 0;
+  if (!A_log || !dA_log) return KDA_ERR_INVALID_ARG;
+  if (tokens && (!q || !k || !v || !g || !beta || !dO || !dq || !dk || !dv || !dg || !dbeta))
+    return KDA_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, g, beta, A_log, h0, dO, dh_T, dq, dk, dv, dg, dbeta, dA_log,
+                        dh0, states};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  const size_t need = kda_workspace_bytes(shape);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return KDA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return KDA_ERR_WORKSPACE;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  char *w = static_cast<char *>(ws);
+  const size_t sb = states_bytes(shape);
+  kda::KdaParams p;
+  fill_params(shape, p);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.g = g;
+  p.beta = beta;
+  p.dO = dO;
+  p.A_log = A_log;
+  p.h0 = h0;
+  p.dhT = dh_T;
+  p.states = states ? const_cast<void *>(states) : w;
+  p.hT = nullptr;
+  p.dstates = w + sb;
+  p.dh0 = dh0;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.dg = dg;
+  p.dbeta = dbeta;
+  p.dA_part = reinterpret_cast<float *>(w + 2 * sb);
+  p.dA_log = dA_log;
+  const bool bf = shape->dtype == KDA_BF16;
+  auto mark = [&](int i) {
+    if (events != nullptr && events[i] != nullptr)
+      cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), cs);
+  };
+  mark(0);
+  // 1. scans: forward states (unless given) and the reverse dS scan, one launch
+  const int nroles = states ? 1 : 2;
+  p.role_base = states ? 1 : 0;
+  const int bv = pick_band(shape, nroles);
+  p.nb = shape->V / bv;
+  cudaError_t e = kda::scan_dispatch(p, shape->K, bf, bv, nroles, cs);
+  if (e != cudaSuccess) return KDA_ERR_CUDA;
+  mark(1);
+  // 2. per-chunk gradients and the dA_log reduction
+  e = kda::grads_dispatch(p, shape->K, bf, p.states, cs, events ? events[2] : nullptr);
+  mark(3);
+  return from_cuda(e);
+}
+
+kda_status kda_get_device_status(kda_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  const int a = kda::scan_status_take();
+  const int b = kda::grads_status_take();
+  if (a < 0 || b < 0) return KDA_ERR_CUDA;
+  if (a != 0) return (kda_status)a;
+  return (kda_status)b;
+}
+
+}  // extern "C"

@@ -1,0 +1,266 @@
+// kda_scan.cu -- the two serial chunk scans of the KDA backward, one CTA per
+// (sequence, head, V band):
+//
+//  * forward role: the chunk-state recompute ("all_states", read by kernel
+//    B2 in "bwd-kernelB-beginner-guide-full", Part 2, B2 optimisation 4)
+//      U       = (I + Akk)^-1 diag(beta) (v - kd S_n)            (v_new)
+//      S_{n+1} = diag(e^gT) S_n + kr^T U
+//  * backward role: Kernel A, the reverse scan of the per-chunk state
+//    gradient ("bwd-ncu-and-optimization-playbook", A/B table; guide Part 2,
+//    B1 for dU and dvcorr)
+//      dU      = scale Mqk^T dO + kr dS_{n+1}
+//      dvcorr  = (I + Akk)^-T dU
+//      dS_n    = diag(e^gT) dS_{n+1} + scale qd^T dO - kd^T diag(beta) dvcorr
+//
+// Both recurrences are column-separable in V, so the V axis is split into
+// bands (the split-V grid (N, H, VSplit) of the playbook, section 3.5); every
+// band recomputes the chunk prep.  The two roles do not depend on each other
+// and run side by side in one launch (blockIdx.y = role).  The running state
+// stays in registers (mma accumulators) across chunks: warp w owns state rows
+// [16 (w % (K/16)), +16).
+#include "kda_chunk.cuh"
+
+namespace kda {
+
+template <typename E, int K, int BV> struct ScanSmem {
+  static constexpr int LD = tile_ld<E>(K);
+  static constexpr int LDB = tile_ld<E>(BV);
+  static constexpr int LDF = K + 4;
+  static constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
+  static constexpr size_t sz_gc = cmax(64 * LDF * 4, 64 * 68 * 4 + 768 * 4);
+  static constexpr size_t sz_small = (3 * 4 * K + 6 * K + K + 3 * 64) * 4;
+  static constexpr size_t sz_tile = 64 * LD * sizeof(E);
+  static constexpr size_t sz_band = 64 * LDB * sizeof(E);
+  static constexpr size_t sz_G = cmax(64 * 68 * 4, sz_band);
+  static constexpr size_t sz_sq = 64 * tile_ld<E>(64) * sizeof(E);
+  static constexpr size_t sz_state = K * LDB * sizeof(E);
+  // offsets
+  static constexpr size_t o_gc = 0;                       // gc, later inv32 + tbuf
+  static constexpr size_t o_small = o_gc + sz_gc;
+  static constexpr size_t o_QM = o_small + sz_small;      // QM, KM, KP; later stateT, U
+  static constexpr size_t o_KM = o_QM + sz_tile;
+  static constexpr size_t o_KP = o_KM + sz_tile;
+  static constexpr size_t o_KD = o_KP + sz_tile;
+  static constexpr size_t o_KR = o_KD + sz_tile;
+  static constexpr size_t o_QD = o_KR + sz_tile;
+  static constexpr size_t o_G = o_QD + sz_tile;           // G, later W
+  static constexpr size_t o_INV = o_G + sz_G;
+  static constexpr size_t o_MQK = o_INV + sz_sq;
+  static constexpr size_t o_BAND = o_MQK + sz_sq;         // v band (fwd) / dO band (bwd)
+  static constexpr size_t total = o_BAND + sz_band;
+  static constexpr size_t o_STATE = o_QM;                 // aliases QM/KM/KP after intra_pairs
+  static constexpr size_t o_U = o_QM + sz_state;
+  static_assert(sz_state + sz_band <= 3 * sz_tile, "state + U must fit in QM/KM/KP");
+  static_assert(sz_band <= sz_G, "W must fit in G");
+  static_assert(64 * 68 * 4 + 768 * 4 <= sz_gc, "inverse scratch must fit in gc");
+};
+
+template <typename E, int K>
+__device__ __forceinline__ PrepView<E, K> make_view(char *smem, size_t o_gc, size_t o_small) {
+  PrepView<E, K> v;
+  v.gc = reinterpret_cast<float *>(smem + o_gc);
+  float *s = reinterpret_cast<float *>(smem + o_small);
+  v.m = s;
+  v.em = s + 4 * K;
+  v.egm = s + 8 * K;
+  v.F = s + 12 * K;
+  v.gT = s + 18 * K;
+  v.rq = s + 19 * K;
+  v.rk = v.rq + 64;
+  v.beta = v.rk + 64;
+  return v;
+}
+
+template <typename E, int K, int BV>
+__global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
+  using SM = ScanSmem<E, K, BV>;
+  extern __shared__ __align__(128) char smem[];
+  constexpr int LD = SM::LD, LDB = SM::LDB;
+  constexpr int WM = K / 16;          // warps along state rows
+  constexpr int WN = NWARPS / WM;     // warps along the band columns
+  constexpr int SCOLS = BV / WN;      // state columns per warp
+  constexpr int NFS = SCOLS / 8;
+  constexpr int NFC = BV / 16;        // chunk-row GEMMs: 4 row blocks x 2 column halves
+
+  const int role = p.role_base + blockIdx.y;  // 0: forward states, 1: reverse dS scan
+  const int unit = blockIdx.x;
+  const int band = unit % p.nb;
+  const int sh = unit / p.nb;
+  const int h = sh % p.H, s = sh / p.H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H;
+  int64_t tok_seq, slot0;
+  int L;
+  if (!seq_bounds(p, s, tok_seq, L, slot0)) return;
+  const int nck = (L + CHUNK - 1) / CHUNK;
+  const int v0 = band * BV;
+
+  PrepView<E, K> sv = make_view<E, K>(smem, SM::o_gc, SM::o_small);
+  E *QM = reinterpret_cast<E *>(smem + SM::o_QM);
+  E *KM = reinterpret_cast<E *>(smem + SM::o_KM);
+  E *KP = reinterpret_cast<E *>(smem + SM::o_KP);
+  E *KD = reinterpret_cast<E *>(smem + SM::o_KD);
+  E *KR = reinterpret_cast<E *>(smem + SM::o_KR);
+  E *QD = reinterpret_cast<E *>(smem + SM::o_QD);
+  float *G = reinterpret_cast<float *>(smem + SM::o_G);
+  E *W = reinterpret_cast<E *>(smem + SM::o_G);
+  E *INV = reinterpret_cast<E *>(smem + SM::o_INV);
+  E *MQK = reinterpret_cast<E *>(smem + SM::o_MQK);
+  E *BAND = reinterpret_cast<E *>(smem + SM::o_BAND);
+  E *ST = reinterpret_cast<E *>(smem + SM::o_STATE);
+  E *UB = reinterpret_cast<E *>(smem + SM::o_U);
+  float *inv32 = sv.gc;
+  float *tbuf = sv.gc + 64 * 68;
+
+  // state rows owned by this warp
+  const int srow0 = 16 * (warp % WM);
+  const int scol0 = SCOLS * (warp / WM);
+  float S[NFS][4];
+  const size_t KV = (size_t)K * (size_t)(BV * p.nb);
+  const int Vtot = BV * p.nb;
+  {
+    const float *init = role == 0 ? p.h0 : p.dhT;
+    for_acc(S, [&](int r, int c, float &x) {
+      x = init ? init[((size_t)s * H + h) * KV + (size_t)(srow0 + r) * Vtot + v0 + scol0 + c] : 0.f;
+    });
+  }
+  const int rb = warp & 3;            // chunk-row block of this warp
+  const int ch = (warp >> 2) * (BV / 2);  // column half of the band
+
+  for (int it = 0; it < nck; ++it) {
+    const int j = role == 0 ? it : nck - 1 - it;
+    const int64_t tok0 = tok_seq + (int64_t)j * CHUNK;
+    const int len = min(CHUNK, L - j * CHUNK);
+    const int64_t slot = slot0 + j;
+    __syncthreads();
+    // band rows of v (fwd) or dO (bwd)
+    {
+      const void *src = role == 0 ? p.v : p.dO;
+      for (int e = tid; e < CHUNK * BV / 2; e += NTHREADS) {
+        const int i = e / (BV / 2), c = 2 * (e % (BV / 2));
+        float2 x = make_float2(0.f, 0.f);
+        if (i < len) x = load2(elem_ptr<E>(src, ((tok0 + i) * H + h) * Vtot + v0 + c));
+        store2(BAND + i * LDB + c, x.x, x.y);
+      }
+    }
+    PrepTiles<E> tl;
+    tl.KM = KM;
+    tl.KP = KP;
+    tl.KD = KD;
+    tl.KR = KR;
+    if (role == 1) {
+      tl.QM = QM;
+      tl.QD = QD;
+    }
+    chunk_prep<E, K>(p, h, tok0, len, role == 1, sv, tl);
+    intra_pairs<E, K>(QM, KM, KP, sv.F, G, 68, role == 1 ? MQK : nullptr, tile_ld<E>(64), p.scale);
+    __syncthreads();
+    wy_inverse<E>(G, 68, sv.beta, inv32, tbuf, INV, tile_ld<E>(64));
+    // publish the current state: to HBM (states / dstates) and to smem as an operand
+    {
+      E *dst = reinterpret_cast<E *>(role == 0 ? p.states : p.dstates) +
+               ((size_t)slot * H + h) * (size_t)K * Vtot + v0;
+      for_acc(S, [&](int r, int c, float &x) {
+        ST[(srow0 + r) * LDB + scol0 + c] = from_f<E>(x);
+      });
+      __syncthreads();
+      for (int e = tid; e < K * BV / 2; e += NTHREADS) {
+        const int r = e / (BV / 2), c = 2 * (e % (BV / 2));
+        const float2 x = load2(ST + r * LDB + c);
+        store2(dst + (size_t)r * Vtot + c, x.x, x.y);
+      }
+    }
+    if (role == 0) {
+      // kdS = kd S_n ; Xr = v - kdS  (in place in BAND)
+      float acc[NFC][4];
+      zero_acc(acc);
+      warp_gemm<NFC, true, false>(acc, KD + 16 * rb * LD, LD, ST + ch, LDB, K);
+      for_acc(acc, [&](int r, int c, float &x) {
+        E *pv = BAND + (16 * rb + r) * LDB + ch + c;
+        *pv = from_f<E>(to_f(*pv) - x);
+      });
+      __syncthreads();
+      // U = INV diag(beta) Xr
+      zero_acc(acc);
+      warp_gemm<NFC, true, false>(acc, INV + 16 * rb * tile_ld<E>(64), tile_ld<E>(64), BAND + ch, LDB, 64,
+                                  sv.beta);
+      store_acc(UB + 16 * rb * LDB + ch, LDB, acc);
+      __syncthreads();
+      // S <- diag(e^gT) S + kr^T U
+      for_acc(S, [&](int r, int c, float &x) { x *= __expf(sv.gT[srow0 + r]); });
+      warp_gemm<NFS, false, false>(S, KR + srow0, LD, UB + scol0, LDB, 64);
+    } else {
+      // dU = scale Mqk^T dO + kr dS
+      float acc[NFC][4];
+      zero_acc(acc);
+      warp_gemm<NFC, false, false>(acc, MQK + 16 * rb, tile_ld<E>(64), BAND + ch, LDB, 64);
+      warp_gemm<NFC, true, false>(acc, KR + 16 * rb * LD, LD, ST + ch, LDB, K);
+      store_acc(UB + 16 * rb * LDB + ch, LDB, acc);
+      __syncthreads();
+      // dvcorr = INV^T dU ; W = -beta dvcorr
+      zero_acc(acc);
+      warp_gemm<NFC, false, false>(acc, INV + 16 * rb, tile_ld<E>(64), UB + ch, LDB, 64);
+      for_acc(acc, [&](int r, int c, float &x) {
+        W[(16 * rb + r) * LDB + ch + c] = from_f<E>(-sv.beta[16 * rb + r] * x);
+      });
+      __syncthreads();
+      // dS <- diag(e^gT) dS + scale qd^T dO - kd^T diag(beta) dvcorr
+      for_acc(S, [&](int r, int c, float &x) { x *= __expf(sv.gT[srow0 + r]); });
+      warp_gemm<NFS, false, false>(S, QD + srow0, LD, BAND + scol0, LDB, 64);
+      warp_gemm<NFS, false, false>(S, KD + srow0, LD, W + scol0, LDB, 64);
+    }
+  }
+  float *fin = role == 0 ? p.hT : p.dh0;
+  if (fin != nullptr) {
+    for_acc(S, [&](int r, int c, float &x) {
+      fin[((size_t)s * H + h) * KV + (size_t)(srow0 + r) * Vtot + v0 + scol0 + c] = x;
+    });
+  }
+  (void)lane;
+}
+
+template <typename E, int K, int BV>
+static cudaError_t launch_scan(const KdaParams &p, int nroles, cudaStream_t st) {
+  using SM = ScanSmem<E, K, BV>;
+  auto kfn = kda_scan_kernel<E, K, BV>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SM::total);
+  if (e != cudaSuccess) return e;
+  const int nunits = (p.cu ? p.num_seqs : p.B) * p.H * p.nb;
+  if (nunits == 0 || nroles == 0) return cudaSuccess;
+  kfn<<<dim3(nunits, nroles), NTHREADS, SM::total, st>>>(p);
+  return cudaGetLastError();
+}
+
+#define KDA_SCAN_CASES(X)            \
+  X(bf16, 128, 128) X(bf16, 128, 64) \
+  X(bf16, 128, 32) X(bf16, 64, 64)   \
+  X(bf16, 64, 32) X(float, 64, 64)   \
+  X(float, 64, 32)
+
+cudaError_t scan_dispatch(const KdaParams &p, int K, bool is_bf16, int bv, int nroles,
+                          cudaStream_t st) {
+#define X(E, KK, BB)                                                          \
+  if (is_bf16 == (sizeof(E) == 2) && K == KK && bv == BB)                     \
+    return launch_scan<E, KK, BB>(p, nroles, st);
+  KDA_SCAN_CASES(X)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+size_t scan_smem_bytes(int K, bool is_bf16, int bv) {
+#define X(E, KK, BB)                                                          \
+  if (is_bf16 == (sizeof(E) == 2) && K == KK && bv == BB) return ScanSmem<E, KK, BB>::total;
+  KDA_SCAN_CASES(X)
+#undef X
+  return 0;
+}
+
+int scan_status_take() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -1;
+  if (cudaMemcpyToSymbol(g_status, &z, sizeof(int)) != cudaSuccess) return -1;
+  return v;
+}
+
+}  // namespace kda

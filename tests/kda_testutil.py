@@ -1,0 +1,66 @@
+"""Shared helpers of the test-suite: oracle runs on workload inputs, the
+per-tensor relative L2 error, and GPU runs through the C ABI."""
+import numpy as np
+import torch
+
+import oracle
+from linear_attention_backward_gb300 import workloads as wl
+
+GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "dh0")
+
+
+def f64_tokens(t):
+    """[B, T, H, ...] torch tensor -> fp64 numpy [B*T, H, ...]."""
+    return t.double().reshape(-1, *t.shape[2:]).numpy()
+
+
+def oracle_bwd(x, **kw):
+    return oracle.backward(
+        f64_tokens(x["q"]), f64_tokens(x["k"]), f64_tokens(x["v"]), f64_tokens(x["g"]),
+        f64_tokens(x["beta"]), x["A_log"].double().numpy(), x["h0"].double().numpy(),
+        f64_tokens(x["dO"]), x["dhT"].double().numpy(), cu_seqlens=wl.seq_bounds(x), **kw)
+
+
+def oracle_states(x, chunk=64):
+    _, hT, cs = oracle.forward(
+        f64_tokens(x["q"]), f64_tokens(x["k"]), f64_tokens(x["v"]), f64_tokens(x["g"]),
+        f64_tokens(x["beta"]), x["A_log"].double().numpy(), x["h0"].double().numpy(),
+        cu_seqlens=wl.seq_bounds(x), chunk=chunk, want_chunk_states=True)
+    return cs, hT
+
+
+def rel_l2(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    nr = np.linalg.norm(ref)
+    d = np.linalg.norm(got - ref)
+    return d / nr if nr > 0 else d
+
+
+def to_dev(x, dev="cuda"):
+    return {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+
+
+def gpu_bwd(x, states=None, **kw):
+    import linear_attention_backward_gb300 as kda
+    d = to_dev(x)
+    g = kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"], d["dO"],
+                d["dhT"], cu_seqlens=d["cu_seqlens"], states=states, **kw)
+    torch.cuda.synchronize()
+    return g, d
+
+
+def slot_index(x, chunk=64):
+    """(sequence, chunk) -> slot for the library's slot map, as a list of
+    arrays of slots per sequence (dense oracle chunk order = concatenation)."""
+    cu = wl.seq_bounds(x)
+    out = []
+    fixed = x["cu_seqlens"] is None
+    T = x["q"].shape[1]
+    nps = (T + chunk - 1) // chunk
+    for s in range(len(cu) - 1):
+        L = cu[s + 1] - cu[s]
+        n = (L + chunk - 1) // chunk
+        base = s * nps if fixed else cu[s] // chunk + s
+        out.append(np.arange(base, base + n))
+    return out

@@ -1,0 +1,106 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry
+point include/kda.h declares, and validates arguments on the host (these
+calls return before anything touches CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import __graft_entry__
+import linear_attention_backward_gb300 as kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    __graft_entry__.build()
+    return kda.lib()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert {"kda_bwd", "kda_fwd_states", "kda_workspace_bytes"} <= names
+    for n in sorted(names):
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_abi_version_and_strings(L):
+    assert L.kda_abi_version() == 1
+    for st in range(7):
+        assert len(L.kda_status_str(st)) > 0
+
+
+def _shape(**kw):
+    d = dict(B=2, T=130, H=3, K=128, V=128, chunk=64, num_seqs=0, cu_seqlens=None,
+             scale=0.0, l2_eps=-1.0, dtype=kda.KDA_BF16)
+    d.update(kw)
+    return kda.KdaShape(d["B"], d["T"], d["H"], d["K"], d["V"], d["chunk"], d["num_seqs"],
+                        d["cu_seqlens"], d["scale"], d["l2_eps"], d["dtype"])
+
+
+def test_slots_and_workspace(L):
+    s = _shape()
+    assert kda.num_chunk_slots(s) == 2 * 3
+    sb = 6 * 3 * 128 * 128 * 2
+    sb = (sb + 255) // 256 * 256
+    assert kda.workspace_dstates_offset(s) == sb
+    assert kda.workspace_bytes(s) == 2 * sb + ((6 * 3 * 4 + 255) // 256) * 256
+    v = _shape(B=1, T=300, num_seqs=4, cu_seqlens=0x1000)
+    assert kda.num_chunk_slots(v) == 300 // 64 + 4
+    f = _shape(K=64, V=64, dtype=kda.KDA_FP32, T=64, B=1)
+    assert kda.workspace_dstates_offset(f) == 1 * 3 * 64 * 64 * 4
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=96, V=96), 2), (dict(K=128, V=64), 2), (dict(chunk=32), 2),
+    (dict(B=0), 1), (dict(H=0), 1), (dict(T=-1), 1), (dict(dtype=7), 1),
+    (dict(num_seqs=3), 1), (dict(cu_seqlens=0x1000, num_seqs=2), 1),
+    (dict(K=128, V=128, dtype=kda.KDA_FP32), 2),
+])
+def test_bad_shapes_rejected(L, kw, code):
+    s = _shape(**kw)
+    assert kda.workspace_bytes(s) == 0
+    fake = ctypes.c_void_p(1 << 20)
+    st = L.kda_bwd(ctypes.byref(s), *([fake] * 17), fake, ctypes.c_size_t(1 << 40), None)
+    assert st == code
+
+
+def test_bwd_pointer_checks(L):
+    s = _shape()
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake] * 17
+    ws_ok = ctypes.c_size_t(kda.workspace_bytes(s))
+    # a required pointer missing
+    a = list(args); a[0] = None
+    assert L.kda_bwd(ctypes.byref(s), *a, fake, ws_ok, None) == 1
+    # misaligned tensor
+    a = list(args); a[3] = ctypes.c_void_p((1 << 20) + 4)
+    assert L.kda_bwd(ctypes.byref(s), *a, fake, ws_ok, None) == 1
+    # workspace: missing, too small, misaligned
+    assert L.kda_bwd(ctypes.byref(s), *args, None, ws_ok, None) == 3
+    assert L.kda_bwd(ctypes.byref(s), *args, fake, ctypes.c_size_t(ws_ok.value - 1), None) == 3
+    assert L.kda_bwd(ctypes.byref(s), *args, ctypes.c_void_p((1 << 20) + 16), ws_ok, None) == 3
+    # fwd_states: missing states
+    st = L.kda_fwd_states(ctypes.byref(s), fake, fake, fake, fake, fake, None, None, None, None)
+    assert st == 1
+
+
+def test_host_cu_seqlens_check(L):
+    good = torch.tensor([0, 5, 5, 70], dtype=torch.int32)
+    assert kda.check_cu_seqlens_host(good, 70) == 0
+    assert kda.check_cu_seqlens_host(good, 71) == 1
+    assert kda.check_cu_seqlens_host(torch.tensor([1, 5, 70], dtype=torch.int32), 70) == 1
+    assert kda.check_cu_seqlens_host(torch.tensor([0, 9, 5, 70], dtype=torch.int32), 70) == 1
