@@ -224,7 +224,8 @@ def workload_config(w):
                         f"K={w.K} V={w.V} chunk={w.chunk}, states recomputed in the call",
             "global_batch": w.B, "seq_len": w.T, "heads": w.H, "head_dim": w.K,
             "parallelism": "replicas (one independent batch per GPU)",
-            "l2": "inputs larger than L2 (268 MB per input tensor), no flush"}
+            "l2": "inputs larger than L2 (each input tensor is B*T*H*128*2 bytes; "
+                  "268 MB at B=4), no flush"}
 
 
 def main():
@@ -235,6 +236,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload name (default: the main B=4 T=8192 H=32 batch)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_setup()
@@ -256,7 +259,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    w = wl.WORKLOADS[WORKLOAD]
+    w = wl.WORKLOADS[args.workload]
     xh = wl.make_inputs(w, seed=rank)
     names_in = ["q", "k", "v", "g", "beta", "dO", "A_log"]
     if w.with_h0:

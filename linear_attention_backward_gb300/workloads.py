@@ -45,6 +45,8 @@ WORKLOADS = {
     "lowpar_bf16": Workload("lowpar_bf16", 1, 4096, 16, 128, 128, "bf16"),
     # B=4 T=8192 H=32 K=V=128, bf16 (the main benchmark workload)
     "main_bf16": Workload("main_bf16", 4, 8192, 32, 128, 128, "bf16"),
+    # a quarter of the main batch (B=1), the size used for ncu captures
+    "main_b1_bf16": Workload("main_b1_bf16", 1, 8192, 32, 128, 128, "bf16"),
     # B=8 T=16384 H=32 K=V=128, bf16, with h0 and dh_T
     "large_bf16": Workload("large_bf16", 8, 16384, 32, 128, 128, "bf16", True, True),
     # 16 packed sequences, lengths U[512, 8192], H=32 K=V=128, bf16, h0 and dh_T
