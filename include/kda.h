@@ -69,7 +69,8 @@ typedef enum {
   KDA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than kda_workspace_bytes */
   KDA_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
   KDA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
-  KDA_ERR_DEVICE_ARG = 6   /* the device found a bad cu_seqlens table */
+  KDA_ERR_DEVICE_ARG = 6,  /* the device found a bad cu_seqlens table */
+  KDA_ERR_TOO_LARGE = 7    /* kda_bwd_noalloc: problem needs more than its fixed scratch */
 } kda_status;
 
 typedef enum { KDA_FP32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -140,6 +141,37 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k,
                          void *dbeta, float *dA_log, float *dh0, const void *states,
                          void *ws, size_t ws_bytes, kda_stream_t stream,
                          void *const *events);
+
+/* Backward pass for callers that cannot allocate device memory (no
+ * counterpart on the pages; a service of this library).  Some callers have
+ * no way to hand kda_bwd a workspace: code running inside a device-memory
+ * allocator or pool that owns every device allocation, processes that may
+ * only use memory reserved up front, or plugin hosts that expose no
+ * allocation API.  This entry point takes the same inputs and outputs as
+ * kda_bwd (states always recomputed) but keeps its scratch -- the per-chunk
+ * states, state gradients and dA_log partials -- in a fixed array of
+ * kda_noalloc_scratch_bytes() bytes (64 MiB) compiled into the library.
+ * That array exists once per GPU that loads the library and stays allocated
+ * until the process exits.
+ *  - Size limit: problems whose kda_workspace_bytes() exceeds the array are
+ *    rejected with KDA_ERR_TOO_LARGE before anything is launched (64 MiB
+ *    holds about 1000 chunk-heads of 64 tokens at K = V = 128, bf16).
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress, with that device current) and caches
+ *    it; make that first call before capturing any stream.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - Every call on a device shares the same array: calls whose work
+ *    overlaps on the GPU (different streams, or different host threads)
+ *    race on it and must be serialised by the caller.  The array needs no
+ *    initial content; each call writes every part it reads. */
+kda_status kda_bwd_noalloc(const kda_shape *shape, const void *q, const void *k,
+                           const void *v, const void *g, const void *beta,
+                           const float *A_log, const float *h0, const void *dO,
+                           const float *dh_T, void *dq, void *dk, void *dv, void *dg,
+                           void *dbeta, float *dA_log, float *dh0, kda_stream_t stream);
+
+/* Capacity in bytes of kda_bwd_noalloc's fixed scratch array. */
+size_t kda_noalloc_scratch_bytes(void);
 
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device (KDA_OK, KDA_ERR_DEVICE_ARG or KDA_ERR_TIMEOUT), or

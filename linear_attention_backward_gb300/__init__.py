@@ -23,7 +23,8 @@ _LIB_PATH = os.path.join(_PKG, "_build", "libkda.so")
 
 KDA_OK = 0
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace",
-                4: "cuda error", 5: "timeout", 6: "bad cu_seqlens on device"}
+                4: "cuda error", 5: "timeout", 6: "bad cu_seqlens on device",
+                7: "too large for the no-allocation scratch"}
 KDA_FP32, KDA_BF16 = 0, 1
 
 
@@ -72,6 +73,10 @@ def lib():
         L.kda_bwd.restype = ctypes.c_int
         L.kda_bwd_timed.argtypes = [S] + [_VP] * 18 + [ctypes.c_size_t, _VP, _VP]
         L.kda_bwd_timed.restype = ctypes.c_int
+        L.kda_bwd_noalloc.argtypes = [S] + [_VP] * 16 + [_VP]
+        L.kda_bwd_noalloc.restype = ctypes.c_int
+        L.kda_noalloc_scratch_bytes.argtypes = []
+        L.kda_noalloc_scratch_bytes.restype = ctypes.c_size_t
         L.kda_get_device_status.argtypes = [_VP]
         L.kda_get_device_status.restype = ctypes.c_int
         L.kda_check_cu_seqlens_host.argtypes = [_VP, ctypes.c_int, ctypes.c_int]
@@ -192,3 +197,25 @@ def bwd(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, cu_seqlens=None, scale=No
     _check(st, "kda_bwd")
     o["_workspace"] = workspace
     return o
+
+
+def noalloc_scratch_bytes() -> int:
+    """Capacity of the fixed scratch array used by :func:`bwd_noalloc`."""
+    return int(lib().kda_noalloc_scratch_bytes())
+
+
+def bwd_noalloc(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, out, cu_seqlens=None,
+                scale=None, l2_eps=None):
+    """Backward pass through ``kda_bwd_noalloc``: for callers that cannot
+    allocate device memory, the library uses its own fixed scratch array
+    instead of a caller workspace.  ``out`` must hold preallocated dq, dk,
+    dv, dg, dbeta, dA_log and dh0; nothing is allocated here.  Raises
+    KdaError(7) when the problem does not fit the scratch array."""
+    shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2_eps=l2_eps)
+    st = lib().kda_bwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                               _ptr(beta), _ptr(A_log), _ptr(h0), _ptr(dO), _ptr(dh_T),
+                               _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                               _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["dA_log"]),
+                               _ptr(out.get("dh0")), _stream())
+    _check(st, "kda_bwd_noalloc")
+    return out

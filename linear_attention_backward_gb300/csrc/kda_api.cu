@@ -91,6 +91,7 @@ const char *kda_status_str(kda_status st) {
     case KDA_ERR_CUDA: return "CUDA error";
     case KDA_ERR_TIMEOUT: return "device-side wait timed out";
     case KDA_ERR_DEVICE_ARG: return "device found a malformed cu_seqlens table";
+    case KDA_ERR_TOO_LARGE: return "problem exceeds the fixed no-allocation scratch";
   }
   return "unknown status";
 }

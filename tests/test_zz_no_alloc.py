@@ -1,0 +1,74 @@
+"""kda_bwd_noalloc: the backward entry point for callers that cannot allocate
+device memory (it keeps its scratch in a fixed array inside the library
+instead of a caller workspace).  Its results must match kda_bwd's, call
+after call, and it must refuse problems larger than its fixed scratch.
+
+This file is named to be collected last, so that a failure here leaves every
+other test already run."""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+import linear_attention_backward_gb300 as kda
+from linear_attention_backward_gb300 import workloads as wl
+from kda_testutil import GRADS, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def _fresh_out(d, H, N, K, V):
+    o = {n: torch.full_like(d[m], float("nan")) for n, m in
+         (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
+    o["dA_log"] = torch.full((H,), float("nan"), dtype=torch.float32, device="cuda")
+    o["dh0"] = torch.full((N, H, K, V), float("nan"), dtype=torch.float32, device="cuda")
+    return o
+
+
+@pytest.mark.parametrize("case", ["fixed", "varlen"])
+def test_noalloc_matches_workspace_entry_point_twice(case):
+    if case == "fixed":
+        w = wl.custom("na", B=2, T=333, H=3, K=128, V=128, dtype="bf16", with_h0=True,
+                      with_dhT=True)
+        x = wl.make_inputs(w, seed=21)
+    else:
+        w = wl.custom("nav", H=2, K=128, V=128, dtype="bf16", with_h0=True, with_dhT=True,
+                      varlen=(4, 1, 300))
+        x = wl.make_inputs(w, seed=22, lengths=[130, 1, 0, 257])
+    d = to_dev(x)
+    ref = kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"], d["dO"],
+                  d["dhT"], cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    shape = kda.make_shape(d["q"], d["v"], cu_seqlens=d["cu_seqlens"])
+    assert kda.workspace_bytes(shape) <= kda.noalloc_scratch_bytes()
+    N, H = d["h0"].shape[:2]
+    for call in range(2):
+        out = _fresh_out(d, H, N, 128, 128)
+        kda.bwd_noalloc(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"], d["dO"],
+                        d["dhT"], cu_seqlens=d["cu_seqlens"], out=out)
+        torch.cuda.synchronize()
+        assert kda.get_device_status() == 0
+        for key in GRADS:
+            got = out[key].double().cpu().numpy()
+            exp = ref[key].double().cpu().numpy()
+            assert np.isfinite(got).all(), (call, key)
+            assert rel_l2(got, exp) <= 2e-2, (call, key, rel_l2(got, exp))
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    cap = kda.noalloc_scratch_bytes()
+    assert cap == 64 << 20
+    # the main workload needs far more scratch than the fixed array holds
+    big = kda.KdaShape(4, 8192, 32, 128, 128, 64, 0, None, 0.0, -1.0, kda.KDA_BF16)
+    assert kda.workspace_bytes(big) > cap
+    fake = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    import ctypes
+    p = ctypes.c_void_p(fake.data_ptr())
+    st = kda.lib().kda_bwd_noalloc(ctypes.byref(big), *([p] * 16), None)
+    assert st == 7
