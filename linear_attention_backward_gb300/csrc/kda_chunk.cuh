@@ -73,20 +73,77 @@ __device__ __forceinline__ bool slot_owner(const KdaParams &p, int64_t slot, int
 }
 
 // ---------------------------------------------------------------------------
+// Asynchronous staging of the chunk's raw rows into shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
+  // src-size 0 fills the 16 bytes with zeros (phantom rows)
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)),
+               "l"(gmem), "r"(valid ? 16 : 0));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
+
+// Rows [0, 64) of the head-h slice of a token-major [*, H, D] tensor starting
+// at token tok0, columns [col0, col0 + ncols), into dst (row stride ld
+// elements).  Rows >= len are zero-filled; their source is never read.
+template <typename E>
+__device__ __forceinline__ void stage_rows(E *dst, int ld, const void *src, int64_t tok0, int len,
+                                           int H, int h, int D, int col0, int ncols) {
+  constexpr int EPC = 16 / sizeof(E);  // elements per 16-byte chunk
+  const int cpr = ncols / EPC;          // chunks per row
+  const E *base = reinterpret_cast<const E *>(src);
+  for (int e = threadIdx.x; e < CHUNK * cpr; e += NTHREADS) {
+    const int i = e / cpr, c = (e % cpr) * EPC;
+    const bool valid = i < len;
+    const E *g = base + ((tok0 + (valid ? i : 0)) * H + h) * (int64_t)D + col0 + c;
+    cp_async16(dst + i * ld + c, g, valid);
+  }
+}
+
+// L2 prefetch of the same rows (used for the next chunk of a serial scan).
+__device__ __forceinline__ void prefetch_rows_l2(const void *src, int64_t tok0, int len, int H,
+                                                 int h, int rowbytes, int elem, int D,
+                                                 int col0) {
+  const char *base = reinterpret_cast<const char *>(src);
+  const int lines = (rowbytes + 127) / 128;
+  for (int e = threadIdx.x; e < len * lines; e += NTHREADS) {
+    const int i = e / lines, l = e % lines;
+    const char *ptr = base + (((tok0 + i) * H + h) * (int64_t)D + col0) * elem + 128 * l;
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(ptr));
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Shared-memory views used by the prep.
 // ---------------------------------------------------------------------------
 template <typename E, int K> struct PrepView {
-  float *gc;      // [64][LDF] fp32: gk, then gc, then (optionally) E = e^(gc - m)
-  float *m;       // [4][K]   block reference gates
+  float *m;       // [4][K]   scratch (block partial sums of the gate)
   float *em;      // [4][K]   e^(m_I)
   float *egm;     // [4][K]   e^(gT - m_I)
   float *F;       // [6][K]   e^(m_I - m_J), J < I, pair index I(I-1)/2 + J
   float *gT;      // [K]
   float *rq, *rk; // [64] 1 / sqrt(|x|^2 + eps)
   float *beta;    // [64]
+  float *part;    // [2 NTHREADS / K][K] column partial sums (scratch)
   static constexpr int LDF = K + 4;
   static constexpr int LD = tile_ld<E>(K);
+  static constexpr size_t floats = 19 * K + 3 * 64 + 2 * NTHREADS;
 };
+
+template <typename E, int K>
+__device__ __forceinline__ PrepView<E, K> make_view(float *s) {
+  PrepView<E, K> v;
+  v.m = s;
+  v.em = s + 4 * K;
+  v.egm = s + 8 * K;
+  v.F = s + 12 * K;
+  v.gT = s + 18 * K;
+  v.rq = s + 19 * K;
+  v.rk = v.rq + 64;
+  v.beta = v.rk + 64;
+  v.part = v.beta + 64;
+  return v;
+}
 
 __device__ __forceinline__ int pair_index(int I, int J) { return I * (I - 1) / 2 + J; }
 
@@ -102,44 +159,48 @@ template <typename E> struct PrepTiles {
   E *KD = nullptr;   // k^ e^gc
   E *KR = nullptr;   // k^ e^(gT - gc)
   E *QD = nullptr;   // scale * q^ e^gc
-  bool keep_E = false;  // leave E = e^(gc - m) in view.gc
+  float *Et = nullptr;  // optional fp32 [64][LDF]: E = e^(gc - m)
 };
 
-// Per-chunk prep.  Rows >= len are phantom rows: q = k = 0, beta = 0 and a
-// zero log-decay, so they change nothing and the last real row's gc is gT.
+// Stage the chunk's raw q (optional), k, g rows (cp.async, zero-filled past
+// len) and beta; the caller waits (cp_async_wait_all + __syncthreads) before
+// chunk_prep.
 template <typename E, int K>
-__device__ void chunk_prep(const KdaParams &p, int h, int64_t tok0, int len, bool need_q,
-                           const PrepView<E, K> &sv, const PrepTiles<E> &tiles) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = p.H;
-  const float A = __expf(p.A_log[h]);
-  constexpr int LDF = PrepView<E, K>::LDF;
+__device__ __forceinline__ void stage_chunk(const KdaParams &p, int h, int64_t tok0, int len,
+                                            bool need_q, E *Qr, E *Kr, E *Gr, float *beta) {
+  if (need_q) stage_rows<E>(Qr, K, p.q, tok0, len, p.H, h, K, 0, K);
+  stage_rows<E>(Kr, K, p.k, tok0, len, p.H, h, K, 0, K);
+  stage_rows<E>(Gr, K, p.g, tok0, len, p.H, h, K, 0, K);
+  if (threadIdx.x < CHUNK)
+    beta[threadIdx.x] =
+        threadIdx.x < len ? to_f(elem_ptr<E>(p.beta, (tok0 + threadIdx.x) * p.H + h)[0]) : 0.f;
+}
+
+// Per-chunk prep from the staged raw rows.  Rows >= len are phantom rows:
+// q = k = 0, beta = 0 and a zero log-decay, so they change nothing and the
+// last real row's gc is gT.
+template <typename E, int K>
+__device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, const E *Qr,
+                           const E *Kr, const E *Gr, const PrepView<E, K> &sv,
+                           const PrepTiles<E> &tiles) {
   constexpr int LD = PrepView<E, K>::LD;
-  // 1. log-decay gk (fp32) and beta
-  for (int e = tid; e < CHUNK * K; e += NTHREADS) {
-    const int i = e / K, c = e % K;
-    float gk = 0.f;
-    if (i < len) {
-      const float gv = to_f(elem_ptr<E>(p.g, ((tok0 + i) * H + h) * K)[c]);
-      gk = -A * softplus_f(gv);
-    }
-    sv.gc[i * LDF + c] = gk;
-  }
-  if (tid < CHUNK)
-    sv.beta[tid] = tid < len ? to_f(elem_ptr<E>(p.beta, (tok0 + tid) * H + h)[0]) : 0.f;
-  // 2. L2 norms (one warp per row)
+  constexpr int LDF = PrepView<E, K>::LDF;
+  constexpr int PAIRS = K / 2;               // column pairs
+  constexpr int PARTS = NTHREADS / PAIRS;    // row segments
+  constexpr int ROWS = CHUNK / PARTS;        // rows per segment (16 or 8)
+  static_assert(ROWS == 16 || ROWS == 8, "segment must tile the 16-row blocks");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float A = __expf(p.A_log[h]);
+  // 1. L2 norms: one warp per row, 4 (K = 128) or 2 (K = 64) channels per lane
   for (int i = warp; i < CHUNK; i += NWARPS) {
     float sk = 0.f, sq = 0.f;
-    if (i < len) {
-      const E *kr = elem_ptr<E>(p.k, ((tok0 + i) * H + h) * K);
-      const E *qr = elem_ptr<E>(p.q, ((tok0 + i) * H + h) * K);
-      for (int c = lane; c < K; c += 32) {
-        const float kv = to_f(kr[c]);
-        sk = fmaf(kv, kv, sk);
-        if (need_q) {
-          const float qv = to_f(qr[c]);
-          sq = fmaf(qv, qv, sq);
-        }
+#pragma unroll
+    for (int c = 2 * lane; c < K; c += 64) {
+      const float2 kv = load2(Kr + i * K + c);
+      sk = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, sk));
+      if (need_q) {
+        const float2 qv = load2(Qr + i * K + c);
+        sq = fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, sq));
       }
     }
     sk = warp_sum(sk);
@@ -149,62 +210,105 @@ __device__ void chunk_prep(const KdaParams &p, int h, int64_t tok0, int len, boo
       sv.rq[i] = rsqrtf(sq + p.eps);
     }
   }
+  // 2. gate log-decay and its running sum, two channels per thread, one
+  //    ROWS-row segment per thread, held in registers as sums local to the
+  //    segment.  Every exponent used below is formed from such local sums
+  //    (gc - m_I within a block, and block partials for m_I - m_J and
+  //    gT - m_I), never as a difference of two chunk-long sums, which would
+  //    cost ~|gc| * 2^-24 of absolute accuracy.
+  const int cp = tid % PAIRS, seg = tid / PAIRS;
+  const int c = 2 * cp, r0 = seg * ROWS;
+  const int I = r0 >> 4;  // 16-row block of this segment
+  float g0[ROWS], g1[ROWS];
+  float run0 = 0.f, run1 = 0.f;
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    const int i = r0 + r;
+    const float2 gv = load2(Gr + i * K + c);
+    const bool ok = i < len;
+    run0 += ok ? -A * softplus_f(gv.x) : 0.f;
+    run1 += ok ? -A * softplus_f(gv.y) : 0.f;
+    g0[r] = run0;
+    g1[r] = run1;
+  }
+  // block partials: Ablk = sum of rows 16I .. 16I+7 (through the reference
+  // row), Bblk = rows 16I+8 .. 16I+15
+  float *Ablk = sv.part, *Bblk = sv.m;  // [4][K] each (sv.m reused as scratch)
+  if (ROWS == 16) {
+    Ablk[I * K + c] = g0[7];
+    Ablk[I * K + c + 1] = g1[7];
+    Bblk[I * K + c] = g0[ROWS - 1] - g0[7];
+    Bblk[I * K + c + 1] = g1[ROWS - 1] - g1[7];
+  } else {
+    float *dst = (r0 & 15) ? Bblk : Ablk;
+    dst[I * K + c] = run0;
+    dst[I * K + c + 1] = run1;
+  }
   __syncthreads();
-  // 3. running sum over the chunk rows (one thread per channel)
-  if (tid < K) {
-    float run = 0.f;
-    for (int i = 0; i < CHUNK; ++i) {
-      run += sv.gc[i * LDF + tid];
-      sv.gc[i * LDF + tid] = run;
-      if ((i & 15) == 7) sv.m[(i >> 4) * K + tid] = run;
+  // 3. per-(block, channel) factors from the block partials
+  for (int e = tid; e < K; e += NTHREADS) {
+    float a[4], bb[4];
+#pragma unroll
+    for (int L = 0; L < 4; ++L) {
+      a[L] = Ablk[L * K + e];
+      bb[L] = Bblk[L * K + e];
     }
-    sv.gT[tid] = run;
-  }
-  __syncthreads();
-  for (int e = tid; e < 4 * K; e += NTHREADS) {
-    const int I = e / K, c = e % K;
-    const float mI = sv.m[I * K + c];
-    sv.em[e] = __expf(mI);
-    sv.egm[e] = __expf(sv.gT[c] - mI);
-  }
-  for (int e = tid; e < 6 * K; e += NTHREADS) {
-    const int pi = e / K, c = e % K;
-    const int I = pi < 1 ? 1 : (pi < 3 ? 2 : 3);
-    const int J = pi - pair_index(I, 0);
-    sv.F[e] = __expf(sv.m[I * K + c] - sv.m[J * K + c]);
-  }
-  __syncthreads();
-  // 4. operand tiles (two consecutive channels per thread)
-  for (int e = tid; e < CHUNK * K / 2; e += NTHREADS) {
-    const int i = e / (K / 2), c = 2 * (e % (K / 2));
-    const int I = i >> 4;
-    float kh0 = 0.f, kh1 = 0.f, qh0 = 0.f, qh1 = 0.f;
-    if (i < len) {
-      const float2 kv = load2(elem_ptr<E>(p.k, ((tok0 + i) * H + h) * K + c));
-      kh0 = kv.x * sv.rk[i];
-      kh1 = kv.y * sv.rk[i];
-      if (need_q) {
-        const float2 qv = load2(elem_ptr<E>(p.q, ((tok0 + i) * H + h) * K + c));
-        qh0 = qv.x * sv.rq[i];
-        qh1 = qv.y * sv.rq[i];
+    float before = 0.f, tot = 0.f;
+#pragma unroll
+    for (int L = 0; L < 4; ++L) tot += a[L] + bb[L];
+#pragma unroll
+    for (int L = 0; L < 4; ++L) {
+      float after = bb[L];
+#pragma unroll
+      for (int L2 = L + 1; L2 < 4; ++L2) after += a[L2] + bb[L2];
+      sv.em[L * K + e] = __expf(before + a[L]);   // e^(m_L)
+      sv.egm[L * K + e] = __expf(after);          // e^(gT - m_L)
+      before += a[L] + bb[L];
+    }
+#pragma unroll
+    for (int I2 = 1; I2 < 4; ++I2)
+#pragma unroll
+      for (int J = 0; J < I2; ++J) {
+        float d = bb[J] + a[I2];
+#pragma unroll
+        for (int L = J + 1; L < I2; ++L) d += a[L] + bb[L];
+        sv.F[pair_index(I2, J) * K + e] = __expf(d);  // e^(m_I - m_J)
       }
-    }
-    const float gc0 = sv.gc[i * LDF + c], gc1 = sv.gc[i * LDF + c + 1];
-    const float m0 = sv.m[I * K + c], m1 = sv.m[I * K + c + 1];
-    const float e0 = __expf(gc0 - m0), e1 = __expf(gc1 - m1);
-    const float ei0 = __expf(m0 - gc0), ei1 = __expf(m1 - gc1);
-    const float em0 = sv.em[I * K + c], em1 = sv.em[I * K + c + 1];
-    const float eg0 = sv.egm[I * K + c], eg1 = sv.egm[I * K + c + 1];
-    if (tiles.QM) store2(tiles.QM + i * LD + c, qh0 * e0, qh1 * e1);
+    sv.gT[e] = tot;
+  }
+  __syncthreads();
+  // 4. operand tiles.  gc_i - m_I from the segment's local sums: the
+  //    reference row 16I+7 lies in this segment (local index 7) unless the
+  //    segment is the second half of its block, where it is the row just
+  //    before the segment.
+  const bool ref_here = (r0 & 15) == 0;
+  const float ref0 = ref_here ? g0[7] : 0.f, ref1 = ref_here ? g1[7] : 0.f;
+  const float em0 = sv.em[I * K + c], em1 = sv.em[I * K + c + 1];
+  const float eg0 = sv.egm[I * K + c], eg1 = sv.egm[I * K + c + 1];
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    const int i = r0 + r;
+    const float2 kv = load2(Kr + i * K + c);
+    const float rk = sv.rk[i];
+    const float kh0 = kv.x * rk, kh1 = kv.y * rk;
+    const float d0 = g0[r] - ref0, d1 = g1[r] - ref1;
+    const float e0 = __expf(d0), e1 = __expf(d1);
+    const float ei0 = __expf(-d0), ei1 = __expf(-d1);
     if (tiles.KM) store2(tiles.KM + i * LD + c, kh0 * e0, kh1 * e1);
     if (tiles.KP) store2(tiles.KP + i * LD + c, kh0 * ei0, kh1 * ei1);
     if (tiles.KD) store2(tiles.KD + i * LD + c, (kh0 * e0) * em0, (kh1 * e1) * em1);
     if (tiles.KR) store2(tiles.KR + i * LD + c, (kh0 * ei0) * eg0, (kh1 * ei1) * eg1);
-    if (tiles.QD)
-      store2(tiles.QD + i * LD + c, p.scale * (qh0 * e0) * em0, p.scale * (qh1 * e1) * em1);
-    if (tiles.keep_E) {
-      sv.gc[i * LDF + c] = e0;
-      sv.gc[i * LDF + c + 1] = e1;
+    if (need_q) {
+      const float2 qv = load2(Qr + i * K + c);
+      const float rq = sv.rq[i];
+      const float qh0 = qv.x * rq, qh1 = qv.y * rq;
+      if (tiles.QM) store2(tiles.QM + i * LD + c, qh0 * e0, qh1 * e1);
+      if (tiles.QD)
+        store2(tiles.QD + i * LD + c, p.scale * (qh0 * e0) * em0, p.scale * (qh1 * e1) * em1);
+    }
+    if (tiles.Et) {
+      tiles.Et[i * LDF + c] = e0;
+      tiles.Et[i * LDF + c + 1] = e1;
     }
   }
   __syncthreads();
@@ -241,56 +345,85 @@ __device__ void intra_pairs(const E *QM, const E *KM, const E *KP, const float *
 }
 
 // ---------------------------------------------------------------------------
-// WY / UT inverse: INV = (I + A)^-1 with A_ij = beta_i G_ij (j < i), by 16x16
-// diagonal-block forward substitution followed by block forward substitution
-// for the off-diagonal blocks, all in fp32.  inv32 is [64][68] fp32 scratch,
-// tbuf holds 3 * 256 floats.  Output INV in E, [64][tile_ld(64)].
+// WY / UT inverse: INV = (I + A)^-1 with A_ij = beta_i G_ij (j < i), all fp32.
+// The four 16x16 diagonal blocks are inverted by forward substitution, one
+// warp per block with one column per lane held in registers; the off-diagonal
+// blocks follow by block forward substitution,
+//   X_IJ = -X_II sum_{J <= L < I} A_IL X_LJ,
+// one level (block row) at a time over all threads.  inv32 is [64][68] fp32
+// scratch, tbuf holds 3 * 256 floats.  Output INV in E, [64][ldi].
 // ---------------------------------------------------------------------------
 template <typename E>
 __device__ void wy_inverse(const float *G, int ldg, const float *beta, float *inv32, float *tbuf,
                            E *inv, int ldi) {
   constexpr int L32 = 68;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // zero everything above the diagonal blocks
   for (int e = tid; e < 64 * 64; e += NTHREADS) {
     const int r = e >> 6, c = e & 63;
     if ((c >> 4) > (r >> 4)) inv32[r * L32 + c] = 0.f;
   }
-  if (tid < 64) {
-    const int b = tid >> 4, c = tid & 15;
-    const int o = 16 * b;
+  if (warp < 4) {
+    const int o = 16 * warp, col = lane & 15;
+    float x[16];
+#pragma unroll
     for (int r = 0; r < 16; ++r) {
-      float x = (r == c) ? 1.f : 0.f;
       const float br = beta[o + r];
-      for (int j = c; j < r; ++j) x -= br * G[(o + r) * ldg + o + j] * inv32[(o + j) * L32 + o + c];
-      inv32[(o + r) * L32 + o + c] = (r >= c) ? x : 0.f;
+      const float *grow = G + (o + r) * ldg + o;
+      float s0 = (r == col) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < r; ++j) {
+        if (j & 1)
+          s1 = fmaf(-br * grow[j], x[j], s1);
+        else
+          s0 = fmaf(-br * grow[j], x[j], s0);
+      }
+      x[r] = s0 + s1;
+    }
+    if (lane < 16) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) inv32[(o + r) * L32 + o + col] = x[r];
     }
   }
   __syncthreads();
   for (int I = 1; I < 4; ++I) {
     for (int e = tid; e < I * 256; e += NTHREADS) {
-      const int J = e >> 8, r = (e >> 4) & 15, c = e & 15;
+      const int J = e >> 8, r = (e >> 4) & 15, cc = e & 15;
       const int row = 16 * I + r;
-      const float br = beta[row];
-      float t = 0.f;
-      for (int Lb = J; Lb < I; ++Lb)
-        for (int x = 0; x < 16; ++x)
-          t = fmaf(br * G[row * ldg + 16 * Lb + x], inv32[(16 * Lb + x) * L32 + 16 * J + c], t);
-      tbuf[e] = t;
+      const float *grow = G + row * ldg;
+      float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+      for (int Lb = J; Lb < I; ++Lb) {
+        const float *xc = inv32 + (16 * Lb) * L32 + 16 * J + cc;
+#pragma unroll
+        for (int x = 0; x < 16; x += 4) {
+          t0 = fmaf(grow[16 * Lb + x], xc[x * L32], t0);
+          t1 = fmaf(grow[16 * Lb + x + 1], xc[(x + 1) * L32], t1);
+          t2 = fmaf(grow[16 * Lb + x + 2], xc[(x + 2) * L32], t2);
+          t3 = fmaf(grow[16 * Lb + x + 3], xc[(x + 3) * L32], t3);
+        }
+      }
+      tbuf[e] = beta[row] * ((t0 + t1) + (t2 + t3));
     }
     __syncthreads();
     for (int e = tid; e < I * 256; e += NTHREADS) {
-      const int J = e >> 8, r = (e >> 4) & 15, c = e & 15;
-      float t = 0.f;
-      for (int x = 0; x < 16; ++x)
-        t = fmaf(inv32[(16 * I + r) * L32 + 16 * I + x], tbuf[(J << 8) + (x << 4) + c], t);
-      inv32[(16 * I + r) * L32 + 16 * J + c] = -t;
+      const int J = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+      const float *xr = inv32 + (16 * I + r) * L32 + 16 * I;
+      const float *tc = tbuf + (J << 8) + cc;
+      float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+#pragma unroll
+      for (int x = 0; x < 16; x += 4) {
+        t0 = fmaf(xr[x], tc[x << 4], t0);
+        t1 = fmaf(xr[x + 1], tc[(x + 1) << 4], t1);
+        t2 = fmaf(xr[x + 2], tc[(x + 2) << 4], t2);
+        t3 = fmaf(xr[x + 3], tc[(x + 3) << 4], t3);
+      }
+      inv32[(16 * I + r) * L32 + 16 * J + cc] = -((t0 + t1) + (t2 + t3));
     }
     __syncthreads();
   }
   for (int e = tid; e < 64 * 32; e += NTHREADS) {
-    const int r = e >> 5, c = 2 * (e & 31);
-    store2(inv + r * ldi + c, inv32[r * L32 + c], inv32[r * L32 + c + 1]);
+    const int r = e >> 5, cc = 2 * (e & 31);
+    store2(inv + r * ldi + cc, inv32[r * L32 + cc], inv32[r * L32 + cc + 1]);
   }
   __syncthreads();
 }

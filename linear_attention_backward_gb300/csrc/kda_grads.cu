@@ -29,9 +29,9 @@ template <typename E, int D> struct GradSmem {
   static constexpr int LDS = tile_ld<E>(64);
   static constexpr int LDF = D + 4;
   static constexpr size_t sz_E = 64 * LDF * 4;
-  // m, em, egm (4D each), F (6D), gT, dgT (D each), rq, rk, beta (64 each),
-  // rowdot (2 x 64), dbeta parts (4 x 64), partsum (NTHREADS), dA (8)
-  static constexpr size_t n_small = 12 * D + 6 * D + 2 * D + 3 * 64 + 2 * 64 + 4 * 64 + NTHREADS + 8;
+  // the prep view, then dgT (D) and dA (8); the dbeta parts and row dots
+  // reuse the view's column-partial scratch between the prep and the cumsum
+  static constexpr size_t n_small = PrepView<E, D>::floats + D + 8;
   static constexpr size_t sz_small = ((n_small * 4 + 127) / 128) * 128;
   static constexpr size_t sz_G = 64 * 68 * 4;
   static constexpr size_t sz_sq = 64 * LDS * sizeof(E);
@@ -51,6 +51,7 @@ template <typename E, int D> struct GradSmem {
   static constexpr size_t total = o_G + (sz_G > sz_tile ? sz_G : sz_tile);
   static_assert(D * LD * sizeof(E) <= 2 * sz_tile, "state tile must fit two chunk tiles");
   static_assert(64 * 68 * 4 + 768 * 4 <= 3 * sz_tile, "inverse scratch must fit in U, dO, V");
+  static_assert(3 * 64 * D * sizeof(E) <= 3 * sz_tile, "raw q, k, g must fit in U, dO, V");
   static_assert(64 * LDF * 4 <= sz_tile + (sz_G > sz_tile ? sz_G : sz_tile), "dgc must fit");
 };
 
@@ -76,21 +77,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
   // ---- shared memory views ----
   float *Eg = reinterpret_cast<float *>(smem + SM::o_E);
   float *sm = reinterpret_cast<float *>(smem + SM::o_small);
-  PrepView<E, D> sv;
-  sv.gc = Eg;
-  sv.m = sm;
-  sv.em = sm + 4 * D;
-  sv.egm = sm + 8 * D;
-  sv.F = sm + 12 * D;
-  sv.gT = sm + 18 * D;
-  float *dgT = sm + 19 * D;
-  sv.rq = sm + 20 * D;
-  sv.rk = sv.rq + 64;
-  sv.beta = sv.rk + 64;
-  float *rowdot = sv.beta + 64;     // [2][64]
-  float *dbp = rowdot + 128;        // [4][64]: dbeta1 halves, dbeta2 halves
-  float *partsum = dbp + 256;       // [NTHREADS / D][D]
-  float *dAred = partsum + NTHREADS;  // [8]
+  PrepView<E, D> sv = make_view<E, D>(sm);
+  float *dgT = sm + PrepView<E, D>::floats;  // [D]
+  float *dAred = dgT + D;           // [8]
+  float *dbp = sv.part;             // [4][64]: dbeta1 halves, dbeta2 halves
+  float *rowdot = sv.part + 256;    // [2][64]
+  float *partsum = sv.part;         // [NTHREADS / D][D], reused by the gate cumsum
   E *INV = reinterpret_cast<E *>(smem + SM::o_INV);
   E *MQK = reinterpret_cast<E *>(smem + SM::o_MQK);
   E *DA = reinterpret_cast<E *>(smem + SM::o_DA);
@@ -116,14 +108,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
 
   // ---- prep: norms, gates, operand tiles, pair matrices, inverse ----
   {
+    // raw q, k, g rows staged into the (still unused) U / dO / v tiles
+    E *Qr = reinterpret_cast<E *>(smem + SM::o_U);
+    E *Kr = Qr + 64 * D;
+    E *Gr = Kr + 64 * D;
+    stage_chunk<E, D>(p, h, tok0, len, true, Qr, Kr, Gr, sv.beta);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
     PrepTiles<E> tl;
     tl.QM = BIG1;
     tl.KM = BIG1 + 64 * LD;
     tl.KP = BIG2;
     tl.KD = BIG2 + 64 * LD;
     tl.KR = KRt;
-    tl.keep_E = true;
-    chunk_prep<E, D>(p, h, tok0, len, true, sv, tl);
+    tl.Et = Eg;
+    chunk_prep<E, D>(p, h, len, true, Qr, Kr, Gr, sv, tl);
   }
   intra_pairs<E, D>(BIG1, BIG1 + 64 * LD, BIG2, sv.F, G, 68, MQK, LDS, scale);
   __syncthreads();

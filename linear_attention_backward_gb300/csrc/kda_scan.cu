@@ -25,51 +25,34 @@ namespace kda {
 template <typename E, int K, int BV> struct ScanSmem {
   static constexpr int LD = tile_ld<E>(K);
   static constexpr int LDB = tile_ld<E>(BV);
-  static constexpr int LDF = K + 4;
   static constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
-  static constexpr size_t sz_gc = cmax(64 * LDF * 4, 64 * 68 * 4 + 768 * 4);
-  static constexpr size_t sz_small = (3 * 4 * K + 6 * K + K + 3 * 64) * 4;
+  static constexpr size_t sz_small = ((PrepView<E, K>::floats * 4 + 127) / 128) * 128;
+  static constexpr size_t sz_raw = 3 * 64 * K * sizeof(E);
   static constexpr size_t sz_tile = 64 * LD * sizeof(E);
   static constexpr size_t sz_band = 64 * LDB * sizeof(E);
-  static constexpr size_t sz_G = cmax(64 * 68 * 4, sz_band);
+  static constexpr size_t sz_G = 64 * 68 * 4;
   static constexpr size_t sz_sq = 64 * tile_ld<E>(64) * sizeof(E);
   static constexpr size_t sz_state = K * LDB * sizeof(E);
   // offsets
-  static constexpr size_t o_gc = 0;                       // gc, later inv32 + tbuf
-  static constexpr size_t o_small = o_gc + sz_gc;
-  static constexpr size_t o_QM = o_small + sz_small;      // QM, KM, KP; later stateT, U
-  static constexpr size_t o_KM = o_QM + sz_tile;
-  static constexpr size_t o_KP = o_KM + sz_tile;
+  static constexpr size_t o_small = 0;
+  static constexpr size_t o_raw = o_small + sz_small;     // raw q, k, g; later G and W
+  static constexpr size_t o_QM = o_raw + cmax(sz_raw, sz_G + sz_band);
+  static constexpr size_t o_KM = o_QM + sz_tile;          // QM, KM, KP; later inverse
+  static constexpr size_t o_KP = o_KM + sz_tile;          // scratch, then state + U
   static constexpr size_t o_KD = o_KP + sz_tile;
   static constexpr size_t o_KR = o_KD + sz_tile;
   static constexpr size_t o_QD = o_KR + sz_tile;
-  static constexpr size_t o_G = o_QD + sz_tile;           // G, later W
-  static constexpr size_t o_INV = o_G + sz_G;
+  static constexpr size_t o_INV = o_QD + sz_tile;
   static constexpr size_t o_MQK = o_INV + sz_sq;
   static constexpr size_t o_BAND = o_MQK + sz_sq;         // v band (fwd) / dO band (bwd)
   static constexpr size_t total = o_BAND + sz_band;
-  static constexpr size_t o_STATE = o_QM;                 // aliases QM/KM/KP after intra_pairs
+  static constexpr size_t o_G = o_raw;
+  static constexpr size_t o_W = o_raw + sz_G;
+  static constexpr size_t o_STATE = o_QM;
   static constexpr size_t o_U = o_QM + sz_state;
   static_assert(sz_state + sz_band <= 3 * sz_tile, "state + U must fit in QM/KM/KP");
-  static_assert(sz_band <= sz_G, "W must fit in G");
-  static_assert(64 * 68 * 4 + 768 * 4 <= sz_gc, "inverse scratch must fit in gc");
+  static_assert(64 * 68 * 4 + 768 * 4 <= 3 * sz_tile, "inverse scratch must fit in QM/KM/KP");
 };
-
-template <typename E, int K>
-__device__ __forceinline__ PrepView<E, K> make_view(char *smem, size_t o_gc, size_t o_small) {
-  PrepView<E, K> v;
-  v.gc = reinterpret_cast<float *>(smem + o_gc);
-  float *s = reinterpret_cast<float *>(smem + o_small);
-  v.m = s;
-  v.em = s + 4 * K;
-  v.egm = s + 8 * K;
-  v.F = s + 12 * K;
-  v.gT = s + 18 * K;
-  v.rq = s + 19 * K;
-  v.rk = v.rq + 64;
-  v.beta = v.rk + 64;
-  return v;
-}
 
 template <typename E, int K, int BV>
 __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
@@ -95,7 +78,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
   const int nck = (L + CHUNK - 1) / CHUNK;
   const int v0 = band * BV;
 
-  PrepView<E, K> sv = make_view<E, K>(smem, SM::o_gc, SM::o_small);
+  PrepView<E, K> sv = make_view<E, K>(reinterpret_cast<float *>(smem + SM::o_small));
+  E *Qr = reinterpret_cast<E *>(smem + SM::o_raw);
+  E *Kr = Qr + 64 * K;
+  E *Gr = Kr + 64 * K;
   E *QM = reinterpret_cast<E *>(smem + SM::o_QM);
   E *KM = reinterpret_cast<E *>(smem + SM::o_KM);
   E *KP = reinterpret_cast<E *>(smem + SM::o_KP);
@@ -103,14 +89,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
   E *KR = reinterpret_cast<E *>(smem + SM::o_KR);
   E *QD = reinterpret_cast<E *>(smem + SM::o_QD);
   float *G = reinterpret_cast<float *>(smem + SM::o_G);
-  E *W = reinterpret_cast<E *>(smem + SM::o_G);
+  E *W = reinterpret_cast<E *>(smem + SM::o_W);
   E *INV = reinterpret_cast<E *>(smem + SM::o_INV);
   E *MQK = reinterpret_cast<E *>(smem + SM::o_MQK);
   E *BAND = reinterpret_cast<E *>(smem + SM::o_BAND);
   E *ST = reinterpret_cast<E *>(smem + SM::o_STATE);
   E *UB = reinterpret_cast<E *>(smem + SM::o_U);
-  float *inv32 = sv.gc;
-  float *tbuf = sv.gc + 64 * 68;
+  float *inv32 = reinterpret_cast<float *>(smem + SM::o_QM);
+  float *tbuf = inv32 + 64 * 68;
 
   // state rows owned by this warp
   const int srow0 = 16 * (warp % WM);
@@ -133,16 +119,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
     const int len = min(CHUNK, L - j * CHUNK);
     const int64_t slot = slot0 + j;
     __syncthreads();
-    // band rows of v (fwd) or dO (bwd)
-    {
-      const void *src = role == 0 ? p.v : p.dO;
-      for (int e = tid; e < CHUNK * BV / 2; e += NTHREADS) {
-        const int i = e / (BV / 2), c = 2 * (e % (BV / 2));
-        float2 x = make_float2(0.f, 0.f);
-        if (i < len) x = load2(elem_ptr<E>(src, ((tok0 + i) * H + h) * Vtot + v0 + c));
-        store2(BAND + i * LDB + c, x.x, x.y);
-      }
+    // stage this chunk's raw rows and the v (fwd) / dO (bwd) band; prefetch
+    // the next chunk's rows into L2 while this one is processed
+    const void *bsrc = role == 0 ? p.v : p.dO;
+    stage_chunk<E, K>(p, h, tok0, len, role == 1, Qr, Kr, Gr, sv.beta);
+    stage_rows<E>(BAND, LDB, bsrc, tok0, len, H, h, Vtot, v0, BV);
+    cp_async_commit();
+    if (it + 1 < nck) {
+      const int jn = role == 0 ? j + 1 : j - 1;
+      const int64_t tn = tok_seq + (int64_t)jn * CHUNK;
+      const int ln = min(CHUNK, L - jn * CHUNK);
+      const int es = sizeof(E);
+      prefetch_rows_l2(p.k, tn, ln, H, h, K * es, es, K, 0);
+      prefetch_rows_l2(p.g, tn, ln, H, h, K * es, es, K, 0);
+      prefetch_rows_l2(bsrc, tn, ln, H, h, BV * es, es, Vtot, v0);
+      if (role == 1) prefetch_rows_l2(p.q, tn, ln, H, h, K * es, es, K, 0);
     }
+    cp_async_wait_all();
+    __syncthreads();
     PrepTiles<E> tl;
     tl.KM = KM;
     tl.KP = KP;
@@ -152,7 +146,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
       tl.QM = QM;
       tl.QD = QD;
     }
-    chunk_prep<E, K>(p, h, tok0, len, role == 1, sv, tl);
+    chunk_prep<E, K>(p, h, len, role == 1, Qr, Kr, Gr, sv, tl);
     intra_pairs<E, K>(QM, KM, KP, sv.F, G, 68, role == 1 ? MQK : nullptr, tile_ld<E>(64), p.scale);
     __syncthreads();
     wy_inverse<E>(G, 68, sv.beta, inv32, tbuf, INV, tile_ld<E>(64));
