@@ -173,6 +173,16 @@ kda_status kda_bwd_noalloc(const kda_shape *shape, const void *q, const void *k,
 /* Capacity in bytes of kda_bwd_noalloc's fixed scratch array. */
 size_t kda_noalloc_scratch_bytes(void);
 
+/* Device self-test of the fifth-generation tensor-core path (no counterpart
+ * on the pages): computes D = A B^T for one M = 128 tile through shared-memory
+ * descriptors, Tensor Memory and tcgen05 loads, with A ([128][K] bf16,
+ * row-major, device) and B ([N][K] bf16, row-major, device) staged in K-major
+ * (0) or MN-major (1) core-matrix layout; D is [128][N] fp32 (device).
+ * N in {32, 64, 128}, K a multiple of 16 up to 128.  swap_lbo_sbo exchanges
+ * the two descriptor strides (a diagnostic of the encoding). */
+kda_status kda_selftest_umma(const void *A, const void *B, float *D, int N, int K, int a_mn,
+                             int b_mn, int swap_lbo_sbo, kda_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device (KDA_OK, KDA_ERR_DEVICE_ARG or KDA_ERR_TIMEOUT), or
  * KDA_ERR_CUDA if the synchronisation itself reported an error. */

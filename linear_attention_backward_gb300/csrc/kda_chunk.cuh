@@ -100,6 +100,18 @@ __device__ __forceinline__ void stage_rows(E *dst, int ld, const void *src, int6
   }
 }
 
+// A dense row-major [rows][cols] matrix (row stride cols) into dst (row
+// stride ld elements).
+template <typename E>
+__device__ __forceinline__ void stage_dense(E *dst, int ld, const E *src, int rows, int cols) {
+  constexpr int EPC = 16 / sizeof(E);
+  const int cpr = cols / EPC;
+  for (int e = threadIdx.x; e < rows * cpr; e += NTHREADS) {
+    const int r = e / cpr, c = (e % cpr) * EPC;
+    cp_async16(dst + r * ld + c, src + (int64_t)r * cols + c, true);
+  }
+}
+
 // L2 prefetch of the same rows (used for the next chunk of a serial scan).
 __device__ __forceinline__ void prefetch_rows_l2(const void *src, int64_t tok0, int len, int H,
                                                  int h, int rowbytes, int elem, int D,
@@ -353,6 +365,55 @@ __device__ void intra_pairs(const E *QM, const E *KM, const E *KP, const float *
 // one level (block row) at a time over all threads.  inv32 is [64][68] fp32
 // scratch, tbuf holds 3 * 256 floats.  Output INV in E, [64][ldi].
 // ---------------------------------------------------------------------------
+// One level of the block forward substitution: block row I, all J < I.
+// Thread t owns row r = t / 4 % 16 and columns 4 (t % 4) .. + 4 of one J
+// block; X rows are read as float4, G rows once per thread.
+template <int I>
+__device__ __forceinline__ void inv_level(const float *G, int ldg, const float *beta,
+                                          float *inv32, float *tbuf) {
+  constexpr int L32 = 68;
+  const int tid = threadIdx.x;
+  const int J = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+  const int row = 16 * I + r;
+  if (J < I) {
+    const float *grow = G + row * ldg;
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int Lb = 0; Lb < I; ++Lb) {
+      if (Lb < J) continue;
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const float gv = grow[16 * Lb + x];
+        const float4 xv = *reinterpret_cast<const float4 *>(inv32 + (16 * Lb + x) * L32 + 16 * J + c4);
+        t.x = fmaf(gv, xv.x, t.x);
+        t.y = fmaf(gv, xv.y, t.y);
+        t.z = fmaf(gv, xv.z, t.z);
+        t.w = fmaf(gv, xv.w, t.w);
+      }
+    }
+    const float br = beta[row];
+    *reinterpret_cast<float4 *>(tbuf + (J << 8) + (r << 4) + c4) =
+        make_float4(br * t.x, br * t.y, br * t.z, br * t.w);
+  }
+  __syncthreads();
+  if (J < I) {
+    const float *xr = inv32 + row * L32 + 16 * I;
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+      const float xv = xr[x];
+      const float4 tv = *reinterpret_cast<const float4 *>(tbuf + (J << 8) + (x << 4) + c4);
+      t.x = fmaf(xv, tv.x, t.x);
+      t.y = fmaf(xv, tv.y, t.y);
+      t.z = fmaf(xv, tv.z, t.z);
+      t.w = fmaf(xv, tv.w, t.w);
+    }
+    *reinterpret_cast<float4 *>(inv32 + row * L32 + 16 * J + c4) =
+        make_float4(-t.x, -t.y, -t.z, -t.w);
+  }
+  __syncthreads();
+}
+
 template <typename E>
 __device__ void wy_inverse(const float *G, int ldg, const float *beta, float *inv32, float *tbuf,
                            E *inv, int ldi) {
@@ -386,41 +447,9 @@ __device__ void wy_inverse(const float *G, int ldg, const float *beta, float *in
     }
   }
   __syncthreads();
-  for (int I = 1; I < 4; ++I) {
-    for (int e = tid; e < I * 256; e += NTHREADS) {
-      const int J = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-      const int row = 16 * I + r;
-      const float *grow = G + row * ldg;
-      float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
-      for (int Lb = J; Lb < I; ++Lb) {
-        const float *xc = inv32 + (16 * Lb) * L32 + 16 * J + cc;
-#pragma unroll
-        for (int x = 0; x < 16; x += 4) {
-          t0 = fmaf(grow[16 * Lb + x], xc[x * L32], t0);
-          t1 = fmaf(grow[16 * Lb + x + 1], xc[(x + 1) * L32], t1);
-          t2 = fmaf(grow[16 * Lb + x + 2], xc[(x + 2) * L32], t2);
-          t3 = fmaf(grow[16 * Lb + x + 3], xc[(x + 3) * L32], t3);
-        }
-      }
-      tbuf[e] = beta[row] * ((t0 + t1) + (t2 + t3));
-    }
-    __syncthreads();
-    for (int e = tid; e < I * 256; e += NTHREADS) {
-      const int J = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-      const float *xr = inv32 + (16 * I + r) * L32 + 16 * I;
-      const float *tc = tbuf + (J << 8) + cc;
-      float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
-#pragma unroll
-      for (int x = 0; x < 16; x += 4) {
-        t0 = fmaf(xr[x], tc[x << 4], t0);
-        t1 = fmaf(xr[x + 1], tc[(x + 1) << 4], t1);
-        t2 = fmaf(xr[x + 2], tc[(x + 2) << 4], t2);
-        t3 = fmaf(xr[x + 3], tc[(x + 3) << 4], t3);
-      }
-      inv32[(16 * I + r) * L32 + 16 * J + cc] = -((t0 + t1) + (t2 + t3));
-    }
-    __syncthreads();
-  }
+  inv_level<1>(G, ldg, beta, inv32, tbuf);
+  inv_level<2>(G, ldg, beta, inv32, tbuf);
+  inv_level<3>(G, ldg, beta, inv32, tbuf);
   for (int e = tid; e < 64 * 32; e += NTHREADS) {
     const int r = e >> 5, cc = 2 * (e & 31);
     store2(inv + r * ldi + cc, inv32[r * L32 + cc], inv32[r * L32 + cc + 1]);

@@ -97,7 +97,7 @@ __device__ __forceinline__ void warp_gemm(float (&acc)[NF][4], const bf16 *a, in
                                           const float *kscale = nullptr) {
   static_assert(NF % 2 == 0, "NF must be even");
   const int lane = threadIdx.x & 31;
-#pragma unroll 2
+#pragma unroll
   for (int k0 = 0; k0 < kdim; k0 += 16) {
     uint32_t af[4];
     if (AK)
@@ -197,8 +197,9 @@ __device__ __forceinline__ float quad_sum(float v) {
 }
 
 __device__ __forceinline__ float softplus_f(float x) {
-  // log(1 + e^x) = max(x, 0) + log1p(e^-|x|)
-  return fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x)));
+  // log(1 + e^x) = max(x, 0) + log(1 + e^-|x|); the second term is in
+  // (0, log 2], where the fast log's absolute error (~1e-7) is harmless
+  return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
 }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + __expf(-x)); }
 

@@ -128,18 +128,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
   intra_pairs<E, D>(BIG1, BIG1 + 64 * LD, BIG2, sv.F, G, 68, MQK, LDS, scale);
   __syncthreads();
   wy_inverse<E>(G, 68, sv.beta, inv32, tbuf, INV, LDS);
-  // S_n -> BIG1, v -> Vt
-  for (int e = tid; e < D * D / 2; e += NTHREADS) {
-    const int r = e / (D / 2), c = 2 * (e % (D / 2));
-    const float2 x = load2(Sg + (size_t)r * D + c);
-    store2(BIG1 + r * LD + c, x.x, x.y);
-  }
-  for (int e = tid; e < 64 * D / 2; e += NTHREADS) {
-    const int i = e / (D / 2), c = 2 * (e % (D / 2));
-    float2 x = make_float2(0.f, 0.f);
-    if (i < len) x = load2(elem_ptr<E>(p.v, ((tok0 + i) * H + h) * D + c));
-    store2(Vt + i * LD + c, x.x, x.y);
-  }
+  // S_n -> BIG1, v -> Vt, asynchronously
+  stage_dense<E>(BIG1, LD, Sg, D, D);
+  stage_rows<E>(Vt, LD, p.v, tok0, len, H, h, D, 0, D);
+  cp_async_commit();
+  cp_async_wait_all();
   __syncthreads();
 
   float acc[NF][4], tmp[NF][4], dkr[NF][4];
@@ -154,19 +147,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
   // ---- U = INV diag(beta) Xr ; load dS_{n+1} -> BIG2, dO -> DOt ----
   zero_acc(acc);
   warp_gemm<NF, true, false>(acc, INV + 16 * rb * LDS, LDS, Vt + ch, LD, 64, sv.beta);
-  for (int e = tid; e < D * D / 2; e += NTHREADS) {
-    const int r = e / (D / 2), c = 2 * (e % (D / 2));
-    const float2 x = load2(dSg + (size_t)r * D + c);
-    store2(BIG2 + r * LD + c, x.x, x.y);
-  }
-  __syncthreads();  // everyone is done with inv32 (in Ut) and KD (in BIG2)
+  // dS_{n+1} -> BIG2 (kd is dead), dO -> DOt (inverse scratch is dead)
+  stage_dense<E>(BIG2, LD, dSg, D, D);
+  stage_rows<E>(DOt, LD, p.dO, tok0, len, H, h, D, 0, D);
+  cp_async_commit();
   store_acc(Ut + 16 * rb * LD + ch, LD, acc);
-  for (int e = tid; e < 64 * D / 2; e += NTHREADS) {
-    const int i = e / (D / 2), c = 2 * (e % (D / 2));
-    float2 x = make_float2(0.f, 0.f);
-    if (i < len) x = load2(elem_ptr<E>(p.dO, ((tok0 + i) * H + h) * D + c));
-    store2(DOt + i * LD + c, x.x, x.y);
-  }
+  cp_async_wait_all();
   __syncthreads();
 
   // ---- B1: dU = scale Mqk^T dO + kr dS ; dkr = U dS^T ; B0: p ----
@@ -175,43 +161,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
   warp_gemm<NF, true, false>(acc, KRt + 16 * rb * LD, LD, BIG2 + ch, LD, D);
   zero_acc(dkr);
   warp_gemm<NF, true, true>(dkr, Ut + 16 * rb * LD, LD, BIG2 + ch * LD, LD, D);
-  {
-    // dkr' = dkr e^(gT - gc) and its contribution sum_i dkr' k^ to dgT
-    float colp[NF][2];
-#pragma unroll
-    for (int f = 0; f < NF; ++f) colp[f][0] = colp[f][1] = 0.f;
-    const int r0 = lane >> 2, c0 = 2 * (lane & 3);
-#pragma unroll
-    for (int f = 0; f < NF; ++f) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int i = 16 * rb + r0 + 8 * hh;
-        const int c = ch + 8 * f + c0;
-        float kh0 = 0.f, kh1 = 0.f;
-        if (i < len) {
-          const float2 kv = load2(elem_ptr<E>(p.k, ((tok0 + i) * H + h) * D + c));
-          kh0 = kv.x * sv.rk[i];
-          kh1 = kv.y * sv.rk[i];
-        }
-        const float f0 = sv.egm[rb * D + c] / Eg[i * LDF + c];
-        const float f1 = sv.egm[rb * D + c + 1] / Eg[i * LDF + c + 1];
-        dkr[f][2 * hh] *= f0;
-        dkr[f][2 * hh + 1] *= f1;
-        colp[f][0] = fmaf(dkr[f][2 * hh], kh0, colp[f][0]);
-        colp[f][1] = fmaf(dkr[f][2 * hh + 1], kh1, colp[f][1]);
-      }
-    }
-#pragma unroll
-    for (int f = 0; f < NF; ++f)
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        float v = colp[f][x];
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        if ((lane >> 2) == 0) atomicAdd(&dgT[ch + 8 * f + c0 + x], v);
-      }
-  }
+  // dkr' = dkr e^(gT - gc) (its column sums enter dgT in pass 2)
+  for_acc(dkr, [&](int r, int c, float &x) {
+    const int i = 16 * rb + r, cc = ch + c;
+    x *= sv.egm[rb * D + cc] / Eg[i * LDF + cc];
+  });
   // p_c = e^gT_c sum_d dS_cd S_cd  (D rows, 256 / D threads per row)
   {
     constexpr int TPR = NTHREADS / D;
@@ -300,13 +254,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
     const float db = dbp[tid] + dbp[64 + tid] + dbp[128 + tid] + dbp[192 + tid];
     reinterpret_cast<E *>(p.dbeta)[(tok0 + tid) * H + h] = from_f<E>(db);
   }
+  // raw q, k rows -> the v / G tiles (both dead after B3), in flight while
+  // the inter-chunk products run
+  E *Qraw = Vt, *Kraw = Vt + 64 * D;
+  stage_rows<E>(Qraw, D, p.q, tok0, len, H, h, D, 0, D);
+  stage_rows<E>(Kraw, D, p.k, tok0, len, H, h, D, 0, D);
+  cp_async_commit();
   // ---- B2 inter-chunk products while S_n and dO are resident ----
   float bq[NF][4], bk[NF][4];
   zero_acc(bq);
   zero_acc(bk);
   warp_gemm<NF, true, true>(bq, DOt + 16 * rb * LD, LD, BIG1 + ch * LD, LD, D);  // dO S^T
   warp_gemm<NF, true, true>(bk, KRt + 16 * rb * LD, LD, BIG1 + ch * LD, LD, D);  // dvcorr S^T
-  __syncthreads();  // S_n (BIG1) and dO (DOt) are dead from here on
+  __syncthreads();  // S_n (BIG1), dO (DOt) and dvcorr (KRt) are dead from here on
+  // raw g rows -> KRt, for the gate epilogue
+  E *Graw = KRt;
+  stage_rows<E>(Graw, D, p.g, tok0, len, H, h, D, 0, D);
+  cp_async_commit();
+  asm volatile("cp.async.wait_group 1;\n" ::);  // q, k have landed
+  __syncthreads();
   // Operands of the intra-chunk gradient products, rebuilt in fp32 from q, k
   // and E.  These products feed the gate gradient, whose reverse cumulative
   // sum cancels them pairwise; bf16 rounding of the keys / queries alone
@@ -318,15 +284,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
   constexpr bool kSplit = sizeof(E) == 2;
   for (int e = tid; e < 64 * D / 2; e += NTHREADS) {
     const int i = e / (D / 2), c = 2 * (e % (D / 2));
-    float q0 = 0.f, q1 = 0.f, k0 = 0.f, k1 = 0.f;
-    if (i < len) {
-      const float2 qv = load2(elem_ptr<E>(p.q, ((tok0 + i) * H + h) * D + c));
-      const float2 kv = load2(elem_ptr<E>(p.k, ((tok0 + i) * H + h) * D + c));
-      q0 = qv.x * sv.rq[i];
-      q1 = qv.y * sv.rq[i];
-      k0 = kv.x * sv.rk[i];
-      k1 = kv.y * sv.rk[i];
-    }
+    const float2 qv = load2(Qraw + i * D + c);
+    const float2 kv = load2(Kraw + i * D + c);
+    const float q0 = qv.x * sv.rq[i], q1 = qv.y * sv.rq[i];
+    const float k0 = kv.x * sv.rk[i], k1 = kv.y * sv.rk[i];
     const float e0 = Eg[i * LDF + c], e1 = Eg[i * LDF + c + 1];
     const float x[6] = {q0 * e0, q1 * e1, k0 * e0, k1 * e1, k0 / e0, k1 / e1};
     E *hi[3] = {QMt, KMt, KPt};
@@ -341,6 +302,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
     }
   }
   __syncthreads();
+  // normalised q / k of an element from the resident operand tiles
+  auto qhat = [&](int i, int c) {
+    float x = to_f(QMt[i * LD + c]);
+    if (kSplit) x += to_f(QMl[i * LD + c]);
+    return x / Eg[i * LDF + c];
+  };
+  auto khat = [&](int i, int c) {
+    float x = to_f(KMt[i * LD + c]);
+    if (kSplit) x += to_f(KMl[i * LD + c]);
+    return x / Eg[i * LDF + c];
+  };
 
   const int r0 = lane >> 2, c0 = 2 * (lane & 3);
   // W_I,J (16 x 16 block of W) times the hi + lo operand rows of block J
@@ -379,8 +351,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
         const float gam = Ev * sv.em[rb * D + c];
         const float dqh = scale * gam * bq[f][e] + Ev * intra[f][e];
         bq[f][e] = dqh;
-        float qh = 0.f;
-        if (i < len) qh = to_f(elem_ptr<E>(p.q, ((tok0 + i) * H + h) * D + c)[0]) * sv.rq[i];
+        const float qh = qhat(i, c);
         tmp[f][e] = qh;
         dgc[i * LDF + c] = dqh * qh;
         rp[e >> 1] = fmaf(dqh, qh, rp[e >> 1]);
@@ -445,6 +416,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
         }
     }
     float rp[2] = {0.f, 0.f};
+    float colp[NF][2];
+#pragma unroll
+    for (int f = 0; f < NF; ++f) colp[f][0] = colp[f][1] = 0.f;
 #pragma unroll
     for (int f = 0; f < NF; ++f)
 #pragma unroll
@@ -455,12 +429,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
         const float dkd = bk[f][e];
         const float dkh = dkd + dki + dkr[f][e];
         const float dks = dkd - dki - dkr[f][e];
-        float kh = 0.f;
-        if (i < len) kh = to_f(elem_ptr<E>(p.k, ((tok0 + i) * H + h) * D + c)[0]) * sv.rk[i];
+        const float kh = khat(i, c);
         bk[f][e] = dkh;
         tmp[f][e] = kh;
         dgc[i * LDF + c] += dks * kh;
         rp[e >> 1] = fmaf(dkh, kh, rp[e >> 1]);
+        colp[f][e & 1] = fmaf(dkr[f][e], kh, colp[f][e & 1]);
+      }
+    // dgT += sum over the chunk rows of dkr' k^ (same k^ as the cancelling term)
+#pragma unroll
+    for (int f = 0; f < NF; ++f)
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        float v = colp[f][x];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        if ((lane >> 2) == 0) atomicAdd(&dgT[ch + 8 * f + c0 + x], v);
       }
     rp[0] = quad_sum(rp[0]);
     rp[1] = quad_sum(rp[1]);
@@ -484,6 +469,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
         }
       }
   }
+  cp_async_wait_all();  // raw g
   __syncthreads();
 
   // ---- K1: reverse cumsum of dgc over the chunk rows, dg, dA_log ----
@@ -504,7 +490,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
     for (int i = ra + SEG - 1; i >= ra; --i) {
       run += dgc[i * LDF + c];
       if (i < len) {
-        const float gv = to_f(elem_ptr<E>(p.g, ((tok0 + i) * H + h) * D)[c]);
+        const float gv = to_f(Graw[i * D + c]);
         const float gk = -A * softplus_f(gv);
         dgg[((tok0 + i) * H + h) * D + c] = from_f<E>(run * (-A) * sigmoid_f(gv));
         dA = fmaf(run, gk, dA);

@@ -35,8 +35,10 @@ template <typename E, int K, int BV> struct ScanSmem {
   static constexpr size_t sz_state = K * LDB * sizeof(E);
   // offsets
   static constexpr size_t o_small = 0;
-  static constexpr size_t o_raw = o_small + sz_small;     // raw q, k, g; later G and W
-  static constexpr size_t o_QM = o_raw + cmax(sz_raw, sz_G + sz_band);
+  static constexpr size_t o_raw = o_small + sz_small;     // raw q, k, g (next chunk's
+                                                          // land here during the chain)
+  static constexpr size_t o_G = o_raw + sz_raw;           // G, later W
+  static constexpr size_t o_QM = o_G + cmax(sz_G, sz_band);
   static constexpr size_t o_KM = o_QM + sz_tile;          // QM, KM, KP; later inverse
   static constexpr size_t o_KP = o_KM + sz_tile;          // scratch, then state + U
   static constexpr size_t o_KD = o_KP + sz_tile;
@@ -46,8 +48,7 @@ template <typename E, int K, int BV> struct ScanSmem {
   static constexpr size_t o_MQK = o_INV + sz_sq;
   static constexpr size_t o_BAND = o_MQK + sz_sq;         // v band (fwd) / dO band (bwd)
   static constexpr size_t total = o_BAND + sz_band;
-  static constexpr size_t o_G = o_raw;
-  static constexpr size_t o_W = o_raw + sz_G;
+  static constexpr size_t o_W = o_G;
   static constexpr size_t o_STATE = o_QM;
   static constexpr size_t o_U = o_QM + sz_state;
   static_assert(sz_state + sz_band <= 3 * sz_tile, "state + U must fit in QM/KM/KP");
@@ -113,29 +114,44 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
   const int rb = warp & 3;            // chunk-row block of this warp
   const int ch = (warp >> 2) * (BV / 2);  // column half of the band
 
+  const void *bsrc = role == 0 ? p.v : p.dO;
+  const int es = sizeof(E);
+  auto chunk_rows = [&](int jj, int64_t &t0, int &ln) {
+    t0 = tok_seq + (int64_t)jj * CHUNK;
+    ln = min(CHUNK, L - jj * CHUNK);
+  };
+  // Pipeline: the raw q / k / g rows of chunk j+1 are copied (cp.async)
+  // while chunk j's intra products, inverse and chain run; the v / dO band
+  // of chunk j+1 while... after chunk j's chain.  Commit groups alternate
+  // raw(j), band(j), raw(j+1), band(j+1), ...
+  if (nck > 0) {
+    int64_t t0;
+    int ln;
+    chunk_rows(role == 0 ? 0 : nck - 1, t0, ln);
+    stage_chunk<E, K>(p, h, t0, ln, role == 1, Qr, Kr, Gr, sv.beta);
+    cp_async_commit();
+    stage_rows<E>(BAND, LDB, bsrc, t0, ln, H, h, Vtot, v0, BV);
+    cp_async_commit();
+  }
+  float beta_next = 0.f;
   for (int it = 0; it < nck; ++it) {
     const int j = role == 0 ? it : nck - 1 - it;
-    const int64_t tok0 = tok_seq + (int64_t)j * CHUNK;
-    const int len = min(CHUNK, L - j * CHUNK);
+    const int jn = role == 0 ? j + 1 : j - 1;
+    int64_t tok0;
+    int len;
+    chunk_rows(j, tok0, len);
     const int64_t slot = slot0 + j;
-    __syncthreads();
-    // stage this chunk's raw rows and the v (fwd) / dO (bwd) band; prefetch
-    // the next chunk's rows into L2 while this one is processed
-    const void *bsrc = role == 0 ? p.v : p.dO;
-    stage_chunk<E, K>(p, h, tok0, len, role == 1, Qr, Kr, Gr, sv.beta);
-    stage_rows<E>(BAND, LDB, bsrc, tok0, len, H, h, Vtot, v0, BV);
-    cp_async_commit();
-    if (it + 1 < nck) {
-      const int jn = role == 0 ? j + 1 : j - 1;
-      const int64_t tn = tok_seq + (int64_t)jn * CHUNK;
-      const int ln = min(CHUNK, L - jn * CHUNK);
-      const int es = sizeof(E);
-      prefetch_rows_l2(p.k, tn, ln, H, h, K * es, es, K, 0);
-      prefetch_rows_l2(p.g, tn, ln, H, h, K * es, es, K, 0);
-      prefetch_rows_l2(bsrc, tn, ln, H, h, BV * es, es, Vtot, v0);
-      if (role == 1) prefetch_rows_l2(p.q, tn, ln, H, h, K * es, es, K, 0);
+    if (it + 2 < nck) {  // warm L2 for the chunk after next
+      int64_t t2;
+      int l2;
+      chunk_rows(role == 0 ? j + 2 : j - 2, t2, l2);
+      prefetch_rows_l2(p.k, t2, l2, H, h, K * es, es, K, 0);
+      prefetch_rows_l2(p.g, t2, l2, H, h, K * es, es, K, 0);
+      prefetch_rows_l2(bsrc, t2, l2, H, h, BV * es, es, Vtot, v0);
+      if (role == 1) prefetch_rows_l2(p.q, t2, l2, H, h, K * es, es, K, 0);
     }
-    cp_async_wait_all();
+    if (it > 0 && tid < CHUNK) sv.beta[tid] = beta_next;  // chunk j's beta
+    asm volatile("cp.async.wait_group 1;\n" ::);  // raw(j) has landed
     __syncthreads();
     PrepTiles<E> tl;
     tl.KM = KM;
@@ -147,6 +163,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
       tl.QD = QD;
     }
     chunk_prep<E, K>(p, h, len, role == 1, Qr, Kr, Gr, sv, tl);
+    if (it + 1 < nck) {
+      int64_t tn;
+      int ln;
+      chunk_rows(jn, tn, ln);
+      if (role == 1) stage_rows<E>(Qr, K, p.q, tn, ln, H, h, K, 0, K);
+      stage_rows<E>(Kr, K, p.k, tn, ln, H, h, K, 0, K);
+      stage_rows<E>(Gr, K, p.g, tn, ln, H, h, K, 0, K);
+      if (tid < CHUNK)  // beta(j+1) waits in a register until chunk j is done
+        beta_next = tid < ln ? to_f(elem_ptr<E>(p.beta, (tn + tid) * H + h)[0]) : 0.f;
+    }
+    cp_async_commit();
     intra_pairs<E, K>(QM, KM, KP, sv.F, G, 68, role == 1 ? MQK : nullptr, tile_ld<E>(64), p.scale);
     __syncthreads();
     wy_inverse<E>(G, 68, sv.beta, inv32, tbuf, INV, tile_ld<E>(64));
@@ -157,6 +184,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
       for_acc(S, [&](int r, int c, float &x) {
         ST[(srow0 + r) * LDB + scol0 + c] = from_f<E>(x);
       });
+      asm volatile("cp.async.wait_group 1;\n" ::);  // band(j) has landed
       __syncthreads();
       for (int e = tid; e < K * BV / 2; e += NTHREADS) {
         const int r = e / (BV / 2), c = 2 * (e % (BV / 2));
@@ -203,7 +231,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
       warp_gemm<NFS, false, false>(S, QD + srow0, LD, BAND + scol0, LDB, 64);
       warp_gemm<NFS, false, false>(S, KD + srow0, LD, W + scol0, LDB, 64);
     }
+    __syncthreads();  // the band, beta and the chain's tiles are free again
+    if (it + 1 < nck) {
+      int64_t tn;
+      int ln;
+      chunk_rows(jn, tn, ln);
+      stage_rows<E>(BAND, LDB, bsrc, tn, ln, H, h, Vtot, v0, BV);
+    }
+    cp_async_commit();
   }
+  cp_async_wait_all();
   float *fin = role == 0 ? p.hT : p.dh0;
   if (fin != nullptr) {
     for_acc(S, [&](int r, int c, float &x) {
