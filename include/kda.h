@@ -178,8 +178,10 @@ size_t kda_noalloc_scratch_bytes(void);
  * descriptors, Tensor Memory and tcgen05 loads, with A ([128][K] bf16,
  * row-major, device) and B ([N][K] bf16, row-major, device) staged in K-major
  * (0) or MN-major (1) core-matrix layout; D is [128][N] fp32 (device).
- * N in {32, 64, 128}, K a multiple of 16 up to 128.  swap_lbo_sbo exchanges
- * the two descriptor strides (a diagnostic of the encoding). */
+ * N in {32, 64, 128}, K a multiple of 16 up to 128.  layout: 0 = core matrices
+ * packed (128-byte stride), 2 = padded core layout (144-byte stride, the one
+ * the kernels use), 1 = packed with the two descriptor strides exchanged (a
+ * diagnostic of the encoding; gives wrong results). */
 kda_status kda_selftest_umma(const void *A, const void *B, float *D, int N, int K, int a_mn,
                              int b_mn, int swap_lbo_sbo, kda_stream_t stream);
 

@@ -18,19 +18,22 @@ __global__ void __launch_bounds__(128) kda_selftest_umma_kernel(const bf16 *A, c
   extern __shared__ __align__(1024) char smem[];
   constexpr int M = 128;
   bf16 *As = reinterpret_cast<bf16 *>(smem);
-  bf16 *Bs = reinterpret_cast<bf16 *>(smem + 32768);
-  uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + 65536);
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + 65536 + 64);
+  // a padded 128 x 128 tile takes 36 KB
+  bf16 *Bs = reinterpret_cast<bf16 *>(smem + 40960);
+  uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + 81920);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + 81920 + 64);
   const int tid = threadIdx.x, warp = tid >> 5;
   // A element (m, k): K-major -> core_off(m, k, K); MN-major -> core_off(k, m, M)
   for (int e = tid; e < M * K; e += 128) {
     const int m = e / K, k = e % K;
-    const uint32_t off = a_mn ? umma::core_off(k, m, M) : umma::core_off(m, k, K);
+    const uint32_t off = swap_lbo_sbo == 2 ? (a_mn ? umma::pcore_off(k, m, M) : umma::pcore_off(m, k, K))
+                                           : (a_mn ? umma::core_off(k, m, M) : umma::core_off(m, k, K));
     *reinterpret_cast<bf16 *>(reinterpret_cast<char *>(As) + off) = A[e];
   }
   for (int e = tid; e < N * K; e += 128) {
     const int n = e / K, k = e % K;
-    const uint32_t off = b_mn ? umma::core_off(k, n, N) : umma::core_off(n, k, K);
+    const uint32_t off = swap_lbo_sbo == 2 ? (b_mn ? umma::pcore_off(k, n, N) : umma::pcore_off(n, k, K))
+                                           : (b_mn ? umma::core_off(k, n, N) : umma::core_off(n, k, K));
     *reinterpret_cast<bf16 *>(reinterpret_cast<char *>(Bs) + off) = B[e];
   }
   if (tid == 0) umma::mbar_init(mbar, 1);
@@ -54,7 +57,13 @@ __global__ void __launch_bounds__(128) kda_selftest_umma_kernel(const bf16 *A, c
       else { a_lead = (M / 8) * 128; a_str = 128; a_step = 2 * (M / 8) * 128; }
       if (!b_mn) { b_lead = 128; b_str = (K / 8) * 128; b_step = 256; }
       else { b_lead = (N / 8) * 128; b_str = 128; b_step = 2 * (N / 8) * 128; }
-      if (swap_lbo_sbo) {
+      if (swap_lbo_sbo == 2) {  // padded core layout
+        const uint32_t cs = umma::kCoreStride;
+        if (!a_mn) { a_lead = cs; a_str = (K / 8) * cs; a_step = 2 * cs; }
+        else { a_lead = (M / 8) * cs; a_str = cs; a_step = 2 * (M / 8) * cs; }
+        if (!b_mn) { b_lead = cs; b_str = (K / 8) * cs; b_step = 2 * cs; }
+        else { b_lead = (N / 8) * cs; b_str = cs; b_step = 2 * (N / 8) * cs; }
+      } else if (swap_lbo_sbo) {
         uint32_t t = a_lead; a_lead = a_str; a_str = t;
         t = b_lead; b_lead = b_str; b_str = t;
       }
@@ -88,7 +97,7 @@ extern "C" kda_status kda_selftest_umma(const void *A, const void *B, float *D, 
   if (!A || !B || !D || (N != 32 && N != 64 && N != 128) || K < 16 || K > 128 || K % 16)
     return KDA_ERR_INVALID_ARG;
   auto k = kda::kda_selftest_umma_kernel;
-  // generous allocation: the tiles use the first 64 KB only
+  // generous allocation: the tiles use the first 80 KB only
   const int smem = 180 * 1024;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return KDA_ERR_CUDA;

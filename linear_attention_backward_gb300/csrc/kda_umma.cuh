@@ -23,6 +23,17 @@ namespace umma {
 __host__ __device__ __forceinline__ uint32_t core_off(int r, int c, int C) {
   return (uint32_t)((((r >> 3) * (C >> 3) + (c >> 3)) << 7) + ((r & 7) << 4) + ((c & 7) << 1));
 }
+// Padded variant: core matrices along a row of cores sit 144 bytes apart
+// (128 + 16), so that the 16-byte rows of the four cores a warp's 32 columns
+// touch fall on different banks.  Row groups of 8 are (C / 8) * 144 apart.
+constexpr uint32_t kCoreStride = 144;
+__host__ __device__ __forceinline__ uint32_t pcore_off(int r, int c, int C) {
+  return (uint32_t)((r >> 3) * (C >> 3) * kCoreStride + (c >> 3) * kCoreStride + ((r & 7) << 4) +
+                    ((c & 7) << 1));
+}
+__host__ __device__ constexpr uint32_t ptile_bytes(int R, int C) {
+  return (uint32_t)((R / 8) * (C / 8) * kCoreStride);
+}
 
 // ---- shared-memory matrix descriptor (no swizzle) ----------------------------
 // lbo = byte distance between core matrices adjacent along K, sbo = along M

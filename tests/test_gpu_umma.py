@@ -16,7 +16,8 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("N", [32, 64, 128])
 @pytest.mark.parametrize("K", [16, 64, 128])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
-def test_umma_tile(N, K, a_mn, b_mn):
+@pytest.mark.parametrize("layout", [0, 2])
+def test_umma_tile(N, K, a_mn, b_mn, layout):
     __graft_entry__.build()
     L = kda.lib()
     L.kda_selftest_umma.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p]
@@ -25,7 +26,8 @@ def test_umma_tile(N, K, a_mn, b_mn):
     A = torch.randn(128, K, device="cuda", generator=g).bfloat16()
     B = torch.randn(N, K, device="cuda", generator=g).bfloat16()
     D = torch.full((128, N), float("nan"), device="cuda")
-    st = L.kda_selftest_umma(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K, a_mn, b_mn, 0, None)
+    st = L.kda_selftest_umma(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K, a_mn, b_mn, layout,
+                             None)
     torch.cuda.synchronize()
     assert st == 0 and kda.get_device_status() == 0
     ref = A.float() @ B.float().T
