@@ -227,9 +227,11 @@ kda_status kda_get_device_status(kda_stream_t stream) {
     return KDA_ERR_CUDA;
   const int a = kda::scan_status_take();
   const int b = kda::grads_status_take();
-  if (a < 0 || b < 0) return KDA_ERR_CUDA;
+  const int t = kda::grads_tc_status_take();
+  if (a < 0 || b < 0 || t < 0) return KDA_ERR_CUDA;
   if (a != 0) return (kda_status)a;
-  return (kda_status)b;
+  if (b != 0) return (kda_status)b;
+  return (kda_status)t;
 }
 
 }  // extern "C"

@@ -20,6 +20,8 @@
 // normalised-key frame: dq^ = dqd e^gc, dkd' = dkd e^gc, dki' = dki e^-gc,
 // dkr' = dkr e^(gT - gc); dk^ = dkd' + dki' + dkr'.  Everything after the
 // bf16 tensor-core products is fp32 (the guide's fp32-only gate epilogue).
+#include <stdlib.h>
+
 #include "kda_chunk.cuh"
 
 namespace kda {
@@ -524,18 +526,30 @@ __global__ void kda_dalog_reduce_kernel(const float *part, int64_t nslots, int H
   }
 }
 
+// bf16 K = V = 128 runs on the tcgen05 kernel (kda_grads_tc.cu) unless the
+// environment variable KDA_GRADS_MMA_SYNC is set (A/B comparisons).
+static bool use_tc_kernel() {
+  static const bool tc = getenv("KDA_GRADS_MMA_SYNC") == nullptr;
+  return tc;
+}
+
 template <typename E, int D>
 static cudaError_t launch_grads(const KdaParams &p, const void *states, cudaStream_t st,
                                 void *after) {
   using SM = GradSmem<E, D>;
-  auto kfn = kda_grads_kernel<E, D>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::total);
-  if (e != cudaSuccess) return e;
-  if (p.nslots > 0) {
-    kfn<<<dim3((unsigned)p.nslots, p.H), NTHREADS, SM::total, st>>>(p, states);
-    e = cudaGetLastError();
+  cudaError_t e;
+  if (sizeof(E) == 2 && D == 128 && use_tc_kernel()) {
+    e = grads_tc_launch(p, states, st);
     if (e != cudaSuccess) return e;
+  } else {
+    auto kfn = kda_grads_kernel<E, D>;
+    e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::total);
+    if (e != cudaSuccess) return e;
+    if (p.nslots > 0) {
+      kfn<<<dim3((unsigned)p.nslots, p.H), NTHREADS, SM::total, st>>>(p, states);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
   }
   if (after != nullptr) cudaEventRecord(reinterpret_cast<cudaEvent_t>(after), st);
   kda_dalog_reduce_kernel<<<p.H, NTHREADS, 0, st>>>(p.dA_part, p.nslots, p.H, p.dA_log);

@@ -1,0 +1,935 @@
+// kda_grads_tc.cu -- per-chunk gradients of the KDA backward on the
+// fifth-generation tensor cores (tcgen05, Tensor Memory), bf16, K = V = 128.
+//
+// The work per (chunk, head) is the same as kda_grads.cu (the B1 / B2 / B0 /
+// B3 / K1 split of "bwd-kernelB-beginner-guide-full", Part 1, in one CTA), laid
+// out for tcgen05: every large contraction is taken TRANSPOSED, with the
+// channel (K or V = 128) dimension as the MMA's M, so that M = 128 and the
+// result lands in Tensor Memory with lane = channel.  Thread t of the CTA
+// owns channel c = t % 128 and chunk rows i in [32 g, 32 g + 32), g = t / 128;
+// it reads exactly its lane and its 32 columns of every accumulator, keeps
+// E = e^(gc - m) for its (i, c) in registers for the whole kernel, and does
+// the gate epilogue (the 64-row reverse cumulative sum) sequentially.
+//
+// Products (D = A B^T, A: 128 x K, B: N x K; tiles in the padded core layout,
+// "K" / "MN" = how the stored tile is read):
+//   P1  kdS^T[d][i]   = S[c][d] (MN)            x kd[i][c] (K)          N = 64
+//   P2  U^T[d][i]     = Xr^T[d][j] (K)          x INVb[i][j] (K)        N = 64
+//   P3  dU^T[d][i]    = dO[i'][d] (MN) x Mqk[i'][i] (MN)
+//                     + dS[c][d] (MN)  x kr[i][c] (K)                   N = 64
+//       dkr^T[c][i]   = dS[c][d] (K)            x U[i][d] (K)           N = 64
+//   P5  dvcorr^T[d][i]= dU^T[d][i'] (K)         x INV[i'][i] (MN)       N = 64
+//   P6  [dvcorr; dO] U^T = [-dAkk | dMqk / s] (rows: dvcorr, then dO)   N = 64
+//   P8  S [dvcorr; dO]^T = [dvcorr S^T | dO S^T]^T                     N = 128
+//   P9  intra-chunk terms, per 16-row block pair, hi + lo operands      N = 64
+// The pair matrices Akk / Mqk and the WY inverse are formed as in the other
+// kernels (mma.sync on the same padded core tiles, fp32 substitution).
+#include "kda_chunk.cuh"
+#include "kda_umma.cuh"
+
+namespace kda {
+namespace gtc {
+
+using umma::pcore_off;
+constexpr int D = 128;
+constexpr uint32_t CS = umma::kCoreStride;
+constexpr uint32_t T64x128 = umma::ptile_bytes(64, 128);    // 18432
+constexpr uint32_t T128x128 = umma::ptile_bytes(128, 128);  // 36864
+constexpr uint32_t T64x64 = umma::ptile_bytes(64, 64);      // 9216
+constexpr uint32_t T128x64 = umma::ptile_bytes(128, 64);    // 18432
+
+__device__ __forceinline__ bf16 *pel(void *t, int r, int c, int C) {
+  return reinterpret_cast<bf16 *>(reinterpret_cast<char *>(t) + pcore_off(r, c, C));
+}
+__device__ __forceinline__ float pget(const void *t, int r, int c, int C) {
+  return __bfloat162float(
+      *reinterpret_cast<const bf16 *>(reinterpret_cast<const char *>(t) + pcore_off(r, c, C)));
+}
+// 8 consecutive columns c0 .. c0 + 7 (c0 % 8 == 0) of row r, one 16-byte store
+__device__ __forceinline__ void pstore8(void *t, int r, int c0, int C, const float *v) {
+  __nv_bfloat162 h[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+  *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(t) + pcore_off(r, c0, C)) =
+      *reinterpret_cast<uint4 *>(h);
+}
+__device__ __forceinline__ void pload8(const void *t, int r, int c0, int C, float *v) {
+  const uint4 u =
+      *reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(t) + pcore_off(r, c0, C));
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __bfloat1622float2(h[q]);
+    v[2 * q] = f.x;
+    v[2 * q + 1] = f.y;
+  }
+}
+
+// ---- tcgen05 operands -------------------------------------------------------
+struct Op {
+  uint32_t addr, lbo, sbo, step;
+};
+// stored tile [R][C] read with K along its columns, from column k0
+__device__ __forceinline__ Op opk(const void *t, int C, int k0 = 0) {
+  return Op{smem_u32(t) + (uint32_t)(k0 / 8) * CS, CS, (uint32_t)(C / 8) * CS, 2 * CS};
+}
+// stored tile [R][C] read with K along its rows, from row r0
+__device__ __forceinline__ Op opmn(const void *t, int C, int r0 = 0) {
+  return Op{smem_u32(t) + (uint32_t)(r0 / 8) * (C / 8) * CS, (uint32_t)(C / 8) * CS, CS,
+            2 * (uint32_t)(C / 8) * CS};
+}
+__device__ __forceinline__ void gemm(uint32_t d, Op a, bool amn, Op b, bool bmn, int N, int ksteps,
+                                     bool accumulate) {
+  const uint32_t id = umma::idesc_bf16(128, N, amn, bmn);
+  for (int s = 0; s < ksteps; ++s)
+    umma::mma_bf16(d, umma::smem_desc(a.addr + s * a.step, a.lbo, a.sbo),
+                   umma::smem_desc(b.addr + s * b.step, b.lbo, b.sbo), id, accumulate || s > 0);
+}
+
+// ---- mma.sync on padded core tiles (pair matrices) ---------------------------
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t a) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t a) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+// acc (16 x 8 NF) += A (16 x kdim) B (kdim x 8 NF) from transposed tiles:
+// A(m, k) = tile A[ak0 + k][am0 + m], B(k, n) = tile B[bk0 + k][bn0 + n];
+// kscale per k (the tiles' row index).
+template <int NF>
+__device__ __forceinline__ void wg_core_t(float (&acc)[NF][4], const void *A, int AC, int ak0,
+                                          int am0, const void *B, int BC, int bk0, int bn0,
+                                          int kdim, const float *kscale) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+#pragma unroll
+  for (int k0 = 0; k0 < kdim; k0 += 16) {
+    uint32_t af[4];
+    ldsm4t(af, a0 + pcore_off(ak0 + k0 + (lane & 7) + (lane >> 4) * 8,
+                              am0 + ((lane >> 3) & 1) * 8, AC));
+    if (kscale != nullptr) {
+      const int c = k0 + 2 * (lane & 3);
+      const float s0 = kscale[c], s1 = kscale[c + 1], s8 = kscale[c + 8], s9 = kscale[c + 9];
+      af[0] = scale_pair(af[0], s0, s1);
+      af[1] = scale_pair(af[1], s0, s1);
+      af[2] = scale_pair(af[2], s8, s9);
+      af[3] = scale_pair(af[3], s8, s9);
+    }
+#pragma unroll
+    for (int f = 0; f < NF; f += 2) {
+      uint32_t bfr[4];
+      ldsm4t(bfr, b0 + pcore_off(bk0 + k0 + (lane & 7) + ((lane >> 3) & 1) * 8,
+                                 bn0 + f * 8 + (lane >> 4) * 8, BC));
+      mma_16816(acc[f], af, bfr[0], bfr[1]);
+      mma_16816(acc[f + 1], af, bfr[2], bfr[3]);
+    }
+  }
+}
+// acc (16 x 8 NF) += A (16 x kdim) B (kdim x 8 NF); A(m, k) = tile A[ar0 + m][ac0 + k],
+// B(k, n) = tile B[br0 + n][bc0 + k]; both K-contiguous tiles; kscale per k.
+template <int NF>
+__device__ __forceinline__ void wg_core(float (&acc)[NF][4], const void *A, int AC, int ar0,
+                                        int ac0, const void *B, int BC, int br0, int bc0,
+                                        int kdim, const float *kscale) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+#pragma unroll
+  for (int k0 = 0; k0 < kdim; k0 += 16) {
+    uint32_t af[4];
+    ldsm4(af, a0 + pcore_off(ar0 + (lane & 15), ac0 + k0 + (lane >> 4) * 8, AC));
+    if (kscale != nullptr) {
+      const int c = k0 + 2 * (lane & 3);
+      const float s0 = kscale[c], s1 = kscale[c + 1], s8 = kscale[c + 8], s9 = kscale[c + 9];
+      af[0] = scale_pair(af[0], s0, s1);
+      af[1] = scale_pair(af[1], s0, s1);
+      af[2] = scale_pair(af[2], s8, s9);
+      af[3] = scale_pair(af[3], s8, s9);
+    }
+#pragma unroll
+    for (int f = 0; f < NF; f += 2) {
+      uint32_t bfr[4];
+      ldsm4(bfr, b0 + pcore_off(br0 + f * 8 + (lane & 7) + (lane >> 4) * 8,
+                                bc0 + k0 + ((lane >> 3) & 1) * 8, BC));
+      mma_16816(acc[f], af, bfr[0], bfr[1]);
+      mma_16816(acc[f + 1], af, bfr[2], bfr[3]);
+    }
+  }
+}
+
+// ---- shared memory plan (bytes) ----------------------------------------------
+struct Smem {
+  static constexpr size_t n_view = PrepView<bf16, D>::floats;
+  // extra floats: tbuf 768, dgT 2 x 128, red 8 x 64, dbeta 2 x 64, dA 8
+  static constexpr size_t n_extra = 768 + 256 + 512 + 128 + 8;
+  static constexpr size_t sz_small = (((n_view + n_extra) * 4 + 64 + 1023) / 1024) * 1024;
+  static constexpr size_t o_small = 0;
+  // R_A: raw q, k, g (prep, later again) | Gf fp32, Gbf, Mqk, INV, INVb
+  static constexpr size_t o_A = o_small + sz_small;
+  static constexpr size_t o_Gf = o_A;
+  static constexpr size_t o_Gbf = o_Gf + 64 * 64 * 4;
+  static constexpr size_t o_Mqk = o_Gbf + T64x64;
+  static constexpr size_t o_INV = o_Mqk + T64x64;
+  static constexpr size_t o_INVb = o_INV + T64x64;
+  static constexpr size_t sz_A = 64 * 64 * 4 + 4 * T64x64;  // >= 3 raw tiles
+  // R_B: QMh, KMh, KPh (prep)  ->  S, U  ->  hi tiles (intra)
+  static constexpr size_t o_B = o_A + sz_A;
+  static constexpr size_t o_S = o_B;
+  static constexpr size_t o_U = o_B + T128x128;
+  static constexpr size_t sz_B = 3 * T64x128;
+  // R_C: kd, kr (prep)  ->  Xr^T, dU^T  ->  lo tiles QMl, KMl (intra)
+  static constexpr size_t o_C = o_B + sz_B;
+  static constexpr size_t sz_C = 2 * T64x128;
+  // R_D: dS (128 x 128), then dO (64 x 128)  ->  dMqk, dA | dvcorr ; dvcorr | dO is the
+  // stacked 128-row operand of P6 / P8; KPl (intra) reuses the dvcorr slot
+  static constexpr size_t o_D = o_C + sz_C;
+  static constexpr size_t o_dS = o_D;
+  static constexpr size_t o_dMqk = o_D;
+  static constexpr size_t o_dA = o_D + T64x64;
+  static constexpr size_t o_dvc = o_D + T64x128;
+  static constexpr size_t o_dO = o_D + T128x128;
+  static constexpr size_t sz_D = T128x128 + T64x128;
+  static constexpr size_t total = o_D + sz_D;
+  static_assert(sz_A >= 3 * 64 * D * 2, "raw tiles must fit R_A");
+  static_assert(T128x128 + T128x64 <= sz_B, "S + U must fit R_B");
+  static_assert(2 * T64x128 == T128x128, "dvcorr | dO stacking");
+  static_assert(total <= 232448, "shared memory budget");
+};
+
+// prep in the (channel, 32-row segment) mapping; E kept in registers
+__device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, const bf16 *Kr,
+                        const bf16 *Gr, const PrepView<bf16, D> &sv, float (&E)[32], void *KDt,
+                        void *KRt, void *QMt, void *KMt, void *KPt) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = tid & 127, g = tid >> 7;
+  const float A = __expf(p.A_log[h]);
+  // L2 norms, one warp per row
+  for (int i = warp; i < CHUNK; i += NWARPS) {
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int cc = 2 * lane; cc < D; cc += 64) {
+      const float2 kv = load2(Kr + i * D + cc);
+      const float2 qv = load2(Qr + i * D + cc);
+      sk = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, sk));
+      sq = fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, sq));
+    }
+    sk = warp_sum(sk);
+    sq = warp_sum(sq);
+    if (lane == 0) {
+      sv.rk[i] = rsqrtf(sk + p.eps);
+      sv.rq[i] = rsqrtf(sq + p.eps);
+    }
+  }
+  // gate: per 16-row block sums local to the block (see kda_chunk.cuh)
+  float d[32];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    float run = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int i = 32 * g + 16 * b + r;
+      const float gv = __bfloat162float(Gr[i * D + c]);
+      run += i < len ? -A * softplus_f(gv) : 0.f;
+      d[16 * b + r] = run;
+    }
+    const int I = 2 * g + b;
+    sv.part[I * D + c] = d[16 * b + 7];                 // rows 16I .. 16I+7
+    sv.m[I * D + c] = d[16 * b + 15] - d[16 * b + 7];   // rows 16I+8 .. 16I+15
+    const float ref = d[16 * b + 7];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) d[16 * b + r] -= ref;  // gc - m_I
+  }
+  __syncthreads();
+  if (tid < D) {
+    float a[4], bb[4];
+#pragma unroll
+    for (int L = 0; L < 4; ++L) {
+      a[L] = sv.part[L * D + tid];
+      bb[L] = sv.m[L * D + tid];
+    }
+    float before = 0.f, tot = 0.f;
+#pragma unroll
+    for (int L = 0; L < 4; ++L) tot += a[L] + bb[L];
+#pragma unroll
+    for (int L = 0; L < 4; ++L) {
+      float after = bb[L];
+#pragma unroll
+      for (int L2 = L + 1; L2 < 4; ++L2) after += a[L2] + bb[L2];
+      sv.em[L * D + tid] = __expf(before + a[L]);
+      sv.egm[L * D + tid] = __expf(after);
+      before += a[L] + bb[L];
+    }
+#pragma unroll
+    for (int I2 = 1; I2 < 4; ++I2)
+#pragma unroll
+      for (int J = 0; J < I2; ++J) {
+        float dd = bb[J] + a[I2];
+#pragma unroll
+        for (int L = J + 1; L < I2; ++L) dd += a[L] + bb[L];
+        sv.F[pair_index(I2, J) * D + tid] = __expf(dd);
+      }
+    sv.gT[tid] = tot;
+  }
+  __syncthreads();
+  // tiles are stored transposed, [c][i] (128 x 64), one 16-byte store per
+  // 8 rows: kd / kr are read MN-major (B, K = c), qm / km / kp K-major-by-
+  // transposition by the pair-matrix mma.sync (ldmatrix.trans)
+  const float em0 = sv.em[(2 * g) * D + c], em1 = sv.em[(2 * g + 1) * D + c];
+  const float eg0 = sv.egm[(2 * g) * D + c], eg1 = sv.egm[(2 * g + 1) * D + c];
+#pragma unroll
+  for (int q8 = 0; q8 < 4; ++q8) {
+    float vkd[8], vkr[8], vqm[8], vkm[8], vkp[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int r = 8 * q8 + t, i = 32 * g + r;
+      const float em = (r < 16) ? em0 : em1, eg = (r < 16) ? eg0 : eg1;
+      const float e = __expf(d[r]), ei = __expf(-d[r]);
+      E[r] = e;
+      const float kh = __bfloat162float(Kr[i * D + c]) * sv.rk[i];
+      const float qh = __bfloat162float(Qr[i * D + c]) * sv.rq[i];
+      vkd[t] = (kh * e) * em;
+      vkr[t] = (kh * ei) * eg;
+      vqm[t] = qh * e;
+      vkm[t] = kh * e;
+      vkp[t] = kh * ei;
+    }
+    const int i0 = 32 * g + 8 * q8;
+    pstore8(KDt, c, i0, 64, vkd);
+    pstore8(KRt, c, i0, 64, vkr);
+    pstore8(QMt, c, i0, 64, vqm);
+    pstore8(KMt, c, i0, 64, vkm);
+    pstore8(KPt, c, i0, 64, vkp);
+  }
+  __syncthreads();
+}
+
+// Gf [64][64] fp32 holds G (strictly lower) on entry and (I + diag(beta) G)^-1
+// on exit (block forward substitution in place; see wy_inverse).
+__device__ void inverse_inplace(float *Gf, const float *beta, float *tbuf) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int LG = 64;
+  if (warp < 4) {
+    const int o = 16 * warp, col = lane & 15;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float br = beta[o + r];
+      const float *grow = Gf + (o + r) * LG + o;
+      float s0 = (r == col) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < r; ++j) {
+        if (j & 1)
+          s1 = fmaf(-br * grow[j], x[j], s1);
+        else
+          s0 = fmaf(-br * grow[j], x[j], s0);
+      }
+      x[r] = s0 + s1;
+    }
+    __syncwarp();
+    if (lane < 16) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) Gf[(o + r) * LG + o + col] = x[r];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int I = 1; I < 4; ++I) {
+    const int J = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+    const int row = 16 * I + r;
+    if (J < I) {
+      const float *grow = Gf + row * LG;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int Lb = J; Lb < I; ++Lb) {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const float gv = grow[16 * Lb + x];
+          const float4 xv = *reinterpret_cast<const float4 *>(Gf + (16 * Lb + x) * LG + 16 * J + c4);
+          t.x = fmaf(gv, xv.x, t.x);
+          t.y = fmaf(gv, xv.y, t.y);
+          t.z = fmaf(gv, xv.z, t.z);
+          t.w = fmaf(gv, xv.w, t.w);
+        }
+      }
+      const float br = beta[row];
+      *reinterpret_cast<float4 *>(tbuf + (J << 8) + (r << 4) + c4) =
+          make_float4(br * t.x, br * t.y, br * t.z, br * t.w);
+    }
+    __syncthreads();
+    if (J < I) {
+      const float *xr = Gf + row * LG + 16 * I;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const float xv = xr[x];
+        const float4 tv = *reinterpret_cast<const float4 *>(tbuf + (J << 8) + (x << 4) + c4);
+        t.x = fmaf(xv, tv.x, t.x);
+        t.y = fmaf(xv, tv.y, t.y);
+        t.z = fmaf(xv, tv.z, t.z);
+        t.w = fmaf(xv, tv.w, t.w);
+      }
+      *reinterpret_cast<float4 *>(Gf + row * LG + 16 * J + c4) = make_float4(-t.x, -t.y, -t.z, -t.w);
+    }
+    __syncthreads();
+  }
+}
+
+// Row sums over the warp's 32 lanes for 32 rows at once: lane l returns
+// sum over lanes of v[l] (31 shuffles instead of 32 x 5); v is consumed.
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < s; ++k) {
+      const float send = up ? v[k] : v[k + s];
+      const float keep = up ? v[k + s] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
+// TMEM address of this thread's lane (warp quarter) at column col
+__device__ __forceinline__ uint32_t tm(uint32_t tbase, int col) {
+  return tbase + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16) + (uint32_t)col;
+}
+// this thread's 32 columns [col0 + 32 g, +32) of its lane
+__device__ __forceinline__ void tld32(uint32_t tbase, int col0, float (&v)[32]) {
+  const int g = threadIdx.x >> 7;
+  float a[16], b[16];
+  umma::tmem_ld16(tm(tbase, col0 + 32 * g), a);
+  umma::tmem_ld16(tm(tbase, col0 + 32 * g + 16), b);
+  umma::tmem_ld_wait();
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    v[q] = a[q];
+    v[16 + q] = b[q];
+  }
+}
+
+}  // namespace gtc
+
+__global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, const void *states) {
+  using namespace gtc;
+  using SM = Smem;
+  extern __shared__ __align__(1024) char smem[];
+  const int64_t slot = blockIdx.x;
+  const int h = blockIdx.y;
+  const int H = p.H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = tid & 127, g = tid >> 7, wq = warp & 3;
+  int s_, j_, len;
+  int64_t tok0;
+  if (!slot_owner(p, slot, s_, j_, tok0, len)) {
+    if (tid == 0) p.dA_part[slot * H + h] = 0.f;
+    return;
+  }
+  // ---- views ----
+  float *smf = reinterpret_cast<float *>(smem + SM::o_small);
+  PrepView<bf16, D> sv = make_view<bf16, D>(smf);
+  float *tbuf = smf + SM::n_view;
+  float *dgT = tbuf + 768;         // [2][128] (per row half)
+  float *red = dgT + 256;          // [8 warps][64]
+  float *dbs = red + 512;          // [2][64]
+  float *dAred = dbs + 128;        // [8]
+  uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + SM::o_small + (SM::n_view + SM::n_extra) * 4);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 1);
+  bf16 *Qr = reinterpret_cast<bf16 *>(smem + SM::o_A);
+  bf16 *Kr = Qr + 64 * D;
+  bf16 *Gr = Kr + 64 * D;
+  float *Gf = reinterpret_cast<float *>(smem + SM::o_Gf);
+  char *Gbf = smem + SM::o_Gbf, *Mqk = smem + SM::o_Mqk, *INV = smem + SM::o_INV,
+       *INVb = smem + SM::o_INVb;
+  char *QMh = smem + SM::o_B, *KMh = QMh + T64x128, *KPh = KMh + T64x128;
+  char *St = smem + SM::o_S, *Ut = smem + SM::o_U;
+  char *KDt = smem + SM::o_C, *KRt = KDt + T64x128;
+  char *XrT = KDt, *dUT = KRt, *QMl = KDt, *KMl = KRt;
+  char *dSt = smem + SM::o_dS, *dMqk = smem + SM::o_dMqk, *dAt = smem + SM::o_dA,
+       *dvc = smem + SM::o_dvc, *dOt = smem + SM::o_dO, *KPl = dvc;
+  const float scale = p.scale;
+  const size_t DD = (size_t)D * D;
+  const bf16 *Sg = reinterpret_cast<const bf16 *>(states) + ((size_t)slot * H + h) * DD;
+  const bf16 *dSg = reinterpret_cast<const bf16 *>(p.dstates) + ((size_t)slot * H + h) * DD;
+
+  // ---- Tensor Memory (all 512 columns) and the MMA-completion barrier ----
+  if (warp == 0) umma::tmem_alloc(tslot, 512);
+  if (tid == 0) umma::mbar_init(mbar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  // ---- stage: raw q, k, g (group 1); dS, dO into padded core tiles (group 2) ----
+  stage_chunk<bf16, D>(p, h, tok0, len, true, Qr, Kr, Gr, sv.beta);
+  cp_async_commit();
+  for (int e = tid; e < D * (D / 8); e += NTHREADS) {  // dS rows c, 8-column chunks
+    const int r = e >> 4, c8 = (e & 15) * 8;
+    cp_async16(smem + SM::o_dS + pcore_off(r, c8, D), dSg + (size_t)r * D + c8, true);
+  }
+  for (int e = tid; e < 64 * (D / 8); e += NTHREADS) {
+    const int i = e >> 4, c8 = (e & 15) * 8;
+    const bool ok = i < len;
+    cp_async16(dOt + pcore_off(i, c8, D),
+               reinterpret_cast<const bf16 *>(p.dO) + ((tok0 + (ok ? i : 0)) * H + h) * D + c8, ok);
+  }
+  cp_async_commit();
+  if (tid < D) {
+    dgT[tid] = 0.f;
+    dgT[D + tid] = 0.f;
+  }
+  umma::tc_fence_before();
+  asm volatile("cp.async.wait_group 1;\n" ::);
+  __syncthreads();
+  umma::tc_fence_after();
+  const uint32_t tbase = *tslot;
+  uint32_t phase = 0;
+  auto mma_wait = [&]() {
+    const bool ok = umma::mbar_wait(mbar, phase & 1, 1u << 20);
+    phase++;
+    umma::tc_fence_after();
+    return ok;
+  };
+
+  // ---- prep ----
+  float E[32];
+  prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, KRt, QMh, KMh, KPh);
+  // ---- pair matrices (mma.sync): G (fp32, strictly lower) and scale * Mqk ----
+  {
+    const int I = warp & 3;
+    const bool is_q = warp >= 4;
+    const char *X = is_q ? QMh : KMh;
+    for (int J = 0; J < 4; ++J) {
+      float acc[2][4];
+      zero_acc(acc);
+      if (J <= I)
+        wg_core_t<2>(acc, X, 64, 0, 16 * I, KPh, 64, 0, 16 * J, D,
+                   J < I ? sv.F + pair_index(I, J) * D : nullptr);
+      for_acc(acc, [&](int r, int cc, float &v) {
+        const int i = 16 * I + r, jj = 16 * J + cc;
+        if (is_q)
+          *pel(Mqk, i, jj, 64) = __float2bfloat16_rn(jj <= i ? scale * v : 0.f);
+        else
+          Gf[i * 64 + jj] = jj < i ? v : 0.f;
+      });
+    }
+  }
+  __syncthreads();
+  // S -> R_B (QMh/KMh/KPh are dead) while the inverse runs
+  for (int e = tid; e < D * (D / 8); e += NTHREADS) {
+    const int r = e >> 4, c8 = (e & 15) * 8;
+    cp_async16(St + pcore_off(r, c8, D), Sg + (size_t)r * D + c8, true);
+  }
+  cp_async_commit();
+  for (int e = tid; e < 64 * 64; e += NTHREADS) {
+    const int i = e >> 6, jj = e & 63;
+    *pel(Gbf, i, jj, 64) = __float2bfloat16_rn(Gf[e]);
+  }
+  __syncthreads();
+  inverse_inplace(Gf, sv.beta, tbuf);
+  for (int e = tid; e < 64 * 64; e += NTHREADS) {
+    const int i = e >> 6, jj = e & 63;
+    const float x = Gf[e];
+    *pel(INV, i, jj, 64) = __float2bfloat16_rn(x);
+    *pel(INVb, i, jj, 64) = __float2bfloat16_rn(x * sv.beta[jj]);
+  }
+  cp_async_wait_all();
+  umma::fence_async_smem();
+  __syncthreads();
+
+  // ---- P1: kdS^T = S^T kd^T ; the epilogue forms Xr^T = v^T - kdS^T ----
+  if (tid == 0) {
+    umma::tc_fence_after();
+    gemm(tbase + 0, opmn(St, D), true, opmn(KDt, 64), true, 64, D / 16, false);
+    umma::mma_commit(mbar);
+  }
+  float vv[32];
+  {
+    const bf16 *vg = reinterpret_cast<const bf16 *>(p.v);
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int i = 32 * g + r;
+      vv[r] = i < len ? __bfloat162float(vg[((tok0 + i) * H + h) * D + c]) : 0.f;
+    }
+  }
+  const bool ok1 = mma_wait();
+  float acc[32];
+  tld32(tbase, 0, acc);
+#pragma unroll
+  for (int r = 0; r < 32; ++r) acc[r] = vv[r] - acc[r];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) pstore8(XrT, c, 32 * g + 8 * q, 64, acc + 8 * q);  // Xr^T[d][i]
+  umma::fence_async_smem();
+  umma::tc_fence_before();
+  __syncthreads();
+
+  // ---- P2: U^T = Xr^T INVb^T ; U[i][d] for the later products ----
+  if (tid == 0) {
+    umma::tc_fence_after();
+    gemm(tbase + 64, opk(XrT, 64), false, opk(INVb, 64), false, 64, 4, false);
+    umma::mma_commit(mbar);
+  }
+  mma_wait();
+  tld32(tbase, 64, acc);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) pstore8(Ut, c, 32 * g + 8 * q, 64, acc + 8 * q);  // U^T[d][i]
+  umma::fence_async_smem();
+  umma::tc_fence_before();
+  __syncthreads();
+
+  // ---- P3: dU^T = dO^T Mqk + dS^T kr^T ; dkr^T = dS U^T ; B0: p ----
+  if (tid == 0) {
+    umma::tc_fence_after();
+    gemm(tbase + 128, opmn(dOt, D), true, opmn(Mqk, 64), true, 64, 4, false);
+    gemm(tbase + 128, opmn(dSt, D), true, opmn(KRt, 64), true, 64, D / 16, true);
+    gemm(tbase + 448, opk(dSt, D), false, opmn(Ut, 64), true, 64, D / 16, false);
+    umma::mma_commit(mbar);
+  }
+  {
+    // p_c = e^gT_c sum_d dS[c][d] S[c][d]; thread (c, g) takes d in [64 g, 64 g + 64)
+    float pp = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float a8[8], b8[8];
+      pload8(dSt, c, 64 * g + 8 * q, D, a8);
+      pload8(St, c, 64 * g + 8 * q, D, b8);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) pp = fmaf(a8[t], b8[t], pp);
+    }
+    dgT[g * D + c] = __expf(sv.gT[c]) * pp;
+  }
+  mma_wait();
+  tld32(tbase, 128, acc);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) pstore8(dUT, c, 32 * g + 8 * q, 64, acc + 8 * q);  // dU^T[d][i]
+  umma::fence_async_smem();
+  umma::tc_fence_before();
+  __syncthreads();
+
+  // ---- P5: dvcorr^T = dU^T INV ; dv, dbeta1, dvcorr[i][d] ----
+  if (tid == 0) {
+    umma::tc_fence_after();
+    gemm(tbase + 0, opk(dUT, 64), false, opmn(INV, 64), true, 64, 4, false);
+    umma::mma_commit(mbar);
+  }
+  mma_wait();
+  tld32(tbase, 0, acc);
+  {
+    bf16 *dvg = reinterpret_cast<bf16 *>(p.dv);
+    float xr[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) pload8(XrT, c, 32 * g + 8 * q, 64, xr + 8 * q);
+    float pr[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int i = 32 * g + r;
+      *pel(dvc, i, c, D) = __float2bfloat16_rn(acc[r]);
+      if (i < len) dvg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn(sv.beta[i] * acc[r]);
+      pr[r] = acc[r] * xr[r];
+    }
+    // sums over this warp's 32 channels; lane l gets row 32 g + l
+    red[warp * 64 + 32 * g + lane] = warp_transpose_sum(pr);
+  }
+  umma::fence_async_smem();
+  umma::tc_fence_before();
+  __syncthreads();
+  if (tid < 64) {  // dbeta1_i: warps 0..3 (g = 0) hold rows 0..31, warps 4..7 rows 32..63
+    const int i = tid, w0 = (i >> 5) * 4;
+    dbs[i] = red[(w0 + 0) * 64 + i] + red[(w0 + 1) * 64 + i] + red[(w0 + 2) * 64 + i] +
+             red[(w0 + 3) * 64 + i];
+  }
+  __syncthreads();  // red is rewritten by the P6 epilogue
+
+  // ---- P6: [dvcorr; dO] U^T  and  P8: S [dvcorr; dO]^T ----
+  if (tid == 0) {
+    umma::tc_fence_after();
+    gemm(tbase + 64, opk(dvc, D), false, opmn(Ut, 64), true, 64, D / 16, false);
+    gemm(tbase + 256, opk(St, D), false, opk(dvc, D), false, 128, D / 16, false);
+    umma::mma_commit(mbar);
+  }
+  mma_wait();
+  {
+    // lanes 0..63: -dAkk rows (dvcorr U^T), lanes 64..127: dMqk / scale rows
+    float v32[32];
+    tld32(tbase, 64, v32);  // columns j in [32 g, 32 g + 32)
+    if (c < 64) {
+      const int i = c;
+      float db2 = 0.f;
+      float o8[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int jj = 32 * g + 8 * q + t;
+          const float dak = jj < i ? -v32[8 * q + t] : 0.f;
+          db2 = fmaf(dak, pget(Gbf, i, jj, 64), db2);
+          o8[t] = sv.beta[i] * dak;
+        }
+        pstore8(dAt, i, 32 * g + 8 * q, 64, o8);
+      }
+      red[(g * 2) * 64 + i] = db2;
+    } else {
+      const int i = c - 64;
+      float o8[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int jj = 32 * g + 8 * q + t;
+          o8[t] = jj <= i ? scale * v32[8 * q + t] : 0.f;
+        }
+        pstore8(dMqk, i, 32 * g + 8 * q, 64, o8);
+      }
+    }
+  }
+  umma::fence_async_smem();
+  umma::tc_fence_before();
+  __syncthreads();
+  if (tid < 64 && tid < len) {
+    const float db = dbs[tid] + red[0 * 64 + tid] + red[2 * 64 + tid];
+    reinterpret_cast<bf16 *>(p.dbeta)[(tok0 + tid) * H + h] = __float2bfloat16_rn(db);
+  }
+  // raw q, k, g again (L2), for the hi / lo operands and the epilogues
+  stage_chunk<bf16, D>(p, h, tok0, len, true, Qr, Kr, Gr, dbs);
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
+  // ---- intra-chunk operands, hi + lo (see kda_grads.cu) ----
+  float qh[32], kh[32];
+#pragma unroll
+  for (int q8 = 0; q8 < 4; ++q8) {
+    float hv[3][8], lv[3][8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int r = 8 * q8 + t, i = 32 * g + r;
+      qh[r] = __bfloat162float(Qr[i * D + c]) * sv.rq[i];
+      kh[r] = __bfloat162float(Kr[i * D + c]) * sv.rk[i];
+      const float x[3] = {qh[r] * E[r], kh[r] * E[r], __fdividef(kh[r], E[r])};
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        hv[u][t] = __bfloat162float(__float2bfloat16_rn(x[u]));
+        lv[u][t] = x[u] - hv[u][t];
+      }
+    }
+    const int i0 = 32 * g + 8 * q8;
+    char *hi[3] = {QMh, KMh, KPh};
+    char *lo[3] = {QMl, KMl, KPl};
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      pstore8(hi[u], c, i0, 64, hv[u]);
+      pstore8(lo[u], c, i0, 64, lv[u]);
+    }
+  }
+  umma::fence_async_smem();
+  umma::tc_fence_before();
+  __syncthreads();
+
+  // per-thread block factors: Fq[b][J] = F_{I,J} (I = 2 g + b, J <= I) for the
+  // query-side sums, Fk[b][I] = F_{I,J} (J = 2 g + b, I >= J) for the key side
+  float Fq[2][4], Fk[2][4];
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+#pragma unroll
+    for (int X = 0; X < 4; ++X) {
+      const int Ib = 2 * g + b;
+      Fq[b][X] = X < Ib ? sv.F[pair_index(Ib, X) * D + c] : (X == Ib ? 1.f : 0.f);
+      Fk[b][X] = X > Ib ? sv.F[pair_index(X, Ib) * D + c] : (X == Ib ? 1.f : 0.f);
+    }
+  // ---- P9a: dq^ intra, one accumulator per key block J ----
+  if (tid == 0) {
+    umma::tc_fence_after();
+    for (int J = 0; J < 4; ++J) {
+      gemm(tbase + 64 * J, opk(KPh, 64, 16 * J), false, opk(dMqk, 64, 16 * J), false, 64, 1, false);
+      gemm(tbase + 64 * J, opk(KPl, 64, 16 * J), false, opk(dMqk, 64, 16 * J), false, 64, 1, true);
+    }
+    umma::mma_commit(mbar);
+  }
+  mma_wait();
+  float dgc[32];
+  {
+    float bq[32];
+    tld32(tbase, 320, bq);  // dO S^T (rows 64..127 of the stacked operand)
+    float in[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) in[r] = 0.f;
+#pragma unroll
+    for (int J = 0; J < 4; ++J) {
+      float a32[32];
+      tld32(tbase, 64 * J, a32);
+#pragma unroll
+      for (int r = 0; r < 32; ++r) in[r] = fmaf(Fq[r >> 4][J], a32[r], in[r]);
+    }
+    float dq[32], pr[32];
+    const float emq0 = sv.em[(2 * g) * D + c], emq1 = sv.em[(2 * g + 1) * D + c];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const float gam = E[r] * (r < 16 ? emq0 : emq1);
+      dq[r] = scale * gam * bq[r] + E[r] * in[r];
+      dgc[r] = dq[r] * qh[r];
+      pr[r] = dgc[r];
+    }
+    red[warp * 64 + 32 * g + lane] = warp_transpose_sum(pr);
+    umma::tc_fence_before();
+    __syncthreads();
+    bf16 *dqg = reinterpret_cast<bf16 *>(p.dq);
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int i = 32 * g + r;
+      const int w0 = 4 * g;
+      const float rd = red[(w0 + 0) * 64 + i] + red[(w0 + 1) * 64 + i] +
+                       red[(w0 + 2) * 64 + i] + red[(w0 + 3) * 64 + i];
+      if (i < len)
+        dqg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn((dq[r] - qh[r] * rd) * sv.rq[i]);
+    }
+    __syncthreads();
+  }
+
+  // ---- P9b: dkd' intra (dA with kp) ----
+  if (tid == 0) {
+    umma::tc_fence_after();
+    for (int J = 0; J < 4; ++J) {
+      gemm(tbase + 64 * J, opk(KPh, 64, 16 * J), false, opk(dAt, 64, 16 * J), false, 64, 1, false);
+      gemm(tbase + 64 * J, opk(KPl, 64, 16 * J), false, opk(dAt, 64, 16 * J), false, 64, 1, true);
+    }
+    umma::mma_commit(mbar);
+  }
+  mma_wait();
+  float dkt[32];
+  {
+    float bk[32];
+    tld32(tbase, 256, bk);  // dvcorr S^T
+#pragma unroll
+    for (int r = 0; r < 32; ++r) dkt[r] = 0.f;
+#pragma unroll
+    for (int J = 0; J < 4; ++J) {
+      float a32[32];
+      tld32(tbase, 64 * J, a32);
+#pragma unroll
+      for (int r = 0; r < 32; ++r) dkt[r] = fmaf(Fq[r >> 4][J], a32[r], dkt[r]);
+    }
+    const float emk0 = sv.em[(2 * g) * D + c], emk1 = sv.em[(2 * g + 1) * D + c];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int i = 32 * g + r;
+      const float gam = E[r] * (r < 16 ? emk0 : emk1);
+      dkt[r] = -sv.beta[i] * gam * bk[r] + E[r] * dkt[r];
+    }
+  }
+  umma::tc_fence_before();
+  __syncthreads();
+
+  // ---- P9c: dki' = E^-1 sum_{I >= J} (Mqk-side + A-side) with qm / km, per query block I ----
+  if (tid == 0) {
+    umma::tc_fence_after();
+    for (int I = 0; I < 4; ++I) {
+      const uint32_t d = tbase + 64 * I;
+      gemm(d, opk(QMh, 64, 16 * I), false, opmn(dMqk, 64, 16 * I), true, 64, 1, false);
+      gemm(d, opk(QMl, 64, 16 * I), false, opmn(dMqk, 64, 16 * I), true, 64, 1, true);
+      gemm(d, opk(KMh, 64, 16 * I), false, opmn(dAt, 64, 16 * I), true, 64, 1, true);
+      gemm(d, opk(KMl, 64, 16 * I), false, opmn(dAt, 64, 16 * I), true, 64, 1, true);
+    }
+    umma::mma_commit(mbar);
+  }
+  mma_wait();
+  {
+    float dki[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) dki[r] = 0.f;
+#pragma unroll
+    for (int I = 0; I < 4; ++I) {
+      float a32[32];
+      tld32(tbase, 64 * I, a32);
+#pragma unroll
+      for (int r = 0; r < 32; ++r) dki[r] = fmaf(Fk[r >> 4][I], a32[r], dki[r]);
+    }
+    float dkr[32];
+    tld32(tbase, 448, dkr);
+    float dk[32], pr[32], colp = 0.f;
+    const float egk0 = sv.egm[(2 * g) * D + c], egk1 = sv.egm[(2 * g + 1) * D + c];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const float rE = __fdividef(1.f, E[r]);
+      const float dkip = dki[r] * rE;
+      const float dkrp = dkr[r] * (r < 16 ? egk0 : egk1) * rE;
+      dk[r] = dkt[r] + dkip + dkrp;
+      const float dks = dkt[r] - dkip - dkrp;
+      dgc[r] = fmaf(dks, kh[r], dgc[r]);
+      colp = fmaf(dkrp, kh[r], colp);
+      pr[r] = dk[r] * kh[r];
+    }
+    red[warp * 64 + 32 * g + lane] = warp_transpose_sum(pr);
+    dgT[g * D + c] += colp;
+    __syncthreads();
+    bf16 *dkg = reinterpret_cast<bf16 *>(p.dk);
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int i = 32 * g + r;
+      const int w0 = 4 * g;
+      const float rd = red[(w0 + 0) * 64 + i] + red[(w0 + 1) * 64 + i] +
+                       red[(w0 + 2) * 64 + i] + red[(w0 + 3) * 64 + i];
+      if (i < len)
+        dkg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn((dk[r] - kh[r] * rd) * sv.rk[i]);
+    }
+  }
+
+  // ---- K1: reverse cumsum over the chunk rows, dg, dA_log ----
+  {
+    float tot = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) tot += dgc[r];
+    __syncthreads();
+    red[g * 128 + c] = tot;  // (red is free again) row-half totals per channel
+    __syncthreads();
+    float run = dgT[c] + dgT[D + c] + (g == 0 ? red[128 + c] : 0.f);
+    const float A = __expf(p.A_log[h]);
+    float dA = 0.f;
+    bf16 *dgg = reinterpret_cast<bf16 *>(p.dg);
+#pragma unroll
+    for (int r = 31; r >= 0; --r) {
+      const int i = 32 * g + r;
+      run += dgc[r];
+      if (i < len) {
+        const float gv = __bfloat162float(Gr[i * D + c]);
+        const float sg = __fdividef(1.f, 1.f + __expf(-gv));
+        dgg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn(run * (-A) * sg);
+        dA = fmaf(run, -A * softplus_f(gv), dA);
+      }
+    }
+    dA = warp_sum(dA);
+    if (lane == 0) dAred[warp] = dA;
+    umma::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < NWARPS; ++w) t += dAred[w];
+      p.dA_part[slot * H + h] = t;
+    }
+  }
+  (void)ok1;
+  if (warp == 0) {
+    umma::tc_fence_after();
+    umma::tmem_dealloc(tbase, 512);
+  }
+}
+
+cudaError_t grads_tc_launch(const KdaParams &p, const void *states, cudaStream_t st) {
+  auto kfn = kda_grads_tc_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)gtc::Smem::total);
+  if (e != cudaSuccess) return e;
+  if (p.nslots > 0) {
+    kfn<<<dim3((unsigned)p.nslots, p.H), NTHREADS, gtc::Smem::total, st>>>(p, states);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+size_t grads_tc_smem_bytes() { return gtc::Smem::total; }
+
+int grads_tc_status_take() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -1;
+  if (cudaMemcpyToSymbol(g_status, &z, sizeof(int)) != cudaSuccess) return -1;
+  return v;
+}
+
+}  // namespace kda

@@ -41,4 +41,9 @@ cudaError_t grads_dispatch(const KdaParams &p, int K, bool bf16, const void *sta
 size_t grads_smem_bytes(int K, bool bf16);
 int grads_status_take();
 
+// kda_grads_tc.cu: the same per-chunk gradients on tcgen05 (bf16, K = V = 128).
+cudaError_t grads_tc_launch(const KdaParams &p, const void *states, cudaStream_t st);
+size_t grads_tc_smem_bytes();
+int grads_tc_status_take();
+
 }  // namespace kda
