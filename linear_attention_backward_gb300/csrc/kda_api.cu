@@ -4,6 +4,7 @@
 
 #include <stdint.h>
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "kda.h"
@@ -74,6 +75,22 @@ int pick_band(const kda_shape *s, int nroles) {
   return bv;
 }
 
+// The tcgen05 state path (chunk-parallel prep + streaming scans) serves bf16
+// with K = V = 128; its per-chunk operand blocks live in the workspace.
+bool tc_state_path(const kda_shape *s) { return s->dtype == KDA_BF16 && s->K == 128; }
+
+size_t prep_bytes(const kda_shape *s) {
+  if (!tc_state_path(s)) return 0;
+  return round_up((size_t)slots_of(s) * s->H * kda::kPrepUnitBytes);
+}
+
+// KDA_SCAN_LEGACY=1 selects the per-band scans (which redo the chunk prep
+// in every band) instead of prep + tcgen05 scans, for comparisons.
+bool legacy_scan() {
+  const char *e = getenv("KDA_SCAN_LEGACY");
+  return e != nullptr && e[0] == '1';
+}
+
 kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
 }  // namespace
@@ -109,7 +126,7 @@ size_t kda_workspace_dstates_offset(const kda_shape *shape) {
 size_t kda_workspace_bytes(const kda_shape *shape) {
   if (check_shape(shape) != KDA_OK) return 0;
   const size_t part = round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
-  return 2 * states_bytes(shape) + part;
+  return 2 * states_bytes(shape) + part + prep_bytes(shape);
 }
 
 kda_status kda_check_cu_seqlens_host(const int32_t *cu, int num_seqs, int total_T) {
@@ -211,9 +228,16 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
   // 1. scans: forward states (unless given) and the reverse dS scan, one launch
   const int nroles = states ? 1 : 2;
   p.role_base = states ? 1 : 0;
-  const int bv = pick_band(shape, nroles);
-  p.nb = shape->V / bv;
-  cudaError_t e = kda::scan_dispatch(p, shape->K, bf, bv, nroles, cs);
+  cudaError_t e;
+  if (tc_state_path(shape) && !legacy_scan()) {
+    void *prep = w + 2 * sb + round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
+    e = kda::prep_tc_launch(p, prep, cs);
+    if (e == cudaSuccess) e = kda::scan_tc_launch(p, prep, nroles, cs);
+  } else {
+    const int bv = pick_band(shape, nroles);
+    p.nb = shape->V / bv;
+    e = kda::scan_dispatch(p, shape->K, bf, bv, nroles, cs);
+  }
   if (e != cudaSuccess) return KDA_ERR_CUDA;
   mark(1);
   // 2. per-chunk gradients and the dA_log reduction
@@ -225,13 +249,14 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
 kda_status kda_get_device_status(kda_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KDA_ERR_CUDA;
-  const int a = kda::scan_status_take();
-  const int b = kda::grads_status_take();
-  const int t = kda::grads_tc_status_take();
-  if (a < 0 || b < 0 || t < 0) return KDA_ERR_CUDA;
-  if (a != 0) return (kda_status)a;
-  if (b != 0) return (kda_status)b;
-  return (kda_status)t;
+  const int words[] = {kda::scan_status_take(), kda::prep_tc_status_take(),
+                       kda::scan_tc_status_take(), kda::grads_status_take(),
+                       kda::grads_tc_status_take()};
+  for (int v : words)
+    if (v < 0) return KDA_ERR_CUDA;
+  for (int v : words)
+    if (v != 0) return (kda_status)v;
+  return KDA_OK;
 }
 
 }  // extern "C"

@@ -27,6 +27,32 @@ struct KdaParams {
   int role_base;              // first scan role of a launch (0 forward, 1 reverse)
 };
 
+// Per-chunk operands of the state scans (bf16, K = V = 128), one block of
+// kPrepUnitBytes per (chunk slot, head), written by the chunk-parallel prep
+// kernel and streamed by the tcgen05 scans.  Every tile is a 128 x 64 or
+// 64 x 128 bf16 matrix in packed core-matrix order (8 x 8 cores of 128
+// bytes, cores along the columns first):
+//   gT   fp32 [128]          total log-decay of the chunk per channel
+//   Wt   [c][i]  W^T,  W  = (I + Akk)^-1 diag(beta) kd
+//   KR   [i][c]  kr  = k^ e^(gT - gc)
+//   U0t  [v][i]  U0^T, U0 = (I + Akk)^-1 diag(beta) v
+//   QEt  [c][i]  QE^T, QE = scale (qd - Mqk W)
+constexpr size_t kPrepGT = 0;
+constexpr size_t kPrepW = 512;
+constexpr size_t kPrepKR = kPrepW + 16384;
+constexpr size_t kPrepU0 = kPrepKR + 16384;
+constexpr size_t kPrepQE = kPrepU0 + 16384;
+constexpr size_t kPrepUnitBytes = kPrepQE + 16384;
+
+// kda_prep_tc.cu: the per-chunk scan operands above (bf16, K = V = 128).
+cudaError_t prep_tc_launch(const KdaParams &p, void *prep, cudaStream_t st);
+int prep_tc_status_take();
+
+// kda_scan_tc.cu: both state scans on tcgen05 from the prep buffer; roles
+// as in scan_dispatch.
+cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cudaStream_t st);
+int scan_tc_status_take();
+
 // kda_scan.cu: forward-state scan (role 0) and reverse dS scan (role 1).
 cudaError_t scan_dispatch(const KdaParams &p, int K, bool bf16, int bv, int nroles,
                           cudaStream_t st);

@@ -1,0 +1,362 @@
+// kda_prep_tc.cu -- chunk-parallel prep of the state-scan operands (bf16,
+// K = V = 128): one CTA per (chunk slot, head), two CTAs per SM.
+//
+// Per chunk it forms, from q, k, v, g and beta (gate and range-safety
+// conventions as in kda_chunk.cuh):
+//   W  = (I + Akk)^-1 diag(beta) kd       U0 = (I + Akk)^-1 diag(beta) v
+//   QE = scale (qd - Mqk W)               kr = k^ e^(gT - gc),  gT
+// With these the two serial recurrences of the backward ("all_states" of
+// kernel B2 and Kernel A, "bwd-kernelB-beginner-guide-full", Part 2, and the
+// A/B table of "bwd-ncu-and-optimization-playbook") need nothing else per
+// chunk than products with the running state:
+//   U     = U0 - W S_n,                  S_{n+1} = e^gT S_n + kr^T U
+//   dS_n  = e^gT dS_{n+1} - W^T (kr dS_{n+1}) + QE^T dO
+// The second line is Kernel A's update with dU and dvcorr substituted:
+// kd^T diag(beta) (I + Akk)^-T = W^T, so
+//   scale qd^T dO - kd^T diag(beta) dvcorr
+//     = scale qd^T dO - W^T (scale Mqk^T dO + kr dS_{n+1}).
+//
+// Layout of the work: thread (channel pair, 16-row block) for the gate, the
+// norms and the decay-scaled tiles (loaded straight from HBM into
+// registers); mma.sync for the 16-row pair blocks of Akk and Mqk (they carry
+// a per-channel factor on the contraction index, see kda_chunk.cuh); the
+// WY inverse in fp32; tcgen05 for the three 64 x 64 x 128 products, whose
+// results land transposed (channel = TMEM lane) and are written to HBM as
+// 16-byte rows of packed core matrices, the byte order the scans copy into
+// shared memory as one bulk copy.
+#include "kda_chunk.cuh"
+#include "kda_tc_tiles.cuh"
+
+namespace kda {
+namespace ptc {
+
+using namespace tct;
+constexpr int D = 128;
+constexpr uint32_t T64x128 = umma::ptile_bytes(64, 128);  // 18432 (padded)
+constexpr uint32_t T64x64 = umma::ptile_bytes(64, 64);    // 9216 (padded)
+
+struct Smem {
+  static constexpr size_t n_view = PrepView<bf16, D>::floats;
+  // extra floats: tbuf 768 (inverse), red 2 x 8 x 16 (row norms)
+  static constexpr size_t n_extra = 768 + 256;
+  static constexpr size_t sz_small = (((n_view + n_extra) * 4 + 64 + 127) / 128) * 128;
+  static constexpr size_t o_QM = sz_small;          // q^ e^(gc - m)  [i][c] padded
+  static constexpr size_t o_KM = o_QM + T64x128;    // k^ e^(gc - m)  [i][c] padded
+  static constexpr size_t o_KP = o_KM + T64x128;    // k^ e^(m - gc)  -> later Mqk [i][j]
+  static constexpr size_t o_V = o_KP + T64x128;     // v [j][v] packed
+  static constexpr size_t o_G = o_V + 16384;        // G / INV fp32 [64][64] -> later W^T
+  static constexpr size_t o_INVb = o_G + 16384;     // INV diag(beta) [i][j] padded
+  static constexpr size_t total = o_INVb + T64x64;
+  static_assert(total + 1024 <= 233472 / 2, "two CTAs per SM");
+};
+
+// Row sums of a 16-vector over the warp's 32 lanes: lane l returns the sum
+// of v[l % 16] over all lanes (31 shuffles).
+__device__ __forceinline__ float half_transpose_sum(float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) v[r] += __shfl_xor_sync(0xffffffffu, v[r], 16);
+#pragma unroll
+  for (int s = 8; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < s; ++k) {
+      const float send = up ? v[k] : v[k + s];
+      const float keep = up ? v[k + s] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
+}  // namespace ptc
+
+__global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, char *prep) {
+  using namespace ptc;
+  using SM = ptc::Smem;
+  extern __shared__ __align__(1024) char smem[];
+  const int64_t slot = blockIdx.x;
+  const int h = blockIdx.y;
+  const int H = p.H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int s_, j_, len;
+  int64_t tok0;
+  if (!slot_owner(p, slot, s_, j_, tok0, len)) return;  // padding slot: never read
+  char *unit = prep + ((size_t)slot * H + h) * kPrepUnitBytes;
+
+  float *smf = reinterpret_cast<float *>(smem);
+  PrepView<bf16, D> sv = make_view<bf16, D>(smf);
+  float *tbuf = smf + SM::n_view;
+  float *red = tbuf + 768;  // [2 (k, q)][8 warps][16 rows]
+  uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + (SM::n_view + SM::n_extra) * 4);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 1);
+  char *QM = smem + SM::o_QM, *KM = smem + SM::o_KM, *KP = smem + SM::o_KP;
+  char *Mqk = KP;
+  char *Vt = smem + SM::o_V;
+  float *Gf = reinterpret_cast<float *>(smem + SM::o_G);
+  char *Wt = smem + SM::o_G;
+  char *INVb = smem + SM::o_INVb;
+  const float scale = p.scale;
+
+  if (warp == 0) umma::tmem_alloc(tslot, 256);
+  if (tid == 0) umma::mbar_init(mbar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  // v rows -> packed core tile [j][v] (the MN-major A operand of U0^T)
+  {
+    const bf16 *vg = reinterpret_cast<const bf16 *>(p.v);
+    for (int e = tid; e < 64 * (D / 8); e += NTHREADS) {
+      const int i = e >> 4, c8 = (e & 15) * 8;
+      const bool ok = i < len;
+      cp_async16(Vt + umma::core_off(i, c8, D), vg + ((tok0 + (ok ? i : 0)) * H + h) * D + c8, ok);
+    }
+    cp_async_commit();
+  }
+  if (tid < CHUNK)
+    sv.beta[tid] = tid < len ? __bfloat162float(reinterpret_cast<const bf16 *>(p.beta)[(tok0 + tid) * H + h])
+                             : 0.f;
+
+  // ---- raw rows straight into registers: thread (channel pair cp, block I) ----
+  const int cp = tid & 63, I = tid >> 6, c = 2 * cp;
+  uint32_t kraw[16], qraw[16];
+  float g0[16], g1[16];
+  {
+    const size_t HD = (size_t)H * D;
+    const bf16 *kb = reinterpret_cast<const bf16 *>(p.k) + (size_t)tok0 * HD + (size_t)h * D + c;
+    const bf16 *qb = reinterpret_cast<const bf16 *>(p.q) + (size_t)tok0 * HD + (size_t)h * D + c;
+    const bf16 *gb = reinterpret_cast<const bf16 *>(p.g) + (size_t)tok0 * HD + (size_t)h * D + c;
+    uint32_t graw[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int i = 16 * I + r;
+      const bool ok = i < len;
+      const size_t off = (size_t)(ok ? i : 0) * HD;
+      kraw[r] = ok ? *reinterpret_cast<const uint32_t *>(kb + off) : 0u;
+      qraw[r] = ok ? *reinterpret_cast<const uint32_t *>(qb + off) : 0u;
+      graw[r] = ok ? *reinterpret_cast<const uint32_t *>(gb + off) : 0u;
+    }
+    // norms: per-row partial sums over this thread's two channels
+    float sk[16], sq[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float2 kv = bf2_to_f2(kraw[r]), qv = bf2_to_f2(qraw[r]);
+      sk[r] = fmaf(kv.x, kv.x, kv.y * kv.y);
+      sq[r] = fmaf(qv.x, qv.x, qv.y * qv.y);
+    }
+    const float tk = half_transpose_sum(sk);
+    const float tq = half_transpose_sum(sq);
+    if (lane < 16) {
+      red[warp * 16 + lane] = tk;
+      red[128 + warp * 16 + lane] = tq;
+    }
+    // gate: running sum over the block (sums local to the block)
+    const float A = __expf(p.A_log[h]);
+    float run0 = 0.f, run1 = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const bool ok = 16 * I + r < len;
+      const float2 gv = bf2_to_f2(graw[r]);
+      run0 += ok ? -A * softplus_f(gv.x) : 0.f;
+      run1 += ok ? -A * softplus_f(gv.y) : 0.f;
+      g0[r] = run0;
+      g1[r] = run1;
+    }
+    float *Ablk = sv.part, *Bblk = sv.m;
+    Ablk[I * D + c] = g0[7];
+    Ablk[I * D + c + 1] = g1[7];
+    Bblk[I * D + c] = g0[15] - g0[7];
+    Bblk[I * D + c + 1] = g1[15] - g1[7];
+  }
+  __syncthreads();
+  if (tid < CHUNK) {  // row norms: block I's rows live in warps 2I, 2I + 1
+    const int ib = tid >> 4, r = tid & 15;
+    sv.rk[tid] = rsqrtf(red[(2 * ib) * 16 + r] + red[(2 * ib + 1) * 16 + r] + p.eps);
+    sv.rq[tid] = rsqrtf(red[128 + (2 * ib) * 16 + r] + red[128 + (2 * ib + 1) * 16 + r] + p.eps);
+  } else if (tid >= 128) {  // per-(block, channel) factors from the block partials
+    const int e = tid - 128;
+    float a[4], bb[4];
+#pragma unroll
+    for (int L = 0; L < 4; ++L) {
+      a[L] = sv.part[L * D + e];
+      bb[L] = sv.m[L * D + e];
+    }
+    float before = 0.f, tot = 0.f;
+#pragma unroll
+    for (int L = 0; L < 4; ++L) tot += a[L] + bb[L];
+#pragma unroll
+    for (int L = 0; L < 4; ++L) {
+      float after = bb[L];
+#pragma unroll
+      for (int L2 = L + 1; L2 < 4; ++L2) after += a[L2] + bb[L2];
+      sv.em[L * D + e] = __expf(before + a[L]);  // e^(m_L)
+      sv.egm[L * D + e] = __expf(after);         // e^(gT - m_L)
+      before += a[L] + bb[L];
+    }
+#pragma unroll
+    for (int I2 = 1; I2 < 4; ++I2)
+#pragma unroll
+      for (int J = 0; J < I2; ++J) {
+        float d = bb[J] + a[I2];
+#pragma unroll
+        for (int L = J + 1; L < I2; ++L) d += a[L] + bb[L];
+        sv.F[pair_index(I2, J) * D + e] = __expf(d);  // e^(m_I - m_J)
+      }
+    reinterpret_cast<float *>(unit + kPrepGT)[e] = tot;
+  }
+  __syncthreads();
+  // ---- decay-scaled tiles; kr goes straight to HBM ----
+  {
+    const float eg0 = sv.egm[I * D + c], eg1 = sv.egm[I * D + c + 1];
+    char *kr_out = unit + kPrepKR;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int i = 16 * I + r;
+      const float rk = sv.rk[i], rq = sv.rq[i];
+      const float2 kv = bf2_to_f2(kraw[r]), qv = bf2_to_f2(qraw[r]);
+      const float kh0 = kv.x * rk, kh1 = kv.y * rk, qh0 = qv.x * rq, qh1 = qv.y * rq;
+      const float d0 = g0[r] - g0[7], d1 = g1[r] - g1[7];
+      const float e0 = __expf(d0), e1 = __expf(d1);
+      const float ei0 = __expf(-d0), ei1 = __expf(-d1);
+      const uint32_t off = pcore_off(i, c, D);
+      *reinterpret_cast<uint32_t *>(QM + off) = f2_to_bf2(qh0 * e0, qh1 * e1);
+      *reinterpret_cast<uint32_t *>(KM + off) = f2_to_bf2(kh0 * e0, kh1 * e1);
+      *reinterpret_cast<uint32_t *>(KP + off) = f2_to_bf2(kh0 * ei0, kh1 * ei1);
+      *reinterpret_cast<uint32_t *>(kr_out + umma::core_off(i, c, D)) =
+          f2_to_bf2((kh0 * ei0) * eg0, (kh1 * ei1) * eg1);
+    }
+  }
+  __syncthreads();
+  // ---- pair blocks: G = kd ki^T (strictly lower, fp32), scale * Mqk (lower) ----
+  {
+    const int Ib = warp & 3;
+    const bool is_q = warp >= 4;
+    const char *X = is_q ? QM : KM;
+    float acc[4][2][4];
+#pragma unroll
+    for (int J = 0; J < 4; ++J) {
+      zero_acc(acc[J]);
+      if (J <= Ib)
+        wg_core<2>(acc[J], X, D, 16 * Ib, 0, KP, D, 16 * J, 0, D,
+                   J < Ib ? sv.F + pair_index(Ib, J) * D : nullptr);
+      if (!is_q)
+        for_acc(acc[J], [&](int r, int cc, float &v) {
+          const int i = 16 * Ib + r, jj = 16 * J + cc;
+          Gf[i * 64 + jj] = jj < i ? v : 0.f;
+        });
+    }
+    __syncthreads();  // KP is read by every warp above; Mqk overwrites it
+    if (is_q) {
+#pragma unroll
+      for (int J = 0; J < 4; ++J)
+        for_acc(acc[J], [&](int r, int cc, float &v) {
+          const int i = 16 * Ib + r, jj = 16 * J + cc;
+          *pel(Mqk, i, jj, 64) = __float2bfloat16_rn(jj <= i ? scale * v : 0.f);
+        });
+    }
+  }
+  __syncthreads();
+  inverse_inplace(Gf, sv.beta, tbuf);
+  for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
+    const int i = e8 >> 3, j0 = (e8 & 7) * 8;
+    float x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) x[u] = Gf[i * 64 + j0 + u] * sv.beta[j0 + u];
+    pstore8(INVb, i, j0, 64, x);
+  }
+  umma::fence_async_smem();
+  umma::tc_fence_before();
+  __syncthreads();
+  umma::tc_fence_after();
+  const uint32_t tbase = *tslot;
+  uint32_t phase = 0;
+  auto mma_wait = [&]() {
+    const bool ok = umma::mbar_wait(mbar, phase & 1, 1u << 20);
+    phase++;
+    umma::tc_fence_after();
+    return ok;
+  };
+  // ---- W^T per key block J (the block factor e^(m_J) is applied per lane below) ----
+  if (tid == 0) {
+    for (int J = 0; J < 4; ++J)
+      gemm(tbase + 64 * J, opmn(KM, D, 16 * J), true, opk(INVb, 64, 16 * J), false, 64, 1, false);
+    umma::mma_commit(mbar);
+  }
+  mma_wait();
+  const int ch = tid & 127, gq = tid >> 7;  // TMEM lane (channel) and 32-column group
+  {
+    float w[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) w[r] = 0.f;
+#pragma unroll
+    for (int J = 0; J < 4; ++J) {
+      float a[32];
+      tld32(tbase, 64 * J, a);
+      const float em = sv.em[J * D + ch];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) w[r] = fmaf(em, a[r], w[r]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t off = umma::core_off(ch, 32 * gq + 8 * q, 64);
+      st16_bf(Wt + off, w + 8 * q);
+      st16_bf(unit + kPrepW + off, w + 8 * q);
+    }
+  }
+  cp_async_wait_all();  // v has landed
+  umma::fence_async_smem();
+  umma::tc_fence_before();
+  __syncthreads();
+  // ---- U0^T = v^T (INV diag(beta))^T ;  (Mqk W)^T = W^T Mqk^T ----
+  if (tid == 0) {
+    umma::tc_fence_after();
+    gemm(tbase + 0, opmn(Vt, D, 0, CP), true, opk(INVb, 64), false, 64, 4, false);
+    gemm(tbase + 64, opk(Wt, 64, 0, CP), false, opk(Mqk, 64), false, 64, 4, false);
+    umma::mma_commit(mbar);
+  }
+  mma_wait();
+  {
+    float a[32];
+    tld32(tbase, 0, a);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st16_bf(unit + kPrepU0 + umma::core_off(ch, 32 * gq + 8 * q, 64), a + 8 * q);
+    tld32(tbase, 64, a);
+    const float em0 = sv.em[(2 * gq) * D + ch], em1 = sv.em[(2 * gq + 1) * D + ch];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int i = 32 * gq + r;
+      const float qd = pget(QM, i, ch, D) * (r < 16 ? em0 : em1);
+      a[r] = fmaf(scale, qd, -a[r]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st16_bf(unit + kPrepQE + umma::core_off(ch, 32 * gq + 8 * q, 64), a + 8 * q);
+  }
+  umma::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    umma::tc_fence_after();
+    umma::tmem_dealloc(tbase, 256);
+  }
+}
+
+cudaError_t prep_tc_launch(const KdaParams &p, void *prep, cudaStream_t st) {
+  auto kfn = kda_prep_tc_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)ptc::Smem::total);
+  if (e != cudaSuccess) return e;
+  if (p.nslots > 0) {
+    kfn<<<dim3((unsigned)p.nslots, p.H), NTHREADS, ptc::Smem::total, st>>>(
+        p, static_cast<char *>(prep));
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+int prep_tc_status_take() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -1;
+  if (cudaMemcpyToSymbol(g_status, &z, sizeof(int)) != cudaSuccess) return -1;
+  return v;
+}
+
+}  // namespace kda

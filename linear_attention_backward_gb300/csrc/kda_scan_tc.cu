@@ -1,0 +1,300 @@
+// kda_scan_tc.cu -- the two serial chunk scans of the KDA backward on the
+// fifth-generation tensor cores (bf16, K = V = 128), streaming the per-chunk
+// operands written by the prep kernel (kda_prep_tc.cu):
+//
+//  * forward role: the chunk-state recompute ("all_states", read by kernel
+//    B2 of "bwd-kernelB-beginner-guide-full", Part 2, B2 optimisation 4)
+//      U = U0 - W S_n,          S_{n+1} = e^gT S_n + kr^T U
+//  * reverse role: Kernel A, the reverse scan of the per-chunk state
+//    gradient ("bwd-ncu-and-optimization-playbook", A/B table)
+//      dS_n = e^gT dS_{n+1} - W^T (kr dS_{n+1}) + QE^T dO
+//
+// One CTA per (sequence, head, role), two CTAs per SM, all 256 threads on
+// the epilogues.  Per chunk two tcgen05 products, both with the channel
+// dimension (128) as M:
+//   MMA1  T1[v][i] = sum_c X[c][v] B1[i][c]       N = 64,  K = 128
+//         (B1 = W forward, kr reverse; T1^T = W S_n or kr dS_{n+1})
+//   MMA2  T2[c][v] = sum_i A2[i][c] U[i][v] (+ sum_i QE[i][c] dO[i][v])
+//         (A2 = kr forward, W reverse)             N = 128, K = 64
+// The fp32 running state X stays in registers (thread = TMEM lane c and one
+// half of the V columns); its bf16 copy in shared memory is MMA1's operand
+// and is what goes to HBM as the chunk's state (the grads kernel reads the
+// same rounding the scan used).  The chunk's operand block (gT, W^T, kr,
+// U0^T or QE^T; 48.5 KB) arrives by bulk TMA copies on an mbarrier, issued
+// as soon as MMA2 of the previous chunk has consumed the buffer, with an L2
+// prefetch two chunks ahead; the reverse role's dO rows come by cp.async.
+#include "kda_chunk.cuh"
+#include "kda_tc_tiles.cuh"
+
+namespace kda {
+namespace stc {
+
+using namespace tct;
+constexpr int D = 128;
+constexpr uint32_t kInFwd = (uint32_t)kPrepQE;                 // gT, W^T, kr, U0^T
+constexpr uint32_t kInRevA = (uint32_t)kPrepU0;                // gT, W^T, kr
+constexpr uint32_t kQEHere = (uint32_t)kPrepU0;                // QE^T lands where U0^T would
+struct Smem {
+  static constexpr size_t o_X = 0;                 // state [c][v] packed, 32 KB
+  static constexpr size_t o_IN = o_X + 32768;      // operand block, 48.5 KB
+  static constexpr size_t o_dO = o_IN + kInFwd;    // dO [i][v] packed (reverse role)
+  static constexpr size_t o_U = o_dO + 16384;      // U^T [v][i] packed
+  static constexpr size_t o_bar = o_U + 16384;
+  static constexpr size_t total = o_bar + 64;
+  static_assert(total + 1024 <= 233472 / 2, "two CTAs per SM");
+  static_assert(o_IN % 16 == 0 && o_dO % 16 == 0, "bulk copy alignment");
+};
+
+}  // namespace stc
+
+__global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, const char *prep) {
+  using namespace stc;
+  using SM = stc::Smem;
+  extern __shared__ __align__(1024) char smem[];
+  const int role = p.role_base + blockIdx.y;  // 0: forward states, 1: reverse dS scan
+  const bool fwd = role == 0;
+  const int h = blockIdx.x % p.H, s = blockIdx.x / p.H;
+  const int H = p.H;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  int64_t tok_seq, slot0;
+  int L;
+  if (!seq_bounds(p, s, tok_seq, L, slot0)) return;
+  const int nck = (L + CHUNK - 1) / CHUNK;
+  char *Xs = smem + SM::o_X, *IN = smem + SM::o_IN, *dOs = smem + SM::o_dO, *Us = smem + SM::o_U;
+  uint64_t *bar_in = reinterpret_cast<uint64_t *>(smem + SM::o_bar);
+  uint64_t *bar_mma = bar_in + 1;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_in + 2);
+
+  const int ch = tid & 127, hf = tid >> 7;  // TMEM lane; half of the columns
+  const size_t DD = (size_t)D * D;
+  // running state: row ch, columns [64 hf, 64 hf + 64)
+  float X[64];
+  {
+    const float *init = fwd ? p.h0 : p.dhT;
+    const float *src = init ? init + ((size_t)s * H + h) * DD + (size_t)ch * D + 64 * hf : nullptr;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float4 v = src ? *reinterpret_cast<const float4 *>(src + 4 * q)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      X[4 * q] = v.x;
+      X[4 * q + 1] = v.y;
+      X[4 * q + 2] = v.z;
+      X[4 * q + 3] = v.w;
+    }
+  }
+  if (warp == 0) umma::tmem_alloc(tslot, 256);
+  if (tid == 0) {
+    umma::mbar_init(bar_in, 1);
+    umma::mbar_init(bar_mma, 1);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  __syncthreads();
+
+  auto chunk_of = [&](int it) { return fwd ? it : nck - 1 - it; };
+  auto unit_of = [&](int j) {
+    return prep + ((size_t)(slot0 + j) * H + h) * kPrepUnitBytes;
+  };
+  const bf16 *dOg = reinterpret_cast<const bf16 *>(p.dO);
+  auto issue_loads = [&](int it) {
+    const int j = chunk_of(it);
+    const char *u = unit_of(j);
+    if (tid == 0) {
+      umma::mbar_expect_tx(bar_in, fwd ? kInFwd : kInRevA + 16384u);
+      if (fwd) {
+        umma::bulk_g2s(IN, u, kInFwd, bar_in);
+      } else {
+        umma::bulk_g2s(IN, u, kInRevA, bar_in);
+        umma::bulk_g2s(IN + kQEHere, u + kPrepQE, 16384u, bar_in);
+      }
+    }
+    if (!fwd) {  // dO rows -> packed core tile [i][v]
+      const int64_t t0 = tok_seq + (int64_t)j * CHUNK;
+      const int ln = min(CHUNK, L - j * CHUNK);
+      for (int e = tid; e < 64 * (D / 8); e += NTHREADS) {
+        const int i = e >> 4, c8 = (e & 15) * 8;
+        const bool ok = i < ln;
+        cp_async16(dOs + umma::core_off(i, c8, D), dOg + ((t0 + (ok ? i : 0)) * H + h) * D + c8,
+                   ok);
+      }
+      cp_async_commit();
+    }
+  };
+  auto prefetch = [&](int it) {
+    const int j = chunk_of(it);
+    const char *u = unit_of(j);
+    if (tid == 0) {
+      if (fwd) {
+        umma::bulk_prefetch_l2(u, kInFwd);
+      } else {
+        umma::bulk_prefetch_l2(u, kInRevA);
+        umma::bulk_prefetch_l2(u + kPrepQE, 16384u);
+      }
+    }
+    if (!fwd && tid >= 64 && tid < 128) {
+      const int i = tid - 64;
+      const int64_t t0 = tok_seq + (int64_t)j * CHUNK;
+      if (i < L - j * CHUNK) umma::bulk_prefetch_l2(dOg + ((t0 + i) * H + h) * D, D * 2);
+    }
+  };
+  // bf16 state -> shared operand tile and the chunk's slot in HBM
+  bf16 *states_out = reinterpret_cast<bf16 *>(fwd ? p.states : p.dstates);
+  auto publish = [&](int j) {
+    bf16 *dst = states_out + ((size_t)(slot0 + j) * H + h) * DD + (size_t)ch * D + 64 * hf;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      st16_bf(Xs + umma::core_off(ch, 64 * hf + 8 * q, D), X + 8 * q);
+      st16_bf(dst + 8 * q, X + 8 * q);
+    }
+  };
+
+  if (nck > 0) {
+    issue_loads(0);
+    if (nck > 1) prefetch(1);
+    publish(chunk_of(0));
+  }
+  umma::fence_async_smem();
+  umma::tc_fence_before();
+  __syncthreads();
+  umma::tc_fence_after();
+  const uint32_t tbase = *tslot;
+  uint32_t ph_in = 0, ph_mma = 0;
+  bool bad = false, in_pending = nck > 0;
+  const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's TMEM lanes
+
+  for (int it = 0; it < nck; ++it) {
+    if (it + 2 < nck) prefetch(it + 2);
+    // ---- operands of this chunk ----
+    bool ok = umma::mbar_wait(bar_in, ph_in & 1);
+    ph_in++;
+    in_pending = !ok;
+    if (!fwd) {
+      cp_async_wait_all();
+      umma::fence_async_smem();
+    }
+    if (__syncthreads_or(!ok)) {
+      bad = true;
+      break;
+    }
+    // ---- MMA1: T1 = (B1 X)^T into columns [0, 64) ----
+    if (tid == 0) {
+      umma::tc_fence_after();
+      const Op a = opmn(Xs, D, 0, CP);
+      if (fwd)
+        gemm(tbase, a, true, opmn(IN + kPrepW, 64, 0, CP), true, 64, D / 16, false);
+      else
+        gemm(tbase, a, true, opk(IN + kPrepKR, D, 0, CP), false, 64, D / 16, false);
+      umma::mma_commit(bar_mma);
+    }
+    const float eg = __expf(reinterpret_cast<const float *>(IN + kPrepGT)[ch]);
+    ok = umma::mbar_wait(bar_mma, ph_mma & 1);
+    ph_mma++;
+    umma::tc_fence_after();
+    // ---- U^T[v][i] for lane v = ch, i in [32 hf, 32 hf + 32) ----
+    {
+      float t[32];
+      tld32(tbase, 0, t);
+      if (fwd) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float u0[8];
+          ld16_bf(IN + kPrepU0 + umma::core_off(ch, 32 * hf + 8 * q, 64), u0);
+#pragma unroll
+          for (int n = 0; n < 8; ++n) t[8 * q + n] = u0[n] - t[8 * q + n];
+        }
+      } else {
+#pragma unroll
+        for (int n = 0; n < 32; ++n) t[n] = -t[n];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) st16_bf(Us + umma::core_off(ch, 32 * hf + 8 * q, 64), t + 8 * q);
+    }
+    umma::fence_async_smem();
+    umma::tc_fence_before();
+    if (__syncthreads_or(!ok)) {
+      bad = true;
+      break;
+    }
+    // ---- MMA2: T2 into columns [64, 192) ----
+    if (tid == 0) {
+      umma::tc_fence_after();
+      const Op b = opk(Us, 64, 0, CP);
+      if (fwd) {
+        gemm(tbase + 64, opmn(IN + kPrepKR, D, 0, CP), true, b, false, 128, 4, false);
+      } else {
+        gemm(tbase + 64, opk(IN + kPrepW, 64, 0, CP), false, b, false, 128, 4, false);
+        gemm(tbase + 64, opk(IN + kQEHere, 64, 0, CP), false, opmn(dOs, D, 0, CP), true, 128, 4,
+             true);
+      }
+      umma::mma_commit(bar_mma);
+    }
+    ok = umma::mbar_wait(bar_mma, ph_mma & 1);
+    ph_mma++;
+    umma::tc_fence_after();
+    if (__syncthreads_or(!ok)) {
+      bad = true;
+      break;
+    }
+    // every operand of this chunk is consumed: start the next chunk's copies
+    if (it + 1 < nck) {
+      issue_loads(it + 1);
+      in_pending = true;
+    }
+    // ---- state update: X = e^gT X + T2 ----
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float t[16];
+      umma::tmem_ld16(tl + 64 + 64 * hf + 16 * q, t);
+      umma::tmem_ld_wait();
+#pragma unroll
+      for (int n = 0; n < 16; ++n) X[16 * q + n] = fmaf(eg, X[16 * q + n], t[n]);
+    }
+    if (it + 1 < nck) publish(chunk_of(it + 1));
+    umma::fence_async_smem();
+    umma::tc_fence_before();
+    __syncthreads();
+  }
+  if (bad) {
+    // a bounded wait gave up (status already flagged): let copies and MMAs in
+    // flight land before the buffers and Tensor Memory are released
+    if (in_pending) umma::mbar_wait(bar_in, ph_in & 1);
+    cp_async_wait_all();
+    umma::mbar_wait(bar_mma, ph_mma & 1, 1u << 16);
+    __syncthreads();
+  } else {
+    float *fin = fwd ? p.hT : p.dh0;
+    if (fin != nullptr) {
+      float *dst = fin + ((size_t)s * H + h) * DD + (size_t)ch * D + 64 * hf;
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        *reinterpret_cast<float4 *>(dst + 4 * q) =
+            make_float4(X[4 * q], X[4 * q + 1], X[4 * q + 2], X[4 * q + 3]);
+    }
+  }
+  umma::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    umma::tc_fence_after();
+    umma::tmem_dealloc(tbase, 256);
+  }
+}
+
+cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cudaStream_t st) {
+  auto kfn = kda_scan_tc_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)stc::Smem::total);
+  if (e != cudaSuccess) return e;
+  const int nunits = (p.cu ? p.num_seqs : p.B) * p.H;
+  if (nunits == 0 || nroles == 0) return cudaSuccess;
+  kfn<<<dim3(nunits, nroles), NTHREADS, stc::Smem::total, st>>>(p,
+                                                                 static_cast<const char *>(prep));
+  return cudaGetLastError();
+}
+
+int scan_tc_status_take() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -1;
+  if (cudaMemcpyToSymbol(g_status, &z, sizeof(int)) != cudaSuccess) return -1;
+  return v;
+}
+
+}  // namespace kda

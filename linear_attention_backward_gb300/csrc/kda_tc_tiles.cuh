@@ -1,0 +1,269 @@
+// kda_tc_tiles.cuh -- shared-memory tile helpers for the tcgen05 kernels:
+// element access in the padded core-matrix layout, tcgen05 operand
+// descriptors for tiles read K-major or MN-major, and mma.sync products on
+// the same padded tiles (used for the small 16-row pair blocks).
+#pragma once
+
+#include "kda_umma.cuh"
+
+namespace kda {
+namespace tct {
+
+using umma::pcore_off;
+constexpr uint32_t CS = umma::kCoreStride;  // padded core stride (144 bytes)
+constexpr uint32_t CP = 128;                // packed core stride
+
+
+__device__ __forceinline__ bf16 *pel(void *t, int r, int c, int C) {
+  return reinterpret_cast<bf16 *>(reinterpret_cast<char *>(t) + pcore_off(r, c, C));
+}
+__device__ __forceinline__ float pget(const void *t, int r, int c, int C) {
+  return __bfloat162float(
+      *reinterpret_cast<const bf16 *>(reinterpret_cast<const char *>(t) + pcore_off(r, c, C)));
+}
+// 8 consecutive columns c0 .. c0 + 7 (c0 % 8 == 0) of row r, one 16-byte store
+__device__ __forceinline__ void pstore8(void *t, int r, int c0, int C, const float *v) {
+  __nv_bfloat162 h[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+  *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(t) + pcore_off(r, c0, C)) =
+      *reinterpret_cast<uint4 *>(h);
+}
+__device__ __forceinline__ void pload8(const void *t, int r, int c0, int C, float *v) {
+  const uint4 u =
+      *reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(t) + pcore_off(r, c0, C));
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __bfloat1622float2(h[q]);
+    v[2 * q] = f.x;
+    v[2 * q + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+// 8 fp32 -> one 16-byte row of a packed core tile (global or shared)
+__device__ __forceinline__ void st16_bf(void *dst, const float *v) {
+  uint4 u;
+  u.x = f2_to_bf2(v[0], v[1]);
+  u.y = f2_to_bf2(v[2], v[3]);
+  u.z = f2_to_bf2(v[4], v[5]);
+  u.w = f2_to_bf2(v[6], v[7]);
+  *reinterpret_cast<uint4 *>(dst) = u;
+}
+// one 16-byte row of 8 bf16 -> 8 fp32
+__device__ __forceinline__ void ld16_bf(const void *src, float *v) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(src);
+  const float2 a = bf2_to_f2(u.x), b = bf2_to_f2(u.y), c = bf2_to_f2(u.z), d = bf2_to_f2(u.w);
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+  v[4] = c.x; v[5] = c.y; v[6] = d.x; v[7] = d.y;
+}
+
+// ---- tcgen05 operands -------------------------------------------------------
+struct Op {
+  uint32_t addr, lbo, sbo, step;
+};
+// stored tile [R][C] read with K along its columns, from column k0
+__device__ __forceinline__ Op opk(const void *t, int C, int k0 = 0, uint32_t cs = CS) {
+  return Op{smem_u32(t) + (uint32_t)(k0 / 8) * cs, cs, (uint32_t)(C / 8) * cs, 2 * cs};
+}
+// stored tile [R][C] read with K along its rows, from row r0
+__device__ __forceinline__ Op opmn(const void *t, int C, int r0 = 0, uint32_t cs = CS) {
+  return Op{smem_u32(t) + (uint32_t)(r0 / 8) * (C / 8) * cs, (uint32_t)(C / 8) * cs, cs,
+            2 * (uint32_t)(C / 8) * cs};
+}
+__device__ __forceinline__ void gemm(uint32_t d, Op a, bool amn, Op b, bool bmn, int N, int ksteps,
+                                     bool accumulate) {
+  const uint32_t id = umma::idesc_bf16(128, N, amn, bmn);
+  for (int s = 0; s < ksteps; ++s)
+    umma::mma_bf16(d, umma::smem_desc(a.addr + s * a.step, a.lbo, a.sbo),
+                   umma::smem_desc(b.addr + s * b.step, b.lbo, b.sbo), id, accumulate || s > 0);
+}
+
+// ---- mma.sync on padded core tiles (pair matrices) ---------------------------
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t a) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t a) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+// acc (16 x 8 NF) += A (16 x kdim) B (kdim x 8 NF) from transposed tiles:
+// A(m, k) = tile A[ak0 + k][am0 + m], B(k, n) = tile B[bk0 + k][bn0 + n];
+// kscale per k (the tiles' row index).
+template <int NF>
+__device__ __forceinline__ void wg_core_t(float (&acc)[NF][4], const void *A, int AC, int ak0,
+                                          int am0, const void *B, int BC, int bk0, int bn0,
+                                          int kdim, const float *kscale) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+#pragma unroll
+  for (int k0 = 0; k0 < kdim; k0 += 16) {
+    uint32_t af[4];
+    ldsm4t(af, a0 + pcore_off(ak0 + k0 + (lane & 7) + (lane >> 4) * 8,
+                              am0 + ((lane >> 3) & 1) * 8, AC));
+    if (kscale != nullptr) {
+      const int c = k0 + 2 * (lane & 3);
+      const float s0 = kscale[c], s1 = kscale[c + 1], s8 = kscale[c + 8], s9 = kscale[c + 9];
+      af[0] = scale_pair(af[0], s0, s1);
+      af[1] = scale_pair(af[1], s0, s1);
+      af[2] = scale_pair(af[2], s8, s9);
+      af[3] = scale_pair(af[3], s8, s9);
+    }
+#pragma unroll
+    for (int f = 0; f < NF; f += 2) {
+      uint32_t bfr[4];
+      ldsm4t(bfr, b0 + pcore_off(bk0 + k0 + (lane & 7) + ((lane >> 3) & 1) * 8,
+                                 bn0 + f * 8 + (lane >> 4) * 8, BC));
+      mma_16816(acc[f], af, bfr[0], bfr[1]);
+      mma_16816(acc[f + 1], af, bfr[2], bfr[3]);
+    }
+  }
+}
+// acc (16 x 8 NF) += A (16 x kdim) B (kdim x 8 NF); A(m, k) = tile A[ar0 + m][ac0 + k],
+// B(k, n) = tile B[br0 + n][bc0 + k]; both K-contiguous tiles; kscale per k.
+template <int NF>
+__device__ __forceinline__ void wg_core(float (&acc)[NF][4], const void *A, int AC, int ar0,
+                                        int ac0, const void *B, int BC, int br0, int bc0,
+                                        int kdim, const float *kscale) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+#pragma unroll
+  for (int k0 = 0; k0 < kdim; k0 += 16) {
+    uint32_t af[4];
+    ldsm4(af, a0 + pcore_off(ar0 + (lane & 15), ac0 + k0 + (lane >> 4) * 8, AC));
+    if (kscale != nullptr) {
+      const int c = k0 + 2 * (lane & 3);
+      const float s0 = kscale[c], s1 = kscale[c + 1], s8 = kscale[c + 8], s9 = kscale[c + 9];
+      af[0] = scale_pair(af[0], s0, s1);
+      af[1] = scale_pair(af[1], s0, s1);
+      af[2] = scale_pair(af[2], s8, s9);
+      af[3] = scale_pair(af[3], s8, s9);
+    }
+#pragma unroll
+    for (int f = 0; f < NF; f += 2) {
+      uint32_t bfr[4];
+      ldsm4(bfr, b0 + pcore_off(br0 + f * 8 + (lane & 7) + (lane >> 4) * 8,
+                                bc0 + k0 + ((lane >> 3) & 1) * 8, BC));
+      mma_16816(acc[f], af, bfr[0], bfr[1]);
+      mma_16816(acc[f + 1], af, bfr[2], bfr[3]);
+    }
+  }
+}
+
+// Gf [64][64] fp32 holds G (strictly lower) on entry and (I + diag(beta) G)^-1
+// on exit (block forward substitution in place; see wy_inverse).
+__device__ inline void inverse_inplace(float *Gf, const float *beta, float *tbuf) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int LG = 64;
+  if (warp < 4) {
+    const int o = 16 * warp, col = lane & 15;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float br = beta[o + r];
+      const float *grow = Gf + (o + r) * LG + o;
+      float s0 = (r == col) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < r; ++j) {
+        if (j & 1)
+          s1 = fmaf(-br * grow[j], x[j], s1);
+        else
+          s0 = fmaf(-br * grow[j], x[j], s0);
+      }
+      x[r] = s0 + s1;
+    }
+    __syncwarp();
+    if (lane < 16) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) Gf[(o + r) * LG + o + col] = x[r];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int I = 1; I < 4; ++I) {
+    const int J = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+    const int row = 16 * I + r;
+    if (J < I) {
+      const float *grow = Gf + row * LG;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int Lb = J; Lb < I; ++Lb) {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const float gv = grow[16 * Lb + x];
+          const float4 xv = *reinterpret_cast<const float4 *>(Gf + (16 * Lb + x) * LG + 16 * J + c4);
+          t.x = fmaf(gv, xv.x, t.x);
+          t.y = fmaf(gv, xv.y, t.y);
+          t.z = fmaf(gv, xv.z, t.z);
+          t.w = fmaf(gv, xv.w, t.w);
+        }
+      }
+      const float br = beta[row];
+      *reinterpret_cast<float4 *>(tbuf + (J << 8) + (r << 4) + c4) =
+          make_float4(br * t.x, br * t.y, br * t.z, br * t.w);
+    }
+    __syncthreads();
+    if (J < I) {
+      const float *xr = Gf + row * LG + 16 * I;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const float xv = xr[x];
+        const float4 tv = *reinterpret_cast<const float4 *>(tbuf + (J << 8) + (x << 4) + c4);
+        t.x = fmaf(xv, tv.x, t.x);
+        t.y = fmaf(xv, tv.y, t.y);
+        t.z = fmaf(xv, tv.z, t.z);
+        t.w = fmaf(xv, tv.w, t.w);
+      }
+      *reinterpret_cast<float4 *>(Gf + row * LG + 16 * J + c4) = make_float4(-t.x, -t.y, -t.z, -t.w);
+    }
+    __syncthreads();
+  }
+}
+
+// Row sums over the warp's 32 lanes for 32 rows at once: lane l returns
+// sum over lanes of v[l] (31 shuffles instead of 32 x 5); v is consumed.
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < s; ++k) {
+      const float send = up ? v[k] : v[k + s];
+      const float keep = up ? v[k + s] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
+// TMEM address of this thread's lane (warp quarter) at column col
+__device__ __forceinline__ uint32_t tm(uint32_t tbase, int col) {
+  return tbase + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16) + (uint32_t)col;
+}
+// this thread's 32 columns [col0 + 32 g, +32) of its lane
+__device__ __forceinline__ void tld32(uint32_t tbase, int col0, float (&v)[32]) {
+  const int g = threadIdx.x >> 7;
+  float a[16], b[16];
+  umma::tmem_ld16(tm(tbase, col0 + 32 * g), a);
+  umma::tmem_ld16(tm(tbase, col0 + 32 * g + 16), b);
+  umma::tmem_ld_wait();
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    v[q] = a[q];
+    v[16 + q] = b[q];
+  }
+}
+
+}  // namespace tct
+}  // namespace kda

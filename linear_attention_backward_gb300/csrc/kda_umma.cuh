@@ -118,6 +118,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity,
   return false;
 }
 
+// ---- bulk copies (the non-tensor TMA path) ------------------------------------
+// One thread arms the barrier with the byte count of the copies that complete it.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(mbar)),
+               "r"(bytes)
+               : "memory");
+}
+// global -> shared, `bytes` a multiple of 16, both addresses 16-byte aligned
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(mbar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---- fences ------------------------------------------------------------------
 // generic-proxy smem writes -> visible to the tensor core (async proxy)
 __device__ __forceinline__ void fence_async_smem() {

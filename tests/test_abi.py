@@ -57,11 +57,16 @@ def test_slots_and_workspace(L):
     sb = 6 * 3 * 128 * 128 * 2
     sb = (sb + 255) // 256 * 256
     assert kda.workspace_dstates_offset(s) == sb
-    assert kda.workspace_bytes(s) == 2 * sb + ((6 * 3 * 4 + 255) // 256) * 256
+    # states, dS, dA_log partials and (bf16, K = V = 128) the per-chunk operand
+    # blocks of the tcgen05 scans: 66048 bytes per (slot, head)
+    prep = (6 * 3 * 66048 + 255) // 256 * 256
+    assert kda.workspace_bytes(s) == 2 * sb + ((6 * 3 * 4 + 255) // 256) * 256 + prep
     v = _shape(B=1, T=300, num_seqs=4, cu_seqlens=0x1000)
     assert kda.num_chunk_slots(v) == 300 // 64 + 4
     f = _shape(K=64, V=64, dtype=kda.KDA_FP32, T=64, B=1)
     assert kda.workspace_dstates_offset(f) == 1 * 3 * 64 * 64 * 4
+    sf = 1 * 3 * 64 * 64 * 4
+    assert kda.workspace_bytes(f) == 2 * sf + 256  # no operand blocks off the tcgen05 path
 
 
 @pytest.mark.parametrize("kw,code", [
