@@ -5,11 +5,13 @@
 // B3 / K1 split of "bwd-kernelB-beginner-guide-full", Part 1, in one CTA), laid
 // out for tcgen05: every large contraction is taken TRANSPOSED, with the
 // channel (K or V = 128) dimension as the MMA's M, so that M = 128 and the
-// result lands in Tensor Memory with lane = channel.  Thread t of the CTA
-// owns channel c = t % 128 and chunk rows i in [32 g, 32 g + 32), g = t / 128;
-// it reads exactly its lane and its 32 columns of every accumulator, keeps
-// E = e^(gc - m) for its (i, c) in registers for the whole kernel, and does
-// the gate epilogue (the 64-row reverse cumulative sum) sequentially.
+// result lands in Tensor Memory with lane = channel.  The CTA has 512
+// threads (16 warps); thread t owns channel c = t % 128 and the 16-row block
+// I = t / 128 of the chunk (rows 16 I .. 16 I + 15), reads exactly its lane
+// and its 16 columns of every accumulator, keeps E = e^(gc - m_I) for its
+// (i, c) in registers for the whole kernel, and runs the gate epilogue (the
+// reverse cumulative sum over the chunk) over its block with the carry of
+// the later blocks.
 //
 // Products (D = A B^T, A: 128 x K, B: N x K; tiles in the padded core layout,
 // "K" / "MN" = how the stored tile is read):
@@ -37,11 +39,14 @@ constexpr uint32_t T128x128 = umma::ptile_bytes(128, 128);  // 36864
 constexpr uint32_t T64x64 = umma::ptile_bytes(64, 64);      // 9216
 constexpr uint32_t T128x64 = umma::ptile_bytes(128, 64);    // 18432
 
+constexpr int NT = 512;            // threads per CTA
+constexpr int NW = NT / 32;        // warps
+
 // ---- shared memory plan (bytes) ----------------------------------------------
 struct Smem {
   static constexpr size_t n_view = PrepView<bf16, D>::floats;
-  // extra floats: tbuf 768, dgT 2 x 128, red 8 x 64, dbeta 2 x 64, dA 8
-  static constexpr size_t n_extra = 768 + 256 + 512 + 128 + 8;
+  // extra floats: tbuf 768, dgT 4 x 128, red 16 x 64, red2 4 x 64, dbeta 64, dA 16
+  static constexpr size_t n_extra = 768 + 512 + 1024 + 256 + 64 + 16;
   static constexpr size_t sz_small = (((n_view + n_extra) * 4 + 64 + 1023) / 1024) * 1024;
   static constexpr size_t o_small = 0;
   // R_A: raw q, k, g (prep, later again) | Gf fp32, Gbf, Mqk, INV, INVb
@@ -76,15 +81,61 @@ struct Smem {
   static_assert(total <= 232448, "shared memory budget");
 };
 
-// prep in the (channel, 32-row segment) mapping; E kept in registers
+// Raw q, k, g rows of the chunk (row-major [64][128], zero past len) and beta.
+__device__ __forceinline__ void stage_raw(const KdaParams &p, int h, int64_t tok0, int len,
+                                          bf16 *Qr, bf16 *Kr, bf16 *Gr, float *beta) {
+  const int H = p.H;
+  for (int e = threadIdx.x; e < 3 * 64 * (D / 8); e += NT) {
+    const int t = e >> 10, r = (e >> 4) & 63, c8 = (e & 15) * 8;
+    const bf16 *src = reinterpret_cast<const bf16 *>(t == 0 ? p.q : (t == 1 ? p.k : p.g));
+    bf16 *dst = (t == 0 ? Qr : (t == 1 ? Kr : Gr)) + r * D + c8;
+    const bool ok = r < len;
+    cp_async16(dst, src + ((tok0 + (ok ? r : 0)) * H + h) * D + c8, ok);
+  }
+  if (beta != nullptr && threadIdx.x < CHUNK)
+    beta[threadIdx.x] = threadIdx.x < len
+                            ? __bfloat162float(reinterpret_cast<const bf16 *>(p.beta)[(tok0 + threadIdx.x) * H + h])
+                            : 0.f;
+}
+
+// TMEM address of this thread's lane (warp quarter) at column col
+__device__ __forceinline__ uint32_t tlane(uint32_t tbase, int col) {
+  return tbase + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16) + (uint32_t)col;
+}
+// this thread's 16 columns [col0 + 16 I, +16) of its lane, I = tid / 128
+__device__ __forceinline__ void tld16(uint32_t tbase, int col0, float (&v)[16]) {
+  umma::tmem_ld16(tlane(tbase, col0 + 16 * (int)(threadIdx.x >> 7)), v);
+  umma::tmem_ld_wait();
+}
+
+// Row sums over the warp's 32 lanes for the thread's 16 rows: lanes l and
+// l + 16 return the sum of row l (31 shuffles); v is consumed.
+__device__ __forceinline__ float rows16_sum(float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) v[r] += __shfl_xor_sync(0xffffffffu, v[r], 16);
+#pragma unroll
+  for (int s = 8; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < s; ++k) {
+      const float send = up ? v[k] : v[k + s];
+      const float keep = up ? v[k + s] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
+// prep in the (channel, 16-row block) mapping; E kept in registers
 __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, const bf16 *Kr,
-                        const bf16 *Gr, const PrepView<bf16, D> &sv, float (&E)[32], void *KDt,
+                        const bf16 *Gr, const PrepView<bf16, D> &sv, float (&E)[16], void *KDt,
                         void *KRt, void *QMt, void *KMt, void *KPt) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int c = tid & 127, g = tid >> 7;
+  const int c = tid & 127, I = tid >> 7;
   const float A = __expf(p.A_log[h]);
   // L2 norms, one warp per row
-  for (int i = warp; i < CHUNK; i += NWARPS) {
+  for (int i = warp; i < CHUNK; i += NW) {
     float sk = 0.f, sq = 0.f;
 #pragma unroll
     for (int cc = 2 * lane; cc < D; cc += 64) {
@@ -100,24 +151,22 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
       sv.rq[i] = rsqrtf(sq + p.eps);
     }
   }
-  // gate: per 16-row block sums local to the block (see kda_chunk.cuh)
-  float d[32];
-#pragma unroll
-  for (int b = 0; b < 2; ++b) {
+  // gate: running sum over the block, local to the block (see kda_chunk.cuh)
+  float d[16];
+  {
     float run = 0.f;
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      const int i = 32 * g + 16 * b + r;
+      const int i = 16 * I + r;
       const float gv = __bfloat162float(Gr[i * D + c]);
       run += i < len ? -A * softplus_f(gv) : 0.f;
-      d[16 * b + r] = run;
+      d[r] = run;
     }
-    const int I = 2 * g + b;
-    sv.part[I * D + c] = d[16 * b + 7];                 // rows 16I .. 16I+7
-    sv.m[I * D + c] = d[16 * b + 15] - d[16 * b + 7];   // rows 16I+8 .. 16I+15
-    const float ref = d[16 * b + 7];
+    sv.part[I * D + c] = d[7];         // rows 16I .. 16I+7
+    sv.m[I * D + c] = d[15] - d[7];    // rows 16I+8 .. 16I+15
+    const float ref = d[7];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) d[16 * b + r] -= ref;  // gc - m_I
+    for (int r = 0; r < 16; ++r) d[r] -= ref;  // gc - m_I
   }
   __syncthreads();
   if (tid < D) {
@@ -154,15 +203,13 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
   // tiles are stored transposed, [c][i] (128 x 64), one 16-byte store per
   // 8 rows: kd / kr are read MN-major (B, K = c), qm / km / kp K-major-by-
   // transposition by the pair-matrix mma.sync (ldmatrix.trans)
-  const float em0 = sv.em[(2 * g) * D + c], em1 = sv.em[(2 * g + 1) * D + c];
-  const float eg0 = sv.egm[(2 * g) * D + c], eg1 = sv.egm[(2 * g + 1) * D + c];
+  const float em = sv.em[I * D + c], eg = sv.egm[I * D + c];
 #pragma unroll
-  for (int q8 = 0; q8 < 4; ++q8) {
+  for (int q8 = 0; q8 < 2; ++q8) {
     float vkd[8], vkr[8], vqm[8], vkm[8], vkp[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      const int r = 8 * q8 + t, i = 32 * g + r;
-      const float em = (r < 16) ? em0 : em1, eg = (r < 16) ? eg0 : eg1;
+      const int r = 8 * q8 + t, i = 16 * I + r;
       const float e = __expf(d[r]), ei = __expf(-d[r]);
       E[r] = e;
       const float kh = __bfloat162float(Kr[i * D + c]) * sv.rk[i];
@@ -173,7 +220,7 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
       vkm[t] = kh * e;
       vkp[t] = kh * ei;
     }
-    const int i0 = 32 * g + 8 * q8;
+    const int i0 = 16 * I + 8 * q8;
     pstore8(KDt, c, i0, 64, vkd);
     pstore8(KRt, c, i0, 64, vkr);
     pstore8(QMt, c, i0, 64, vqm);
@@ -185,7 +232,7 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
 
 }  // namespace gtc
 
-__global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, const void *states) {
+__global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, const void *states) {
   using namespace gtc;
   using SM = Smem;
   extern __shared__ __align__(1024) char smem[];
@@ -193,7 +240,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
   const int h = blockIdx.y;
   const int H = p.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = tid & 127, g = tid >> 7;
+  const int c = tid & 127, I = tid >> 7;  // channel (TMEM lane) and 16-row block
   int s_, j_, len;
   int64_t tok0;
   if (!slot_owner(p, slot, s_, j_, tok0, len)) {
@@ -204,10 +251,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
   float *smf = reinterpret_cast<float *>(smem + SM::o_small);
   PrepView<bf16, D> sv = make_view<bf16, D>(smf);
   float *tbuf = smf + SM::n_view;
-  float *dgT = tbuf + 768;         // [2][128] (per row half)
-  float *red = dgT + 256;          // [8 warps][64]
-  float *dbs = red + 512;          // [2][64]
-  float *dAred = dbs + 128;        // [8]
+  float *dgT = tbuf + 768;         // [4][128] per-block partials of the gT gradient
+  float *red = dgT + 512;          // [16 warps][64]
+  float *red2 = red + 1024;        // [4][64]
+  float *dbs = red2 + 256;         // [64]
+  float *dAred = dbs + 64;         // [16]
   uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + SM::o_small + (SM::n_view + SM::n_extra) * 4);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 1);
   bf16 *Qr = reinterpret_cast<bf16 *>(smem + SM::o_A);
@@ -232,23 +280,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
   if (tid == 0) umma::mbar_init(mbar, 1);
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   // ---- stage: raw q, k, g (group 1); dS, dO into padded core tiles (group 2) ----
-  stage_chunk<bf16, D>(p, h, tok0, len, true, Qr, Kr, Gr, sv.beta);
+  stage_raw(p, h, tok0, len, Qr, Kr, Gr, sv.beta);
   cp_async_commit();
-  for (int e = tid; e < D * (D / 8); e += NTHREADS) {  // dS rows c, 8-column chunks
+  for (int e = tid; e < D * (D / 8); e += NT) {  // dS rows c, 8-column chunks
     const int r = e >> 4, c8 = (e & 15) * 8;
-    cp_async16(smem + SM::o_dS + pcore_off(r, c8, D), dSg + (size_t)r * D + c8, true);
+    cp_async16(dSt + pcore_off(r, c8, D), dSg + (size_t)r * D + c8, true);
   }
-  for (int e = tid; e < 64 * (D / 8); e += NTHREADS) {
+  for (int e = tid; e < 64 * (D / 8); e += NT) {
     const int i = e >> 4, c8 = (e & 15) * 8;
     const bool ok = i < len;
     cp_async16(dOt + pcore_off(i, c8, D),
                reinterpret_cast<const bf16 *>(p.dO) + ((tok0 + (ok ? i : 0)) * H + h) * D + c8, ok);
   }
   cp_async_commit();
-  if (tid < D) {
-    dgT[tid] = 0.f;
-    dgT[D + tid] = 0.f;
-  }
   umma::tc_fence_before();
   asm volatile("cp.async.wait_group 1;\n" ::);
   __syncthreads();
@@ -263,46 +307,45 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
   };
 
   // ---- prep ----
-  float E[32];
+  float E[16];
   prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, KRt, QMh, KMh, KPh);
   // ---- pair matrices (mma.sync): G (fp32, strictly lower) and scale * Mqk ----
-  {
-    const int I = warp & 3;
-    const bool is_q = warp >= 4;
-    const char *X = is_q ? QMh : KMh;
-    for (int J = 0; J < 4; ++J) {
-      float acc[2][4];
-      zero_acc(acc);
-      if (J <= I)
-        wg_core_t<2>(acc, X, 64, 0, 16 * I, KPh, 64, 0, 16 * J, D,
-                   J < I ? sv.F + pair_index(I, J) * D : nullptr);
-      for_acc(acc, [&](int r, int cc, float &v) {
-        const int i = 16 * I + r, jj = 16 * J + cc;
-        if (is_q)
-          *pel(Mqk, i, jj, 64) = __float2bfloat16_rn(jj <= i ? scale * v : 0.f);
-        else
-          Gf[i * 64 + jj] = jj < i ? v : 0.f;
-      });
-    }
+  for (int task = warp; task < 32; task += NW) {
+    const bool is_q = task >= 16;
+    const int Ib = (task >> 2) & 3, J = task & 3;
+    float acc[2][4];
+    zero_acc(acc);
+    if (J <= Ib)
+      wg_core_t<2>(acc, is_q ? QMh : KMh, 64, 0, 16 * Ib, KPh, 64, 0, 16 * J, D,
+                   J < Ib ? sv.F + pair_index(Ib, J) * D : nullptr);
+    for_acc(acc, [&](int r, int cc, float &v) {
+      const int i = 16 * Ib + r, jj = 16 * J + cc;
+      if (is_q)
+        *pel(Mqk, i, jj, 64) = __float2bfloat16_rn(jj <= i ? scale * v : 0.f);
+      else
+        Gf[i * 64 + jj] = jj < i ? v : 0.f;
+    });
   }
   __syncthreads();
   // S -> R_B (QMh/KMh/KPh are dead) while the inverse runs
-  for (int e = tid; e < D * (D / 8); e += NTHREADS) {
+  for (int e = tid; e < D * (D / 8); e += NT) {
     const int r = e >> 4, c8 = (e & 15) * 8;
     cp_async16(St + pcore_off(r, c8, D), Sg + (size_t)r * D + c8, true);
   }
   cp_async_commit();
-  for (int e = tid; e < 64 * 64; e += NTHREADS) {
-    const int i = e >> 6, jj = e & 63;
-    *pel(Gbf, i, jj, 64) = __float2bfloat16_rn(Gf[e]);
+  for (int e8 = tid; e8 < 64 * 8; e8 += NT) {
+    const int i = e8 >> 3, j0 = (e8 & 7) * 8;
+    pstore8(Gbf, i, j0, 64, Gf + i * 64 + j0);
   }
   __syncthreads();
   inverse_inplace(Gf, sv.beta, tbuf);
-  for (int e = tid; e < 64 * 64; e += NTHREADS) {
-    const int i = e >> 6, jj = e & 63;
-    const float x = Gf[e];
-    *pel(INV, i, jj, 64) = __float2bfloat16_rn(x);
-    *pel(INVb, i, jj, 64) = __float2bfloat16_rn(x * sv.beta[jj]);
+  for (int e8 = tid; e8 < 64 * 8; e8 += NT) {
+    const int i = e8 >> 3, j0 = (e8 & 7) * 8;
+    float xb[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) xb[u] = Gf[i * 64 + j0 + u] * sv.beta[j0 + u];
+    pstore8(INV, i, j0, 64, Gf + i * 64 + j0);
+    pstore8(INVb, i, j0, 64, xb);
   }
   cp_async_wait_all();
   umma::fence_async_smem();
@@ -314,22 +357,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
     gemm(tbase + 0, opmn(St, D), true, opmn(KDt, 64), true, 64, D / 16, false);
     umma::mma_commit(mbar);
   }
-  float vv[32];
+  float vv[16];
   {
     const bf16 *vg = reinterpret_cast<const bf16 *>(p.v);
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int i = 32 * g + r;
+    for (int r = 0; r < 16; ++r) {
+      const int i = 16 * I + r;
       vv[r] = i < len ? __bfloat162float(vg[((tok0 + i) * H + h) * D + c]) : 0.f;
     }
   }
-  const bool ok1 = mma_wait();
-  float acc[32];
-  tld32(tbase, 0, acc);
+  mma_wait();
+  float acc[16];
+  tld16(tbase, 0, acc);
 #pragma unroll
-  for (int r = 0; r < 32; ++r) acc[r] = vv[r] - acc[r];
+  for (int r = 0; r < 16; ++r) acc[r] = vv[r] - acc[r];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) pstore8(XrT, c, 32 * g + 8 * q, 64, acc + 8 * q);  // Xr^T[d][i]
+  for (int q = 0; q < 2; ++q) pstore8(XrT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // Xr^T[d][i]
   umma::fence_async_smem();
   umma::tc_fence_before();
   __syncthreads();
@@ -341,9 +384,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
     umma::mma_commit(mbar);
   }
   mma_wait();
-  tld32(tbase, 64, acc);
+  tld16(tbase, 64, acc);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) pstore8(Ut, c, 32 * g + 8 * q, 64, acc + 8 * q);  // U^T[d][i]
+  for (int q = 0; q < 2; ++q) pstore8(Ut, c, 16 * I + 8 * q, 64, acc + 8 * q);  // U^T[d][i]
   umma::fence_async_smem();
   umma::tc_fence_before();
   __syncthreads();
@@ -357,22 +400,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
     umma::mma_commit(mbar);
   }
   {
-    // p_c = e^gT_c sum_d dS[c][d] S[c][d]; thread (c, g) takes d in [64 g, 64 g + 64)
+    // p_c = e^gT_c sum_d dS[c][d] S[c][d]; thread (c, I) takes d in [32 I, 32 I + 32)
     float pp = 0.f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
       float a8[8], b8[8];
-      pload8(dSt, c, 64 * g + 8 * q, D, a8);
-      pload8(St, c, 64 * g + 8 * q, D, b8);
+      pload8(dSt, c, 32 * I + 8 * q, D, a8);
+      pload8(St, c, 32 * I + 8 * q, D, b8);
 #pragma unroll
       for (int t = 0; t < 8; ++t) pp = fmaf(a8[t], b8[t], pp);
     }
-    dgT[g * D + c] = __expf(sv.gT[c]) * pp;
+    dgT[I * D + c] = __expf(sv.gT[c]) * pp;
   }
   mma_wait();
-  tld32(tbase, 128, acc);
+  tld16(tbase, 128, acc);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) pstore8(dUT, c, 32 * g + 8 * q, 64, acc + 8 * q);  // dU^T[d][i]
+  for (int q = 0; q < 2; ++q) pstore8(dUT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // dU^T[d][i]
   umma::fence_async_smem();
   umma::tc_fence_before();
   __syncthreads();
@@ -384,32 +427,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
     umma::mma_commit(mbar);
   }
   mma_wait();
-  tld32(tbase, 0, acc);
+  tld16(tbase, 0, acc);
   {
     bf16 *dvg = reinterpret_cast<bf16 *>(p.dv);
-    float xr[32];
+    float xr[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) pload8(XrT, c, 32 * g + 8 * q, 64, xr + 8 * q);
-    float pr[32];
+    for (int q = 0; q < 2; ++q) pload8(XrT, c, 16 * I + 8 * q, 64, xr + 8 * q);
+    float pr[16];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int i = 32 * g + r;
+    for (int r = 0; r < 16; ++r) {
+      const int i = 16 * I + r;
       *pel(dvc, i, c, D) = __float2bfloat16_rn(acc[r]);
       if (i < len) dvg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn(sv.beta[i] * acc[r]);
       pr[r] = acc[r] * xr[r];
     }
-    // sums over this warp's 32 channels; lane l gets row 32 g + l
-    red[warp * 64 + 32 * g + lane] = warp_transpose_sum(pr);
+    // sums over this warp's 32 channels; lane l < 16 holds row 16 I + l
+    const float t = rows16_sum(pr);
+    if (lane < 16) red[warp * 16 + lane] = t;
   }
   umma::fence_async_smem();
   umma::tc_fence_before();
   __syncthreads();
-  if (tid < 64) {  // dbeta1_i: warps 0..3 (g = 0) hold rows 0..31, warps 4..7 rows 32..63
-    const int i = tid, w0 = (i >> 5) * 4;
-    dbs[i] = red[(w0 + 0) * 64 + i] + red[(w0 + 1) * 64 + i] + red[(w0 + 2) * 64 + i] +
-             red[(w0 + 3) * 64 + i];
+  if (tid < 64) {  // dbeta1_i: block i / 16 lives in warps 4 (i / 16) .. + 3
+    const int i = tid, w0 = (i >> 4) * 4, r = i & 15;
+    dbs[i] = red[(w0 + 0) * 16 + r] + red[(w0 + 1) * 16 + r] + red[(w0 + 2) * 16 + r] +
+             red[(w0 + 3) * 16 + r];
   }
-  __syncthreads();  // red is rewritten by the P6 epilogue
 
   // ---- P6: [dvcorr; dO] U^T  and  P8: S [dvcorr; dO]^T ----
   if (tid == 0) {
@@ -421,35 +464,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
   mma_wait();
   {
     // lanes 0..63: -dAkk rows (dvcorr U^T), lanes 64..127: dMqk / scale rows
-    float v32[32];
-    tld32(tbase, 64, v32);  // columns j in [32 g, 32 g + 32)
+    float v16[16];
+    tld16(tbase, 64, v16);  // columns j in [16 I, 16 I + 16)
     if (c < 64) {
       const int i = c;
       float db2 = 0.f;
       float o8[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-          const int jj = 32 * g + 8 * q + t;
-          const float dak = jj < i ? -v32[8 * q + t] : 0.f;
+          const int jj = 16 * I + 8 * q + t;
+          const float dak = jj < i ? -v16[8 * q + t] : 0.f;
           db2 = fmaf(dak, pget(Gbf, i, jj, 64), db2);
           o8[t] = sv.beta[i] * dak;
         }
-        pstore8(dAt, i, 32 * g + 8 * q, 64, o8);
+        pstore8(dAt, i, 16 * I + 8 * q, 64, o8);
       }
-      red[(g * 2) * 64 + i] = db2;
+      red2[I * 64 + i] = db2;
     } else {
       const int i = c - 64;
       float o8[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-          const int jj = 32 * g + 8 * q + t;
-          o8[t] = jj <= i ? scale * v32[8 * q + t] : 0.f;
+          const int jj = 16 * I + 8 * q + t;
+          o8[t] = jj <= i ? scale * v16[8 * q + t] : 0.f;
         }
-        pstore8(dMqk, i, 32 * g + 8 * q, 64, o8);
+        pstore8(dMqk, i, 16 * I + 8 * q, 64, o8);
       }
     }
   }
@@ -457,22 +500,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
   umma::tc_fence_before();
   __syncthreads();
   if (tid < 64 && tid < len) {
-    const float db = dbs[tid] + red[0 * 64 + tid] + red[2 * 64 + tid];
+    const float db = dbs[tid] + red2[tid] + red2[64 + tid] + red2[128 + tid] + red2[192 + tid];
     reinterpret_cast<bf16 *>(p.dbeta)[(tok0 + tid) * H + h] = __float2bfloat16_rn(db);
   }
   // raw q, k, g again (L2), for the hi / lo operands and the epilogues
-  stage_chunk<bf16, D>(p, h, tok0, len, true, Qr, Kr, Gr, dbs);
+  stage_raw(p, h, tok0, len, Qr, Kr, Gr, nullptr);
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();
   // ---- intra-chunk operands, hi + lo (see kda_grads.cu) ----
-  float qh[32], kh[32];
+  float qh[16], kh[16];
 #pragma unroll
-  for (int q8 = 0; q8 < 4; ++q8) {
+  for (int q8 = 0; q8 < 2; ++q8) {
     float hv[3][8], lv[3][8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      const int r = 8 * q8 + t, i = 32 * g + r;
+      const int r = 8 * q8 + t, i = 16 * I + r;
       qh[r] = __bfloat162float(Qr[i * D + c]) * sv.rq[i];
       kh[r] = __bfloat162float(Kr[i * D + c]) * sv.rk[i];
       const float x[3] = {qh[r] * E[r], kh[r] * E[r], __fdividef(kh[r], E[r])};
@@ -482,7 +525,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
         lv[u][t] = x[u] - hv[u][t];
       }
     }
-    const int i0 = 32 * g + 8 * q8;
+    const int i0 = 16 * I + 8 * q8;
     char *hi[3] = {QMh, KMh, KPh};
     char *lo[3] = {QMl, KMl, KPl};
 #pragma unroll
@@ -495,17 +538,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
   umma::tc_fence_before();
   __syncthreads();
 
-  // per-thread block factors: Fq[b][J] = F_{I,J} (I = 2 g + b, J <= I) for the
-  // query-side sums, Fk[b][I] = F_{I,J} (J = 2 g + b, I >= J) for the key side
-  float Fq[2][4], Fk[2][4];
+  // per-thread block factors: Fq[J] = F_{I,J} (J <= I) for the query-side
+  // sums, Fk[X] = F_{X,I} (X >= I) for the key side
+  float Fq[4], Fk[4];
 #pragma unroll
-  for (int b = 0; b < 2; ++b)
-#pragma unroll
-    for (int X = 0; X < 4; ++X) {
-      const int Ib = 2 * g + b;
-      Fq[b][X] = X < Ib ? sv.F[pair_index(Ib, X) * D + c] : (X == Ib ? 1.f : 0.f);
-      Fk[b][X] = X > Ib ? sv.F[pair_index(X, Ib) * D + c] : (X == Ib ? 1.f : 0.f);
-    }
+  for (int X = 0; X < 4; ++X) {
+    Fq[X] = X < I ? sv.F[pair_index(I, X) * D + c] : (X == I ? 1.f : 0.f);
+    Fk[X] = X > I ? sv.F[pair_index(X, I) * D + c] : (X == I ? 1.f : 0.f);
+  }
+  const float emI = sv.em[I * D + c];
   // ---- P9a: dq^ intra, one accumulator per key block J ----
   if (tid == 0) {
     umma::tc_fence_after();
@@ -516,39 +557,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
     umma::mma_commit(mbar);
   }
   mma_wait();
-  float dgc[32];
+  float dgc[16];
   {
-    float bq[32];
-    tld32(tbase, 320, bq);  // dO S^T (rows 64..127 of the stacked operand)
-    float in[32];
+    float bq[16];
+    tld16(tbase, 320, bq);  // dO S^T (rows 64..127 of the stacked operand)
+    float in[16];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) in[r] = 0.f;
+    for (int r = 0; r < 16; ++r) in[r] = 0.f;
 #pragma unroll
     for (int J = 0; J < 4; ++J) {
-      float a32[32];
-      tld32(tbase, 64 * J, a32);
+      float a16[16];
+      tld16(tbase, 64 * J, a16);
 #pragma unroll
-      for (int r = 0; r < 32; ++r) in[r] = fmaf(Fq[r >> 4][J], a32[r], in[r]);
+      for (int r = 0; r < 16; ++r) in[r] = fmaf(Fq[J], a16[r], in[r]);
     }
-    float dq[32], pr[32];
-    const float emq0 = sv.em[(2 * g) * D + c], emq1 = sv.em[(2 * g + 1) * D + c];
+    float dq[16], pr[16];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const float gam = E[r] * (r < 16 ? emq0 : emq1);
-      dq[r] = scale * gam * bq[r] + E[r] * in[r];
+    for (int r = 0; r < 16; ++r) {
+      dq[r] = scale * E[r] * emI * bq[r] + E[r] * in[r];
       dgc[r] = dq[r] * qh[r];
       pr[r] = dgc[r];
     }
-    red[warp * 64 + 32 * g + lane] = warp_transpose_sum(pr);
+    const float t = rows16_sum(pr);
+    if (lane < 16) red[warp * 16 + lane] = t;
     umma::tc_fence_before();
     __syncthreads();
     bf16 *dqg = reinterpret_cast<bf16 *>(p.dq);
+    const int w0 = 4 * I;
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int i = 32 * g + r;
-      const int w0 = 4 * g;
-      const float rd = red[(w0 + 0) * 64 + i] + red[(w0 + 1) * 64 + i] +
-                       red[(w0 + 2) * 64 + i] + red[(w0 + 3) * 64 + i];
+    for (int r = 0; r < 16; ++r) {
+      const int i = 16 * I + r;
+      const float rd = red[(w0 + 0) * 16 + r] + red[(w0 + 1) * 16 + r] +
+                       red[(w0 + 2) * 16 + r] + red[(w0 + 3) * 16 + r];
       if (i < len)
         dqg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn((dq[r] - qh[r] * rd) * sv.rq[i]);
     }
@@ -565,79 +605,78 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
     umma::mma_commit(mbar);
   }
   mma_wait();
-  float dkt[32];
+  float dkt[16];
   {
-    float bk[32];
-    tld32(tbase, 256, bk);  // dvcorr S^T
+    float bk[16];
+    tld16(tbase, 256, bk);  // dvcorr S^T
 #pragma unroll
-    for (int r = 0; r < 32; ++r) dkt[r] = 0.f;
+    for (int r = 0; r < 16; ++r) dkt[r] = 0.f;
 #pragma unroll
     for (int J = 0; J < 4; ++J) {
-      float a32[32];
-      tld32(tbase, 64 * J, a32);
+      float a16[16];
+      tld16(tbase, 64 * J, a16);
 #pragma unroll
-      for (int r = 0; r < 32; ++r) dkt[r] = fmaf(Fq[r >> 4][J], a32[r], dkt[r]);
+      for (int r = 0; r < 16; ++r) dkt[r] = fmaf(Fq[J], a16[r], dkt[r]);
     }
-    const float emk0 = sv.em[(2 * g) * D + c], emk1 = sv.em[(2 * g + 1) * D + c];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int i = 32 * g + r;
-      const float gam = E[r] * (r < 16 ? emk0 : emk1);
-      dkt[r] = -sv.beta[i] * gam * bk[r] + E[r] * dkt[r];
+    for (int r = 0; r < 16; ++r) {
+      const int i = 16 * I + r;
+      dkt[r] = -sv.beta[i] * E[r] * emI * bk[r] + E[r] * dkt[r];
     }
   }
   umma::tc_fence_before();
   __syncthreads();
 
-  // ---- P9c: dki' = E^-1 sum_{I >= J} (Mqk-side + A-side) with qm / km, per query block I ----
+  // ---- P9c: dki' = E^-1 sum_{X >= J} (Mqk-side + A-side) with qm / km, per query block X ----
   if (tid == 0) {
     umma::tc_fence_after();
-    for (int I = 0; I < 4; ++I) {
-      const uint32_t d = tbase + 64 * I;
-      gemm(d, opk(QMh, 64, 16 * I), false, opmn(dMqk, 64, 16 * I), true, 64, 1, false);
-      gemm(d, opk(QMl, 64, 16 * I), false, opmn(dMqk, 64, 16 * I), true, 64, 1, true);
-      gemm(d, opk(KMh, 64, 16 * I), false, opmn(dAt, 64, 16 * I), true, 64, 1, true);
-      gemm(d, opk(KMl, 64, 16 * I), false, opmn(dAt, 64, 16 * I), true, 64, 1, true);
+    for (int X = 0; X < 4; ++X) {
+      const uint32_t d = tbase + 64 * X;
+      gemm(d, opk(QMh, 64, 16 * X), false, opmn(dMqk, 64, 16 * X), true, 64, 1, false);
+      gemm(d, opk(QMl, 64, 16 * X), false, opmn(dMqk, 64, 16 * X), true, 64, 1, true);
+      gemm(d, opk(KMh, 64, 16 * X), false, opmn(dAt, 64, 16 * X), true, 64, 1, true);
+      gemm(d, opk(KMl, 64, 16 * X), false, opmn(dAt, 64, 16 * X), true, 64, 1, true);
     }
     umma::mma_commit(mbar);
   }
   mma_wait();
   {
-    float dki[32];
+    float dki[16];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) dki[r] = 0.f;
+    for (int r = 0; r < 16; ++r) dki[r] = 0.f;
 #pragma unroll
-    for (int I = 0; I < 4; ++I) {
-      float a32[32];
-      tld32(tbase, 64 * I, a32);
+    for (int X = 0; X < 4; ++X) {
+      float a16[16];
+      tld16(tbase, 64 * X, a16);
 #pragma unroll
-      for (int r = 0; r < 32; ++r) dki[r] = fmaf(Fk[r >> 4][I], a32[r], dki[r]);
+      for (int r = 0; r < 16; ++r) dki[r] = fmaf(Fk[X], a16[r], dki[r]);
     }
-    float dkr[32];
-    tld32(tbase, 448, dkr);
-    float dk[32], pr[32], colp = 0.f;
-    const float egk0 = sv.egm[(2 * g) * D + c], egk1 = sv.egm[(2 * g + 1) * D + c];
+    float dkr[16];
+    tld16(tbase, 448, dkr);
+    float dk[16], pr[16], colp = 0.f;
+    const float egI = sv.egm[I * D + c];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
+    for (int r = 0; r < 16; ++r) {
       const float rE = __fdividef(1.f, E[r]);
       const float dkip = dki[r] * rE;
-      const float dkrp = dkr[r] * (r < 16 ? egk0 : egk1) * rE;
+      const float dkrp = dkr[r] * egI * rE;
       dk[r] = dkt[r] + dkip + dkrp;
       const float dks = dkt[r] - dkip - dkrp;
       dgc[r] = fmaf(dks, kh[r], dgc[r]);
       colp = fmaf(dkrp, kh[r], colp);
       pr[r] = dk[r] * kh[r];
     }
-    red[warp * 64 + 32 * g + lane] = warp_transpose_sum(pr);
-    dgT[g * D + c] += colp;
+    const float t = rows16_sum(pr);
+    if (lane < 16) red[warp * 16 + lane] = t;
+    dgT[I * D + c] += colp;
     __syncthreads();
     bf16 *dkg = reinterpret_cast<bf16 *>(p.dk);
+    const int w0 = 4 * I;
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int i = 32 * g + r;
-      const int w0 = 4 * g;
-      const float rd = red[(w0 + 0) * 64 + i] + red[(w0 + 1) * 64 + i] +
-                       red[(w0 + 2) * 64 + i] + red[(w0 + 3) * 64 + i];
+    for (int r = 0; r < 16; ++r) {
+      const int i = 16 * I + r;
+      const float rd = red[(w0 + 0) * 16 + r] + red[(w0 + 1) * 16 + r] +
+                       red[(w0 + 2) * 16 + r] + red[(w0 + 3) * 16 + r];
       if (i < len)
         dkg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn((dk[r] - kh[r] * rd) * sv.rk[i]);
     }
@@ -647,17 +686,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
   {
     float tot = 0.f;
 #pragma unroll
-    for (int r = 0; r < 32; ++r) tot += dgc[r];
+    for (int r = 0; r < 16; ++r) tot += dgc[r];
     __syncthreads();
-    red[g * 128 + c] = tot;  // (red is free again) row-half totals per channel
+    red[I * 128 + c] = tot;  // (red is free again) block totals per channel
     __syncthreads();
-    float run = dgT[c] + dgT[D + c] + (g == 0 ? red[128 + c] : 0.f);
+    float run = dgT[c] + dgT[D + c] + dgT[2 * D + c] + dgT[3 * D + c];
+#pragma unroll
+    for (int X = 1; X < 4; ++X)
+      if (X > I) run += red[X * 128 + c];
     const float A = __expf(p.A_log[h]);
     float dA = 0.f;
     bf16 *dgg = reinterpret_cast<bf16 *>(p.dg);
 #pragma unroll
-    for (int r = 31; r >= 0; --r) {
-      const int i = 32 * g + r;
+    for (int r = 15; r >= 0; --r) {
+      const int i = 16 * I + r;
       run += dgc[r];
       if (i < len) {
         const float gv = __bfloat162float(Gr[i * D + c]);
@@ -672,11 +714,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_tc_kernel(KdaParams p, 
     __syncthreads();
     if (tid == 0) {
       float t = 0.f;
-      for (int w = 0; w < NWARPS; ++w) t += dAred[w];
+      for (int w = 0; w < NW; ++w) t += dAred[w];
       p.dA_part[slot * H + h] = t;
     }
   }
-  (void)ok1;
   if (warp == 0) {
     umma::tc_fence_after();
     umma::tmem_dealloc(tbase, 512);
@@ -689,7 +730,7 @@ cudaError_t grads_tc_launch(const KdaParams &p, const void *states, cudaStream_t
                                        (int)gtc::Smem::total);
   if (e != cudaSuccess) return e;
   if (p.nslots > 0) {
-    kfn<<<dim3((unsigned)p.nslots, p.H), NTHREADS, gtc::Smem::total, st>>>(p, states);
+    kfn<<<dim3((unsigned)p.nslots, p.H), gtc::NT, gtc::Smem::total, st>>>(p, states);
     e = cudaGetLastError();
   }
   return e;
