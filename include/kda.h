@@ -90,16 +90,18 @@ int64_t kda_num_chunk_slots(const kda_shape *shape);
 
 /* Bytes of workspace kda_bwd needs: the per-chunk states (dtype of the
  * shape, [slots, H, K, V]) unless the caller passes them, the per-chunk
- * state gradients dS (same size) and per-chunk dA_log partials.  Returns 0
- * on a bad shape. */
+ * state gradients dS (same size), per-chunk dA_log partials and, for bf16
+ * with K = V = 128, the per-chunk operand blocks of the tensor-core scans
+ * (66048 bytes per slot and head).  Returns 0 on a bad shape. */
 size_t kda_workspace_bytes(const kda_shape *shape);
-
 /* Byte offset inside the workspace of the per-chunk state gradients
- * dS_{n+1} (the adjoint of the state at the END of chunk n), layout
- * [slots, H, K, V] in the shape's dtype.  Exposed so that tests can check
- * the reverse scan on its own. */
+ * dS_{n+1} (the adjoint of the state at the END of chunk n), [slots, H]
+ * tiles of K x V in the shape's dtype.  For bf16 with K = V = 128 each tile
+ * is in packed core-matrix order -- element (k, v) at element offset
+ * ((k / 8) * (V / 8) + v / 8) * 64 + (k % 8) * 8 + v % 8 -- and so are the
+ * states kda_bwd recomputes at the start of the workspace; otherwise tiles
+ * are row-major.  Exposed so that tests can check the scans on their own. */
 size_t kda_workspace_dstates_offset(const kda_shape *shape);
-
 /* Forward chunk-state recompute (the "all_states" operand of kernel B2 in
  * "bwd-kernelB-beginner-guide-full", Part 2, B2 optimisation 4).
  *   states : OUT [slots, H, K, V], dtype of the shape: S at the start of

@@ -230,6 +230,9 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
   p.role_base = states ? 1 : 0;
   cudaError_t e;
   if (tc_state_path(shape) && !legacy_scan()) {
+    // the tcgen05 scans store their tiles in packed core-matrix order
+    p.states_packed = states ? 0 : 1;
+    p.dstates_packed = 1;
     void *prep = w + 2 * sb + round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
     e = kda::prep_tc_launch(p, prep, cs);
     if (e == cudaSuccess) e = kda::scan_tc_launch(p, prep, nroles, cs);

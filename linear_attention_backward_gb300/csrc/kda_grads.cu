@@ -538,7 +538,8 @@ static cudaError_t launch_grads(const KdaParams &p, const void *states, cudaStre
                                 void *after) {
   using SM = GradSmem<E, D>;
   cudaError_t e;
-  if (sizeof(E) == 2 && D == 128 && use_tc_kernel()) {
+  // packed state tiles (tcgen05 scans) are read by the tcgen05 kernel only
+  if (sizeof(E) == 2 && D == 128 && (use_tc_kernel() || p.states_packed || p.dstates_packed)) {
     e = grads_tc_launch(p, states, st);
     if (e != cudaSuccess) return e;
   } else {

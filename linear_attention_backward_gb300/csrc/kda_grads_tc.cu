@@ -284,7 +284,9 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   cp_async_commit();
   for (int e = tid; e < D * (D / 8); e += NT) {  // dS rows c, 8-column chunks
     const int r = e >> 4, c8 = (e & 15) * 8;
-    cp_async16(dSt + pcore_off(r, c8, D), dSg + (size_t)r * D + c8, true);
+    cp_async16(dSt + pcore_off(r, c8, D),
+               p.dstates_packed ? dSg + umma::core_off(r, c8, D) / 2 : dSg + (size_t)r * D + c8,
+               true);
   }
   for (int e = tid; e < 64 * (D / 8); e += NT) {
     const int i = e >> 4, c8 = (e & 15) * 8;
@@ -330,7 +332,8 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   // S -> R_B (QMh/KMh/KPh are dead) while the inverse runs
   for (int e = tid; e < D * (D / 8); e += NT) {
     const int r = e >> 4, c8 = (e & 15) * 8;
-    cp_async16(St + pcore_off(r, c8, D), Sg + (size_t)r * D + c8, true);
+    cp_async16(St + pcore_off(r, c8, D),
+               p.states_packed ? Sg + umma::core_off(r, c8, D) / 2 : Sg + (size_t)r * D + c8, true);
   }
   cp_async_commit();
   for (int e8 = tid; e8 < 64 * 8; e8 += NT) {

@@ -25,6 +25,10 @@ struct KdaParams {
   float *dA_log;              // [H]
   int nb;                     // V bands of the scan kernels
   int role_base;              // first scan role of a launch (0 forward, 1 reverse)
+  // Layout of each K x V tile of states / dstates: 0 = row-major, 1 = packed
+  // core-matrix order (8 x 8 bf16 cores of 128 bytes, cores along V first),
+  // the shared-memory operand layout the tcgen05 scans store with one bulk copy.
+  int states_packed, dstates_packed;
 };
 
 // Per-chunk operands of the state scans (bf16, K = V = 128), one block of
@@ -34,7 +38,7 @@ struct KdaParams {
 // bytes, cores along the columns first):
 //   gT   fp32 [128]          total log-decay of the chunk per channel
 //   Wt   [c][i]  W^T,  W  = (I + Akk)^-1 diag(beta) kd
-//   KR   [i][c]  kr  = k^ e^(gT - gc)
+//   KRt  [c][i]  kr^T, kr = k^ e^(gT - gc)
 //   U0t  [v][i]  U0^T, U0 = (I + Akk)^-1 diag(beta) v
 //   QEt  [c][i]  QE^T, QE = scale (qd - Mqk W)
 constexpr size_t kPrepGT = 0;

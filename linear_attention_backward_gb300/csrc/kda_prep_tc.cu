@@ -5,6 +5,7 @@
 // conventions as in kda_chunk.cuh):
 //   W  = (I + Akk)^-1 diag(beta) kd       U0 = (I + Akk)^-1 diag(beta) v
 //   QE = scale (qd - Mqk W)               kr = k^ e^(gT - gc),  gT
+// (all four 64 x 128 tiles stored transposed, channel-major, see kda_params.h)
 // With these the two serial recurrences of the backward ("all_states" of
 // kernel B2 and Kernel A, "bwd-kernelB-beginner-guide-full", Part 2, and the
 // A/B table of "bwd-ncu-and-optimization-playbook") need nothing else per
@@ -203,25 +204,32 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, c
     reinterpret_cast<float *>(unit + kPrepGT)[e] = tot;
   }
   __syncthreads();
-  // ---- decay-scaled tiles; kr goes straight to HBM ----
+  // ---- decay-scaled tiles; kr^T goes straight to HBM ----
   {
     const float eg0 = sv.egm[I * D + c], eg1 = sv.egm[I * D + c + 1];
     char *kr_out = unit + kPrepKR;
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const int i = 16 * I + r;
-      const float rk = sv.rk[i], rq = sv.rq[i];
-      const float2 kv = bf2_to_f2(kraw[r]), qv = bf2_to_f2(qraw[r]);
-      const float kh0 = kv.x * rk, kh1 = kv.y * rk, qh0 = qv.x * rq, qh1 = qv.y * rq;
-      const float d0 = g0[r] - g0[7], d1 = g1[r] - g1[7];
-      const float e0 = __expf(d0), e1 = __expf(d1);
-      const float ei0 = __expf(-d0), ei1 = __expf(-d1);
-      const uint32_t off = pcore_off(i, c, D);
-      *reinterpret_cast<uint32_t *>(QM + off) = f2_to_bf2(qh0 * e0, qh1 * e1);
-      *reinterpret_cast<uint32_t *>(KM + off) = f2_to_bf2(kh0 * e0, kh1 * e1);
-      *reinterpret_cast<uint32_t *>(KP + off) = f2_to_bf2(kh0 * ei0, kh1 * ei1);
-      *reinterpret_cast<uint32_t *>(kr_out + umma::core_off(i, c, D)) =
-          f2_to_bf2((kh0 * ei0) * eg0, (kh1 * ei1) * eg1);
+    for (int h8 = 0; h8 < 2; ++h8) {
+      float kr0[8], kr1[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int r = 8 * h8 + t, i = 16 * I + r;
+        const float rk = sv.rk[i], rq = sv.rq[i];
+        const float2 kv = bf2_to_f2(kraw[r]), qv = bf2_to_f2(qraw[r]);
+        const float kh0 = kv.x * rk, kh1 = kv.y * rk, qh0 = qv.x * rq, qh1 = qv.y * rq;
+        const float d0 = g0[r] - g0[7], d1 = g1[r] - g1[7];
+        const float e0 = __expf(d0), e1 = __expf(d1);
+        const float ei0 = __expf(-d0), ei1 = __expf(-d1);
+        const uint32_t off = pcore_off(i, c, D);
+        *reinterpret_cast<uint32_t *>(QM + off) = f2_to_bf2(qh0 * e0, qh1 * e1);
+        *reinterpret_cast<uint32_t *>(KM + off) = f2_to_bf2(kh0 * e0, kh1 * e1);
+        *reinterpret_cast<uint32_t *>(KP + off) = f2_to_bf2(kh0 * ei0, kh1 * ei1);
+        kr0[t] = (kh0 * ei0) * eg0;
+        kr1[t] = (kh1 * ei1) * eg1;
+      }
+      // kr^T [c][i]: rows 16 I + 8 h8 .. + 7 of channels c and c + 1, 16-byte rows
+      st16_bf(kr_out + umma::core_off(c, 16 * I + 8 * h8, 64), kr0);
+      st16_bf(kr_out + umma::core_off(c + 1, 16 * I + 8 * h8, 64), kr1);
     }
   }
   __syncthreads();

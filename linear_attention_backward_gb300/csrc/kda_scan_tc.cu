@@ -19,10 +19,13 @@
 // The fp32 running state X stays in registers (thread = TMEM lane c and one
 // half of the V columns); its bf16 copy in shared memory is MMA1's operand
 // and is what goes to HBM as the chunk's state (the grads kernel reads the
-// same rounding the scan used).  The chunk's operand block (gT, W^T, kr,
-// U0^T or QE^T; 48.5 KB) arrives by bulk TMA copies on an mbarrier, issued
-// as soon as MMA2 of the previous chunk has consumed the buffer, with an L2
-// prefetch two chunks ahead; the reverse role's dO rows come by cp.async.
+// same rounding the scan used), stored from the tile with one bulk copy per
+// chunk: states and dstates written here are in packed core-matrix order.  The chunk's
+// operands (gT, W^T, kr^T, U0^T or QE^T; 48.5 KB) arrive by bulk TMA copies
+// into three regions with one mbarrier each; a region is refilled with the
+// next chunk's data as soon as its consumer (MMA1, the U epilogue or MMA2)
+// is done, behind an L2 prefetch two chunks ahead.  The reverse role's dO
+// rows come by cp.async with MMA2's region.
 #include "kda_chunk.cuh"
 #include "kda_tc_tiles.cuh"
 
@@ -61,9 +64,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   if (!seq_bounds(p, s, tok_seq, L, slot0)) return;
   const int nck = (L + CHUNK - 1) / CHUNK;
   char *Xs = smem + SM::o_X, *IN = smem + SM::o_IN, *dOs = smem + SM::o_dO, *Us = smem + SM::o_U;
-  uint64_t *bar_in = reinterpret_cast<uint64_t *>(smem + SM::o_bar);
-  uint64_t *bar_mma = bar_in + 1;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_in + 2);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::o_bar);  // 3 operand slots + MMA
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 4);
 
   const int ch = tid & 127, hf = tid >> 7;  // TMEM lane; half of the columns
   const size_t DD = (size_t)D * D;
@@ -84,8 +86,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   }
   if (warp == 0) umma::tmem_alloc(tslot, 256);
   if (tid == 0) {
-    umma::mbar_init(bar_in, 1);
-    umma::mbar_init(bar_mma, 1);
+    for (int k = 0; k < 4; ++k) umma::mbar_init(bars + k, 1);
   }
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   __syncthreads();
@@ -95,19 +96,37 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
     return prep + ((size_t)(slot0 + j) * H + h) * kPrepUnitBytes;
   };
   const bf16 *dOg = reinterpret_cast<const bf16 *>(p.dO);
-  auto issue_loads = [&](int it) {
-    const int j = chunk_of(it);
-    const char *u = unit_of(j);
+  // Operand regions of IN and the barrier each one completes on:
+  //   forward: slot 0 = gT | W^T (MMA1), slot 1 = U0^T (epilogue 1), slot 2 = kr^T (MMA2)
+  //   reverse: slot 0 = kr^T (MMA1), slot 1 = gT | W^T, QE^T (+ dO rows) (MMA2)
+  // A slot is refilled with the next chunk's data as soon as its consumer is done.
+  auto load_slot = [&](int sl, int it) {
+    const char *u = unit_of(chunk_of(it));
     if (tid == 0) {
-      umma::mbar_expect_tx(bar_in, fwd ? kInFwd : kInRevA + 16384u);
       if (fwd) {
-        umma::bulk_g2s(IN, u, kInFwd, bar_in);
+        if (sl == 0) {
+          umma::mbar_expect_tx(bars + 0, kPrepKR);
+          umma::bulk_g2s(IN, u, kPrepKR, bars + 0);
+        } else if (sl == 1) {
+          umma::mbar_expect_tx(bars + 1, 16384u);
+          umma::bulk_g2s(IN + kPrepU0, u + kPrepU0, 16384u, bars + 1);
+        } else {
+          umma::mbar_expect_tx(bars + 2, 16384u);
+          umma::bulk_g2s(IN + kPrepKR, u + kPrepKR, 16384u, bars + 2);
+        }
       } else {
-        umma::bulk_g2s(IN, u, kInRevA, bar_in);
-        umma::bulk_g2s(IN + kQEHere, u + kPrepQE, 16384u, bar_in);
+        if (sl == 0) {
+          umma::mbar_expect_tx(bars + 0, 16384u);
+          umma::bulk_g2s(IN + kPrepKR, u + kPrepKR, 16384u, bars + 0);
+        } else {
+          umma::mbar_expect_tx(bars + 1, kPrepKR + 16384u);
+          umma::bulk_g2s(IN, u, kPrepKR, bars + 1);
+          umma::bulk_g2s(IN + kQEHere, u + kPrepQE, 16384u, bars + 1);
+        }
       }
     }
-    if (!fwd) {  // dO rows -> packed core tile [i][v]
+    if (!fwd && sl == 1) {  // dO rows -> packed core tile [i][v]
+      const int j = chunk_of(it);
       const int64_t t0 = tok_seq + (int64_t)j * CHUNK;
       const int ln = min(CHUNK, L - j * CHUNK);
       for (int e = tid; e < 64 * (D / 8); e += NTHREADS) {
@@ -130,70 +149,82 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
         umma::bulk_prefetch_l2(u + kPrepQE, 16384u);
       }
     }
-    if (!fwd && tid >= 64 && tid < 128) {
-      const int i = tid - 64;
+    if (!fwd && tid >= 128) {  // dO rows: two 128-byte lines each, plain L2 prefetches
+      const int i = (tid - 128) >> 1;
       const int64_t t0 = tok_seq + (int64_t)j * CHUNK;
-      if (i < L - j * CHUNK) umma::bulk_prefetch_l2(dOg + ((t0 + i) * H + h) * D, D * 2);
+      if (i < L - j * CHUNK) {
+        const bf16 *row = dOg + ((t0 + i) * H + h) * D + 64 * (tid & 1);
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row));
+      }
     }
   };
-  // bf16 state -> shared operand tile and the chunk's slot in HBM
   bf16 *states_out = reinterpret_cast<bf16 *>(fwd ? p.states : p.dstates);
-  auto publish = [&](int j) {
-    bf16 *dst = states_out + ((size_t)(slot0 + j) * H + h) * DD + (size_t)ch * D + 64 * hf;
+  // bf16 running state -> MMA1's operand tile
+  auto to_tile = [&]() {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      st16_bf(Xs + umma::core_off(ch, 64 * hf + 8 * q, D), X + 8 * q);
-      st16_bf(dst + 8 * q, X + 8 * q);
+    for (int q = 0; q < 8; ++q) st16_bf(Xs + umma::core_off(ch, 64 * hf + 8 * q, D), X + 8 * q);
+  };
+  // the bf16 tile (the state chunk j starts from) -> the chunk's slot in HBM,
+  // one bulk copy by thread 0 once the tile is complete and fenced
+  auto publish = [&](int j) {
+    if (tid == 0) {
+      umma::bulk_s2g(states_out + ((size_t)(slot0 + j) * H + h) * DD, Xs, (uint32_t)(DD * 2));
+      umma::bulk_commit();
     }
   };
-
+  const int nslots_in = fwd ? 3 : 2;
   if (nck > 0) {
-    issue_loads(0);
+    for (int sl = 0; sl < nslots_in; ++sl) load_slot(sl, 0);
     if (nck > 1) prefetch(1);
-    publish(chunk_of(0));
+    to_tile();
   }
   umma::fence_async_smem();
   umma::tc_fence_before();
   __syncthreads();
   umma::tc_fence_after();
+  if (nck > 0) publish(chunk_of(0));
   const uint32_t tbase = *tslot;
-  uint32_t ph_in = 0, ph_mma = 0;
-  bool bad = false, in_pending = nck > 0;
+  uint32_t ph[4] = {0u, 0u, 0u, 0u};  // phase of each barrier (bars[3] = MMA completion)
+  auto wait_bar = [&](int k, uint32_t limit = 1u << 24) {
+    const bool ok = umma::mbar_wait(bars + k, ph[k] & 1, limit);
+    ph[k]++;
+    return ok;
+  };
+  bool bad = false;
   const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's TMEM lanes
+  float eg = 1.f;
 
   for (int it = 0; it < nck; ++it) {
+    const bool more = it + 1 < nck;
     if (it + 2 < nck) prefetch(it + 2);
-    // ---- operands of this chunk ----
-    bool ok = umma::mbar_wait(bar_in, ph_in & 1);
-    ph_in++;
-    in_pending = !ok;
-    if (!fwd) {
-      cp_async_wait_all();
-      umma::fence_async_smem();
+    bool ok = true;
+    // ---- MMA1: T1 = (B1 X)^T into columns [0, 64) ----
+    if (fwd) {
+      ok = wait_bar(0);  // gT | W^T (every thread reads gT)
+      eg = __expf(reinterpret_cast<const float *>(IN + kPrepGT)[ch]);
+    } else if (tid == 0) {
+      ok = wait_bar(0);  // kr^T
     }
     if (__syncthreads_or(!ok)) {
       bad = true;
       break;
     }
-    // ---- MMA1: T1 = (B1 X)^T into columns [0, 64) ----
     if (tid == 0) {
       umma::tc_fence_after();
       const Op a = opmn(Xs, D, 0, CP);
-      if (fwd)
-        gemm(tbase, a, true, opmn(IN + kPrepW, 64, 0, CP), true, 64, D / 16, false);
-      else
-        gemm(tbase, a, true, opk(IN + kPrepKR, D, 0, CP), false, 64, D / 16, false);
-      umma::mma_commit(bar_mma);
+      const Op b1 = opmn(IN + (fwd ? kPrepW : kPrepKR), 64, 0, CP);  // W^T / kr^T, [c][i]
+      gemm(tbase, a, true, b1, true, 64, D / 16, false);
+      umma::mma_commit(bars + 3);
     }
-    const float eg = __expf(reinterpret_cast<const float *>(IN + kPrepGT)[ch]);
-    ok = umma::mbar_wait(bar_mma, ph_mma & 1);
-    ph_mma++;
+    ok = wait_bar(3);
     umma::tc_fence_after();
+    if (more && tid == 0) load_slot(0, it + 1);  // MMA1's operand is consumed
     // ---- U^T[v][i] for lane v = ch, i in [32 hf, 32 hf + 32) ----
     {
       float t[32];
       tld32(tbase, 0, t);
       if (fwd) {
+        ok = wait_bar(1) && ok;  // U0^T
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float u0[8];
@@ -208,57 +239,71 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
 #pragma unroll
       for (int q = 0; q < 4; ++q) st16_bf(Us + umma::core_off(ch, 32 * hf + 8 * q, 64), t + 8 * q);
     }
+    if (!fwd) {
+      ok = wait_bar(1) && ok;  // gT | W^T, QE^T
+      eg = __expf(reinterpret_cast<const float *>(IN + kPrepGT)[ch]);
+      cp_async_wait_all();     // dO
+    }
     umma::fence_async_smem();
     umma::tc_fence_before();
     if (__syncthreads_or(!ok)) {
       bad = true;
       break;
     }
+    if (fwd && more && tid == 0) load_slot(1, it + 1);  // U0^T is consumed
     // ---- MMA2: T2 into columns [64, 192) ----
     if (tid == 0) {
+      bool ok2 = true;
+      if (fwd) ok2 = wait_bar(2);  // kr^T
       umma::tc_fence_after();
       const Op b = opk(Us, 64, 0, CP);
-      if (fwd) {
-        gemm(tbase + 64, opmn(IN + kPrepKR, D, 0, CP), true, b, false, 128, 4, false);
-      } else {
-        gemm(tbase + 64, opk(IN + kPrepW, 64, 0, CP), false, b, false, 128, 4, false);
-        gemm(tbase + 64, opk(IN + kQEHere, 64, 0, CP), false, opmn(dOs, D, 0, CP), true, 128, 4,
-             true);
+      if (ok2) {
+        if (fwd) {
+          gemm(tbase + 64, opk(IN + kPrepKR, 64, 0, CP), false, b, false, 128, 4, false);
+        } else {
+          gemm(tbase + 64, opk(IN + kPrepW, 64, 0, CP), false, b, false, 128, 4, false);
+          gemm(tbase + 64, opk(IN + kQEHere, 64, 0, CP), false, opmn(dOs, D, 0, CP), true, 128, 4,
+               true);
+        }
       }
-      umma::mma_commit(bar_mma);
+      umma::mma_commit(bars + 3);
+      ok = ok2;
     }
-    ok = umma::mbar_wait(bar_mma, ph_mma & 1);
-    ph_mma++;
+    ok = wait_bar(3) && ok;
     umma::tc_fence_after();
+    if (tid == 0) umma::bulk_wait_read();  // the tile's previous store has read it
     if (__syncthreads_or(!ok)) {
       bad = true;
       break;
     }
-    // every operand of this chunk is consumed: start the next chunk's copies
-    if (it + 1 < nck) {
-      issue_loads(it + 1);
-      in_pending = true;
-    }
+    // MMA2's operands are consumed: refill for the next chunk
+    if (more) load_slot(fwd ? 2 : 1, it + 1);
     // ---- state update: X = e^gT X + T2 ----
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float t[16];
-      umma::tmem_ld16(tl + 64 + 64 * hf + 16 * q, t);
+    for (int q = 0; q < 4; q += 2) {
+      float t0[16], t1[16];
+      umma::tmem_ld16(tl + 64 + 64 * hf + 16 * q, t0);
+      umma::tmem_ld16(tl + 64 + 64 * hf + 16 * (q + 1), t1);
       umma::tmem_ld_wait();
 #pragma unroll
-      for (int n = 0; n < 16; ++n) X[16 * q + n] = fmaf(eg, X[16 * q + n], t[n]);
+      for (int n = 0; n < 16; ++n) {
+        X[16 * q + n] = fmaf(eg, X[16 * q + n], t0[n]);
+        X[16 * (q + 1) + n] = fmaf(eg, X[16 * (q + 1) + n], t1[n]);
+      }
     }
-    if (it + 1 < nck) publish(chunk_of(it + 1));
+    if (more) to_tile();
     umma::fence_async_smem();
     umma::tc_fence_before();
     __syncthreads();
+    if (more) publish(chunk_of(it + 1));
   }
   if (bad) {
     // a bounded wait gave up (status already flagged): let copies and MMAs in
     // flight land before the buffers and Tensor Memory are released
-    if (in_pending) umma::mbar_wait(bar_in, ph_in & 1);
+    if (tid == 0) {
+      for (int k = 0; k < 4; ++k) umma::mbar_wait(bars + k, ph[k] & 1, 1u << 16);
+    }
     cp_async_wait_all();
-    umma::mbar_wait(bar_mma, ph_mma & 1, 1u << 16);
     __syncthreads();
   } else {
     float *fin = fwd ? p.hT : p.dh0;
@@ -270,6 +315,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
             make_float4(X[4 * q], X[4 * q + 1], X[4 * q + 2], X[4 * q + 3]);
     }
   }
+  if (tid == 0) umma::bulk_wait_all();
   umma::tc_fence_before();
   __syncthreads();
   if (warp == 0) {

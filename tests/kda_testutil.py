@@ -64,3 +64,12 @@ def slot_index(x, chunk=64):
         base = s * nps if fixed else cu[s] // chunk + s
         out.append(np.arange(base, base + n))
     return out
+
+
+def unpack_core_tiles(t):
+    """[..., 128, 128] tiles in packed core-matrix order (8 x 8 cores, cores
+    along the second axis first) -> row-major, as a new tensor."""
+    lead = t.shape[:-2]
+    R, C = t.shape[-2], t.shape[-1]
+    x = t.reshape(*lead, R // 8, C // 8, 8, 8)
+    return x.transpose(-3, -2).reshape(*lead, R, C).contiguous()

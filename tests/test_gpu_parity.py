@@ -9,6 +9,7 @@ import __graft_entry__
 import linear_attention_backward_gb300 as kda
 from linear_attention_backward_gb300 import workloads as wl
 from kda_testutil import (GRADS, f64_tokens, gpu_bwd, oracle_bwd, oracle_states, rel_l2,
+                          unpack_core_tiles,
                           slot_index)
 
 pytestmark = pytest.mark.gpu
@@ -98,11 +99,12 @@ def test_fwd_states_and_reverse_scan_intermediates():
     off = kda.workspace_dstates_offset(shape)
     n = kda.num_chunk_slots(shape) * 2 * 128 * 128
     ws = g["_workspace"]
-    dst = ws[off:off + 2 * n].view(torch.bfloat16).reshape(-1, 2, 128, 128)
+    # bf16 K = V = 128: tiles in packed core-matrix order (include/kda.h)
+    dst = unpack_core_tiles(ws[off:off + 2 * n].view(torch.bfloat16).reshape(-1, 2, 128, 128))
     ref = oracle_bwd(x, want_chunk_dstates=True)
     assert rel_l2(dst.double().cpu().numpy()[slots], ref["chunk_dstates"]) < 1e-2
     # forward states recomputed inside kda_bwd (start of the workspace)
-    ins = ws[:2 * n].view(torch.bfloat16).reshape(-1, 2, 128, 128)
+    ins = unpack_core_tiles(ws[:2 * n].view(torch.bfloat16).reshape(-1, 2, 128, 128))
     assert rel_l2(ins.double().cpu().numpy()[slots], cs) < 1e-2
 
 
@@ -116,7 +118,8 @@ def test_states_given_matches_internal_recompute():
     n = kda.num_chunk_slots(shape) * 2 * 128 * 128
     # the recomputed states sit at the start of the workspace; handing the same
     # bf16 states back must reproduce every gradient bit for bit
-    internal = g1["_workspace"][:2 * n].view(torch.bfloat16).reshape(-1, 2, 128, 128).clone()
+    internal = unpack_core_tiles(
+        g1["_workspace"][:2 * n].view(torch.bfloat16).reshape(-1, 2, 128, 128))
     g2, _ = gpu_bwd(x, states=internal)
     for key in GRADS:
         assert torch.equal(g1[key], g2[key]), key
