@@ -228,15 +228,19 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
   // 1. scans: forward states (unless given) and the reverse dS scan, one launch
   const int nroles = states ? 1 : 2;
   p.role_base = states ? 1 : 0;
-  cudaError_t e;
-  if (tc_state_path(shape) && !legacy_scan()) {
+  cudaError_t e = cudaSuccess;
+  if (tc_state_path(shape)) {
+    // per-chunk operands for the tcgen05 scans and the gradient kernel
+    void *prep = w + 2 * sb + round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
+    p.prep = static_cast<const char *>(prep);
+    e = kda::prep_tc_launch(p, prep, cs);
+  }
+  if (e == cudaSuccess && tc_state_path(shape) && !legacy_scan()) {
     // the tcgen05 scans store their tiles in packed core-matrix order
     p.states_packed = states ? 0 : 1;
     p.dstates_packed = 1;
-    void *prep = w + 2 * sb + round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
-    e = kda::prep_tc_launch(p, prep, cs);
-    if (e == cudaSuccess) e = kda::scan_tc_launch(p, prep, nroles, cs);
-  } else {
+    e = kda::scan_tc_launch(p, p.prep, nroles, cs);
+  } else if (e == cudaSuccess) {
     const int bv = pick_band(shape, nroles);
     p.nb = shape->V / bv;
     e = kda::scan_dispatch(p, shape->K, bf, bv, nroles, cs);

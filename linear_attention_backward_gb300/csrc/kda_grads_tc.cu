@@ -24,8 +24,9 @@
 //   P6  [dvcorr; dO] U^T = [-dAkk | dMqk / s] (rows: dvcorr, then dO)   N = 64
 //   P8  S [dvcorr; dO]^T = [dvcorr S^T | dO S^T]^T                     N = 128
 //   P9  intra-chunk terms, per 16-row block pair, hi + lo operands      N = 64
-// The pair matrices Akk / Mqk and the WY inverse are formed as in the other
-// kernels (mma.sync on the same padded core tiles, fp32 substitution).
+// The pair matrices G = strict_lower(kd ki^T), scale Mqk, the WY inverse
+// INV = (I + Akk)^-1 and INV diag(beta) come from the prep kernel's
+// per-chunk block (kda_prep_tc.cu), as does kr^T.
 #include "kda_chunk.cuh"
 #include "kda_tc_tiles.cuh"
 
@@ -49,7 +50,7 @@ struct Smem {
   static constexpr size_t n_extra = 768 + 512 + 1024 + 256 + 64 + 16;
   static constexpr size_t sz_small = (((n_view + n_extra) * 4 + 64 + 1023) / 1024) * 1024;
   static constexpr size_t o_small = 0;
-  // R_A: raw q, k, g (prep, later again) | Gf fp32, Gbf, Mqk, INV, INVb
+  // R_A: raw q, k, g (prep, later again) | Gbf, Mqk, INV, INVb (from the prep block)
   static constexpr size_t o_A = o_small + sz_small;
   static constexpr size_t o_Gf = o_A;
   static constexpr size_t o_Gbf = o_Gf + 64 * 64 * 4;
@@ -79,6 +80,7 @@ struct Smem {
   static_assert(T128x128 + T128x64 <= sz_B, "S + U must fit R_B");
   static_assert(2 * T64x128 == T128x128, "dvcorr | dO stacking");
   static_assert(total <= 232448, "shared memory budget");
+  static_assert(16 * NT * 4 <= sz_C, "K1 row buffer must fit R_C");
 };
 
 // Raw q, k, g rows of the chunk (row-major [64][128], zero past len) and beta.
@@ -129,8 +131,7 @@ __device__ __forceinline__ float rows16_sum(float (&v)[16]) {
 
 // prep in the (channel, 16-row block) mapping; E kept in registers
 __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, const bf16 *Kr,
-                        const bf16 *Gr, const PrepView<bf16, D> &sv, float (&E)[16], void *KDt,
-                        void *KRt, void *QMt, void *KMt, void *KPt) {
+                        const bf16 *Gr, const PrepView<bf16, D> &sv, float (&E)[16], void *KDt) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = tid & 127, I = tid >> 7;
   const float A = __expf(p.A_log[h]);
@@ -200,32 +201,21 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
     sv.gT[tid] = tot;
   }
   __syncthreads();
-  // tiles are stored transposed, [c][i] (128 x 64), one 16-byte store per
-  // 8 rows: kd / kr are read MN-major (B, K = c), qm / km / kp K-major-by-
-  // transposition by the pair-matrix mma.sync (ldmatrix.trans)
-  const float em = sv.em[I * D + c], eg = sv.egm[I * D + c];
+  // kd^T [c][i] (128 x 64, read MN-major as MMA operand B with K = c), one
+  // 16-byte store per 8 rows
+  const float em = sv.em[I * D + c];
 #pragma unroll
   for (int q8 = 0; q8 < 2; ++q8) {
-    float vkd[8], vkr[8], vqm[8], vkm[8], vkp[8];
+    float vkd[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       const int r = 8 * q8 + t, i = 16 * I + r;
-      const float e = __expf(d[r]), ei = __expf(-d[r]);
+      const float e = __expf(d[r]);
       E[r] = e;
       const float kh = __bfloat162float(Kr[i * D + c]) * sv.rk[i];
-      const float qh = __bfloat162float(Qr[i * D + c]) * sv.rq[i];
       vkd[t] = (kh * e) * em;
-      vkr[t] = (kh * ei) * eg;
-      vqm[t] = qh * e;
-      vkm[t] = kh * e;
-      vkp[t] = kh * ei;
     }
-    const int i0 = 16 * I + 8 * q8;
-    pstore8(KDt, c, i0, 64, vkd);
-    pstore8(KRt, c, i0, 64, vkr);
-    pstore8(QMt, c, i0, 64, vqm);
-    pstore8(KMt, c, i0, 64, vkm);
-    pstore8(KPt, c, i0, 64, vkp);
+    pstore8(KDt, c, 16 * I + 8 * q8, 64, vkd);
   }
   __syncthreads();
 }
@@ -261,7 +251,6 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   bf16 *Qr = reinterpret_cast<bf16 *>(smem + SM::o_A);
   bf16 *Kr = Qr + 64 * D;
   bf16 *Gr = Kr + 64 * D;
-  float *Gf = reinterpret_cast<float *>(smem + SM::o_Gf);
   char *Gbf = smem + SM::o_Gbf, *Mqk = smem + SM::o_Mqk, *INV = smem + SM::o_INV,
        *INVb = smem + SM::o_INVb;
   char *QMh = smem + SM::o_B, *KMh = QMh + T64x128, *KPh = KMh + T64x128;
@@ -274,6 +263,7 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   const size_t DD = (size_t)D * D;
   const bf16 *Sg = reinterpret_cast<const bf16 *>(states) + ((size_t)slot * H + h) * DD;
   const bf16 *dSg = reinterpret_cast<const bf16 *>(p.dstates) + ((size_t)slot * H + h) * DD;
+  const char *unit = p.prep + ((size_t)slot * H + h) * kPrepUnitBytes;
 
   // ---- Tensor Memory (all 512 columns) and the MMA-completion barrier ----
   if (warp == 0) umma::tmem_alloc(tslot, 512);
@@ -294,6 +284,15 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     cp_async16(dOt + pcore_off(i, c8, D),
                reinterpret_cast<const bf16 *>(p.dO) + ((tok0 + (ok ? i : 0)) * H + h) * D + c8, ok);
   }
+  for (int e = tid; e < D * (D / 8); e += NT) {
+    const int r = e >> 4, c8 = (e & 15) * 8;
+    cp_async16(St + pcore_off(r, c8, D),
+               p.states_packed ? Sg + umma::core_off(r, c8, D) / 2 : Sg + (size_t)r * D + c8, true);
+  }
+  for (int e = tid; e < D * 8; e += NT) {  // kr^T [c][i] from the prep block
+    const int r = e >> 3, c8 = (e & 7) * 8;
+    cp_async16(KRt + pcore_off(r, c8, 64), unit + kPrepKR + umma::core_off(r, c8, 64), true);
+  }
   cp_async_commit();
   umma::tc_fence_before();
   asm volatile("cp.async.wait_group 1;\n" ::);
@@ -310,47 +309,17 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
 
   // ---- prep ----
   float E[16];
-  prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, KRt, QMh, KMh, KPh);
-  // ---- pair matrices (mma.sync): G (fp32, strictly lower) and scale * Mqk ----
-  for (int task = warp; task < 32; task += NW) {
-    const bool is_q = task >= 16;
-    const int Ib = (task >> 2) & 3, J = task & 3;
-    float acc[2][4];
-    zero_acc(acc);
-    if (J <= Ib)
-      wg_core_t<2>(acc, is_q ? QMh : KMh, 64, 0, 16 * Ib, KPh, 64, 0, 16 * J, D,
-                   J < Ib ? sv.F + pair_index(Ib, J) * D : nullptr);
-    for_acc(acc, [&](int r, int cc, float &v) {
-      const int i = 16 * Ib + r, jj = 16 * J + cc;
-      if (is_q)
-        *pel(Mqk, i, jj, 64) = __float2bfloat16_rn(jj <= i ? scale * v : 0.f);
-      else
-        Gf[i * 64 + jj] = jj < i ? v : 0.f;
-    });
-  }
-  __syncthreads();
-  // S -> R_B (QMh/KMh/KPh are dead) while the inverse runs
-  for (int e = tid; e < D * (D / 8); e += NT) {
-    const int r = e >> 4, c8 = (e & 15) * 8;
-    cp_async16(St + pcore_off(r, c8, D),
-               p.states_packed ? Sg + umma::core_off(r, c8, D) / 2 : Sg + (size_t)r * D + c8, true);
+  prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt);
+  // pair matrices and inverses, formed by the prep kernel: G, Mqk, INV, INVb
+  // (packed 64 x 64) into the padded tiles of R_A (the raw rows are dead)
+  for (int e = tid; e < 4 * 64 * 8; e += NT) {
+    const int t = e >> 9, r = (e >> 3) & 63, c8 = (e & 7) * 8;
+    char *dst = t == 0 ? Gbf : (t == 1 ? Mqk : (t == 2 ? INV : INVb));
+    const size_t src = t == 0 ? kPrepG : (t == 1 ? kPrepMqk : (t == 2 ? kPrepINV : kPrepINVb));
+    cp_async16(dst + pcore_off(r, c8, 64), unit + src + umma::core_off(r, c8, 64), true);
   }
   cp_async_commit();
-  for (int e8 = tid; e8 < 64 * 8; e8 += NT) {
-    const int i = e8 >> 3, j0 = (e8 & 7) * 8;
-    pstore8(Gbf, i, j0, 64, Gf + i * 64 + j0);
-  }
-  __syncthreads();
-  inverse_inplace(Gf, sv.beta, tbuf);
-  for (int e8 = tid; e8 < 64 * 8; e8 += NT) {
-    const int i = e8 >> 3, j0 = (e8 & 7) * 8;
-    float xb[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) xb[u] = Gf[i * 64 + j0 + u] * sv.beta[j0 + u];
-    pstore8(INV, i, j0, 64, Gf + i * 64 + j0);
-    pstore8(INVb, i, j0, 64, xb);
-  }
-  cp_async_wait_all();
+  asm volatile("cp.async.wait_group 1;\n" ::);  // S, dS, dO, kr^T
   umma::fence_async_smem();
   __syncthreads();
 
@@ -376,6 +345,7 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   for (int r = 0; r < 16; ++r) acc[r] = vv[r] - acc[r];
 #pragma unroll
   for (int q = 0; q < 2; ++q) pstore8(XrT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // Xr^T[d][i]
+  cp_async_wait_all();  // G, Mqk, INV, INVb
   umma::fence_async_smem();
   umma::tc_fence_before();
   __syncthreads();
@@ -700,10 +670,15 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     const float A = __expf(p.A_log[h]);
     float dA = 0.f;
     bf16 *dgg = reinterpret_cast<bf16 *>(p.dg);
+    // the row loop stays rolled (code size), so dgc goes through shared memory
+    // (R_C: the lo tiles are dead once P9c has completed)
+    float *dgs = reinterpret_cast<float *>(smem + SM::o_C);
 #pragma unroll
+    for (int r = 0; r < 16; ++r) dgs[r * NT + tid] = dgc[r];
+#pragma unroll 1
     for (int r = 15; r >= 0; --r) {
       const int i = 16 * I + r;
-      run += dgc[r];
+      run += dgs[r * NT + tid];
       if (i < len) {
         const float gv = __bfloat162float(Gr[i * D + c]);
         const float sg = __fdividef(1.f, 1.f + __expf(-gv));

@@ -29,6 +29,7 @@ struct KdaParams {
   // core-matrix order (8 x 8 bf16 cores of 128 bytes, cores along V first),
   // the shared-memory operand layout the tcgen05 scans store with one bulk copy.
   int states_packed, dstates_packed;
+  const char *prep;           // per-chunk operand blocks (bf16, K = V = 128), see below
 };
 
 // Per-chunk operands of the state scans (bf16, K = V = 128), one block of
@@ -41,12 +42,20 @@ struct KdaParams {
 //   KRt  [c][i]  kr^T, kr = k^ e^(gT - gc)
 //   U0t  [v][i]  U0^T, U0 = (I + Akk)^-1 diag(beta) v
 //   QEt  [c][i]  QE^T, QE = scale (qd - Mqk W)
+// and, for the gradient kernel, 64 x 64 bf16 tiles in the same order:
+//   Mqk  [i][j]  scale * lower(qd ki^T) (diagonal included)
+//   INV  [i][j]  (I + Akk)^-1,  INVb = INV diag(beta)
+//   G    [i][j]  strict_lower(kd ki^T)  (Akk = diag(beta) G)
 constexpr size_t kPrepGT = 0;
 constexpr size_t kPrepW = 512;
 constexpr size_t kPrepKR = kPrepW + 16384;
 constexpr size_t kPrepU0 = kPrepKR + 16384;
 constexpr size_t kPrepQE = kPrepU0 + 16384;
-constexpr size_t kPrepUnitBytes = kPrepQE + 16384;
+constexpr size_t kPrepMqk = kPrepQE + 16384;
+constexpr size_t kPrepINV = kPrepMqk + 8192;
+constexpr size_t kPrepINVb = kPrepINV + 8192;
+constexpr size_t kPrepG = kPrepINVb + 8192;
+constexpr size_t kPrepUnitBytes = kPrepG + 8192;
 
 // kda_prep_tc.cu: the per-chunk scan operands above (bf16, K = V = 128).
 cudaError_t prep_tc_launch(const KdaParams &p, void *prep, cudaStream_t st);

@@ -6,6 +6,8 @@
 //   W  = (I + Akk)^-1 diag(beta) kd       U0 = (I + Akk)^-1 diag(beta) v
 //   QE = scale (qd - Mqk W)               kr = k^ e^(gT - gc),  gT
 // (all four 64 x 128 tiles stored transposed, channel-major, see kda_params.h)
+// and keeps the pair matrices G, scale Mqk and the inverses INV, INV diag(beta)
+// for the gradient kernel, which then does not form them again.
 // With these the two serial recurrences of the backward ("all_states" of
 // kernel B2 and Kernel A, "bwd-kernelB-beginner-guide-full", Part 2, and the
 // A/B table of "bwd-ncu-and-optimization-playbook") need nothing else per
@@ -262,6 +264,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, c
     }
   }
   __syncthreads();
+  // G and scale * Mqk for the gradient kernel (packed 64 x 64 tiles)
+  for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
+    const int i = e8 >> 3, j0 = (e8 & 7) * 8;
+    const uint32_t off = umma::core_off(i, j0, 64);
+    st16_bf(unit + kPrepG + off, Gf + i * 64 + j0);
+    *reinterpret_cast<uint4 *>(unit + kPrepMqk + off) =
+        *reinterpret_cast<const uint4 *>(Mqk + pcore_off(i, j0, 64));
+  }
+  __syncthreads();
   inverse_inplace(Gf, sv.beta, tbuf);
   for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
     const int i = e8 >> 3, j0 = (e8 & 7) * 8;
@@ -269,6 +280,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, c
 #pragma unroll
     for (int u = 0; u < 8; ++u) x[u] = Gf[i * 64 + j0 + u] * sv.beta[j0 + u];
     pstore8(INVb, i, j0, 64, x);
+    const uint32_t off = umma::core_off(i, j0, 64);
+    st16_bf(unit + kPrepINV + off, Gf + i * 64 + j0);
+    st16_bf(unit + kPrepINVb + off, x);
   }
   umma::fence_async_smem();
   umma::tc_fence_before();

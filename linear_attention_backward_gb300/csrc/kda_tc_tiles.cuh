@@ -78,12 +78,19 @@ __device__ __forceinline__ Op opmn(const void *t, int C, int r0 = 0, uint32_t cs
   return Op{smem_u32(t) + (uint32_t)(r0 / 8) * (C / 8) * cs, (uint32_t)(C / 8) * cs, cs,
             2 * (uint32_t)(C / 8) * cs};
 }
+// D (+)= A B^T over `ksteps` K = 16 steps, issued by one thread; a step
+// advances the descriptors' start-address field by step >> 4.
 __device__ __forceinline__ void gemm(uint32_t d, Op a, bool amn, Op b, bool bmn, int N, int ksteps,
                                      bool accumulate) {
   const uint32_t id = umma::idesc_bf16(128, N, amn, bmn);
-  for (int s = 0; s < ksteps; ++s)
-    umma::mma_bf16(d, umma::smem_desc(a.addr + s * a.step, a.lbo, a.sbo),
-                   umma::smem_desc(b.addr + s * b.step, b.lbo, b.sbo), id, accumulate || s > 0);
+  uint64_t da = umma::smem_desc(a.addr, a.lbo, a.sbo);
+  uint64_t db = umma::smem_desc(b.addr, b.lbo, b.sbo);
+  const uint64_t ia = a.step >> 4, ib = b.step >> 4;
+  for (int s = 0; s < ksteps; ++s) {
+    umma::mma_bf16(d, da, db, id, accumulate || s > 0);
+    da += ia;
+    db += ib;
+  }
 }
 
 // ---- mma.sync on padded core tiles (pair matrices) ---------------------------

@@ -58,8 +58,8 @@ def test_slots_and_workspace(L):
     sb = (sb + 255) // 256 * 256
     assert kda.workspace_dstates_offset(s) == sb
     # states, dS, dA_log partials and (bf16, K = V = 128) the per-chunk operand
-    # blocks of the tcgen05 scans: 66048 bytes per (slot, head)
-    prep = (6 * 3 * 66048 + 255) // 256 * 256
+    # blocks of the tcgen05 path: 98816 bytes per (slot, head)
+    prep = (6 * 3 * 98816 + 255) // 256 * 256
     assert kda.workspace_bytes(s) == 2 * sb + ((6 * 3 * 4 + 255) // 256) * 256 + prep
     v = _shape(B=1, T=300, num_seqs=4, cu_seqlens=0x1000)
     assert kda.num_chunk_slots(v) == 300 // 64 + 4
