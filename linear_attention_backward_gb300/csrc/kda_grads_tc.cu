@@ -110,6 +110,15 @@ __device__ __forceinline__ void tld16(uint32_t tbase, int col0, float (&v)[16]) 
   umma::tmem_ld_wait();
 }
 
+// Two bf16 values (raw bits) in one register, and back to fp32 (exact).
+__device__ __forceinline__ uint32_t pack_bf(bf16 a, bf16 b) {
+  return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+// element r of 16 values packed two per register
+#define BF16_AT(arr, r) (((r) & 1) ? bf_hi((arr)[(r) >> 1]) : bf_lo((arr)[(r) >> 1]))
+
 // Row sums over the warp's 32 lanes for the thread's 16 rows: lanes l and
 // l + 16 return the sum of row l (31 shuffles); v is consumed.
 __device__ __forceinline__ float rows16_sum(float (&v)[16]) {
@@ -131,7 +140,8 @@ __device__ __forceinline__ float rows16_sum(float (&v)[16]) {
 
 // prep in the (channel, 16-row block) mapping; E kept in registers
 __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, const bf16 *Kr,
-                        const bf16 *Gr, const PrepView<bf16, D> &sv, float (&E)[16], void *KDt) {
+                        const bf16 *Gr, const PrepView<bf16, D> &sv, float (&E)[16], void *KDt,
+                        uint32_t (&q2)[8], uint32_t (&k2)[8], uint32_t (&g2)[8]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = tid & 127, I = tid >> 7;
   const float A = __expf(p.A_log[h]);
@@ -157,9 +167,16 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
   {
     float run = 0.f;
 #pragma unroll
+    for (int r = 0; r < 16; r += 2) {
+      const int i = 16 * I + r;
+      g2[r >> 1] = pack_bf(Gr[i * D + c], Gr[(i + 1) * D + c]);
+      q2[r >> 1] = pack_bf(Qr[i * D + c], Qr[(i + 1) * D + c]);
+      k2[r >> 1] = pack_bf(Kr[i * D + c], Kr[(i + 1) * D + c]);
+    }
+#pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int i = 16 * I + r;
-      const float gv = __bfloat162float(Gr[i * D + c]);
+      const float gv = BF16_AT(g2, r);
       run += i < len ? -A * softplus_f(gv) : 0.f;
       d[r] = run;
     }
@@ -212,7 +229,7 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
       const int r = 8 * q8 + t, i = 16 * I + r;
       const float e = __expf(d[r]);
       E[r] = e;
-      const float kh = __bfloat162float(Kr[i * D + c]) * sv.rk[i];
+      const float kh = BF16_AT(k2, r) * sv.rk[i];
       vkd[t] = (kh * e) * em;
     }
     pstore8(KDt, c, 16 * I + 8 * q8, 64, vkd);
@@ -309,7 +326,8 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
 
   // ---- prep ----
   float E[16];
-  prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt);
+  uint32_t q2[8], k2[8], g2[8];  // the thread's raw q, k, g rows, two per register
+  prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, q2, k2, g2);
   // pair matrices and inverses, formed by the prep kernel: G, Mqk, INV, INVb
   // (packed 64 x 64) into the padded tiles of R_A (the raw rows are dead)
   for (int e = tid; e < 4 * 64 * 8; e += NT) {
@@ -476,12 +494,13 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     const float db = dbs[tid] + red2[tid] + red2[64 + tid] + red2[128 + tid] + red2[192 + tid];
     reinterpret_cast<bf16 *>(p.dbeta)[(tok0 + tid) * H + h] = __float2bfloat16_rn(db);
   }
-  // raw q, k, g again (L2), for the hi / lo operands and the epilogues
-  stage_raw(p, h, tok0, len, Qr, Kr, Gr, nullptr);
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncthreads();
   // ---- intra-chunk operands, hi + lo (see kda_grads.cu) ----
+  // (R_A [0, 16K), the old raw q rows, keeps the g rows for the gate epilogue)
+  bf16 *gs = reinterpret_cast<bf16 *>(smem + SM::o_A);
+#pragma unroll
+  for (int r = 0; r < 16; r += 2) {
+    *reinterpret_cast<uint32_t *>(gs + (r >> 1) * 2 * NT + 2 * tid) = g2[r >> 1];
+  }
   float qh[16], kh[16];
 #pragma unroll
   for (int q8 = 0; q8 < 2; ++q8) {
@@ -489,8 +508,8 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       const int r = 8 * q8 + t, i = 16 * I + r;
-      qh[r] = __bfloat162float(Qr[i * D + c]) * sv.rq[i];
-      kh[r] = __bfloat162float(Kr[i * D + c]) * sv.rk[i];
+      qh[r] = BF16_AT(q2, r) * sv.rq[i];
+      kh[r] = BF16_AT(k2, r) * sv.rk[i];
       const float x[3] = {qh[r] * E[r], kh[r] * E[r], __fdividef(kh[r], E[r])};
 #pragma unroll
       for (int u = 0; u < 3; ++u) {
@@ -530,6 +549,10 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     umma::mma_commit(mbar);
   }
   mma_wait();
+  // dq / dk rows are finished in shared memory (R_A [16K, 48K): the prep tiles
+  // are dead after P6) and written to HBM as 16-byte row pieces
+  bf16 *dqs = reinterpret_cast<bf16 *>(smem + SM::o_A + 16384);
+  bf16 *dks = dqs + 64 * D;
   float dgc[16];
   {
     float bq[16];
@@ -539,10 +562,12 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     for (int r = 0; r < 16; ++r) in[r] = 0.f;
 #pragma unroll
     for (int J = 0; J < 4; ++J) {
-      float a16[16];
-      tld16(tbase, 64 * J, a16);
+      if (J <= I) {  // F_{I,J} = 0 above the diagonal blocks
+        float a16[16];
+        tld16(tbase, 64 * J, a16);
 #pragma unroll
-      for (int r = 0; r < 16; ++r) in[r] = fmaf(Fq[J], a16[r], in[r]);
+        for (int r = 0; r < 16; ++r) in[r] = fmaf(Fq[J], a16[r], in[r]);
+      }
     }
     float dq[16], pr[16];
 #pragma unroll
@@ -555,17 +580,14 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     if (lane < 16) red[warp * 16 + lane] = t;
     umma::tc_fence_before();
     __syncthreads();
-    bf16 *dqg = reinterpret_cast<bf16 *>(p.dq);
-    const int w0 = 4 * I;
+    // lane l < 16: row 16 I + l summed over the block's 4 warps; broadcast below
+    const float tot = red[(4 * I) * 16 + (lane & 15)] + red[(4 * I + 1) * 16 + (lane & 15)] +
+                      red[(4 * I + 2) * 16 + (lane & 15)] + red[(4 * I + 3) * 16 + (lane & 15)];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      const int i = 16 * I + r;
-      const float rd = red[(w0 + 0) * 16 + r] + red[(w0 + 1) * 16 + r] +
-                       red[(w0 + 2) * 16 + r] + red[(w0 + 3) * 16 + r];
-      if (i < len)
-        dqg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn((dq[r] - qh[r] * rd) * sv.rq[i]);
+      const float rd = __shfl_sync(0xffffffffu, tot, r);
+      dqs[(16 * I + r) * D + c] = __float2bfloat16_rn((dq[r] - qh[r] * rd) * sv.rq[16 * I + r]);
     }
-    __syncthreads();
   }
 
   // ---- P9b: dkd' intra (dA with kp) ----
@@ -586,10 +608,12 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     for (int r = 0; r < 16; ++r) dkt[r] = 0.f;
 #pragma unroll
     for (int J = 0; J < 4; ++J) {
-      float a16[16];
-      tld16(tbase, 64 * J, a16);
+      if (J <= I) {
+        float a16[16];
+        tld16(tbase, 64 * J, a16);
 #pragma unroll
-      for (int r = 0; r < 16; ++r) dkt[r] = fmaf(Fq[J], a16[r], dkt[r]);
+        for (int r = 0; r < 16; ++r) dkt[r] = fmaf(Fq[J], a16[r], dkt[r]);
+      }
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -599,6 +623,16 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   }
   umma::tc_fence_before();
   __syncthreads();
+  {
+    bf16 *dqg = reinterpret_cast<bf16 *>(p.dq);
+#pragma unroll 1
+    for (int e = tid; e < 64 * (D / 8); e += NT) {
+      const int i = e >> 4, c8 = (e & 15) * 8;
+      if (i < len)
+        *reinterpret_cast<uint4 *>(dqg + ((tok0 + i) * H + h) * D + c8) =
+            *reinterpret_cast<const uint4 *>(dqs + i * D + c8);
+    }
+  }
 
   // ---- P9c: dki' = E^-1 sum_{X >= J} (Mqk-side + A-side) with qm / km, per query block X ----
   if (tid == 0) {
@@ -619,10 +653,12 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     for (int r = 0; r < 16; ++r) dki[r] = 0.f;
 #pragma unroll
     for (int X = 0; X < 4; ++X) {
-      float a16[16];
-      tld16(tbase, 64 * X, a16);
+      if (X >= I) {  // F_{X,I} = 0 for X < I
+        float a16[16];
+        tld16(tbase, 64 * X, a16);
 #pragma unroll
-      for (int r = 0; r < 16; ++r) dki[r] = fmaf(Fk[X], a16[r], dki[r]);
+        for (int r = 0; r < 16; ++r) dki[r] = fmaf(Fk[X], a16[r], dki[r]);
+      }
     }
     float dkr[16];
     tld16(tbase, 448, dkr);
@@ -643,15 +679,12 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     if (lane < 16) red[warp * 16 + lane] = t;
     dgT[I * D + c] += colp;
     __syncthreads();
-    bf16 *dkg = reinterpret_cast<bf16 *>(p.dk);
-    const int w0 = 4 * I;
+    const float tot = red[(4 * I) * 16 + (lane & 15)] + red[(4 * I + 1) * 16 + (lane & 15)] +
+                      red[(4 * I + 2) * 16 + (lane & 15)] + red[(4 * I + 3) * 16 + (lane & 15)];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      const int i = 16 * I + r;
-      const float rd = red[(w0 + 0) * 16 + r] + red[(w0 + 1) * 16 + r] +
-                       red[(w0 + 2) * 16 + r] + red[(w0 + 3) * 16 + r];
-      if (i < len)
-        dkg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn((dk[r] - kh[r] * rd) * sv.rk[i]);
+      const float rd = __shfl_sync(0xffffffffu, tot, r);
+      dks[(16 * I + r) * D + c] = __float2bfloat16_rn((dk[r] - kh[r] * rd) * sv.rk[16 * I + r]);
     }
   }
 
@@ -660,8 +693,23 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     float tot = 0.f;
 #pragma unroll
     for (int r = 0; r < 16; ++r) tot += dgc[r];
-    __syncthreads();
-    red[I * 128 + c] = tot;  // (red is free again) block totals per channel
+    __syncthreads();         // red is free again; the dk rows are complete
+    red[I * 128 + c] = tot;  // block totals per channel
+    // the row loop stays rolled (code size): dgc goes through shared memory
+    // (R_C: the lo tiles are dead once P9c has completed)
+    float *dgs = reinterpret_cast<float *>(smem + SM::o_C);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) dgs[r * NT + tid] = dgc[r];
+    {
+      bf16 *dkg = reinterpret_cast<bf16 *>(p.dk);
+#pragma unroll 1
+      for (int e = tid; e < 64 * (D / 8); e += NT) {
+        const int i = e >> 4, c8 = (e & 15) * 8;
+        if (i < len)
+          *reinterpret_cast<uint4 *>(dkg + ((tok0 + i) * H + h) * D + c8) =
+              *reinterpret_cast<const uint4 *>(dks + i * D + c8);
+      }
+    }
     __syncthreads();
     float run = dgT[c] + dgT[D + c] + dgT[2 * D + c] + dgT[3 * D + c];
 #pragma unroll
@@ -669,22 +717,15 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
       if (X > I) run += red[X * 128 + c];
     const float A = __expf(p.A_log[h]);
     float dA = 0.f;
-    bf16 *dgg = reinterpret_cast<bf16 *>(p.dg);
-    // the row loop stays rolled (code size), so dgc goes through shared memory
-    // (R_C: the lo tiles are dead once P9c has completed)
-    float *dgs = reinterpret_cast<float *>(smem + SM::o_C);
-#pragma unroll
-    for (int r = 0; r < 16; ++r) dgs[r * NT + tid] = dgc[r];
+    bf16 *dgsm = dqs;  // dg rows, [64][128]
 #pragma unroll 1
     for (int r = 15; r >= 0; --r) {
       const int i = 16 * I + r;
       run += dgs[r * NT + tid];
-      if (i < len) {
-        const float gv = __bfloat162float(Gr[i * D + c]);
-        const float sg = __fdividef(1.f, 1.f + __expf(-gv));
-        dgg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn(run * (-A) * sg);
-        dA = fmaf(run, -A * softplus_f(gv), dA);
-      }
+      const float gv = __bfloat162float(gs[(r >> 1) * 2 * NT + 2 * tid + (r & 1)]);
+      const float sg = __fdividef(1.f, 1.f + __expf(-gv));
+      dgsm[i * D + c] = __float2bfloat16_rn(run * (-A) * sg);
+      if (i < len) dA = fmaf(run, -A * softplus_f(gv), dA);
     }
     dA = warp_sum(dA);
     if (lane == 0) dAred[warp] = dA;
@@ -694,6 +735,14 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
       float t = 0.f;
       for (int w = 0; w < NW; ++w) t += dAred[w];
       p.dA_part[slot * H + h] = t;
+    }
+    bf16 *dgg = reinterpret_cast<bf16 *>(p.dg);
+#pragma unroll 1
+    for (int e = tid; e < 64 * (D / 8); e += NT) {
+      const int i = e >> 4, c8 = (e & 15) * 8;
+      if (i < len)
+        *reinterpret_cast<uint4 *>(dgg + ((tok0 + i) * H + h) * D + c8) =
+            *reinterpret_cast<const uint4 *>(dgsm + i * D + c8);
     }
   }
   if (warp == 0) {
