@@ -33,27 +33,37 @@ sys.path.insert(0, ROOT)
 METRIC = "KDA backward tokens/s on 1×GB300 and % of bf16-TC/HBM roofline; vs CPU oracle"
 WORKLOAD = "main_bf16"
 
-# Algorithmic HBM bytes per (token, head) for K = V = 128, bf16:
-#   gradient kernel: reads q, k, v, dO, g (5 x 256 B), beta (2 B), the chunk
-#   state S_n and state gradient dS_{n+1} (2 x 32 KiB per 64 tokens = 1024 B);
-#   writes dq, dk, dv, dg (4 x 256 B) and dbeta (2 B)            -> 3332 B
-#   scan kernel: forward role reads k, v, g, beta (770 B) and writes S_n
-#   (512 B); reverse role reads q, k, g, beta, dO (1026 B) and writes
-#   dS_{n+1} (512 B)                                              -> 2820 B
-ALG_BYTES = {"grads": 3332, "scan": 2820}
-# Dense-equivalent FLOP per (token, head), K = V = 128 (chunk 64).
-ALG_FLOP = {"grads": 22.0e6 / 64, "scan": 17.0e6 / 64}
-KERNEL_NAMES = {"scan": "kda_scan_kernel", "grads": "kda_grads_kernel",
-                "reduce": "kda_dalog_reduce_kernel"}
+# Algorithmic HBM bytes per (token, head) for K = V = 128, bf16 (chunk 64):
+#   path: read q, k, v, dO, g (5 x 256 B) and beta (2 B); write dq, dk, dv, dg
+#   (4 x 256 B) and dbeta (2 B); write and read the bf16 chunk states S_n once
+#   each (2 x 32 KiB per 64 tokens = 1024 B)                       -> 3332 B
+#   gradient kernel: the same inputs and outputs, plus S_n and dS_{n+1}
+#   (2 x 512 B) read                                               -> 3332 B
+ALG_BYTES = {"grads": 3332, "path": 3332}
+# Dense-equivalent FLOP per (token, head): the gradient kernel's contractions
+# (16.8 MFLOP per 64-token chunk and head) and the whole path (38.1 MFLOP).
+ALG_FLOP = {"grads": 16.8e6 / 64, "path": 38.1e6 / 64}
+# phases recorded by kda_bwd_timed (5 events) and the kernel each one runs
+PHASES = ("prep", "scan", "grads", "reduce")
+KERNEL_NAMES = {"prep": "kda_prep_tc_kernel", "scan": "kda_scan_tc_kernel",
+                "grads": "kda_grads_tc_kernel", "reduce": "kda_dalog_reduce_kernel"}
+LAUNCHES_PER_STEP = 4
 
-# DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum)
-# on the main workload, keyed by the hash of the kernel sources it was taken
-# from; a changed kernel reports null until it is measured again.
-NCU_TRAFFIC = {}
+# DRAM traffic per launch of the gradient kernel from ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the hash of the
+# kernel sources it was taken from; a changed kernel reports null until it
+# is measured again.
+NCU_TRAFFIC = {
+    # ncu --set full on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read
+    # 808.0 MB + write 245.7 MB, scaled by 4 to the main workload's 16384
+    # chunk-heads (the kernel's traffic is proportional to the chunk-heads)
+    "kda_grads_tc_kernel": {"sha": "1ee5091438565846", "workload": "main_bf16",
+                            "bytes_per_launch": 4214933504},
+}
 
 KERNEL_SOURCES = {
-    "grads": ["kda_grads.cu", "kda_chunk.cuh", "kda_device.cuh"],
-    "scan": ["kda_scan.cu", "kda_chunk.cuh", "kda_device.cuh"],
+    "grads": ["kda_grads_tc.cu", "kda_tc_tiles.cuh", "kda_umma.cuh", "kda_chunk.cuh",
+              "kda_device.cuh", "kda_params.h"],
 }
 
 
@@ -147,7 +157,8 @@ def oracle_sample(x, n_units, t_sample, nthreads):
     import numpy as np
     import oracle
     B, T, H, K = x["q"].shape
-    units = [(u % B, (u * 7) % H) for u in range(n_units)]
+    units = [(b, h) for b in range(B) for h in range(H)]
+    units = (units * (n_units // len(units) + 1))[:n_units]
     t_sample = min(t_sample, T)
     pick = lambda t, b, h: t[b, :t_sample, h:h + 1].double().numpy()
     cat = lambda name: np.concatenate([pick(x[name], b, h) for b, h in units], 0)
@@ -166,10 +177,12 @@ def oracle_sample(x, n_units, t_sample, nthreads):
 
 
 def cpu_baseline(x, steps=1):
+    """The oracle on the whole workload (every (sequence, head) unit, all
+    tokens): about 10 s of fp64 work on 16 host cores."""
     cores = os.cpu_count() or 1
-    n_units = cores
-    t_sample = 2048
-    H = x["q"].shape[2]
+    B, T, H, _ = x["q"].shape
+    n_units = B * H
+    t_sample = T
     times = []
     head_tokens = 0
     for _ in range(steps):
@@ -178,9 +191,9 @@ def cpu_baseline(x, steps=1):
     sec = statistics.median(times)
     return {"value": (head_tokens / H) / sec, "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{n_units} (sequence, head) units x first {t_sample} tokens of the "
-                      f"{WORKLOAD} workload (= {head_tokens} head-tokens), fp64, "
-                      f"{cores} OpenMP threads; tokens = head-tokens / H",
+            "sample": f"the whole {WORKLOAD} workload: all {n_units} (sequence, head) units x "
+                      f"{t_sample} tokens (= {head_tokens} head-tokens), fp64, {cores} OpenMP "
+                      f"threads, one run; tokens = head-tokens / H",
             "seconds": sec}
 
 
@@ -286,7 +299,7 @@ def main():
     assert kda.get_device_status() == 0
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     for e4 in evs:  # materialise the events (created lazily by torch)
         for e in e4:
             e.record()
@@ -308,11 +321,10 @@ def main():
     if pg:
         pg.barrier()
     ms = start.elapsed_time(end)
-    phase = {"scan": [], "grads": [], "reduce": []}
-    for e4 in evs:
-        phase["scan"].append(e4[0].elapsed_time(e4[1]))
-        phase["grads"].append(e4[1].elapsed_time(e4[2]))
-        phase["reduce"].append(e4[2].elapsed_time(e4[3]))
+    phase = {n: [] for n in PHASES}
+    for e5 in evs:
+        for j, n in enumerate(PHASES):
+            phase[n].append(e5[j].elapsed_time(e5[j + 1]))
     if pg:
         t = torch.tensor([ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -350,28 +362,36 @@ def main():
     e2e = {"value": tokens * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
 
-    # ---- roofline of the dominant kernel ----
+    # ---- roofline of the dominant kernel, and of the whole step ----
     hbm, tflops, src = load_peaks()
     kern_ms = {k: statistics.mean(v) for k, v in phase.items()}
-    dom = max(("scan", "grads"), key=lambda k: kern_ms[k])
+    dom = "grads"  # the largest phase on every workload measured
     head_tokens = tokens * w.H
     alg = ALG_BYTES[dom] * head_tokens
     achieved = alg / (kern_ms[dom] * 1e-3) / 1e9
     tr = NCU_TRAFFIC.get(KERNEL_NAMES[dom])
-    traffic = tr["bytes_per_launch"] if tr and tr.get("sha") == src_hash(dom) else None
+    traffic = None
+    if tr and tr.get("sha") == src_hash(dom) and tr.get("workload") == args.workload:
+        traffic = tr["bytes_per_launch"]
     roofline = {"kernel": KERNEL_NAMES[dom], "bound": "hbm", "achieved": achieved,
                 "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                "alg_bytes_per_launch": alg, "peak_source": f"{src} (MEASURED_PEAKS hbm_gbs)",
+                "alg_bytes_per_launch": alg,
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
                 "tensor_frac": (ALG_FLOP[dom] * head_tokens / (kern_ms[dom] * 1e-3) / 1e12)
                 / tflops}
+    path_alg = ALG_BYTES["path"] * head_tokens
+    path = {"alg_bytes_per_step": path_alg,
+            "achieved_gbs": path_alg / (ms_step * 1e-3) / 1e9,
+            "frac_hbm": path_alg / (ms_step * 1e-3) / 1e9 / hbm,
+            "frac_tensor": ALG_FLOP["path"] * head_tokens / (ms_step * 1e-3) / 1e12 / tflops}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(w), "clocks": clocks, "e2e": e2e,
-        "gpu_launches": 3 * K, "roofline": roofline,
-        "kernels_ms": kern_ms,
+        "gpu_launches": LAUNCHES_PER_STEP * K, "roofline": roofline, "path_roofline": path,
+        "kernels_ms": kern_ms, "kernels": KERNEL_NAMES,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in cpu_baseline(xh).items() if k != "seconds"}

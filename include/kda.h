@@ -131,11 +131,12 @@ kda_status kda_bwd(const kda_shape *shape, const void *q, const void *k,
                    void *dbeta, float *dA_log, float *dh0, const void *states,
                    void *ws, size_t ws_bytes, kda_stream_t stream);
 
-/* kda_bwd with phase timing: `events` (nullable) points at 4 cudaEvent_t
+/* kda_bwd with phase timing: `events` (nullable) points at 5 cudaEvent_t
  * created by the caller (timing enabled).  They are recorded on `stream`
- * at the start of the call, after the chunk scans (forward-state recompute
- * and reverse dS scan), after the per-chunk gradient kernel and at the end
- * (after the dA_log reduction).  Otherwise identical to kda_bwd. */
+ * at the start of the call, after the per-chunk prep (bf16, K = V = 128;
+ * otherwise right after the first), after the chunk scans (forward-state
+ * recompute and reverse dS scan), after the per-chunk gradient kernel and
+ * at the end (after the dA_log reduction).  Otherwise identical to kda_bwd. */
 kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k,
                          const void *v, const void *g, const void *beta,
                          const float *A_log, const float *h0, const void *dO,
@@ -157,7 +158,7 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k,
  * until the process exits.
  *  - Size limit: problems whose kda_workspace_bytes() exceeds the array are
  *    rejected with KDA_ERR_TOO_LARGE before anything is launched (64 MiB
- *    holds about 1000 chunk-heads of 64 tokens at K = V = 128, bf16).
+ *    holds about 400 chunk-heads of 64 tokens at K = V = 128, bf16).
  *  - Set-up: the first call on each device looks up the array's device
  *    address (cudaGetSymbolAddress, with that device current) and caches
  *    it; make that first call before capturing any stream.

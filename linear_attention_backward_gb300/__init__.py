@@ -163,7 +163,7 @@ def bwd(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, cu_seqlens=None, scale=No
 
     ``out`` may hold preallocated output tensors under the same keys and
     ``workspace`` a uint8 CUDA tensor of at least ``workspace_bytes`` bytes.
-    ``events``: optional 4 ``torch.cuda.Event(enable_timing=True)`` recorded at
+    ``events``: optional 5 ``torch.cuda.Event(enable_timing=True)`` recorded at
     the phase boundaries (see ``kda_bwd_timed`` in include/kda.h).
     """
     shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2_eps=l2_eps)
@@ -186,7 +186,9 @@ def bwd(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, cu_seqlens=None, scale=No
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     ev = None
     if events is not None:
-        ev = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        if len(events) != 5:
+            raise ValueError("events: 5 timing events expected")
+        ev = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     st = lib().kda_bwd_timed(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                              _ptr(beta), _ptr(A_log), _ptr(h0), _ptr(dO), _ptr(dh_T),
                              _ptr(o["dq"]), _ptr(o["dk"]), _ptr(o["dv"]), _ptr(o["dg"]),

@@ -97,7 +97,7 @@ kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR
 
 extern "C" {
 
-int kda_abi_version(void) { return 1; }
+int kda_abi_version(void) { return 2; }
 
 const char *kda_status_str(kda_status st) {
   switch (st) {
@@ -235,6 +235,7 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
     p.prep = static_cast<const char *>(prep);
     e = kda::prep_tc_launch(p, prep, cs);
   }
+  mark(1);
   if (e == cudaSuccess && tc_state_path(shape) && !legacy_scan()) {
     // the tcgen05 scans store their tiles in packed core-matrix order
     p.states_packed = states ? 0 : 1;
@@ -246,10 +247,10 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
     e = kda::scan_dispatch(p, shape->K, bf, bv, nroles, cs);
   }
   if (e != cudaSuccess) return KDA_ERR_CUDA;
-  mark(1);
+  mark(2);
   // 2. per-chunk gradients and the dA_log reduction
-  e = kda::grads_dispatch(p, shape->K, bf, p.states, cs, events ? events[2] : nullptr);
-  mark(3);
+  e = kda::grads_dispatch(p, shape->K, bf, p.states, cs, events ? events[3] : nullptr);
+  mark(4);
   return from_cuda(e);
 }
 

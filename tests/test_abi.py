@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_strings(L):
-    assert L.kda_abi_version() == 1
+    assert L.kda_abi_version() == 2
     for st in range(7):
         assert len(L.kda_status_str(st)) > 0
 
