@@ -109,6 +109,10 @@ __device__ __forceinline__ void tld16(uint32_t tbase, int col0, float (&v)[16]) 
   umma::tmem_ld16(tlane(tbase, col0 + 16 * (int)(threadIdx.x >> 7)), v);
   umma::tmem_ld_wait();
 }
+// the same load without the wait (batch several, then umma::tmem_ld_wait)
+__device__ __forceinline__ void tld16_nw(uint32_t tbase, int col0, float (&v)[16]) {
+  umma::tmem_ld16(tlane(tbase, col0 + 16 * (int)(threadIdx.x >> 7)), v);
+}
 
 // Two bf16 values (raw bits) in one register, and back to fp32 (exact).
 __device__ __forceinline__ uint32_t pack_bf(bf16 a, bf16 b) {
@@ -118,6 +122,15 @@ __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u <<
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 // element r of 16 values packed two per register
 #define BF16_AT(arr, r) (((r) & 1) ? bf_hi((arr)[(r) >> 1]) : bf_lo((arr)[(r) >> 1]))
+
+// Triangle-sized accumulators of the intra-chunk products.  Key-block J of
+// P9a / P9b holds output rows i >= 16 J only (N = 64 - 16 J), query-block X
+// of P9c output columns j < 16 (X + 1) only (N = 16 (X + 1)).  TMEM column
+// bases: P9a in [0, 160), P9b in [160, 256) and [384, 448) (P8's results sit in
+// [256, 384) and dkr in [448, 512)), P9c in [0, 160).
+__device__ __forceinline__ int col_p9a(int J) { return J == 0 ? 0 : (J == 1 ? 64 : (J == 2 ? 112 : 144)); }
+__device__ __forceinline__ int col_p9b(int J) { return J == 0 ? 384 : (J == 1 ? 160 : (J == 2 ? 208 : 240)); }
+__device__ __forceinline__ int col_p9c(int X) { return X == 0 ? 0 : (X == 1 ? 16 : (X == 2 ? 48 : 96)); }
 
 // Row sums over the warp's 32 lanes for the thread's 16 rows: lanes l and
 // l + 16 return the sum of row l (31 shuffles); v is consumed.
@@ -306,6 +319,12 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     cp_async16(St + pcore_off(r, c8, D),
                p.states_packed ? Sg + umma::core_off(r, c8, D) / 2 : Sg + (size_t)r * D + c8, true);
   }
+  for (int e = tid; e < 64 * (D / 8); e += NT) {  // v rows -> U's slot (free until P2)
+    const int i = e >> 4, c8 = (e & 15) * 8;
+    const bool ok = i < len;
+    cp_async16(Ut + pcore_off(i, c8, D),
+               reinterpret_cast<const bf16 *>(p.v) + ((tok0 + (ok ? i : 0)) * H + h) * D + c8, ok);
+  }
   for (int e = tid; e < D * 8; e += NT) {  // kr^T [c][i] from the prep block
     const int r = e >> 3, c8 = (e & 7) * 8;
     cp_async16(KRt + pcore_off(r, c8, 64), unit + kPrepKR + umma::core_off(r, c8, 64), true);
@@ -341,26 +360,17 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   umma::fence_async_smem();
   __syncthreads();
 
-  // ---- P1: kdS^T = S^T kd^T ; the epilogue forms Xr^T = v^T - kdS^T ----
+  // ---- R1 = P1: kdS^T = S^T kd^T ; the epilogue forms Xr^T = v^T - kdS^T ----
   if (tid == 0) {
     umma::tc_fence_after();
     gemm(tbase + 0, opmn(St, D), true, opmn(KDt, 64), true, 64, D / 16, false);
     umma::mma_commit(mbar);
   }
-  float vv[16];
-  {
-    const bf16 *vg = reinterpret_cast<const bf16 *>(p.v);
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const int i = 16 * I + r;
-      vv[r] = i < len ? __bfloat162float(vg[((tok0 + i) * H + h) * D + c]) : 0.f;
-    }
-  }
   mma_wait();
   float acc[16];
   tld16(tbase, 0, acc);
 #pragma unroll
-  for (int r = 0; r < 16; ++r) acc[r] = vv[r] - acc[r];
+  for (int r = 0; r < 16; ++r) acc[r] = pget(Ut, 16 * I + r, c, D) - acc[r];  // v rows in U's slot
 #pragma unroll
   for (int q = 0; q < 2; ++q) pstore8(XrT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // Xr^T[d][i]
   cp_async_wait_all();  // G, Mqk, INV, INVb
@@ -368,30 +378,16 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   umma::tc_fence_before();
   __syncthreads();
 
-  // ---- P2: U^T = Xr^T INVb^T ; U[i][d] for the later products ----
+  // ---- R2 = P2 + P3a: U^T = Xr^T INVb^T ; dU^T = dO^T Mqk + dS^T kr^T (dU needs no U) ----
   if (tid == 0) {
     umma::tc_fence_after();
     gemm(tbase + 64, opk(XrT, 64), false, opk(INVb, 64), false, 64, 4, false);
-    umma::mma_commit(mbar);
-  }
-  mma_wait();
-  tld16(tbase, 64, acc);
-#pragma unroll
-  for (int q = 0; q < 2; ++q) pstore8(Ut, c, 16 * I + 8 * q, 64, acc + 8 * q);  // U^T[d][i]
-  umma::fence_async_smem();
-  umma::tc_fence_before();
-  __syncthreads();
-
-  // ---- P3: dU^T = dO^T Mqk + dS^T kr^T ; dkr^T = dS U^T ; B0: p ----
-  if (tid == 0) {
-    umma::tc_fence_after();
     gemm(tbase + 128, opmn(dOt, D), true, opmn(Mqk, 64), true, 64, 4, false);
     gemm(tbase + 128, opmn(dSt, D), true, opmn(KRt, 64), true, 64, D / 16, true);
-    gemm(tbase + 448, opk(dSt, D), false, opmn(Ut, 64), true, 64, D / 16, false);
     umma::mma_commit(mbar);
   }
   {
-    // p_c = e^gT_c sum_d dS[c][d] S[c][d]; thread (c, I) takes d in [32 I, 32 I + 32)
+    // B0: p_c = e^gT_c sum_d dS[c][d] S[c][d]; thread (c, I) takes d in [32 I, 32 I + 32)
     float pp = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -404,6 +400,9 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     dgT[I * D + c] = __expf(sv.gT[c]) * pp;
   }
   mma_wait();
+  tld16(tbase, 64, acc);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) pstore8(Ut, c, 16 * I + 8 * q, 64, acc + 8 * q);  // U^T[d][i]
   tld16(tbase, 128, acc);
 #pragma unroll
   for (int q = 0; q < 2; ++q) pstore8(dUT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // dU^T[d][i]
@@ -411,10 +410,11 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   umma::tc_fence_before();
   __syncthreads();
 
-  // ---- P5: dvcorr^T = dU^T INV ; dv, dbeta1, dvcorr[i][d] ----
+  // ---- R3 = P5 + P3b: dvcorr^T = dU^T INV ; dkr^T = dS U^T ; dv, dbeta1, dvcorr[i][d] ----
   if (tid == 0) {
     umma::tc_fence_after();
     gemm(tbase + 0, opk(dUT, 64), false, opmn(INV, 64), true, 64, 4, false);
+    gemm(tbase + 448, opk(dSt, D), false, opmn(Ut, 64), true, 64, D / 16, false);
     umma::mma_commit(mbar);
   }
   mma_wait();
@@ -539,12 +539,21 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     Fk[X] = X > I ? sv.F[pair_index(X, I) * D + c] : (X == I ? 1.f : 0.f);
   }
   const float emI = sv.em[I * D + c];
-  // ---- P9a: dq^ intra, one accumulator per key block J ----
+  // ---- R5 = P9a + P9b: dq^ intra (dMqk with kp) and dkd' intra (dA with kp), per key block J ----
+  // (descriptors built once and shifted per block: one thread issues all 16 MMAs)
   if (tid == 0) {
     umma::tc_fence_after();
+    const Desc aH = mkdesc(opk(KPh, 64)), aL = mkdesc(opk(KPl, 64));
+    const Desc bM = mkdesc(opk(dMqk, 64)), bA = mkdesc(opk(dAt, 64));
+#pragma unroll
     for (int J = 0; J < 4; ++J) {
-      gemm(tbase + 64 * J, opk(KPh, 64, 16 * J), false, opk(dMqk, 64, 16 * J), false, 64, 1, false);
-      gemm(tbase + 64 * J, opk(KPl, 64, 16 * J), false, opk(dMqk, 64, 16 * J), false, 64, 1, true);
+      const uint32_t id = umma::idesc_bf16(128, 64 - 16 * J, false, false);
+      const uint32_t ka = (uint32_t)(2 * J) * CS;                      // K offset (columns 16 J)
+      const uint32_t kb = ka + (uint32_t)(2 * J) * (64 / 8) * CS;      // and rows 16 J of B
+      mma1(tbase + col_p9a(J), dshift(aH, ka), dshift(bM, kb), id, false);
+      mma1(tbase + col_p9a(J), dshift(aL, ka), dshift(bM, kb), id, true);
+      mma1(tbase + col_p9b(J), dshift(aH, ka), dshift(bA, kb), id, false);
+      mma1(tbase + col_p9b(J), dshift(aL, ka), dshift(bA, kb), id, true);
     }
     umma::mma_commit(mbar);
   }
@@ -555,18 +564,25 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   bf16 *dks = dqs + 64 * D;
   float dgc[16];
   {
-    float bq[16];
-    tld16(tbase, 320, bq);  // dO S^T (rows 64..127 of the stacked operand)
-    float in[16];
+    // dO S^T (rows 64..127 of the stacked operand) and key blocks J <= I
+    // (F_{I,J} = 0 above the diagonal blocks; rows 16 I .. of block J's
+    // accumulator), TMEM loads in two batches
+    float bq[16], in[16];
+    {
+      float a0[16], a1[16];
+      tld16_nw(tbase, 320, bq);
+      tld16_nw(tbase, col_p9a(0), a0);
+      if (I >= 1) tld16_nw(tbase, col_p9a(1) - 16, a1);
+      umma::tmem_ld_wait();
 #pragma unroll
-    for (int r = 0; r < 16; ++r) in[r] = 0.f;
+      for (int r = 0; r < 16; ++r) in[r] = Fq[0] * a0[r] + (I >= 1 ? Fq[1] * a1[r] : 0.f);
+      if (I >= 2) {
+        tld16_nw(tbase, col_p9a(2) - 32, a0);
+        if (I >= 3) tld16_nw(tbase, col_p9a(3) - 48, a1);
+        umma::tmem_ld_wait();
 #pragma unroll
-    for (int J = 0; J < 4; ++J) {
-      if (J <= I) {  // F_{I,J} = 0 above the diagonal blocks
-        float a16[16];
-        tld16(tbase, 64 * J, a16);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) in[r] = fmaf(Fq[J], a16[r], in[r]);
+        for (int r = 0; r < 16; ++r)
+          in[r] = fmaf(Fq[2], a0[r], in[r]) + (I >= 3 ? Fq[3] * a1[r] : 0.f);
       }
     }
     float dq[16], pr[16];
@@ -590,29 +606,24 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     }
   }
 
-  // ---- P9b: dkd' intra (dA with kp) ----
-  if (tid == 0) {
-    umma::tc_fence_after();
-    for (int J = 0; J < 4; ++J) {
-      gemm(tbase + 64 * J, opk(KPh, 64, 16 * J), false, opk(dAt, 64, 16 * J), false, 64, 1, false);
-      gemm(tbase + 64 * J, opk(KPl, 64, 16 * J), false, opk(dAt, 64, 16 * J), false, 64, 1, true);
-    }
-    umma::mma_commit(mbar);
-  }
-  mma_wait();
   float dkt[16];
   {
-    float bk[16];
-    tld16(tbase, 256, bk);  // dvcorr S^T
+    float bk[16];  // dvcorr S^T, and the key blocks as for dq
+    {
+      float a0[16], a1[16];
+      tld16_nw(tbase, 256, bk);
+      tld16_nw(tbase, col_p9b(0), a0);
+      if (I >= 1) tld16_nw(tbase, col_p9b(1) - 16, a1);
+      umma::tmem_ld_wait();
 #pragma unroll
-    for (int r = 0; r < 16; ++r) dkt[r] = 0.f;
+      for (int r = 0; r < 16; ++r) dkt[r] = Fq[0] * a0[r] + (I >= 1 ? Fq[1] * a1[r] : 0.f);
+      if (I >= 2) {
+        tld16_nw(tbase, col_p9b(2) - 32, a0);
+        if (I >= 3) tld16_nw(tbase, col_p9b(3) - 48, a1);
+        umma::tmem_ld_wait();
 #pragma unroll
-    for (int J = 0; J < 4; ++J) {
-      if (J <= I) {
-        float a16[16];
-        tld16(tbase, 64 * J, a16);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) dkt[r] = fmaf(Fq[J], a16[r], dkt[r]);
+        for (int r = 0; r < 16; ++r)
+          dkt[r] = fmaf(Fq[2], a0[r], dkt[r]) + (I >= 3 ? Fq[3] * a1[r] : 0.f);
       }
     }
 #pragma unroll
@@ -634,34 +645,46 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     }
   }
 
-  // ---- P9c: dki' = E^-1 sum_{X >= J} (Mqk-side + A-side) with qm / km, per query block X ----
+  // ---- R6 = P9c: dki' = E^-1 sum_{X >= J} (Mqk-side + A-side) with qm / km, per query block X ----
   if (tid == 0) {
     umma::tc_fence_after();
+    const Desc aQH = mkdesc(opk(QMh, 64)), aQL = mkdesc(opk(QMl, 64));
+    const Desc aKH = mkdesc(opk(KMh, 64)), aKL = mkdesc(opk(KMl, 64));
+    const Desc bM = mkdesc(opmn(dMqk, 64)), bA = mkdesc(opmn(dAt, 64));
+#pragma unroll
     for (int X = 0; X < 4; ++X) {
-      const uint32_t d = tbase + 64 * X;
-      gemm(d, opk(QMh, 64, 16 * X), false, opmn(dMqk, 64, 16 * X), true, 64, 1, false);
-      gemm(d, opk(QMl, 64, 16 * X), false, opmn(dMqk, 64, 16 * X), true, 64, 1, true);
-      gemm(d, opk(KMh, 64, 16 * X), false, opmn(dAt, 64, 16 * X), true, 64, 1, true);
-      gemm(d, opk(KMl, 64, 16 * X), false, opmn(dAt, 64, 16 * X), true, 64, 1, true);
+      const uint32_t d = tbase + col_p9c(X);
+      const uint32_t id = umma::idesc_bf16(128, 16 * (X + 1), false, true);
+      const uint32_t ka = (uint32_t)(2 * X) * CS;                      // K offset (columns 16 X)
+      const uint32_t kb = (uint32_t)(2 * X) * (64 / 8) * CS;           // K offset (rows 16 X)
+      mma1(d, dshift(aQH, ka), dshift(bM, kb), id, false);
+      mma1(d, dshift(aQL, ka), dshift(bM, kb), id, true);
+      mma1(d, dshift(aKH, ka), dshift(bA, kb), id, true);
+      mma1(d, dshift(aKL, ka), dshift(bA, kb), id, true);
     }
     umma::mma_commit(mbar);
   }
   mma_wait();
   {
-    float dki[16];
+    // query blocks X >= I (F_{X,I} = 0 for X < I) and dkr, in two batches
+    float dki[16], dkr[16];
+    {
+      float a0[16], a1[16];
+      tld16_nw(tbase, 448, dkr);
+      tld16_nw(tbase, col_p9c(3), a0);
+      if (I <= 2) tld16_nw(tbase, col_p9c(2), a1);
+      umma::tmem_ld_wait();
 #pragma unroll
-    for (int r = 0; r < 16; ++r) dki[r] = 0.f;
+      for (int r = 0; r < 16; ++r) dki[r] = Fk[3] * a0[r] + (I <= 2 ? Fk[2] * a1[r] : 0.f);
+      if (I <= 1) {
+        tld16_nw(tbase, col_p9c(1), a0);
+        if (I == 0) tld16_nw(tbase, col_p9c(0), a1);
+        umma::tmem_ld_wait();
 #pragma unroll
-    for (int X = 0; X < 4; ++X) {
-      if (X >= I) {  // F_{X,I} = 0 for X < I
-        float a16[16];
-        tld16(tbase, 64 * X, a16);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) dki[r] = fmaf(Fk[X], a16[r], dki[r]);
+        for (int r = 0; r < 16; ++r)
+          dki[r] = fmaf(Fk[1], a0[r], dki[r]) + (I == 0 ? Fk[0] * a1[r] : 0.f);
       }
     }
-    float dkr[16];
-    tld16(tbase, 448, dkr);
     float dk[16], pr[16], colp = 0.f;
     const float egI = sv.egm[I * D + c];
 #pragma unroll
@@ -718,14 +741,18 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     const float A = __expf(p.A_log[h]);
     float dA = 0.f;
     bf16 *dgsm = dqs;  // dg rows, [64][128]
-#pragma unroll 1
+#pragma unroll 4
     for (int r = 15; r >= 0; --r) {
       const int i = 16 * I + r;
       run += dgs[r * NT + tid];
       const float gv = __bfloat162float(gs[(r >> 1) * 2 * NT + 2 * tid + (r & 1)]);
-      const float sg = __fdividef(1.f, 1.f + __expf(-gv));
+      // sigmoid and softplus from one exponential, t = e^-|g|
+      const float t = __expf(-fabsf(gv));
+      const float inv = __fdividef(1.f, 1.f + t);
+      const float sg = gv >= 0.f ? inv : t * inv;
+      const float sp = fmaxf(gv, 0.f) + __logf(1.f + t);
       dgsm[i * D + c] = __float2bfloat16_rn(run * (-A) * sg);
-      if (i < len) dA = fmaf(run, -A * softplus_f(gv), dA);
+      if (i < len) dA = fmaf(run, -A * sp, dA);
     }
     dA = warp_sum(dA);
     if (lane == 0) dAred[warp] = dA;

@@ -47,8 +47,8 @@ struct Smem {
   static constexpr size_t o_KM = o_QM + T64x128;    // k^ e^(gc - m)  [i][c] padded
   static constexpr size_t o_KP = o_KM + T64x128;    // k^ e^(m - gc)  -> later Mqk [i][j]
   static constexpr size_t o_V = o_KP + T64x128;     // v [j][v] packed
-  static constexpr size_t o_G = o_V + 16384;        // G / INV fp32 [64][64] -> later W^T
-  static constexpr size_t o_INVb = o_G + 16384;     // INV diag(beta) [i][j] padded
+  static constexpr size_t o_G = o_V + 16384;        // G / INV fp32 [64][68] -> later W^T
+  static constexpr size_t o_INVb = o_G + 64 * kGfStride * 4;  // INV diag(beta) [i][j] padded
   static constexpr size_t total = o_INVb + T64x64;
   static_assert(total + 1024 <= 233472 / 2, "two CTAs per SM");
 };
@@ -236,31 +236,59 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, c
   }
   __syncthreads();
   // ---- pair blocks: G = kd ki^T (strictly lower, fp32), scale * Mqk (lower) ----
+  // 20 nonzero 16 x 16 blocks (I >= J, two sides); the 12 off-diagonal ones
+  // carry the per-channel factor F_IJ.  Warp w takes one diagonal block
+  // (side w / 4, I = w % 4) and off-diagonal blocks w and w + 8 of the list
+  // below, so no warp does more than one diagonal and two scaled blocks.
   {
-    const int Ib = warp & 3;
-    const bool is_q = warp >= 4;
-    const char *X = is_q ? QM : KM;
-    float acc[4][2][4];
+    const int Ib0 = warp & 3;
+    const bool q0 = warp >= 4;
+    float acc[3][2][4];
+    int tI[3], tJ[3];
+    bool tq[3], tv[3];
+    tI[0] = Ib0; tJ[0] = Ib0; tq[0] = q0; tv[0] = true;
 #pragma unroll
-    for (int J = 0; J < 4; ++J) {
-      zero_acc(acc[J]);
-      if (J <= Ib)
-        wg_core<2>(acc[J], X, D, 16 * Ib, 0, KP, D, 16 * J, 0, D,
-                   J < Ib ? sv.F + pair_index(Ib, J) * D : nullptr);
-      if (!is_q)
-        for_acc(acc[J], [&](int r, int cc, float &v) {
-          const int i = 16 * Ib + r, jj = 16 * J + cc;
-          Gf[i * 64 + jj] = jj < i ? v : 0.f;
+    for (int t = 1; t < 3; ++t) {
+      const int o = warp + 8 * (t - 1);  // off-diagonal task index, 0..11
+      tv[t] = o < 12;
+      const int oi = o % 6;               // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+      tI[t] = oi == 0 ? 1 : (oi < 3 ? 2 : 3);
+      tJ[t] = oi == 0 ? 0 : (oi == 1 ? 0 : (oi == 2 ? 1 : oi - 3));
+      tq[t] = o >= 6;
+    }
+#pragma unroll
+    for (int t = 0; t < 3; ++t) {
+      zero_acc(acc[t]);
+      if (tv[t])
+        wg_core<2>(acc[t], tq[t] ? QM : KM, D, 16 * tI[t], 0, KP, D, 16 * tJ[t], 0, D,
+                   t > 0 ? sv.F + pair_index(tI[t], tJ[t]) * D : nullptr);
+    }
+    // G (fp32, strictly lower) and the zero blocks above the diagonal
+#pragma unroll
+    for (int t = 0; t < 3; ++t)
+      if (tv[t] && !tq[t])
+        for_acc(acc[t], [&](int r, int cc, float &v) {
+          const int i = 16 * tI[t] + r, jj = 16 * tJ[t] + cc;
+          Gf[i * kGfStride + jj] = jj < i ? v : 0.f;
         });
+    // blocks above the diagonal, u -> (I, J): (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+    for (int e = tid; e < 6 * 256; e += NTHREADS) {
+      const int u = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+      const int Iu = u < 3 ? 0 : (u < 5 ? 1 : 2), Ju = u < 3 ? u + 1 : (u < 5 ? u - 1 : 3);
+      Gf[(16 * Iu + r) * kGfStride + 16 * Ju + cc] = 0.f;
     }
     __syncthreads();  // KP is read by every warp above; Mqk overwrites it
-    if (is_q) {
 #pragma unroll
-      for (int J = 0; J < 4; ++J)
-        for_acc(acc[J], [&](int r, int cc, float &v) {
-          const int i = 16 * Ib + r, jj = 16 * J + cc;
+    for (int t = 0; t < 3; ++t)
+      if (tv[t] && tq[t])
+        for_acc(acc[t], [&](int r, int cc, float &v) {
+          const int i = 16 * tI[t] + r, jj = 16 * tJ[t] + cc;
           *pel(Mqk, i, jj, 64) = __float2bfloat16_rn(jj <= i ? scale * v : 0.f);
         });
+    for (int e = tid; e < 6 * 256; e += NTHREADS) {  // the same blocks of Mqk
+      const int u = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+      const int Iu = u < 3 ? 0 : (u < 5 ? 1 : 2), Ju = u < 3 ? u + 1 : (u < 5 ? u - 1 : 3);
+      *pel(Mqk, 16 * Iu + r, 16 * Ju + cc, 64) = __float2bfloat16_rn(0.f);
     }
   }
   __syncthreads();
@@ -268,7 +296,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, c
   for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
     const int i = e8 >> 3, j0 = (e8 & 7) * 8;
     const uint32_t off = umma::core_off(i, j0, 64);
-    st16_bf(unit + kPrepG + off, Gf + i * 64 + j0);
+    st16_bf(unit + kPrepG + off, Gf + i * kGfStride + j0);
     *reinterpret_cast<uint4 *>(unit + kPrepMqk + off) =
         *reinterpret_cast<const uint4 *>(Mqk + pcore_off(i, j0, 64));
   }
@@ -278,10 +306,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, c
     const int i = e8 >> 3, j0 = (e8 & 7) * 8;
     float x[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) x[u] = Gf[i * 64 + j0 + u] * sv.beta[j0 + u];
+    for (int u = 0; u < 8; ++u) x[u] = Gf[i * kGfStride + j0 + u] * sv.beta[j0 + u];
     pstore8(INVb, i, j0, 64, x);
     const uint32_t off = umma::core_off(i, j0, 64);
-    st16_bf(unit + kPrepINV + off, Gf + i * 64 + j0);
+    st16_bf(unit + kPrepINV + off, Gf + i * kGfStride + j0);
     st16_bf(unit + kPrepINVb + off, x);
   }
   umma::fence_async_smem();

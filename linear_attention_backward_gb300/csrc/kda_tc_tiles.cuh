@@ -93,6 +93,25 @@ __device__ __forceinline__ void gemm(uint32_t d, Op a, bool amn, Op b, bool bmn,
   }
 }
 
+// Precomputed form of an operand: its descriptor, and the descriptor step
+// (start address >> 4) per K = 16 step.
+struct Desc {
+  uint64_t d;
+  uint32_t step;
+};
+__device__ __forceinline__ Desc mkdesc(Op o) {
+  return Desc{umma::smem_desc(o.addr, o.lbo, o.sbo), o.step >> 4};
+}
+// the descriptor of the same operand shifted by `bytes` (a multiple of 16)
+__device__ __forceinline__ uint64_t dshift(const Desc &o, uint32_t bytes) {
+  return o.d + (bytes >> 4);
+}
+// one K = 16 MMA from precomputed descriptors
+__device__ __forceinline__ void mma1(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc,
+                                     bool accumulate) {
+  umma::mma_bf16(d, da, db, idesc, accumulate);
+}
+
 // ---- mma.sync on padded core tiles (pair matrices) ---------------------------
 __device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t a) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -167,11 +186,15 @@ __device__ __forceinline__ void wg_core(float (&acc)[NF][4], const void *A, int 
   }
 }
 
-// Gf [64][64] fp32 holds G (strictly lower) on entry and (I + diag(beta) G)^-1
-// on exit (block forward substitution in place; see wy_inverse).
+// Row stride (floats) of the fp32 G / INV tile: 68, so that the 8 rows a
+// warp reads at once in the block levels fall on different banks.
+constexpr int kGfStride = 68;
+// Gf [64][kGfStride] fp32 holds G (strictly lower) on entry and
+// (I + diag(beta) G)^-1 on exit (block forward substitution in place, as
+// wy_inverse in kda_chunk.cuh).
 __device__ inline void inverse_inplace(float *Gf, const float *beta, float *tbuf) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int LG = 64;
+  constexpr int LG = kGfStride;
   if (warp < 4) {
     const int o = 16 * warp, col = lane & 15;
     float x[16];
