@@ -53,10 +53,11 @@ struct Smem {
   // R_A: raw q, k, g (prep, later again) | Gbf, Mqk, INV, INVb (from the prep block)
   static constexpr size_t o_A = o_small + sz_small;
   static constexpr size_t o_Gf = o_A;
-  static constexpr size_t o_Gbf = o_Gf + 64 * 64 * 4;
-  static constexpr size_t o_Mqk = o_Gbf + T64x64;
-  static constexpr size_t o_INV = o_Mqk + T64x64;
-  static constexpr size_t o_INVb = o_INV + T64x64;
+  // packed 64 x 64 tiles in the prep block's order, filled by one bulk copy
+  static constexpr size_t o_Mqk = o_Gf + 64 * 64 * 4;
+  static constexpr size_t o_INV = o_Mqk + 8192;
+  static constexpr size_t o_INVb = o_INV + 8192;
+  static constexpr size_t o_Gbf = o_INVb + 8192;
   static constexpr size_t sz_A = 64 * 64 * 4 + 4 * T64x64;  // >= 3 raw tiles
   // R_B: QMh, KMh, KPh (prep)  ->  S, U  ->  hi tiles (intra)
   static constexpr size_t o_B = o_A + sz_A;
@@ -77,6 +78,10 @@ struct Smem {
   static constexpr size_t sz_D = T128x128 + T64x128;
   static constexpr size_t total = o_D + sz_D;
   static_assert(sz_A >= 3 * 64 * D * 2, "raw tiles must fit R_A");
+  static_assert(o_Gbf + 8192 <= o_A + sz_A, "prep tiles must fit R_A");
+  static_assert(kPrepINV == kPrepMqk + 8192 && kPrepINVb == kPrepINV + 8192 &&
+                    kPrepG == kPrepINVb + 8192,
+                "prep tiles are copied as one block");
   static_assert(T128x128 + T128x64 <= sz_B, "S + U must fit R_B");
   static_assert(2 * T64x128 == T128x128, "dvcorr | dO stacking");
   static_assert(total <= 232448, "shared memory budget");
@@ -277,7 +282,10 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   float *dbs = red2 + 256;         // [64]
   float *dAred = dbs + 64;         // [16]
   uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + SM::o_small + (SM::n_view + SM::n_extra) * 4);
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 1);
+  uint64_t *lbar = mbar + 1;   // bulk copies of S, dS, kr^T
+  uint64_t *pbar = mbar + 2;   // bulk copy of the prep tiles (its own barrier: it is armed
+                               // while the first group may still be in flight)
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 3);
   bf16 *Qr = reinterpret_cast<bf16 *>(smem + SM::o_A);
   bf16 *Kr = Qr + 64 * D;
   bf16 *Gr = Kr + 64 * D;
@@ -297,37 +305,48 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
 
   // ---- Tensor Memory (all 512 columns) and the MMA-completion barrier ----
   if (warp == 0) umma::tmem_alloc(tslot, 512);
-  if (tid == 0) umma::mbar_init(mbar, 1);
+  if (tid == 0) {
+    umma::mbar_init(mbar, 1);
+    umma::mbar_init(lbar, 1);
+    umma::mbar_init(pbar, 1);
+  }
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  // ---- stage: raw q, k, g (group 1); dS, dO into padded core tiles (group 2) ----
+  __syncthreads();
+  // S (packed in the workspace), dS and kr^T: bulk copies into packed tiles
+  if (tid == 0) {
+    const uint32_t bytes =
+        (p.states_packed ? 32768u : 0u) + (p.dstates_packed ? 32768u : 0u) + 16384u;
+    umma::mbar_expect_tx(lbar, bytes);
+    if (p.states_packed) umma::bulk_g2s(St, Sg, 32768u, lbar);
+    if (p.dstates_packed) umma::bulk_g2s(dSt, dSg, 32768u, lbar);
+    umma::bulk_g2s(KRt, unit + kPrepKR, 16384u, lbar);
+  }
+  // ---- stage: raw q, k, g (group 1); dO, v (group 2) by cp.async ----
   stage_raw(p, h, tok0, len, Qr, Kr, Gr, sv.beta);
   cp_async_commit();
-  for (int e = tid; e < D * (D / 8); e += NT) {  // dS rows c, 8-column chunks
-    const int r = e >> 4, c8 = (e & 15) * 8;
-    cp_async16(dSt + pcore_off(r, c8, D),
-               p.dstates_packed ? dSg + umma::core_off(r, c8, D) / 2 : dSg + (size_t)r * D + c8,
-               true);
-  }
   for (int e = tid; e < 64 * (D / 8); e += NT) {
     const int i = e >> 4, c8 = (e & 15) * 8;
     const bool ok = i < len;
     cp_async16(dOt + pcore_off(i, c8, D),
                reinterpret_cast<const bf16 *>(p.dO) + ((tok0 + (ok ? i : 0)) * H + h) * D + c8, ok);
   }
-  for (int e = tid; e < D * (D / 8); e += NT) {
-    const int r = e >> 4, c8 = (e & 15) * 8;
-    cp_async16(St + pcore_off(r, c8, D),
-               p.states_packed ? Sg + umma::core_off(r, c8, D) / 2 : Sg + (size_t)r * D + c8, true);
+  if (!p.states_packed) {  // row-major states (caller-provided) -> packed tile
+    for (int e = tid; e < D * (D / 8); e += NT) {
+      const int r = e >> 4, c8 = (e & 15) * 8;
+      cp_async16(St + umma::core_off(r, c8, D), Sg + (size_t)r * D + c8, true);
+    }
+  }
+  if (!p.dstates_packed) {  // row-major state gradients (the per-band scans)
+    for (int e = tid; e < D * (D / 8); e += NT) {
+      const int r = e >> 4, c8 = (e & 15) * 8;
+      cp_async16(dSt + umma::core_off(r, c8, D), dSg + (size_t)r * D + c8, true);
+    }
   }
   for (int e = tid; e < 64 * (D / 8); e += NT) {  // v rows -> U's slot (free until P2)
     const int i = e >> 4, c8 = (e & 15) * 8;
     const bool ok = i < len;
     cp_async16(Ut + pcore_off(i, c8, D),
                reinterpret_cast<const bf16 *>(p.v) + ((tok0 + (ok ? i : 0)) * H + h) * D + c8, ok);
-  }
-  for (int e = tid; e < D * 8; e += NT) {  // kr^T [c][i] from the prep block
-    const int r = e >> 3, c8 = (e & 7) * 8;
-    cp_async16(KRt + pcore_off(r, c8, 64), unit + kPrepKR + umma::core_off(r, c8, 64), true);
   }
   cp_async_commit();
   umma::tc_fence_before();
@@ -347,23 +366,21 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   float E[16];
   uint32_t q2[8], k2[8], g2[8];  // the thread's raw q, k, g rows, two per register
   prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, q2, k2, g2);
-  // pair matrices and inverses, formed by the prep kernel: G, Mqk, INV, INVb
-  // (packed 64 x 64) into the padded tiles of R_A (the raw rows are dead)
-  for (int e = tid; e < 4 * 64 * 8; e += NT) {
-    const int t = e >> 9, r = (e >> 3) & 63, c8 = (e & 7) * 8;
-    char *dst = t == 0 ? Gbf : (t == 1 ? Mqk : (t == 2 ? INV : INVb));
-    const size_t src = t == 0 ? kPrepG : (t == 1 ? kPrepMqk : (t == 2 ? kPrepINV : kPrepINVb));
-    cp_async16(dst + pcore_off(r, c8, 64), unit + src + umma::core_off(r, c8, 64), true);
+  // pair matrices and inverses, formed by the prep kernel: Mqk, INV, INVb, G
+  // (packed 64 x 64) into R_A (the raw rows are dead), one bulk copy
+  if (tid == 0) {
+    umma::mbar_expect_tx(pbar, 32768u);
+    umma::bulk_g2s(Mqk, unit + kPrepMqk, 32768u, pbar);
   }
-  cp_async_commit();
-  asm volatile("cp.async.wait_group 1;\n" ::);  // S, dS, dO, kr^T
+  cp_async_wait_all();                 // dO, v (and row-major S)
+  umma::mbar_wait(lbar, 0);            // S, dS, kr^T
   umma::fence_async_smem();
   __syncthreads();
 
   // ---- R1 = P1: kdS^T = S^T kd^T ; the epilogue forms Xr^T = v^T - kdS^T ----
   if (tid == 0) {
     umma::tc_fence_after();
-    gemm(tbase + 0, opmn(St, D), true, opmn(KDt, 64), true, 64, D / 16, false);
+    gemm(tbase + 0, opmn(St, D, 0, CP), true, opmn(KDt, 64), true, 64, D / 16, false);
     umma::mma_commit(mbar);
   }
   mma_wait();
@@ -373,7 +390,7 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   for (int r = 0; r < 16; ++r) acc[r] = pget(Ut, 16 * I + r, c, D) - acc[r];  // v rows in U's slot
 #pragma unroll
   for (int q = 0; q < 2; ++q) pstore8(XrT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // Xr^T[d][i]
-  cp_async_wait_all();  // G, Mqk, INV, INVb
+  umma::mbar_wait(pbar, 0);  // Mqk, INV, INVb, G
   umma::fence_async_smem();
   umma::tc_fence_before();
   __syncthreads();
@@ -381,9 +398,9 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   // ---- R2 = P2 + P3a: U^T = Xr^T INVb^T ; dU^T = dO^T Mqk + dS^T kr^T (dU needs no U) ----
   if (tid == 0) {
     umma::tc_fence_after();
-    gemm(tbase + 64, opk(XrT, 64), false, opk(INVb, 64), false, 64, 4, false);
-    gemm(tbase + 128, opmn(dOt, D), true, opmn(Mqk, 64), true, 64, 4, false);
-    gemm(tbase + 128, opmn(dSt, D), true, opmn(KRt, 64), true, 64, D / 16, true);
+    gemm(tbase + 64, opk(XrT, 64), false, opk(INVb, 64, 0, CP), false, 64, 4, false);
+    gemm(tbase + 128, opmn(dOt, D), true, opmn(Mqk, 64, 0, CP), true, 64, 4, false);
+    gemm(tbase + 128, opmn(dSt, D, 0, CP), true, opmn(KRt, 64, 0, CP), true, 64, D / 16, true);
     umma::mma_commit(mbar);
   }
   {
@@ -392,8 +409,8 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       float a8[8], b8[8];
-      pload8(dSt, c, 32 * I + 8 * q, D, a8);
-      pload8(St, c, 32 * I + 8 * q, D, b8);
+      ld16_bf(dSt + umma::core_off(c, 32 * I + 8 * q, D), a8);
+      ld16_bf(St + umma::core_off(c, 32 * I + 8 * q, D), b8);
 #pragma unroll
       for (int t = 0; t < 8; ++t) pp = fmaf(a8[t], b8[t], pp);
     }
@@ -413,8 +430,8 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   // ---- R3 = P5 + P3b: dvcorr^T = dU^T INV ; dkr^T = dS U^T ; dv, dbeta1, dvcorr[i][d] ----
   if (tid == 0) {
     umma::tc_fence_after();
-    gemm(tbase + 0, opk(dUT, 64), false, opmn(INV, 64), true, 64, 4, false);
-    gemm(tbase + 448, opk(dSt, D), false, opmn(Ut, 64), true, 64, D / 16, false);
+    gemm(tbase + 0, opk(dUT, 64), false, opmn(INV, 64, 0, CP), true, 64, 4, false);
+    gemm(tbase + 448, opk(dSt, D, 0, CP), false, opmn(Ut, 64), true, 64, D / 16, false);
     umma::mma_commit(mbar);
   }
   mma_wait();
@@ -449,7 +466,7 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   if (tid == 0) {
     umma::tc_fence_after();
     gemm(tbase + 64, opk(dvc, D), false, opmn(Ut, 64), true, 64, D / 16, false);
-    gemm(tbase + 256, opk(St, D), false, opk(dvc, D), false, 128, D / 16, false);
+    gemm(tbase + 256, opk(St, D, 0, CP), false, opk(dvc, D), false, 128, D / 16, false);
     umma::mma_commit(mbar);
   }
   mma_wait();
@@ -467,7 +484,7 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
         for (int t = 0; t < 8; ++t) {
           const int jj = 16 * I + 8 * q + t;
           const float dak = jj < i ? -v16[8 * q + t] : 0.f;
-          db2 = fmaf(dak, pget(Gbf, i, jj, 64), db2);
+          db2 = fmaf(dak, __bfloat162float(*reinterpret_cast<const bf16 *>(Gbf + umma::core_off(i, jj, 64))), db2);
           o8[t] = sv.beta[i] * dak;
         }
         pstore8(dAt, i, 16 * I + 8 * q, 64, o8);

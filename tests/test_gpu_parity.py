@@ -241,3 +241,14 @@ def test_full_size_sampled(name, units, dalog_head):
     # properties at full size: every gradient finite
     for key in GRADS:
         assert torch.isfinite(g[key].float()).all(), key
+
+
+def test_per_band_scans_feed_the_tensor_core_gradients(monkeypatch):
+    """KDA_SCAN_LEGACY=1: the per-band scans (row-major states and state
+    gradients) in front of the tensor-core gradient kernel."""
+    monkeypatch.setenv("KDA_SCAN_LEGACY", "1")
+    w = wl.custom("lg", B=2, T=200, H=2, K=128, V=128, dtype="bf16", with_h0=True,
+                  with_dhT=True)
+    x = wl.make_inputs(w, seed=17)
+    g, _ = gpu_bwd(x)
+    _compare(g, oracle_bwd(x), x, TOL["bf16"])
