@@ -229,11 +229,14 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
   const int nroles = states ? 1 : 2;
   p.role_base = states ? 1 : 0;
   cudaError_t e = cudaSuccess;
+  kda::TokenMaps tm;
   if (tc_state_path(shape)) {
-    // per-chunk operands for the tcgen05 scans and the gradient kernel
+    // TMA maps of the token-major inputs, and the per-chunk operands for the
+    // tcgen05 scans and the gradient kernel
+    if (!kda::encode_token_maps(p, tm)) return KDA_ERR_CUDA;
     void *prep = w + 2 * sb + round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
     p.prep = static_cast<const char *>(prep);
-    e = kda::prep_tc_launch(p, prep, cs);
+    e = kda::prep_tc_launch(p, tm, prep, cs);
   }
   mark(1);
   if (e == cudaSuccess && tc_state_path(shape) && !legacy_scan()) {
@@ -249,7 +252,8 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
   if (e != cudaSuccess) return KDA_ERR_CUDA;
   mark(2);
   // 2. per-chunk gradients and the dA_log reduction
-  e = kda::grads_dispatch(p, shape->K, bf, p.states, cs, events ? events[3] : nullptr);
+  e = kda::grads_dispatch(p, shape->K, bf, p.states, cs, events ? events[3] : nullptr,
+                          tc_state_path(shape) ? &tm : nullptr);
   mark(4);
   return from_cuda(e);
 }

@@ -535,12 +535,14 @@ static bool use_tc_kernel() {
 
 template <typename E, int D>
 static cudaError_t launch_grads(const KdaParams &p, const void *states, cudaStream_t st,
-                                void *after) {
+                                void *after, const TokenMaps *tm) {
   using SM = GradSmem<E, D>;
   cudaError_t e;
   // packed state tiles (tcgen05 scans) are read by the tcgen05 kernel only
-  if (sizeof(E) == 2 && D == 128 && (use_tc_kernel() || p.states_packed || p.dstates_packed)) {
-    e = grads_tc_launch(p, states, st);
+  if ((p.states_packed || p.dstates_packed) && tm == nullptr) return cudaErrorInvalidValue;
+  if (sizeof(E) == 2 && D == 128 && tm != nullptr &&
+      (use_tc_kernel() || p.states_packed || p.dstates_packed)) {
+    e = grads_tc_launch(p, *tm, states, st);
     if (e != cudaSuccess) return e;
   } else {
     auto kfn = kda_grads_kernel<E, D>;
@@ -558,12 +560,12 @@ static cudaError_t launch_grads(const KdaParams &p, const void *states, cudaStre
 }
 
 cudaError_t grads_dispatch(const KdaParams &p, int K, bool is_bf16, const void *states,
-                           cudaStream_t st, void *after) {
+                           cudaStream_t st, void *after, const TokenMaps *tm) {
   if (is_bf16) {
-    if (K == 128) return launch_grads<bf16, 128>(p, states, st, after);
-    if (K == 64) return launch_grads<bf16, 64>(p, states, st, after);
+    if (K == 128) return launch_grads<bf16, 128>(p, states, st, after, tm);
+    if (K == 64) return launch_grads<bf16, 64>(p, states, st, after, tm);
   } else {
-    if (K == 64) return launch_grads<float, 64>(p, states, st, after);
+    if (K == 64) return launch_grads<float, 64>(p, states, st, after, tm);
   }
   return cudaErrorInvalidValue;
 }

@@ -88,23 +88,6 @@ struct Smem {
   static_assert(16 * NT * 4 <= sz_C, "K1 row buffer must fit R_C");
 };
 
-// Raw q, k, g rows of the chunk (row-major [64][128], zero past len) and beta.
-__device__ __forceinline__ void stage_raw(const KdaParams &p, int h, int64_t tok0, int len,
-                                          bf16 *Qr, bf16 *Kr, bf16 *Gr, float *beta) {
-  const int H = p.H;
-  for (int e = threadIdx.x; e < 3 * 64 * (D / 8); e += NT) {
-    const int t = e >> 10, r = (e >> 4) & 63, c8 = (e & 15) * 8;
-    const bf16 *src = reinterpret_cast<const bf16 *>(t == 0 ? p.q : (t == 1 ? p.k : p.g));
-    bf16 *dst = (t == 0 ? Qr : (t == 1 ? Kr : Gr)) + r * D + c8;
-    const bool ok = r < len;
-    cp_async16(dst, src + ((tok0 + (ok ? r : 0)) * H + h) * D + c8, ok);
-  }
-  if (beta != nullptr && threadIdx.x < CHUNK)
-    beta[threadIdx.x] = threadIdx.x < len
-                            ? __bfloat162float(reinterpret_cast<const bf16 *>(p.beta)[(tok0 + threadIdx.x) * H + h])
-                            : 0.f;
-}
-
 // TMEM address of this thread's lane (warp quarter) at column col
 __device__ __forceinline__ uint32_t tlane(uint32_t tbase, int col) {
   return tbase + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16) + (uint32_t)col;
@@ -257,7 +240,8 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
 
 }  // namespace gtc
 
-__global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, const void *states) {
+__global__ void __launch_bounds__(gtc::NT, 1)
+    kda_grads_tc_kernel(KdaParams p, const __grid_constant__ TokenMaps tm, const void *states) {
   using namespace gtc;
   using SM = Smem;
   extern __shared__ __align__(1024) char smem[];
@@ -285,7 +269,8 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   uint64_t *lbar = mbar + 1;   // bulk copies of S, dS, kr^T
   uint64_t *pbar = mbar + 2;   // bulk copy of the prep tiles (its own barrier: it is armed
                                // while the first group may still be in flight)
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 3);
+  uint64_t *rbar = mbar + 3;   // TMA boxes of the raw q, k, g, v rows
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 4);
   bf16 *Qr = reinterpret_cast<bf16 *>(smem + SM::o_A);
   bf16 *Kr = Qr + 64 * D;
   bf16 *Gr = Kr + 64 * D;
@@ -309,6 +294,7 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     umma::mbar_init(mbar, 1);
     umma::mbar_init(lbar, 1);
     umma::mbar_init(pbar, 1);
+    umma::mbar_init(rbar, 1);
   }
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   __syncthreads();
@@ -321,9 +307,19 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
     if (p.dstates_packed) umma::bulk_g2s(dSt, dSg, 32768u, lbar);
     umma::bulk_g2s(KRt, unit + kPrepKR, 16384u, lbar);
   }
-  // ---- stage: raw q, k, g (group 1); dO, v (group 2) by cp.async ----
-  stage_raw(p, h, tok0, len, Qr, Kr, Gr, sv.beta);
-  cp_async_commit();
+  // raw q, k, g rows (row-major, R_A) and v rows (U's slot, free until P2):
+  // one TMA box each
+  if (tid == 0) {
+    umma::mbar_expect_tx(rbar, 4 * 16384u);
+    umma::tma_load_3d(Qr, &tm.q, 0, h, (int)tok0, rbar);
+    umma::tma_load_3d(Kr, &tm.k, 0, h, (int)tok0, rbar);
+    umma::tma_load_3d(Gr, &tm.g, 0, h, (int)tok0, rbar);
+    umma::tma_load_3d(Ut, &tm.v, 0, h, (int)tok0, rbar);
+  }
+  if (tid < CHUNK)
+    sv.beta[tid] = tid < len ? __bfloat162float(reinterpret_cast<const bf16 *>(p.beta)[(tok0 + tid) * H + h])
+                             : 0.f;
+  // ---- dO (and row-major states) by cp.async ----
   for (int e = tid; e < 64 * (D / 8); e += NT) {
     const int i = e >> 4, c8 = (e & 15) * 8;
     const bool ok = i < len;
@@ -342,15 +338,18 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
       cp_async16(dSt + umma::core_off(r, c8, D), dSg + (size_t)r * D + c8, true);
     }
   }
-  for (int e = tid; e < 64 * (D / 8); e += NT) {  // v rows -> U's slot (free until P2)
-    const int i = e >> 4, c8 = (e & 15) * 8;
-    const bool ok = i < len;
-    cp_async16(Ut + pcore_off(i, c8, D),
-               reinterpret_cast<const bf16 *>(p.v) + ((tok0 + (ok ? i : 0)) * H + h) * D + c8, ok);
-  }
   cp_async_commit();
   umma::tc_fence_before();
-  asm volatile("cp.async.wait_group 1;\n" ::);
+  umma::mbar_wait(rbar, 0);
+  if (len < CHUNK) {  // the boxes' rows past the chunk belong to the next sequence: zero them
+    for (int e = tid; e < 4 * 64 * 16; e += NT) {
+      const int t = e >> 10, i = (e >> 4) & 63, c8 = (e & 15) * 8;
+      if (i >= len) {
+        bf16 *base = t == 0 ? Qr : (t == 1 ? Kr : (t == 2 ? Gr : reinterpret_cast<bf16 *>(Ut)));
+        *reinterpret_cast<uint4 *>(base + i * D + c8) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
   __syncthreads();
   umma::tc_fence_after();
   const uint32_t tbase = *tslot;
@@ -387,7 +386,8 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   float acc[16];
   tld16(tbase, 0, acc);
 #pragma unroll
-  for (int r = 0; r < 16; ++r) acc[r] = pget(Ut, 16 * I + r, c, D) - acc[r];  // v rows in U's slot
+  for (int r = 0; r < 16; ++r)  // v rows, row-major in U's slot
+    acc[r] = __bfloat162float(reinterpret_cast<const bf16 *>(Ut)[(16 * I + r) * D + c]) - acc[r];
 #pragma unroll
   for (int q = 0; q < 2; ++q) pstore8(XrT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // Xr^T[d][i]
   umma::mbar_wait(pbar, 0);  // Mqk, INV, INVb, G
@@ -795,13 +795,14 @@ __global__ void __launch_bounds__(gtc::NT, 1) kda_grads_tc_kernel(KdaParams p, c
   }
 }
 
-cudaError_t grads_tc_launch(const KdaParams &p, const void *states, cudaStream_t st) {
+cudaError_t grads_tc_launch(const KdaParams &p, const TokenMaps &tm, const void *states,
+                            cudaStream_t st) {
   auto kfn = kda_grads_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)gtc::Smem::total);
   if (e != cudaSuccess) return e;
   if (p.nslots > 0) {
-    kfn<<<dim3((unsigned)p.nslots, p.H), gtc::NT, gtc::Smem::total, st>>>(p, states);
+    kfn<<<dim3((unsigned)p.nslots, p.H), gtc::NT, gtc::Smem::total, st>>>(p, tm, states);
     e = cudaGetLastError();
   }
   return e;

@@ -2,6 +2,7 @@
 // and the host-side entry points of the kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -57,8 +58,17 @@ constexpr size_t kPrepINVb = kPrepINV + 8192;
 constexpr size_t kPrepG = kPrepINVb + 8192;
 constexpr size_t kPrepUnitBytes = kPrepG + 8192;
 
+// TMA tensor maps of the token-major bf16 inputs [B * T, H, 128]: one box is
+// the 64 rows x 128 channels of one chunk and head, landing row-major
+// (256-byte rows) in shared memory; rows past the tensor's end read as zero.
+struct TokenMaps {
+  CUtensorMap q, k, g, v, dO;
+};
+// kda_tmap.cu: encodes the five maps; false if the driver refuses one.
+bool encode_token_maps(const KdaParams &p, TokenMaps &m);
+
 // kda_prep_tc.cu: the per-chunk scan operands above (bf16, K = V = 128).
-cudaError_t prep_tc_launch(const KdaParams &p, void *prep, cudaStream_t st);
+cudaError_t prep_tc_launch(const KdaParams &p, const TokenMaps &tm, void *prep, cudaStream_t st);
 int prep_tc_status_take();
 
 // kda_scan_tc.cu: both state scans on tcgen05 from the prep buffer; roles
@@ -76,12 +86,14 @@ int scan_status_take();
 // `after_grads` (nullable cudaEvent_t) is recorded between the gradient
 // kernel and the dA_log reduction.
 cudaError_t grads_dispatch(const KdaParams &p, int K, bool bf16, const void *states,
-                           cudaStream_t st, void *after_grads = nullptr);
+                           cudaStream_t st, void *after_grads = nullptr,
+                           const TokenMaps *tm = nullptr);
 size_t grads_smem_bytes(int K, bool bf16);
 int grads_status_take();
 
 // kda_grads_tc.cu: the same per-chunk gradients on tcgen05 (bf16, K = V = 128).
-cudaError_t grads_tc_launch(const KdaParams &p, const void *states, cudaStream_t st);
+cudaError_t grads_tc_launch(const KdaParams &p, const TokenMaps &tm, const void *states,
+                            cudaStream_t st);
 size_t grads_tc_smem_bytes();
 int grads_tc_status_take();
 

@@ -74,7 +74,8 @@ __device__ __forceinline__ float half_transpose_sum(float (&v)[16]) {
 
 }  // namespace ptc
 
-__global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, char *prep) {
+__global__ void __launch_bounds__(NTHREADS, 2)
+    kda_prep_tc_kernel(KdaParams p, const __grid_constant__ TokenMaps tm, char *prep) {
   using namespace ptc;
   using SM = ptc::Smem;
   extern __shared__ __align__(1024) char smem[];
@@ -92,7 +93,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, c
   float *tbuf = smf + SM::n_view;
   float *red = tbuf + 768;  // [2 (k, q)][8 warps][16 rows]
   uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + (SM::n_view + SM::n_extra) * 4);
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 1);
+  uint64_t *rbar = mbar + 1;  // TMA boxes of the raw q, k, g rows
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 2);
   char *QM = smem + SM::o_QM, *KM = smem + SM::o_KM, *KP = smem + SM::o_KP;
   char *Mqk = KP;
   char *Vt = smem + SM::o_V;
@@ -102,8 +104,22 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, c
   const float scale = p.scale;
 
   if (warp == 0) umma::tmem_alloc(tslot, 256);
-  if (tid == 0) umma::mbar_init(mbar, 1);
+  if (tid == 0) {
+    umma::mbar_init(mbar, 1);
+    umma::mbar_init(rbar, 1);
+  }
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  __syncthreads();
+  // raw q, k, g rows (row-major [64][128]) into the tile region, which the
+  // tiles overwrite only after every thread has taken its rows
+  const bf16 *Qraw = reinterpret_cast<const bf16 *>(QM);
+  const bf16 *Kraw = Qraw + 64 * D, *Graw = Kraw + 64 * D;
+  if (tid == 0) {
+    umma::mbar_expect_tx(rbar, 3 * 16384u);
+    umma::tma_load_3d(QM, &tm.q, 0, h, (int)tok0, rbar);
+    umma::tma_load_3d(QM + 16384, &tm.k, 0, h, (int)tok0, rbar);
+    umma::tma_load_3d(QM + 32768, &tm.g, 0, h, (int)tok0, rbar);
+  }
   // v rows -> packed core tile [j][v] (the MN-major A operand of U0^T)
   {
     const bf16 *vg = reinterpret_cast<const bf16 *>(p.v);
@@ -123,19 +139,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, c
   uint32_t kraw[16], qraw[16];
   float g0[16], g1[16];
   {
-    const size_t HD = (size_t)H * D;
-    const bf16 *kb = reinterpret_cast<const bf16 *>(p.k) + (size_t)tok0 * HD + (size_t)h * D + c;
-    const bf16 *qb = reinterpret_cast<const bf16 *>(p.q) + (size_t)tok0 * HD + (size_t)h * D + c;
-    const bf16 *gb = reinterpret_cast<const bf16 *>(p.g) + (size_t)tok0 * HD + (size_t)h * D + c;
     uint32_t graw[16];
+    umma::mbar_wait(rbar, 0);
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
+    for (int r = 0; r < 16; ++r) {  // rows past the chunk (the next sequence's) read as zero
       const int i = 16 * I + r;
       const bool ok = i < len;
-      const size_t off = (size_t)(ok ? i : 0) * HD;
-      kraw[r] = ok ? *reinterpret_cast<const uint32_t *>(kb + off) : 0u;
-      qraw[r] = ok ? *reinterpret_cast<const uint32_t *>(qb + off) : 0u;
-      graw[r] = ok ? *reinterpret_cast<const uint32_t *>(gb + off) : 0u;
+      kraw[r] = ok ? *reinterpret_cast<const uint32_t *>(Kraw + i * D + c) : 0u;
+      qraw[r] = ok ? *reinterpret_cast<const uint32_t *>(Qraw + i * D + c) : 0u;
+      graw[r] = ok ? *reinterpret_cast<const uint32_t *>(Graw + i * D + c) : 0u;
     }
     // norms: per-row partial sums over this thread's two channels
     float sk[16], sq[16];
@@ -389,14 +401,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_prep_tc_kernel(KdaParams p, c
   }
 }
 
-cudaError_t prep_tc_launch(const KdaParams &p, void *prep, cudaStream_t st) {
+cudaError_t prep_tc_launch(const KdaParams &p, const TokenMaps &tm, void *prep, cudaStream_t st) {
   auto kfn = kda_prep_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)ptc::Smem::total);
   if (e != cudaSuccess) return e;
   if (p.nslots > 0) {
     kfn<<<dim3((unsigned)p.nslots, p.H), NTHREADS, ptc::Smem::total, st>>>(
-        p, static_cast<char *>(prep));
+        p, tm, static_cast<char *>(prep));
     e = cudaGetLastError();
   }
   return e;

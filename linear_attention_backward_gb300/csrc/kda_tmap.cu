@@ -1,0 +1,52 @@
+// kda_tmap.cu -- host-side encoding of the TMA tensor maps of the token-major
+// inputs.  The driver's encoder is looked up through the runtime once per
+// process, so the library needs no link against the driver library.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "kda_params.h"
+
+namespace kda {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [ntok, H, 128] bf16, box = 64 tokens x 1 head x 128 channels
+bool encode(CUtensorMap *m, const void *base, int64_t ntok, int H) {
+  auto fn = encoder();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)ntok};
+  const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};  // bytes, dims 1 and 2
+  const cuuint32_t box[3] = {128, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool encode_token_maps(const KdaParams &p, TokenMaps &m) {
+  const int64_t ntok = (int64_t)p.B * p.T;
+  if (ntok <= 0) return true;  // nothing is launched
+  return encode(&m.q, p.q, ntok, p.H) && encode(&m.k, p.k, ntok, p.H) &&
+         encode(&m.g, p.g, ntok, p.H) && encode(&m.v, p.v, ntok, p.H) &&
+         encode(&m.dO, p.dO, ntok, p.H);
+}
+
+}  // namespace kda

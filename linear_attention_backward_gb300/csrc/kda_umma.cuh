@@ -134,6 +134,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(mbar))
       : "memory");
 }
+// One box of a 3-D tensor map (tiled, no swizzle) -> shared memory at dst
+// (128-byte aligned), completing `mbar` with the box's bytes.  `map` is the
+// address of a __grid_constant__ kernel parameter.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, int y, int z,
+                                            uint64_t *mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(mbar))
+      : "memory");
+}
+
 // shared -> global, tracked by the issuing thread's bulk-group counter
 __device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
