@@ -316,9 +316,10 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     umma::tma_load_3d(Gr, &tm.g, 0, h, (int)tok0, rbar);
     umma::tma_load_3d(Ut, &tm.v, 0, h, (int)tok0, rbar);
   }
-  if (tid < CHUNK)
-    sv.beta[tid] = tid < len ? __bfloat162float(reinterpret_cast<const bf16 *>(p.beta)[(tok0 + tid) * H + h])
-                             : 0.f;
+  // beta: the load's latency overlaps the copies; stored after they land
+  const float beta_i = tid < len && tid < CHUNK
+                           ? __bfloat162float(reinterpret_cast<const bf16 *>(p.beta)[(tok0 + tid) * H + h])
+                           : 0.f;
   // ---- dO (and row-major states) by cp.async ----
   for (int e = tid; e < 64 * (D / 8); e += NT) {
     const int i = e >> 4, c8 = (e & 15) * 8;
@@ -340,6 +341,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   cp_async_commit();
   umma::tc_fence_before();
+  if (tid < CHUNK) sv.beta[tid] = beta_i;
   umma::mbar_wait(rbar, 0);
   if (len < CHUNK) {  // the boxes' rows past the chunk belong to the next sequence: zero them
     for (int e = tid; e < 4 * 64 * 16; e += NT) {
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   mma_wait();
   tld16(tbase, 0, acc);
   {
-    bf16 *dvg = reinterpret_cast<bf16 *>(p.dv);
+    bf16 *dvs = reinterpret_cast<bf16 *>(smem + SM::o_A);  // dv rows [64][128]
     float xr[16];
 #pragma unroll
     for (int q = 0; q < 2; ++q) pload8(XrT, c, 16 * I + 8 * q, 64, xr + 8 * q);
@@ -446,7 +448,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     for (int r = 0; r < 16; ++r) {
       const int i = 16 * I + r;
       *pel(dvc, i, c, D) = __float2bfloat16_rn(acc[r]);
-      if (i < len) dvg[((tok0 + i) * H + h) * D + c] = __float2bfloat16_rn(sv.beta[i] * acc[r]);
+      dvs[i * D + c] = __float2bfloat16_rn(sv.beta[i] * acc[r]);
       pr[r] = acc[r] * xr[r];
     }
     // sums over this warp's 32 channels; lane l < 16 holds row 16 I + l
@@ -460,6 +462,17 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     const int i = tid, w0 = (i >> 4) * 4, r = i & 15;
     dbs[i] = red[(w0 + 0) * 16 + r] + red[(w0 + 1) * 16 + r] + red[(w0 + 2) * 16 + r] +
              red[(w0 + 3) * 16 + r];
+  }
+  {  // dv rows: 16-byte row pieces (they run alongside P6 / P8 below)
+    const bf16 *dvs = reinterpret_cast<const bf16 *>(smem + SM::o_A);
+    bf16 *dvg = reinterpret_cast<bf16 *>(p.dv);
+#pragma unroll 1
+    for (int e = tid; e < 64 * (D / 8); e += NT) {
+      const int i = e >> 4, c8 = (e & 15) * 8;
+      if (i < len)
+        *reinterpret_cast<uint4 *>(dvg + ((tok0 + i) * H + h) * D + c8) =
+            *reinterpret_cast<const uint4 *>(dvs + i * D + c8);
+    }
   }
 
   // ---- P6: [dvcorr; dO] U^T  and  P8: S [dvcorr; dO]^T ----
