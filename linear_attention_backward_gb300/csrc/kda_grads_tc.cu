@@ -298,23 +298,21 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   __syncthreads();
-  // S (packed in the workspace), dS and kr^T: bulk copies into packed tiles
+  // raw q, k, g rows (row-major, R_A) first: the prep phase waits on them;
+  // then v rows (U's slot, free until P2), S (packed in the workspace), dS
+  // and kr^T, which stream in during the prep phase
   if (tid == 0) {
-    const uint32_t bytes =
-        (p.states_packed ? 32768u : 0u) + (p.dstates_packed ? 32768u : 0u) + 16384u;
-    umma::mbar_expect_tx(lbar, bytes);
-    if (p.states_packed) umma::bulk_g2s(St, Sg, 32768u, lbar);
-    if (p.dstates_packed) umma::bulk_g2s(dSt, dSg, 32768u, lbar);
-    umma::bulk_g2s(KRt, unit + kPrepKR, 16384u, lbar);
-  }
-  // raw q, k, g rows (row-major, R_A) and v rows (U's slot, free until P2):
-  // one TMA box each
-  if (tid == 0) {
-    umma::mbar_expect_tx(rbar, 4 * 16384u);
+    umma::mbar_expect_tx(rbar, 3 * 16384u);
     umma::tma_load_3d(Qr, &tm.q, 0, h, (int)tok0, rbar);
     umma::tma_load_3d(Kr, &tm.k, 0, h, (int)tok0, rbar);
     umma::tma_load_3d(Gr, &tm.g, 0, h, (int)tok0, rbar);
-    umma::tma_load_3d(Ut, &tm.v, 0, h, (int)tok0, rbar);
+    const uint32_t bytes = 16384u + (p.states_packed ? 32768u : 0u) +
+                           (p.dstates_packed ? 32768u : 0u) + 16384u;
+    umma::mbar_expect_tx(lbar, bytes);
+    umma::tma_load_3d(Ut, &tm.v, 0, h, (int)tok0, lbar);
+    if (p.states_packed) umma::bulk_g2s(St, Sg, 32768u, lbar);
+    if (p.dstates_packed) umma::bulk_g2s(dSt, dSg, 32768u, lbar);
+    umma::bulk_g2s(KRt, unit + kPrepKR, 16384u, lbar);
   }
   // beta: the load's latency overlaps the copies; stored after they land
   const float beta_i = tid < len && tid < CHUNK
@@ -344,10 +342,10 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   if (tid < CHUNK) sv.beta[tid] = beta_i;
   umma::mbar_wait(rbar, 0);
   if (len < CHUNK) {  // the boxes' rows past the chunk belong to the next sequence: zero them
-    for (int e = tid; e < 4 * 64 * 16; e += NT) {
+    for (int e = tid; e < 3 * 64 * 16; e += NT) {
       const int t = e >> 10, i = (e >> 4) & 63, c8 = (e & 15) * 8;
       if (i >= len) {
-        bf16 *base = t == 0 ? Qr : (t == 1 ? Kr : (t == 2 ? Gr : reinterpret_cast<bf16 *>(Ut)));
+        bf16 *base = t == 0 ? Qr : (t == 1 ? Kr : Gr);
         *reinterpret_cast<uint4 *>(base + i * D + c8) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
@@ -388,8 +386,9 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   float acc[16];
   tld16(tbase, 0, acc);
 #pragma unroll
-  for (int r = 0; r < 16; ++r)  // v rows, row-major in U's slot
-    acc[r] = __bfloat162float(reinterpret_cast<const bf16 *>(Ut)[(16 * I + r) * D + c]) - acc[r];
+  for (int r = 0; r < 16; ++r)  // v rows, row-major in U's slot (rows past the chunk: zero)
+    acc[r] = (16 * I + r < len ? __bfloat162float(reinterpret_cast<const bf16 *>(Ut)[(16 * I + r) * D + c])
+                               : 0.f) - acc[r];
 #pragma unroll
   for (int q = 0; q < 2; ++q) pstore8(XrT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // Xr^T[d][i]
   umma::mbar_wait(pbar, 0);  // Mqk, INV, INVb, G
