@@ -186,6 +186,25 @@ __device__ __forceinline__ void wg_core(float (&acc)[NF][4], const void *A, int 
   }
 }
 
+// fp32 -> tf32 (round to nearest, ties away) and one mma.m16n8k8 tf32 step:
+// acc (16 x 8, fp32) += A (16 x 8) B (8 x 8), register fragments of the PTX
+// ISA's m16n8k8 layouts (g = lane / 4, t = lane % 4): a = A[g][t], A[g+8][t],
+// A[g][t+4], A[g+8][t+4]; b = B[t][g], B[t+4][g]; acc = C[g][2t], C[g][2t+1],
+// C[g+8][2t], C[g+8][2t+1].
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&acc)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // Row stride (floats) of the fp32 G / INV tile: 68, so that the 8 rows a
 // warp reads at once in the block levels fall on different banks.
 constexpr int kGfStride = 68;
@@ -219,42 +238,65 @@ __device__ inline void inverse_inplace(float *Gf, const float *beta, float *tbuf
     }
   }
   __syncthreads();
-#pragma unroll
+  // Block levels, X_IJ = -X_II diag(beta_I) sum_{L=J}^{I-1} G_IL X_LJ, on the
+  // tensor cores: warp J < I takes block (I, J) with mma.m16n8k8 tf32 (fp32
+  // accumulation).  tf32 operands round to 2^-11, finer than the bf16 in
+  // which the inverse is used.
+  const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll 1
   for (int I = 1; I < 4; ++I) {
-    const int J = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
-    const int row = 16 * I + r;
-    if (J < I) {
-      const float *grow = Gf + row * LG;
-      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int Lb = J; Lb < I; ++Lb) {
+    float *tw = tbuf + warp * 256;  // this warp's 16 x 16 scratch
+    if (warp < I) {
+      const int J = warp;
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      for (int L = J; L < I; ++L) {
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const float gv = grow[16 * Lb + x];
-          const float4 xv = *reinterpret_cast<const float4 *>(Gf + (16 * Lb + x) * LG + 16 * J + c4);
-          t.x = fmaf(gv, xv.x, t.x);
-          t.y = fmaf(gv, xv.y, t.y);
-          t.z = fmaf(gv, xv.z, t.z);
-          t.w = fmaf(gv, xv.w, t.w);
+        for (int kk = 0; kk < 2; ++kk) {
+          const float *ga = Gf + (16 * I + gid) * LG + 16 * L + 8 * kk + tig;
+          const uint32_t af[4] = {to_tf32(ga[0]), to_tf32(ga[8 * LG]), to_tf32(ga[4]),
+                                  to_tf32(ga[8 * LG + 4])};
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const float *xb = Gf + (16 * L + 8 * kk + tig) * LG + 16 * J + 8 * nt + gid;
+            const uint32_t bf[2] = {to_tf32(xb[0]), to_tf32(xb[4 * LG])};
+            mma_tf32(acc[nt], af, bf);
+          }
         }
       }
-      const float br = beta[row];
-      *reinterpret_cast<float4 *>(tbuf + (J << 8) + (r << 4) + c4) =
-          make_float4(br * t.x, br * t.y, br * t.z, br * t.w);
-    }
-    __syncthreads();
-    if (J < I) {
-      const float *xr = Gf + row * LG + 16 * I;
-      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      // T' = diag(beta_I) T into the scratch (row-major 16 x 16)
+      const float b0 = beta[16 * I + gid], b8 = beta[16 * I + gid + 8];
 #pragma unroll
-      for (int x = 0; x < 16; ++x) {
-        const float xv = xr[x];
-        const float4 tv = *reinterpret_cast<const float4 *>(tbuf + (J << 8) + (x << 4) + c4);
-        t.x = fmaf(xv, tv.x, t.x);
-        t.y = fmaf(xv, tv.y, t.y);
-        t.z = fmaf(xv, tv.z, t.z);
-        t.w = fmaf(xv, tv.w, t.w);
+      for (int nt = 0; nt < 2; ++nt) {
+        tw[gid * 16 + 8 * nt + 2 * tig] = b0 * acc[nt][0];
+        tw[gid * 16 + 8 * nt + 2 * tig + 1] = b0 * acc[nt][1];
+        tw[(gid + 8) * 16 + 8 * nt + 2 * tig] = b8 * acc[nt][2];
+        tw[(gid + 8) * 16 + 8 * nt + 2 * tig + 1] = b8 * acc[nt][3];
       }
-      *reinterpret_cast<float4 *>(Gf + row * LG + 16 * J + c4) = make_float4(-t.x, -t.y, -t.z, -t.w);
+    }
+    __syncthreads();  // every warp has read the G blocks of row I before any is overwritten
+    if (warp < I) {
+      const int J = warp;
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const float *xa = Gf + (16 * I + gid) * LG + 16 * I + 8 * kk + tig;  // X_II
+        const uint32_t af[4] = {to_tf32(xa[0]), to_tf32(xa[8 * LG]), to_tf32(xa[4]),
+                                to_tf32(xa[8 * LG + 4])};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float *tb = tw + (8 * kk + tig) * 16 + 8 * nt + gid;
+          const uint32_t bf[2] = {to_tf32(tb[0]), to_tf32(tb[4 * 16])};
+          mma_tf32(acc[nt], af, bf);
+        }
+      }
+      float *xo = Gf + (16 * I + gid) * LG + 16 * J;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        xo[8 * nt + 2 * tig] = -acc[nt][0];
+        xo[8 * nt + 2 * tig + 1] = -acc[nt][1];
+        xo[8 * LG + 8 * nt + 2 * tig] = -acc[nt][2];
+        xo[8 * LG + 8 * nt + 2 * tig + 1] = -acc[nt][3];
+      }
     }
     __syncthreads();
   }
