@@ -233,7 +233,9 @@ def run_reference(args, ws, rank):
 
 
 def workload_config(w):
-    return {"workload": f"{w.name}: KDA chunked backward, B={w.B} T={w.T} H={w.H} "
+    shape = (f"{w.varlen[0]} packed sequences of U[{w.varlen[1]}, {w.varlen[2]}] tokens"
+             if w.varlen else f"B={w.B} T={w.T}")
+    return {"workload": f"{w.name}: KDA chunked backward, {shape} H={w.H} "
                         f"K={w.K} V={w.V} chunk={w.chunk}, states recomputed in the call",
             "global_batch": w.B, "seq_len": w.T, "heads": w.H, "head_dim": w.K,
             "parallelism": "replicas (one independent batch per GPU)",
@@ -279,19 +281,23 @@ def main():
         names_in.append("h0")
     if w.with_dhT:
         names_in.append("dhT")
+    if xh["cu_seqlens"] is not None:  # varlen: the packed sequences' bounds
+        names_in.append("cu_seqlens")
     d = {n: xh[n].to(dev) for n in names_in}
     h0 = d.get("h0")
     dhT = d.get("dhT")
-    shape = kda.make_shape(d["q"], d["v"])
+    cu = d.get("cu_seqlens")
+    nseq = w.B if cu is None else cu.numel() - 1
+    shape = kda.make_shape(d["q"], d["v"], cu_seqlens=cu)
     wsb = torch.empty((kda.workspace_bytes(shape),), dtype=torch.uint8, device=dev)
     out = {n: torch.empty_like(d[m]) for n, m in
            (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
     out["dA_log"] = torch.empty((w.H,), dtype=torch.float32, device=dev)
-    out["dh0"] = torch.empty((w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+    out["dh0"] = torch.empty((nseq, w.H, w.K, w.V), dtype=torch.float32, device=dev)
 
     def step(events=None):
         kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], h0, d["dO"], dhT,
-                out=out, workspace=wsb, events=events)
+                cu_seqlens=cu, out=out, workspace=wsb, events=events)
 
     for _ in range(args.warmup):
         step()
@@ -330,7 +336,7 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t.item())
     ms_step = ms / K
-    tokens = w.B * w.T
+    tokens = int(xh["q"].shape[0] * xh["q"].shape[1])  # B * T, or the packed total (varlen)
     value = tokens * ws / (ms_step * 1e-3)
     assert kda.get_device_status() == 0
 

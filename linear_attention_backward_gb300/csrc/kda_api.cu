@@ -243,7 +243,14 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
     // the tcgen05 scans store their tiles in packed core-matrix order
     p.states_packed = states ? 0 : 1;
     p.dstates_packed = 1;
-    e = kda::scan_tc_launch(p, p.prep, nroles, cs);
+    if (p.cu != nullptr) {
+      // varlen: the scans take the sequences longest first; the order lives in
+      // the dA_log partials (slots x H >= num_seqs floats), which the gradient
+      // kernel overwrites only after the scans
+      p.seq_order = reinterpret_cast<const int32_t *>(p.dA_part);
+      e = kda::seq_order_launch(p.cu, p.num_seqs, reinterpret_cast<int32_t *>(p.dA_part), cs);
+    }
+    if (e == cudaSuccess) e = kda::scan_tc_launch(p, p.prep, nroles, cs);
   } else if (e == cudaSuccess) {
     const int bv = pick_band(shape, nroles);
     p.nb = shape->V / bv;

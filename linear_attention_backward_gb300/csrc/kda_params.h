@@ -31,6 +31,7 @@ struct KdaParams {
   // the shared-memory operand layout the tcgen05 scans store with one bulk copy.
   int states_packed, dstates_packed;
   const char *prep;           // per-chunk operand blocks (bf16, K = V = 128), see below
+  const int32_t *seq_order;   // tcgen05 scans: sequences longest first (varlen), or null
 };
 
 // Per-chunk operands of the state scans (bf16, K = V = 128), one block of
@@ -74,6 +75,8 @@ int prep_tc_status_take();
 // kda_scan_tc.cu: both state scans on tcgen05 from the prep buffer; roles
 // as in scan_dispatch.
 cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cudaStream_t st);
+// order[r] = the sequence of rank r by length (longest first, ties by index)
+cudaError_t seq_order_launch(const int32_t *cu, int num_seqs, int32_t *order, cudaStream_t st);
 int scan_tc_status_take();
 
 // kda_scan.cu: forward-state scan (role 0) and reverse dS scan (role 1).

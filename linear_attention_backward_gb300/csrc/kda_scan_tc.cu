@@ -54,10 +54,16 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   using namespace stc;
   using SM = stc::Smem;
   extern __shared__ __align__(1024) char smem[];
-  const int role = p.role_base + blockIdx.y;  // 0: forward states, 1: reverse dS scan
-  const bool fwd = role == 0;
-  const int h = blockIdx.x % p.H, s = blockIdx.x / p.H;
+  // block b -> (sequence rank r, role, head): the chains of the longest
+  // sequences are dispatched first (varlen), so that short chains fill in
+  // behind them instead of a long one starting last
   const int H = p.H;
+  const int nroles = 2 - p.role_base;
+  const int r = (int)(blockIdx.x / (unsigned)(nroles * H));
+  const int rem = (int)(blockIdx.x % (unsigned)(nroles * H));
+  const int role = p.role_base + rem / H;  // 0: forward states, 1: reverse dS scan
+  const bool fwd = role == 0;
+  const int h = rem % H, s = p.seq_order ? p.seq_order[r] : r;
   const int tid = threadIdx.x, warp = tid >> 5;
   int64_t tok_seq, slot0;
   int L;
@@ -329,10 +335,31 @@ cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cud
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)stc::Smem::total);
   if (e != cudaSuccess) return e;
-  const int nunits = (p.cu ? p.num_seqs : p.B) * p.H;
+  const int64_t nunits = (int64_t)(p.cu ? p.num_seqs : p.B) * p.H;
   if (nunits == 0 || nroles == 0) return cudaSuccess;
-  kfn<<<dim3(nunits, nroles), NTHREADS, stc::Smem::total, st>>>(p,
-                                                                 static_cast<const char *>(prep));
+  if (nroles != 2 - p.role_base) return cudaErrorInvalidValue;
+  kfn<<<(unsigned)(nunits * nroles), NTHREADS, stc::Smem::total, st>>>(
+      p, static_cast<const char *>(prep));
+  return cudaGetLastError();
+}
+
+// rank of sequence s = the number of sequences longer than s, or as long and
+// before it; every thread ranks one sequence against all (num_seqs reads)
+__global__ void kda_seq_order_kernel(const int32_t *cu, int n, int32_t *order) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= n) return;
+  const int Ls = cu[s + 1] - cu[s];
+  int r = 0;
+  for (int t = 0; t < n; ++t) {
+    const int Lt = cu[t + 1] - cu[t];
+    r += (Lt > Ls || (Lt == Ls && t < s)) ? 1 : 0;
+  }
+  order[r] = s;
+}
+
+cudaError_t seq_order_launch(const int32_t *cu, int num_seqs, int32_t *order, cudaStream_t st) {
+  if (num_seqs <= 0) return cudaSuccess;
+  kda_seq_order_kernel<<<(num_seqs + 255) / 256, 256, 0, st>>>(cu, num_seqs, order);
   return cudaGetLastError();
 }
 

@@ -78,6 +78,18 @@ def test_varlen_bf16_with_empty_sequence():
     np.testing.assert_allclose(g["dh0"][2].cpu().numpy(), x["dhT"][2].numpy(), rtol=0, atol=0)
 
 
+def test_varlen_many_sequences_with_ties():
+    # the scans take the sequences longest first: equal lengths (ties broken by
+    # index), empty sequences and more sequences than one wave of scan CTAs
+    lengths = [64, 0, 130, 64, 1, 200, 130, 0, 63, 64, 129, 5] * 4
+    w = wl.custom("vt", H=2, K=128, V=128, dtype="bf16", with_h0=True, with_dhT=True,
+                  varlen=(len(lengths), 0, 256))
+    x = wl.make_inputs(w, seed=11, lengths=lengths)
+    g, _ = gpu_bwd(x)
+    _check_status()
+    _compare(g, oracle_bwd(x), x, TOL["bf16"])
+
+
 def test_fwd_states_and_reverse_scan_intermediates():
     w = wl.custom("s", B=2, T=190, H=2, K=128, V=128, dtype="bf16", with_h0=True,
                   with_dhT=True)
