@@ -114,6 +114,22 @@ kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v,
                           const float *A_log, const float *h0, void *states,
                           float *hT, kda_stream_t stream);
 
+/* Forward pass: the read-out o_t = scale * S_t^T q^_t of every token and the
+ * final states ("bwd-kernelB-beginner-guide-full", Part 1: the chunked KDA
+ * recurrence whose backward kda_bwd computes), on the same per-chunk operands
+ * as kda_bwd: with U = U0 - W S_n the corrected values of chunk n and
+ * QE = scale (qd - Mqk W),  o = QE S_n + (scale Mqk) U0  row by row.
+ * bf16 with K = V = 128 only (KDA_ERR_UNSUPPORTED otherwise).
+ *   o      : OUT [B, T, H, V] bf16, overwritten (rows of every sequence).
+ *   h0     : nullable (zero initial state), fp32 [N, H, K, V].
+ *   hT     : nullable OUT fp32 [N, H, K, V]: the final state of each sequence.
+ *   ws     : DEVICE workspace of at least kda_workspace_bytes(shape) bytes,
+ *            256-byte aligned (the layout kda_bwd uses; its dS part is unused).
+ * q, k, v, g, beta and A_log are required. */
+kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const void *v,
+                   const void *g, const void *beta, const float *A_log, const float *h0,
+                   void *o, float *hT, void *ws, size_t ws_bytes, kda_stream_t stream);
+
 /* Backward pass.
  *   dh_T   : nullable (zero), fp32 [N, H, K, V].
  *   dq, dk, dv, dg, dbeta : OUT, overwritten, dtype of the shape.

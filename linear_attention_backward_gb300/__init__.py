@@ -69,6 +69,8 @@ def lib():
         L.kda_workspace_dstates_offset.restype = ctypes.c_size_t
         L.kda_fwd_states.argtypes = [S] + [_VP] * 9
         L.kda_fwd_states.restype = ctypes.c_int
+        L.kda_fwd.argtypes = [S] + [_VP] * 10 + [ctypes.c_size_t, _VP]
+        L.kda_fwd.restype = ctypes.c_int
         L.kda_bwd.argtypes = [S] + [_VP] * 18 + [ctypes.c_size_t, _VP]
         L.kda_bwd.restype = ctypes.c_int
         L.kda_bwd_timed.argtypes = [S] + [_VP] * 18 + [ctypes.c_size_t, _VP, _VP]
@@ -155,6 +157,27 @@ def fwd_states(k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None, l2
                               _ptr(A_log), _ptr(h0), _ptr(states), _ptr(hT), _stream())
     _check(st, "kda_fwd_states")
     return (states, hT) if want_hT else states
+
+
+def fwd(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None, l2_eps=None,
+        o=None, hT=None, want_hT=False, workspace=None):
+    """Forward read-out ``o`` [B, T, H, V] (bf16, K = V = 128) and, if asked,
+    the final states ``hT`` [N, H, K, V] fp32: ``(o, hT)`` or ``o``."""
+    shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2_eps=l2_eps)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, T, H, V), dtype=v.dtype, device=dev)
+    if want_hT and hT is None:
+        hT = torch.empty((_nseq(B, cu_seqlens), H, K, V), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty((workspace_bytes(shape),), dtype=torch.uint8, device=dev)
+    st = lib().kda_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                       _ptr(A_log), _ptr(h0), _ptr(o), _ptr(hT), _ptr(workspace),
+                       ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream())
+    _check(st, "kda_fwd")
+    return (o, hT) if want_hT else o
 
 
 def bwd(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, cu_seqlens=None, scale=None,

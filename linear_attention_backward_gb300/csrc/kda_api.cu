@@ -97,7 +97,7 @@ kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR
 
 extern "C" {
 
-int kda_abi_version(void) { return 2; }
+int kda_abi_version(void) { return 3; }
 
 const char *kda_status_str(kda_status st) {
   switch (st) {
@@ -163,6 +163,55 @@ kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v, 
   p.nb = shape->V / bv;
   return from_cuda(kda::scan_dispatch(p, shape->K, shape->dtype == KDA_BF16, bv, 1,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const void *v,
+                   const void *g, const void *beta, const float *A_log, const float *h0, void *o,
+                   float *hT, void *ws, size_t ws_bytes, kda_stream_t stream) {
+  kda_status st = check_shape(shape);
+  if (st != KDA_OK) return st;
+  if (!tc_state_path(shape)) return KDA_ERR_UNSUPPORTED;
+  const bool tokens = (int64_t)shape->B * shape->T > 0;
+  if (!A_log) return KDA_ERR_INVALID_ARG;
+  if (tokens && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, g, beta, A_log, h0, o, hT};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return KDA_ERR_INVALID_ARG;
+  const size_t need = kda_workspace_bytes(shape);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return KDA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return KDA_ERR_WORKSPACE;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  char *w = static_cast<char *>(ws);
+  const size_t sb = states_bytes(shape);
+  kda::KdaParams p;
+  fill_params(shape, p);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.g = g;
+  p.beta = beta;
+  p.A_log = A_log;
+  p.h0 = h0;
+  p.hT = hT;
+  p.states = w;  // packed chunk states, as kda_bwd keeps them
+  p.dA_part = reinterpret_cast<float *>(w + 2 * sb);
+  kda::TokenMaps tm;
+  if (!kda::encode_token_maps(p, tm)) return KDA_ERR_CUDA;
+  void *prep = w + 2 * sb + round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
+  p.prep = static_cast<const char *>(prep);
+  // 1. per-chunk operands, 2. forward state scan (S_n of every chunk, hT),
+  // 3. the chunk outputs
+  cudaError_t e = kda::prep_tc_launch(p, tm, prep, cs);
+  p.role_base = 0;
+  p.states_packed = 1;
+  if (e == cudaSuccess && p.cu != nullptr) {
+    p.seq_order = reinterpret_cast<const int32_t *>(p.dA_part);
+    e = kda::seq_order_launch(p.cu, p.num_seqs, reinterpret_cast<int32_t *>(p.dA_part), cs);
+  }
+  if (e == cudaSuccess) e = kda::scan_tc_launch(p, p.prep, 1, cs);
+  if (e == cudaSuccess) e = kda::out_tc_launch(p, p.states, o, cs);
+  return from_cuda(e);
 }
 
 kda_status kda_bwd(const kda_shape *shape, const void *q, const void *k, const void *v,
@@ -270,7 +319,7 @@ kda_status kda_get_device_status(kda_stream_t stream) {
     return KDA_ERR_CUDA;
   const int words[] = {kda::scan_status_take(), kda::prep_tc_status_take(),
                        kda::scan_tc_status_take(), kda::grads_status_take(),
-                       kda::grads_tc_status_take()};
+                       kda::grads_tc_status_take(), kda::out_tc_status_take()};
   for (int v : words)
     if (v < 0) return KDA_ERR_CUDA;
   for (int v : words)

@@ -79,6 +79,11 @@ cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cud
 cudaError_t seq_order_launch(const int32_t *cu, int num_seqs, int32_t *order, cudaStream_t st);
 int scan_tc_status_take();
 
+// kda_out_tc.cu: forward outputs o = QE S_n + Mqk U0 per chunk (bf16, K = V =
+// 128) from the prep blocks and the packed chunk states.
+cudaError_t out_tc_launch(const KdaParams &p, const void *states, void *o, cudaStream_t st);
+int out_tc_status_take();
+
 // kda_scan.cu: forward-state scan (role 0) and reverse dS scan (role 1).
 cudaError_t scan_dispatch(const KdaParams &p, int K, bool bf16, int bv, int nroles,
                           cudaStream_t st);

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   // sequences are dispatched first (varlen), so that short chains fill in
   // behind them instead of a long one starting last
   const int H = p.H;
-  const int nroles = 2 - p.role_base;
+  const int nroles = (int)(gridDim.x / (unsigned)((p.cu ? p.num_seqs : p.B) * H));
   const int r = (int)(blockIdx.x / (unsigned)(nroles * H));
   const int rem = (int)(blockIdx.x % (unsigned)(nroles * H));
   const int role = p.role_base + rem / H;  // 0: forward states, 1: reverse dS scan
@@ -337,7 +337,7 @@ cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cud
   if (e != cudaSuccess) return e;
   const int64_t nunits = (int64_t)(p.cu ? p.num_seqs : p.B) * p.H;
   if (nunits == 0 || nroles == 0) return cudaSuccess;
-  if (nroles != 2 - p.role_base) return cudaErrorInvalidValue;
+  if (nroles < 1 || p.role_base + nroles > 2) return cudaErrorInvalidValue;
   kfn<<<(unsigned)(nunits * nroles), NTHREADS, stc::Smem::total, st>>>(
       p, static_cast<const char *>(prep));
   return cudaGetLastError();

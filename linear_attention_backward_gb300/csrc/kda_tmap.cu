@@ -44,9 +44,12 @@ bool encode(CUtensorMap *m, const void *base, int64_t ntok, int H) {
 bool encode_token_maps(const KdaParams &p, TokenMaps &m) {
   const int64_t ntok = (int64_t)p.B * p.T;
   if (ntok <= 0) return true;  // nothing is launched
-  return encode(&m.q, p.q, ntok, p.H) && encode(&m.k, p.k, ntok, p.H) &&
-         encode(&m.g, p.g, ntok, p.H) && encode(&m.v, p.v, ntok, p.H) &&
-         encode(&m.dO, p.dO, ntok, p.H);
+  // a tensor the call does not have (dO in the forward) keeps an empty map
+  auto enc = [&](CUtensorMap *mp, const void *base) {
+    return base == nullptr || encode(mp, base, ntok, p.H);
+  };
+  return enc(&m.q, p.q) && enc(&m.k, p.k) && enc(&m.g, p.g) && enc(&m.v, p.v) &&
+         enc(&m.dO, p.dO);
 }
 
 }  // namespace kda

@@ -32,13 +32,13 @@ def _declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = _declared_functions()
-    assert {"kda_bwd", "kda_fwd_states", "kda_workspace_bytes"} <= names
+    assert {"kda_bwd", "kda_fwd", "kda_fwd_states", "kda_workspace_bytes"} <= names
     for n in sorted(names):
         assert hasattr(L, n), f"{n} declared in include/ but not exported"
 
 
 def test_abi_version_and_strings(L):
-    assert L.kda_abi_version() == 2
+    assert L.kda_abi_version() == 3
     for st in range(7):
         assert len(L.kda_status_str(st)) > 0
 
@@ -109,3 +109,23 @@ def test_host_cu_seqlens_check(L):
     assert kda.check_cu_seqlens_host(good, 71) == 1
     assert kda.check_cu_seqlens_host(torch.tensor([1, 5, 70], dtype=torch.int32), 70) == 1
     assert kda.check_cu_seqlens_host(torch.tensor([0, 9, 5, 70], dtype=torch.int32), 70) == 1
+
+
+def test_fwd_argument_checks(L):
+    s = _shape()
+    fake = ctypes.c_void_p(1 << 20)
+    ws_ok = ctypes.c_size_t(kda.workspace_bytes(s))
+    args = [fake] * 6 + [None, fake, None]  # q k v g beta A_log, h0, o, hT
+    # a required pointer missing, a misaligned one
+    a = list(args); a[7] = None
+    assert L.kda_fwd(ctypes.byref(s), *a, fake, ws_ok, None) == 1
+    a = list(args); a[2] = ctypes.c_void_p((1 << 20) + 2)
+    assert L.kda_fwd(ctypes.byref(s), *a, fake, ws_ok, None) == 1
+    # workspace missing or too small
+    assert L.kda_fwd(ctypes.byref(s), *args, None, ws_ok, None) == 3
+    assert L.kda_fwd(ctypes.byref(s), *args, fake, ctypes.c_size_t(ws_ok.value - 1), None) == 3
+    # the forward runs the bf16, K = V = 128 path only
+    f = _shape(K=64, V=64)
+    assert L.kda_fwd(ctypes.byref(f), *args, fake, ctypes.c_size_t(1 << 40), None) == 2
+    f = _shape(dtype=kda.KDA_FP32, K=64, V=64)
+    assert L.kda_fwd(ctypes.byref(f), *args, fake, ctypes.c_size_t(1 << 40), None) == 2
