@@ -45,6 +45,7 @@ class _Cfg(ctypes.Structure):
         ("normalize", ctypes.c_int),
         ("chunk", ctypes.c_int),
         ("nthreads", ctypes.c_int),
+        ("dt_bias", ctypes.POINTER(ctypes.c_double)),
     ]
 
 
@@ -71,7 +72,7 @@ def _load():
             dp = ctypes.POINTER(ctypes.c_double)
             lib.kda_oracle_forward.argtypes = [ctypes.POINTER(_Cfg)] + [dp] * 10
             lib.kda_oracle_forward.restype = ctypes.c_int
-            lib.kda_oracle_backward.argtypes = [ctypes.POINTER(_Cfg)] + [dp] * 17
+            lib.kda_oracle_backward.argtypes = [ctypes.POINTER(_Cfg)] + [dp] * 18
             lib.kda_oracle_backward.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -91,12 +92,14 @@ def _f64(a):
 
 
 def _cfg(cu_seqlens, H, K, V, scale, eps, gate_mode, erase, normalize, chunk,
-         nthreads):
+         nthreads, dt_bias=None):
+    """The C config; returns it with the arrays it points at (keep them alive)."""
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    db = None if dt_bias is None else _f64(np.reshape(dt_bias, (H, K)))
     c = _Cfg(len(cu) - 1, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
              H, K, V, float(scale), float(eps), int(gate_mode), int(erase),
-             int(normalize), int(chunk), int(nthreads))
-    return c, cu
+             int(normalize), int(chunk), int(nthreads), _ptr(db))
+    return c, (cu, db)
 
 
 def num_chunks(cu_seqlens, chunk):
@@ -107,7 +110,7 @@ def num_chunks(cu_seqlens, chunk):
 
 def forward(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens, scale=None,
             eps=1e-6, gate_mode=0, erase=1, normalize=1, chunk=64,
-            want_chunk_states=False, nthreads=0):
+            want_chunk_states=False, nthreads=0, dt_bias=None):
     """Token-serial fp64 forward.
 
     Returns ``(o, hT, chunk_states)``; ``chunk_states`` is ``[NTc, H, K, V]``
@@ -118,8 +121,9 @@ def forward(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens, scale=None,
     V = v.shape[2]
     if scale is None:
         scale = K ** -0.5
-    c, cu = _cfg(cu_seqlens, H, K, V, scale, eps, gate_mode, erase, normalize,
-                 chunk, nthreads)
+    c, keep = _cfg(cu_seqlens, H, K, V, scale, eps, gate_mode, erase, normalize,
+                   chunk, nthreads, dt_bias)
+    cu = keep[0]
     N = len(cu) - 1
     o = np.zeros((Ttot, H, V))
     hT = np.zeros((N, H, K, V))
@@ -134,10 +138,12 @@ def forward(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens, scale=None,
 
 def backward(q, k, v, g, beta, A_log, h0, dO, dhT, *, cu_seqlens, scale=None,
              eps=1e-6, gate_mode=0, erase=1, normalize=1, chunk=64,
-             want_chunk_dstates=False, nthreads=0):
+             want_chunk_dstates=False, nthreads=0, dt_bias=None):
     """Token-serial fp64 backward.
 
-    Returns a dict with ``dq, dk, dv, dg, dbeta, dA_log, dh0`` and, if asked,
+    ``dt_bias`` (optional, ``[H, K]``) is the gate's per-channel bias,
+    ``gk = -exp(A_log) softplus(g + dt_bias)``.
+    Returns a dict with ``dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dh0`` and, if asked,
     ``chunk_dstates`` ``[NTc, H, K, V]`` (the adjoint of the state at the end
     of every chunk).
     """
@@ -147,20 +153,21 @@ def backward(q, k, v, g, beta, A_log, h0, dO, dhT, *, cu_seqlens, scale=None,
     V = v.shape[2]
     if scale is None:
         scale = K ** -0.5
-    c, cu = _cfg(cu_seqlens, H, K, V, scale, eps, gate_mode, erase, normalize,
-                 chunk, nthreads)
+    c, keep = _cfg(cu_seqlens, H, K, V, scale, eps, gate_mode, erase, normalize,
+                   chunk, nthreads, dt_bias)
+    cu = keep[0]
     N = len(cu) - 1
     out = dict(
         dq=np.zeros((Ttot, H, K)), dk=np.zeros((Ttot, H, K)),
         dv=np.zeros((Ttot, H, V)), dg=np.zeros((Ttot, H, K)),
-        dbeta=np.zeros((Ttot, H)), dA_log=np.zeros((H,)),
+        dbeta=np.zeros((Ttot, H)), dA_log=np.zeros((H,)), ddt_bias=np.zeros((H, K)),
         dh0=np.zeros((N, H, K, V)))
     cds = np.zeros((num_chunks(cu, chunk), H, K, V)) if want_chunk_dstates else None
     rc = _load().kda_oracle_backward(
         ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
         _ptr(A_log), _ptr(h0), _ptr(dO), _ptr(dhT), _ptr(out["dq"]),
         _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]),
-        _ptr(out["dA_log"]), _ptr(out["dh0"]), _ptr(cds))
+        _ptr(out["dA_log"]), _ptr(out["ddt_bias"]), _ptr(out["dh0"]), _ptr(cds))
     if rc != 0:
         raise ValueError(f"kda_oracle_backward failed ({rc})")
     if want_chunk_dstates:

@@ -56,10 +56,11 @@ def _unit_chunks(L, C):
 
 
 def backward(q, k, v, g, beta, A_log, h0, dO, dhT, *, cu_seqlens, scale=None,
-             eps=1e-6, chunk=64):
+             eps=1e-6, chunk=64, dt_bias=None):
     """Chunked fp64 backward (and the forward states it needs).
 
-    Returns a dict with dq, dk, dv, dg, dbeta, dA_log, dh0 and the per-chunk
+    ``dt_bias`` (optional ``[H, K]``) enters the gate as softplus(g + dt_bias).
+    Returns a dict with dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dh0 and the per-chunk
     intermediates ``states`` (S_n, state at chunk start) and ``dstates``
     (dS_{n+1}, adjoint of the state at chunk end), both ``[NTc, H, K, V]``.
     """
@@ -75,7 +76,7 @@ def backward(q, k, v, g, beta, A_log, h0, dO, dhT, *, cu_seqlens, scale=None,
     base = np.concatenate([[0], np.cumsum(nck)]).astype(np.int64)
     out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v),
                dg=np.zeros_like(g), dbeta=np.zeros_like(beta),
-               dA_log=np.zeros(H), dh0=np.zeros((N, H, K, V)),
+               dA_log=np.zeros(H), ddt_bias=np.zeros((H, K)), dh0=np.zeros((N, H, K, V)),
                states=np.zeros((int(base[-1]), H, K, V)),
                dstates=np.zeros((int(base[-1]), H, K, V)))
     for sq in range(N):
@@ -83,7 +84,8 @@ def backward(q, k, v, g, beta, A_log, h0, dO, dhT, *, cu_seqlens, scale=None,
         for h in range(H):
             A = np.exp(A_log[h])
             rows = slice(t0, t0 + L)
-            qh, kh, gh = q[rows, h], k[rows, h], g[rows, h]
+            qh, kh = q[rows, h], k[rows, h]
+            gh = g[rows, h] + (0.0 if dt_bias is None else np.asarray(dt_bias, np.float64)[h])
             nq = np.sqrt((qh ** 2).sum(-1, keepdims=True) + eps)
             nk = np.sqrt((kh ** 2).sum(-1, keepdims=True) + eps)
             qn, kn = qh / nq, kh / nk
@@ -146,5 +148,6 @@ def backward(q, k, v, g, beta, A_log, h0, dO, dhT, *, cu_seqlens, scale=None,
             out["dq"][rows, h] = (dqn - qn * (qn * dqn).sum(-1, keepdims=True)) / nq
             out["dk"][rows, h] = (dkn - kn * (kn * dkn).sum(-1, keepdims=True)) / nk
             out["dg"][rows, h] = dgk * (-A) * _sigmoid(gh)
+            out["ddt_bias"][h] += out["dg"][rows, h].sum(0)
             out["dA_log"][h] += np.sum(dgk * gk)
     return out

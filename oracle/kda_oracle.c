@@ -13,9 +13,11 @@
  *       (the in-kernel L2 norm whose backward the kernel-B guide inlines in
  *        its B3 epilogue: "bwd-kernelB-beginner-guide-full", Part 2, B3,
  *        optimisation 4 and 7)
- *   gk_t = -exp(A_log[h]) * softplus(g_t)          (per channel, K values)
- *       (A_log is a learned per-head scalar: same guide, B3 optimisation 7,
- *        where dA_log is reduced to one scalar per head)
+ *   gk_t = -exp(A_log[h]) * softplus(g_t + dt_bias[h])   (per channel, K values)
+ *       (A_log is a learned per-head scalar and dt_bias a learned per-channel
+ *        bias of the gate: same guide, B3 optimisation 7, where the reverse
+ *        cumulative sum accumulates dA_log, one scalar per head, and
+ *        ddt_bias, one value per channel; dt_bias is nullable = 0)
  *   a_t  = exp(gk_t)
  *   S'_t = Diag(a_t) S_{t-1}
  *   delta_t = v_t - S'_t^T k^_t
@@ -62,7 +64,13 @@ typedef struct {
   int chunk;                 /* checkpoint spacing and chunk size of the
                                 optional per-chunk state outputs (> 0) */
   int nthreads;              /* OpenMP threads (<= 0: runtime default) */
+  const double *dt_bias;     /* nullable [H, K]: bias added to g inside softplus */
 } kda_oracle_cfg;
+
+/* the gate pre-activation g_t[i] + dt_bias[h][i] of token element `off` */
+static double gate_x(const kda_oracle_cfg *c, const double *g, size_t off, int h, int i) {
+  return g[off + i] + (c->dt_bias ? c->dt_bias[(size_t)h * c->K + i] : 0.0);
+}
 
 static double softplus(double x) {
   /* log(1 + e^x) written without overflow */
@@ -110,7 +118,7 @@ static void prep_unit(const kda_oracle_cfg *c, int s, int h, const double *q,
       p->qn[(size_t)t * K + i] = q[off + i] / nq;
       p->kn[(size_t)t * K + i] = k[off + i] / nk;
       p->gk[(size_t)t * K + i] =
-          c->gate_mode == 0 ? -A * softplus(g[off + i]) : g[off + i];
+          c->gate_mode == 0 ? -A * softplus(gate_x(c, g, off, h, i)) : g[off + i];
     }
   }
 }
@@ -205,7 +213,8 @@ int kda_oracle_forward(const kda_oracle_cfg *c, const double *q,
 
 /* ------------------------------------------------------------------------ */
 /* Backward.  Outputs (all overwritten): dq, dk, dg [Ttot,H,K]; dv [Ttot,H,V];*/
-/* dbeta [Ttot,H]; dA_log [H] (summed over sequences and tokens); dh0        */
+/* dbeta [Ttot,H]; dA_log [H] (summed over sequences and tokens); ddt_bias  */
+/* [H,K] (nullable; summed over sequences and tokens); dh0                   */
 /* [N,H,K,V] (nullable); chunk_dstates (nullable) [NTc,H,K,V]: the gradient  */
 /* with respect to the state at the END of each chunk, i.e. the adjoint that */
 /* enters that chunk's reverse walk.                                         */
@@ -215,8 +224,8 @@ int kda_oracle_backward(const kda_oracle_cfg *c, const double *q,
                         const double *beta, const double *A_log,
                         const double *h0, const double *dO, const double *dhT,
                         double *dq, double *dk, double *dv, double *dg,
-                        double *dbeta, double *dA_log, double *dh0,
-                        double *chunk_dstates) {
+                        double *dbeta, double *dA_log, double *ddt_bias,
+                        double *dh0, double *chunk_dstates) {
   const int H = c->H, K = c->K, V = c->V, N = c->num_seqs, C = c->chunk;
   if (N < 0 || H <= 0 || K <= 0 || V <= 0 || C <= 0) return 1;
   int64_t *chunk_base = (int64_t *)malloc(sizeof(int64_t) * (N + 1));
@@ -228,6 +237,8 @@ int kda_oracle_backward(const kda_oracle_cfg *c, const double *q,
   }
   /* per-unit dA_log contributions, summed in a fixed order afterwards */
   double *dA_unit = (double *)calloc((size_t)(N > 0 ? N : 1) * H, sizeof(double));
+  /* per-unit ddt_bias contributions, the same way */
+  double *db_unit = (double *)calloc((size_t)(N > 0 ? N : 1) * H * K, sizeof(double));
 #ifdef _OPENMP
   if (c->nthreads > 0) omp_set_num_threads(c->nthreads);
 #pragma omp parallel for schedule(dynamic, 1)
@@ -368,7 +379,9 @@ int kda_oracle_backward(const kda_oracle_cfg *c, const double *q,
         }
         const double d = dgk[(size_t)t * K + i];
         if (c->gate_mode == 0) {
-          dg[off + i] = d * (-A) * sigmoid(g[off + i]);  /* d softplus = sigmoid */
+          /* d softplus = sigmoid; the bias enters like g */
+          dg[off + i] = d * (-A) * sigmoid(gate_x(c, g, off, h, i));
+          db_unit[(size_t)u * K + i] += dg[off + i];
           dA += d * p.gk[(size_t)t * K + i];             /* d gk / d A_log = gk */
         } else {
           dg[off + i] = d;
@@ -388,9 +401,17 @@ int kda_oracle_backward(const kda_oracle_cfg *c, const double *q,
       for (int s = 0; s < N; ++s) acc += dA_unit[(size_t)s * H + h];
       dA_log[h] = acc;
     }
+  if (ddt_bias)
+    for (int h = 0; h < H; ++h)
+      for (int i = 0; i < K; ++i) {
+        double acc = 0.0;
+        for (int s = 0; s < N; ++s) acc += db_unit[((size_t)s * H + h) * K + i];
+        ddt_bias[(size_t)h * K + i] = acc;
+      }
   free(dA_unit);
+  free(db_unit);
   free(chunk_base);
   return 0;
 }
 
-int kda_oracle_abi_version(void) { return 1; }
+int kda_oracle_abi_version(void) { return 2; }

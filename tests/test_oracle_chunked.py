@@ -37,3 +37,18 @@ def test_chunked_equals_token_serial(C, cu):
                                   d["h0"], cu_seqlens=cu, chunk=C, want_chunk_states=True)
     np.testing.assert_allclose(got["states"], states, rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(got["dstates"], ref["chunk_dstates"], rtol=1e-10, atol=1e-12)
+
+
+def test_chunked_equals_token_serial_with_gate_bias():
+    rng = np.random.default_rng(3)
+    cu = [0, 1, 63, 128, 193]
+    H, K, V = 2, 8, 6
+    d = _inputs(rng, cu[-1], H, K, V, len(cu) - 1)
+    b = rng.standard_normal((H, K))
+    ref = oracle.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"],
+                          d["dO"], d["dhT"], cu_seqlens=cu, chunk=16, dt_bias=b)
+    got = chunked.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"],
+                           d["dO"], d["dhT"], cu_seqlens=cu, chunk=16, dt_bias=b)
+    for key in KEYS + ("ddt_bias",):
+        err = np.linalg.norm(got[key] - ref[key]) / np.linalg.norm(ref[key])
+        assert err < 1e-10, (key, err)

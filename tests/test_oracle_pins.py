@@ -38,7 +38,7 @@ def _rand_inputs(rng, Ttot, H, K, V, N=1, h0=True, dhT=True):
 def _loss(inp, cu, **kw):
     o, hT, _ = oracle.forward(inp["q"], inp["k"], inp["v"], inp["g"],
                               inp["beta"], inp["A_log"], inp["h0"],
-                              cu_seqlens=cu, **kw)
+                              cu_seqlens=cu, dt_bias=inp.get("dt_bias"), **kw)
     L = float(np.sum(o * inp["dO"]))
     if inp["dhT"] is not None:
         L += float(np.sum(hT * inp["dhT"]))
@@ -48,17 +48,17 @@ def _loss(inp, cu, **kw):
 def _grads(inp, cu, **kw):
     return oracle.backward(inp["q"], inp["k"], inp["v"], inp["g"],
                            inp["beta"], inp["A_log"], inp["h0"], inp["dO"],
-                           inp["dhT"], cu_seqlens=cu, **kw)
+                           inp["dhT"], cu_seqlens=cu, dt_bias=inp.get("dt_bias"), **kw)
 
 
 GRAD_OF = dict(q="dq", k="dk", v="dv", g="dg", beta="dbeta", A_log="dA_log",
-               h0="dh0")
+               h0="dh0", dt_bias="ddt_bias")
 
 
 def _fd_check(inp, cu, max_elems=48, step=1e-6, tol=1e-6, rng=RNG, **kw):
     an = _grads(inp, cu, **kw)
     for name, gname in GRAD_OF.items():
-        if inp[name] is None:
+        if inp.get(name) is None:
             continue
         x = inp[name]
         flat = x.reshape(-1)
@@ -105,6 +105,34 @@ def test_fd_erase_off_and_raw_gate():
     inp = _rand_inputs(rng, 12, 2, 4, 4)
     inp["g"] = -np.abs(inp["g"])
     _fd_check(inp, [0, 12], chunk=4, gate_mode=1, erase=0, rng=rng)
+
+
+def test_fd_gate_bias():
+    # the gate's per-channel bias: gk = -exp(A_log) softplus(g + dt_bias)
+    rng = np.random.default_rng(17)
+    cu = [0, 7, 19, 20]
+    inp = _rand_inputs(rng, 20, 2, 4, 5, N=3)
+    inp["dt_bias"] = rng.standard_normal((2, 4))
+    _fd_check(inp, cu, chunk=4, rng=rng)
+
+
+def test_gate_bias_is_a_shift_of_g():
+    # the bias only shifts g inside softplus: (g, b) and (g + b, 0) are the
+    # same model with the same gradients (ddt_bias included, it is the sum of
+    # dg); and no bias at all equals a zero bias
+    rng = np.random.default_rng(19)
+    cu = [0, 9, 30]
+    inp = _rand_inputs(rng, 30, 2, 4, 4, N=2)
+    b = rng.standard_normal((2, 4))
+    ref = _grads(dict(inp, dt_bias=b), cu, chunk=8)
+    shifted = dict(inp, g=inp["g"] + b[None], dt_bias=np.zeros((2, 4)))
+    got = _grads(shifted, cu, chunk=8)
+    for key in ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "dh0", "ddt_bias"):
+        np.testing.assert_allclose(got[key], ref[key], rtol=1e-12, atol=1e-12)
+    plain = _grads(inp, cu, chunk=8)
+    zero = _grads(dict(inp, dt_bias=np.zeros((2, 4))), cu, chunk=8)
+    for key in ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "dh0", "ddt_bias"):
+        np.testing.assert_array_equal(plain[key], zero[key])
 
 
 def test_beta_zero_closed_form():
