@@ -3,11 +3,14 @@
  *
  * The operation.  Per sequence and head, with t the token index,
  *   q^_t = q_t / sqrt(|q_t|^2 + l2_eps), k^_t likewise      (in-library L2 norm)
- *   gk_t = -exp(A_log[h]) * softplus(g_t)                     (per-channel log-decay)
+ *   gk_t = -exp(A_log[h]) * softplus(g_t + dt_bias[h])        (per-channel log-decay)
  *   S_t  = (I - beta_t k^_t k^_t^T) Diag(exp(gk_t)) S_{t-1} + beta_t k^_t v_t^T
  *   o_t  = scale * S_t^T q^_t,     S_0 = h0
  * and kda_bwd returns the gradients of  sum_t <dO_t, o_t> + <dh_T, S_T>  with
- * respect to q, k, v, g, beta, A_log and h0.
+ * respect to q, k, v, g, beta, A_log, dt_bias and h0.  dt_bias, the gate's
+ * per-channel bias (the kernel-B guide, Part 2, B3 optimisation 7: the
+ * reverse cumulative sum accumulates dA_log and ddt_bias), is optional: a
+ * NULL dt_bias is a zero bias, and a NULL ddt_bias skips that gradient.
  * The work is the chunked backward described on the pages
  * "bwd-kernelB-beginner-guide-full" (Part 1: the per-chunk gradient kernel
  * B1/B2/B0/B3 and its outputs dq, dk, dv, dbeta, dg, dA_log; Part 2, B3:
@@ -23,6 +26,7 @@
  *      v, dO, dv           : [B, T, H, V]
  *      beta, dbeta         : [B, T, H]
  *      A_log, dA_log       : [H] fp32
+ *      dt_bias, ddt_bias   : [H, K] fp32
  *      h0, hT, dh_T, dh0   : [N, H, K, V] fp32, N = B (fixed length) or
  *                            num_seqs (varlen)
  *    q, k, v, g, beta, dO and the gradients dq, dk, dv, dg, dbeta all have the
@@ -90,7 +94,8 @@ int64_t kda_num_chunk_slots(const kda_shape *shape);
 
 /* Bytes of workspace kda_bwd needs: the per-chunk states (dtype of the
  * shape, [slots, H, K, V]) unless the caller passes them, the per-chunk
- * state gradients dS (same size), per-chunk dA_log partials and, for bf16
+ * state gradients dS (same size), per-chunk dA_log and ddt_bias partials
+ * ([slots, H] and [slots, H, K] fp32) and, for bf16
  * with K = V = 128, the per-chunk operand blocks of the tensor-core scans
  * (98816 bytes per slot and head).  Returns 0 on a bad shape. */
 size_t kda_workspace_bytes(const kda_shape *shape);
@@ -110,8 +115,8 @@ size_t kda_workspace_dstates_offset(const kda_shape *shape);
  *   hT     : nullable OUT fp32 [N, H, K, V]: the final state of each sequence.
  * No workspace is needed. */
 kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v,
-                          const void *g, const void *beta,
-                          const float *A_log, const float *h0, void *states,
+                          const void *g, const void *beta, const float *A_log,
+                          const float *dt_bias, const float *h0, void *states,
                           float *hT, kda_stream_t stream);
 
 /* Forward pass: the read-out o_t = scale * S_t^T q^_t of every token and the
@@ -127,13 +132,15 @@ kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v,
  *            256-byte aligned (the layout kda_bwd uses; its dS part is unused).
  * q, k, v, g, beta and A_log are required. */
 kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const void *v,
-                   const void *g, const void *beta, const float *A_log, const float *h0,
-                   void *o, float *hT, void *ws, size_t ws_bytes, kda_stream_t stream);
+                   const void *g, const void *beta, const float *A_log,
+                   const float *dt_bias, const float *h0, void *o, float *hT, void *ws,
+                   size_t ws_bytes, kda_stream_t stream);
 
 /* Backward pass.
  *   dh_T   : nullable (zero), fp32 [N, H, K, V].
  *   dq, dk, dv, dg, dbeta : OUT, overwritten, dtype of the shape.
  *   dA_log : OUT fp32 [H], overwritten (summed over sequences and tokens).
+ *   ddt_bias : nullable OUT fp32 [H, K], overwritten (summed likewise).
  *   dh0    : nullable OUT fp32 [N, H, K, V].
  *   states : nullable; the output of kda_fwd_states for the same inputs.
  *            NULL recomputes them inside the workspace.
@@ -142,23 +149,24 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
  * q, k, v, g, beta, A_log and dO are required. */
 kda_status kda_bwd(const kda_shape *shape, const void *q, const void *k,
                    const void *v, const void *g, const void *beta,
-                   const float *A_log, const float *h0, const void *dO,
-                   const float *dh_T, void *dq, void *dk, void *dv, void *dg,
-                   void *dbeta, float *dA_log, float *dh0, const void *states,
-                   void *ws, size_t ws_bytes, kda_stream_t stream);
+                   const float *A_log, const float *dt_bias, const float *h0,
+                   const void *dO, const float *dh_T, void *dq, void *dk, void *dv,
+                   void *dg, void *dbeta, float *dA_log, float *ddt_bias, float *dh0,
+                   const void *states, void *ws, size_t ws_bytes, kda_stream_t stream);
 
 /* kda_bwd with phase timing: `events` (nullable) points at 5 cudaEvent_t
  * created by the caller (timing enabled).  They are recorded on `stream`
  * at the start of the call, after the per-chunk prep (bf16, K = V = 128;
  * otherwise right after the first), after the chunk scans (forward-state
  * recompute and reverse dS scan), after the per-chunk gradient kernel and
- * at the end (after the dA_log reduction).  Otherwise identical to kda_bwd. */
+ * at the end (after the dA_log and ddt_bias reductions).  Otherwise identical
+ * to kda_bwd. */
 kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k,
                          const void *v, const void *g, const void *beta,
-                         const float *A_log, const float *h0, const void *dO,
-                         const float *dh_T, void *dq, void *dk, void *dv, void *dg,
-                         void *dbeta, float *dA_log, float *dh0, const void *states,
-                         void *ws, size_t ws_bytes, kda_stream_t stream,
+                         const float *A_log, const float *dt_bias, const float *h0,
+                         const void *dO, const float *dh_T, void *dq, void *dk, void *dv,
+                         void *dg, void *dbeta, float *dA_log, float *ddt_bias, float *dh0,
+                         const void *states, void *ws, size_t ws_bytes, kda_stream_t stream,
                          void *const *events);
 
 /* Backward pass for callers that cannot allocate device memory (no
@@ -168,7 +176,7 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k,
  * only use memory reserved up front, or plugin hosts that expose no
  * allocation API.  This entry point takes the same inputs and outputs as
  * kda_bwd (states always recomputed) but keeps its scratch -- the per-chunk
- * states, state gradients and dA_log partials -- in a fixed array of
+ * states, state gradients and dA_log / ddt_bias partials -- in a fixed array of
  * kda_noalloc_scratch_bytes() bytes (64 MiB) compiled into the library.
  * That array exists once per GPU that loads the library and stays allocated
  * until the process exits.
@@ -185,9 +193,10 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k,
  *    initial content; each call writes every part it reads. */
 kda_status kda_bwd_noalloc(const kda_shape *shape, const void *q, const void *k,
                            const void *v, const void *g, const void *beta,
-                           const float *A_log, const float *h0, const void *dO,
-                           const float *dh_T, void *dq, void *dk, void *dv, void *dg,
-                           void *dbeta, float *dA_log, float *dh0, kda_stream_t stream);
+                           const float *A_log, const float *dt_bias, const float *h0,
+                           const void *dO, const float *dh_T, void *dq, void *dk, void *dv,
+                           void *dg, void *dbeta, float *dA_log, float *ddt_bias,
+                           float *dh0, kda_stream_t stream);
 
 /* Capacity in bytes of kda_bwd_noalloc's fixed scratch array. */
 size_t kda_noalloc_scratch_bytes(void);

@@ -67,15 +67,15 @@ def lib():
         L.kda_workspace_bytes.restype = ctypes.c_size_t
         L.kda_workspace_dstates_offset.argtypes = [S]
         L.kda_workspace_dstates_offset.restype = ctypes.c_size_t
-        L.kda_fwd_states.argtypes = [S] + [_VP] * 9
+        L.kda_fwd_states.argtypes = [S] + [_VP] * 10
         L.kda_fwd_states.restype = ctypes.c_int
-        L.kda_fwd.argtypes = [S] + [_VP] * 10 + [ctypes.c_size_t, _VP]
+        L.kda_fwd.argtypes = [S] + [_VP] * 11 + [ctypes.c_size_t, _VP]
         L.kda_fwd.restype = ctypes.c_int
-        L.kda_bwd.argtypes = [S] + [_VP] * 18 + [ctypes.c_size_t, _VP]
+        L.kda_bwd.argtypes = [S] + [_VP] * 20 + [ctypes.c_size_t, _VP]
         L.kda_bwd.restype = ctypes.c_int
-        L.kda_bwd_timed.argtypes = [S] + [_VP] * 18 + [ctypes.c_size_t, _VP, _VP]
+        L.kda_bwd_timed.argtypes = [S] + [_VP] * 20 + [ctypes.c_size_t, _VP, _VP]
         L.kda_bwd_timed.restype = ctypes.c_int
-        L.kda_bwd_noalloc.argtypes = [S] + [_VP] * 16 + [_VP]
+        L.kda_bwd_noalloc.argtypes = [S] + [_VP] * 18 + [_VP]
         L.kda_bwd_noalloc.restype = ctypes.c_int
         L.kda_noalloc_scratch_bytes.argtypes = []
         L.kda_noalloc_scratch_bytes.restype = ctypes.c_size_t
@@ -144,7 +144,7 @@ def _nseq(B, cu_seqlens):
 
 
 def fwd_states(k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None, l2_eps=None,
-               states=None, hT=None, want_hT=False):
+               states=None, hT=None, want_hT=False, dt_bias=None):
     """Chunk-start states ``[slots, H, K, V]`` (dtype of k) and optionally hT."""
     shape = make_shape(k, v, cu_seqlens=cu_seqlens, scale=scale, l2_eps=l2_eps)
     B, T, H, K = k.shape
@@ -154,15 +154,17 @@ def fwd_states(k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None, l2
     if want_hT and hT is None:
         hT = torch.empty((_nseq(B, cu_seqlens), H, K, V), dtype=torch.float32, device=k.device)
     st = lib().kda_fwd_states(ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                              _ptr(A_log), _ptr(h0), _ptr(states), _ptr(hT), _stream())
+                              _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(states), _ptr(hT),
+                              _stream())
     _check(st, "kda_fwd_states")
     return (states, hT) if want_hT else states
 
 
 def fwd(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None, l2_eps=None,
-        o=None, hT=None, want_hT=False, workspace=None):
+        o=None, hT=None, want_hT=False, workspace=None, dt_bias=None):
     """Forward read-out ``o`` [B, T, H, V] (bf16, K = V = 128) and, if asked,
-    the final states ``hT`` [N, H, K, V] fp32: ``(o, hT)`` or ``o``."""
+    the final states ``hT`` [N, H, K, V] fp32: ``(o, hT)`` or ``o``.
+    ``dt_bias`` (optional fp32 [H, K]) is the gate's per-channel bias."""
     shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2_eps=l2_eps)
     B, T, H, K = q.shape
     V = v.shape[-1]
@@ -174,15 +176,17 @@ def fwd(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None, l2_eps
     if workspace is None:
         workspace = torch.empty((workspace_bytes(shape),), dtype=torch.uint8, device=dev)
     st = lib().kda_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                       _ptr(A_log), _ptr(h0), _ptr(o), _ptr(hT), _ptr(workspace),
+                       _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(o), _ptr(hT),
+                       _ptr(workspace),
                        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream())
     _check(st, "kda_fwd")
     return (o, hT) if want_hT else o
 
 
 def bwd(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, cu_seqlens=None, scale=None,
-        l2_eps=None, states=None, out=None, workspace=None, events=None):
-    """Gradients ``dict(dq, dk, dv, dg, dbeta, dA_log, dh0)``.
+        l2_eps=None, states=None, out=None, workspace=None, events=None, dt_bias=None):
+    """Gradients ``dict(dq, dk, dv, dg, dbeta, dA_log, dh0)``, plus ``ddt_bias``
+    [H, K] fp32 when ``dt_bias`` (the gate's per-channel bias) is given.
 
     ``out`` may hold preallocated output tensors under the same keys and
     ``workspace`` a uint8 CUDA tensor of at least ``workspace_bytes`` bytes.
@@ -202,6 +206,8 @@ def bwd(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, cu_seqlens=None, scale=No
     o.setdefault("dg", torch.empty_like(g))
     o.setdefault("dbeta", torch.empty_like(beta))
     o.setdefault("dA_log", torch.empty((H,), dtype=torch.float32, device=dev))
+    if dt_bias is not None:
+        o.setdefault("ddt_bias", torch.empty((H, K), dtype=torch.float32, device=dev))
     o.setdefault("dh0", torch.empty((_nseq(B, cu_seqlens), H, K, V), dtype=torch.float32,
                                     device=dev))
     need = workspace_bytes(shape)
@@ -213,9 +219,10 @@ def bwd(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, cu_seqlens=None, scale=No
             raise ValueError("events: 5 timing events expected")
         ev = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     st = lib().kda_bwd_timed(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                             _ptr(beta), _ptr(A_log), _ptr(h0), _ptr(dO), _ptr(dh_T),
-                             _ptr(o["dq"]), _ptr(o["dk"]), _ptr(o["dv"]), _ptr(o["dg"]),
-                             _ptr(o["dbeta"]), _ptr(o["dA_log"]), _ptr(o["dh0"]),
+                             _ptr(beta), _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(dO),
+                             _ptr(dh_T), _ptr(o["dq"]), _ptr(o["dk"]), _ptr(o["dv"]),
+                             _ptr(o["dg"]), _ptr(o["dbeta"]), _ptr(o["dA_log"]),
+                             _ptr(o.get("ddt_bias")), _ptr(o["dh0"]),
                              _ptr(states), _ptr(workspace),
                              ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                              _stream(), ev)
@@ -230,17 +237,18 @@ def noalloc_scratch_bytes() -> int:
 
 
 def bwd_noalloc(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, out, cu_seqlens=None,
-                scale=None, l2_eps=None):
+                scale=None, l2_eps=None, dt_bias=None):
     """Backward pass through ``kda_bwd_noalloc``: for callers that cannot
     allocate device memory, the library uses its own fixed scratch array
     instead of a caller workspace.  ``out`` must hold preallocated dq, dk,
-    dv, dg, dbeta, dA_log and dh0; nothing is allocated here.  Raises
+    dv, dg, dbeta, dA_log and dh0 (and ddt_bias for a ``dt_bias``); nothing is
+    allocated here.  Raises
     KdaError(7) when the problem does not fit the scratch array."""
     shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2_eps=l2_eps)
     st = lib().kda_bwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                               _ptr(beta), _ptr(A_log), _ptr(h0), _ptr(dO), _ptr(dh_T),
-                               _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                               _ptr(beta), _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(dO),
+                               _ptr(dh_T), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
                                _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["dA_log"]),
-                               _ptr(out.get("dh0")), _stream())
+                               _ptr(out.get("ddt_bias")), _ptr(out.get("dh0")), _stream())
     _check(st, "kda_bwd_noalloc")
     return out

@@ -93,11 +93,21 @@ bool legacy_scan() {
 
 kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+// Workspace layout: states | dS | dA_log partials [slots, H] | ddt_bias
+// partials [slots, H, K] | per-chunk operand blocks (tcgen05 path).
+size_t dA_part_offset(const kda_shape *s) { return 2 * states_bytes(s); }
+size_t ddt_part_offset(const kda_shape *s) {
+  return dA_part_offset(s) + round_up((size_t)slots_of(s) * s->H * sizeof(float));
+}
+size_t prep_offset(const kda_shape *s) {
+  return ddt_part_offset(s) + round_up((size_t)slots_of(s) * s->H * s->K * sizeof(float));
+}
+
 }  // namespace
 
 extern "C" {
 
-int kda_abi_version(void) { return 3; }
+int kda_abi_version(void) { return 4; }
 
 const char *kda_status_str(kda_status st) {
   switch (st) {
@@ -125,8 +135,7 @@ size_t kda_workspace_dstates_offset(const kda_shape *shape) {
 
 size_t kda_workspace_bytes(const kda_shape *shape) {
   if (check_shape(shape) != KDA_OK) return 0;
-  const size_t part = round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
-  return 2 * states_bytes(shape) + part + prep_bytes(shape);
+  return prep_offset(shape) + prep_bytes(shape);
 }
 
 kda_status kda_check_cu_seqlens_host(const int32_t *cu, int num_seqs, int total_T) {
@@ -138,14 +147,14 @@ kda_status kda_check_cu_seqlens_host(const int32_t *cu, int num_seqs, int total_
 }
 
 kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v, const void *g,
-                          const void *beta, const float *A_log, const float *h0, void *states,
-                          float *hT, kda_stream_t stream) {
+                          const void *beta, const float *A_log, const float *dt_bias,
+                          const float *h0, void *states, float *hT, kda_stream_t stream) {
   kda_status st = check_shape(shape);
   if (st != KDA_OK) return st;
   const bool tokens = (int64_t)shape->B * shape->T > 0;
   if (!A_log) return KDA_ERR_INVALID_ARG;
   if (tokens && (!k || !v || !g || !beta || !states)) return KDA_ERR_INVALID_ARG;
-  const void *ptrs[] = {k, v, g, beta, A_log, h0, states, hT};
+  const void *ptrs[] = {k, v, g, beta, A_log, dt_bias, h0, states, hT};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
   kda::KdaParams p;
@@ -155,6 +164,7 @@ kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v, 
   p.g = g;
   p.beta = beta;
   p.A_log = A_log;
+  p.dt_bias = dt_bias;
   p.h0 = h0;
   p.states = states;
   p.hT = hT;
@@ -166,15 +176,16 @@ kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v, 
 }
 
 kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const void *v,
-                   const void *g, const void *beta, const float *A_log, const float *h0, void *o,
-                   float *hT, void *ws, size_t ws_bytes, kda_stream_t stream) {
+                   const void *g, const void *beta, const float *A_log, const float *dt_bias,
+                   const float *h0, void *o, float *hT, void *ws, size_t ws_bytes,
+                   kda_stream_t stream) {
   kda_status st = check_shape(shape);
   if (st != KDA_OK) return st;
   if (!tc_state_path(shape)) return KDA_ERR_UNSUPPORTED;
   const bool tokens = (int64_t)shape->B * shape->T > 0;
   if (!A_log) return KDA_ERR_INVALID_ARG;
   if (tokens && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
-  const void *ptrs[] = {q, k, v, g, beta, A_log, h0, o, hT};
+  const void *ptrs[] = {q, k, v, g, beta, A_log, dt_bias, h0, o, hT};
   for (const void *ptr : ptrs)
     if (ptr && !aligned16(ptr)) return KDA_ERR_INVALID_ARG;
   const size_t need = kda_workspace_bytes(shape);
@@ -192,13 +203,14 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
   p.g = g;
   p.beta = beta;
   p.A_log = A_log;
+  p.dt_bias = dt_bias;
   p.h0 = h0;
   p.hT = hT;
   p.states = w;  // packed chunk states, as kda_bwd keeps them
-  p.dA_part = reinterpret_cast<float *>(w + 2 * sb);
+  p.dA_part = reinterpret_cast<float *>(w + dA_part_offset(shape));
   kda::TokenMaps tm;
   if (!kda::encode_token_maps(p, tm)) return KDA_ERR_CUDA;
-  void *prep = w + 2 * sb + round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
+  void *prep = w + prep_offset(shape);
   p.prep = static_cast<const char *>(prep);
   // 1. per-chunk operands, 2. forward state scan (S_n of every chunk, hT),
   // 3. the chunk outputs
@@ -215,18 +227,19 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
 }
 
 kda_status kda_bwd(const kda_shape *shape, const void *q, const void *k, const void *v,
-                   const void *g, const void *beta, const float *A_log, const float *h0,
-                   const void *dO, const float *dh_T, void *dq, void *dk, void *dv, void *dg,
-                   void *dbeta, float *dA_log, float *dh0, const void *states, void *ws,
-                   size_t ws_bytes, kda_stream_t stream) {
-  return kda_bwd_timed(shape, q, k, v, g, beta, A_log, h0, dO, dh_T, dq, dk, dv, dg, dbeta,
-                       dA_log, dh0, states, ws, ws_bytes, stream, nullptr);
+                   const void *g, const void *beta, const float *A_log, const float *dt_bias,
+                   const float *h0, const void *dO, const float *dh_T, void *dq, void *dk,
+                   void *dv, void *dg, void *dbeta, float *dA_log, float *ddt_bias, float *dh0,
+                   const void *states, void *ws, size_t ws_bytes, kda_stream_t stream) {
+  return kda_bwd_timed(shape, q, k, v, g, beta, A_log, dt_bias, h0, dO, dh_T, dq, dk, dv, dg,
+                       dbeta, dA_log, ddt_bias, dh0, states, ws, ws_bytes, stream, nullptr);
 }
 
 kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, const void *v,
-                         const void *g, const void *beta, const float *A_log, const float *h0,
-                         const void *dO, const float *dh_T, void *dq, void *dk, void *dv,
-                         void *dg, void *dbeta, float *dA_log, float *dh0, const void *states,
+                         const void *g, const void *beta, const float *A_log,
+                         const float *dt_bias, const float *h0, const void *dO,
+                         const float *dh_T, void *dq, void *dk, void *dv, void *dg, void *dbeta,
+                         float *dA_log, float *ddt_bias, float *dh0, const void *states,
                          void *ws, size_t ws_bytes, kda_stream_t stream, void *const *events) {
   kda_status st = check_shape(shape);
   if (st != KDA_OK) return st;
@@ -235,8 +248,8 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
   if (!A_log || !dA_log) return KDA_ERR_INVALID_ARG;
   if (tokens && (!q || !k || !v || !g || !beta || !dO || !dq || !dk || !dv || !dg || !dbeta))
     return KDA_ERR_INVALID_ARG;
-  const void *ptrs[] = {q, k, v, g, beta, A_log, h0, dO, dh_T, dq, dk, dv, dg, dbeta, dA_log,
-                        dh0, states};
+  const void *ptrs[] = {q, k, v, g, beta, A_log, dt_bias, h0, dO, dh_T, dq, dk, dv, dg, dbeta,
+                        dA_log, ddt_bias, dh0, states};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
   const size_t need = kda_workspace_bytes(shape);
@@ -255,6 +268,7 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
   p.beta = beta;
   p.dO = dO;
   p.A_log = A_log;
+  p.dt_bias = dt_bias;
   p.h0 = h0;
   p.dhT = dh_T;
   p.states = states ? const_cast<void *>(states) : w;
@@ -266,8 +280,10 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
   p.dv = dv;
   p.dg = dg;
   p.dbeta = dbeta;
-  p.dA_part = reinterpret_cast<float *>(w + 2 * sb);
+  p.dA_part = reinterpret_cast<float *>(w + dA_part_offset(shape));
   p.dA_log = dA_log;
+  p.ddt_part = reinterpret_cast<float *>(w + ddt_part_offset(shape));
+  p.ddt_bias = ddt_bias;
   const bool bf = shape->dtype == KDA_BF16;
   auto mark = [&](int i) {
     if (events != nullptr && events[i] != nullptr)
@@ -283,7 +299,7 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
     // TMA maps of the token-major inputs, and the per-chunk operands for the
     // tcgen05 scans and the gradient kernel
     if (!kda::encode_token_maps(p, tm)) return KDA_ERR_CUDA;
-    void *prep = w + 2 * sb + round_up((size_t)slots_of(shape) * shape->H * sizeof(float));
+    void *prep = w + prep_offset(shape);
     p.prep = static_cast<const char *>(prep);
     e = kda::prep_tc_launch(p, tm, prep, cs);
   }

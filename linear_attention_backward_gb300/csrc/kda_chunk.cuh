@@ -47,6 +47,12 @@ __device__ __forceinline__ bool seq_bounds(const KdaParams &p, int s, int64_t &t
 }
 
 // Inverse of the slot map: the sequence and chunk index that own `slot`.
+// The gate's bias for head h, channel c (zero without one): the gate is
+// gk = -exp(A_log[h]) * softplus(g + dt_bias[h][c]).
+__device__ __forceinline__ float gate_bias(const KdaParams &p, int h, int c, int K) {
+  return p.dt_bias != nullptr ? p.dt_bias[h * K + c] : 0.f;
+}
+
 __device__ __forceinline__ bool slot_owner(const KdaParams &p, int64_t slot, int &s, int &j,
                                            int64_t &tok0, int &len) {
   int64_t t0;
@@ -233,13 +239,14 @@ __device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, cons
   const int I = r0 >> 4;  // 16-row block of this segment
   float g0[ROWS], g1[ROWS];
   float run0 = 0.f, run1 = 0.f;
+  const float bias0 = gate_bias(p, h, c, K), bias1 = gate_bias(p, h, c + 1, K);
 #pragma unroll
   for (int r = 0; r < ROWS; ++r) {
     const int i = r0 + r;
     const float2 gv = load2(Gr + i * K + c);
     const bool ok = i < len;
-    run0 += ok ? -A * softplus_f(gv.x) : 0.f;
-    run1 += ok ? -A * softplus_f(gv.y) : 0.f;
+    run0 += ok ? -A * softplus_f(gv.x + bias0) : 0.f;
+    run1 += ok ? -A * softplus_f(gv.y + bias1) : 0.f;
     g0[r] = run0;
     g1[r] = run1;
   }

@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
   int64_t tok0;
   if (!slot_owner(p, slot, s, j, tok0, len)) {
     if (tid == 0) p.dA_part[slot * H + h] = 0.f;
+    if (p.ddt_part != nullptr && tid < D) p.ddt_part[(slot * H + h) * D + tid] = 0.f;
     return;
   }
   (void)s;
@@ -487,15 +488,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
     float run = dgT[c];
     for (int q2 = part + 1; q2 < PARTS; ++q2) run += partsum[q2 * D + c];
     const float A = __expf(p.A_log[h]);
-    float dA = 0.f;
+    const float bias = gate_bias(p, h, c, D);
+    float dA = 0.f, ddt = 0.f;
     E *dgg = reinterpret_cast<E *>(p.dg);
     for (int i = ra + SEG - 1; i >= ra; --i) {
       run += dgc[i * LDF + c];
       if (i < len) {
-        const float gv = to_f(Graw[i * D + c]);
+        const float gv = to_f(Graw[i * D + c]) + bias;
         const float gk = -A * softplus_f(gv);
-        dgg[((tok0 + i) * H + h) * D + c] = from_f<E>(run * (-A) * sigmoid_f(gv));
+        const float dgv = run * (-A) * sigmoid_f(gv);
+        dgg[((tok0 + i) * H + h) * D + c] = from_f<E>(dgv);
         dA = fmaf(run, gk, dA);
+        ddt += dgv;
       }
     }
     dA = warp_sum(dA);
@@ -505,6 +509,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
       float t = 0.f;
       for (int w = 0; w < NWARPS; ++w) t += dAred[w];
       p.dA_part[slot * H + h] = t;
+    }
+    if (p.ddt_part != nullptr) {  // ddt_bias partial of the chunk: the dg column sums
+      partsum[part * D + c] = ddt;  // (every thread has read partsum above)
+      __syncthreads();
+      if (part == 0) {
+        float t = 0.f;
+        for (int q2 = 0; q2 < PARTS; ++q2) t += partsum[q2 * D + c];
+        p.ddt_part[(slot * H + h) * D + c] = t;
+      }
     }
   }
 }
@@ -523,6 +536,24 @@ __global__ void kda_dalog_reduce_kernel(const float *part, int64_t nslots, int H
     float x = 0.f;
     for (int w = 0; w < NWARPS; ++w) x += red[w];
     dA[h] = x;
+  }
+}
+
+// Deterministic ddt_bias: one CTA per head, thread (c, r) sums the partials of
+// channel c over the slots s = r, r + R, ... (coalesced over c), then the R
+// sums of each channel in a fixed order.
+__global__ void __launch_bounds__(1024) kda_ddt_reduce_kernel(const float *part, int64_t nslots,
+                                                              int H, int K, float *ddt) {
+  __shared__ float red[1024];
+  const int h = blockIdx.x, c = threadIdx.x, r = threadIdx.y, R = blockDim.y;
+  float t = 0.f;
+  for (int64_t s = r; s < nslots; s += R) t += part[(s * H + h) * K + c];
+  red[r * K + c] = t;
+  __syncthreads();
+  if (r == 0) {
+    float x = 0.f;
+    for (int q = 0; q < R; ++q) x += red[q * K + c];
+    ddt[h * K + c] = x;
   }
 }
 
@@ -556,6 +587,9 @@ static cudaError_t launch_grads(const KdaParams &p, const void *states, cudaStre
   }
   if (after != nullptr) cudaEventRecord(reinterpret_cast<cudaEvent_t>(after), st);
   kda_dalog_reduce_kernel<<<p.H, NTHREADS, 0, st>>>(p.dA_part, p.nslots, p.H, p.dA_log);
+  if (p.ddt_bias != nullptr && p.H > 0)
+    kda_ddt_reduce_kernel<<<p.H, dim3(D, 1024 / D), 0, st>>>(p.ddt_part, p.nslots, p.H, D,
+                                                             p.ddt_bias);
   return cudaGetLastError();
 }
 

@@ -146,6 +146,7 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = tid & 127, I = tid >> 7;
   const float A = __expf(p.A_log[h]);
+  const float bias = gate_bias(p, h, c, D);
   // L2 norms, one warp per row
   for (int i = warp; i < CHUNK; i += NW) {
     float sk = 0.f, sq = 0.f;
@@ -177,7 +178,7 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int i = 16 * I + r;
-      const float gv = BF16_AT(g2, r);
+      const float gv = BF16_AT(g2, r) + bias;
       run += i < len ? -A * softplus_f(gv) : 0.f;
       d[r] = run;
     }
@@ -254,6 +255,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   int64_t tok0;
   if (!slot_owner(p, slot, s_, j_, tok0, len)) {
     if (tid == 0) p.dA_part[slot * H + h] = 0.f;
+    if (p.ddt_part != nullptr && tid < D) p.ddt_part[(slot * H + h) * D + tid] = 0.f;
     return;
   }
   // ---- views ----
@@ -768,23 +770,29 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     for (int X = 1; X < 4; ++X)
       if (X > I) run += red[X * 128 + c];
     const float A = __expf(p.A_log[h]);
-    float dA = 0.f;
+    const float bias = gate_bias(p, h, c, D);
+    float dA = 0.f, ddt = 0.f;
     bf16 *dgsm = dqs;  // dg rows, [64][128]
 #pragma unroll 4
     for (int r = 15; r >= 0; --r) {
       const int i = 16 * I + r;
       run += dgs[r * NT + tid];
-      const float gv = __bfloat162float(gs[(r >> 1) * 2 * NT + 2 * tid + (r & 1)]);
+      const float gv = __bfloat162float(gs[(r >> 1) * 2 * NT + 2 * tid + (r & 1)]) + bias;
       // sigmoid and softplus from one exponential, t = e^-|g|
       const float t = __expf(-fabsf(gv));
       const float inv = __fdividef(1.f, 1.f + t);
       const float sg = gv >= 0.f ? inv : t * inv;
       const float sp = fmaxf(gv, 0.f) + __logf(1.f + t);
-      dgsm[i * D + c] = __float2bfloat16_rn(run * (-A) * sg);
-      if (i < len) dA = fmaf(run, -A * sp, dA);
+      const float dgv = run * (-A) * sg;
+      dgsm[i * D + c] = __float2bfloat16_rn(dgv);
+      if (i < len) {
+        dA = fmaf(run, -A * sp, dA);
+        ddt += dgv;
+      }
     }
     dA = warp_sum(dA);
     if (lane == 0) dAred[warp] = dA;
+    tbuf[I * D + c] = ddt;  // ddt_bias partial: this block's dg column sum
     umma::tc_fence_before();
     __syncthreads();
     if (tid == 0) {
@@ -792,6 +800,9 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       for (int w = 0; w < NW; ++w) t += dAred[w];
       p.dA_part[slot * H + h] = t;
     }
+    if (p.ddt_part != nullptr && tid < D)
+      p.ddt_part[(slot * H + h) * D + tid] =
+          (tbuf[tid] + tbuf[D + tid]) + (tbuf[2 * D + tid] + tbuf[3 * D + tid]);
     bf16 *dgg = reinterpret_cast<bf16 *>(p.dg);
 #pragma unroll 1
     for (int e = tid; e < 64 * (D / 8); e += NT) {

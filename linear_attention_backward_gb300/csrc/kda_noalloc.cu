@@ -51,9 +51,10 @@ extern "C" {
 size_t kda_noalloc_scratch_bytes(void) { return kScratchBytes; }
 
 kda_status kda_bwd_noalloc(const kda_shape *shape, const void *q, const void *k, const void *v,
-                           const void *g, const void *beta, const float *A_log, const float *h0,
-                           const void *dO, const float *dh_T, void *dq, void *dk, void *dv,
-                           void *dg, void *dbeta, float *dA_log, float *dh0,
+                           const void *g, const void *beta, const float *A_log,
+                           const float *dt_bias, const float *h0, const void *dO,
+                           const float *dh_T, void *dq, void *dk, void *dv, void *dg,
+                           void *dbeta, float *dA_log, float *ddt_bias, float *dh0,
                            kda_stream_t stream) {
   // a bad shape gives need == 0 here and is rejected by kda_bwd itself
   const size_t need = kda_workspace_bytes(shape);
@@ -62,8 +63,8 @@ kda_status kda_bwd_noalloc(const kda_shape *shape, const void *q, const void *k,
   if (ws == nullptr) return KDA_ERR_CUDA;
   // The scratch needs no initial content: every part the kernels read is
   // written earlier in the same call.
-  return kda_bwd(shape, q, k, v, g, beta, A_log, h0, dO, dh_T, dq, dk, dv, dg, dbeta, dA_log,
-                 dh0, nullptr, ws, kScratchBytes, stream);
+  return kda_bwd(shape, q, k, v, g, beta, A_log, dt_bias, h0, dO, dh_T, dq, dk, dv, dg, dbeta,
+                 dA_log, ddt_bias, dh0, nullptr, ws, kScratchBytes, stream);
 }
 
 }  // extern "C"

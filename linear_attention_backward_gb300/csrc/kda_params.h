@@ -17,6 +17,7 @@ struct KdaParams {
   float scale, eps;
   const void *q, *k, *v, *g, *beta, *dO;
   const float *A_log, *h0, *dhT;
+  const float *dt_bias;       // nullable [H, K]: the gate's per-channel bias
   void *states;               // [slots, H, K, V] (written by the forward scan)
   float *hT;                  // nullable
   void *dstates;              // [slots, H, K, V]
@@ -24,6 +25,8 @@ struct KdaParams {
   void *dq, *dk, *dv, *dg, *dbeta;
   float *dA_part;             // [slots, H]
   float *dA_log;              // [H]
+  float *ddt_part;            // [slots, H, K] per-chunk partials of ddt_bias
+  float *ddt_bias;            // nullable [H, K], overwritten
   int nb;                     // V bands of the scan kernels
   int role_base;              // first scan role of a launch (0 forward, 1 reverse)
   // Layout of each K x V tile of states / dstates: 0 = row-major, 1 = packed

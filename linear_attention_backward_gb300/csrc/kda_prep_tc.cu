@@ -165,13 +165,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
     // gate: running sum over the block (sums local to the block)
     const float A = __expf(p.A_log[h]);
+    const float bias0 = gate_bias(p, h, c, D), bias1 = gate_bias(p, h, c + 1, D);
     float run0 = 0.f, run1 = 0.f;
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const bool ok = 16 * I + r < len;
       const float2 gv = bf2_to_f2(graw[r]);
-      run0 += ok ? -A * softplus_f(gv.x) : 0.f;
-      run1 += ok ? -A * softplus_f(gv.y) : 0.f;
+      run0 += ok ? -A * softplus_f(gv.x + bias0) : 0.f;
+      run1 += ok ? -A * softplus_f(gv.y + bias1) : 0.f;
       g0[r] = run0;
       g1[r] = run1;
     }

@@ -14,18 +14,24 @@ def f64_tokens(t):
     return t.double().reshape(-1, *t.shape[2:]).numpy()
 
 
+def _bias(x):
+    b = x.get("dt_bias")
+    return None if b is None else b.double().numpy()
+
+
 def oracle_bwd(x, **kw):
     return oracle.backward(
         f64_tokens(x["q"]), f64_tokens(x["k"]), f64_tokens(x["v"]), f64_tokens(x["g"]),
         f64_tokens(x["beta"]), x["A_log"].double().numpy(), x["h0"].double().numpy(),
-        f64_tokens(x["dO"]), x["dhT"].double().numpy(), cu_seqlens=wl.seq_bounds(x), **kw)
+        f64_tokens(x["dO"]), x["dhT"].double().numpy(), cu_seqlens=wl.seq_bounds(x),
+        dt_bias=_bias(x), **kw)
 
 
 def oracle_states(x, chunk=64):
     _, hT, cs = oracle.forward(
         f64_tokens(x["q"]), f64_tokens(x["k"]), f64_tokens(x["v"]), f64_tokens(x["g"]),
         f64_tokens(x["beta"]), x["A_log"].double().numpy(), x["h0"].double().numpy(),
-        cu_seqlens=wl.seq_bounds(x), chunk=chunk, want_chunk_states=True)
+        cu_seqlens=wl.seq_bounds(x), chunk=chunk, want_chunk_states=True, dt_bias=_bias(x))
     return cs, hT
 
 
@@ -45,7 +51,8 @@ def gpu_bwd(x, states=None, **kw):
     import linear_attention_backward_gb300 as kda
     d = to_dev(x)
     g = kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"], d["dO"],
-                d["dhT"], cu_seqlens=d["cu_seqlens"], states=states, **kw)
+                d["dhT"], cu_seqlens=d["cu_seqlens"], states=states, dt_bias=d.get("dt_bias"),
+                **kw)
     torch.cuda.synchronize()
     return g, d
 

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_strings(L):
-    assert L.kda_abi_version() == 3
+    assert L.kda_abi_version() == 4
     for st in range(7):
         assert len(L.kda_status_str(st)) > 0
 
@@ -57,16 +57,18 @@ def test_slots_and_workspace(L):
     sb = 6 * 3 * 128 * 128 * 2
     sb = (sb + 255) // 256 * 256
     assert kda.workspace_dstates_offset(s) == sb
-    # states, dS, dA_log partials and (bf16, K = V = 128) the per-chunk operand
-    # blocks of the tcgen05 path: 98816 bytes per (slot, head)
+    # states, dS, dA_log and ddt_bias partials and (bf16, K = V = 128) the
+    # per-chunk operand blocks of the tcgen05 path: 98816 bytes per (slot, head)
     prep = (6 * 3 * 98816 + 255) // 256 * 256
-    assert kda.workspace_bytes(s) == 2 * sb + ((6 * 3 * 4 + 255) // 256) * 256 + prep
+    ddt = (6 * 3 * 128 * 4 + 255) // 256 * 256
+    assert kda.workspace_bytes(s) == 2 * sb + ((6 * 3 * 4 + 255) // 256) * 256 + ddt + prep
     v = _shape(B=1, T=300, num_seqs=4, cu_seqlens=0x1000)
     assert kda.num_chunk_slots(v) == 300 // 64 + 4
     f = _shape(K=64, V=64, dtype=kda.KDA_FP32, T=64, B=1)
     assert kda.workspace_dstates_offset(f) == 1 * 3 * 64 * 64 * 4
     sf = 1 * 3 * 64 * 64 * 4
-    assert kda.workspace_bytes(f) == 2 * sf + 256  # no operand blocks off the tcgen05 path
+    # no operand blocks off the tcgen05 path
+    assert kda.workspace_bytes(f) == 2 * sf + 256 + 3 * 64 * 4
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -79,14 +81,14 @@ def test_bad_shapes_rejected(L, kw, code):
     s = _shape(**kw)
     assert kda.workspace_bytes(s) == 0
     fake = ctypes.c_void_p(1 << 20)
-    st = L.kda_bwd(ctypes.byref(s), *([fake] * 17), fake, ctypes.c_size_t(1 << 40), None)
+    st = L.kda_bwd(ctypes.byref(s), *([fake] * 19), fake, ctypes.c_size_t(1 << 40), None)
     assert st == code
 
 
 def test_bwd_pointer_checks(L):
     s = _shape()
     fake = ctypes.c_void_p(1 << 20)
-    args = [fake] * 17
+    args = [fake] * 19
     ws_ok = ctypes.c_size_t(kda.workspace_bytes(s))
     # a required pointer missing
     a = list(args); a[0] = None
@@ -99,7 +101,8 @@ def test_bwd_pointer_checks(L):
     assert L.kda_bwd(ctypes.byref(s), *args, fake, ctypes.c_size_t(ws_ok.value - 1), None) == 3
     assert L.kda_bwd(ctypes.byref(s), *args, ctypes.c_void_p((1 << 20) + 16), ws_ok, None) == 3
     # fwd_states: missing states
-    st = L.kda_fwd_states(ctypes.byref(s), fake, fake, fake, fake, fake, None, None, None, None)
+    st = L.kda_fwd_states(ctypes.byref(s), fake, fake, fake, fake, fake, None, None, None, None,
+                          None)
     assert st == 1
 
 
@@ -115,9 +118,9 @@ def test_fwd_argument_checks(L):
     s = _shape()
     fake = ctypes.c_void_p(1 << 20)
     ws_ok = ctypes.c_size_t(kda.workspace_bytes(s))
-    args = [fake] * 6 + [None, fake, None]  # q k v g beta A_log, h0, o, hT
+    args = [fake] * 6 + [None, None, fake, None]  # q k v g beta A_log, dt_bias, h0, o, hT
     # a required pointer missing, a misaligned one
-    a = list(args); a[7] = None
+    a = list(args); a[8] = None
     assert L.kda_fwd(ctypes.byref(s), *a, fake, ws_ok, None) == 1
     a = list(args); a[2] = ctypes.c_void_p((1 << 20) + 2)
     assert L.kda_fwd(ctypes.byref(s), *a, fake, ws_ok, None) == 1

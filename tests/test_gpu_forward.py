@@ -23,17 +23,18 @@ def _built():
 
 
 def oracle_fwd(x):
+    b = x.get("dt_bias")
     o, hT, _ = oracle.forward(
         f64_tokens(x["q"]), f64_tokens(x["k"]), f64_tokens(x["v"]), f64_tokens(x["g"]),
         f64_tokens(x["beta"]), x["A_log"].double().numpy(), x["h0"].double().numpy(),
-        cu_seqlens=wl.seq_bounds(x))
+        cu_seqlens=wl.seq_bounds(x), dt_bias=None if b is None else b.double().numpy())
     return o, hT
 
 
 def gpu_fwd(x):
     d = to_dev(x)
     o, hT = kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"],
-                    cu_seqlens=d["cu_seqlens"], want_hT=True)
+                    cu_seqlens=d["cu_seqlens"], want_hT=True, dt_bias=d.get("dt_bias"))
     torch.cuda.synchronize()
     assert kda.get_device_status() == 0
     return o, hT
@@ -54,6 +55,14 @@ def test_fixed_ragged(T):
     # several chunks and a ragged last chunk; nonzero initial state
     w = wl.custom("f", B=2, T=T, H=3, K=128, V=128, dtype="bf16", with_h0=True)
     x = wl.make_inputs(w, seed=21 + T)
+    _check(x, *gpu_fwd(x))
+
+
+def test_gate_bias():
+    w = wl.custom("fgb", B=2, T=150, H=2, K=128, V=128, dtype="bf16", with_h0=True)
+    x = wl.make_inputs(w, seed=8)
+    gen = torch.Generator().manual_seed(3)
+    x["dt_bias"] = torch.randn(2, 128, generator=gen) * 0.5
     _check(x, *gpu_fwd(x))
 
 

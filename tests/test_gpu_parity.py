@@ -78,6 +78,54 @@ def test_varlen_bf16_with_empty_sequence():
     np.testing.assert_allclose(g["dh0"][2].cpu().numpy(), x["dhT"][2].numpy(), rtol=0, atol=0)
 
 
+def _with_bias(x, seed):
+    H, K = x["q"].shape[2], x["q"].shape[3]
+    gen = torch.Generator().manual_seed(seed)
+    return dict(x, dt_bias=torch.randn(H, K, generator=gen) * 0.5)
+
+
+def _check_dalog(g, ref, x, tol):
+    """dA_log[h] sums dgk * gk over every token and channel of head h, terms
+    of both signs: its error is that of the terms (per-tensor tol, as dg)
+    times the cancellation ||terms||_2 / |sum|.  Bounded here against the
+    L2 norm of the oracle's terms, per head (dgk * gk = dg softplus / sigmoid
+    of the biased gate)."""
+    z = f64_tokens(x["g"]) + (0.0 if x.get("dt_bias") is None
+                              else x["dt_bias"].double().numpy()[None])
+    terms = ref["dg"] * np.logaddexp(0.0, z) * (1.0 + np.exp(-z))
+    got = g["dA_log"].double().cpu().numpy()
+    for h in range(got.shape[0]):
+        l2 = np.linalg.norm(terms[:, h])
+        assert abs(got[h] - ref["dA_log"][h]) <= tol * l2, (h, got[h], ref["dA_log"][h], l2)
+
+
+@pytest.mark.parametrize("dtype,K,T", [("bf16", 128, 200), ("bf16", 64, 130), ("fp32", 64, 97)])
+def test_gate_bias(dtype, K, T):
+    # gk = -exp(A_log) softplus(g + dt_bias) and its gradient ddt_bias, on the
+    # tcgen05 path (bf16, K = 128) and the mma.sync paths
+    w = wl.custom("gb", B=2, T=T, H=2, K=K, V=K, dtype=dtype, with_h0=True, with_dhT=True)
+    x = _with_bias(wl.make_inputs(w, seed=31 + T), 5)
+    g, _ = gpu_bwd(x)
+    _check_status()
+    ref = oracle_bwd(x)
+    keys = tuple(k for k in GRADS if k != "dA_log") + ("ddt_bias",)
+    _compare(g, ref, x, TOL[dtype], keys=keys)
+    _check_dalog(g, ref, x, TOL[dtype])
+
+
+def test_gate_bias_varlen():
+    lengths = [64, 0, 130, 1, 70]
+    w = wl.custom("gbv", H=2, K=128, V=128, dtype="bf16", with_h0=True, with_dhT=True,
+                  varlen=(5, 0, 256))
+    x = _with_bias(wl.make_inputs(w, seed=12, lengths=lengths), 6)
+    g, _ = gpu_bwd(x)
+    _check_status()
+    ref = oracle_bwd(x)
+    keys = tuple(k for k in GRADS if k != "dA_log") + ("ddt_bias",)
+    _compare(g, ref, x, TOL["bf16"], keys=keys)
+    _check_dalog(g, ref, x, TOL["bf16"])
+
+
 def test_varlen_many_sequences_with_ties():
     # the scans take the sequences longest first: equal lengths (ties broken by
     # index), empty sequences and more sequences than one wave of scan CTAs

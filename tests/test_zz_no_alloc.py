@@ -70,5 +70,5 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     fake = torch.empty(16, dtype=torch.bfloat16, device="cuda")
     import ctypes
     p = ctypes.c_void_p(fake.data_ptr())
-    st = kda.lib().kda_bwd_noalloc(ctypes.byref(big), *([p] * 16), None)
+    st = kda.lib().kda_bwd_noalloc(ctypes.byref(big), *([p] * 18), None)
     assert st == 7
