@@ -78,19 +78,10 @@ __device__ __forceinline__ Op opmn(const void *t, int C, int r0 = 0, uint32_t cs
   return Op{smem_u32(t) + (uint32_t)(r0 / 8) * (C / 8) * cs, (uint32_t)(C / 8) * cs, cs,
             2 * (uint32_t)(C / 8) * cs};
 }
-// An opaque copy of a shared-memory address: descriptors built from it are
-// formed where the MMAs are issued instead of being hoisted out of a loop
-// (and kept in registers across it).
-__device__ __forceinline__ uint32_t here(uint32_t a) {
-  asm volatile("" : "+r"(a));
-  return a;
-}
 // D (+)= A B^T over `ksteps` K = 16 steps, issued by one thread; a step
 // advances the descriptors' start-address field by step >> 4.
 __device__ __forceinline__ void gemm(uint32_t d, Op a, bool amn, Op b, bool bmn, int N, int ksteps,
                                      bool accumulate) {
-  a.addr = here(a.addr);
-  b.addr = here(b.addr);
   const uint32_t id = umma::idesc_bf16(128, N, amn, bmn);
   uint64_t da = umma::smem_desc(a.addr, a.lbo, a.sbo);
   uint64_t db = umma::smem_desc(b.addr, b.lbo, b.sbo);
@@ -109,7 +100,7 @@ struct Desc {
   uint32_t step;
 };
 __device__ __forceinline__ Desc mkdesc(Op o) {
-  return Desc{umma::smem_desc(here(o.addr), o.lbo, o.sbo), o.step >> 4};
+  return Desc{umma::smem_desc(o.addr, o.lbo, o.sbo), o.step >> 4};
 }
 // the descriptor of the same operand shifted by `bytes` (a multiple of 16)
 __device__ __forceinline__ uint64_t dshift(const Desc &o, uint32_t bytes) {
