@@ -97,7 +97,7 @@ int64_t kda_num_chunk_slots(const kda_shape *shape);
  * state gradients dS (same size), per-chunk dA_log and ddt_bias partials
  * ([slots, H] and [slots, H, K] fp32) and, for bf16
  * with K = V = 128, the per-chunk operand blocks of the tensor-core scans
- * (98816 bytes per slot and head).  Returns 0 on a bad shape. */
+ * (107008 bytes per slot and head).  Returns 0 on a bad shape. */
 size_t kda_workspace_bytes(const kda_shape *shape);
 /* Byte offset inside the workspace of the per-chunk state gradients
  * dS_{n+1} (the adjoint of the state at the END of chunk n), [slots, H]

@@ -139,31 +139,17 @@ __device__ __forceinline__ float rows16_sum(float (&v)[16]) {
   return v[0];
 }
 
-// prep in the (channel, 16-row block) mapping; E kept in registers
+// prep in the (channel, 16-row block) mapping; E kept in registers.  The row
+// norms and the block factors (em, egm, F, gT) come with the prep kernel's
+// operand block; here only the thread's own gate running sum (for E) and the
+// kd^T tile are formed.
 __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, const bf16 *Kr,
                         const bf16 *Gr, const PrepView<bf16, D> &sv, float (&E)[16], void *KDt,
                         uint32_t (&q2)[8], uint32_t (&k2)[8], uint32_t (&g2)[8]) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int c = tid & 127, I = tid >> 7;
   const float A = __expf(p.A_log[h]);
   const float bias = gate_bias(p, h, c, D);
-  // L2 norms, one warp per row
-  for (int i = warp; i < CHUNK; i += NW) {
-    float sk = 0.f, sq = 0.f;
-#pragma unroll
-    for (int cc = 2 * lane; cc < D; cc += 64) {
-      const float2 kv = load2(Kr + i * D + cc);
-      const float2 qv = load2(Qr + i * D + cc);
-      sk = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, sk));
-      sq = fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, sq));
-    }
-    sk = warp_sum(sk);
-    sq = warp_sum(sq);
-    if (lane == 0) {
-      sv.rk[i] = rsqrtf(sk + p.eps);
-      sv.rq[i] = rsqrtf(sq + p.eps);
-    }
-  }
   // gate: running sum over the block, local to the block (see kda_chunk.cuh)
   float d[16];
   {
@@ -182,44 +168,10 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
       run += i < len ? -A * softplus_f(gv) : 0.f;
       d[r] = run;
     }
-    sv.part[I * D + c] = d[7];         // rows 16I .. 16I+7
-    sv.m[I * D + c] = d[15] - d[7];    // rows 16I+8 .. 16I+15
     const float ref = d[7];
 #pragma unroll
     for (int r = 0; r < 16; ++r) d[r] -= ref;  // gc - m_I
   }
-  __syncthreads();
-  if (tid < D) {
-    float a[4], bb[4];
-#pragma unroll
-    for (int L = 0; L < 4; ++L) {
-      a[L] = sv.part[L * D + tid];
-      bb[L] = sv.m[L * D + tid];
-    }
-    float before = 0.f, tot = 0.f;
-#pragma unroll
-    for (int L = 0; L < 4; ++L) tot += a[L] + bb[L];
-#pragma unroll
-    for (int L = 0; L < 4; ++L) {
-      float after = bb[L];
-#pragma unroll
-      for (int L2 = L + 1; L2 < 4; ++L2) after += a[L2] + bb[L2];
-      sv.em[L * D + tid] = __expf(before + a[L]);
-      sv.egm[L * D + tid] = __expf(after);
-      before += a[L] + bb[L];
-    }
-#pragma unroll
-    for (int I2 = 1; I2 < 4; ++I2)
-#pragma unroll
-      for (int J = 0; J < I2; ++J) {
-        float dd = bb[J] + a[I2];
-#pragma unroll
-        for (int L = J + 1; L < I2; ++L) dd += a[L] + bb[L];
-        sv.F[pair_index(I2, J) * D + tid] = __expf(dd);
-      }
-    sv.gT[tid] = tot;
-  }
-  __syncthreads();
   // kd^T [c][i] (128 x 64, read MN-major as MMA operand B with K = c), one
   // 16-byte store per 8 rows
   const float em = sv.em[I * D + c];
@@ -304,10 +256,11 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   // then v rows (U's slot, free until P2), S (packed in the workspace), dS
   // and kr^T, which stream in during the prep phase
   if (tid == 0) {
-    umma::mbar_expect_tx(rbar, 3 * 16384u);
+    umma::mbar_expect_tx(rbar, 3 * 16384u + (uint32_t)kPrepSVBytes);
     umma::tma_load_3d(Qr, &tm.q, 0, h, (int)tok0, rbar);
     umma::tma_load_3d(Kr, &tm.k, 0, h, (int)tok0, rbar);
     umma::tma_load_3d(Gr, &tm.g, 0, h, (int)tok0, rbar);
+    umma::bulk_g2s(sv.em, unit + kPrepSV, (uint32_t)kPrepSVBytes, rbar);  // factors, norms
     const uint32_t bytes = 16384u + (p.states_packed ? 32768u : 0u) +
                            (p.dstates_packed ? 32768u : 0u) + 16384u;
     umma::mbar_expect_tx(lbar, bytes);

@@ -51,6 +51,11 @@ struct KdaParams {
 //   Mqk  [i][j]  scale * lower(qd ki^T) (diagonal included)
 //   INV  [i][j]  (I + Akk)^-1,  INVb = INV diag(beta)
 //   G    [i][j]  strict_lower(kd ki^T)  (Akk = diag(beta) G)
+// and the per-chunk factors of the 16-row blocks, fp32, 8 KB:
+//   SV   e^(m_I) [4][128] | e^(gT - m_I) [4][128] | e^(m_I - m_J) [6][128] |
+//        gT [128] | 1/|q_i| [64] | 1/|k_i| [64]
+//   (m_I = gc at row 16 I + 7; the layout of the kernels' shared-memory view
+//   from its e^(m_I) array on)
 constexpr size_t kPrepGT = 0;
 constexpr size_t kPrepW = 512;
 constexpr size_t kPrepKR = kPrepW + 16384;
@@ -60,7 +65,9 @@ constexpr size_t kPrepMqk = kPrepQE + 16384;
 constexpr size_t kPrepINV = kPrepMqk + 8192;
 constexpr size_t kPrepINVb = kPrepINV + 8192;
 constexpr size_t kPrepG = kPrepINVb + 8192;
-constexpr size_t kPrepUnitBytes = kPrepG + 8192;
+constexpr size_t kPrepSV = kPrepG + 8192;
+constexpr size_t kPrepSVBytes = 8192;
+constexpr size_t kPrepUnitBytes = kPrepSV + kPrepSVBytes;
 
 // TMA tensor maps of the token-major bf16 inputs [B * T, H, 128]: one box is
 // the 64 rows x 128 channels of one chunk and head, landing row-major

@@ -217,8 +217,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         sv.F[pair_index(I2, J) * D + e] = __expf(d);  // e^(m_I - m_J)
       }
     reinterpret_cast<float *>(unit + kPrepGT)[e] = tot;
+    sv.gT[e] = tot;
   }
   __syncthreads();
+  // the block factors and the row norms for the gradient kernel (one 8 KB span
+  // of the view: e^(m_I), e^(gT - m_I), e^(m_I - m_J), gT, 1/|q|, 1/|k|)
+  static_assert(19 * D + 128 - 4 * D == kPrepSVBytes / 4, "factor span");
+  for (int e = tid; e < (int)(kPrepSVBytes / 16); e += NTHREADS)
+    reinterpret_cast<uint4 *>(unit + kPrepSV)[e] = reinterpret_cast<const uint4 *>(sv.em)[e];
   // ---- decay-scaled tiles; kr^T goes straight to HBM ----
   {
     const float eg0 = sv.egm[I * D + c], eg1 = sv.egm[I * D + c + 1];

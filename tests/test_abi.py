@@ -58,8 +58,8 @@ def test_slots_and_workspace(L):
     sb = (sb + 255) // 256 * 256
     assert kda.workspace_dstates_offset(s) == sb
     # states, dS, dA_log and ddt_bias partials and (bf16, K = V = 128) the
-    # per-chunk operand blocks of the tcgen05 path: 98816 bytes per (slot, head)
-    prep = (6 * 3 * 98816 + 255) // 256 * 256
+    # per-chunk operand blocks of the tcgen05 path: 107008 bytes per (slot, head)
+    prep = (6 * 3 * 107008 + 255) // 256 * 256
     ddt = (6 * 3 * 128 * 4 + 255) // 256 * 256
     assert kda.workspace_bytes(s) == 2 * sb + ((6 * 3 * 4 + 255) // 256) * 256 + ddt + prep
     v = _shape(B=1, T=300, num_seqs=4, cu_seqlens=0x1000)
