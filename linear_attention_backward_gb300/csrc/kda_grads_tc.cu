@@ -71,7 +71,7 @@ struct Smem {
   // stacked 128-row operand of P6 / P8; KPl (intra) reuses the dvcorr slot
   static constexpr size_t o_D = o_C + sz_C;
   static constexpr size_t o_dS = o_D;
-  static constexpr size_t o_dMqk = o_D;
+  static constexpr size_t o_dMqk = o_D;  // dMqk | dA interleaved by 16-row blocks, 128 x 64
   static constexpr size_t o_dA = o_D + T64x64;
   static constexpr size_t o_dvc = o_D + T64x128;
   static constexpr size_t o_dO = o_D + T128x128;
@@ -111,14 +111,18 @@ __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 
 // element r of 16 values packed two per register
 #define BF16_AT(arr, r) (((r) & 1) ? bf_hi((arr)[(r) >> 1]) : bf_lo((arr)[(r) >> 1]))
 
-// Triangle-sized accumulators of the intra-chunk products.  Key-block J of
-// P9a / P9b holds output rows i >= 16 J only (N = 64 - 16 J), query-block X
-// of P9c output columns j < 16 (X + 1) only (N = 16 (X + 1)).  TMEM column
-// bases: P9a in [0, 160), P9b in [160, 256) and [384, 448) (P8's results sit in
-// [256, 384) and dkr in [448, 512)), P9c in [0, 160).
-__device__ __forceinline__ int col_p9a(int J) { return J == 0 ? 0 : (J == 1 ? 64 : (J == 2 ? 112 : 144)); }
-__device__ __forceinline__ int col_p9b(int J) { return J == 0 ? 384 : (J == 1 ? 160 : (J == 2 ? 208 : 240)); }
+// Triangle-sized accumulators of the intra-chunk products.  dMqk and dA share
+// one 128 x 64 tile, interleaved by 16-row blocks (rows 32 b .. 32 b + 15 =
+// dMqk block b, the next 16 = dA block b), so that P9a and P9b of key block J
+// are ONE product over the tile's rows 32 J .. 127 (N = 128 - 32 J): its
+// columns 32 (I - J) .. + 15 hold the dMqk side of query block I, the next 16
+// the dA side.  Query-block X of P9c holds output columns j < 16 (X + 1) only
+// (N = 16 (X + 1)).  TMEM column bases: P9ab in [0, 256) and [384, 448) (P8's
+// results sit in [256, 384) and dkr in [448, 512)), P9c in [0, 160).
+__device__ __forceinline__ int col_p9ab(int J) { return J == 0 ? 0 : (J == 1 ? 128 : (J == 2 ? 384 : 224)); }
 __device__ __forceinline__ int col_p9c(int X) { return X == 0 ? 0 : (X == 1 ? 16 : (X == 2 ? 48 : 96)); }
+// row of the interleaved dMqk | dA tile holding row i of dMqk (side 0) or dA (side 1)
+__device__ __forceinline__ int dma_row(int i, int side) { return 32 * (i >> 4) + 16 * side + (i & 15); }
 
 // Row sums over the warp's 32 lanes for the thread's 16 rows: lanes l and
 // l + 16 return the sum of row l (31 shuffles); v is consumed.
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   char *St = smem + SM::o_S, *Ut = smem + SM::o_U;
   char *KDt = smem + SM::o_C, *KRt = KDt + T64x128;
   char *XrT = KDt, *dUT = KRt, *QMl = KDt, *KMl = KRt;
-  char *dSt = smem + SM::o_dS, *dMqk = smem + SM::o_dMqk, *dAt = smem + SM::o_dA,
+  char *dSt = smem + SM::o_dS, *dMA = smem + SM::o_dMqk,
        *dvc = smem + SM::o_dvc, *dOt = smem + SM::o_dO, *KPl = dvc;
   const float scale = p.scale;
   const size_t DD = (size_t)D * D;
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
           db2 = fmaf(dak, __bfloat162float(*reinterpret_cast<const bf16 *>(Gbf + umma::core_off(i, jj, 64))), db2);
           o8[t] = sv.beta[i] * dak;
         }
-        pstore8(dAt, i, 16 * I + 8 * q, 64, o8);
+        pstore8(dMA, dma_row(i, 1), 16 * I + 8 * q, 64, o8);
       }
       red2[I * 64 + i] = db2;
     } else {
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
           const int jj = 16 * I + 8 * q + t;
           o8[t] = jj <= i ? scale * v16[8 * q + t] : 0.f;
         }
-        pstore8(dMqk, i, 16 * I + 8 * q, 64, o8);
+        pstore8(dMA, dma_row(i, 0), 16 * I + 8 * q, 64, o8);
       }
     }
   }
@@ -523,21 +527,19 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     Fk[X] = X > I ? sv.F[pair_index(X, I) * D + c] : (X == I ? 1.f : 0.f);
   }
   const float emI = sv.em[I * D + c];
-  // ---- R5 = P9a + P9b: dq^ intra (dMqk with kp) and dkd' intra (dA with kp), per key block J ----
-  // (descriptors built once and shifted per block: one thread issues all 16 MMAs)
+  // ---- R5 = P9a + P9b: dq^ intra (dMqk with kp) and dkd' intra (dA with kp), per key block J,
+  // both sides in one product over the interleaved tile (8 MMAs, hi + lo) ----
   if (tid == 0) {
     umma::tc_fence_after();
     const Desc aH = mkdesc(opk(KPh, 64)), aL = mkdesc(opk(KPl, 64));
-    const Desc bM = mkdesc(opk(dMqk, 64)), bA = mkdesc(opk(dAt, 64));
+    const Desc bMA = mkdesc(opk(dMA, 64));
 #pragma unroll
     for (int J = 0; J < 4; ++J) {
-      const uint32_t id = umma::idesc_bf16(128, 64 - 16 * J, false, false);
+      const uint32_t id = umma::idesc_bf16(128, 128 - 32 * J, false, false);
       const uint32_t ka = (uint32_t)(2 * J) * CS;                      // K offset (columns 16 J)
-      const uint32_t kb = ka + (uint32_t)(2 * J) * (64 / 8) * CS;      // and rows 16 J of B
-      mma1(tbase + col_p9a(J), dshift(aH, ka), dshift(bM, kb), id, false);
-      mma1(tbase + col_p9a(J), dshift(aL, ka), dshift(bM, kb), id, true);
-      mma1(tbase + col_p9b(J), dshift(aH, ka), dshift(bA, kb), id, false);
-      mma1(tbase + col_p9b(J), dshift(aL, ka), dshift(bA, kb), id, true);
+      const uint32_t kb = ka + (uint32_t)(4 * J) * (64 / 8) * CS;      // and rows 32 J of B
+      mma1(tbase + col_p9ab(J), dshift(aH, ka), dshift(bMA, kb), id, false);
+      mma1(tbase + col_p9ab(J), dshift(aL, ka), dshift(bMA, kb), id, true);
     }
     umma::mma_commit(mbar);
   }
@@ -555,14 +557,15 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     {
       float a0[16], a1[16];
       tld16_nw(tbase, 320, bq);
-      tld16_nw(tbase, col_p9a(0), a0);
-      if (I >= 1) tld16_nw(tbase, col_p9a(1) - 16, a1);
+      // (tld16 adds 16 I: key block J's dMqk side of block I is at col_p9ab(J) + 32 (I - J))
+      tld16_nw(tbase, col_p9ab(0) + 16 * I, a0);
+      if (I >= 1) tld16_nw(tbase, col_p9ab(1) - 32 + 16 * I, a1);
       umma::tmem_ld_wait();
 #pragma unroll
       for (int r = 0; r < 16; ++r) in[r] = Fq[0] * a0[r] + (I >= 1 ? Fq[1] * a1[r] : 0.f);
       if (I >= 2) {
-        tld16_nw(tbase, col_p9a(2) - 32, a0);
-        if (I >= 3) tld16_nw(tbase, col_p9a(3) - 48, a1);
+        tld16_nw(tbase, col_p9ab(2) - 64 + 16 * I, a0);
+        if (I >= 3) tld16_nw(tbase, col_p9ab(3) - 96 + 16 * I, a1);
         umma::tmem_ld_wait();
 #pragma unroll
         for (int r = 0; r < 16; ++r)
@@ -596,14 +599,14 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     {
       float a0[16], a1[16];
       tld16_nw(tbase, 256, bk);
-      tld16_nw(tbase, col_p9b(0), a0);
-      if (I >= 1) tld16_nw(tbase, col_p9b(1) - 16, a1);
+      tld16_nw(tbase, col_p9ab(0) + 16 + 16 * I, a0);  // the dA side: 16 further
+      if (I >= 1) tld16_nw(tbase, col_p9ab(1) - 16 + 16 * I, a1);
       umma::tmem_ld_wait();
 #pragma unroll
       for (int r = 0; r < 16; ++r) dkt[r] = Fq[0] * a0[r] + (I >= 1 ? Fq[1] * a1[r] : 0.f);
       if (I >= 2) {
-        tld16_nw(tbase, col_p9b(2) - 32, a0);
-        if (I >= 3) tld16_nw(tbase, col_p9b(3) - 48, a1);
+        tld16_nw(tbase, col_p9ab(2) - 48 + 16 * I, a0);
+        if (I >= 3) tld16_nw(tbase, col_p9ab(3) - 80 + 16 * I, a1);
         umma::tmem_ld_wait();
 #pragma unroll
         for (int r = 0; r < 16; ++r)
@@ -634,17 +637,18 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     umma::tc_fence_after();
     const Desc aQH = mkdesc(opk(QMh, 64)), aQL = mkdesc(opk(QMl, 64));
     const Desc aKH = mkdesc(opk(KMh, 64)), aKL = mkdesc(opk(KMl, 64));
-    const Desc bM = mkdesc(opmn(dMqk, 64)), bA = mkdesc(opmn(dAt, 64));
+    const Desc bMA = mkdesc(opmn(dMA, 64));
 #pragma unroll
     for (int X = 0; X < 4; ++X) {
       const uint32_t d = tbase + col_p9c(X);
       const uint32_t id = umma::idesc_bf16(128, 16 * (X + 1), false, true);
       const uint32_t ka = (uint32_t)(2 * X) * CS;                      // K offset (columns 16 X)
-      const uint32_t kb = (uint32_t)(2 * X) * (64 / 8) * CS;           // K offset (rows 16 X)
-      mma1(d, dshift(aQH, ka), dshift(bM, kb), id, false);
-      mma1(d, dshift(aQL, ka), dshift(bM, kb), id, true);
-      mma1(d, dshift(aKH, ka), dshift(bA, kb), id, true);
-      mma1(d, dshift(aKL, ka), dshift(bA, kb), id, true);
+      const uint32_t kbm = (uint32_t)(4 * X) * (64 / 8) * CS;          // dMqk block X: rows 32 X
+      const uint32_t kba = kbm + (uint32_t)2 * (64 / 8) * CS;          // dA block X: 16 rows on
+      mma1(d, dshift(aQH, ka), dshift(bMA, kbm), id, false);
+      mma1(d, dshift(aQL, ka), dshift(bMA, kbm), id, true);
+      mma1(d, dshift(aKH, ka), dshift(bMA, kba), id, true);
+      mma1(d, dshift(aKL, ka), dshift(bMA, kba), id, true);
     }
     umma::mma_commit(mbar);
   }
