@@ -54,16 +54,28 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   using namespace stc;
   using SM = stc::Smem;
   extern __shared__ __align__(1024) char smem[];
-  // block b -> (sequence rank r, role, head): the chains of the longest
-  // sequences are dispatched first (varlen), so that short chains fill in
-  // behind them instead of a long one starting last
+  // block b -> (sequence rank r, role, head) for varlen: the chains of the
+  // longest sequences are dispatched first, so that short chains fill in
+  // behind them instead of a long one starting last; fixed length (all
+  // chains equally long): (role, sequence, head)
   const int H = p.H;
-  const int nroles = (int)(gridDim.x / (unsigned)((p.cu ? p.num_seqs : p.B) * H));
-  const int r = (int)(blockIdx.x / (unsigned)(nroles * H));
-  const int rem = (int)(blockIdx.x % (unsigned)(nroles * H));
-  const int role = p.role_base + rem / H;  // 0: forward states, 1: reverse dS scan
+  const int nseq = p.cu ? p.num_seqs : p.B;
+  const int nroles = (int)(gridDim.x / (unsigned)(nseq * H));
+  int r, rl, h;
+  if (p.seq_order != nullptr) {
+    r = (int)(blockIdx.x / (unsigned)(nroles * H));
+    const int rem = (int)(blockIdx.x % (unsigned)(nroles * H));
+    rl = rem / H;
+    h = rem % H;
+  } else {
+    rl = (int)(blockIdx.x / (unsigned)(nseq * H));
+    const int rem = (int)(blockIdx.x % (unsigned)(nseq * H));
+    r = rem / H;
+    h = rem % H;
+  }
+  const int role = p.role_base + rl;  // 0: forward states, 1: reverse dS scan
   const bool fwd = role == 0;
-  const int h = rem % H, s = p.seq_order ? p.seq_order[r] : r;
+  const int s = p.seq_order ? p.seq_order[r] : r;
   const int tid = threadIdx.x, warp = tid >> 5;
   int64_t tok_seq, slot0;
   int L;
