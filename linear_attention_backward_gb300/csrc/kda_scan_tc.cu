@@ -57,7 +57,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   // block b -> (sequence rank r, role, head) for varlen: the chains of the
   // longest sequences are dispatched first, so that short chains fill in
   // behind them instead of a long one starting last; fixed length (all
-  // chains equally long): (role, sequence, head)
+  // chains equally long): (role, sequence, head).  The reverse role (the
+  // longer chain of work per chunk) goes first in both.
   const int H = p.H;
   const int nseq = p.cu ? p.num_seqs : p.B;
   const int nroles = (int)(gridDim.x / (unsigned)(nseq * H));
@@ -65,10 +66,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   if (p.seq_order != nullptr) {
     r = (int)(blockIdx.x / (unsigned)(nroles * H));
     const int rem = (int)(blockIdx.x % (unsigned)(nroles * H));
-    rl = rem / H;
+    rl = nroles - 1 - rem / H;
     h = rem % H;
   } else {
-    rl = (int)(blockIdx.x / (unsigned)(nseq * H));
+    rl = nroles - 1 - (int)(blockIdx.x / (unsigned)(nseq * H));
     const int rem = (int)(blockIdx.x % (unsigned)(nseq * H));
     r = rem / H;
     h = rem % H;
