@@ -61,6 +61,11 @@ NCU_TRAFFIC = {
                             "bytes_per_launch": 4361564160},
 }
 
+KERNEL_SOURCES = {
+    "grads": ["kda_grads_tc.cu", "kda_tc_tiles.cuh", "kda_umma.cuh", "kda_chunk.cuh",
+              "kda_device.cuh", "kda_params.h"],
+}
+
 
 def src_hash(kernel):
     h = hashlib.sha256()
