@@ -118,70 +118,43 @@ __device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t a) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(a));
 }
-__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t a) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(a));
-}
-// acc (16 x 8 NF) += A (16 x kdim) B (kdim x 8 NF) from transposed tiles:
-// A(m, k) = tile A[ak0 + k][am0 + m], B(k, n) = tile B[bk0 + k][bn0 + n];
-// kscale per k (the tiles' row index).
-template <int NF>
-__device__ __forceinline__ void wg_core_t(float (&acc)[NF][4], const void *A, int AC, int ak0,
-                                          int am0, const void *B, int BC, int bk0, int bn0,
-                                          int kdim, const float *kscale) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
-#pragma unroll
-  for (int k0 = 0; k0 < kdim; k0 += 16) {
-    uint32_t af[4];
-    ldsm4t(af, a0 + pcore_off(ak0 + k0 + (lane & 7) + (lane >> 4) * 8,
-                              am0 + ((lane >> 3) & 1) * 8, AC));
-    if (kscale != nullptr) {
-      const int c = k0 + 2 * (lane & 3);
-      const float s0 = kscale[c], s1 = kscale[c + 1], s8 = kscale[c + 8], s9 = kscale[c + 9];
-      af[0] = scale_pair(af[0], s0, s1);
-      af[1] = scale_pair(af[1], s0, s1);
-      af[2] = scale_pair(af[2], s8, s9);
-      af[3] = scale_pair(af[3], s8, s9);
-    }
-#pragma unroll
-    for (int f = 0; f < NF; f += 2) {
-      uint32_t bfr[4];
-      ldsm4t(bfr, b0 + pcore_off(bk0 + k0 + (lane & 7) + ((lane >> 3) & 1) * 8,
-                                 bn0 + f * 8 + (lane >> 4) * 8, BC));
-      mma_16816(acc[f], af, bfr[0], bfr[1]);
-      mma_16816(acc[f + 1], af, bfr[2], bfr[3]);
-    }
-  }
-}
 // acc (16 x 8 NF) += A (16 x kdim) B (kdim x 8 NF); A(m, k) = tile A[ar0 + m][ac0 + k],
 // B(k, n) = tile B[br0 + n][bc0 + k]; both K-contiguous tiles; kscale per k.
+// The fragments of step k + 16 are loaded before the MMAs of step k are
+// issued (the loads and MMAs are ordered asm statements), so that no MMA waits
+// on the shared-memory latency of its own operands.
 template <int NF>
 __device__ __forceinline__ void wg_core(float (&acc)[NF][4], const void *A, int AC, int ar0,
                                         int ac0, const void *B, int BC, int br0, int bc0,
                                         int kdim, const float *kscale) {
   const int lane = threadIdx.x & 31;
   const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+  uint32_t af[2][4], bfr[2][NF / 2][4];
+  auto load = [&](int k0, int buf) {
+    ldsm4(af[buf], a0 + pcore_off(ar0 + (lane & 15), ac0 + k0 + (lane >> 4) * 8, AC));
+#pragma unroll
+    for (int f = 0; f < NF; f += 2)
+      ldsm4(bfr[buf][f / 2], b0 + pcore_off(br0 + f * 8 + (lane & 7) + (lane >> 4) * 8,
+                                            bc0 + k0 + ((lane >> 3) & 1) * 8, BC));
+  };
+  load(0, 0);
 #pragma unroll
   for (int k0 = 0; k0 < kdim; k0 += 16) {
-    uint32_t af[4];
-    ldsm4(af, a0 + pcore_off(ar0 + (lane & 15), ac0 + k0 + (lane >> 4) * 8, AC));
+    const int cur = (k0 >> 4) & 1;
+    if (k0 + 16 < kdim) load(k0 + 16, cur ^ 1);
+    uint32_t a[4] = {af[cur][0], af[cur][1], af[cur][2], af[cur][3]};
     if (kscale != nullptr) {
       const int c = k0 + 2 * (lane & 3);
       const float s0 = kscale[c], s1 = kscale[c + 1], s8 = kscale[c + 8], s9 = kscale[c + 9];
-      af[0] = scale_pair(af[0], s0, s1);
-      af[1] = scale_pair(af[1], s0, s1);
-      af[2] = scale_pair(af[2], s8, s9);
-      af[3] = scale_pair(af[3], s8, s9);
+      a[0] = scale_pair(a[0], s0, s1);
+      a[1] = scale_pair(a[1], s0, s1);
+      a[2] = scale_pair(a[2], s8, s9);
+      a[3] = scale_pair(a[3], s8, s9);
     }
 #pragma unroll
     for (int f = 0; f < NF; f += 2) {
-      uint32_t bfr[4];
-      ldsm4(bfr, b0 + pcore_off(br0 + f * 8 + (lane & 7) + (lane >> 4) * 8,
-                                bc0 + k0 + ((lane >> 3) & 1) * 8, BC));
-      mma_16816(acc[f], af, bfr[0], bfr[1]);
-      mma_16816(acc[f + 1], af, bfr[2], bfr[3]);
+      mma_16816(acc[f], a, bfr[cur][f / 2][0], bfr[cur][f / 2][1]);
+      mma_16816(acc[f + 1], a, bfr[cur][f / 2][2], bfr[cur][f / 2][3]);
     }
   }
 }
@@ -249,7 +222,9 @@ __device__ inline void inverse_inplace(float *Gf, const float *beta, float *tbuf
     if (warp < I) {
       const int J = warp;
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      for (int L = J; L < I; ++L) {
+#pragma unroll
+      for (int L = 0; L < 3; ++L) {  // terms L = J .. I - 1 (unrolled: their loads overlap)
+        if (L < J || L >= I) continue;
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           const float *ga = Gf + (16 * I + gid) * LG + 16 * L + 8 * kk + tig;
