@@ -246,20 +246,18 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   const bf16 *dSg = reinterpret_cast<const bf16 *>(p.dstates) + ((size_t)slot * H + h) * DD;
   const char *unit = p.prep + ((size_t)slot * H + h) * kPrepUnitBytes;
 
-  // ---- Tensor Memory (all 512 columns) and the MMA-completion barrier ----
-  if (warp == 0) umma::tmem_alloc(tslot, 512);
+  // ---- barriers, the first copies, then Tensor Memory (all 512 columns) ----
+  // Thread 0 initialises the barriers and at once issues the copies: the raw
+  // q, k, g rows (row-major, R_A) and the block factors first, the prep phase
+  // waits on them; then v rows (U's slot, free until P2), S (packed in the
+  // workspace), dS and kr^T, which stream in during the prep phase.  Warp 0
+  // allocates Tensor Memory meanwhile.
   if (tid == 0) {
     umma::mbar_init(mbar, 1);
     umma::mbar_init(lbar, 1);
     umma::mbar_init(pbar, 1);
     umma::mbar_init(rbar, 1);
-  }
-  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  __syncthreads();
-  // raw q, k, g rows (row-major, R_A) first: the prep phase waits on them;
-  // then v rows (U's slot, free until P2), S (packed in the workspace), dS
-  // and kr^T, which stream in during the prep phase
-  if (tid == 0) {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     umma::mbar_expect_tx(rbar, 3 * 16384u + (uint32_t)kPrepSVBytes);
     umma::tma_load_3d(Qr, &tm.q, 0, h, (int)tok0, rbar);
     umma::tma_load_3d(Kr, &tm.k, 0, h, (int)tok0, rbar);
@@ -273,6 +271,8 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     if (p.dstates_packed) umma::bulk_g2s(dSt, dSg, 32768u, lbar);
     umma::bulk_g2s(KRt, unit + kPrepKR, 16384u, lbar);
   }
+  if (warp == 0) umma::tmem_alloc(tslot, 512);
+  __syncthreads();
   // beta: the load's latency overlaps the copies; stored after they land
   const float beta_i = tid < len && tid < CHUNK
                            ? __bfloat162float(reinterpret_cast<const bf16 *>(p.beta)[(tok0 + tid) * H + h])

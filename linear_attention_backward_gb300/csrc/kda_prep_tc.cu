@@ -103,23 +103,22 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   char *INVb = smem + SM::o_INVb;
   const float scale = p.scale;
 
-  if (warp == 0) umma::tmem_alloc(tslot, 256);
-  if (tid == 0) {
-    umma::mbar_init(mbar, 1);
-    umma::mbar_init(rbar, 1);
-  }
-  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  __syncthreads();
   // raw q, k, g rows (row-major [64][128]) into the tile region, which the
-  // tiles overwrite only after every thread has taken its rows
+  // tiles overwrite only after every thread has taken its rows; thread 0 issues
+  // them as soon as the barriers exist, warp 0 then allocates Tensor Memory
   const bf16 *Qraw = reinterpret_cast<const bf16 *>(QM);
   const bf16 *Kraw = Qraw + 64 * D, *Graw = Kraw + 64 * D;
   if (tid == 0) {
+    umma::mbar_init(mbar, 1);
+    umma::mbar_init(rbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     umma::mbar_expect_tx(rbar, 3 * 16384u);
     umma::tma_load_3d(QM, &tm.q, 0, h, (int)tok0, rbar);
     umma::tma_load_3d(QM + 16384, &tm.k, 0, h, (int)tok0, rbar);
     umma::tma_load_3d(QM + 32768, &tm.g, 0, h, (int)tok0, rbar);
   }
+  if (warp == 0) umma::tmem_alloc(tslot, 256);
+  __syncthreads();
   // v rows -> packed core tile [j][v] (the MN-major A operand of U0^T)
   {
     const bf16 *vg = reinterpret_cast<const bf16 *>(p.v);
