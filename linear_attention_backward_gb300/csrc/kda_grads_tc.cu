@@ -147,9 +147,13 @@ __device__ __forceinline__ float rows16_sum(float (&v)[16]) {
 // norms and the block factors (em, egm, F, gT) come with the prep kernel's
 // operand block; here only the thread's own gate running sum (for E) and the
 // kd^T tile are formed.
+// Once every thread holds its raw rows, thread 0 issues the copy of the
+// prep block's 64 x 64 tiles (Mqk, INV, INVb, G: 32 KB) over them (tiles, on
+// barrier pbar), so that it lands while the gate and kd^T are formed.
 __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, const bf16 *Kr,
                         const bf16 *Gr, const PrepView<bf16, D> &sv, float (&E)[16], void *KDt,
-                        uint32_t (&q2)[8], uint32_t (&k2)[8], uint32_t (&g2)[8]) {
+                        uint32_t (&q2)[8], uint32_t (&k2)[8], uint32_t (&g2)[8],
+                        const char *tiles_src, void *tiles, uint64_t *pbar) {
   const int tid = threadIdx.x;
   const int c = tid & 127, I = tid >> 7;
   const float A = __expf(p.A_log[h]);
@@ -164,6 +168,11 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
       g2[r >> 1] = pack_bf(Gr[i * D + c], Gr[(i + 1) * D + c]);
       q2[r >> 1] = pack_bf(Qr[i * D + c], Qr[(i + 1) * D + c]);
       k2[r >> 1] = pack_bf(Kr[i * D + c], Kr[(i + 1) * D + c]);
+    }
+    __syncthreads();  // the raw rows are dead
+    if (tid == 0) {
+      umma::mbar_expect_tx(pbar, 32768u);
+      umma::bulk_g2s(tiles, tiles_src, 32768u, pbar);
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -323,13 +332,9 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   // ---- prep ----
   float E[16];
   uint32_t q2[8], k2[8], g2[8];  // the thread's raw q, k, g rows, two per register
-  prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, q2, k2, g2);
-  // pair matrices and inverses, formed by the prep kernel: Mqk, INV, INVb, G
-  // (packed 64 x 64) into R_A (the raw rows are dead), one bulk copy
-  if (tid == 0) {
-    umma::mbar_expect_tx(pbar, 32768u);
-    umma::bulk_g2s(Mqk, unit + kPrepMqk, 32768u, pbar);
-  }
+  // (the pair matrices and inverses formed by the prep kernel -- Mqk, INV,
+  // INVb, G, packed 64 x 64 -- come into R_A over the raw rows from inside)
+  prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, q2, k2, g2, unit + kPrepMqk, Mqk, pbar);
   cp_async_wait_all();                 // dO, v (and row-major S)
   umma::mbar_wait(lbar, 0);            // S, dS, kr^T
   umma::fence_async_smem();
