@@ -255,6 +255,13 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   const bf16 *dSg = reinterpret_cast<const bf16 *>(p.dstates) + ((size_t)slot * H + h) * DD;
   const char *unit = p.prep + ((size_t)slot * H + h) * kPrepUnitBytes;
 
+  // beta, loaded by the last two warps (idle until the CTA barrier below, so
+  // the load's latency hides behind the copies' issue) and stored after it
+  constexpr int kBetaT0 = NT - CHUNK;
+  float beta_i = 0.f;
+  if (tid >= kBetaT0 && tid - kBetaT0 < len)
+    beta_i = __bfloat162float(
+        reinterpret_cast<const bf16 *>(p.beta)[(tok0 + (tid - kBetaT0)) * H + h]);
   // ---- barriers, the first copies, then Tensor Memory (all 512 columns) ----
   // Thread 0 initialises the barriers and at once issues the copies: the raw
   // q, k, g rows (row-major, R_A) and the block factors first, the prep phase
@@ -282,10 +289,6 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   if (warp == 0) umma::tmem_alloc(tslot, 512);
   __syncthreads();
-  // beta: the load's latency overlaps the copies; stored after they land
-  const float beta_i = tid < len && tid < CHUNK
-                           ? __bfloat162float(reinterpret_cast<const bf16 *>(p.beta)[(tok0 + tid) * H + h])
-                           : 0.f;
   // ---- dO (and row-major states) by cp.async ----
   for (int e = tid; e < 64 * (D / 8); e += NT) {
     const int i = e >> 4, c8 = (e & 15) * 8;
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   cp_async_commit();
   umma::tc_fence_before();
-  if (tid < CHUNK) sv.beta[tid] = beta_i;
+  if (tid >= kBetaT0) sv.beta[tid - kBetaT0] = beta_i;
   umma::mbar_wait(rbar, 0);
   if (len < CHUNK) {  // the boxes' rows past the chunk belong to the next sequence: zero them
     for (int e = tid; e < 3 * 64 * 16; e += NT) {
