@@ -429,15 +429,22 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     dbs[i] = red[(w0 + 0) * 16 + r] + red[(w0 + 1) * 16 + r] + red[(w0 + 2) * 16 + r] +
              red[(w0 + 3) * 16 + r];
   }
-  {  // dv rows: 16-byte row pieces (they run alongside P6 / P8 below)
+  {  // dv rows: one TMA box for a whole chunk, else 16-byte row pieces (alongside P6 / P8)
     const bf16 *dvs = reinterpret_cast<const bf16 *>(smem + SM::o_A);
-    bf16 *dvg = reinterpret_cast<bf16 *>(p.dv);
+    if (len == CHUNK) {
+      if (tid == 0) {
+        umma::tma_store_3d(&tm.dv, 0, h, (int)tok0, dvs);
+        umma::bulk_commit();
+      }
+    } else {
+      bf16 *dvg = reinterpret_cast<bf16 *>(p.dv);
 #pragma unroll 1
-    for (int e = tid; e < 64 * (D / 8); e += NT) {
-      const int i = e >> 4, c8 = (e & 15) * 8;
-      if (i < len)
-        *reinterpret_cast<uint4 *>(dvg + ((tok0 + i) * H + h) * D + c8) =
-            *reinterpret_cast<const uint4 *>(dvs + i * D + c8);
+      for (int e = tid; e < 64 * (D / 8); e += NT) {
+        const int i = e >> 4, c8 = (e & 15) * 8;
+        if (i < len)
+          *reinterpret_cast<uint4 *>(dvg + ((tok0 + i) * H + h) * D + c8) =
+              *reinterpret_cast<const uint4 *>(dvs + i * D + c8);
+      }
     }
   }
 
@@ -485,6 +492,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   umma::fence_async_smem();
   umma::tc_fence_before();
+  if (tid == 0) umma::bulk_wait_read();  // the dv box has left R_A [0, 16K) (the g rows go there)
   __syncthreads();
   if (tid < 64 && tid < len) {
     const float db = dbs[tid] + red2[tid] + red2[64 + tid] + red2[128 + tid] + red2[192 + tid];
@@ -627,9 +635,15 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       dkt[r] = -sv.beta[i] * E[r] * emI * bk[r] + E[r] * dkt[r];
     }
   }
+  umma::fence_async_smem();  // the dq rows, for the TMA store
   umma::tc_fence_before();
   __syncthreads();
-  {
+  if (len == CHUNK) {
+    if (tid == 0) {
+      umma::tma_store_3d(&tm.dq, 0, h, (int)tok0, dqs);
+      umma::bulk_commit();
+    }
+  } else {
     bf16 *dqg = reinterpret_cast<bf16 *>(p.dq);
 #pragma unroll 1
     for (int e = tid; e < 64 * (D / 8); e += NT) {
@@ -712,14 +726,20 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     float tot = 0.f;
 #pragma unroll
     for (int r = 0; r < 16; ++r) tot += dgc[r];
-    __syncthreads();         // red is free again; the dk rows are complete
+    umma::fence_async_smem();  // the dk rows, for the TMA store
+    __syncthreads();           // red is free again; the dk rows are complete
     red[I * 128 + c] = tot;  // block totals per channel
     // the row loop stays rolled (code size): dgc goes through shared memory
     // (R_C: the lo tiles are dead once P9c has completed)
     float *dgs = reinterpret_cast<float *>(smem + SM::o_C);
 #pragma unroll
     for (int r = 0; r < 16; ++r) dgs[r * NT + tid] = dgc[r];
-    {
+    if (len == CHUNK) {
+      if (tid == 0) {
+        umma::tma_store_3d(&tm.dk, 0, h, (int)tok0, dks);
+        umma::bulk_commit();
+      }
+    } else {
       bf16 *dkg = reinterpret_cast<bf16 *>(p.dk);
 #pragma unroll 1
       for (int e = tid; e < 64 * (D / 8); e += NT) {
@@ -729,6 +749,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
               *reinterpret_cast<const uint4 *>(dks + i * D + c8);
       }
     }
+    if (tid == 0) umma::bulk_wait_read_but1();  // the dq box has left (dg rows go there)
     __syncthreads();
     float run = dgT[c] + dgT[D + c] + dgT[2 * D + c] + dgT[3 * D + c];
 #pragma unroll
@@ -758,6 +779,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     dA = warp_sum(dA);
     if (lane == 0) dAred[warp] = dA;
     tbuf[I * D + c] = ddt;  // ddt_bias partial: this block's dg column sum
+    umma::fence_async_smem();  // the dg rows, for the TMA store
     umma::tc_fence_before();
     __syncthreads();
     if (tid == 0) {
@@ -768,15 +790,23 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     if (p.ddt_part != nullptr && tid < D)
       p.ddt_part[(slot * H + h) * D + tid] =
           (tbuf[tid] + tbuf[D + tid]) + (tbuf[2 * D + tid] + tbuf[3 * D + tid]);
-    bf16 *dgg = reinterpret_cast<bf16 *>(p.dg);
+    if (len == CHUNK) {
+      if (tid == 0) {
+        umma::tma_store_3d(&tm.dg, 0, h, (int)tok0, dgsm);
+        umma::bulk_commit();
+      }
+    } else {
+      bf16 *dgg = reinterpret_cast<bf16 *>(p.dg);
 #pragma unroll 1
-    for (int e = tid; e < 64 * (D / 8); e += NT) {
-      const int i = e >> 4, c8 = (e & 15) * 8;
-      if (i < len)
-        *reinterpret_cast<uint4 *>(dgg + ((tok0 + i) * H + h) * D + c8) =
-            *reinterpret_cast<const uint4 *>(dgsm + i * D + c8);
+      for (int e = tid; e < 64 * (D / 8); e += NT) {
+        const int i = e >> 4, c8 = (e & 15) * 8;
+        if (i < len)
+          *reinterpret_cast<uint4 *>(dgg + ((tok0 + i) * H + h) * D + c8) =
+              *reinterpret_cast<const uint4 *>(dgsm + i * D + c8);
+      }
     }
   }
+  if (tid == 0) umma::bulk_wait_all();  // the stored boxes are complete before the CTA ends
   if (warp == 0) {
     umma::tc_fence_after();
     umma::tmem_dealloc(tbase, 512);

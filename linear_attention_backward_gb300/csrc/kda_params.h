@@ -69,11 +69,15 @@ constexpr size_t kPrepSV = kPrepG + 8192;
 constexpr size_t kPrepSVBytes = 8192;
 constexpr size_t kPrepUnitBytes = kPrepSV + kPrepSVBytes;
 
-// TMA tensor maps of the token-major bf16 inputs [B * T, H, 128]: one box is
-// the 64 rows x 128 channels of one chunk and head, landing row-major
-// (256-byte rows) in shared memory; rows past the tensor's end read as zero.
+// TMA tensor maps of the token-major bf16 tensors [B * T, H, 128]: one box is
+// the 64 rows x 128 channels of one chunk and head, row-major (256-byte rows)
+// in shared memory; rows past the tensor's end read as zero (and are not
+// written by a store).  Inputs q, k, g, v, dO; gradients dq, dk, dv, dg
+// (stored from shared memory for whole chunks).  A null tensor keeps an
+// empty map.
 struct TokenMaps {
   CUtensorMap q, k, g, v, dO;
+  CUtensorMap dq, dk, dv, dg;
 };
 // kda_tmap.cu: encodes the five maps; false if the driver refuses one.
 bool encode_token_maps(const KdaParams &p, TokenMaps &m);

@@ -49,7 +49,8 @@ bool encode_token_maps(const KdaParams &p, TokenMaps &m) {
     return base == nullptr || encode(mp, base, ntok, p.H);
   };
   return enc(&m.q, p.q) && enc(&m.k, p.k) && enc(&m.g, p.g) && enc(&m.v, p.v) &&
-         enc(&m.dO, p.dO);
+         enc(&m.dO, p.dO) && enc(&m.dq, p.dq) && enc(&m.dk, p.dk) && enc(&m.dv, p.dv) &&
+         enc(&m.dg, p.dg);
 }
 
 }  // namespace kda

@@ -146,6 +146,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, i
       : "memory");
 }
 
+// one box of a 3-D tensor map, shared -> global, tracked by the issuing
+// thread's bulk-group counter (the source rows are the box, row-major)
+__device__ __forceinline__ void tma_store_3d(const void *map, int x, int y, int z,
+                                             const void *src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+      : "memory");
+}
 // shared -> global, tracked by the issuing thread's bulk-group counter
 __device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
@@ -158,6 +168,10 @@ __device__ __forceinline__ void bulk_commit() {
 // all committed bulk stores of this thread have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+// all but the most recent committed group have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_but1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
 }
 // ... and are complete
 __device__ __forceinline__ void bulk_wait_all() {
