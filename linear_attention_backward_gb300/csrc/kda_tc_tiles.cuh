@@ -215,16 +215,18 @@ __device__ inline void inverse_inplace(float *Gf, const float *beta, float *tbuf
   // tensor cores: warp J < I takes block (I, J) with mma.m16n8k8 tf32 (fp32
   // accumulation).  tf32 operands round to 2^-11, finer than the bf16 in
   // which the inverse is used.
+  // The sum runs over L = 0 .. I - 1 for every J: the blocks X_LJ above the
+  // diagonal (L < J) hold zeros, so the extra terms vanish and each level's
+  // terms are a fixed, fully unrolled set whose loads overlap.
   const int gid = lane >> 2, tig = lane & 3;
-#pragma unroll 1
+#pragma unroll
   for (int I = 1; I < 4; ++I) {
     float *tw = tbuf + warp * 256;  // this warp's 16 x 16 scratch
     if (warp < I) {
       const int J = warp;
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int L = 0; L < 3; ++L) {  // terms L = J .. I - 1 (unrolled: their loads overlap)
-        if (L < J || L >= I) continue;
+      for (int L = 0; L < I; ++L) {
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           const float *ga = Gf + (16 * I + gid) * LG + 16 * L + 8 * kk + tig;
