@@ -55,10 +55,10 @@ LAUNCHES_PER_STEP = 4
 # is measured again.
 NCU_TRAFFIC = {
     # ncu --set full on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read
-    # 841.3 MB + write 249.1 MB, scaled by 4 to the main workload's 16384
+    # 841.4 MB + write 248.0 MB, scaled by 4 to the main workload's 16384
     # chunk-heads (the kernel's traffic is proportional to the chunk-heads)
-    "kda_grads_tc_kernel": {"sha": "e37eb05d8d49f234", "workload": "main_bf16",
-                            "bytes_per_launch": 4361564160},
+    "kda_grads_tc_kernel": {"sha": "ff27652eece1a9a6", "workload": "main_bf16",
+                            "bytes_per_launch": 4357324800},
 }
 
 KERNEL_SOURCES = {
