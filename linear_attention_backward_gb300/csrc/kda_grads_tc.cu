@@ -153,11 +153,10 @@ __device__ __forceinline__ float rows16_sum(float (&v)[16]) {
 __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, const bf16 *Kr,
                         const bf16 *Gr, const PrepView<bf16, D> &sv, float (&E)[16], void *KDt,
                         uint32_t (&q2)[8], uint32_t (&k2)[8], uint32_t (&g2)[8],
-                        const char *tiles_src, void *tiles, uint64_t *pbar) {
+                        const char *tiles_src, void *tiles, uint64_t *pbar, const float *gsc) {
   const int tid = threadIdx.x;
   const int c = tid & 127, I = tid >> 7;
-  const float A = __expf(p.A_log[h]);
-  const float bias = gate_bias(p, h, c, D);
+  const float A = gsc[0], bias = gsc[D + c];  // e^A_log[h], dt_bias[h][c]
   // gate: running sum over the block, local to the block (see kda_chunk.cuh)
   float d[16];
   {
@@ -226,7 +225,8 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   // ---- views ----
   float *smf = reinterpret_cast<float *>(smem + SM::o_small);
   PrepView<bf16, D> sv = make_view<bf16, D>(smf);
-  float *tbuf = smf + SM::n_view;
+  float *tbuf = smf + SM::n_view;  // [0, 512): ddt_bias partials (K1)
+  float *gsc = tbuf + 512;         // [0]: e^A_log[h]; [128, 256): dt_bias[h][c]
   float *dgT = tbuf + 768;         // [4][128] per-block partials of the gT gradient
   float *red = dgT + 512;          // [16 warps][64]
   float *red2 = red + 1024;        // [4][64]
@@ -262,6 +262,12 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   if (tid >= kBetaT0 && tid - kBetaT0 < len)
     beta_i = __bfloat162float(
         reinterpret_cast<const bf16 *>(p.beta)[(tok0 + (tid - kBetaT0)) * H + h]);
+  // the gate's scalars likewise, by the four warps before them: e^A_log[h] and
+  // the per-channel bias, kept in shared memory (gsc) for the prep and K1 phases
+  constexpr int kGateT0 = kBetaT0 - D;
+  float gate_s = 0.f;
+  if (tid >= kGateT0 && tid < kBetaT0) gate_s = gate_bias(p, h, tid - kGateT0, D);
+  const float eA = tid == kGateT0 ? __expf(p.A_log[h]) : 0.f;
   // ---- barriers, the first copies, then Tensor Memory (all 512 columns) ----
   // Thread 0 initialises the barriers and at once issues the copies: the raw
   // q, k, g rows (row-major, R_A) and the block factors first, the prep phase
@@ -311,6 +317,8 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   cp_async_commit();
   umma::tc_fence_before();
   if (tid >= kBetaT0) sv.beta[tid - kBetaT0] = beta_i;
+  if (tid >= kGateT0 && tid < kBetaT0) gsc[D + tid - kGateT0] = gate_s;
+  if (tid == kGateT0) gsc[0] = eA;
   umma::mbar_wait(rbar, 0);
   if (len < CHUNK) {  // the boxes' rows past the chunk belong to the next sequence: zero them
     for (int e = tid; e < 3 * 64 * 16; e += NT) {
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   uint32_t q2[8], k2[8], g2[8];  // the thread's raw q, k, g rows, two per register
   // (the pair matrices and inverses formed by the prep kernel -- Mqk, INV,
   // INVb, G, packed 64 x 64 -- come into R_A over the raw rows from inside)
-  prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, q2, k2, g2, unit + kPrepMqk, Mqk, pbar);
+  prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, q2, k2, g2, unit + kPrepMqk, Mqk, pbar, gsc);
   cp_async_wait_all();                 // dO, v (and row-major S)
   umma::mbar_wait(lbar, 0);            // S, dS, kr^T
   umma::fence_async_smem();
@@ -755,8 +763,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
 #pragma unroll
     for (int X = 1; X < 4; ++X)
       if (X > I) run += red[X * 128 + c];
-    const float A = __expf(p.A_log[h]);
-    const float bias = gate_bias(p, h, c, D);
+    const float A = gsc[0], bias = gsc[D + c];
     float dA = 0.f, ddt = 0.f;
     bf16 *dgsm = dqs;  // dg rows, [64][128]
 #pragma unroll 4
