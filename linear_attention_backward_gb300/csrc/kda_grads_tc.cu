@@ -13,8 +13,8 @@
 // reverse cumulative sum over the chunk) over its block with the carry of
 // the later blocks.
 //
-// Products (D = A B^T, A: 128 x K, B: N x K; tiles in the padded core layout,
-// "K" / "MN" = how the stored tile is read):
+// Products (D = A B^T, A: 128 x K, B: N x K; tiles in the padded or packed
+// core-matrix layout, "K" / "MN" = how the stored tile is read):
 //   P1  kdS^T[d][i]   = S[c][d] (MN)            x kd[i][c] (K)          N = 64
 //   P2  U^T[d][i]     = Xr^T[d][j] (K)          x INVb[i][j] (K)        N = 64
 //   P3  dU^T[d][i]    = dO[i'][d] (MN) x Mqk[i'][i] (MN)
@@ -23,10 +23,12 @@
 //   P5  dvcorr^T[d][i]= dU^T[d][i'] (K)         x INV[i'][i] (MN)       N = 64
 //   P6  [dvcorr; dO] U^T = [-dAkk | dMqk / s] (rows: dvcorr, then dO)   N = 64
 //   P8  S [dvcorr; dO]^T = [dvcorr S^T | dO S^T]^T                     N = 128
-//   P9  intra-chunk terms, per 16-row block pair, hi + lo operands      N = 64
+//   P9  intra-chunk terms with hi + lo operands: per key block J the dMqk and
+//       dA sides in one product (N = 128 - 32 J), per query block X the
+//       P9c sums (N = 16 (X + 1))
 // The pair matrices G = strict_lower(kd ki^T), scale Mqk, the WY inverse
-// INV = (I + Akk)^-1 and INV diag(beta) come from the prep kernel's
-// per-chunk block (kda_prep_tc.cu), as does kr^T.
+// INV = (I + Akk)^-1 and INV diag(beta), kr^T and the 16-row block factors
+// and row norms come from the prep kernel's per-chunk block (kda_prep_tc.cu).
 #include "kda_chunk.cuh"
 #include "kda_tc_tiles.cuh"
 
@@ -46,25 +48,26 @@ constexpr int NW = NT / 32;        // warps
 // ---- shared memory plan (bytes) ----------------------------------------------
 struct Smem {
   static constexpr size_t n_view = PrepView<bf16, D>::floats;
-  // extra floats: tbuf 768, dgT 4 x 128, red 16 x 64, red2 4 x 64, dbeta 64, dA 16
+  // extra floats: tbuf 768 (ddt_bias partials, gate scalars), dgT 4 x 128, red 16 x 64,
+  // red2 4 x 64, dbeta 64, dA 16
   static constexpr size_t n_extra = 768 + 512 + 1024 + 256 + 64 + 16;
   static constexpr size_t sz_small = (((n_view + n_extra) * 4 + 64 + 1023) / 1024) * 1024;
   static constexpr size_t o_small = 0;
-  // R_A: raw q, k, g (prep, later again) | Gbf, Mqk, INV, INVb (from the prep block)
+  // R_A: raw q, k, g rows (prep phase)  ->  [0, 16K): dv rows, then g rows (K1);
+  // [16K, 48K): Mqk, INV, INVb, G (packed 64 x 64, the prep block's order, one
+  // bulk copy), then dq / dg rows and dk rows
   static constexpr size_t o_A = o_small + sz_small;
-  static constexpr size_t o_Gf = o_A;
-  // packed 64 x 64 tiles in the prep block's order, filled by one bulk copy
-  static constexpr size_t o_Mqk = o_Gf + 64 * 64 * 4;
+  static constexpr size_t o_Mqk = o_A + 16384;
   static constexpr size_t o_INV = o_Mqk + 8192;
   static constexpr size_t o_INVb = o_INV + 8192;
   static constexpr size_t o_Gbf = o_INVb + 8192;
   static constexpr size_t sz_A = 64 * 64 * 4 + 4 * T64x64;  // >= 3 raw tiles
-  // R_B: QMh, KMh, KPh (prep)  ->  S, U  ->  hi tiles (intra)
+  // R_B: S | v rows  ->  S | U^T  ->  hi tiles QMh, KMh, KPh (intra)
   static constexpr size_t o_B = o_A + sz_A;
   static constexpr size_t o_S = o_B;
   static constexpr size_t o_U = o_B + T128x128;
   static constexpr size_t sz_B = 3 * T64x128;
-  // R_C: kd, kr (prep)  ->  Xr^T, dU^T  ->  lo tiles QMl, KMl (intra)
+  // R_C: kd^T, kr^T  ->  Xr^T, dU^T  ->  lo tiles QMl, KMl (intra)  ->  dg columns (K1)
   static constexpr size_t o_C = o_B + sz_B;
   static constexpr size_t sz_C = 2 * T64x128;
   // R_D: dS (128 x 128), then dO (64 x 128)  ->  dMqk, dA | dvcorr ; dvcorr | dO is the
