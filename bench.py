@@ -243,6 +243,57 @@ def workload_config(w):
                   "268 MB at B=4), no flush"}
 
 
+def run_forward(args, w, xh, dev, ws, pg):
+    """The forward pass (prep, forward state scan, chunk outputs) on the
+    workload's inputs, resident in HBM: one JSON line."""
+    import torch
+    import linear_attention_backward_gb300 as kda
+    d = {n: (t.to(dev) if t is not None else None) for n, t in xh.items()}
+    cu = d["cu_seqlens"]
+    shape = kda.make_shape(d["q"], d["v"], cu_seqlens=cu)
+    wsb = torch.empty((kda.workspace_bytes(shape),), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(d["v"])
+    nseq = w.B if cu is None else cu.numel() - 1
+    hT = torch.empty((nseq, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+
+    def step():
+        kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d.get("h0"),
+                cu_seqlens=cu, o=o, hT=hT, want_hT=True, workspace=wsb)
+
+    for _ in range(args.warmup):
+        step()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    s0.record()
+    for _ in range(args.steps):
+        step()
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / args.steps
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    assert kda.get_device_status() == 0
+    tokens = int(xh["q"].shape[0] * xh["q"].shape[1])
+    cfg = workload_config(w)
+    cfg["workload"] = cfg["workload"].replace("chunked backward", "chunked forward").replace(
+        "states recomputed in the call", "o and hT")
+    line = {"metric": "KDA forward tokens/s (kda_fwd: o and hT)", "value": tokens * ws / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "gpu_launches": 3 + (0 if cu is None else 1)}
+    if int(os.environ.get("RANK", "0")) == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -253,6 +304,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload name (default: the main B=4 T=8192 H=32 batch)")
+    ap.add_argument("--forward", action="store_true",
+                    help="time the forward pass (kda_fwd: o and hT) instead of the backward")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_setup()
@@ -276,6 +329,8 @@ def main():
 
     w = wl.WORKLOADS[args.workload]
     xh = wl.make_inputs(w, seed=rank)
+    if args.forward:
+        return run_forward(args, w, xh, dev, ws, pg)
     names_in = ["q", "k", "v", "g", "beta", "dO", "A_log"]
     if w.with_h0:
         names_in.append("h0")
