@@ -195,6 +195,22 @@ def test_states_given_matches_internal_recompute():
     _compare(g3, ref, x, TOL["bf16"])
 
 
+def test_states_given_with_gate_bias():
+    # kda_fwd_states with the gate bias feeds kda_bwd with the same bias
+    w = wl.custom("sb", B=2, T=170, H=2, K=128, V=128, dtype="bf16", with_h0=True,
+                  with_dhT=True)
+    x = _with_bias(wl.make_inputs(w, seed=14), 9)
+    d = {n: (t.cuda() if t is not None else None) for n, t in x.items()}
+    states = kda.fwd_states(d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"],
+                            dt_bias=d["dt_bias"])
+    g, _ = gpu_bwd(x, states=states)
+    _check_status()
+    ref = oracle_bwd(x)
+    keys = tuple(k for k in GRADS if k != "dA_log") + ("ddt_bias",)
+    _compare(g, ref, x, TOL["bf16"], keys=keys)
+    _check_dalog(g, ref, x, TOL["bf16"])
+
+
 def test_repeatable_bitwise():
     w = wl.custom("r", B=2, T=256, H=4, K=128, V=128, dtype="bf16")
     x = wl.make_inputs(w, seed=2)
