@@ -119,9 +119,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   //   forward: slot 0 = gT | W^T (MMA1), slot 1 = U0^T (epilogue 1), slot 2 = kr^T (MMA2)
   //   reverse: slot 0 = kr^T (MMA1), slot 1 = gT | W^T, QE^T (+ dO rows) (MMA2)
   // A slot is refilled with the next chunk's data as soon as its consumer is done.
+  // Slot sl's copies are issued by thread 32 (sl + 1) (warps 1-3), publishing
+  // and prefetching by threads 160 and 192: thread 0 only issues the MMAs.
   auto load_slot = [&](int sl, int it) {
     const char *u = unit_of(chunk_of(it));
-    if (tid == 0) {
+    if (tid == 32 * (sl + 1)) {
       if (fwd) {
         if (sl == 0) {
           umma::mbar_expect_tx(bars + 0, kPrepKR);
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   auto prefetch = [&](int it) {
     const int j = chunk_of(it);
     const char *u = unit_of(j);
-    if (tid == 0) {
+    if (tid == 192) {
       if (fwd) {
         umma::bulk_prefetch_l2(u, kInFwd);
       } else {
@@ -184,9 +186,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
     for (int q = 0; q < 8; ++q) st16_bf(Xs + umma::core_off(ch, 64 * hf + 8 * q, D), X + 8 * q);
   };
   // the bf16 tile (the state chunk j starts from) -> the chunk's slot in HBM,
-  // one bulk copy by thread 0 once the tile is complete and fenced
+  // one bulk copy by thread 160 once the tile is complete and fenced
   auto publish = [&](int j) {
-    if (tid == 0) {
+    if (tid == 160) {
       umma::bulk_s2g(states_out + ((size_t)(slot0 + j) * H + h) * DD, Xs, (uint32_t)(DD * 2));
       umma::bulk_commit();
     }
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
     }
     ok = wait_bar(3);
     umma::tc_fence_after();
-    if (more && tid == 0) load_slot(0, it + 1);  // MMA1's operand is consumed
+    if (more) load_slot(0, it + 1);  // MMA1's operand is consumed
     // ---- U^T[v][i] for lane v = ch, i in [32 hf, 32 hf + 32) ----
     {
       float t[32];
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
       bad = true;
       break;
     }
-    if (fwd && more && tid == 0) load_slot(1, it + 1);  // U0^T is consumed
+    if (fwd && more) load_slot(1, it + 1);  // U0^T is consumed
     // ---- MMA2: T2 into columns [64, 192) ----
     if (tid == 0) {
       bool ok2 = true;
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
     }
     ok = wait_bar(3) && ok;
     umma::tc_fence_after();
-    if (tid == 0) umma::bulk_wait_read();  // the tile's previous store has read it
+    if (tid == 160) umma::bulk_wait_read();  // the tile's previous store has read it
     if (__syncthreads_or(!ok)) {
       bad = true;
       break;
@@ -334,7 +336,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
             make_float4(X[4 * q], X[4 * q + 1], X[4 * q + 2], X[4 * q + 3]);
     }
   }
-  if (tid == 0) umma::bulk_wait_all();
+  if (tid == 160) umma::bulk_wait_all();
   umma::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
