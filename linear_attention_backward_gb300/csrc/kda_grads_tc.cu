@@ -44,6 +44,9 @@ constexpr uint32_t T128x64 = umma::ptile_bytes(128, 64);    // 18432
 
 constexpr int NT = 512;            // threads per CTA
 constexpr int NW = NT / 32;        // warps
+// the thread that issues the TMA stores of the gradient rows (and waits on
+// them): not thread 0, which issues the MMAs that follow some of them
+constexpr int kStoreT = 32;
 
 // ---- shared memory plan (bytes) ----------------------------------------------
 struct Smem {
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   {  // dv rows: one TMA box for a whole chunk, else 16-byte row pieces (alongside P6 / P8)
     const bf16 *dvs = reinterpret_cast<const bf16 *>(smem + SM::o_A);
     if (len == CHUNK) {
-      if (tid == 0) {
+      if (tid == kStoreT) {
         umma::tma_store_3d(&tm.dv, 0, h, (int)tok0, dvs);
         umma::bulk_commit();
       }
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   umma::fence_async_smem();
   umma::tc_fence_before();
-  if (tid == 0) umma::bulk_wait_read();  // the dv box has left R_A [0, 16K) (the g rows go there)
+  if (tid == kStoreT) umma::bulk_wait_read();  // the dv box has left R_A [0, 16K) (the g rows go there)
   __syncthreads();
   if (tid < 64 && tid < len) {
     const float db = dbs[tid] + red2[tid] + red2[64 + tid] + red2[128 + tid] + red2[192 + tid];
@@ -650,7 +653,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   umma::tc_fence_before();
   __syncthreads();
   if (len == CHUNK) {
-    if (tid == 0) {
+    if (tid == kStoreT) {
       umma::tma_store_3d(&tm.dq, 0, h, (int)tok0, dqs);
       umma::bulk_commit();
     }
@@ -746,7 +749,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
 #pragma unroll
     for (int r = 0; r < 16; ++r) dgs[r * NT + tid] = dgc[r];
     if (len == CHUNK) {
-      if (tid == 0) {
+      if (tid == kStoreT) {
         umma::tma_store_3d(&tm.dk, 0, h, (int)tok0, dks);
         umma::bulk_commit();
       }
@@ -760,7 +763,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
               *reinterpret_cast<const uint4 *>(dks + i * D + c8);
       }
     }
-    if (tid == 0) umma::bulk_wait_read_but1();  // the dq box has left (dg rows go there)
+    if (tid == kStoreT) umma::bulk_wait_read_but1();  // the dq box has left (dg rows go there)
     __syncthreads();
     float run = dgT[c] + dgT[D + c] + dgT[2 * D + c] + dgT[3 * D + c];
 #pragma unroll
@@ -801,7 +804,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       p.ddt_part[(slot * H + h) * D + tid] =
           (tbuf[tid] + tbuf[D + tid]) + (tbuf[2 * D + tid] + tbuf[3 * D + tid]);
     if (len == CHUNK) {
-      if (tid == 0) {
+      if (tid == kStoreT) {
         umma::tma_store_3d(&tm.dg, 0, h, (int)tok0, dgsm);
         umma::bulk_commit();
       }
@@ -816,7 +819,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       }
     }
   }
-  if (tid == 0) umma::bulk_wait_all();  // the stored boxes are complete before the CTA ends
+  if (tid == kStoreT) umma::bulk_wait_all();  // the stored boxes are complete before the CTA ends
   if (warp == 0) {
     umma::tc_fence_after();
     umma::tmem_dealloc(tbase, 512);
