@@ -47,7 +47,16 @@ ALG_FLOP = {"grads": 16.8e6 / 64, "path": 38.1e6 / 64}
 PHASES = ("prep", "scan", "grads", "reduce")
 KERNEL_NAMES = {"prep": "kda_prep_tc_kernel", "scan": "kda_scan_tc_kernel",
                 "grads": "kda_grads_tc_kernel", "reduce": "kda_dalog_reduce_kernel"}
+# kernels of one kda_bwd call: prep, scans, gradients, dA_log reduction; a
+# varlen call adds the sequence-order kernel, context-parallel scans (few
+# (sequence, head) chains) add their combine kernel and second scan pass
 LAUNCHES_PER_STEP = 4
+
+
+def launches_per_step(shape, cu, forward=False):
+    import linear_attention_backward_gb300 as kda
+    n = (3 if forward else LAUNCHES_PER_STEP) + (0 if cu is None else 1)
+    return n + (2 if kda.scan_segments(shape) > 0 else 0)
 
 # DRAM traffic per launch of the gradient kernel from ncu
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the hash of the
@@ -55,10 +64,10 @@ LAUNCHES_PER_STEP = 4
 # is measured again.
 NCU_TRAFFIC = {
     # ncu --set full on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read
-    # 841.4 MB + write 248.0 MB, scaled by 4 to the main workload's 16384
+    # 841.2 MB + write 248.0 MB, scaled by 4 to the main workload's 16384
     # chunk-heads (the kernel's traffic is proportional to the chunk-heads)
-    "kda_grads_tc_kernel": {"sha": "ff27652eece1a9a6", "workload": "main_bf16",
-                            "bytes_per_launch": 4357324800},
+    "kda_grads_tc_kernel": {"sha": "6cc2332ec6f4c1b5", "workload": "main_bf16",
+                            "bytes_per_launch": 4356828160},
 }
 
 KERNEL_SOURCES = {
@@ -232,6 +241,15 @@ def run_reference(args, ws, rank):
     return 0
 
 
+L2_BYTES = 129 << 20  # GB300 L2
+
+
+def flushes_l2(w):
+    """Workloads whose input tensors fit in L2 get a 256 MB write between
+    timed steps, and only the calls themselves are timed."""
+    return w.B * w.T * w.H * w.K * 2 < L2_BYTES if not w.varlen else False
+
+
 def workload_config(w):
     shape = (f"{w.varlen[0]} packed sequences of U[{w.varlen[1]}, {w.varlen[2]}] tokens"
              if w.varlen else f"B={w.B} T={w.T}")
@@ -239,8 +257,11 @@ def workload_config(w):
                         f"K={w.K} V={w.V} chunk={w.chunk}, states recomputed in the call",
             "global_batch": w.B, "seq_len": w.T, "heads": w.H, "head_dim": w.K,
             "parallelism": "replicas (one independent batch per GPU)",
-            "l2": "inputs larger than L2 (each input tensor is B*T*H*128*2 bytes; "
-                  "268 MB at B=4), no flush"}
+            "l2": ("L2 flushed between timed steps (a 256 MB buffer written outside the "
+                   "timed calls; each input tensor is B*T*H*128*2 bytes, below the 129 MB L2)"
+                   if flushes_l2(w) else
+                   "inputs larger than L2 (each input tensor is B*T*H*128*2 bytes; "
+                   "268 MB at B=4), no flush")}
 
 
 def run_forward(args, w, xh, dev, ws, pg):
@@ -267,12 +288,21 @@ def run_forward(args, w, xh, dev, ws, pg):
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev) if flushes_l2(w) else None
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
     s0.record()
-    for _ in range(args.steps):
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 255)
+        pairs[i][0].record()
         step()
+        pairs[i][1].record()
     s1.record()
     torch.cuda.synchronize()
     ms = s0.elapsed_time(s1) / args.steps
+    if flush is not None:  # the calls alone
+        ms = sum(a.elapsed_time(b) for a, b in pairs) / args.steps
     if pg:
         t = torch.tensor([ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -286,7 +316,8 @@ def run_forward(args, w, xh, dev, ws, pg):
             "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": cfg,
-            "gpu_launches": 3 + (0 if cu is None else 1)}
+            "gpu_launches": launches_per_step(shape, cu, forward=True) * args.steps,
+            "scan_segments": kda.scan_segments(shape)}
     if int(os.environ.get("RANK", "0")) == 0:
         print(json.dumps(line), flush=True)
     if pg:
@@ -366,6 +397,7 @@ def main():
             e.record()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev) if flushes_l2(w) else None
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
@@ -375,6 +407,8 @@ def main():
     torch.cuda.synchronize()
     start.record()
     for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 255)
         step(evs[i])
     end.record()
     torch.cuda.synchronize()
@@ -382,6 +416,8 @@ def main():
     if pg:
         pg.barrier()
     ms = start.elapsed_time(end)
+    if flush is not None:  # the calls alone, from their first to their last event
+        ms = sum(e5[0].elapsed_time(e5[4]) for e5 in evs)
     phase = {n: [] for n in PHASES}
     for e5 in evs:
         for j, n in enumerate(PHASES):
@@ -490,7 +526,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(w), "clocks": clocks, "e2e": e2e,
-        "gpu_launches": LAUNCHES_PER_STEP * K, "roofline": roofline, "path_roofline": path,
+        "gpu_launches": launches_per_step(shape, cu) * K, "scan_segments": kda.scan_segments(shape),
+        "roofline": roofline, "path_roofline": path,
         "kernels_ms": kern_ms, "kernels": KERNEL_NAMES,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

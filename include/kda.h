@@ -97,7 +97,9 @@ int64_t kda_num_chunk_slots(const kda_shape *shape);
  * state gradients dS (same size), per-chunk dA_log and ddt_bias partials
  * ([slots, H] and [slots, H, K] fp32) and, for bf16
  * with K = V = 128, the per-chunk operand blocks of the tensor-core scans
- * (107008 bytes per slot and head).  Returns 0 on a bad shape. */
+ * (107008 bytes per slot and head) and, where kda_scan_segments() > 0, the
+ * segment boundary tiles of the context-parallel scans.  Returns 0 on a bad
+ * shape. */
 size_t kda_workspace_bytes(const kda_shape *shape);
 /* Byte offset inside the workspace of the per-chunk state gradients
  * dS_{n+1} (the adjoint of the state at the END of chunk n), [slots, H]
@@ -107,6 +109,26 @@ size_t kda_workspace_bytes(const kda_shape *shape);
  * states kda_bwd recomputes at the start of the workspace; otherwise tiles
  * are row-major.  Exposed so that tests can check the scans on their own. */
 size_t kda_workspace_dstates_offset(const kda_shape *shape);
+/* Segments per sequence of the context-parallel state scans that kda_bwd and
+ * kda_fwd run for this shape; 0 means one scan chain per (sequence, head,
+ * role).  The serial chunk scans are the part of the backward that does not
+ * fill the GPU when B * H is small (with a single sequence the reverse scan,
+ * Kernel A of "bwd-ncu-and-optimization-playbook", A/B table, takes about
+ * half of the backward there; its split-V remedy, ibid. §3.5, adds CTAs but
+ * shortens no chain).  With A_n = diag(e^gT) - kr^T W the chunk
+ * updates are affine (S_{n+1} = A_n S_n + kr^T U0, dS_n = A_n^T dS_{n+1} +
+ * QE^T dO), so each sequence's chunks split into P segments: every segment is
+ * scanned from zero, the inner segments' transfer products A_{b-1}..A_a are
+ * formed, a combine kernel chains the segment boundaries, and the segments
+ * are scanned again from the true boundaries (two more launches than the
+ * whole-sequence scans).  Used for fixed-length bf16 K = V = 128 shapes with
+ * 2 * B * H < 152 (the SM count) and at least 4 P chunks per sequence: the
+ * most segments, 3 to 8, whose first-pass chains fit one per SM.  The
+ * workspace then ends with (3 P - 4) fp32 K x V tiles per (sequence, head).
+ * The environment variable KDA_SCAN_CP=0 turns this off per call, and
+ * KDA_SCAN_CP=n (3 <= n <= the value without it) takes n segments.
+ * Returns 0 on a bad shape. */
+int kda_scan_segments(const kda_shape *shape);
 /* Forward chunk-state recompute (the "all_states" operand of kernel B2 in
  * "bwd-kernelB-beginner-guide-full", Part 2, B2 optimisation 4).
  *   states : OUT [slots, H, K, V], dtype of the shape: S at the start of

@@ -67,6 +67,8 @@ def lib():
         L.kda_workspace_bytes.restype = ctypes.c_size_t
         L.kda_workspace_dstates_offset.argtypes = [S]
         L.kda_workspace_dstates_offset.restype = ctypes.c_size_t
+        L.kda_scan_segments.argtypes = [S]
+        L.kda_scan_segments.restype = ctypes.c_int
         L.kda_fwd_states.argtypes = [S] + [_VP] * 10
         L.kda_fwd_states.restype = ctypes.c_int
         L.kda_fwd.argtypes = [S] + [_VP] * 11 + [ctypes.c_size_t, _VP]
@@ -122,6 +124,11 @@ def workspace_bytes(shape: KdaShape) -> int:
 
 def workspace_dstates_offset(shape: KdaShape) -> int:
     return int(lib().kda_workspace_dstates_offset(ctypes.byref(shape)))
+
+
+def scan_segments(shape: KdaShape) -> int:
+    """Segments of the context-parallel state scans for this shape (0: none)."""
+    return int(lib().kda_scan_segments(ctypes.byref(shape)))
 
 
 def check_cu_seqlens_host(cu_seqlens_cpu: torch.Tensor, total_T: int) -> int:

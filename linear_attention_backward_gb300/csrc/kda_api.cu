@@ -93,8 +93,42 @@ bool legacy_scan() {
 
 kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+// Segments of the context-parallel tcgen05 scans (0: whole-sequence chains).
+// Used for fixed-length sequences when the whole-sequence chains (two per
+// sequence and head) leave most SMs idle: the most segments (3..8, at least
+// four chunks each) whose phase-1 chains, kda_cp_tiles(P) per sequence and
+// head, still fit one per SM.  A function of the shape, so that the
+// workspace size is too.
+int cp_segments(const kda_shape *s) {
+  if (!tc_state_path(s) || s->cu_seqlens != nullptr) return 0;
+  const int64_t units = (int64_t)s->B * s->H;
+  const int nck = (s->T + kChunk - 1) / kChunk;
+  if (2 * units >= kTargetCtas) return 0;
+  int best = 0;
+  for (int P = 3; P <= 8; ++P)
+    if (kda::kda_cp_tiles(P) * units <= kTargetCtas && nck >= 4 * P) best = P;
+  return best;
+}
+
+// Segments a call uses: KDA_SCAN_CP=0 turns the context-parallel scans off,
+// KDA_SCAN_CP=n (3 <= n <= cp_segments) takes n segments, for comparisons.
+int cp_segments_used(const kda_shape *s) {
+  const int P = cp_segments(s);
+  const char *e = getenv("KDA_SCAN_CP");
+  if (e == nullptr || P == 0) return P;
+  const int n = atoi(e);
+  if (n == 0) return 0;
+  return n >= 3 && n <= P ? n : P;
+}
+
+size_t cp_bytes(const kda_shape *s) {
+  return round_up((size_t)s->B * s->H * (size_t)kda::kda_cp_tiles(cp_segments(s)) * s->K *
+                  s->V * sizeof(float));
+}
+
 // Workspace layout: states | dS | dA_log partials [slots, H] | ddt_bias
-// partials [slots, H, K] | per-chunk operand blocks (tcgen05 path).
+// partials [slots, H, K] | per-chunk operand blocks (tcgen05 path) |
+// boundary tiles of the context-parallel scans.
 size_t dA_part_offset(const kda_shape *s) { return 2 * states_bytes(s); }
 size_t ddt_part_offset(const kda_shape *s) {
   return dA_part_offset(s) + round_up((size_t)slots_of(s) * s->H * sizeof(float));
@@ -102,12 +136,13 @@ size_t ddt_part_offset(const kda_shape *s) {
 size_t prep_offset(const kda_shape *s) {
   return ddt_part_offset(s) + round_up((size_t)slots_of(s) * s->H * s->K * sizeof(float));
 }
+size_t cp_offset(const kda_shape *s) { return prep_offset(s) + prep_bytes(s); }
 
 }  // namespace
 
 extern "C" {
 
-int kda_abi_version(void) { return 4; }
+int kda_abi_version(void) { return 5; }
 
 const char *kda_status_str(kda_status st) {
   switch (st) {
@@ -133,9 +168,14 @@ size_t kda_workspace_dstates_offset(const kda_shape *shape) {
   return states_bytes(shape);
 }
 
+int kda_scan_segments(const kda_shape *shape) {
+  if (check_shape(shape) != KDA_OK) return 0;
+  return cp_segments_used(shape);
+}
+
 size_t kda_workspace_bytes(const kda_shape *shape) {
   if (check_shape(shape) != KDA_OK) return 0;
-  return prep_offset(shape) + prep_bytes(shape);
+  return cp_offset(shape) + cp_bytes(shape);
 }
 
 kda_status kda_check_cu_seqlens_host(const int32_t *cu, int num_seqs, int total_T) {
@@ -221,7 +261,15 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
     p.seq_order = reinterpret_cast<const int32_t *>(p.dA_part);
     e = kda::seq_order_launch(p.cu, p.num_seqs, reinterpret_cast<int32_t *>(p.dA_part), cs);
   }
-  if (e == cudaSuccess) e = kda::scan_tc_launch(p, p.prep, 1, cs);
+  const int cp = cp_segments_used(shape);
+  if (e == cudaSuccess && cp >= 3) {
+    p.cp_segs = cp;
+    p.cp_buf = reinterpret_cast<float *>(w + cp_offset(shape));
+    e = kda::scan_tc_cp_launch(p, p.prep, 1, cs);
+    p.cp_segs = 0;
+  } else if (e == cudaSuccess) {
+    e = kda::scan_tc_launch(p, p.prep, 1, cs);
+  }
   if (e == cudaSuccess) e = kda::out_tc_launch(p, p.states, o, cs);
   return from_cuda(e);
 }
@@ -315,7 +363,16 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
       p.seq_order = reinterpret_cast<const int32_t *>(p.dA_part);
       e = kda::seq_order_launch(p.cu, p.num_seqs, reinterpret_cast<int32_t *>(p.dA_part), cs);
     }
-    if (e == cudaSuccess) e = kda::scan_tc_launch(p, p.prep, nroles, cs);
+    const int cp = cp_segments_used(shape);
+    if (e == cudaSuccess && cp >= 3) {
+      // few (sequence, head) chains: context-parallel scans over segments
+      p.cp_segs = cp;
+      p.cp_buf = reinterpret_cast<float *>(w + cp_offset(shape));
+      e = kda::scan_tc_cp_launch(p, p.prep, nroles, cs);
+      p.cp_segs = 0;
+    } else if (e == cudaSuccess) {
+      e = kda::scan_tc_launch(p, p.prep, nroles, cs);
+    }
   } else if (e == cudaSuccess) {
     const int bv = pick_band(shape, nroles);
     p.nb = shape->V / bv;

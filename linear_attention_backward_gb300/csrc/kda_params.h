@@ -35,7 +35,22 @@ struct KdaParams {
   int states_packed, dstates_packed;
   const char *prep;           // per-chunk operand blocks (bf16, K = V = 128), see below
   const int32_t *seq_order;   // tcgen05 scans: sequences longest first (varlen), or null
+  // Context-parallel tcgen05 scans (fixed-length sequences only): each
+  // sequence's chunks are split into cp_segs >= 3 segments, segment g holding
+  // chunks [g nck / cp_segs, (g + 1) nck / cp_segs).  cp_phase 1 runs every
+  // segment's local scan and the transfer matrices, 2 (the combine kernel)
+  // chains them into the true segment boundaries, 3 reruns the segments
+  // from those boundaries; cp_nroles roles from role_base take part.
+  // cp_buf holds kda_cp_tiles(cp_segs) fp32 K x V row-major tiles per
+  // (sequence, head); see kda_scan_tc.cu.  cp_segs = 0: whole-sequence chains.
+  int cp_segs, cp_phase, cp_nroles;
+  float *cp_buf;
 };
+
+// fp32 K x V tiles per (sequence, head) of the context-parallel scans:
+// forward segment starts (P - 1), reverse segment ends (P - 1) and the
+// transfer matrices of the inner segments (P - 2).
+__host__ __device__ constexpr int kda_cp_tiles(int P) { return P >= 3 ? 3 * P - 4 : 0; }
 
 // Per-chunk operands of the state scans (bf16, K = V = 128), one block of
 // kPrepUnitBytes per (chunk slot, head), written by the chunk-parallel prep
@@ -89,6 +104,9 @@ int prep_tc_status_take();
 // kda_scan_tc.cu: both state scans on tcgen05 from the prep buffer; roles
 // as in scan_dispatch.
 cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cudaStream_t st);
+// the three phases of the context-parallel scans (p.cp_segs >= 3, fixed
+// length); p.role_base and nroles as for scan_tc_launch
+cudaError_t scan_tc_cp_launch(KdaParams p, const void *prep, int nroles, cudaStream_t st);
 // order[r] = the sequence of rank r by length (longest first, ties by index)
 cudaError_t seq_order_launch(const int32_t *cu, int num_seqs, int32_t *order, cudaStream_t st);
 int scan_tc_status_take();

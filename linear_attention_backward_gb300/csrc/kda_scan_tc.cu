@@ -54,45 +54,125 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   using namespace stc;
   using SM = stc::Smem;
   extern __shared__ __align__(1024) char smem[];
-  // block b -> (sequence rank r, role, head) for varlen: the chains of the
-  // longest sequences are dispatched first, so that short chains fill in
-  // behind them instead of a long one starting last; fixed length (all
-  // chains equally long): (role, sequence, head).  The reverse role (the
-  // longer chain of work per chunk) goes first in both.
   const int H = p.H;
   const int nseq = p.cu ? p.num_seqs : p.B;
-  const int nroles = (int)(gridDim.x / (unsigned)(nseq * H));
-  int r, rl, h;
-  if (p.seq_order != nullptr) {
-    r = (int)(blockIdx.x / (unsigned)(nroles * H));
-    const int rem = (int)(blockIdx.x % (unsigned)(nroles * H));
-    rl = nroles - 1 - rem / H;
-    h = rem % H;
-  } else {
-    rl = nroles - 1 - (int)(blockIdx.x / (unsigned)(nseq * H));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const size_t DD = (size_t)D * D;
+  int r, h, role;
+  int g = -1;  // context-parallel segment (-1: the whole sequence)
+  if (p.cp_segs >= 3) {
+    // context-parallel chain kinds (fixed length), kind-major then (sequence, head):
+    //  phase 1: reverse-local g = 1..P-1, forward-local g = 0..P-2 (zero
+    //           start, or dh_T / h0 for the outermost), transfers g = 1..P-2;
+    //  phase 3: reverse g = 0..P-2, forward g = 1..P-1 from the combined
+    //           boundaries.
+    const int P = p.cp_segs;
+    const bool has_rev = p.role_base + p.cp_nroles > 1, has_fwd = p.role_base == 0;
+    int kind = (int)(blockIdx.x / (unsigned)(nseq * H));
     const int rem = (int)(blockIdx.x % (unsigned)(nseq * H));
     r = rem / H;
     h = rem % H;
+    role = -1;
+    if (has_rev) {
+      if (kind < P - 1) {
+        role = 1;
+        g = p.cp_phase == 1 ? kind + 1 : kind;
+      }
+      kind -= P - 1;
+    }
+    if (role < 0 && has_fwd) {
+      if (kind >= 0 && kind < P - 1) {
+        role = 0;
+        g = p.cp_phase == 1 ? kind : kind + 1;
+      }
+      kind -= P - 1;
+    }
+    if (role < 0 && p.cp_phase == 1 && kind >= 0 && kind < P - 2) {
+      role = 2;
+      g = kind + 1;
+    }
+    if (role < 0) return;
+  } else {
+    // block b -> (sequence rank r, role, head) for varlen: the chains of the
+    // longest sequences are dispatched first, so that short chains fill in
+    // behind them instead of a long one starting last; fixed length (all
+    // chains equally long): (role, sequence, head).  The reverse role (the
+    // longer chain of work per chunk) goes first in both.
+    const int nroles = (int)(gridDim.x / (unsigned)(nseq * H));
+    int rl;
+    if (p.seq_order != nullptr) {
+      r = (int)(blockIdx.x / (unsigned)(nroles * H));
+      const int rem = (int)(blockIdx.x % (unsigned)(nroles * H));
+      rl = nroles - 1 - rem / H;
+      h = rem % H;
+    } else {
+      rl = nroles - 1 - (int)(blockIdx.x / (unsigned)(nseq * H));
+      const int rem = (int)(blockIdx.x % (unsigned)(nseq * H));
+      r = rem / H;
+      h = rem % H;
+    }
+    role = p.role_base + rl;
   }
-  const int role = p.role_base + rl;  // 0: forward states, 1: reverse dS scan
-  const bool fwd = role == 0;
+  // role 0: forward states, 1: reverse dS scan, 2: forward transfer matrix
+  // (the forward update with U0 = 0 from the identity: the product of the
+  // segment's chunk transitions S -> e^gT S - kr^T W S)
+  const bool fwd = role != 1;
   const int s = p.seq_order ? p.seq_order[r] : r;
-  const int tid = threadIdx.x, warp = tid >> 5;
   int64_t tok_seq, slot0;
   int L;
   if (!seq_bounds(p, s, tok_seq, L, slot0)) return;
-  const int nck = (L + CHUNK - 1) / CHUNK;
+  const int nck_seq = (L + CHUNK - 1) / CHUNK;
+  // this chain's chunks [c0, c0 + nck), its start and end tiles (row-major
+  // fp32 K x V, nullable) and whether it stores the chunk states
+  int c0 = 0, nck = nck_seq;
+  const float *init;
+  float *fin;
+  bool pub = true;
+  {
+    const size_t sh = ((size_t)s * H + h) * DD;
+    const float *outer_in = role == 1 ? p.dhT : p.h0;
+    float *outer_out = role == 1 ? p.dh0 : p.hT;
+    init = outer_in ? outer_in + sh : nullptr;
+    fin = outer_out ? outer_out + sh : nullptr;
+    if (g >= 0) {
+      const int P = p.cp_segs;
+      c0 = (int)((int64_t)g * nck_seq / P);
+      nck = (int)((int64_t)(g + 1) * nck_seq / P) - c0;
+      float *tiles = p.cp_buf + ((size_t)s * H + h) * (size_t)kda_cp_tiles(P) * DD;
+      if (p.cp_phase == 1) {
+        if (role == 0) {  // local from h0 (g = 0, the true states) or zero
+          if (g > 0) init = nullptr;
+          pub = g == 0;
+          fin = tiles + (size_t)g * DD;
+        } else if (role == 1) {  // local from dh_T (g = P - 1) or zero
+          if (g < P - 1) init = nullptr;
+          pub = g == P - 1;
+          fin = tiles + (size_t)(P - 1 + g - 1) * DD;
+        } else {
+          init = nullptr;
+          pub = false;
+          fin = tiles + (size_t)(2 * (P - 1) + g - 1) * DD;
+        }
+      } else {
+        if (role == 0) {
+          init = tiles + (size_t)(g - 1) * DD;
+          if (g < P - 1) fin = nullptr;
+        } else {
+          init = tiles + (size_t)(P - 1 + g) * DD;
+          if (g > 0) fin = nullptr;
+        }
+      }
+    }
+  }
   char *Xs = smem + SM::o_X, *IN = smem + SM::o_IN, *dOs = smem + SM::o_dO, *Us = smem + SM::o_U;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::o_bar);  // 3 operand slots + MMA
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 4);
 
   const int ch = tid & 127, hf = tid >> 7;  // TMEM lane; half of the columns
-  const size_t DD = (size_t)D * D;
   // running state: row ch, columns [64 hf, 64 hf + 64)
   float X[64];
   {
-    const float *init = fwd ? p.h0 : p.dhT;
-    const float *src = init ? init + ((size_t)s * H + h) * DD + (size_t)ch * D + 64 * hf : nullptr;
+    const float *src = init ? init + (size_t)ch * D + 64 * hf : nullptr;
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
       const float4 v = src ? *reinterpret_cast<const float4 *>(src + 4 * q)
@@ -102,6 +182,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
       X[4 * q + 2] = v.z;
       X[4 * q + 3] = v.w;
     }
+    if (role == 2) {  // the identity
+#pragma unroll
+      for (int q = 0; q < 64; ++q) X[q] = 64 * hf + q == ch ? 1.f : 0.f;
+    }
   }
   if (warp == 0) umma::tmem_alloc(tslot, 256);
   if (tid == 0) {
@@ -110,7 +194,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   __syncthreads();
 
-  auto chunk_of = [&](int it) { return fwd ? it : nck - 1 - it; };
+  auto chunk_of = [&](int it) { return fwd ? c0 + it : c0 + nck - 1 - it; };
   auto unit_of = [&](int j) {
     return prep + ((size_t)(slot0 + j) * H + h) * kPrepUnitBytes;
   };
@@ -188,7 +272,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   // the bf16 tile (the state chunk j starts from) -> the chunk's slot in HBM,
   // one bulk copy by thread 160 once the tile is complete and fenced
   auto publish = [&](int j) {
-    if (tid == 160) {
+    if (pub && tid == 160) {
       umma::bulk_s2g(states_out + ((size_t)(slot0 + j) * H + h) * DD, Xs, (uint32_t)(DD * 2));
       umma::bulk_commit();
     }
@@ -250,8 +334,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
         for (int q = 0; q < 4; ++q) {
           float u0[8];
           ld16_bf(IN + kPrepU0 + umma::core_off(ch, 32 * hf + 8 * q, 64), u0);
+          const float keep = role == 0 ? 1.f : 0.f;  // the transfer drops U0
 #pragma unroll
-          for (int n = 0; n < 8; ++n) t[8 * q + n] = u0[n] - t[8 * q + n];
+          for (int n = 0; n < 8; ++n) t[8 * q + n] = fmaf(keep, u0[n], -t[8 * q + n]);
         }
       } else {
 #pragma unroll
@@ -327,9 +412,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
     cp_async_wait_all();
     __syncthreads();
   } else {
-    float *fin = fwd ? p.hT : p.dh0;
     if (fin != nullptr) {
-      float *dst = fin + ((size_t)s * H + h) * DD + (size_t)ch * D + 64 * hf;
+      float *dst = fin + (size_t)ch * D + 64 * hf;
 #pragma unroll
       for (int q = 0; q < 16; ++q)
         *reinterpret_cast<float4 *>(dst + 4 * q) =
@@ -354,6 +438,126 @@ cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cud
   if (nunits == 0 || nroles == 0) return cudaSuccess;
   if (nroles < 1 || p.role_base + nroles > 2) return cudaErrorInvalidValue;
   kfn<<<(unsigned)(nunits * nroles), NTHREADS, stc::Smem::total, st>>>(
+      p, static_cast<const char *>(prep));
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Context-parallel scans.  With A_n = e^gT - kr^T W the forward update is
+// S_{n+1} = A_n S_n + kr^T U0 and the reverse one dS_n = A_n^T dS_{n+1} +
+// QE^T dO, so over a segment of chunks [a, b), with P_g = A_{b-1} ... A_a,
+//   S_b  = P_g S_a + E_g       (E_g: the segment's forward scan from zero)
+//   dS_a = P_g^T dS_b + F_g    (F_g: its reverse scan from zero)
+// Phase 1 scans every segment from zero (the first forward and the last
+// reverse segment from h0 / dh_T, which makes their states final) and the
+// inner segments' P_g from the identity; the combine kernel below chains the
+// boundaries; phase 3 rescans the remaining segments from them.  Tiles per
+// (sequence, head), fp32 row-major K x V:
+//   [0, P-1)        forward start of segment g + 1 (E_g, combined in place)
+//   [P-1, 2P-2)     reverse end of segment g (F_{g+1}, combined in place)
+//   [2P-2, 3P-4)    P_g of the inner segments g = 1 .. P-2
+// ---------------------------------------------------------------------------
+namespace stc {
+constexpr int kCombCols = 8;                 // V columns per combine CTA
+constexpr int kPmStride = D + 1;             // padded rows of the staged P_g
+constexpr size_t kCombSmem = (size_t)(D * kPmStride + D * kCombCols) * sizeof(float);
+}  // namespace stc
+
+// One CTA per (sequence, head) x 8-column block of V x direction (0 forward,
+// 1 reverse); the columns of a state evolve independently.  Thread = row c
+// and four of the block's columns; P - 2 dependent steps:
+//   forward  start(g) = P_{g-1} start(g-1) + E_{g-1},        g = 2 .. P-1
+//   reverse  end(g)   = P_{g+1}^T end(g+1) + F_{g+1},        g = P-3 .. 0
+__global__ void __launch_bounds__(NTHREADS) kda_cp_combine_kernel(KdaParams p) {
+  using namespace stc;
+  extern __shared__ __align__(16) float csm[];
+  float *Pm = csm, *Sin = csm + D * kPmStride;
+  const int P = p.cp_segs;
+  const int dir = p.role_base + (int)blockIdx.z;
+  const int j0 = (int)blockIdx.y * kCombCols;
+  const int tid = threadIdx.x, c = tid & (D - 1), jq = (tid >> 7) * 4;
+  const size_t DD = (size_t)D * D;
+  float *tiles = p.cp_buf + (size_t)blockIdx.x * (size_t)kda_cp_tiles(P) * DD;
+  for (int st = 0; st < P - 2; ++st) {
+    int tin, tout, tp;
+    if (dir == 0) {
+      const int g = st + 2;
+      tin = g - 2;
+      tout = g - 1;
+      tp = 2 * (P - 1) + g - 2;
+    } else {
+      const int g = P - 3 - st;
+      tin = P - 1 + g + 1;
+      tout = P - 1 + g;
+      tp = 2 * (P - 1) + g;
+    }
+    __syncthreads();  // the previous step's reads of Pm and Sin are done
+    const float *Pg = tiles + (size_t)tp * DD;
+    for (int e = tid; e < D * D / 4; e += NTHREADS) {
+      const float4 v = reinterpret_cast<const float4 *>(Pg)[e];
+      float *d = Pm + (e >> 5) * kPmStride + 4 * (e & 31);
+      d[0] = v.x;
+      d[1] = v.y;
+      d[2] = v.z;
+      d[3] = v.w;
+    }
+    if (st == 0) {  // the first input: rows of the outermost boundary tile
+      const float *src = tiles + (size_t)tin * DD;
+      for (int e = tid; e < D * kCombCols; e += NTHREADS)
+        Sin[e] = src[(size_t)(e / kCombCols) * D + j0 + e % kCombCols];
+    }
+    __syncthreads();
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int k = 0; k < D; ++k) {
+      const float a = dir == 0 ? Pm[c * kPmStride + k] : Pm[k * kPmStride + c];
+      const float4 x = *reinterpret_cast<const float4 *>(Sin + k * kCombCols + jq);
+      acc[0] = fmaf(a, x.x, acc[0]);
+      acc[1] = fmaf(a, x.y, acc[1]);
+      acc[2] = fmaf(a, x.z, acc[2]);
+      acc[3] = fmaf(a, x.w, acc[3]);
+    }
+    float *dst = tiles + (size_t)tout * DD + (size_t)c * D + j0 + jq;
+    const float4 loc = *reinterpret_cast<const float4 *>(dst);
+    const float4 out = make_float4(acc[0] + loc.x, acc[1] + loc.y, acc[2] + loc.z, acc[3] + loc.w);
+    *reinterpret_cast<float4 *>(dst) = out;
+    __syncthreads();  // every thread has read Sin
+    *reinterpret_cast<float4 *>(Sin + c * kCombCols + jq) = out;
+  }
+}
+
+cudaError_t scan_tc_cp_launch(KdaParams p, const void *prep, int nroles, cudaStream_t st) {
+  const int P = p.cp_segs;
+  if (P < 3 || p.cu != nullptr || p.cp_buf == nullptr) return cudaErrorInvalidValue;
+  if (nroles < 1 || p.role_base < 0 || p.role_base + nroles > 2) return cudaErrorInvalidValue;
+  auto kfn = kda_scan_tc_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)stc::Smem::total);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kda_cp_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)stc::kCombSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t nunits = (int64_t)p.B * p.H;
+  if (nunits == 0) return cudaSuccess;
+  const bool has_fwd = p.role_base == 0, has_rev = p.role_base + nroles > 1;
+  const int roles = (has_fwd ? 1 : 0) + (has_rev ? 1 : 0);
+  p.cp_nroles = nroles;
+  p.seq_order = nullptr;
+  // 1. local segment scans and the inner transfer matrices
+  p.cp_phase = 1;
+  kfn<<<(unsigned)(nunits * (roles * (P - 1) + (P - 2))), NTHREADS, stc::Smem::total, st>>>(
+      p, static_cast<const char *>(prep));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // 2. the segment boundaries
+  p.cp_phase = 2;
+  kda_cp_combine_kernel<<<dim3((unsigned)nunits, stc::D / stc::kCombCols, (unsigned)roles),
+                          NTHREADS, stc::kCombSmem, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // 3. the remaining segments from their true boundaries
+  p.cp_phase = 3;
+  kfn<<<(unsigned)(nunits * roles * (P - 1)), NTHREADS, stc::Smem::total, st>>>(
       p, static_cast<const char *>(prep));
   return cudaGetLastError();
 }

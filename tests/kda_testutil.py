@@ -80,3 +80,18 @@ def unpack_core_tiles(t):
     R, C = t.shape[-2], t.shape[-1]
     x = t.reshape(*lead, R // 8, C // 8, 8, 8)
     return x.transpose(-3, -2).reshape(*lead, R, C).contiguous()
+
+
+def check_dalog(g, ref, x, tol):
+    """dA_log[h] sums dgk * gk over every token and channel of head h, terms
+    of both signs: its error is that of the terms (per-tensor tol, as dg)
+    times the cancellation ||terms||_2 / |sum|.  Bounded here against the
+    L2 norm of the oracle's terms, per head (dgk * gk = dg softplus / sigmoid
+    of the biased gate)."""
+    z = f64_tokens(x["g"]) + (0.0 if x.get("dt_bias") is None
+                              else x["dt_bias"].double().numpy()[None])
+    terms = ref["dg"] * np.logaddexp(0.0, z) * (1.0 + np.exp(-z))
+    got = g["dA_log"].double().cpu().numpy()
+    for h in range(got.shape[0]):
+        l2 = np.linalg.norm(terms[:, h])
+        assert abs(got[h] - ref["dA_log"][h]) <= tol * l2, (h, got[h], ref["dA_log"][h], l2)

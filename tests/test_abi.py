@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_strings(L):
-    assert L.kda_abi_version() == 4
+    assert L.kda_abi_version() == 5
     for st in range(7):
         assert len(L.kda_status_str(st)) > 0
 
@@ -64,11 +64,27 @@ def test_slots_and_workspace(L):
     assert kda.workspace_bytes(s) == 2 * sb + ((6 * 3 * 4 + 255) // 256) * 256 + ddt + prep
     v = _shape(B=1, T=300, num_seqs=4, cu_seqlens=0x1000)
     assert kda.num_chunk_slots(v) == 300 // 64 + 4
+    assert kda.scan_segments(v) == 0 and kda.scan_segments(s) == 0
     f = _shape(K=64, V=64, dtype=kda.KDA_FP32, T=64, B=1)
     assert kda.workspace_dstates_offset(f) == 1 * 3 * 64 * 64 * 4
     sf = 1 * 3 * 64 * 64 * 4
     # no operand blocks off the tcgen05 path
     assert kda.workspace_bytes(f) == 2 * sf + 256 + 3 * 64 * 4
+    # few (sequence, head) chains and 16 chunks: the context-parallel scans take
+    # P = 4 segments of 4 chunks and 3P - 4 = 8 fp32 boundary tiles per
+    # (sequence, head) at the end of the workspace
+    r = lambda x: (x + 255) // 256 * 256
+    c = _shape(B=1, T=1024)
+    assert kda.scan_segments(c) == 4
+    n = 16 * 3
+    base = 2 * r(n * 128 * 128 * 2) + r(n * 4) + r(n * 128 * 4) + r(n * 107008)
+    assert kda.workspace_bytes(c) == base + r(3 * 8 * 128 * 128 * 4)
+    # 15 chunks allow 3 segments (5 tiles); varlen shapes use whole-sequence chains
+    c = _shape(B=1, T=960)
+    assert kda.scan_segments(c) == 3
+    n = 15 * 3
+    base = 2 * r(n * 128 * 128 * 2) + r(n * 4) + r(n * 128 * 4) + r(n * 107008)
+    assert kda.workspace_bytes(c) == base + r(3 * 5 * 128 * 128 * 4)
 
 
 @pytest.mark.parametrize("kw,code", [

@@ -8,7 +8,8 @@ import torch
 import __graft_entry__
 import linear_attention_backward_gb300 as kda
 from linear_attention_backward_gb300 import workloads as wl
-from kda_testutil import (GRADS, f64_tokens, gpu_bwd, oracle_bwd, oracle_states, rel_l2,
+from kda_testutil import (GRADS, check_dalog as _check_dalog, f64_tokens, gpu_bwd, oracle_bwd,
+                          oracle_states, rel_l2,
                           unpack_core_tiles,
                           slot_index)
 
@@ -82,21 +83,6 @@ def _with_bias(x, seed):
     H, K = x["q"].shape[2], x["q"].shape[3]
     gen = torch.Generator().manual_seed(seed)
     return dict(x, dt_bias=torch.randn(H, K, generator=gen) * 0.5)
-
-
-def _check_dalog(g, ref, x, tol):
-    """dA_log[h] sums dgk * gk over every token and channel of head h, terms
-    of both signs: its error is that of the terms (per-tensor tol, as dg)
-    times the cancellation ||terms||_2 / |sum|.  Bounded here against the
-    L2 norm of the oracle's terms, per head (dgk * gk = dg softplus / sigmoid
-    of the biased gate)."""
-    z = f64_tokens(x["g"]) + (0.0 if x.get("dt_bias") is None
-                              else x["dt_bias"].double().numpy()[None])
-    terms = ref["dg"] * np.logaddexp(0.0, z) * (1.0 + np.exp(-z))
-    got = g["dA_log"].double().cpu().numpy()
-    for h in range(got.shape[0]):
-        l2 = np.linalg.norm(terms[:, h])
-        assert abs(got[h] - ref["dA_log"][h]) <= tol * l2, (h, got[h], ref["dA_log"][h], l2)
 
 
 @pytest.mark.parametrize("dtype,K,T", [("bf16", 128, 200), ("bf16", 64, 130), ("fp32", 64, 97)])
