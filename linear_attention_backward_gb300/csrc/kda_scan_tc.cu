@@ -458,71 +458,109 @@ cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cud
 //   [2P-2, 3P-4)    P_g of the inner segments g = 1 .. P-2
 // ---------------------------------------------------------------------------
 namespace stc {
-constexpr int kCombCols = 8;                 // V columns per combine CTA
-constexpr int kPmStride = D + 1;             // padded rows of the staged P_g
-constexpr size_t kCombSmem = (size_t)(D * kPmStride + D * kCombCols) * sizeof(float);
+constexpr int kCombCols = 32;  // V columns per combine CTA
+constexpr int kSinLd = 40;     // row stride (floats) of the staged columns: B fragments conflict-free
 }  // namespace stc
 
-// One CTA per (sequence, head) x 8-column block of V x direction (0 forward,
-// 1 reverse); the columns of a state evolve independently.  Thread = row c
-// and four of the block's columns; P - 2 dependent steps:
+// One CTA per (sequence, head) x 32-column block of V x direction (0 forward,
+// 1 reverse); the columns of a state evolve independently.  P - 2 dependent
+// steps, each a 128 x 128 by 128 x 32 product on the tensor cores (mma.sync
+// m16n8k8 tf32, fp32 accumulation; tf32 rounds to 2^-11, finer than the
+// bf16 of the published states) plus the local tile:
 //   forward  start(g) = P_{g-1} start(g-1) + E_{g-1},        g = 2 .. P-1
 //   reverse  end(g)   = P_{g+1}^T end(g+1) + F_{g+1},        g = P-3 .. 0
+// Warp w owns rows [16 w, 16 w + 16) and all 32 columns (four n-tiles).  The
+// transfer products do not depend on the chain: each thread's A fragments of
+// the next step (64 floats, read straight from L2) are loaded while the
+// current step multiplies.
 __global__ void __launch_bounds__(NTHREADS) kda_cp_combine_kernel(KdaParams p) {
   using namespace stc;
-  extern __shared__ __align__(16) float csm[];
-  float *Pm = csm, *Sin = csm + D * kPmStride;
+  __shared__ __align__(16) float Sin[D * kSinLd];
   const int P = p.cp_segs;
   const int dir = p.role_base + (int)blockIdx.z;
   const int j0 = (int)blockIdx.y * kCombCols;
-  const int tid = threadIdx.x, c = tid & (D - 1), jq = (tid >> 7) * 4;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int gq = lane >> 2, tq = lane & 3, r0 = 16 * w + gq;
   const size_t DD = (size_t)D * D;
   float *tiles = p.cp_buf + (size_t)blockIdx.x * (size_t)kda_cp_tiles(P) * DD;
+  // tile indices of step st: input boundary, output boundary, transfer
+  auto t_in = [&](int st) { return dir == 0 ? st : 2 * P - 3 - st; };
+  auto t_out = [&](int st) { return dir == 0 ? st + 1 : 2 * P - 4 - st; };
+  auto t_p = [&](int st) { return dir == 0 ? 2 * P - 2 + st : 3 * P - 5 - st; };
+  // A = P_g (forward) or P_g^T (reverse); fragment q of k-step ks holds
+  // A[r0 + 8 (q & 1)][8 ks + tq + 4 (q >> 1)]
+  float pa[D / 8][4];
+  auto load_a = [&](int st) {
+    const float *Pg = tiles + (size_t)t_p(st) * DD;
+#pragma unroll
+    for (int ks = 0; ks < D / 8; ++ks) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = r0 + 8 * (q & 1), k = 8 * ks + tq + 4 * (q >> 1);
+        pa[ks][q] = dir == 0 ? Pg[r * D + k] : Pg[k * D + r];
+      }
+    }
+  };
+  if (P >= 3) load_a(0);
+  {  // the first input: the outermost boundary tile's columns [j0, j0 + 32)
+    const float *src = tiles + (size_t)t_in(0) * DD;
+    float4 v[D * kCombCols / 4 / NTHREADS];
+#pragma unroll
+    for (int i = 0; i < D * kCombCols / 4 / NTHREADS; ++i) {
+      const int e = tid + i * NTHREADS;
+      v[i] = *reinterpret_cast<const float4 *>(src + (size_t)(e >> 3) * D + j0 + 4 * (e & 7));
+    }
+#pragma unroll
+    for (int i = 0; i < D * kCombCols / 4 / NTHREADS; ++i) {
+      const int e = tid + i * NTHREADS;
+      *reinterpret_cast<float4 *>(Sin + (e >> 3) * kSinLd + 4 * (e & 7)) = v[i];
+    }
+  }
+  __syncthreads();
   for (int st = 0; st < P - 2; ++st) {
-    int tin, tout, tp;
-    if (dir == 0) {
-      const int g = st + 2;
-      tin = g - 2;
-      tout = g - 1;
-      tp = 2 * (P - 1) + g - 2;
-    } else {
-      const int g = P - 3 - st;
-      tin = P - 1 + g + 1;
-      tout = P - 1 + g;
-      tp = 2 * (P - 1) + g;
+    uint32_t af[D / 8][4];
+#pragma unroll
+    for (int ks = 0; ks < D / 8; ++ks)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) af[ks][q] = to_tf32(pa[ks][q]);
+    if (st + 1 < P - 2) load_a(st + 1);
+    float *out = tiles + (size_t)t_out(st) * DD;
+    float acc[4][4];  // [n-tile][fragment]: the local tile plus the product
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float2 lo = *reinterpret_cast<const float2 *>(out + (size_t)r0 * D + j0 + 8 * nt + 2 * tq);
+      const float2 hi =
+          *reinterpret_cast<const float2 *>(out + (size_t)(r0 + 8) * D + j0 + 8 * nt + 2 * tq);
+      acc[nt][0] = lo.x;
+      acc[nt][1] = lo.y;
+      acc[nt][2] = hi.x;
+      acc[nt][3] = hi.y;
     }
-    __syncthreads();  // the previous step's reads of Pm and Sin are done
-    const float *Pg = tiles + (size_t)tp * DD;
-    for (int e = tid; e < D * D / 4; e += NTHREADS) {
-      const float4 v = reinterpret_cast<const float4 *>(Pg)[e];
-      float *d = Pm + (e >> 5) * kPmStride + 4 * (e & 31);
-      d[0] = v.x;
-      d[1] = v.y;
-      d[2] = v.z;
-      d[3] = v.w;
+#pragma unroll
+    for (int ks = 0; ks < D / 8; ++ks) {
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float *b = Sin + (8 * ks + tq) * kSinLd + 8 * nt + gq;
+        const uint32_t bf[2] = {to_tf32(b[0]), to_tf32(b[4 * kSinLd])};
+        mma_tf32(acc[nt], af[ks], bf);
+      }
     }
-    if (st == 0) {  // the first input: rows of the outermost boundary tile
-      const float *src = tiles + (size_t)tin * DD;
-      for (int e = tid; e < D * kCombCols; e += NTHREADS)
-        Sin[e] = src[(size_t)(e / kCombCols) * D + j0 + e % kCombCols];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      *reinterpret_cast<float2 *>(out + (size_t)r0 * D + j0 + 8 * nt + 2 * tq) =
+          make_float2(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<float2 *>(out + (size_t)(r0 + 8) * D + j0 + 8 * nt + 2 * tq) =
+          make_float2(acc[nt][2], acc[nt][3]);
+    }
+    __syncthreads();  // every warp is done reading Sin
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      *reinterpret_cast<float2 *>(Sin + r0 * kSinLd + 8 * nt + 2 * tq) =
+          make_float2(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<float2 *>(Sin + (r0 + 8) * kSinLd + 8 * nt + 2 * tq) =
+          make_float2(acc[nt][2], acc[nt][3]);
     }
     __syncthreads();
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int k = 0; k < D; ++k) {
-      const float a = dir == 0 ? Pm[c * kPmStride + k] : Pm[k * kPmStride + c];
-      const float4 x = *reinterpret_cast<const float4 *>(Sin + k * kCombCols + jq);
-      acc[0] = fmaf(a, x.x, acc[0]);
-      acc[1] = fmaf(a, x.y, acc[1]);
-      acc[2] = fmaf(a, x.z, acc[2]);
-      acc[3] = fmaf(a, x.w, acc[3]);
-    }
-    float *dst = tiles + (size_t)tout * DD + (size_t)c * D + j0 + jq;
-    const float4 loc = *reinterpret_cast<const float4 *>(dst);
-    const float4 out = make_float4(acc[0] + loc.x, acc[1] + loc.y, acc[2] + loc.z, acc[3] + loc.w);
-    *reinterpret_cast<float4 *>(dst) = out;
-    __syncthreads();  // every thread has read Sin
-    *reinterpret_cast<float4 *>(Sin + c * kCombCols + jq) = out;
   }
 }
 
@@ -533,9 +571,6 @@ cudaError_t scan_tc_cp_launch(KdaParams p, const void *prep, int nroles, cudaStr
   auto kfn = kda_scan_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)stc::Smem::total);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kda_cp_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)stc::kCombSmem);
   if (e != cudaSuccess) return e;
   const int64_t nunits = (int64_t)p.B * p.H;
   if (nunits == 0) return cudaSuccess;
@@ -552,7 +587,7 @@ cudaError_t scan_tc_cp_launch(KdaParams p, const void *prep, int nroles, cudaStr
   // 2. the segment boundaries
   p.cp_phase = 2;
   kda_cp_combine_kernel<<<dim3((unsigned)nunits, stc::D / stc::kCombCols, (unsigned)roles),
-                          NTHREADS, stc::kCombSmem, st>>>(p);
+                          NTHREADS, 0, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // 3. the remaining segments from their true boundaries
