@@ -431,6 +431,32 @@ def main():
     value = tokens * ws / (ms_step * 1e-3)
     assert kda.get_device_status() == 0
 
+    # ---- with the chunk states given: kda_fwd_states, then kda_bwd on them ----
+    def timed(fn, n=10):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    states = kda.fwd_states(d["k"], d["v"], d["g"], d["beta"], d["A_log"], h0, cu_seqlens=cu)
+    states_given = {
+        "fwd_states_ms": timed(lambda: kda.fwd_states(d["k"], d["v"], d["g"], d["beta"],
+                                                      d["A_log"], h0, cu_seqlens=cu,
+                                                      states=states)),
+        "bwd_ms": timed(lambda: kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                                        h0, d["dO"], dhT, cu_seqlens=cu, out=out, workspace=wsb,
+                                        states=states)),
+        "what": "kda_fwd_states (row-major chunk states, per-band scan kernel) and kda_bwd "
+                "given those states (no forward scan), CUDA events, 10 calls each"}
+    del states
+    assert kda.get_device_status() == 0
+
     # ---- end to end through the public API with host buffers ----
     # Every step copies its inputs up from pinned host memory, runs the
     # backward and reads every gradient back.  Steps are pipelined over three
@@ -528,7 +554,7 @@ def main():
         "config": workload_config(w), "clocks": clocks, "e2e": e2e,
         "gpu_launches": launches_per_step(shape, cu) * K, "scan_segments": kda.scan_segments(shape),
         "roofline": roofline, "path_roofline": path,
-        "kernels_ms": kern_ms, "kernels": KERNEL_NAMES,
+        "kernels_ms": kern_ms, "kernels": KERNEL_NAMES, "states_given": states_given,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in cpu_baseline(xh).items() if k != "seconds"}

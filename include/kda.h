@@ -121,10 +121,12 @@ size_t kda_workspace_dstates_offset(const kda_shape *shape);
  * scanned from zero, the inner segments' transfer products A_{b-1}..A_a are
  * formed, a combine kernel chains the segment boundaries, and the segments
  * are scanned again from the true boundaries (two more launches than the
- * whole-sequence scans).  Used for fixed-length bf16 K = V = 128 shapes with
- * 2 * B * H < 152 (the SM count) and at least 4 P chunks per sequence: the
- * most segments, 3 to 8, whose first-pass chains fit one per SM.  The
- * workspace then ends with (3 P - 4) fp32 K x V tiles per (sequence, head).
+ * whole-sequence scans).  Used for bf16 K = V = 128 shapes with 2 N H < 152
+ * (N sequences; 152 is the SM count) and at least 4 P chunks per sequence
+ * (for varlen, on average: T / 64 / N, since the host never reads
+ * cu_seqlens; shorter sequences get shorter or empty segments): the most
+ * segments, 3 to 8, whose first-pass chains fit one per SM.  The workspace
+ * then ends with (3 P - 4) fp32 K x V tiles per (sequence, head).
  * The environment variable KDA_SCAN_CP=0 turns this off per call, and
  * KDA_SCAN_CP=n (3 <= n <= the value without it) takes n segments.
  * Returns 0 on a bad shape. */

@@ -94,15 +94,18 @@ bool legacy_scan() {
 kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
 // Segments of the context-parallel tcgen05 scans (0: whole-sequence chains).
-// Used for fixed-length sequences when the whole-sequence chains (two per
-// sequence and head) leave most SMs idle: the most segments (3..8, at least
-// four chunks each) whose phase-1 chains, kda_cp_tiles(P) per sequence and
-// head, still fit one per SM.  A function of the shape, so that the
-// workspace size is too.
+// Used when the whole-sequence chains (two per sequence and head) leave most
+// SMs idle: the most segments (3..8, at least four chunks each) whose phase-1
+// chains, kda_cp_tiles(P) per sequence and head, still fit one per SM.  A
+// function of the shape, so that the workspace size is too: for varlen the
+// host does not read cu_seqlens, and the chunks per sequence are taken as
+// the average T / 64 / num_seqs (shorter sequences get shorter, possibly
+// empty, segments).
 int cp_segments(const kda_shape *s) {
-  if (!tc_state_path(s) || s->cu_seqlens != nullptr) return 0;
-  const int64_t units = (int64_t)s->B * s->H;
-  const int nck = (s->T + kChunk - 1) / kChunk;
+  if (!tc_state_path(s)) return 0;
+  const int64_t units = (int64_t)num_seqs_of(s) * s->H;
+  const int nck = s->cu_seqlens ? (int)((s->T / kChunk) / s->num_seqs)
+                                : (s->T + kChunk - 1) / kChunk;
   if (2 * units >= kTargetCtas) return 0;
   int best = 0;
   for (int P = 3; P <= 8; ++P)
@@ -122,8 +125,8 @@ int cp_segments_used(const kda_shape *s) {
 }
 
 size_t cp_bytes(const kda_shape *s) {
-  return round_up((size_t)s->B * s->H * (size_t)kda::kda_cp_tiles(cp_segments(s)) * s->K *
-                  s->V * sizeof(float));
+  return round_up((size_t)num_seqs_of(s) * s->H * (size_t)kda::kda_cp_tiles(cp_segments(s)) *
+                  s->K * s->V * sizeof(float));
 }
 
 // Workspace layout: states | dS | dA_log partials [slots, H] | ddt_bias
@@ -257,11 +260,11 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
   cudaError_t e = kda::prep_tc_launch(p, tm, prep, cs);
   p.role_base = 0;
   p.states_packed = 1;
-  if (e == cudaSuccess && p.cu != nullptr) {
+  const int cp = cp_segments_used(shape);
+  if (e == cudaSuccess && p.cu != nullptr && cp < 3) {
     p.seq_order = reinterpret_cast<const int32_t *>(p.dA_part);
     e = kda::seq_order_launch(p.cu, p.num_seqs, reinterpret_cast<int32_t *>(p.dA_part), cs);
   }
-  const int cp = cp_segments_used(shape);
   if (e == cudaSuccess && cp >= 3) {
     p.cp_segs = cp;
     p.cp_buf = reinterpret_cast<float *>(w + cp_offset(shape));
@@ -356,14 +359,14 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
     // the tcgen05 scans store their tiles in packed core-matrix order
     p.states_packed = states ? 0 : 1;
     p.dstates_packed = 1;
-    if (p.cu != nullptr) {
+    const int cp = cp_segments_used(shape);
+    if (p.cu != nullptr && cp < 3) {
       // varlen: the scans take the sequences longest first; the order lives in
       // the dA_log partials (slots x H >= num_seqs floats), which the gradient
       // kernel overwrites only after the scans
       p.seq_order = reinterpret_cast<const int32_t *>(p.dA_part);
       e = kda::seq_order_launch(p.cu, p.num_seqs, reinterpret_cast<int32_t *>(p.dA_part), cs);
     }
-    const int cp = cp_segments_used(shape);
     if (e == cudaSuccess && cp >= 3) {
       // few (sequence, head) chains: context-parallel scans over segments
       p.cp_segs = cp;

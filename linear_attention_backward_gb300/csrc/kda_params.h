@@ -35,8 +35,8 @@ struct KdaParams {
   int states_packed, dstates_packed;
   const char *prep;           // per-chunk operand blocks (bf16, K = V = 128), see below
   const int32_t *seq_order;   // tcgen05 scans: sequences longest first (varlen), or null
-  // Context-parallel tcgen05 scans (fixed-length sequences only): each
-  // sequence's chunks are split into cp_segs >= 3 segments, segment g holding
+  // Context-parallel tcgen05 scans: each sequence's chunks (nck of them) are
+  // split into cp_segs >= 3 segments, segment g holding
   // chunks [g nck / cp_segs, (g + 1) nck / cp_segs).  cp_phase 1 runs every
   // segment's local scan and the transfer matrices, 2 (the combine kernel)
   // chains them into the true segment boundaries, 3 reruns the segments
@@ -104,8 +104,8 @@ int prep_tc_status_take();
 // kda_scan_tc.cu: both state scans on tcgen05 from the prep buffer; roles
 // as in scan_dispatch.
 cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cudaStream_t st);
-// the three phases of the context-parallel scans (p.cp_segs >= 3, fixed
-// length); p.role_base and nroles as for scan_tc_launch
+// the three phases of the context-parallel scans (p.cp_segs >= 3); p.role_base
+// and nroles as for scan_tc_launch
 cudaError_t scan_tc_cp_launch(KdaParams p, const void *prep, int nroles, cudaStream_t st);
 // order[r] = the sequence of rank r by length (longest first, ties by index)
 cudaError_t seq_order_launch(const int32_t *cu, int num_seqs, int32_t *order, cudaStream_t st);

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   int r, h, role;
   int g = -1;  // context-parallel segment (-1: the whole sequence)
   if (p.cp_segs >= 3) {
-    // context-parallel chain kinds (fixed length), kind-major then (sequence, head):
+    // context-parallel chain kinds, kind-major then (sequence, head):
     //  phase 1: reverse-local g = 1..P-1, forward-local g = 0..P-2 (zero
     //           start, or dh_T / h0 for the outermost), transfers g = 1..P-2;
     //  phase 3: reverse g = 0..P-2, forward g = 1..P-1 from the combined
@@ -566,13 +566,13 @@ __global__ void __launch_bounds__(NTHREADS) kda_cp_combine_kernel(KdaParams p) {
 
 cudaError_t scan_tc_cp_launch(KdaParams p, const void *prep, int nroles, cudaStream_t st) {
   const int P = p.cp_segs;
-  if (P < 3 || p.cu != nullptr || p.cp_buf == nullptr) return cudaErrorInvalidValue;
+  if (P < 3 || p.cp_buf == nullptr) return cudaErrorInvalidValue;
   if (nroles < 1 || p.role_base < 0 || p.role_base + nroles > 2) return cudaErrorInvalidValue;
   auto kfn = kda_scan_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)stc::Smem::total);
   if (e != cudaSuccess) return e;
-  const int64_t nunits = (int64_t)p.B * p.H;
+  const int64_t nunits = (int64_t)(p.cu ? p.num_seqs : p.B) * p.H;
   if (nunits == 0) return cudaSuccess;
   const bool has_fwd = p.role_base == 0, has_rev = p.role_base + nroles > 1;
   const int roles = (has_fwd ? 1 : 0) + (has_rev ? 1 : 0);

@@ -65,6 +65,13 @@ def test_slots_and_workspace(L):
     v = _shape(B=1, T=300, num_seqs=4, cu_seqlens=0x1000)
     assert kda.num_chunk_slots(v) == 300 // 64 + 4
     assert kda.scan_segments(v) == 0 and kda.scan_segments(s) == 0
+    # varlen: P from the average chunks per sequence (86 chunks / 5 sequences)
+    v = _shape(B=1, T=5507, num_seqs=5, cu_seqlens=0x1000)
+    assert kda.scan_segments(v) == 4
+    r = lambda x: (x + 255) // 256 * 256
+    n = (5507 // 64 + 5) * 3
+    assert kda.workspace_bytes(v) == (2 * r(n * 128 * 128 * 2) + r(n * 4) + r(n * 128 * 4)
+                                      + r(n * 107008) + r(5 * 3 * 8 * 128 * 128 * 4))
     f = _shape(K=64, V=64, dtype=kda.KDA_FP32, T=64, B=1)
     assert kda.workspace_dstates_offset(f) == 1 * 3 * 64 * 64 * 4
     sf = 1 * 3 * 64 * 64 * 4

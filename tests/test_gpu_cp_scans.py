@@ -137,3 +137,34 @@ def test_cp_forward(monkeypatch, segs):
         cu_seqlens=wl.seq_bounds(x))
     assert rel_l2(o.double().cpu().numpy().reshape(ro.shape), ro) <= TOL
     assert rel_l2(hT.double().cpu().numpy(), rhT) <= TOL
+
+
+def test_cp_varlen_with_short_and_empty_sequences():
+    # 86 chunks over 5 sequences: 4 segments of each sequence's own chunks;
+    # the empty and the 70-token sequence get empty or one-chunk segments
+    lengths = [2000, 0, 1537, 70, 1900]
+    w = wl.custom("cpv", H=2, K=128, V=128, dtype="bf16", with_h0=True, with_dhT=True,
+                  varlen=(5, 0, 2048))
+    x = wl.make_inputs(w, seed=37, lengths=lengths)
+    d = to_dev(x)
+    assert kda.scan_segments(kda.make_shape(d["q"], d["v"], cu_seqlens=d["cu_seqlens"])) == 4
+    g, _ = gpu_bwd(x)
+    assert kda.get_device_status() == 0
+    ref = oracle_bwd(x)
+    _compare(g, ref)
+    # the empty sequence passes its state gradient straight through (its
+    # boundaries cross the tf32 combine: identity products rounded to 2^-11)
+    np.testing.assert_allclose(g["dh0"][1].cpu().numpy(), x["dhT"][1].numpy(), rtol=1e-3,
+                               atol=1e-6)
+    # the forward pass on the same batch
+    o, hT = kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"],
+                    cu_seqlens=d["cu_seqlens"], want_hT=True)
+    torch.cuda.synchronize()
+    assert kda.get_device_status() == 0
+    ro, rhT, _ = oracle.forward(
+        f64_tokens(x["q"]), f64_tokens(x["k"]), f64_tokens(x["v"]), f64_tokens(x["g"]),
+        f64_tokens(x["beta"]), x["A_log"].double().numpy(), x["h0"].double().numpy(),
+        cu_seqlens=wl.seq_bounds(x))
+    assert rel_l2(o.double().cpu().numpy().reshape(ro.shape), ro) <= TOL
+    assert rel_l2(hT.double().cpu().numpy(), rhT) <= TOL
+    np.testing.assert_allclose(hT[1].cpu().numpy(), x["h0"][1].numpy(), rtol=1e-3, atol=1e-6)
