@@ -251,7 +251,7 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
   p.hT = hT;
   p.states = w;  // packed chunk states, as kda_bwd keeps them
   p.dA_part = reinterpret_cast<float *>(w + dA_part_offset(shape));
-  kda::TokenMaps tm;
+  kda::TokenMaps tm{};  // left zero when there are no tokens (no kernel then reads it)
   if (!kda::encode_token_maps(p, tm)) return KDA_ERR_CUDA;
   void *prep = w + prep_offset(shape);
   p.prep = static_cast<const char *>(prep);
@@ -345,7 +345,7 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
   const int nroles = states ? 1 : 2;
   p.role_base = states ? 1 : 0;
   cudaError_t e = cudaSuccess;
-  kda::TokenMaps tm;
+  kda::TokenMaps tm{};  // left zero when there are no tokens (no kernel then reads it)
   if (tc_state_path(shape)) {
     // TMA maps of the token-major inputs, and the per-chunk operands for the
     // tcgen05 scans and the gradient kernel
