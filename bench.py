@@ -153,6 +153,23 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def max_over_ranks(ms, pg, device):
+    """The slowest rank's time: every rank's timed region counts, and the job
+    is done when the last rank is (pg None: one process)."""
+    if pg is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world_size, ms):
+    """Whole-job throughput: the units all ranks processed (each rank its own
+    batch of the same size: weak scaling) over the slowest rank's time."""
+    return units_per_rank * world_size / (ms * 1e-3)
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -303,16 +320,13 @@ def run_forward(args, w, xh, dev, ws, pg):
     ms = s0.elapsed_time(s1) / args.steps
     if flush is not None:  # the calls alone
         ms = sum(a.elapsed_time(b) for a, b in pairs) / args.steps
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, pg, dev)
     assert kda.get_device_status() == 0
     tokens = int(xh["q"].shape[0] * xh["q"].shape[1])
     cfg = workload_config(w)
     cfg["workload"] = cfg["workload"].replace("chunked backward", "chunked forward").replace(
         "states recomputed in the call", "o and hT")
-    line = {"metric": "KDA forward tokens/s (kda_fwd: o and hT)", "value": tokens * ws / (ms * 1e-3),
+    line = {"metric": "KDA forward tokens/s (kda_fwd: o and hT)", "value": job_rate(tokens, ws, ms),
             "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": cfg,
@@ -422,13 +436,10 @@ def main():
     for e5 in evs:
         for j, n in enumerate(PHASES):
             phase[n].append(e5[j].elapsed_time(e5[j + 1]))
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, pg, dev)
     ms_step = ms / K
     tokens = int(xh["q"].shape[0] * xh["q"].shape[1])  # B * T, or the packed total (varlen)
-    value = tokens * ws / (ms_step * 1e-3)
+    value = job_rate(tokens, ws, ms_step)
     assert kda.get_device_status() == 0
 
     # ---- with the chunk states given: kda_fwd_states, then kda_bwd on them ----
@@ -515,11 +526,8 @@ def main():
     s1.record(comp)
     torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / E
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": tokens * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
+    e2e_ms = max_over_ranks(e2e_ms, pg, dev)
+    e2e = {"value": job_rate(tokens, ws, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
            "steps": E, "pipeline": "H2D / backward / D2H on three streams, two device "
                                    "buffer sets, every step's inputs up and gradients down"}
