@@ -74,7 +74,11 @@ typedef enum {
   KDA_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
   KDA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
   KDA_ERR_DEVICE_ARG = 6,  /* the device found a bad cu_seqlens table */
-  KDA_ERR_TOO_LARGE = 7    /* kda_bwd_noalloc: problem needs more than its fixed scratch */
+  KDA_ERR_TOO_LARGE = 7,   /* kda_bwd_noalloc: problem needs more than its fixed scratch */
+  KDA_ERR_GATE_RANGE = 8   /* the device found a channel whose gate log-decay over the
+                              7 or 8 tokens on either side of a 16-row block's reference
+                              row exceeds 88 nats: the block factors e^x leave the fp32
+                              range, and the outputs of that call are not valid */
 } kda_status;
 
 typedef enum { KDA_FP32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -238,7 +242,8 @@ kda_status kda_selftest_umma(const void *A, const void *B, float *D, int N, int 
                              int b_mn, int swap_lbo_sbo, kda_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the device status word of
- * the current device (KDA_OK, KDA_ERR_DEVICE_ARG or KDA_ERR_TIMEOUT), or
+ * the current device (KDA_OK, KDA_ERR_DEVICE_ARG, KDA_ERR_TIMEOUT or
+ * KDA_ERR_GATE_RANGE: the first error any kernel raised since the last read), or
  * KDA_ERR_CUDA if the synchronisation itself reported an error. */
 kda_status kda_get_device_status(kda_stream_t stream);
 

@@ -157,6 +157,7 @@ const char *kda_status_str(kda_status st) {
     case KDA_ERR_TIMEOUT: return "device-side wait timed out";
     case KDA_ERR_DEVICE_ARG: return "device found a malformed cu_seqlens table";
     case KDA_ERR_TOO_LARGE: return "problem exceeds the fixed no-allocation scratch";
+    case KDA_ERR_GATE_RANGE: return "gate log-decay around a 16-row block exceeds 88 nats";
   }
   return "unknown status";
 }

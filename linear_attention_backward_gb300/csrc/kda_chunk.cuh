@@ -250,6 +250,17 @@ __device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, cons
     g0[r] = run0;
     g1[r] = run1;
   }
+  // log-decay around the block's reference row 16 I + 7 that the block
+  // factors carry: a whole block (rows 0..7 before it, 8..15 after it), or a
+  // half block ending at it (rows 0..7) or starting after it (rows 8..15)
+  if constexpr (ROWS == 16) {
+    check_block_log_decay(fmaxf(fmaxf(g0[0] - g0[7], g0[7] - g0[ROWS - 1]),
+                                fmaxf(g1[0] - g1[7], g1[7] - g1[ROWS - 1])));
+  } else if ((r0 & 15) == 0) {
+    check_block_log_decay(fmaxf(g0[0] - g0[ROWS - 1], g1[0] - g1[ROWS - 1]));
+  } else {
+    check_block_log_decay(fmaxf(-g0[ROWS - 1], -g1[ROWS - 1]));
+  }
   // block partials: Ablk = sum of rows 16I .. 16I+7 (through the reference
   // row), Bblk = rows 16I+8 .. 16I+15
   float *Ablk = sv.part, *Bblk = sv.m;  // [4][K] each (sv.m reused as scratch)

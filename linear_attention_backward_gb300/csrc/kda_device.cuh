@@ -22,6 +22,19 @@ static __device__ int g_status = 0;
 
 __device__ __forceinline__ void set_status(int code) { atomicCAS(&g_status, 0, code); }
 
+// The intra-chunk products carry the gate through 16-row block factors
+// e^(gc_i - m_I) and e^(m_I - gc_j) around each block's reference row (up to
+// 7 and 8 tokens of log-decay).  Past 88 nats such a factor is infinite in
+// fp32 and the gradients cannot be finite: the prep kernels then raise this
+// status code (KDA_ERR_GATE_RANGE) instead of returning them silently.
+// (Below it the factors are finite; sums of them stay finite for ordinary
+// operands: a parity test reaches 85.6 nats.)
+constexpr float kMaxBlockLogDecay = 88.f;
+constexpr int kStatusGateRange = 8;
+__device__ __forceinline__ void check_block_log_decay(float span) {
+  if (span > kMaxBlockLogDecay) set_status(kStatusGateRange);
+}
+
 // Row stride (elements) of a shared tile with `cols` columns: 16 bytes of
 // padding per row for bf16 keeps ldmatrix row addresses on distinct 16-byte
 // bank groups (stride = 16 mod 128 bytes).  fp32 tiles feed the SIMT path

@@ -175,6 +175,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       g0[r] = run0;
       g1[r] = run1;
     }
+    // log-decay around the block's reference row (row 7): rows 0..7 and 8..15
+    check_block_log_decay(fmaxf(fmaxf(g0[0] - g0[7], g0[7] - g0[15]),
+                                fmaxf(g1[0] - g1[7], g1[7] - g1[15])));
     float *Ablk = sv.part, *Bblk = sv.m;
     Ablk[I * D + c] = g0[7];
     Ablk[I * D + c + 1] = g1[7];

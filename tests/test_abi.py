@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(L):
 
 def test_abi_version_and_strings(L):
     assert L.kda_abi_version() == 5
-    for st in range(7):
+    for st in range(9):
         assert len(L.kda_status_str(st)) > 0
 
 

@@ -1,9 +1,9 @@
 """GPU parity on the degenerate cases of the method, through the C ABI:
 no tokens at all, beta = 0 (no writes: the state only decays), all-zero
 query / key rows (the L2 norm's epsilon carries them), no decay (the gate
-saturates at zero: the plain delta rule) and heavy decay inside the range the
-16-row block factors cover (a channel's log-decay over 8 tokens below ~85
-nats).  Tolerances as for the other bf16 parity tests: 2e-2 per-tensor
+saturates at zero: the plain delta rule), heavy decay inside the range the
+16-row block factors cover, and a gate beyond it (reported by the status
+word).  Tolerances as for the other bf16 parity tests: 2e-2 per-tensor
 relative L2 against the fp64 oracle (absolute L2 where the oracle's tensor
 is exactly zero)."""
 import numpy as np
@@ -101,9 +101,10 @@ def test_no_decay_delta_rule():
 
 
 def test_heavy_decay_inside_the_block_range():
-    # up to ~7 nats of log-decay per token and channel (e^A_log <= e, g ~ N(1.5, 0.3)):
-    # ~56 nats over 8 tokens, inside the 16-row block factors' range; the
-    # states of earlier chunks decay away (e^gT underflows to zero)
+    # about 3.5 nats of log-decay per token and channel (e^A_log <= e,
+    # g ~ N(1.5, 0.3)), up to 28 nats around a 16-row block's reference row:
+    # every chunk's gT is near -200, so the states of earlier chunks decay away
+    # (e^gT underflows to zero in fp32)
     w = wl.custom("hd", B=1, T=260, H=2, K=128, V=128, dtype="bf16", with_h0=True,
                   with_dhT=True)
     x = wl.make_inputs(w, seed=44)
@@ -117,3 +118,25 @@ def test_heavy_decay_inside_the_block_range():
         assert np.isfinite(g[k].double().cpu().numpy()).all(), k
     _compare(g, ref, ("dq", "dk", "dv", "dg", "dbeta", "dh0"))
     check_dalog(g, ref, x, TOL)
+
+
+@pytest.mark.parametrize("dtype,K", [("bf16", 128), ("bf16", 64), ("fp32", 64)])
+def test_gate_beyond_block_range_is_reported(dtype, K):
+    # g = +20 on a run of tokens of one sequence, e^A_log >= 1: over 20 nats of
+    # log-decay per token, far beyond the 88 nats around a 16-row block's
+    # reference row that the block factors hold in fp32.  The call is flagged (KDA_ERR_GATE_RANGE)
+    # instead of returning non-finite values silently; the next valid call is
+    # clean.
+    w = wl.custom("gr", B=2, T=130, H=2, K=K, V=K, dtype=dtype)
+    x = wl.make_inputs(w, seed=45)
+    x["g"][1, 20:40] = 20.0
+    gpu_bwd(x)
+    assert kda.get_device_status() == 8
+    if dtype == "bf16" and K == 128:
+        d = {n: (t.cuda() if t is not None else None) for n, t in x.items()}
+        kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"])
+        assert kda.get_device_status() == 8
+    g, _ = gpu_bwd(wl.make_inputs(w, seed=46))
+    assert kda.get_device_status() == 0
+    for k in GRADS:
+        assert torch.isfinite(g[k]).all(), k
