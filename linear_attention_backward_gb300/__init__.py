@@ -259,3 +259,37 @@ def bwd_noalloc(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, out, cu_seqlens=N
                                _ptr(out.get("ddt_bias")), _ptr(out.get("dh0")), _stream())
     _check(st, "kda_bwd_noalloc")
     return out
+
+
+class KDAFunction(torch.autograd.Function):
+    """Differentiable KDA layer core: ``(o, hT) = KDAFunction.apply(q, k, v, g,
+    beta, A_log, h0, dt_bias, cu_seqlens, scale, l2_eps)``.  The forward is
+    :func:`fwd` (bf16, K = V = 128) and the backward :func:`bwd`, which
+    recomputes the chunk states from the saved inputs.  Gradients flow to q,
+    k, v, g, beta, A_log and, where given, h0 and dt_bias."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, A_log, h0, dt_bias, cu_seqlens, scale, l2_eps):
+        o, hT = fwd(q, k, v, g, beta, A_log, h0, cu_seqlens=cu_seqlens, scale=scale,
+                    l2_eps=l2_eps, want_hT=True, dt_bias=dt_bias)
+        ctx.save_for_backward(q, k, v, g, beta, A_log, h0, dt_bias, cu_seqlens)
+        ctx.scale, ctx.l2_eps = scale, l2_eps
+        return o, hT
+
+    @staticmethod
+    def backward(ctx, dO, dhT):
+        q, k, v, g, beta, A_log, h0, dt_bias, cu_seqlens = ctx.saved_tensors
+        if dO is None:
+            dO = torch.zeros_like(v)
+        gr = bwd(q, k, v, g, beta, A_log, h0, dO.contiguous(),
+                 None if dhT is None else dhT.contiguous(), cu_seqlens=cu_seqlens,
+                 scale=ctx.scale, l2_eps=ctx.l2_eps, dt_bias=dt_bias)
+        return (gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], gr["dA_log"],
+                gr["dh0"] if h0 is not None else None,
+                gr.get("ddt_bias") if dt_bias is not None else None, None, None, None)
+
+
+def kda(q, k, v, g, beta, A_log, h0=None, *, dt_bias=None, cu_seqlens=None, scale=None,
+        l2_eps=None):
+    """The differentiable forward ``(o, hT)`` through :class:`KDAFunction`."""
+    return KDAFunction.apply(q, k, v, g, beta, A_log, h0, dt_bias, cu_seqlens, scale, l2_eps)
