@@ -64,10 +64,10 @@ def launches_per_step(shape, cu, forward=False):
 # is measured again.
 NCU_TRAFFIC = {
     # ncu --set full on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read
-    # 841.3 MB + write 247.8 MB, scaled by 4 to the main workload's 16384
+    # 841.2 MB + write 248.4 MB, scaled by 4 to the main workload's 16384
     # chunk-heads (the kernel's traffic is proportional to the chunk-heads)
-    "kda_grads_tc_kernel": {"sha": "69fb2dbfda5a226d", "workload": "main_bf16",
-                            "bytes_per_launch": 4356639744},
+    "kda_grads_tc_kernel": {"sha": "7e16f7b7974e15f1", "workload": "main_bf16",
+                            "bytes_per_launch": 4358414336},
 }
 
 KERNEL_SOURCES = {

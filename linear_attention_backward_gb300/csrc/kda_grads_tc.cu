@@ -261,19 +261,20 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   const bf16 *dSg = reinterpret_cast<const bf16 *>(p.dstates) + ((size_t)slot * H + h) * DD;
   const char *unit = p.prep + ((size_t)slot * H + h) * kPrepUnitBytes;
 
-  // beta, loaded by the last two warps (idle until the CTA barrier below, so
-  // the load's latency hides behind the copies' issue) and stored after it
+  // beta, loaded by the last two warps and stored after the CTA barrier
+  // below: the raw bits stay in a register until then, so no warp waits for
+  // the load before the barrier
   constexpr int kBetaT0 = NT - CHUNK;
-  float beta_i = 0.f;
+  uint32_t beta_bits = 0u;
   if (tid >= kBetaT0 && tid - kBetaT0 < len)
-    beta_i = __bfloat162float(
-        reinterpret_cast<const bf16 *>(p.beta)[(tok0 + (tid - kBetaT0)) * H + h]);
-  // the gate's scalars likewise, by the four warps before them: e^A_log[h] and
-  // the per-channel bias, kept in shared memory (gsc) for the prep and K1 phases
+    beta_bits = reinterpret_cast<const unsigned short *>(p.beta)[(tok0 + (tid - kBetaT0)) * H + h];
+  // the gate's scalars likewise, by the four warps before them: A_log[h] (its
+  // exponential is taken after the barrier) and the per-channel bias, kept in
+  // shared memory (gsc) for the prep and K1 phases
   constexpr int kGateT0 = kBetaT0 - D;
   float gate_s = 0.f;
   if (tid >= kGateT0 && tid < kBetaT0) gate_s = gate_bias(p, h, tid - kGateT0, D);
-  const float eA = tid == kGateT0 ? __expf(p.A_log[h]) : 0.f;
+  const float a_log = tid == kGateT0 ? p.A_log[h] : 0.f;
   // ---- barriers, the first copies, then Tensor Memory (all 512 columns) ----
   // Thread 0 initialises the barriers and at once issues the copies: the raw
   // q, k, g rows (row-major, R_A) and the block factors first, the prep phase
@@ -322,9 +323,9 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   cp_async_commit();
   umma::tc_fence_before();
-  if (tid >= kBetaT0) sv.beta[tid - kBetaT0] = beta_i;
+  if (tid >= kBetaT0) sv.beta[tid - kBetaT0] = __uint_as_float(beta_bits << 16);  // bf16 -> fp32
   if (tid >= kGateT0 && tid < kBetaT0) gsc[D + tid - kGateT0] = gate_s;
-  if (tid == kGateT0) gsc[0] = eA;
+  if (tid == kGateT0) gsc[0] = __expf(a_log);
   umma::mbar_wait(rbar, 0);
   if (len < CHUNK) {  // the boxes' rows past the chunk belong to the next sequence: zero them
     for (int e = tid; e < 3 * 64 * 16; e += NT) {

@@ -87,6 +87,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   int64_t tok0;
   if (!slot_owner(p, slot, s_, j_, tok0, len)) return;  // padding slot: never read
   char *unit = prep + ((size_t)slot * H + h) * kPrepUnitBytes;
+  // the gate's per-head scale and per-channel bias, loaded now (first used
+  // after the raw rows have landed, so their latency hides behind that wait)
+  const int c_g = 2 * (tid & 63);
+  const float a_log = p.A_log[h];
+  const float bias0 = gate_bias(p, h, c_g, D), bias1 = gate_bias(p, h, c_g + 1, D);
 
   float *smf = reinterpret_cast<float *>(smem);
   PrepView<bf16, D> sv = make_view<bf16, D>(smf);
@@ -163,8 +168,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       red[128 + warp * 16 + lane] = tq;
     }
     // gate: running sum over the block (sums local to the block)
-    const float A = __expf(p.A_log[h]);
-    const float bias0 = gate_bias(p, h, c, D), bias1 = gate_bias(p, h, c + 1, D);
+    const float A = __expf(a_log);
     float run0 = 0.f, run1 = 0.f;
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
