@@ -152,6 +152,16 @@ def test_cp_varlen_with_short_and_empty_sequences():
     assert kda.get_device_status() == 0
     ref = oracle_bwd(x)
     _compare(g, ref)
+    # the same states handed back: the reverse scan alone runs, context-parallel
+    # over the same segments, and reproduces every gradient bit for bit
+    shape = kda.make_shape(d["q"], d["v"], cu_seqlens=d["cu_seqlens"])
+    n = kda.num_chunk_slots(shape) * 2 * 128 * 128
+    internal = unpack_core_tiles(
+        g["_workspace"][:2 * n].view(torch.bfloat16).reshape(-1, 2, 128, 128))
+    g2, _ = gpu_bwd(x, states=internal)
+    assert kda.get_device_status() == 0
+    for k in GRADS:
+        assert torch.equal(g[k], g2[k]), k
     # the empty sequence passes its state gradient straight through (its
     # boundaries cross the tf32 combine: identity products rounded to 2^-11)
     np.testing.assert_allclose(g["dh0"][1].cpu().numpy(), x["dhT"][1].numpy(), rtol=1e-3,
