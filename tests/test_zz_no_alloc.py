@@ -31,12 +31,18 @@ def _fresh_out(d, H, N, K, V):
     return o
 
 
-@pytest.mark.parametrize("case", ["fixed", "varlen"])
+@pytest.mark.parametrize("case", ["fixed", "varlen", "context-parallel"])
 def test_noalloc_matches_workspace_entry_point_twice(case):
     if case == "fixed":
         w = wl.custom("na", B=2, T=333, H=3, K=128, V=128, dtype="bf16", with_h0=True,
                       with_dhT=True)
         x = wl.make_inputs(w, seed=21)
+    elif case == "context-parallel":
+        # few chains and 20 chunks: the scans' segment boundary tiles live in
+        # the fixed scratch too
+        w = wl.custom("nacp", B=1, T=64 * 20, H=2, K=128, V=128, dtype="bf16", with_h0=True,
+                      with_dhT=True)
+        x = wl.make_inputs(w, seed=23)
     else:
         w = wl.custom("nav", H=2, K=128, V=128, dtype="bf16", with_h0=True, with_dhT=True,
                       varlen=(4, 1, 300))
@@ -47,6 +53,7 @@ def test_noalloc_matches_workspace_entry_point_twice(case):
     torch.cuda.synchronize()
     shape = kda.make_shape(d["q"], d["v"], cu_seqlens=d["cu_seqlens"])
     assert kda.workspace_bytes(shape) <= kda.noalloc_scratch_bytes()
+    assert (kda.scan_segments(shape) > 0) == (case == "context-parallel")
     N, H = d["h0"].shape[:2]
     for call in range(2):
         out = _fresh_out(d, H, N, 128, 128)
