@@ -26,6 +26,11 @@
 // next chunk's data as soon as its consumer (MMA1, the U epilogue or MMA2)
 // is done, behind an L2 prefetch two chunks ahead.  The reverse role's dO
 // rows come by cp.async with MMA2's region.
+//
+// With few (sequence, head) chains the same kernel runs context-parallel
+// (see scan_tc_cp_launch below): chains over segments of a sequence, a third
+// role that forms a segment's transfer product from the identity, and a
+// combine kernel that chains the segment boundaries between the two passes.
 #include "kda_chunk.cuh"
 #include "kda_tc_tiles.cuh"
 

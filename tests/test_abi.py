@@ -155,3 +155,27 @@ def test_fwd_argument_checks(L):
     assert L.kda_fwd(ctypes.byref(f), *args, fake, ctypes.c_size_t(1 << 40), None) == 2
     f = _shape(dtype=kda.KDA_FP32, K=64, V=64)
     assert L.kda_fwd(ctypes.byref(f), *args, fake, ctypes.c_size_t(1 << 40), None) == 2
+
+
+@pytest.mark.parametrize("B,T,H,expect", [
+    (1, 4096, 16, 4),     # 16 sequence-heads: (3P - 4) * 16 <= 152 -> P = 4
+    (1, 8192, 2, 8),      # 2 sequence-heads, 128 chunks: capped at 8
+    (1, 1024, 2, 4),      # 16 chunks: at least 4 per segment -> P = 4
+    (1, 704, 2, 0),       # 11 chunks: fewer than 4 per segment for P = 3
+    (4, 8192, 19, 0),     # 2 * 76 chains fill the 152 SMs
+    (1, 8192, 32, 0),     # 32 sequence-heads: (3 * 3 - 4) * 32 > 152
+    (1, 8192, 30, 3),     # 30: (3 * 3 - 4) * 30 = 150 <= 152
+])
+def test_scan_segments_rule(L, B, T, H, expect):
+    assert kda.scan_segments(_shape(B=B, T=T, H=H)) == expect
+    # other dtypes and head sizes run the per-band scans: no segments
+    assert kda.scan_segments(_shape(B=B, T=T, H=H, K=64, V=64)) == 0
+
+
+@pytest.mark.parametrize("env,expect", [("0", 0), ("3", 3), ("4", 4), ("9", 4), ("2", 4),
+                                        ("x", 0)])
+def test_scan_segments_env_override(L, monkeypatch, env, expect):
+    # KDA_SCAN_CP=0 (or anything non-numeric) turns the split off; 3..P takes
+    # that many segments; other values keep the shape's own P (4 here)
+    monkeypatch.setenv("KDA_SCAN_CP", env)
+    assert kda.scan_segments(_shape(B=1, T=4096, H=16)) == expect
