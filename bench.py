@@ -455,16 +455,18 @@ def main():
         torch.cuda.synchronize()
         return a.elapsed_time(b) / n
 
-    states = kda.fwd_states(d["k"], d["v"], d["g"], d["beta"], d["A_log"], h0, cu_seqlens=cu)
+    states = kda.fwd_states(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], h0,
+                            cu_seqlens=cu, workspace=wsb)
     states_given = {
-        "fwd_states_ms": timed(lambda: kda.fwd_states(d["k"], d["v"], d["g"], d["beta"],
+        "fwd_states_ms": timed(lambda: kda.fwd_states(d["q"], d["k"], d["v"], d["g"], d["beta"],
                                                       d["A_log"], h0, cu_seqlens=cu,
-                                                      states=states)),
+                                                      states=states, workspace=wsb)),
         "bwd_ms": timed(lambda: kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
                                         h0, d["dO"], dhT, cu_seqlens=cu, out=out, workspace=wsb,
                                         states=states)),
-        "what": "kda_fwd_states (row-major chunk states, per-band scan kernel) and kda_bwd "
-                "given those states (no forward scan), CUDA events, 10 calls each"}
+        "what": "kda_fwd_states (chunk-parallel prep and the forward tcgen05 scan, packed "
+                "chunk states) and kda_bwd given those states (prep, reverse scan, gradients), "
+                "CUDA events, 10 calls each"}
     del states
     assert kda.get_device_status() == 0
 

@@ -49,8 +49,19 @@
  *    stream, except kda_get_device_status which synchronises its stream.
  *  - Errors: argument errors are returned before anything is launched.  A
  *    failed launch returns KDA_ERR_CUDA.  Errors found on the device (a bad
- *    cu_seqlens table) are recorded in a device status word read by
- *    kda_get_device_status.
+ *    cu_seqlens table, a gate beyond the block range, a bounded wait that
+ *    gave up) are recorded in a device status word read by
+ *    kda_get_device_status; the outputs of that call are then not valid.
+ *  - Bounded waits.  Every wait of a kernel on a copy or a tensor-core
+ *    product polls a bounded number of times (2^24 polls for copies, 2^20
+ *    for products).  A CTA whose wait gives up records KDA_ERR_TIMEOUT,
+ *    issues no further product and writes no further result, waits once
+ *    more (2^16 polls) for what it still has in flight, releases its Tensor
+ *    Memory and exits; the context stays usable.  Test hook: the environment
+ *    variable KDA_TEST_STARVE_WAITS, a list of kernel names (prep, scan,
+ *    grads, out), makes those kernels arm their first load barrier without
+ *    issuing its copies and caps every wait of the call at 4096 polls, so
+ *    that the timeout path can be exercised without a fault.
  *  - Streams: all work of one call is queued on `stream` in order.  Calls
  *    on different streams that share output or workspace buffers race.
  */
@@ -138,14 +149,28 @@ int kda_scan_segments(const kda_shape *shape);
 /* Forward chunk-state recompute (the "all_states" operand of kernel B2 in
  * "bwd-kernelB-beginner-guide-full", Part 2, B2 optimisation 4).
  *   states : OUT [slots, H, K, V], dtype of the shape: S at the start of
- *            every chunk (S_0 = h0), bf16 rounded to nearest even.
+ *            every chunk (S_0 = h0), bf16 rounded to nearest even.  For bf16
+ *            with K = V = 128 each K x V tile is in packed core-matrix order
+ *            (element (k, v) at element offset ((k / 8) * (V / 8) + v / 8) *
+ *            64 + (k % 8) * 8 + v % 8: 8 x 8 blocks of 128 bytes, blocks along
+ *            V first), the order in which the scans store them and the
+ *            gradient kernel reads them; otherwise row-major.  kda_bwd takes
+ *            them in the same layout.
  *   h0     : nullable (zero initial state), fp32 [N, H, K, V].
  *   hT     : nullable OUT fp32 [N, H, K, V]: the final state of each sequence.
- * No workspace is needed. */
-kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v,
-                          const void *g, const void *beta, const float *A_log,
-                          const float *dt_bias, const float *h0, void *states,
-                          float *hT, kda_stream_t stream);
+ *   ws     : bf16 with K = V = 128: DEVICE workspace of at least
+ *            kda_workspace_bytes(shape) bytes, 256-byte aligned (the layout
+ *            kda_bwd uses; the per-chunk operand blocks of the chunk-parallel
+ *            prep live there).  Other shapes need none (ws may be NULL).
+ * bf16 with K = V = 128 runs the chunk-parallel prep (which also forms the
+ * read-out operands and so needs q) and the forward tcgen05 state scan,
+ * context-parallel where kda_scan_segments() > 0; q is then required.  Other
+ * shapes run the per-band scan and ignore q. */
+kda_status kda_fwd_states(const kda_shape *shape, const void *q, const void *k,
+                          const void *v, const void *g, const void *beta,
+                          const float *A_log, const float *dt_bias, const float *h0,
+                          void *states, float *hT, void *ws, size_t ws_bytes,
+                          kda_stream_t stream);
 
 /* Forward pass: the read-out o_t = scale * S_t^T q^_t of every token and the
  * final states ("bwd-kernelB-beginner-guide-full", Part 1: the chunked KDA
@@ -170,7 +195,8 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
  *   dA_log : OUT fp32 [H], overwritten (summed over sequences and tokens).
  *   ddt_bias : nullable OUT fp32 [H, K], overwritten (summed likewise).
  *   dh0    : nullable OUT fp32 [N, H, K, V].
- *   states : nullable; the output of kda_fwd_states for the same inputs.
+ *   states : nullable; the output of kda_fwd_states for the same inputs, in
+ *            its layout (packed core-matrix tiles for bf16, K = V = 128).
  *            NULL recomputes them inside the workspace.
  *   ws     : DEVICE workspace of at least kda_workspace_bytes(shape) bytes,
  *            256-byte aligned.  Its content on entry is ignored.
@@ -211,9 +237,17 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k,
  *  - Size limit: problems whose kda_workspace_bytes() exceeds the array are
  *    rejected with KDA_ERR_TOO_LARGE before anything is launched (64 MiB
  *    holds about 400 chunk-heads of 64 tokens at K = V = 128, bf16).
- *  - Set-up: the first call on each device looks up the array's device
- *    address (cudaGetSymbolAddress, with that device current) and caches
- *    it; make that first call before capturing any stream.
+ *  - When the array is reserved: it belongs to the library's device image
+ *    and is reserved when the CUDA runtime loads the module holding it --
+ *    under lazy module loading (the default since CUDA 12.2) during the
+ *    first kda_bwd_noalloc call on each device, under eager loading
+ *    (CUDA_MODULE_LOADING=EAGER) when the context is created, for every
+ *    process that loads the library.  Make one warm-up call per device
+ *    outside any allocator callback or restricted region, and before
+ *    capturing any stream; later calls reserve nothing.
+ *  - Each call looks the array's device address up (cudaGetSymbolAddress,
+ *    on the calling thread's current device); nothing is cached across
+ *    calls, so a context that was torn down and re-created is handled.
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.
  *  - Every call on a device shares the same array: calls whose work
  *    overlaps on the GPU (different streams, or different host threads)
@@ -234,12 +268,12 @@ size_t kda_noalloc_scratch_bytes(void);
  * descriptors, Tensor Memory and tcgen05 loads, with A ([128][K] bf16,
  * row-major, device) and B ([N][K] bf16, row-major, device) staged in K-major
  * (0) or MN-major (1) core-matrix layout; D is [128][N] fp32 (device).
- * N in {32, 64, 128}, K a multiple of 16 up to 128.  layout: 0 = core matrices
- * packed (128-byte stride), 2 = padded core layout (144-byte stride, the one
- * the kernels use), 1 = packed with the two descriptor strides exchanged (a
- * diagnostic of the encoding; gives wrong results). */
+ * N in {32, 64, 128}, K a multiple of 16 up to 128.  layout: 0 = core
+ * matrices packed (128-byte stride), 1 = padded core layout (144-byte stride,
+ * the one the kernels use for tiles their threads write).  Other values are
+ * rejected (KDA_ERR_INVALID_ARG). */
 kda_status kda_selftest_umma(const void *A, const void *B, float *D, int N, int K, int a_mn,
-                             int b_mn, int swap_lbo_sbo, kda_stream_t stream);
+                             int b_mn, int layout, kda_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device (KDA_OK, KDA_ERR_DEVICE_ARG, KDA_ERR_TIMEOUT or

@@ -24,7 +24,7 @@ _LIB_PATH = os.path.join(_PKG, "_build", "libkda.so")
 KDA_OK = 0
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace",
                 4: "cuda error", 5: "timeout", 6: "bad cu_seqlens on device",
-                7: "too large for the no-allocation scratch"}
+                7: "too large for the no-allocation scratch", 8: "gate beyond the block range"}
 KDA_FP32, KDA_BF16 = 0, 1
 
 
@@ -69,7 +69,7 @@ def lib():
         L.kda_workspace_dstates_offset.restype = ctypes.c_size_t
         L.kda_scan_segments.argtypes = [S]
         L.kda_scan_segments.restype = ctypes.c_int
-        L.kda_fwd_states.argtypes = [S] + [_VP] * 10
+        L.kda_fwd_states.argtypes = [S] + [_VP] * 11 + [ctypes.c_size_t, _VP]
         L.kda_fwd_states.restype = ctypes.c_int
         L.kda_fwd.argtypes = [S] + [_VP] * 11 + [ctypes.c_size_t, _VP]
         L.kda_fwd.restype = ctypes.c_int
@@ -150,9 +150,16 @@ def _nseq(B, cu_seqlens):
     return B if cu_seqlens is None else cu_seqlens.numel() - 1
 
 
-def fwd_states(k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None, l2_eps=None,
-               states=None, hT=None, want_hT=False, dt_bias=None):
-    """Chunk-start states ``[slots, H, K, V]`` (dtype of k) and optionally hT."""
+def fwd_states(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None, l2_eps=None,
+               states=None, hT=None, want_hT=False, dt_bias=None, workspace=None):
+    """Chunk-start states ``[slots, H, K, V]`` (dtype of k) and optionally hT.
+
+    For bf16 with K = V = 128 every K x V tile is in packed core-matrix order
+    (see ``kda_fwd_states`` in include/kda.h; ``unpack_core_tiles`` in the
+    tests turns it row-major), the layout :func:`bwd` takes back as
+    ``states``; ``workspace`` (uint8 CUDA tensor of at least
+    ``workspace_bytes``) is allocated when not given.  Other shapes return
+    row-major tiles and use no workspace."""
     shape = make_shape(k, v, cu_seqlens=cu_seqlens, scale=scale, l2_eps=l2_eps)
     B, T, H, K = k.shape
     V = v.shape[-1]
@@ -160,9 +167,13 @@ def fwd_states(k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None, l2
         states = torch.empty((num_chunk_slots(shape), H, K, V), dtype=k.dtype, device=k.device)
     if want_hT and hT is None:
         hT = torch.empty((_nseq(B, cu_seqlens), H, K, V), dtype=torch.float32, device=k.device)
-    st = lib().kda_fwd_states(ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                              _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(states), _ptr(hT),
-                              _stream())
+    tc = k.dtype == torch.bfloat16 and K == 128 and V == 128
+    if workspace is None and tc:
+        workspace = torch.empty((workspace_bytes(shape),), dtype=torch.uint8, device=k.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().kda_fwd_states(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                              _ptr(beta), _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(states),
+                              _ptr(hT), _ptr(workspace), ctypes.c_size_t(nbytes), _stream())
     _check(st, "kda_fwd_states")
     return (states, hT) if want_hT else states
 
@@ -197,6 +208,8 @@ def bwd(q, k, v, g, beta, A_log, h0, dO, dh_T=None, *, cu_seqlens=None, scale=No
 
     ``out`` may hold preallocated output tensors under the same keys and
     ``workspace`` a uint8 CUDA tensor of at least ``workspace_bytes`` bytes.
+    ``states`` (optional) are :func:`fwd_states`' output for the same inputs,
+    in its layout.
     ``events``: optional 5 ``torch.cuda.Event(enable_timing=True)`` recorded at
     the phase boundaries (see ``kda_bwd_timed`` in include/kda.h).
     """

@@ -52,6 +52,20 @@ size_t states_bytes(const kda_shape *s) {
   return round_up((size_t)slots_of(s) * s->H * (size_t)s->K * s->V * elem_size(s));
 }
 
+// Test hook of the timeout tests: KDA_TEST_STARVE_WAITS names kernels
+// (any of prep, scan, grads, out) that arm their first load barrier without
+// issuing its copies, so that their bounded waits run out; every bounded
+// wait of such a call then polls at most 4096 times.
+void test_hooks(kda::KdaParams &p) {
+  const char *e = getenv("KDA_TEST_STARVE_WAITS");
+  if (e == nullptr || e[0] == '\0') return;
+  if (strstr(e, "prep")) p.starve |= kda::kStarvePrep;
+  if (strstr(e, "scan")) p.starve |= kda::kStarveScan;
+  if (strstr(e, "grads")) p.starve |= kda::kStarveGrads;
+  if (strstr(e, "out")) p.starve |= kda::kStarveOut;
+  if (p.starve != 0u) p.poll_limit = 4096u;
+}
+
 void fill_params(const kda_shape *s, kda::KdaParams &p) {
   memset(&p, 0, sizeof(p));
   p.B = s->B;
@@ -64,6 +78,7 @@ void fill_params(const kda_shape *s, kda::KdaParams &p) {
   p.scale = s->scale > 0.f ? s->scale : 1.0f / sqrtf((float)s->K);
   p.eps = s->l2_eps >= 0.f ? s->l2_eps : 1e-6f;
   p.nb = 1;
+  test_hooks(p);
 }
 
 // V band width of the scan kernels: wide bands unless the (sequence, head,
@@ -141,11 +156,47 @@ size_t prep_offset(const kda_shape *s) {
 }
 size_t cp_offset(const kda_shape *s) { return prep_offset(s) + prep_bytes(s); }
 
+// The forward half shared by kda_fwd and kda_fwd_states on the tcgen05 path:
+// per-chunk operands into the workspace, then the forward state scan (whole
+// sequences, or context-parallel segments when the chains alone leave most
+// SMs idle), which stores every chunk-start state in packed core-matrix
+// order to p.states and the final states to p.hT.  p holds the inputs, the
+// outputs and p.dA_part (the sequence order of varlen scans lives there).
+cudaError_t forward_states_tc(kda::KdaParams &p, const kda_shape *shape, char *w,
+                              const kda::TokenMaps &tm, cudaStream_t cs) {
+  void *prep = w + prep_offset(shape);
+  p.prep = static_cast<const char *>(prep);
+  cudaError_t e = kda::prep_tc_launch(p, tm, prep, cs);
+  p.role_base = 0;
+  p.states_packed = 1;
+  const int cp = cp_segments_used(shape);
+  if (e == cudaSuccess && p.cu != nullptr && cp < 3) {
+    p.seq_order = reinterpret_cast<const int32_t *>(p.dA_part);
+    e = kda::seq_order_launch(p.cu, p.num_seqs, reinterpret_cast<int32_t *>(p.dA_part), cs);
+  }
+  if (e == cudaSuccess && cp >= 3) {
+    p.cp_segs = cp;
+    p.cp_buf = reinterpret_cast<float *>(w + cp_offset(shape));
+    e = kda::scan_tc_cp_launch(p, p.prep, 1, cs);
+    p.cp_segs = 0;
+  } else if (e == cudaSuccess) {
+    e = kda::scan_tc_launch(p, p.prep, 1, cs);
+  }
+  return e;
+}
+
+kda_status check_ws(const kda_shape *shape, const void *ws, size_t ws_bytes) {
+  const size_t need = kda_workspace_bytes(shape);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return KDA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return KDA_ERR_WORKSPACE;
+  return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-int kda_abi_version(void) { return 5; }
+int kda_abi_version(void) { return 6; }
 
 const char *kda_status_str(kda_status st) {
   switch (st) {
@@ -190,19 +241,23 @@ kda_status kda_check_cu_seqlens_host(const int32_t *cu, int num_seqs, int total_
   return KDA_OK;
 }
 
-kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v, const void *g,
-                          const void *beta, const float *A_log, const float *dt_bias,
-                          const float *h0, void *states, float *hT, kda_stream_t stream) {
+kda_status kda_fwd_states(const kda_shape *shape, const void *q, const void *k, const void *v,
+                          const void *g, const void *beta, const float *A_log,
+                          const float *dt_bias, const float *h0, void *states, float *hT,
+                          void *ws, size_t ws_bytes, kda_stream_t stream) {
   kda_status st = check_shape(shape);
   if (st != KDA_OK) return st;
   const bool tokens = (int64_t)shape->B * shape->T > 0;
+  const bool tc = tc_state_path(shape);
   if (!A_log) return KDA_ERR_INVALID_ARG;
-  if (tokens && (!k || !v || !g || !beta || !states)) return KDA_ERR_INVALID_ARG;
-  const void *ptrs[] = {k, v, g, beta, A_log, dt_bias, h0, states, hT};
+  if (tokens && (!k || !v || !g || !beta || !states || (tc && !q))) return KDA_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, g, beta, A_log, dt_bias, h0, states, hT};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   kda::KdaParams p;
   fill_params(shape, p);
+  p.q = q;
   p.k = k;
   p.v = v;
   p.g = g;
@@ -212,11 +267,23 @@ kda_status kda_fwd_states(const kda_shape *shape, const void *k, const void *v, 
   p.h0 = h0;
   p.states = states;
   p.hT = hT;
+  if (tc) {
+    // the tcgen05 path: the chunk-parallel prep and the forward scan, with
+    // the operand blocks in the caller's workspace
+    st = check_ws(shape, ws, ws_bytes);
+    if (st != KDA_OK) return st;
+    char *w = static_cast<char *>(ws);
+    p.dA_part = reinterpret_cast<float *>(w + dA_part_offset(shape));
+    kda::TokenMaps tm{};  // left zero when there are no tokens (no kernel then reads it)
+    if (!kda::encode_token_maps(p, tm)) return KDA_ERR_CUDA;
+    return from_cuda(forward_states_tc(p, shape, w, tm, cs));
+  }
+  // other dtypes and head sizes: the per-band scan (row-major states; no
+  // workspace)
   p.role_base = 0;
   const int bv = pick_band(shape, 1);
   p.nb = shape->V / bv;
-  return from_cuda(kda::scan_dispatch(p, shape->K, shape->dtype == KDA_BF16, bv, 1,
-                                      reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(kda::scan_dispatch(p, shape->K, shape->dtype == KDA_BF16, bv, 1, cs));
 }
 
 kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const void *v,
@@ -232,13 +299,11 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
   const void *ptrs[] = {q, k, v, g, beta, A_log, dt_bias, h0, o, hT};
   for (const void *ptr : ptrs)
     if (ptr && !aligned16(ptr)) return KDA_ERR_INVALID_ARG;
-  const size_t need = kda_workspace_bytes(shape);
-  if (need > 0 && (ws == nullptr || ws_bytes < need)) return KDA_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return KDA_ERR_WORKSPACE;
+  st = check_ws(shape, ws, ws_bytes);
+  if (st != KDA_OK) return st;
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   char *w = static_cast<char *>(ws);
-  const size_t sb = states_bytes(shape);
   kda::KdaParams p;
   fill_params(shape, p);
   p.q = q;
@@ -254,26 +319,9 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
   p.dA_part = reinterpret_cast<float *>(w + dA_part_offset(shape));
   kda::TokenMaps tm{};  // left zero when there are no tokens (no kernel then reads it)
   if (!kda::encode_token_maps(p, tm)) return KDA_ERR_CUDA;
-  void *prep = w + prep_offset(shape);
-  p.prep = static_cast<const char *>(prep);
   // 1. per-chunk operands, 2. forward state scan (S_n of every chunk, hT),
   // 3. the chunk outputs
-  cudaError_t e = kda::prep_tc_launch(p, tm, prep, cs);
-  p.role_base = 0;
-  p.states_packed = 1;
-  const int cp = cp_segments_used(shape);
-  if (e == cudaSuccess && p.cu != nullptr && cp < 3) {
-    p.seq_order = reinterpret_cast<const int32_t *>(p.dA_part);
-    e = kda::seq_order_launch(p.cu, p.num_seqs, reinterpret_cast<int32_t *>(p.dA_part), cs);
-  }
-  if (e == cudaSuccess && cp >= 3) {
-    p.cp_segs = cp;
-    p.cp_buf = reinterpret_cast<float *>(w + cp_offset(shape));
-    e = kda::scan_tc_cp_launch(p, p.prep, 1, cs);
-    p.cp_segs = 0;
-  } else if (e == cudaSuccess) {
-    e = kda::scan_tc_launch(p, p.prep, 1, cs);
-  }
+  cudaError_t e = forward_states_tc(p, shape, w, tm, cs);
   if (e == cudaSuccess) e = kda::out_tc_launch(p, p.states, o, cs);
   return from_cuda(e);
 }
@@ -304,9 +352,8 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
                         dA_log, ddt_bias, dh0, states};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
-  const size_t need = kda_workspace_bytes(shape);
-  if (need > 0 && (ws == nullptr || ws_bytes < need)) return KDA_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return KDA_ERR_WORKSPACE;
+  st = check_ws(shape, ws, ws_bytes);
+  if (st != KDA_OK) return st;
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   char *w = static_cast<char *>(ws);
@@ -357,8 +404,9 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
   }
   mark(1);
   if (e == cudaSuccess && tc_state_path(shape) && !legacy_scan()) {
-    // the tcgen05 scans store their tiles in packed core-matrix order
-    p.states_packed = states ? 0 : 1;
+    // the tcgen05 scans store their tiles in packed core-matrix order, the
+    // layout kda_fwd_states gives the caller on this path too
+    p.states_packed = 1;
     p.dstates_packed = 1;
     const int cp = cp_segments_used(shape);
     if (p.cu != nullptr && cp < 3) {
@@ -378,6 +426,9 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
       e = kda::scan_tc_launch(p, p.prep, nroles, cs);
     }
   } else if (e == cudaSuccess) {
+    // the per-band scans write row-major tiles; caller states on the tcgen05
+    // path are packed (kda_fwd_states' layout there)
+    p.states_packed = states != nullptr && tc_state_path(shape) ? 1 : 0;
     const int bv = pick_band(shape, nroles);
     p.nb = shape->V / bv;
     e = kda::scan_dispatch(p, shape->K, bf, bv, nroles, cs);

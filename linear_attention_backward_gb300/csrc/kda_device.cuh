@@ -209,10 +209,19 @@ __device__ __forceinline__ float quad_sum(float v) {
   return v;
 }
 
+// log(1 + t) for t in [0, 1].  The fast log of the rounded sum 1 + t keeps
+// an absolute error of ~1e-7 but loses the relative precision of small t
+// (1 + t rounds to 1 below 2^-24), so arguments below 2^-5 take the Taylor
+// series t - t^2/2 + t^3/3 - t^4/4 + t^5/5 instead (relative truncation
+// error below t^5 / 6 < 1e-8 there).
+__device__ __forceinline__ float log1p_unit(float t) {
+  const float s = t * fmaf(-t, fmaf(-t, fmaf(-t, fmaf(-t, 0.2f, 0.25f), 0.33333334f), 0.5f), 1.f);
+  return t < 0.03125f ? s : __logf(1.f + t);
+}
 __device__ __forceinline__ float softplus_f(float x) {
-  // log(1 + e^x) = max(x, 0) + log(1 + e^-|x|); the second term is in
-  // (0, log 2], where the fast log's absolute error (~1e-7) is harmless
-  return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
+  // log(1 + e^x) = max(x, 0) + log(1 + e^-|x|), relative precision kept far
+  // into the negative tail (softplus(-30) ~ 1e-13 is not rounded to zero)
+  return fmaxf(x, 0.f) + log1p_unit(__expf(-fabsf(x)));
 }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + __expf(-x)); }
 

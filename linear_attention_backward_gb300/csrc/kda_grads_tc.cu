@@ -281,6 +281,8 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   // waits on them; then v rows (U's slot, free until P2), S (packed in the
   // workspace), dS and kr^T, which stream in during the prep phase.  Warp 0
   // allocates Tensor Memory meanwhile.
+  // (a timeout test starves both barriers: they are armed, no copy is issued)
+  const bool starve = (p.starve & kStarveGrads) != 0u;
   if (tid == 0) {
     umma::mbar_init(mbar, 1);
     umma::mbar_init(lbar, 1);
@@ -288,17 +290,21 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     umma::mbar_init(rbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     umma::mbar_expect_tx(rbar, 3 * 16384u + (uint32_t)kPrepSVBytes);
-    umma::tma_load_3d(Qr, &tm.q, 0, h, (int)tok0, rbar);
-    umma::tma_load_3d(Kr, &tm.k, 0, h, (int)tok0, rbar);
-    umma::tma_load_3d(Gr, &tm.g, 0, h, (int)tok0, rbar);
-    umma::bulk_g2s(sv.em, unit + kPrepSV, (uint32_t)kPrepSVBytes, rbar);  // factors, norms
+    if (!starve) {
+      umma::tma_load_3d(Qr, &tm.q, 0, h, (int)tok0, rbar);
+      umma::tma_load_3d(Kr, &tm.k, 0, h, (int)tok0, rbar);
+      umma::tma_load_3d(Gr, &tm.g, 0, h, (int)tok0, rbar);
+      umma::bulk_g2s(sv.em, unit + kPrepSV, (uint32_t)kPrepSVBytes, rbar);  // factors, norms
+    }
     const uint32_t bytes = 16384u + (p.states_packed ? 32768u : 0u) +
                            (p.dstates_packed ? 32768u : 0u) + 16384u;
     umma::mbar_expect_tx(lbar, bytes);
-    umma::tma_load_3d(Ut, &tm.v, 0, h, (int)tok0, lbar);
-    if (p.states_packed) umma::bulk_g2s(St, Sg, 32768u, lbar);
-    if (p.dstates_packed) umma::bulk_g2s(dSt, dSg, 32768u, lbar);
-    umma::bulk_g2s(KRt, unit + kPrepKR, 16384u, lbar);
+    if (!starve) {
+      umma::tma_load_3d(Ut, &tm.v, 0, h, (int)tok0, lbar);
+      if (p.states_packed) umma::bulk_g2s(St, Sg, 32768u, lbar);
+      if (p.dstates_packed) umma::bulk_g2s(dSt, dSg, 32768u, lbar);
+      umma::bulk_g2s(KRt, unit + kPrepKR, 16384u, lbar);
+    }
   }
   if (warp == 0) umma::tmem_alloc(tslot, 512);
   __syncthreads();
@@ -326,7 +332,15 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   if (tid >= kBetaT0) sv.beta[tid - kBetaT0] = __uint_as_float(beta_bits << 16);  // bf16 -> fp32
   if (tid >= kGateT0 && tid < kBetaT0) gsc[D + tid - kGateT0] = gate_s;
   if (tid == kGateT0) gsc[0] = __expf(a_log);
-  umma::mbar_wait(rbar, 0);
+  // Every bounded wait below folds its result into `ok`.  The CTA decides at
+  // its barriers (__syncthreads_or): once any thread's wait has given up, no
+  // further MMA is issued and no result leaves the CTA (what a timed-out
+  // product may have left in Tensor Memory reaches shared memory only); the
+  // CTA drains what is in flight and releases Tensor Memory (`drain` below).
+  const uint32_t lim_ld = poll_cap(p, umma::kPollLoads), lim_mma = poll_cap(p, umma::kPollMma);
+  bool ok = umma::mbar_wait(rbar, 0, lim_ld);
+  uint32_t phase = 0;         // completions of the MMA barrier waited for
+  bool past_first = false;    // the prep-tile copy (pbar) has been issued
   if (len < CHUNK) {  // the boxes' rows past the chunk belong to the next sequence: zero them
     for (int e = tid; e < 3 * 64 * 16; e += NT) {
       const int t = e >> 10, i = (e >> 4) & 63, c8 = (e & 15) * 8;
@@ -336,15 +350,15 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       }
     }
   }
-  __syncthreads();
+  if (__syncthreads_or(!ok)) goto drain;
+  {
+  past_first = true;
   umma::tc_fence_after();
   const uint32_t tbase = *tslot;
-  uint32_t phase = 0;
   auto mma_wait = [&]() {
-    const bool ok = umma::mbar_wait(mbar, phase & 1, 1u << 20);
+    ok = umma::mbar_wait(mbar, phase & 1, lim_mma) && ok;
     phase++;
     umma::tc_fence_after();
-    return ok;
   };
 
   // ---- prep ----
@@ -354,9 +368,9 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   // INVb, G, packed 64 x 64 -- come into R_A over the raw rows from inside)
   prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, q2, k2, g2, unit + kPrepMqk, Mqk, pbar, gsc);
   cp_async_wait_all();                 // dO, v (and row-major S)
-  umma::mbar_wait(lbar, 0);            // S, dS, kr^T
+  ok = umma::mbar_wait(lbar, 0, lim_ld) && ok;  // S, dS, kr^T
   umma::fence_async_smem();
-  __syncthreads();
+  if (__syncthreads_or(!ok)) goto drain;
 
   // ---- R1 = P1: kdS^T = S^T kd^T ; the epilogue forms Xr^T = v^T - kdS^T ----
   if (tid == 0) {
@@ -373,10 +387,10 @@ __global__ void __launch_bounds__(gtc::NT, 1)
                                : 0.f) - acc[r];
 #pragma unroll
   for (int q = 0; q < 2; ++q) pstore8(XrT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // Xr^T[d][i]
-  umma::mbar_wait(pbar, 0);  // Mqk, INV, INVb, G
+  ok = umma::mbar_wait(pbar, 0, lim_ld) && ok;  // Mqk, INV, INVb, G
   umma::fence_async_smem();
   umma::tc_fence_before();
-  __syncthreads();
+  if (__syncthreads_or(!ok)) goto drain;
 
   // ---- R2 = P2 + P3a: U^T = Xr^T INVb^T ; dU^T = dO^T Mqk + dS^T kr^T (dU needs no U) ----
   if (tid == 0) {
@@ -408,7 +422,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   for (int q = 0; q < 2; ++q) pstore8(dUT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // dU^T[d][i]
   umma::fence_async_smem();
   umma::tc_fence_before();
-  __syncthreads();
+  if (__syncthreads_or(!ok)) goto drain;
 
   // ---- R3 = P5 + P3b: dvcorr^T = dU^T INV ; dkr^T = dS U^T ; dv, dbeta1, dvcorr[i][d] ----
   if (tid == 0) {
@@ -438,7 +452,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   umma::fence_async_smem();
   umma::tc_fence_before();
-  __syncthreads();
+  if (__syncthreads_or(!ok)) goto drain;
   if (tid < 64) {  // dbeta1_i: block i / 16 lives in warps 4 (i / 16) .. + 3
     const int i = tid, w0 = (i >> 4) * 4, r = i & 15;
     dbs[i] = red[(w0 + 0) * 16 + r] + red[(w0 + 1) * 16 + r] + red[(w0 + 2) * 16 + r] +
@@ -508,7 +522,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   umma::fence_async_smem();
   umma::tc_fence_before();
   if (tid == kStoreT) umma::bulk_wait_read();  // the dv box has left R_A [0, 16K) (the g rows go there)
-  __syncthreads();
+  if (__syncthreads_or(!ok)) goto drain;
   if (tid < 64 && tid < len) {
     const float db = dbs[tid] + red2[tid] + red2[64 + tid] + red2[128 + tid] + red2[192 + tid];
     reinterpret_cast<bf16 *>(p.dbeta)[(tok0 + tid) * H + h] = __float2bfloat16_rn(db);
@@ -613,7 +627,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     const float t = rows16_sum(pr);
     if (lane < 16) red[warp * 16 + lane] = t;
     umma::tc_fence_before();
-    __syncthreads();
+    if (__syncthreads_or(!ok)) goto drain;
     // lane l < 16: row 16 I + l summed over the block's 4 warps; broadcast below
     const float tot = red[(4 * I) * 16 + (lane & 15)] + red[(4 * I + 1) * 16 + (lane & 15)] +
                       red[(4 * I + 2) * 16 + (lane & 15)] + red[(4 * I + 3) * 16 + (lane & 15)];
@@ -726,7 +740,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     const float t = rows16_sum(pr);
     if (lane < 16) red[warp * 16 + lane] = t;
     dgT[I * D + c] += colp;
-    __syncthreads();
+    if (__syncthreads_or(!ok)) goto drain;
     const float tot = red[(4 * I) * 16 + (lane & 15)] + red[(4 * I + 1) * 16 + (lane & 15)] +
                       red[(4 * I + 2) * 16 + (lane & 15)] + red[(4 * I + 3) * 16 + (lane & 15)];
 #pragma unroll
@@ -782,7 +796,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       const float t = __expf(-fabsf(gv));
       const float inv = __fdividef(1.f, 1.f + t);
       const float sg = gv >= 0.f ? inv : t * inv;
-      const float sp = fmaxf(gv, 0.f) + __logf(1.f + t);
+      const float sp = fmaxf(gv, 0.f) + log1p_unit(t);
       const float dgv = run * (-A) * sg;
       dgsm[i * D + c] = __float2bfloat16_rn(dgv);
       if (i < len) {
@@ -820,10 +834,29 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       }
     }
   }
+  }
+drain:
+  // every thread gets here (through a decision above or at the end of the
+  // work); the CTA agrees on whether any wait gave up
+  if (__syncthreads_or(!ok)) {
+    // a bounded wait gave up (the status word says so): let the copies and the
+    // MMA batch that may still be in flight land before the CTA releases its
+    // shared memory and Tensor Memory
+    if (tid == 0) {
+      const uint32_t lim = poll_cap(p, umma::kPollDrain);
+      umma::mbar_wait(rbar, 0, lim);
+      umma::mbar_wait(lbar, 0, lim);
+      if (past_first) umma::mbar_wait(pbar, 0, lim);
+      if (phase > 0) umma::mbar_wait(mbar, (phase - 1) & 1, lim);
+    }
+    cp_async_wait_all();
+  }
   if (tid == kStoreT) umma::bulk_wait_all();  // the stored boxes are complete before the CTA ends
+  umma::tc_fence_before();
+  __syncthreads();
   if (warp == 0) {
     umma::tc_fence_after();
-    umma::tmem_dealloc(tbase, 512);
+    umma::tmem_dealloc(*tslot, 512);
   }
 }
 

@@ -9,43 +9,36 @@
 // from a plugin host that gives the plugin no allocation API.  kda_bwd asks
 // such callers for a workspace buffer they have no way to provide.
 //
-// How it works: the array below is loaded with the module, one copy per GPU
-// that loads the library, and stays allocated until the process exits.  Host
-// code cannot use the array's name as a device address (it denotes a host
-// shadow symbol), so the first call on each device looks the device address
-// up with cudaGetSymbolAddress, with that device current, and caches it.
+// How it works: the array below is part of this library's device image, one
+// copy per GPU, reserved when the runtime loads the module that holds it --
+// under lazy module loading (the CUDA default since 12.2) that is the first
+// kda_bwd_noalloc call on a device, under eager loading the creation of the
+// context -- and kept until the process exits.  Host code cannot use the
+// array's name as a device address (it denotes a host shadow symbol), so
+// every call looks the device address up with cudaGetSymbolAddress, with the
+// calling thread's current device.  After the first call the lookup only
+// reads the runtime's module table; doing it every call (rather than caching
+// the pointer) keeps the address right if the context is torn down and the
+// module reloaded at another address.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "kda.h"
 
 namespace {
 
-constexpr size_t kScratchBytes = (size_t)64 << 20;  // KDA_NOALLOC_SCRATCH_BYTES
-constexpr int kMaxDevices = 64;
+constexpr size_t kScratchBytes = (size_t)64 << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of this device's copy of the scratch array (looked up once
-// per device, then cached).  Returns nullptr on failure.
+// Device address of the current device's copy of the scratch array, or
+// nullptr if the runtime cannot give it.
 void *scratch_for_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = p;
-  }
-  return g_scratch_ptr[dev];
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+  return p;
 }
 
 }  // namespace
-
 extern "C" {
 
 size_t kda_noalloc_scratch_bytes(void) { return kScratchBytes; }

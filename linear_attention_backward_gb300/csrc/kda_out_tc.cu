@@ -71,19 +71,29 @@ __global__ void __launch_bounds__(otc::NT) kda_out_tc_kernel(KdaParams p, const 
   __syncthreads();
   umma::tc_fence_after();
   const uint32_t tbase = *tslot;
+  // Bounded waits: thread 0 waits for the copies and issues the products only
+  // if they landed; the CTA learns the outcome at a barrier, and after a wait
+  // that gave up it writes nothing, drains what is in flight and releases
+  // Tensor Memory.
+  bool ok = true;
   if (tid == 0) {
     umma::mbar_expect_tx(lbar, 32768u + (uint32_t)SM::nB);
-    umma::bulk_g2s(St, static_cast<const char *>(states) + unit * 32768, 32768u, lbar);
-    umma::bulk_g2s(U0t, p.prep + unit * kPrepUnitBytes + kPrepU0, (uint32_t)SM::nB, lbar);
-    umma::mbar_wait(lbar, 0);
+    if ((p.starve & kStarveOut) == 0u) {  // (a timeout test arms the barrier only)
+      umma::bulk_g2s(St, static_cast<const char *>(states) + unit * 32768, 32768u, lbar);
+      umma::bulk_g2s(U0t, p.prep + unit * kPrepUnitBytes + kPrepU0, (uint32_t)SM::nB, lbar);
+    }
+    ok = umma::mbar_wait(lbar, 0, poll_cap(p, umma::kPollLoads));
     umma::tc_fence_after();
-    // o^T = S_n^T QE^T  (A = S read MN-major, B = QE^T [c][i] read MN-major)
-    gemm(tbase, opmn(St, D, 0, CP), true, opmn(QEt, 64, 0, CP), true, 64, D / 16, false);
-    //     + U0^T Mqk^T  (A = U0^T [v][j], B = Mqk [i][j], both read with K = j)
-    gemm(tbase, opk(U0t, 64, 0, CP), false, opk(Mqk, 64, 0, CP), false, 64, 4, true);
-    umma::mma_commit(mbar);
+    if (ok) {
+      // o^T = S_n^T QE^T  (A = S read MN-major, B = QE^T [c][i] read MN-major)
+      gemm(tbase, opmn(St, D, 0, CP), true, opmn(QEt, 64, 0, CP), true, 64, D / 16, false);
+      //     + U0^T Mqk^T  (A = U0^T [v][j], B = Mqk [i][j], both read with K = j)
+      gemm(tbase, opk(U0t, 64, 0, CP), false, opk(Mqk, 64, 0, CP), false, 64, 4, true);
+      umma::mma_commit(mbar);
+    }
   }
-  umma::mbar_wait(mbar, 0, 1u << 20);
+  const bool loaded = !__syncthreads_or(!ok);
+  if (loaded) ok = umma::mbar_wait(mbar, 0, poll_cap(p, umma::kPollMma));
   umma::tc_fence_after();
   // thread v = tid: TMEM lane v holds o^T[v][0..63]; rows land in Os [i][v]
   // (S's region: the products are complete)
@@ -96,14 +106,24 @@ __global__ void __launch_bounds__(otc::NT) kda_out_tc_kernel(KdaParams p, const 
     for (int r = 0; r < 16; ++r) Os[(16 * q + r) * D + tid] = __float2bfloat16_rn(a[r]);
   }
   umma::tc_fence_before();
-  __syncthreads();
-  bf16 *og = static_cast<bf16 *>(out);
+  if (__syncthreads_or(!ok)) {
+    // a bounded wait gave up (the status word says so): the copies or the
+    // products may still be in flight; give them a last bounded wait
+    if (tid == 0) {
+      const uint32_t lim = poll_cap(p, umma::kPollDrain);
+      if (!loaded) umma::mbar_wait(lbar, 0, lim);
+      else umma::mbar_wait(mbar, 0, lim);
+    }
+    __syncthreads();
+  } else {
+    bf16 *og = static_cast<bf16 *>(out);
 #pragma unroll 1
-  for (int e = tid; e < 64 * (D / 8); e += NT) {
-    const int i = e >> 4, c8 = (e & 15) * 8;
-    if (i < len)
-      *reinterpret_cast<uint4 *>(og + ((tok0 + i) * H + h) * D + c8) =
-          *reinterpret_cast<const uint4 *>(Os + i * D + c8);
+    for (int e = tid; e < 64 * (D / 8); e += NT) {
+      const int i = e >> 4, c8 = (e & 15) * 8;
+      if (i < len)
+        *reinterpret_cast<uint4 *>(og + ((tok0 + i) * H + h) * D + c8) =
+            *reinterpret_cast<const uint4 *>(Os + i * D + c8);
+    }
   }
   if (warp == 0) {
     umma::tc_fence_after();

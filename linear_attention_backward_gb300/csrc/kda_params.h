@@ -45,7 +45,18 @@ struct KdaParams {
   // (sequence, head); see kda_scan_tc.cu.  cp_segs = 0: whole-sequence chains.
   int cp_segs, cp_phase, cp_nroles;
   float *cp_buf;
+  // Timeout tests: kernels named in `starve` (kStarve* bits) arm their first
+  // load barrier but issue none of its copies, so that its bounded wait runs
+  // out; `poll_limit` (0 = the kernels' defaults) caps every bounded wait.
+  uint32_t starve, poll_limit;
 };
+
+constexpr uint32_t kStarvePrep = 1, kStarveScan = 2, kStarveGrads = 4, kStarveOut = 8;
+
+// poll limit of a bounded wait: the launch's cap, else the kernel's default
+__host__ __device__ constexpr uint32_t poll_cap(const KdaParams &p, uint32_t dflt) {
+  return p.poll_limit != 0u && p.poll_limit < dflt ? p.poll_limit : dflt;
+}
 
 // fp32 K x V tiles per (sequence, head) of the context-parallel scans:
 // forward segment starts (P - 1), reverse segment ends (P - 1) and the

@@ -118,9 +118,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     umma::mbar_init(rbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     umma::mbar_expect_tx(rbar, 3 * 16384u);
-    umma::tma_load_3d(QM, &tm.q, 0, h, (int)tok0, rbar);
-    umma::tma_load_3d(QM + 16384, &tm.k, 0, h, (int)tok0, rbar);
-    umma::tma_load_3d(QM + 32768, &tm.g, 0, h, (int)tok0, rbar);
+    if ((p.starve & kStarvePrep) == 0u) {  // (a timeout test arms the barrier only)
+      umma::tma_load_3d(QM, &tm.q, 0, h, (int)tok0, rbar);
+      umma::tma_load_3d(QM + 16384, &tm.k, 0, h, (int)tok0, rbar);
+      umma::tma_load_3d(QM + 32768, &tm.g, 0, h, (int)tok0, rbar);
+    }
   }
   if (warp == 0) umma::tmem_alloc(tslot, 256);
   __syncthreads();
@@ -142,9 +144,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   const int cp = tid & 63, I = tid >> 6, c = 2 * cp;
   uint32_t kraw[16], qraw[16];
   float g0[16], g1[16];
+  // Every bounded wait folds its result into `ok`; the CTA decides at its
+  // barriers (__syncthreads_or).  Once a wait has given up no further MMA is
+  // issued, the CTA drains what is in flight and releases Tensor Memory
+  // (`drain` below).  What a timed-out product left in Tensor Memory may
+  // reach this call's operand blocks, whose status word then reports the
+  // timeout.
+  bool ok;
+  uint32_t phase = 0;  // completions of the MMA barrier waited for
   {
     uint32_t graw[16];
-    umma::mbar_wait(rbar, 0);
+    ok = umma::mbar_wait(rbar, 0, poll_cap(p, umma::kPollLoads));
 #pragma unroll
     for (int r = 0; r < 16; ++r) {  // rows past the chunk (the next sequence's) read as zero
       const int i = 16 * I + r;
@@ -188,7 +198,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     Bblk[I * D + c] = g0[15] - g0[7];
     Bblk[I * D + c + 1] = g1[15] - g1[7];
   }
-  __syncthreads();
+  if (__syncthreads_or(!ok)) goto drain;
+  {
   if (tid < CHUNK) {  // row norms: block I's rows live in warps 2I, 2I + 1
     const int ib = tid >> 4, r = tid & 15;
     sv.rk[tid] = rsqrtf(red[(2 * ib) * 16 + r] + red[(2 * ib + 1) * 16 + r] + p.eps);
@@ -342,12 +353,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   __syncthreads();
   umma::tc_fence_after();
   const uint32_t tbase = *tslot;
-  uint32_t phase = 0;
   auto mma_wait = [&]() {
-    const bool ok = umma::mbar_wait(mbar, phase & 1, 1u << 20);
+    ok = umma::mbar_wait(mbar, phase & 1, poll_cap(p, umma::kPollMma)) && ok;
     phase++;
     umma::tc_fence_after();
-    return ok;
   };
   // ---- W^T per key block J (the block factor e^(m_J) is applied per lane below) ----
   if (tid == 0) {
@@ -379,7 +388,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   cp_async_wait_all();  // v has landed
   umma::fence_async_smem();
   umma::tc_fence_before();
-  __syncthreads();
+  if (__syncthreads_or(!ok)) goto drain;
   // ---- U0^T = v^T (INV diag(beta))^T ;  (Mqk W)^T = W^T Mqk^T ----
   if (tid == 0) {
     umma::tc_fence_after();
@@ -406,11 +415,26 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     for (int q = 0; q < 4; ++q)
       st16_bf(unit + kPrepQE + umma::core_off(ch, 32 * gq + 8 * q, 64), a + 8 * q);
   }
+  }
+drain:
+  // every thread gets here (through a decision above or at the end of the
+  // work); the CTA agrees on whether any wait gave up
+  if (__syncthreads_or(!ok)) {
+    // a bounded wait gave up (the status word says so): let the copies and the
+    // MMA batch that may still be in flight land before the CTA releases its
+    // shared memory and Tensor Memory
+    if (tid == 0) {
+      const uint32_t lim = poll_cap(p, umma::kPollDrain);
+      umma::mbar_wait(rbar, 0, lim);
+      if (phase > 0) umma::mbar_wait(mbar, (phase - 1) & 1, lim);
+    }
+    cp_async_wait_all();
+  }
   umma::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     umma::tc_fence_after();
-    umma::tmem_dealloc(tbase, 256);
+    umma::tmem_dealloc(*tslot, 256);
   }
 }
 

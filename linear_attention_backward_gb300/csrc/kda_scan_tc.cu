@@ -210,8 +210,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   // A slot is refilled with the next chunk's data as soon as its consumer is done.
   // Slot sl's copies are issued by thread 32 (sl + 1) (warps 1-3), publishing
   // and prefetching by threads 160 and 192: thread 0 only issues the MMAs.
+  // (a timeout test arms the first chunk's barriers but issues no copies)
+  const bool starve = (p.starve & kStarveScan) != 0u;
   auto load_slot = [&](int sl, int it) {
     const char *u = unit_of(chunk_of(it));
+    if (starve && it == 0) {
+      if (tid == 32 * (sl + 1)) umma::mbar_expect_tx(bars + sl, 16u);
+      return;
+    }
     if (tid == 32 * (sl + 1)) {
       if (fwd) {
         if (sl == 0) {
@@ -295,8 +301,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   if (nck > 0) publish(chunk_of(0));
   const uint32_t tbase = *tslot;
   uint32_t ph[4] = {0u, 0u, 0u, 0u};  // phase of each barrier (bars[3] = MMA completion)
-  auto wait_bar = [&](int k, uint32_t limit = 1u << 24) {
-    const bool ok = umma::mbar_wait(bars + k, ph[k] & 1, limit);
+  auto wait_bar = [&](int k) {
+    const bool ok = umma::mbar_wait(bars + k, ph[k] & 1,
+                                    poll_cap(p, k == 3 ? umma::kPollMma : umma::kPollLoads));
     ph[k]++;
     return ok;
   };
@@ -412,7 +419,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
     // a bounded wait gave up (status already flagged): let copies and MMAs in
     // flight land before the buffers and Tensor Memory are released
     if (tid == 0) {
-      for (int k = 0; k < 4; ++k) umma::mbar_wait(bars + k, ph[k] & 1, 1u << 16);
+      for (int k = 0; k < 4; ++k) umma::mbar_wait(bars + k, ph[k] & 1, poll_cap(p, umma::kPollDrain));
     }
     cp_async_wait_all();
     __syncthreads();

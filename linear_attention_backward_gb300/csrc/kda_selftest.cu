@@ -14,7 +14,7 @@ namespace kda {
 __global__ void __launch_bounds__(128) kda_selftest_umma_kernel(const bf16 *A, const bf16 *B,
                                                                  float *D, int N, int K,
                                                                  int a_mn, int b_mn,
-                                                                 int swap_lbo_sbo) {
+                                                                 int layout) {
   extern __shared__ __align__(1024) char smem[];
   constexpr int M = 128;
   bf16 *As = reinterpret_cast<bf16 *>(smem);
@@ -26,14 +26,14 @@ __global__ void __launch_bounds__(128) kda_selftest_umma_kernel(const bf16 *A, c
   // A element (m, k): K-major -> core_off(m, k, K); MN-major -> core_off(k, m, M)
   for (int e = tid; e < M * K; e += 128) {
     const int m = e / K, k = e % K;
-    const uint32_t off = swap_lbo_sbo == 2 ? (a_mn ? umma::pcore_off(k, m, M) : umma::pcore_off(m, k, K))
-                                           : (a_mn ? umma::core_off(k, m, M) : umma::core_off(m, k, K));
+    const uint32_t off = layout == 1 ? (a_mn ? umma::pcore_off(k, m, M) : umma::pcore_off(m, k, K))
+                                     : (a_mn ? umma::core_off(k, m, M) : umma::core_off(m, k, K));
     *reinterpret_cast<bf16 *>(reinterpret_cast<char *>(As) + off) = A[e];
   }
   for (int e = tid; e < N * K; e += 128) {
     const int n = e / K, k = e % K;
-    const uint32_t off = swap_lbo_sbo == 2 ? (b_mn ? umma::pcore_off(k, n, N) : umma::pcore_off(n, k, K))
-                                           : (b_mn ? umma::core_off(k, n, N) : umma::core_off(n, k, K));
+    const uint32_t off = layout == 1 ? (b_mn ? umma::pcore_off(k, n, N) : umma::pcore_off(n, k, K))
+                                     : (b_mn ? umma::core_off(k, n, N) : umma::core_off(n, k, K));
     *reinterpret_cast<bf16 *>(reinterpret_cast<char *>(Bs) + off) = B[e];
   }
   if (tid == 0) umma::mbar_init(mbar, 1);
@@ -57,15 +57,12 @@ __global__ void __launch_bounds__(128) kda_selftest_umma_kernel(const bf16 *A, c
       else { a_lead = (M / 8) * 128; a_str = 128; a_step = 2 * (M / 8) * 128; }
       if (!b_mn) { b_lead = 128; b_str = (K / 8) * 128; b_step = 256; }
       else { b_lead = (N / 8) * 128; b_str = 128; b_step = 2 * (N / 8) * 128; }
-      if (swap_lbo_sbo == 2) {  // padded core layout
+      if (layout == 1) {  // padded core layout
         const uint32_t cs = umma::kCoreStride;
         if (!a_mn) { a_lead = cs; a_str = (K / 8) * cs; a_step = 2 * cs; }
         else { a_lead = (M / 8) * cs; a_str = cs; a_step = 2 * (M / 8) * cs; }
         if (!b_mn) { b_lead = cs; b_str = (K / 8) * cs; b_step = 2 * cs; }
         else { b_lead = (N / 8) * cs; b_str = cs; b_step = 2 * (N / 8) * cs; }
-      } else if (swap_lbo_sbo) {
-        uint32_t t = a_lead; a_lead = a_str; a_str = t;
-        t = b_lead; b_lead = b_str; b_str = t;
       }
       const uint64_t ad = umma::smem_desc(a0 + s * a_step, a_lead, a_str);
       const uint64_t bd = umma::smem_desc(b0 + s * b_step, b_lead, b_str);
@@ -92,9 +89,10 @@ __global__ void __launch_bounds__(128) kda_selftest_umma_kernel(const bf16 *A, c
 }  // namespace kda
 
 extern "C" kda_status kda_selftest_umma(const void *A, const void *B, float *D, int N, int K,
-                                        int a_mn, int b_mn, int swap_lbo_sbo,
+                                        int a_mn, int b_mn, int layout,
                                         kda_stream_t stream) {
-  if (!A || !B || !D || (N != 32 && N != 64 && N != 128) || K < 16 || K > 128 || K % 16)
+  if (!A || !B || !D || (N != 32 && N != 64 && N != 128) || K < 16 || K > 128 || K % 16 ||
+      (layout != 0 && layout != 1))
     return KDA_ERR_INVALID_ARG;
   auto k = kda::kda_selftest_umma_kernel;
   // generous allocation: the tiles use the first 80 KB only
@@ -103,6 +101,6 @@ extern "C" kda_status kda_selftest_umma(const void *A, const void *B, float *D, 
     return KDA_ERR_CUDA;
   k<<<1, 128, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
       static_cast<const kda::bf16 *>(A), static_cast<const kda::bf16 *>(B), D, N, K, a_mn, b_mn,
-      swap_lbo_sbo);
+      layout);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -108,10 +108,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *mbar, uint32_t parity) {
       : "r"(smem_u32(mbar)), "r"(parity));
   return ok != 0;
 }
+// Poll limits of the bounded waits: copies from HBM, MMA completion, and the
+// last wait for work still in flight after a wait has given up (the drain).
+constexpr uint32_t kPollLoads = 1u << 24;
+constexpr uint32_t kPollMma = 1u << 20;
+constexpr uint32_t kPollDrain = 1u << 16;
 // Bounded wait: gives up after `limit` polls, flags the device status word
-// (timeout) and returns false; the caller must then skip the dependent work.
+// (timeout) and returns false; the caller must then skip the dependent work,
+// drain what is in flight (another bounded wait) and release its resources.
 __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity,
-                                          uint32_t limit = 1u << 24) {
+                                          uint32_t limit = kPollLoads) {
   for (uint32_t n = 0; n < limit; ++n)
     if (mbar_try_wait(mbar, parity)) return true;
   set_status(5);

@@ -82,12 +82,16 @@ def unpack_core_tiles(t):
     return x.transpose(-3, -2).reshape(*lead, R, C).contiguous()
 
 
-def check_dalog(g, ref, x, tol):
-    """dA_log[h] sums dgk * gk over every token and channel of head h, terms
-    of both signs: its error is that of the terms (per-tensor tol, as dg)
-    times the cancellation ||terms||_2 / |sum|.  Bounded here against the
-    L2 norm of the oracle's terms, per head (dgk * gk = dg softplus / sigmoid
-    of the biased gate)."""
+def check_dalog_biased(g, ref, x, tol):
+    """WEAKER dA_log check, used only by the gate-bias (dt_bias) tests.
+
+    Every other test compares dA_log by the plain per-tensor relative L2
+    bound over the [H] vector, like the other gradients.  With a gate bias
+    the sum dA_log[h] = sum dgk * gk cancels by ~20x (terms of both signs),
+    so its relative error is that of the terms (the dg error) times the
+    cancellation.  Here the per-head error is bounded by tol times the L2
+    norm of the oracle's terms (dgk * gk = dg softplus / sigmoid of the
+    biased gate) instead of tol times |dA_log[h]|."""
     z = f64_tokens(x["g"]) + (0.0 if x.get("dt_bias") is None
                               else x["dt_bias"].double().numpy()[None])
     terms = ref["dg"] * np.logaddexp(0.0, z) * (1.0 + np.exp(-z))
@@ -95,3 +99,51 @@ def check_dalog(g, ref, x, tol):
     for h in range(got.shape[0]):
         l2 = np.linalg.norm(terms[:, h])
         assert abs(got[h] - ref["dA_log"][h]) <= tol * l2, (h, got[h], ref["dA_log"][h], l2)
+
+
+def full_parity(x, g, keys=GRADS, nthreads=0):
+    """Per-tensor relative L2 error of every gradient over a whole workload.
+
+    The oracle runs one sequence at a time (all heads, OpenMP over heads) so
+    that its fp64 arrays stay a fraction of the workload's; the squared norms
+    of the error and of the oracle's tensor are summed over sequences, and
+    dA_log (a sum over sequences) is summed before it is compared.  ``g``
+    holds the GPU gradients (device tensors).  Returns {key: rel-L2}."""
+    cu = wl.seq_bounds(x)
+    flat = lambda t: t.reshape(-1, *t.shape[2:])
+    H = x["q"].shape[2]
+    num = {k: 0.0 for k in keys}
+    den = {k: 0.0 for k in keys}
+    dA = np.zeros(H)
+    ddt = None if x.get("dt_bias") is None else np.zeros(tuple(x["dt_bias"].shape))
+    tok_keys = [k for k in ("dq", "dk", "dv", "dg", "dbeta") if k in keys]
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        if b == a:
+            ref = {"dh0": x["dhT"][s].double().numpy()}
+        else:
+            pick = lambda n: flat(x[n])[a:b].double().numpy()
+            ref = oracle.backward(
+                pick("q"), pick("k"), pick("v"), pick("g"), pick("beta"),
+                x["A_log"].double().numpy(), x["h0"][s:s + 1].double().numpy(), pick("dO"),
+                x["dhT"][s:s + 1].double().numpy(), cu_seqlens=[0, b - a],
+                dt_bias=_bias(x), nthreads=nthreads)
+            dA += ref["dA_log"]
+            if ddt is not None:
+                ddt += ref["ddt_bias"]
+            for key in tok_keys:
+                got = flat(g[key])[a:b].double().cpu().numpy()
+                num[key] += float(np.sum((got - ref[key]) ** 2))
+                den[key] += float(np.sum(ref[key] ** 2))
+            ref["dh0"] = ref["dh0"][0]
+        if "dh0" in keys:
+            got = g["dh0"][s].double().cpu().numpy()
+            num["dh0"] += float(np.sum((got - ref["dh0"]) ** 2))
+            den["dh0"] += float(np.sum(ref["dh0"] ** 2))
+    errs = {k: (np.sqrt(num[k] / den[k]) if den[k] > 0 else np.sqrt(num[k]))
+            for k in keys if k != "dA_log"}
+    if "dA_log" in keys:
+        errs["dA_log"] = rel_l2(g["dA_log"].double().cpu().numpy(), dA)
+    if ddt is not None and "ddt_bias" in g:
+        errs["ddt_bias"] = rel_l2(g["ddt_bias"].double().cpu().numpy(), ddt)
+    return errs

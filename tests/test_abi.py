@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_strings(L):
-    assert L.kda_abi_version() == 5
+    assert L.kda_abi_version() == 6
     for st in range(9):
         assert len(L.kda_status_str(st)) > 0
 
@@ -123,10 +123,18 @@ def test_bwd_pointer_checks(L):
     assert L.kda_bwd(ctypes.byref(s), *args, None, ws_ok, None) == 3
     assert L.kda_bwd(ctypes.byref(s), *args, fake, ctypes.c_size_t(ws_ok.value - 1), None) == 3
     assert L.kda_bwd(ctypes.byref(s), *args, ctypes.c_void_p((1 << 20) + 16), ws_ok, None) == 3
-    # fwd_states: missing states
-    st = L.kda_fwd_states(ctypes.byref(s), fake, fake, fake, fake, fake, None, None, None, None,
-                          None)
-    assert st == 1
+    # fwd_states: missing states; missing q (the tcgen05 path's prep needs it);
+    # workspace missing or too small
+    a = [fake] * 6 + [None, None, fake, None]  # q k v g beta A_log, dt_bias, h0, states, hT
+    b = list(a); b[8] = None
+    assert L.kda_fwd_states(ctypes.byref(s), *b, fake, ws_ok, None) == 1
+    b = list(a); b[0] = None
+    assert L.kda_fwd_states(ctypes.byref(s), *b, fake, ws_ok, None) == 1
+    assert L.kda_fwd_states(ctypes.byref(s), *a, None, ws_ok, None) == 3
+    assert L.kda_fwd_states(ctypes.byref(s), *a, fake, ctypes.c_size_t(ws_ok.value - 1),
+                            None) == 3
+    # the selftest's layouts are 0 (packed) and 1 (padded) only
+    assert L.kda_selftest_umma(fake, fake, fake, 64, 64, 0, 0, 2, None) == 1
 
 
 def test_host_cu_seqlens_check(L):

@@ -13,7 +13,7 @@ import torch
 import __graft_entry__
 import linear_attention_backward_gb300 as kda
 from linear_attention_backward_gb300 import workloads as wl
-from kda_testutil import GRADS, check_dalog, gpu_bwd, oracle_bwd, rel_l2
+from kda_testutil import GRADS, gpu_bwd, oracle_bwd, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -61,8 +61,7 @@ def test_beta_zero():
     assert kda.get_device_status() == 0
     ref = oracle_bwd(x)
     assert np.abs(ref["dv"]).max() == 0 and np.abs(ref["dk"]).max() == 0
-    _compare(g, ref, ("dq", "dk", "dv", "dg", "dbeta", "dh0"))
-    check_dalog(g, ref, x, TOL)
+    _compare(g, ref, GRADS)
 
 
 def test_zero_query_and_key_rows():
@@ -93,7 +92,10 @@ def test_no_decay_delta_rule():
     g, _ = gpu_bwd(x)
     assert kda.get_device_status() == 0
     ref = oracle_bwd(x)
-    _compare(g, ref, ("dq", "dk", "dv", "dbeta", "dh0"))
+    # dA_log = sum dgk * gk with gk = -e^A_log softplus(-30) ~ -1e-13 e^A_log:
+    # tiny, but the plain per-tensor bound holds only if softplus keeps its
+    # relative precision far out in the negative tail
+    _compare(g, ref, ("dq", "dk", "dv", "dbeta", "dA_log", "dh0"))
     # dg = dgk * (-e^A_log) * sigmoid(g) carries sigmoid(-30) ~ 1e-13: zero to
     # bf16 output precision on both sides
     got = g["dg"].double().cpu().numpy().reshape(ref["dg"].shape)
@@ -116,8 +118,7 @@ def test_heavy_decay_inside_the_block_range():
     ref = oracle_bwd(x)
     for k in GRADS:
         assert np.isfinite(g[k].double().cpu().numpy()).all(), k
-    _compare(g, ref, ("dq", "dk", "dv", "dg", "dbeta", "dh0"))
-    check_dalog(g, ref, x, TOL)
+    _compare(g, ref, GRADS)
 
 
 @pytest.mark.parametrize("dtype,K", [("bf16", 128), ("bf16", 64), ("fp32", 64)])

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("N", [32, 64, 128])
 @pytest.mark.parametrize("K", [16, 64, 128])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
-@pytest.mark.parametrize("layout", [0, 2])
+@pytest.mark.parametrize("layout", [0, 1])
 def test_umma_tile(N, K, a_mn, b_mn, layout):
     __graft_entry__.build()
     L = kda.lib()
