@@ -94,7 +94,9 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms, each sample
+    stamped with the host clock on arrival, so that the samples taken during
+    the timed region can be kept alone (``window``)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -103,14 +105,15 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, line)
         self.thread = None
+        self.window = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.gpu)],
+                 "-lms", "20", "-i", str(self.gpu)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -120,7 +123,15 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def running(self):
+        """True once the first sample has arrived (or sampling is unavailable)."""
+        return self.proc is None or len(self.lines) > 0
+
+    def mark(self, t0, t1):
+        """Keep only samples that arrived in [t0, t1] (host clock)."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -134,7 +145,13 @@ class ClockSampler:
             self.thread.join(timeout=2)
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        if self.window is not None:
+            inside = [ln for t, ln in lines if self.window[0] <= t <= self.window[1]]
+            lines = inside if inside else [ln for _, ln in lines[-3:]]
+        else:
+            lines = [ln for _, ln in lines]
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -150,7 +167,9 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "interval_ms": 20,
+                "window": "samples that arrived during the timed region" if self.window else
+                          "all samples", "reasons": sorted(reasons)}
 
 
 def max_over_ranks(ms, pg, device):
@@ -412,13 +431,20 @@ def main():
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev) if flushes_l2(w) else None
-    torch.cuda.synchronize()
-    if pg:
-        pg.barrier()
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
                            os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local])
     sampler.start()
+    # untimed steps until the sampler is live (nvidia-smi takes a moment to
+    # start), so that its samples cover the timed region
+    t_wait = time.perf_counter()
+    while not sampler.running() and time.perf_counter() - t_wait < 10.0:
+        step()
+        torch.cuda.synchronize()
     torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
     start.record()
     for i in range(K):
         if flush is not None:
@@ -426,6 +452,7 @@ def main():
         step(evs[i])
     end.record()
     torch.cuda.synchronize()
+    sampler.mark(t0, time.perf_counter())
     clocks = sampler.stop()
     if pg:
         pg.barrier()

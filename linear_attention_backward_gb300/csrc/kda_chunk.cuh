@@ -59,8 +59,11 @@ __device__ __forceinline__ bool slot_owner(const KdaParams &p, int64_t slot, int
   int L;
   int64_t s0;
   if (p.cu == nullptr) {
-    s = (int)(slot / p.nps);
-    j = (int)(slot % p.nps);
+    // slots number fewer than 2^31 (B * T <= 2^31 tokens): 32-bit division
+    // (the 64-bit one is a subroutine call)
+    const uint32_t sl = (uint32_t)slot, nps = (uint32_t)p.nps;
+    s = (int)(sl / nps);
+    j = (int)(sl - (uint32_t)s * nps);
     if (s >= p.B) return false;
   } else {
     int lo = 0, hi = p.num_seqs - 1;
@@ -245,8 +248,8 @@ __device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, cons
     const int i = r0 + r;
     const float2 gv = load2(Gr + i * K + c);
     const bool ok = i < len;
-    run0 += ok ? -A * softplus_f(gv.x + bias0) : 0.f;
-    run1 += ok ? -A * softplus_f(gv.y + bias1) : 0.f;
+    run0 += ok ? -A * softplus_gate(gv.x + bias0) : 0.f;
+    run1 += ok ? -A * softplus_gate(gv.y + bias1) : 0.f;
     g0[r] = run0;
     g1[r] = run1;
   }

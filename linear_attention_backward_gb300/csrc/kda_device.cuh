@@ -218,10 +218,17 @@ __device__ __forceinline__ float log1p_unit(float t) {
   const float s = t * fmaf(-t, fmaf(-t, fmaf(-t, fmaf(-t, 0.2f, 0.25f), 0.33333334f), 0.5f), 1.f);
   return t < 0.03125f ? s : __logf(1.f + t);
 }
+// softplus for the dA_log terms dgk * gk, whose sum needs gk's relative
+// precision: log(1 + e^x) = max(x, 0) + log(1 + e^-|x|) with the accurate
+// log1p above (softplus(-30) ~ 1e-13 is not rounded to zero)
 __device__ __forceinline__ float softplus_f(float x) {
-  // log(1 + e^x) = max(x, 0) + log(1 + e^-|x|), relative precision kept far
-  // into the negative tail (softplus(-30) ~ 1e-13 is not rounded to zero)
   return fmaxf(x, 0.f) + log1p_unit(__expf(-fabsf(x)));
+}
+// softplus for the gate's running sums, which feed the decays e^gc: there an
+// absolute error of ~1e-7 per token is far below the bf16 operands' own, so
+// the plain fast log of 1 + e^-|x| serves (it rounds values below ~1e-7 to 0)
+__device__ __forceinline__ float softplus_gate(float x) {
+  return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
 }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + __expf(-x)); }
 

@@ -183,7 +183,7 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
     for (int r = 0; r < 16; ++r) {
       const int i = 16 * I + r;
       const float gv = BF16_AT(g2, r) + bias;
-      run += i < len ? -A * softplus_f(gv) : 0.f;
+      run += i < len ? -A * softplus_gate(gv) : 0.f;
       d[r] = run;
     }
     const float ref = d[7];
@@ -851,7 +851,9 @@ drain:
     }
     cp_async_wait_all();
   }
-  if (tid == kStoreT) umma::bulk_wait_all();  // the stored boxes are complete before the CTA ends
+  // the stored boxes have read shared memory before the CTA ends (their
+  // global writes complete before the grid does)
+  if (tid == kStoreT) umma::bulk_wait_read();
   umma::tc_fence_before();
   __syncthreads();
   if (warp == 0) {

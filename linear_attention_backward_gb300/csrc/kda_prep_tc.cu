@@ -184,8 +184,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     for (int r = 0; r < 16; ++r) {
       const bool ok = 16 * I + r < len;
       const float2 gv = bf2_to_f2(graw[r]);
-      run0 += ok ? -A * softplus_f(gv.x + bias0) : 0.f;
-      run1 += ok ? -A * softplus_f(gv.y + bias1) : 0.f;
+      run0 += ok ? -A * softplus_gate(gv.x + bias0) : 0.f;
+      run1 += ok ? -A * softplus_gate(gv.y + bias1) : 0.f;
       g0[r] = run0;
       g1[r] = run1;
     }

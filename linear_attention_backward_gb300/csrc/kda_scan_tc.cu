@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
             make_float4(X[4 * q], X[4 * q + 1], X[4 * q + 2], X[4 * q + 3]);
     }
   }
-  if (tid == 160) umma::bulk_wait_all();
+  if (tid == 160) umma::bulk_wait_read();  // (the global writes complete before the grid does)
   umma::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
