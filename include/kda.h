@@ -270,8 +270,11 @@ size_t kda_noalloc_scratch_bytes(void);
  * (0) or MN-major (1) core-matrix layout; D is [128][N] fp32 (device).
  * N in {32, 64, 128}, K a multiple of 16 up to 128.  layout: 0 = core
  * matrices packed (128-byte stride), 1 = padded core layout (144-byte stride,
- * the one the kernels use for tiles their threads write).  Other values are
- * rejected (KDA_ERR_INVALID_ARG). */
+ * the one the kernels use for tiles their threads write), 2 = 128-byte
+ * swizzled layout (8-row x 128-byte atoms, 16-byte chunk j of row r at
+ * j ^ (r % 8): what a TMA copy with 128-byte swizzling writes; K a multiple
+ * of 64, and N >= 64 when B is MN-major).  Other values are rejected
+ * (KDA_ERR_INVALID_ARG). */
 kda_status kda_selftest_umma(const void *A, const void *B, float *D, int N, int K, int a_mn,
                              int b_mn, int layout, kda_stream_t stream);
 

@@ -177,10 +177,10 @@ cudaError_t forward_states_tc(kda::KdaParams &p, const kda_shape *shape, char *w
   if (e == cudaSuccess && cp >= 3) {
     p.cp_segs = cp;
     p.cp_buf = reinterpret_cast<float *>(w + cp_offset(shape));
-    e = kda::scan_tc_cp_launch(p, p.prep, 1, cs);
+    e = kda::scan_tc_cp_launch(p, tm, p.prep, 1, cs);
     p.cp_segs = 0;
   } else if (e == cudaSuccess) {
-    e = kda::scan_tc_launch(p, p.prep, 1, cs);
+    e = kda::scan_tc_launch(p, tm, p.prep, 1, cs);
   }
   return e;
 }
@@ -420,10 +420,10 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
       // few (sequence, head) chains: context-parallel scans over segments
       p.cp_segs = cp;
       p.cp_buf = reinterpret_cast<float *>(w + cp_offset(shape));
-      e = kda::scan_tc_cp_launch(p, p.prep, nroles, cs);
+      e = kda::scan_tc_cp_launch(p, tm, p.prep, nroles, cs);
       p.cp_segs = 0;
     } else if (e == cudaSuccess) {
-      e = kda::scan_tc_launch(p, p.prep, nroles, cs);
+      e = kda::scan_tc_launch(p, tm, p.prep, nroles, cs);
     }
   } else if (e == cudaSuccess) {
     // the per-band scans write row-major tiles; caller states on the tcgen05

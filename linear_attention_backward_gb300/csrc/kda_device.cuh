@@ -214,9 +214,21 @@ __device__ __forceinline__ float quad_sum(float v) {
 // (1 + t rounds to 1 below 2^-24), so arguments below 2^-5 take the Taylor
 // series t - t^2/2 + t^3/3 - t^4/4 + t^5/5 instead (relative truncation
 // error below t^5 / 6 < 1e-8 there).
+__device__ __forceinline__ float log1p_series(float t) {
+  return t * fmaf(-t, fmaf(-t, fmaf(-t, fmaf(-t, 0.2f, 0.25f), 0.33333334f), 0.5f), 1.f);
+}
 __device__ __forceinline__ float log1p_unit(float t) {
-  const float s = t * fmaf(-t, fmaf(-t, fmaf(-t, fmaf(-t, 0.2f, 0.25f), 0.33333334f), 0.5f), 1.f);
-  return t < 0.03125f ? s : __logf(1.f + t);
+  return t < 0.03125f ? log1p_series(t) : __logf(1.f + t);
+}
+// The same for a warp whose 32 arguments are mostly not small: the fast log,
+// replaced by the series only where t < 2^-14 (where the fast log's error of
+// ~6e-8 reaches 1e-3 of the value), behind a warp vote so that the common
+// case pays one vote.  All 32 lanes must call it together.
+__device__ __forceinline__ float log1p_unit_warp(float t) {
+  float l = __logf(1.f + t);
+  const bool tiny = t < 6.103515625e-05f;
+  if (__any_sync(0xffffffffu, tiny) && tiny) l = log1p_series(t);
+  return l;
 }
 // softplus for the dA_log terms dgk * gk, whose sum needs gk's relative
 // precision: log(1 + e^x) = max(x, 0) + log(1 + e^-|x|) with the accurate

@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       }
     }
   }
-  if (__syncthreads_or(!ok)) goto drain;
+  if (__syncthreads_or(!ok)) { ok = false; goto drain; }
   {
   past_first = true;
   umma::tc_fence_after();
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   cp_async_wait_all();                 // dO, v (and row-major S)
   ok = umma::mbar_wait(lbar, 0, lim_ld) && ok;  // S, dS, kr^T
   umma::fence_async_smem();
-  if (__syncthreads_or(!ok)) goto drain;
+  if (__syncthreads_or(!ok)) { ok = false; goto drain; }
 
   // ---- R1 = P1: kdS^T = S^T kd^T ; the epilogue forms Xr^T = v^T - kdS^T ----
   if (tid == 0) {
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   ok = umma::mbar_wait(pbar, 0, lim_ld) && ok;  // Mqk, INV, INVb, G
   umma::fence_async_smem();
   umma::tc_fence_before();
-  if (__syncthreads_or(!ok)) goto drain;
+  if (__syncthreads_or(!ok)) { ok = false; goto drain; }
 
   // ---- R2 = P2 + P3a: U^T = Xr^T INVb^T ; dU^T = dO^T Mqk + dS^T kr^T (dU needs no U) ----
   if (tid == 0) {
@@ -414,15 +414,19 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     dgT[I * D + c] = __expf(sv.gT[c]) * pp;
   }
   mma_wait();
-  tld16(tbase, 64, acc);
+  {
+    float acc2[16];  // both loads in flight before one wait
+    tld16_nw(tbase, 64, acc);
+    tld16_nw(tbase, 128, acc2);
+    umma::tmem_ld_wait();
 #pragma unroll
-  for (int q = 0; q < 2; ++q) pstore8(Ut, c, 16 * I + 8 * q, 64, acc + 8 * q);  // U^T[d][i]
-  tld16(tbase, 128, acc);
+    for (int q = 0; q < 2; ++q) pstore8(Ut, c, 16 * I + 8 * q, 64, acc + 8 * q);  // U^T[d][i]
 #pragma unroll
-  for (int q = 0; q < 2; ++q) pstore8(dUT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // dU^T[d][i]
+    for (int q = 0; q < 2; ++q) pstore8(dUT, c, 16 * I + 8 * q, 64, acc2 + 8 * q);  // dU^T[d][i]
+  }
   umma::fence_async_smem();
   umma::tc_fence_before();
-  if (__syncthreads_or(!ok)) goto drain;
+  if (__syncthreads_or(!ok)) { ok = false; goto drain; }
 
   // ---- R3 = P5 + P3b: dvcorr^T = dU^T INV ; dkr^T = dS U^T ; dv, dbeta1, dvcorr[i][d] ----
   if (tid == 0) {
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   umma::fence_async_smem();
   umma::tc_fence_before();
-  if (__syncthreads_or(!ok)) goto drain;
+  if (__syncthreads_or(!ok)) { ok = false; goto drain; }
   if (tid < 64) {  // dbeta1_i: block i / 16 lives in warps 4 (i / 16) .. + 3
     const int i = tid, w0 = (i >> 4) * 4, r = i & 15;
     dbs[i] = red[(w0 + 0) * 16 + r] + red[(w0 + 1) * 16 + r] + red[(w0 + 2) * 16 + r] +
@@ -495,11 +499,13 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       float o8[8];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
+        float g8[8];  // G[i][16 I + 8 q .. + 7], one 16-byte row of a core matrix
+        ld16_bf(Gbf + umma::core_off(i, 16 * I + 8 * q, 64), g8);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const int jj = 16 * I + 8 * q + t;
           const float dak = jj < i ? -v16[8 * q + t] : 0.f;
-          db2 = fmaf(dak, __bfloat162float(*reinterpret_cast<const bf16 *>(Gbf + umma::core_off(i, jj, 64))), db2);
+          db2 = fmaf(dak, g8[t], db2);
           o8[t] = sv.beta[i] * dak;
         }
         pstore8(dMA, dma_row(i, 1), 16 * I + 8 * q, 64, o8);
@@ -522,7 +528,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   umma::fence_async_smem();
   umma::tc_fence_before();
   if (tid == kStoreT) umma::bulk_wait_read();  // the dv box has left R_A [0, 16K) (the g rows go there)
-  if (__syncthreads_or(!ok)) goto drain;
+  if (__syncthreads_or(!ok)) { ok = false; goto drain; }
   if (tid < 64 && tid < len) {
     const float db = dbs[tid] + red2[tid] + red2[64 + tid] + red2[128 + tid] + red2[192 + tid];
     reinterpret_cast<bf16 *>(p.dbeta)[(tok0 + tid) * H + h] = __float2bfloat16_rn(db);
@@ -627,7 +633,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     const float t = rows16_sum(pr);
     if (lane < 16) red[warp * 16 + lane] = t;
     umma::tc_fence_before();
-    if (__syncthreads_or(!ok)) goto drain;
+    if (__syncthreads_or(!ok)) { ok = false; goto drain; }
     // lane l < 16: row 16 I + l summed over the block's 4 warps; broadcast below
     const float tot = red[(4 * I) * 16 + (lane & 15)] + red[(4 * I + 1) * 16 + (lane & 15)] +
                       red[(4 * I + 2) * 16 + (lane & 15)] + red[(4 * I + 3) * 16 + (lane & 15)];
@@ -740,7 +746,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     const float t = rows16_sum(pr);
     if (lane < 16) red[warp * 16 + lane] = t;
     dgT[I * D + c] += colp;
-    if (__syncthreads_or(!ok)) goto drain;
+    if (__syncthreads_or(!ok)) { ok = false; goto drain; }
     const float tot = red[(4 * I) * 16 + (lane & 15)] + red[(4 * I + 1) * 16 + (lane & 15)] +
                       red[(4 * I + 2) * 16 + (lane & 15)] + red[(4 * I + 3) * 16 + (lane & 15)];
 #pragma unroll
@@ -796,7 +802,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       const float t = __expf(-fabsf(gv));
       const float inv = __fdividef(1.f, 1.f + t);
       const float sg = gv >= 0.f ? inv : t * inv;
-      const float sp = fmaxf(gv, 0.f) + log1p_unit(t);
+      const float sp = fmaxf(gv, 0.f) + log1p_unit_warp(t);
       const float dgv = run * (-A) * sg;
       dgsm[i * D + c] = __float2bfloat16_rn(dgv);
       if (i < len) {
@@ -836,9 +842,9 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   }
 drain:
-  // every thread gets here (through a decision above or at the end of the
-  // work); the CTA agrees on whether any wait gave up
-  if (__syncthreads_or(!ok)) {
+  // `ok` is uniform here: every decision above sets it for the whole CTA
+  // before jumping, and no wait follows the last one
+  if (!ok) {
     // a bounded wait gave up (the status word says so): let the copies and the
     // MMA batch that may still be in flight land before the CTA releases its
     // shared memory and Tensor Memory
@@ -850,13 +856,15 @@ drain:
       if (phase > 0) umma::mbar_wait(mbar, (phase - 1) & 1, lim);
     }
     cp_async_wait_all();
+    umma::tc_fence_before();
+    __syncthreads();
   }
   // the stored boxes have read shared memory before the CTA ends (their
-  // global writes complete before the grid does)
+  // global writes complete before the grid does); on the normal path every
+  // Tensor Memory load completed before the gate epilogue's barriers
   if (tid == kStoreT) umma::bulk_wait_read();
-  umma::tc_fence_before();
-  __syncthreads();
   if (warp == 0) {
+    __syncwarp();  // thread 0 may have drained alone: the release is warp-collective
     umma::tc_fence_after();
     umma::tmem_dealloc(*tslot, 512);
   }

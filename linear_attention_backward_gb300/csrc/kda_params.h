@@ -99,11 +99,13 @@ constexpr size_t kPrepUnitBytes = kPrepSV + kPrepSVBytes;
 // the 64 rows x 128 channels of one chunk and head, row-major (256-byte rows)
 // in shared memory; rows past the tensor's end read as zero (and are not
 // written by a store).  Inputs q, k, g, v, dO; gradients dq, dk, dv, dg
-// (stored from shared memory for whole chunks).  A null tensor keeps an
-// empty map.
+// (stored from shared memory for whole chunks).  dO_sw maps dO with boxes of
+// 64 rows x 64 channels in the 128-byte swizzled layout (umma::sw128_off),
+// which the tensor cores read as it lands.  A null tensor keeps an empty map.
 struct TokenMaps {
   CUtensorMap q, k, g, v, dO;
   CUtensorMap dq, dk, dv, dg;
+  CUtensorMap dO_sw;
 };
 // kda_tmap.cu: encodes the five maps; false if the driver refuses one.
 bool encode_token_maps(const KdaParams &p, TokenMaps &m);
@@ -114,10 +116,13 @@ int prep_tc_status_take();
 
 // kda_scan_tc.cu: both state scans on tcgen05 from the prep buffer; roles
 // as in scan_dispatch.
-cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cudaStream_t st);
+// (the reverse role takes each chunk's dO through tm.dO_sw)
+cudaError_t scan_tc_launch(const KdaParams &p, const TokenMaps &tm, const void *prep, int nroles,
+                           cudaStream_t st);
 // the three phases of the context-parallel scans (p.cp_segs >= 3); p.role_base
 // and nroles as for scan_tc_launch
-cudaError_t scan_tc_cp_launch(KdaParams p, const void *prep, int nroles, cudaStream_t st);
+cudaError_t scan_tc_cp_launch(KdaParams p, const TokenMaps &tm, const void *prep, int nroles,
+                              cudaStream_t st);
 // order[r] = the sequence of rank r by length (longest first, ties by index)
 cudaError_t seq_order_launch(const int32_t *cu, int num_seqs, int32_t *order, cudaStream_t st);
 int scan_tc_status_take();

@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     Bblk[I * D + c] = g0[15] - g0[7];
     Bblk[I * D + c + 1] = g1[15] - g1[7];
   }
-  if (__syncthreads_or(!ok)) goto drain;
+  if (__syncthreads_or(!ok)) { ok = false; goto drain; }
   {
   if (tid < CHUNK) {  // row norms: block I's rows live in warps 2I, 2I + 1
     const int ib = tid >> 4, r = tid & 15;
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   cp_async_wait_all();  // v has landed
   umma::fence_async_smem();
   umma::tc_fence_before();
-  if (__syncthreads_or(!ok)) goto drain;
+  if (__syncthreads_or(!ok)) { ok = false; goto drain; }
   // ---- U0^T = v^T (INV diag(beta))^T ;  (Mqk W)^T = W^T Mqk^T ----
   if (tid == 0) {
     umma::tc_fence_after();
@@ -417,12 +417,16 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   }
   }
 drain:
-  // every thread gets here (through a decision above or at the end of the
-  // work); the CTA agrees on whether any wait gave up
+  // every thread gets here (through a decision above, which set `ok` for the
+  // whole CTA, or at the end of the work, after the last products' wait);
+  // the barrier both ends every thread's Tensor Memory loads before the
+  // release and lets the CTA agree on whether any wait gave up
+  umma::tc_fence_before();
   if (__syncthreads_or(!ok)) {
     // a bounded wait gave up (the status word says so): let the copies and the
     // MMA batch that may still be in flight land before the CTA releases its
-    // shared memory and Tensor Memory
+    // shared memory and Tensor Memory (thread 0, in warp 0, waits before the
+    // release below)
     if (tid == 0) {
       const uint32_t lim = poll_cap(p, umma::kPollDrain);
       umma::mbar_wait(rbar, 0, lim);
@@ -430,9 +434,8 @@ drain:
     }
     cp_async_wait_all();
   }
-  umma::tc_fence_before();
-  __syncthreads();
   if (warp == 0) {
+    __syncwarp();  // thread 0 may have drained alone: the release is warp-collective
     umma::tc_fence_after();
     umma::tmem_dealloc(*tslot, 256);
   }

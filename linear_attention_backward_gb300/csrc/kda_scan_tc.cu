@@ -25,7 +25,8 @@
 // into three regions with one mbarrier each; a region is refilled with the
 // next chunk's data as soon as its consumer (MMA1, the U epilogue or MMA2)
 // is done, behind an L2 prefetch two chunks ahead.  The reverse role's dO
-// rows come by cp.async with MMA2's region.
+// rows come with MMA2's region as two TMA boxes (64 tokens x 64 channels)
+// in the 128-byte swizzled layout, which MMA2 reads as they land.
 //
 // With few (sequence, head) chains the same kernel runs context-parallel
 // (see scan_tc_cp_launch below): chains over segments of a sequence, a third
@@ -44,21 +45,31 @@ constexpr uint32_t kInRevA = (uint32_t)kPrepU0;                // gT, W^T, kr
 constexpr uint32_t kQEHere = (uint32_t)kPrepU0;                // QE^T lands where U0^T would
 struct Smem {
   static constexpr size_t o_X = 0;                 // state [c][v] packed, 32 KB
-  static constexpr size_t o_IN = o_X + 32768;      // operand block, 48.5 KB
-  static constexpr size_t o_dO = o_IN + kInFwd;    // dO [i][v] packed (reverse role)
+  static constexpr size_t o_dO = o_X + 32768;      // dO [i][v], two 128-byte swizzled boxes
   static constexpr size_t o_U = o_dO + 16384;      // U^T [v][i] packed
-  static constexpr size_t o_bar = o_U + 16384;
+  static constexpr size_t o_IN = o_U + 16384;      // operand block, 48.5 KB
+  static constexpr size_t o_bar = o_IN + kInFwd;
   static constexpr size_t total = o_bar + 64;
   static_assert(total + 1024 <= 233472 / 2, "two CTAs per SM");
-  static_assert(o_IN % 16 == 0 && o_dO % 16 == 0, "bulk copy alignment");
+  static_assert(o_IN % 16 == 0, "bulk copy alignment");
+  static_assert(o_dO % 1024 == 0, "the swizzled boxes' atoms are 1024-byte aligned");
 };
+constexpr uint32_t kDOBox = 8192;  // one 64 x 64 swizzled dO box
 
 }  // namespace stc
 
-__global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, const char *prep) {
+__global__ void __launch_bounds__(NTHREADS, 2)
+    kda_scan_tc_kernel(KdaParams p, const __grid_constant__ TokenMaps tm, const char *prep) {
   using namespace stc;
   using SM = stc::Smem;
   extern __shared__ __align__(1024) char smem[];
+  // the swizzled dO boxes need 1024-byte aligned atoms; the dynamic window of
+  // a kernel without static shared memory is, and a launch where it were not
+  // records KDA_ERR_CUDA and does nothing rather than issue a misaligned copy
+  if ((smem_u32(smem) & 1023u) != 0u) {
+    if (threadIdx.x == 0) set_status(4);
+    return;
+  }
   const int H = p.H;
   const int nseq = p.cu ? p.num_seqs : p.B;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -235,23 +246,16 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
           umma::mbar_expect_tx(bars + 0, 16384u);
           umma::bulk_g2s(IN + kPrepKR, u + kPrepKR, 16384u, bars + 0);
         } else {
-          umma::mbar_expect_tx(bars + 1, kPrepKR + 16384u);
+          // gT | W^T, QE^T, and the chunk's dO rows as two swizzled boxes
+          // (channels 0-63, 64-127); rows past the tensor's end read as zero
+          const int t0 = (int)(tok_seq + (int64_t)chunk_of(it) * CHUNK);
+          umma::mbar_expect_tx(bars + 1, kPrepKR + 16384u + 2 * kDOBox);
           umma::bulk_g2s(IN, u, kPrepKR, bars + 1);
           umma::bulk_g2s(IN + kQEHere, u + kPrepQE, 16384u, bars + 1);
+          umma::tma_load_3d(dOs, &tm.dO_sw, 0, h, t0, bars + 1);
+          umma::tma_load_3d(dOs + kDOBox, &tm.dO_sw, 64, h, t0, bars + 1);
         }
       }
-    }
-    if (!fwd && sl == 1) {  // dO rows -> packed core tile [i][v]
-      const int j = chunk_of(it);
-      const int64_t t0 = tok_seq + (int64_t)j * CHUNK;
-      const int ln = min(CHUNK, L - j * CHUNK);
-      for (int e = tid; e < 64 * (D / 8); e += NTHREADS) {
-        const int i = e >> 4, c8 = (e & 15) * 8;
-        const bool ok = i < ln;
-        cp_async16(dOs + umma::core_off(i, c8, D), dOg + ((t0 + (ok ? i : 0)) * H + h) * D + c8,
-                   ok);
-      }
-      cp_async_commit();
     }
   };
   auto prefetch = [&](int it) {
@@ -358,9 +362,19 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
       for (int q = 0; q < 4; ++q) st16_bf(Us + umma::core_off(ch, 32 * hf + 8 * q, 64), t + 8 * q);
     }
     if (!fwd) {
-      ok = wait_bar(1) && ok;  // gT | W^T, QE^T
+      ok = wait_bar(1) && ok;  // gT | W^T, QE^T, dO
       eg = __expf(reinterpret_cast<const float *>(IN + kPrepGT)[ch]);
-      cp_async_wait_all();     // dO
+      // a sequence's partial last chunk: the boxes' rows past it hold the next
+      // sequence's dO; zero them (a row's 128 bytes stay within the row)
+      const int ln = L - chunk_of(it) * CHUNK;
+      if (ln < CHUNK) {
+        for (int e = tid; e < 2 * 64 * 8; e += NTHREADS) {
+          const int row = (e >> 3) & 63;
+          if (row >= ln)
+            *reinterpret_cast<uint4 *>(dOs + (e >> 9) * kDOBox + row * 128 + (e & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
     }
     umma::fence_async_smem();
     umma::tc_fence_before();
@@ -380,8 +394,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
           gemm(tbase + 64, opk(IN + kPrepKR, 64, 0, CP), false, b, false, 128, 4, false);
         } else {
           gemm(tbase + 64, opk(IN + kPrepW, 64, 0, CP), false, b, false, 128, 4, false);
-          gemm(tbase + 64, opk(IN + kQEHere, 64, 0, CP), false, opmn(dOs, D, 0, CP), true, 128, 4,
-               true);
+          // + QE^T dO: dO read MN-major from the swizzled boxes (N = 128 as
+          // two 64-wide slabs kDOBox apart, K = 16 tokens = two 8-row atoms)
+          gemm(tbase + 64, opk(IN + kQEHere, 64, 0, CP), false, opsw_mn(dOs, kDOBox), true, 128,
+               4, true);
         }
       }
       umma::mma_commit(bars + 3);
@@ -441,7 +457,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_scan_tc_kernel(KdaParams p, c
   }
 }
 
-cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cudaStream_t st) {
+cudaError_t scan_tc_launch(const KdaParams &p, const TokenMaps &tm, const void *prep, int nroles,
+                           cudaStream_t st) {
   auto kfn = kda_scan_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)stc::Smem::total);
@@ -450,7 +467,7 @@ cudaError_t scan_tc_launch(const KdaParams &p, const void *prep, int nroles, cud
   if (nunits == 0 || nroles == 0) return cudaSuccess;
   if (nroles < 1 || p.role_base + nroles > 2) return cudaErrorInvalidValue;
   kfn<<<(unsigned)(nunits * nroles), NTHREADS, stc::Smem::total, st>>>(
-      p, static_cast<const char *>(prep));
+      p, tm, static_cast<const char *>(prep));
   return cudaGetLastError();
 }
 
@@ -576,7 +593,8 @@ __global__ void __launch_bounds__(NTHREADS) kda_cp_combine_kernel(KdaParams p) {
   }
 }
 
-cudaError_t scan_tc_cp_launch(KdaParams p, const void *prep, int nroles, cudaStream_t st) {
+cudaError_t scan_tc_cp_launch(KdaParams p, const TokenMaps &tm, const void *prep, int nroles,
+                              cudaStream_t st) {
   const int P = p.cp_segs;
   if (P < 3 || p.cp_buf == nullptr) return cudaErrorInvalidValue;
   if (nroles < 1 || p.role_base < 0 || p.role_base + nroles > 2) return cudaErrorInvalidValue;
@@ -593,7 +611,7 @@ cudaError_t scan_tc_cp_launch(KdaParams p, const void *prep, int nroles, cudaStr
   // 1. local segment scans and the inner transfer matrices
   p.cp_phase = 1;
   kfn<<<(unsigned)(nunits * (roles * (P - 1) + (P - 2))), NTHREADS, stc::Smem::total, st>>>(
-      p, static_cast<const char *>(prep));
+      p, tm, static_cast<const char *>(prep));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // 2. the segment boundaries
@@ -605,7 +623,7 @@ cudaError_t scan_tc_cp_launch(KdaParams p, const void *prep, int nroles, cudaStr
   // 3. the remaining segments from their true boundaries
   p.cp_phase = 3;
   kfn<<<(unsigned)(nunits * roles * (P - 1)), NTHREADS, stc::Smem::total, st>>>(
-      p, static_cast<const char *>(prep));
+      p, tm, static_cast<const char *>(prep));
   return cudaGetLastError();
 }
 

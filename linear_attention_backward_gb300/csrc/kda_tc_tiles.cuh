@@ -68,6 +68,7 @@ __device__ __forceinline__ void ld16_bf(const void *src, float *v) {
 // ---- tcgen05 operands -------------------------------------------------------
 struct Op {
   uint32_t addr, lbo, sbo, step;
+  uint32_t swz = 0;  // descriptor layout type (0: none, 2: 128-byte swizzle)
 };
 // stored tile [R][C] read with K along its columns, from column k0
 __device__ __forceinline__ Op opk(const void *t, int C, int k0 = 0, uint32_t cs = CS) {
@@ -78,13 +79,19 @@ __device__ __forceinline__ Op opmn(const void *t, int C, int r0 = 0, uint32_t cs
   return Op{smem_u32(t) + (uint32_t)(r0 / 8) * (C / 8) * cs, (uint32_t)(C / 8) * cs, cs,
             2 * (uint32_t)(C / 8) * cs};
 }
+// a tile in the 128-byte swizzled layout (umma::sw128_off, 1024-byte
+// aligned), read MN-major: slabs of 64 M / N columns slab_bytes apart, K
+// down its rows (two 8-row atoms per K = 16 step)
+__device__ __forceinline__ Op opsw_mn(const void *t, uint32_t slab_bytes) {
+  return Op{smem_u32(t), slab_bytes, 1024u, 2048u, 2u};
+}
 // D (+)= A B^T over `ksteps` K = 16 steps, issued by one thread; a step
 // advances the descriptors' start-address field by step >> 4.
 __device__ __forceinline__ void gemm(uint32_t d, Op a, bool amn, Op b, bool bmn, int N, int ksteps,
                                      bool accumulate) {
   const uint32_t id = umma::idesc_bf16(128, N, amn, bmn);
-  uint64_t da = umma::smem_desc(a.addr, a.lbo, a.sbo);
-  uint64_t db = umma::smem_desc(b.addr, b.lbo, b.sbo);
+  uint64_t da = umma::smem_desc(a.addr, a.lbo, a.sbo) | ((uint64_t)a.swz << 61);
+  uint64_t db = umma::smem_desc(b.addr, b.lbo, b.sbo) | ((uint64_t)b.swz << 61);
   const uint64_t ia = a.step >> 4, ib = b.step >> 4;
   for (int s = 0; s < ksteps; ++s) {
     umma::mma_bf16(d, da, db, id, accumulate || s > 0);

@@ -26,16 +26,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// [ntok, H, 128] bf16, box = 64 tokens x 1 head x 128 channels
-bool encode(CUtensorMap *m, const void *base, int64_t ntok, int H) {
+// [ntok, H, 128] bf16, box = 64 tokens x 1 head x `width` channels; width
+// 128 without swizzling (row-major rows of 256 bytes), or 64 with 128-byte
+// swizzling (rows of 128 bytes, 16-byte chunks permuted by row % 8)
+bool encode(CUtensorMap *m, const void *base, int64_t ntok, int H, int width = 128,
+            bool swizzle = false) {
   auto fn = encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)ntok};
   const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};  // bytes, dims 1 and 2
-  const cuuint32_t box[3] = {128, 1, 64};
+  const cuuint32_t box[3] = {(cuuint32_t)width, 1, 64};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -50,7 +54,8 @@ bool encode_token_maps(const KdaParams &p, TokenMaps &m) {
   };
   return enc(&m.q, p.q) && enc(&m.k, p.k) && enc(&m.g, p.g) && enc(&m.v, p.v) &&
          enc(&m.dO, p.dO) && enc(&m.dq, p.dq) && enc(&m.dk, p.dk) && enc(&m.dv, p.dv) &&
-         enc(&m.dg, p.dg);
+         enc(&m.dg, p.dg) &&
+         (p.dO == nullptr || encode(&m.dO_sw, p.dO, ntok, p.H, 64, true));
 }
 
 }  // namespace kda

@@ -53,6 +53,29 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// ---- 128-byte swizzled layout (SWIZZLE_128B) --------------------------------
+// A tile is cut into slabs of 64 contiguous-index elements (128 bytes) and
+// each slab into atoms of 8 rows x 128 bytes (1024 bytes, 1024-byte aligned);
+// within an atom the 16-byte chunk j of row r sits at chunk j ^ (r % 8).  This
+// is the pattern a TMA copy with CU_TENSOR_MAP_SWIZZLE_128B writes (box rows
+// of 128 bytes, destination 1024-byte aligned) and the tensor core reads with
+// layout type 2.  Element (row, col) -- col the contiguous index -- of a tile
+// whose 64-column slabs lie slab_bytes apart sits at sw128_off(row, col,
+// slab_bytes).  Read K-major (col = K): each MMA's K = 16 step moves the
+// descriptor start 32 bytes along the row (four steps per slab, then the
+// next slab); SBO = 1024 (8-row groups), LBO unused.  Read MN-major
+// (col = M or N, row = K): each K = 16 step moves the start 2048 bytes (two
+// 8-row groups); SBO = 1024, LBO = slab_bytes (the next 64 M / N).
+__host__ __device__ __forceinline__ uint32_t sw128_off(int row, int col, uint32_t slab_bytes) {
+  return (uint32_t)(col >> 6) * slab_bytes + (uint32_t)((row >> 3) << 10) +
+         (uint32_t)((row & 7) << 7) + (uint32_t)((((col & 63) >> 3) ^ (row & 7)) << 4) +
+         (uint32_t)((col & 7) << 1);
+}
+// descriptor of a 128-byte swizzled operand (layout type 2 in bits 61-63)
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(saddr, lbo, sbo) | ((uint64_t)2 << 61);
+}
+
 // ---- instruction descriptor, kind::f16 with bf16 inputs and fp32 accumulate
 // bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format
 // (1 = bf16), 15 A major (0 = K, 1 = MN), 16 B major, 17-22 N >> 3,

@@ -133,8 +133,10 @@ def test_bwd_pointer_checks(L):
     assert L.kda_fwd_states(ctypes.byref(s), *a, None, ws_ok, None) == 3
     assert L.kda_fwd_states(ctypes.byref(s), *a, fake, ctypes.c_size_t(ws_ok.value - 1),
                             None) == 3
-    # the selftest's layouts are 0 (packed) and 1 (padded) only
-    assert L.kda_selftest_umma(fake, fake, fake, 64, 64, 0, 0, 2, None) == 1
+    # the selftest's layouts are 0 (packed), 1 (padded) and 2 (128-byte
+    # swizzled, K in slabs of 64) only
+    assert L.kda_selftest_umma(fake, fake, fake, 64, 64, 0, 0, 3, None) == 1
+    assert L.kda_selftest_umma(fake, fake, fake, 64, 32, 0, 0, 2, None) == 1
 
 
 def test_host_cu_seqlens_check(L):

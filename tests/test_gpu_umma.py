@@ -1,7 +1,8 @@
 """Device self-test of the fifth-generation tensor-core building blocks
 (tcgen05 MMA from shared-memory descriptors into Tensor Memory, read back
 with tcgen05.ld): D = A B^T against a plain fp32 product, for K-major and
-MN-major operand tiles."""
+MN-major operand tiles in the packed and padded core-matrix layouts and the
+128-byte swizzled layout."""
 import ctypes
 
 import pytest
@@ -16,8 +17,12 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("N", [32, 64, 128])
 @pytest.mark.parametrize("K", [16, 64, 128])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
-@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("layout", [0, 1, 2])
 def test_umma_tile(N, K, a_mn, b_mn, layout):
+    # layout 2, the 128-byte swizzled one, takes K in slabs of 64 and (read
+    # MN-major) N in slabs of 64
+    if layout == 2 and (K % 64 or (b_mn and N < 64)):
+        pytest.skip("not a 128-byte swizzled shape")
     __graft_entry__.build()
     L = kda.lib()
     L.kda_selftest_umma.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p]
