@@ -63,11 +63,11 @@ def launches_per_step(shape, cu, forward=False):
 # kernel sources it was taken from; a changed kernel reports null until it
 # is measured again.
 NCU_TRAFFIC = {
-    # ncu --set full on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read
-    # 841.2 MB + write 248.4 MB, scaled by 4 to the main workload's 16384
-    # chunk-heads (the kernel's traffic is proportional to the chunk-heads)
-    "kda_grads_tc_kernel": {"sha": "7e16f7b7974e15f1", "workload": "main_bf16",
-                            "bytes_per_launch": 4358414336},
+    # ncu on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read 841.7 MB +
+    # write 244.8 MB (profiles/traffic_main_b1_bf16.md), scaled by 4 to the main
+    # workload's 16384 chunk-heads (the kernel's traffic is proportional to them)
+    "kda_grads_tc_kernel": {"sha": "cf4ea4907ec74cd2", "workload": "main_bf16",
+                            "bytes_per_launch": 4345711616},
 }
 
 KERNEL_SOURCES = {

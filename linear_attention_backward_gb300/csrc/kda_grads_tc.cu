@@ -21,8 +21,11 @@
 //                     + dS[c][d] (MN)  x kr[i][c] (K)                   N = 64
 //       dkr^T[c][i]   = dS[c][d] (K)            x U[i][d] (K)           N = 64
 //   P5  dvcorr^T[d][i]= dU^T[d][i'] (K)         x INV[i'][i] (MN)       N = 64
-//   P6  [dvcorr; dO] U^T = [-dAkk | dMqk / s] (rows: dvcorr, then dO)   N = 64
-//   P8  S [dvcorr; dO]^T = [dvcorr S^T | dO S^T]^T                     N = 128
+//   P6  [dO; dvcorr] U^T = [dMqk / s | -dAkk] (rows: dO, then dvcorr)   N = 64
+//   P8  S [dO; dvcorr]^T = [dO S^T | dvcorr S^T]^T                     N = 128
+// dO arrives by TMA as two 64-channel boxes in the 128-byte swizzled layout
+// and is read as it lands: MN-major by P3a, and K-major, stacked over the
+// dvcorr rows the R3 epilogue writes in the same layout, by P6 and P8.
 //   P9  intra-chunk terms with hi + lo operands: per key block J the dMqk and
 //       dA sides in one product (N = 128 - 32 J), per query block X the
 //       P9c sums (N = 16 (X + 1))
@@ -73,15 +76,19 @@ struct Smem {
   // R_C: kd^T, kr^T  ->  Xr^T, dU^T  ->  lo tiles QMl, KMl (intra)  ->  dg columns (K1)
   static constexpr size_t o_C = o_B + sz_B;
   static constexpr size_t sz_C = 2 * T64x128;
-  // R_D: dS (128 x 128), then dO (64 x 128)  ->  dMqk, dA | dvcorr ; dvcorr | dO is the
-  // stacked 128-row operand of P6 / P8; KPl (intra) reuses the dvcorr slot
+  // R_D: the stacked 128-row operand [dO; dvcorr] of P3a / P6 / P8 in the
+  // 128-byte swizzled layout, two 64-column slabs kStk apart (slab 0: dO
+  // [0, 8K), dvcorr [8K, 16K); slab 1: dO [40K, 48K), dvcorr [48K, 56K)),
+  // and dS (packed 128 x 128) in [8K, 40K) until R3 has consumed it (the
+  // dvcorr rows of slab 0 are written over it after) -> dMqk | dA (interleaved
+  // by 16-row blocks, 128 x 64) in [0, 18K) and KPl (intra) after it
   static constexpr size_t o_D = o_C + sz_C;
-  static constexpr size_t o_dS = o_D;
-  static constexpr size_t o_dMqk = o_D;  // dMqk | dA interleaved by 16-row blocks, 128 x 64
-  static constexpr size_t o_dA = o_D + T64x64;
-  static constexpr size_t o_dvc = o_D + T64x128;
-  static constexpr size_t o_dO = o_D + T128x128;
-  static constexpr size_t sz_D = T128x128 + T64x128;
+  static constexpr uint32_t kStk = 40960;
+  static constexpr size_t o_stk = o_D;
+  static constexpr size_t o_dS = o_D + 8192;
+  static constexpr size_t o_dMqk = o_D;
+  static constexpr size_t o_KPl = o_D + T128x64;
+  static constexpr size_t sz_D = kStk + 16384;
   static constexpr size_t total = o_D + sz_D;
   static_assert(sz_A >= 3 * 64 * D * 2, "raw tiles must fit R_A");
   static_assert(o_Gbf + 8192 <= o_A + sz_A, "prep tiles must fit R_A");
@@ -89,7 +96,9 @@ struct Smem {
                     kPrepG == kPrepINVb + 8192,
                 "prep tiles are copied as one block");
   static_assert(T128x128 + T128x64 <= sz_B, "S + U must fit R_B");
-  static_assert(2 * T64x128 == T128x128, "dvcorr | dO stacking");
+  static_assert(o_D % 1024 == 0 && kStk % 1024 == 0, "swizzled atoms are 1024-byte aligned");
+  static_assert(o_dS + 32768 <= o_stk + kStk, "dS ends where slab 1 begins");
+  static_assert(o_KPl + T64x128 <= o_stk + kStk, "KPl stays clear of slab 1");
   static_assert(total <= 232448, "shared memory budget");
   static_assert(16 * NT * 4 <= sz_C, "K1 row buffer must fit R_C");
 };
@@ -253,8 +262,8 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   char *St = smem + SM::o_S, *Ut = smem + SM::o_U;
   char *KDt = smem + SM::o_C, *KRt = KDt + T64x128;
   char *XrT = KDt, *dUT = KRt, *QMl = KDt, *KMl = KRt;
-  char *dSt = smem + SM::o_dS, *dMA = smem + SM::o_dMqk,
-       *dvc = smem + SM::o_dvc, *dOt = smem + SM::o_dO, *KPl = dvc;
+  char *dSt = smem + SM::o_dS, *dMA = smem + SM::o_dMqk, *stk = smem + SM::o_stk,
+       *KPl = smem + SM::o_KPl;
   const float scale = p.scale;
   const size_t DD = (size_t)D * D;
   const bf16 *Sg = reinterpret_cast<const bf16 *>(states) + ((size_t)slot * H + h) * DD;
@@ -297,10 +306,13 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       umma::bulk_g2s(sv.em, unit + kPrepSV, (uint32_t)kPrepSVBytes, rbar);  // factors, norms
     }
     const uint32_t bytes = 16384u + (p.states_packed ? 32768u : 0u) +
-                           (p.dstates_packed ? 32768u : 0u) + 16384u;
+                           (p.dstates_packed ? 32768u : 0u) + 16384u + 16384u;
     umma::mbar_expect_tx(lbar, bytes);
     if (!starve) {
       umma::tma_load_3d(Ut, &tm.v, 0, h, (int)tok0, lbar);
+      // dO: two swizzled 64-channel boxes, the rows of the stacked operand
+      umma::tma_load_3d(stk, &tm.dO_sw, 0, h, (int)tok0, lbar);
+      umma::tma_load_3d(stk + SM::kStk, &tm.dO_sw, 64, h, (int)tok0, lbar);
       if (p.states_packed) umma::bulk_g2s(St, Sg, 32768u, lbar);
       if (p.dstates_packed) umma::bulk_g2s(dSt, dSg, 32768u, lbar);
       umma::bulk_g2s(KRt, unit + kPrepKR, 16384u, lbar);
@@ -308,13 +320,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   }
   if (warp == 0) umma::tmem_alloc(tslot, 512);
   __syncthreads();
-  // ---- dO (and row-major states) by cp.async ----
-  for (int e = tid; e < 64 * (D / 8); e += NT) {
-    const int i = e >> 4, c8 = (e & 15) * 8;
-    const bool ok = i < len;
-    cp_async16(dOt + pcore_off(i, c8, D),
-               reinterpret_cast<const bf16 *>(p.dO) + ((tok0 + (ok ? i : 0)) * H + h) * D + c8, ok);
-  }
+  // ---- row-major states (the per-band scans' or a caller's) by cp.async ----
   if (!p.states_packed) {  // row-major states (caller-provided) -> packed tile
     for (int e = tid; e < D * (D / 8); e += NT) {
       const int r = e >> 4, c8 = (e & 15) * 8;
@@ -367,8 +373,18 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   // (the pair matrices and inverses formed by the prep kernel -- Mqk, INV,
   // INVb, G, packed 64 x 64 -- come into R_A over the raw rows from inside)
   prep_tc(p, h, len, Qr, Kr, Gr, sv, E, KDt, q2, k2, g2, unit + kPrepMqk, Mqk, pbar, gsc);
-  cp_async_wait_all();                 // dO, v (and row-major S)
-  ok = umma::mbar_wait(lbar, 0, lim_ld) && ok;  // S, dS, kr^T
+  cp_async_wait_all();                 // row-major S / dS, if any
+  ok = umma::mbar_wait(lbar, 0, lim_ld) && ok;  // v, dO, S, dS, kr^T
+  if (len < CHUNK) {
+    // a sequence's partial last chunk: the dO boxes' rows past it hold the
+    // next sequence's rows; zero them (a row's 128 bytes stay within the row)
+    for (int e = tid; e < 2 * 64 * 8; e += NT) {
+      const int row = (e >> 3) & 63;
+      if (row >= len)
+        *reinterpret_cast<uint4 *>(stk + (e >> 9) * SM::kStk + row * 128 + (e & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   umma::fence_async_smem();
   if (__syncthreads_or(!ok)) { ok = false; goto drain; }
 
@@ -396,7 +412,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   if (tid == 0) {
     umma::tc_fence_after();
     gemm(tbase + 64, opk(XrT, 64), false, opk(INVb, 64, 0, CP), false, 64, 4, false);
-    gemm(tbase + 128, opmn(dOt, D), true, opmn(Mqk, 64, 0, CP), true, 64, 4, false);
+    gemm(tbase + 128, opsw_mn(stk, SM::kStk), true, opmn(Mqk, 64, 0, CP), true, 64, 4, false);
     gemm(tbase + 128, opmn(dSt, D, 0, CP), true, opmn(KRt, 64, 0, CP), true, 64, D / 16, true);
     umma::mma_commit(mbar);
   }
@@ -446,7 +462,9 @@ __global__ void __launch_bounds__(gtc::NT, 1)
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int i = 16 * I + r;
-      *pel(dvc, i, c, D) = __float2bfloat16_rn(acc[r]);
+      // dvcorr row i = row 64 + i of the stacked swizzled operand
+      *reinterpret_cast<bf16 *>(stk + umma::sw128_off(64 + i, c, SM::kStk)) =
+          __float2bfloat16_rn(acc[r]);
       dvs[i * D + c] = __float2bfloat16_rn(sv.beta[i] * acc[r]);
       pr[r] = acc[r] * xr[r];
     }
@@ -481,20 +499,21 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     }
   }
 
-  // ---- P6: [dvcorr; dO] U^T  and  P8: S [dvcorr; dO]^T ----
+  // ---- P6: [dO; dvcorr] U^T  and  P8: S [dO; dvcorr]^T ----
   if (tid == 0) {
     umma::tc_fence_after();
-    gemm(tbase + 64, opk(dvc, D), false, opmn(Ut, 64), true, 64, D / 16, false);
-    gemm(tbase + 256, opk(St, D, 0, CP), false, opk(dvc, D), false, 128, D / 16, false);
+    gemm(tbase + 64, opsw_k(stk, SM::kStk), false, opmn(Ut, 64), true, 64, D / 16, false);
+    gemm(tbase + 256, opk(St, D, 0, CP), false, opsw_k(stk, SM::kStk), false, 128, D / 16,
+         false);
     umma::mma_commit(mbar);
   }
   mma_wait();
   {
-    // lanes 0..63: -dAkk rows (dvcorr U^T), lanes 64..127: dMqk / scale rows
+    // lanes 0..63: dMqk / scale rows (dO U^T), lanes 64..127: -dAkk rows
     float v16[16];
     tld16(tbase, 64, v16);  // columns j in [16 I, 16 I + 16)
-    if (c < 64) {
-      const int i = c;
+    if (c >= 64) {
+      const int i = c - 64;
       float db2 = 0.f;
       float o8[8];
 #pragma unroll
@@ -512,7 +531,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       }
       red2[I * 64 + i] = db2;
     } else {
-      const int i = c - 64;
+      const int i = c;
       float o8[8];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -601,13 +620,13 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   bf16 *dks = dqs + 64 * D;
   float dgc[16];
   {
-    // dO S^T (rows 64..127 of the stacked operand) and key blocks J <= I
+    // dO S^T (rows 0..63 of the stacked operand) and key blocks J <= I
     // (F_{I,J} = 0 above the diagonal blocks; rows 16 I .. of block J's
     // accumulator), TMEM loads in two batches
     float bq[16], in[16];
     {
       float a0[16], a1[16];
-      tld16_nw(tbase, 320, bq);
+      tld16_nw(tbase, 256, bq);
       // (tld16 adds 16 I: key block J's dMqk side of block I is at col_p9ab(J) + 32 (I - J))
       tld16_nw(tbase, col_p9ab(0) + 16 * I, a0);
       if (I >= 1) tld16_nw(tbase, col_p9ab(1) - 32 + 16 * I, a1);
@@ -649,7 +668,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     float bk[16];  // dvcorr S^T, and the key blocks as for dq
     {
       float a0[16], a1[16];
-      tld16_nw(tbase, 256, bk);
+      tld16_nw(tbase, 320, bk);
       tld16_nw(tbase, col_p9ab(0) + 16 + 16 * I, a0);  // the dA side: 16 further
       if (I >= 1) tld16_nw(tbase, col_p9ab(1) - 16 + 16 * I, a1);
       umma::tmem_ld_wait();

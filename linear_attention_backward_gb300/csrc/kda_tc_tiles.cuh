@@ -68,7 +68,9 @@ __device__ __forceinline__ void ld16_bf(const void *src, float *v) {
 // ---- tcgen05 operands -------------------------------------------------------
 struct Op {
   uint32_t addr, lbo, sbo, step;
-  uint32_t swz = 0;  // descriptor layout type (0: none, 2: 128-byte swizzle)
+  uint32_t swz = 0;   // descriptor layout type (0: none, 2: 128-byte swizzle)
+  uint32_t slab = 0;  // per > 0: K = 16 steps advance by `step` within a slab,
+  uint32_t per = 0;   // `per` steps per slab, slabs `slab` bytes apart
 };
 // stored tile [R][C] read with K along its columns, from column k0
 __device__ __forceinline__ Op opk(const void *t, int C, int k0 = 0, uint32_t cs = CS) {
@@ -85,19 +87,25 @@ __device__ __forceinline__ Op opmn(const void *t, int C, int r0 = 0, uint32_t cs
 __device__ __forceinline__ Op opsw_mn(const void *t, uint32_t slab_bytes) {
   return Op{smem_u32(t), slab_bytes, 1024u, 2048u, 2u};
 }
+// the same layout read K-major: K along the 128-byte rows (32 bytes per
+// K = 16 step, four steps per slab), slabs of 64 K columns slab_bytes apart,
+// M / N down the rows
+__device__ __forceinline__ Op opsw_k(const void *t, uint32_t slab_bytes) {
+  return Op{smem_u32(t), 16u, 1024u, 32u, 2u, slab_bytes, 4u};
+}
 // D (+)= A B^T over `ksteps` K = 16 steps, issued by one thread; a step
 // advances the descriptors' start-address field by step >> 4.
 __device__ __forceinline__ void gemm(uint32_t d, Op a, bool amn, Op b, bool bmn, int N, int ksteps,
                                      bool accumulate) {
   const uint32_t id = umma::idesc_bf16(128, N, amn, bmn);
-  uint64_t da = umma::smem_desc(a.addr, a.lbo, a.sbo) | ((uint64_t)a.swz << 61);
-  uint64_t db = umma::smem_desc(b.addr, b.lbo, b.sbo) | ((uint64_t)b.swz << 61);
-  const uint64_t ia = a.step >> 4, ib = b.step >> 4;
-  for (int s = 0; s < ksteps; ++s) {
-    umma::mma_bf16(d, da, db, id, accumulate || s > 0);
-    da += ia;
-    db += ib;
-  }
+  const uint64_t da = umma::smem_desc(a.addr, a.lbo, a.sbo) | ((uint64_t)a.swz << 61);
+  const uint64_t db = umma::smem_desc(b.addr, b.lbo, b.sbo) | ((uint64_t)b.swz << 61);
+  auto at = [](const Op &o, int s) {  // byte offset of K step s
+    return o.per ? (uint32_t)(s / (int)o.per) * o.slab + (uint32_t)(s % (int)o.per) * o.step
+                 : (uint32_t)s * o.step;
+  };
+  for (int s = 0; s < ksteps; ++s)
+    umma::mma_bf16(d, da + (at(a, s) >> 4), db + (at(b, s) >> 4), id, accumulate || s > 0);
 }
 
 // Precomputed form of an operand: its descriptor, and the descriptor step
