@@ -19,6 +19,16 @@
  * reverse scan of the per-chunk state gradient dS, grid (N, H, VSplit)).
  * Chunk size is 64 tokens.
  *
+ * Head sizes.  bf16 with K = V = 128 runs the fifth-generation tensor-core
+ * kernels.  bf16 with K = V = 64 runs the same kernels on copies of the
+ * inputs zero-padded to 128 channels (exact: a padded channel has q^ = k^ = 0
+ * and zero value columns, so its state rows and columns stay zero and every
+ * gradient term touching it vanishes; the read-out scale stays 64^-1/2); the
+ * padded copies live in the workspace, and the environment variable
+ * KDA_PAD64=0 selects the mma.sync kernels for such shapes instead.  fp32
+ * (K = V = 64) runs mma.sync / fp32 SIMT kernels, whose products keep fp32
+ * precision (the fp32 tolerance of 1e-4 rules out tf32 operands).
+ *
  * Conventions for every entry point.
  *  - Tensors are DEVICE pointers, contiguous, token-major ("native [T,H,D]"
  *    layout of the kernel-B guide, Part 2, B3 optimisation 8):
@@ -113,8 +123,10 @@ int64_t kda_num_chunk_slots(const kda_shape *shape);
  * ([slots, H] and [slots, H, K] fp32) and, for bf16
  * with K = V = 128, the per-chunk operand blocks of the tensor-core scans
  * (107008 bytes per slot and head) and, where kda_scan_segments() > 0, the
- * segment boundary tiles of the context-parallel scans.  Returns 0 on a bad
- * shape. */
+ * segment boundary tiles of the context-parallel scans.  For bf16 with
+ * K = V = 64 it is the workspace of the 128-channel shape plus the padded
+ * copies of the inputs, gradients, h0 / dh_T / dh0, the gate bias and given
+ * states.  Returns 0 on a bad shape. */
 size_t kda_workspace_bytes(const kda_shape *shape);
 /* Byte offset inside the workspace of the per-chunk state gradients
  * dS_{n+1} (the adjoint of the state at the END of chunk n), [slots, H]
@@ -122,7 +134,9 @@ size_t kda_workspace_bytes(const kda_shape *shape);
  * is in packed core-matrix order -- element (k, v) at element offset
  * ((k / 8) * (V / 8) + v / 8) * 64 + (k % 8) * 8 + v % 8 -- and so are the
  * states kda_bwd recomputes at the start of the workspace; otherwise tiles
- * are row-major.  Exposed so that tests can check the scans on their own. */
+ * are row-major.  For bf16 with K = V = 64 (padded path) the tiles are the
+ * padded 128 x 128 ones, in packed order, with the values in the 64 x 64
+ * corner.  Exposed so that tests can check the scans on their own. */
 size_t kda_workspace_dstates_offset(const kda_shape *shape);
 /* Segments per sequence of the context-parallel state scans that kda_bwd and
  * kda_fwd run for this shape; 0 means one scan chain per (sequence, head,
@@ -165,7 +179,8 @@ int kda_scan_segments(const kda_shape *shape);
  * bf16 with K = V = 128 runs the chunk-parallel prep (which also forms the
  * read-out operands and so needs q) and the forward tcgen05 state scan,
  * context-parallel where kda_scan_segments() > 0; q is then required.  Other
- * shapes run the per-band scan and ignore q. */
+ * shapes run the per-band scan and ignore q (bf16 K = V = 64 included: its
+ * row-major 64 x 64 states are packed into the padded layout by kda_bwd). */
 kda_status kda_fwd_states(const kda_shape *shape, const void *q, const void *k,
                           const void *v, const void *g, const void *beta,
                           const float *A_log, const float *dt_bias, const float *h0,
@@ -177,7 +192,7 @@ kda_status kda_fwd_states(const kda_shape *shape, const void *q, const void *k,
  * recurrence whose backward kda_bwd computes), on the same per-chunk operands
  * as kda_bwd: with U = U0 - W S_n the corrected values of chunk n and
  * QE = scale (qd - Mqk W),  o = QE S_n + (scale Mqk) U0  row by row.
- * bf16 with K = V = 128 only (KDA_ERR_UNSUPPORTED otherwise).
+ * bf16 only (K = V = 64 on zero-padded copies); KDA_ERR_UNSUPPORTED for fp32.
  *   o      : OUT [B, T, H, V] bf16, overwritten (rows of every sequence).
  *   h0     : nullable (zero initial state), fp32 [N, H, K, V].
  *   hT     : nullable OUT fp32 [N, H, K, V]: the final state of each sequence.

@@ -180,7 +180,7 @@ def fwd_states(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None,
 
 def fwd(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None, l2_eps=None,
         o=None, hT=None, want_hT=False, workspace=None, dt_bias=None):
-    """Forward read-out ``o`` [B, T, H, V] (bf16, K = V = 128) and, if asked,
+    """Forward read-out ``o`` [B, T, H, V] (bf16, K = V = 128 or 64) and, if asked,
     the final states ``hT`` [N, H, K, V] fp32: ``(o, hT)`` or ``o``.
     ``dt_bias`` (optional fp32 [H, K]) is the gate's per-channel bias."""
     shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2_eps=l2_eps)

@@ -185,6 +185,61 @@ cudaError_t forward_states_tc(kda::KdaParams &p, const kda_shape *shape, char *w
   return e;
 }
 
+// ---- bf16 K = V = 64 on the 128-channel tensor-core path -------------------
+// The shape's channels are zero-padded to 128 (kda_pad.cu explains why the
+// result is exact); the padded copies live behind the padded shape's own
+// workspace.  KDA_PAD64=0 runs such shapes on the mma.sync kernels instead,
+// for comparisons.
+bool pad64_shape(const kda_shape *s) {
+  return s->dtype == KDA_BF16 && s->K == 64 && s->V == 64;
+}
+bool pad64_path(const kda_shape *s) {
+  if (!pad64_shape(s)) return false;
+  const char *e = getenv("KDA_PAD64");
+  return e == nullptr || e[0] != '0';
+}
+kda_shape padded_shape(const kda_shape *s) {
+  kda_shape p = *s;
+  p.K = p.V = 128;
+  p.scale = s->scale > 0.f ? s->scale : 0.125f;  // the 64-channel problem's 64^-1/2
+  return p;
+}
+// byte offsets of the padded copies: the padded shape's workspace [0, inner),
+// then q, k, v, g, dO and dq, dk, dv, dg ([B, T, H, 128] bf16), h0, dh_T,
+// dh0 ([N, H, 128, 128] fp32), dt_bias, ddt_bias ([H, 128] fp32) and given
+// states ([slots, H, 128, 128] bf16, packed)
+struct Pad64 {
+  size_t inner, q, k, v, g, dO, dq, dk, dv, dg, h0, dhT, dh0, dt, ddt, states, total;
+};
+Pad64 pad64_layout(const kda_shape *s) {
+  const kda_shape ps = padded_shape(s);
+  Pad64 L;
+  size_t o = round_up(cp_offset(&ps) + cp_bytes(&ps));
+  L.inner = o;
+  const size_t tok = round_up((size_t)s->B * s->T * s->H * 128 * 2);
+  size_t *toks[] = {&L.q, &L.k, &L.v, &L.g, &L.dO, &L.dq, &L.dk, &L.dv, &L.dg};
+  for (size_t *t : toks) {
+    *t = o;
+    o += tok;
+  }
+  const size_t st = round_up((size_t)num_seqs_of(s) * s->H * 128 * 128 * 4);
+  L.h0 = o;
+  o += st;
+  L.dhT = o;
+  o += st;
+  L.dh0 = o;
+  o += st;
+  const size_t bias = round_up((size_t)s->H * 128 * 4);
+  L.dt = o;
+  o += bias;
+  L.ddt = o;
+  o += bias;
+  L.states = o;
+  o += round_up((size_t)slots_of(s) * s->H * 128 * 128 * 2);
+  L.total = o;
+  return L;
+}
+
 kda_status check_ws(const kda_shape *shape, const void *ws, size_t ws_bytes) {
   const size_t need = kda_workspace_bytes(shape);
   if (need > 0 && (ws == nullptr || ws_bytes < need)) return KDA_ERR_WORKSPACE;
@@ -220,16 +275,25 @@ int64_t kda_num_chunk_slots(const kda_shape *shape) {
 
 size_t kda_workspace_dstates_offset(const kda_shape *shape) {
   if (check_shape(shape) != KDA_OK) return 0;
+  if (pad64_path(shape)) {
+    const kda_shape ps = padded_shape(shape);
+    return states_bytes(&ps);
+  }
   return states_bytes(shape);
 }
 
 int kda_scan_segments(const kda_shape *shape) {
   if (check_shape(shape) != KDA_OK) return 0;
+  if (pad64_path(shape)) {
+    const kda_shape ps = padded_shape(shape);
+    return cp_segments_used(&ps);
+  }
   return cp_segments_used(shape);
 }
 
 size_t kda_workspace_bytes(const kda_shape *shape) {
   if (check_shape(shape) != KDA_OK) return 0;
+  if (pad64_shape(shape)) return pad64_layout(shape).total;  // also covers the mma.sync path
   return cp_offset(shape) + cp_bytes(shape);
 }
 
@@ -292,7 +356,7 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
                    kda_stream_t stream) {
   kda_status st = check_shape(shape);
   if (st != KDA_OK) return st;
-  if (!tc_state_path(shape)) return KDA_ERR_UNSUPPORTED;
+  if (!tc_state_path(shape) && !pad64_path(shape)) return KDA_ERR_UNSUPPORTED;
   const bool tokens = (int64_t)shape->B * shape->T > 0;
   if (!A_log) return KDA_ERR_INVALID_ARG;
   if (tokens && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
@@ -301,6 +365,33 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
     if (ptr && !aligned16(ptr)) return KDA_ERR_INVALID_ARG;
   st = check_ws(shape, ws, ws_bytes);
   if (st != KDA_OK) return st;
+  if (pad64_path(shape)) {
+    // the 128-channel forward on padded copies, then o and hT cut back
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const kda_shape ps = padded_shape(shape);
+    const Pad64 L = pad64_layout(shape);
+    char *w = static_cast<char *>(ws);
+    const int64_t rows = (int64_t)shape->B * shape->T * shape->H;
+    const int64_t nst = (int64_t)num_seqs_of(shape) * shape->H;
+    cudaError_t e = cudaSuccess;
+    const void *src[] = {q, k, v, g};
+    const size_t dst[] = {L.q, L.k, L.v, L.g};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      if (src[i]) e = kda::pad_rows_launch(src[i], w + dst[i], rows, i == 3 ? -30.f : 0.f, cs);
+    float *h0p = h0 ? reinterpret_cast<float *>(w + L.h0) : nullptr;
+    float *dtp = dt_bias ? reinterpret_cast<float *>(w + L.dt) : nullptr;
+    float *hTp = hT ? reinterpret_cast<float *>(w + L.dh0) : nullptr;
+    if (e == cudaSuccess && h0) e = kda::pad_tiles_f32_launch(h0, h0p, nst, 64, 64, 128, 128, false, cs);
+    if (e == cudaSuccess && dt_bias)
+      e = kda::pad_tiles_f32_launch(dt_bias, dtp, shape->H, 1, 64, 1, 128, false, cs);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    st = kda_fwd(&ps, w + L.q, w + L.k, w + L.v, w + L.g, beta, A_log, dtp, h0p, w + L.dq, hTp,
+                 w, L.inner, stream);
+    if (st != KDA_OK) return st;
+    e = kda::unpad_rows_launch(w + L.dq, o, rows, cs);
+    if (e == cudaSuccess && hT) e = kda::pad_tiles_f32_launch(hTp, hT, nst, 64, 64, 128, 128, true, cs);
+    return from_cuda(e);
+  }
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   char *w = static_cast<char *>(ws);
@@ -354,6 +445,46 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
     if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
   st = check_ws(shape, ws, ws_bytes);
   if (st != KDA_OK) return st;
+  if (pad64_path(shape)) {
+    // the 128-channel backward on padded copies, then the gradients cut back
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const kda_shape ps = padded_shape(shape);
+    const Pad64 L = pad64_layout(shape);
+    char *w = static_cast<char *>(ws);
+    const int64_t rows = (int64_t)shape->B * shape->T * shape->H;
+    const int64_t nst = (int64_t)num_seqs_of(shape) * shape->H;
+    cudaError_t e = cudaSuccess;
+    const void *src[] = {q, k, v, g, dO};
+    const size_t dst[] = {L.q, L.k, L.v, L.g, L.dO};
+    for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+      if (src[i]) e = kda::pad_rows_launch(src[i], w + dst[i], rows, i == 3 ? -30.f : 0.f, cs);
+    float *h0p = h0 ? reinterpret_cast<float *>(w + L.h0) : nullptr;
+    float *dhTp = dh_T ? reinterpret_cast<float *>(w + L.dhT) : nullptr;
+    float *dh0p = dh0 ? reinterpret_cast<float *>(w + L.dh0) : nullptr;
+    float *dtp = dt_bias ? reinterpret_cast<float *>(w + L.dt) : nullptr;
+    float *ddtp = ddt_bias ? reinterpret_cast<float *>(w + L.ddt) : nullptr;
+    void *stp = states ? w + L.states : nullptr;
+    if (e == cudaSuccess && h0) e = kda::pad_tiles_f32_launch(h0, h0p, nst, 64, 64, 128, 128, false, cs);
+    if (e == cudaSuccess && dh_T)
+      e = kda::pad_tiles_f32_launch(dh_T, dhTp, nst, 64, 64, 128, 128, false, cs);
+    if (e == cudaSuccess && dt_bias)
+      e = kda::pad_tiles_f32_launch(dt_bias, dtp, shape->H, 1, 64, 1, 128, false, cs);
+    if (e == cudaSuccess && states)
+      e = kda::pack_states64_launch(states, stp, slots_of(shape) * shape->H, cs);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    st = kda_bwd_timed(&ps, w + L.q, w + L.k, w + L.v, w + L.g, beta, A_log, dtp, h0p, w + L.dO,
+                       dhTp, w + L.dq, w + L.dk, w + L.dv, w + L.dg, dbeta, dA_log, ddtp, dh0p, stp,
+                       w, L.inner, stream, events);
+    if (st != KDA_OK) return st;
+    void *outs[] = {dq, dk, dv, dg};
+    const size_t from[] = {L.dq, L.dk, L.dv, L.dg};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      if (outs[i]) e = kda::unpad_rows_launch(w + from[i], outs[i], rows, cs);
+    if (e == cudaSuccess && dh0) e = kda::pad_tiles_f32_launch(dh0p, dh0, nst, 64, 64, 128, 128, true, cs);
+    if (e == cudaSuccess && ddt_bias)
+      e = kda::pad_tiles_f32_launch(ddtp, ddt_bias, shape->H, 1, 64, 1, 128, true, cs);
+    return from_cuda(e);
+  }
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   char *w = static_cast<char *>(ws);

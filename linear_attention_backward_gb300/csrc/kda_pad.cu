@@ -1,0 +1,113 @@
+// kda_pad.cu -- K = V = 64 (bf16) on the 128-channel tensor-core path.
+//
+// The tcgen05 kernels take the channel dimension (K or V = 128) as the MMA's
+// M.  A 64-channel problem runs on them exactly after zero-padding its
+// channels to 128: a padded channel c has q^_c = k^_c = 0 (the L2 norm is
+// unchanged), so row c of (I - beta k^ k^T) is e_c^T and the state's row c
+// stays e^(gk) times its start, zero; padded value columns (v = dO = 0, h0 =
+// dh_T = 0) stay zero likewise.  Every gradient term of a padded channel
+// carries one of these zeros, so dq, dk, dg of the padded channels and their
+// dA_log terms vanish, and the real channels' results are those of the
+// 64-channel problem (the read-out scale stays 64^-1/2).  The padded gate
+// channels take g = -30 (softplus ~ 1e-13: no decay), so that they never
+// approach the 16-row block range the prep kernel checks.
+//
+// These kernels copy the inputs into the padded layout and the gradients
+// back out; both directions are plain HBM-bound copies.
+#include <cuda_runtime.h>
+
+#include "kda_device.cuh"
+#include "kda_params.h"
+
+namespace kda {
+
+namespace {
+
+// rows x 64 bf16 -> rows x 128 bf16, channels 64..127 = fill; one 16-byte
+// piece per thread (8 pieces of the source row, 16 of the destination)
+__global__ void kda_pad_rows_kernel(const uint4 *src, uint4 *dst, int64_t rows, uint32_t fill2) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // destination piece
+  if (e >= rows * 16) return;
+  const int64_t r = e >> 4;
+  const int c = (int)(e & 15);
+  dst[e] = c < 8 ? src[r * 8 + c] : make_uint4(fill2, fill2, fill2, fill2);
+}
+
+// rows x 128 bf16 -> rows x 64 bf16 (channels 0..63)
+__global__ void kda_unpad_rows_kernel(const uint4 *src, uint4 *dst, int64_t rows) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // destination piece
+  if (e >= rows * 8) return;
+  dst[e] = src[(e >> 3) * 16 + (e & 7)];
+}
+
+// n tiles of a x b fp32 (row-major) -> n tiles of A x B, zero outside; or
+// the reverse (take the top-left a x b of each A x B tile)
+__global__ void kda_pad_tiles_f32_kernel(const float *src, float *dst, int64_t n, int a, int b,
+                                         int A, int B, int unpad) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t per = unpad ? (int64_t)a * b : (int64_t)A * B;  // destination elements per tile
+  if (e >= n * per) return;
+  const int64_t t = e / per;
+  const int64_t i = e - t * per;
+  if (unpad) {
+    const int r = (int)(i / b), c = (int)(i % b);
+    dst[e] = src[t * A * B + (int64_t)r * B + c];
+  } else {
+    const int r = (int)(i / B), c = (int)(i % B);
+    dst[e] = (r < a && c < b) ? src[t * a * b + (int64_t)r * b + c] : 0.f;
+  }
+}
+
+// n states [64][64] bf16 row-major -> [128][128] bf16 in packed core-matrix
+// order (element (r, c) at ((r / 8) * 16 + c / 8) * 64 + (r % 8) * 8 + c % 8),
+// zero outside the 64 x 64 corner: one 16-byte core row per thread
+__global__ void kda_pack_states64_kernel(const bf16 *src, uint4 *dst, int64_t n) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // core row of the output
+  if (e >= n * 2048) return;
+  const int64_t t = e >> 11;
+  const int q = (int)(e & 2047);
+  const int core = q >> 3, rr = q & 7;
+  const int r = (core >> 4) * 8 + rr, c0 = (core & 15) * 8;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (r < 64 && c0 < 64) v = *reinterpret_cast<const uint4 *>(src + t * 4096 + r * 64 + c0);
+  dst[e] = v;
+}
+
+unsigned blocks_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
+
+}  // namespace
+
+cudaError_t pad_rows_launch(const void *src, void *dst, int64_t rows, float fill,
+                            cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const bf16 f = __float2bfloat16_rn(fill);
+  const uint32_t f2 = (uint32_t)__bfloat16_as_ushort(f) * 0x10001u;
+  kda_pad_rows_kernel<<<blocks_for(rows * 16, 256), 256, 0, st>>>(
+      static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), rows, f2);
+  return cudaGetLastError();
+}
+
+cudaError_t unpad_rows_launch(const void *src, void *dst, int64_t rows, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  kda_unpad_rows_kernel<<<blocks_for(rows * 8, 256), 256, 0, st>>>(
+      static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), rows);
+  return cudaGetLastError();
+}
+
+cudaError_t pad_tiles_f32_launch(const float *src, float *dst, int64_t n, int a, int b, int A,
+                                 int B, bool unpad, cudaStream_t st) {
+  const int64_t total = n * (unpad ? (int64_t)a * b : (int64_t)A * B);
+  if (total <= 0) return cudaSuccess;
+  kda_pad_tiles_f32_kernel<<<blocks_for(total, 256), 256, 0, st>>>(src, dst, n, a, b, A, B,
+                                                                    unpad ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_states64_launch(const void *src, void *dst, int64_t n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  kda_pack_states64_kernel<<<blocks_for(n * 2048, 256), 256, 0, st>>>(
+      static_cast<const bf16 *>(src), static_cast<uint4 *>(dst), n);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -147,6 +147,16 @@ cudaError_t grads_dispatch(const KdaParams &p, int K, bool bf16, const void *sta
 size_t grads_smem_bytes(int K, bool bf16);
 int grads_status_take();
 
+// kda_pad.cu: bf16 K = V = 64 on the 128-channel path.  rows x 64 bf16 <->
+// rows x 128 bf16 (padded channels = fill), n fp32 tiles a x b <-> A x B
+// (zero outside), and n row-major 64 x 64 bf16 states -> packed 128 x 128.
+cudaError_t pad_rows_launch(const void *src, void *dst, int64_t rows, float fill,
+                            cudaStream_t st);
+cudaError_t unpad_rows_launch(const void *src, void *dst, int64_t rows, cudaStream_t st);
+cudaError_t pad_tiles_f32_launch(const float *src, float *dst, int64_t n, int a, int b, int A,
+                                 int B, bool unpad, cudaStream_t st);
+cudaError_t pack_states64_launch(const void *src, void *dst, int64_t n, cudaStream_t st);
+
 // kda_grads_tc.cu: the same per-chunk gradients on tcgen05 (bf16, K = V = 128).
 cudaError_t grads_tc_launch(const KdaParams &p, const TokenMaps &tm, const void *states,
                             cudaStream_t st);

@@ -160,9 +160,8 @@ def test_fwd_argument_checks(L):
     # workspace missing or too small
     assert L.kda_fwd(ctypes.byref(s), *args, None, ws_ok, None) == 3
     assert L.kda_fwd(ctypes.byref(s), *args, fake, ctypes.c_size_t(ws_ok.value - 1), None) == 3
-    # the forward runs the bf16, K = V = 128 path only
-    f = _shape(K=64, V=64)
-    assert L.kda_fwd(ctypes.byref(f), *args, fake, ctypes.c_size_t(1 << 40), None) == 2
+    # the forward runs bf16 only (K = V = 64 on zero-padded copies): fp32 is
+    # not built
     f = _shape(dtype=kda.KDA_FP32, K=64, V=64)
     assert L.kda_fwd(ctypes.byref(f), *args, fake, ctypes.c_size_t(1 << 40), None) == 2
 
@@ -178,8 +177,10 @@ def test_fwd_argument_checks(L):
 ])
 def test_scan_segments_rule(L, B, T, H, expect):
     assert kda.scan_segments(_shape(B=B, T=T, H=H)) == expect
-    # other dtypes and head sizes run the per-band scans: no segments
-    assert kda.scan_segments(_shape(B=B, T=T, H=H, K=64, V=64)) == 0
+    # bf16 K = V = 64 runs the same scans on zero-padded copies; fp32 runs
+    # the per-band scans: no segments
+    assert kda.scan_segments(_shape(B=B, T=T, H=H, K=64, V=64)) == expect
+    assert kda.scan_segments(_shape(B=B, T=T, H=H, K=64, V=64, dtype=kda.KDA_FP32)) == 0
 
 
 @pytest.mark.parametrize("env,expect", [("0", 0), ("3", 3), ("4", 4), ("9", 4), ("2", 4),
