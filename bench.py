@@ -40,9 +40,17 @@ WORKLOAD = "main_bf16"
 #   gradient kernel: the same inputs and outputs, plus S_n and dS_{n+1}
 #   (2 x 512 B) read                                               -> 3332 B
 ALG_BYTES = {"grads": 3332, "path": 3332}
-# Dense-equivalent FLOP per (token, head): the gradient kernel's contractions
-# (16.8 MFLOP per 64-token chunk and head) and the whole path (38.1 MFLOP).
-ALG_FLOP = {"grads": 16.8e6 / 64, "path": 38.1e6 / 64}
+# Algorithmic FLOP per (token, head): each product of a 64-token chunk (C = 64,
+# D = 128) at its useful size, 2 m n k, triangular ones (the strictly lower or
+# lower pair matrices and inverse, the masked dMqk / dAkk) at half:
+#   prep   G, Mqk 2 x 0.52 M, W, U0, Mqk W 3 x 0.52 M, WY inverse 0.17 M  -> 2.8 M
+#   forward scan   W S_n, kr^T U                 2 x 2.1 M              -> 4.2 M
+#   reverse scan   kr dS, W^T (.), QE^T dO       3 x 2.1 M              -> 6.3 M
+#   gradients  kd S 2.1, INVb Xr 1.05, Mqk^T dO 1.05, kr dS 2.1, U dS^T 2.1,
+#              INV^T dU 1.05, [dO; dvcorr] U^T 1.05, S [dO; dvcorr]^T 4.2,
+#              the four intra-chunk terms 2.1                             -> 16.8 M
+#   path                                                                 -> 30.1 M
+ALG_FLOP = {"grads": 16.8e6 / 64, "path": 30.1e6 / 64}
 # phases recorded by kda_bwd_timed (5 events) and the kernel each one runs
 PHASES = ("prep", "scan", "grads", "reduce")
 KERNEL_NAMES = {"prep": "kda_prep_tc_kernel", "scan": "kda_scan_tc_kernel",
