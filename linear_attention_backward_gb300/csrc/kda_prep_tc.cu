@@ -328,25 +328,29 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
   }
   __syncthreads();
-  // G and scale * Mqk for the gradient kernel (packed 64 x 64 tiles)
+  // G for the gradient kernel (packed 64 x 64 tile; the inverse overwrites Gf)
   for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
     const int i = e8 >> 3, j0 = (e8 & 7) * 8;
-    const uint32_t off = umma::core_off(i, j0, 64);
-    st16_bf(unit + kPrepG + off, Gf + i * kGfStride + j0);
-    *reinterpret_cast<uint4 *>(unit + kPrepMqk + off) =
-        *reinterpret_cast<const uint4 *>(Mqk + pcore_off(i, j0, 64));
+    st16_bf(unit + kPrepG + umma::core_off(i, j0, 64), Gf + i * kGfStride + j0);
   }
   __syncthreads();
-  inverse_inplace(Gf, sv.beta, tbuf);
+  // scale * Mqk for the gradient kernel, stored by the warps the inverse's
+  // diagonal phase leaves idle
+  inverse_inplace(Gf, sv.beta, tbuf, [&](int w4) {
+    for (int e8 = 32 * w4 + lane; e8 < 64 * 8; e8 += 32 * (NWARPS - 4)) {
+      const int i = e8 >> 3, j0 = (e8 & 7) * 8;
+      *reinterpret_cast<uint4 *>(unit + kPrepMqk + umma::core_off(i, j0, 64)) =
+          *reinterpret_cast<const uint4 *>(Mqk + pcore_off(i, j0, 64));
+    }
+  });
+  // INV diag(beta) as the W^T product's operand first; INV and INV diag(beta)
+  // go to HBM while that product runs (it reads only the shared tile)
   for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
     const int i = e8 >> 3, j0 = (e8 & 7) * 8;
     float x[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) x[u] = Gf[i * kGfStride + j0 + u] * sv.beta[j0 + u];
     pstore8(INVb, i, j0, 64, x);
-    const uint32_t off = umma::core_off(i, j0, 64);
-    st16_bf(unit + kPrepINV + off, Gf + i * kGfStride + j0);
-    st16_bf(unit + kPrepINVb + off, x);
   }
   umma::fence_async_smem();
   umma::tc_fence_before();
@@ -364,6 +368,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       gemm(tbase + 64 * J, opmn(KM, D, 16 * J), true, opk(INVb, 64, 16 * J), false, 64, 1, false);
     umma::mma_commit(mbar);
   }
+  for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
+    const int i = e8 >> 3, j0 = (e8 & 7) * 8;
+    float x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) x[u] = Gf[i * kGfStride + j0 + u] * sv.beta[j0 + u];
+    const uint32_t off = umma::core_off(i, j0, 64);
+    st16_bf(unit + kPrepINV + off, Gf + i * kGfStride + j0);
+    st16_bf(unit + kPrepINVb + off, x);
+  }
   mma_wait();
   const int ch = tid & 127, gq = tid >> 7;  // TMEM lane (channel) and 32-column group
   {
@@ -378,6 +391,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
       for (int r = 0; r < 32; ++r) w[r] = fmaf(em, a[r], w[r]);
     }
+    __syncthreads();  // W^T's tile lies over INV's fp32 rows, which the stores above read
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint32_t off = umma::core_off(ch, 32 * gq + 8 * q, 64);

@@ -198,10 +198,14 @@ __device__ __forceinline__ void mma_tf32(float (&acc)[4], const uint32_t (&a)[4]
 constexpr int kGfStride = 68;
 // Gf [64][kGfStride] fp32 holds G (strictly lower) on entry and
 // (I + diag(beta) G)^-1 on exit (block forward substitution in place, as
-// wy_inverse in kda_chunk.cuh).
-__device__ inline void inverse_inplace(float *Gf, const float *beta, float *tbuf) {
+// wy_inverse in kda_chunk.cuh).  While warps 0-3 invert the diagonal blocks,
+// warps 4 and up run side(warp - 4) (independent work of the caller's that
+// touches neither Gf nor tbuf).
+template <typename Side>
+__device__ inline void inverse_inplace(float *Gf, const float *beta, float *tbuf, Side side) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int LG = kGfStride;
+  if (warp >= 4) side(warp - 4);
   if (warp < 4) {
     const int o = 16 * warp, col = lane & 15;
     float x[16];
