@@ -391,7 +391,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
       for (int r = 0; r < 32; ++r) w[r] = fmaf(em, a[r], w[r]);
     }
-    __syncthreads();  // W^T's tile lies over INV's fp32 rows, which the stores above read
+    // W^T's tile lies over INV's fp32 rows, which the stores above read; and
+    // nothing leaves a CTA whose product wait gave up
+    if (__syncthreads_or(!ok)) { ok = false; goto drain; }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint32_t off = umma::core_off(ch, 32 * gq + 8 * q, 64);
@@ -411,6 +413,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     umma::mma_commit(mbar);
   }
   mma_wait();
+  if (__syncthreads_or(!ok)) { ok = false; goto drain; }  // nothing leaves after a timeout
   {
     float a[32];
     tld32(tbase, 0, a);

@@ -63,6 +63,17 @@ def test_fp32_ragged_with_states(T):
     _compare(g, oracle_bwd(x), x, TOL["fp32"])
 
 
+@pytest.mark.parametrize("dtype,K", [("bf16", 128), ("bf16", 64), ("fp32", 64)])
+def test_custom_scale_and_l2_eps(dtype, K):
+    # a read-out scale other than K^-1/2 and a larger epsilon inside the L2
+    # norm, on the tcgen05 path, the padded K = 64 path and the fp32 path
+    w = wl.custom("se", B=2, T=150, H=2, K=K, V=K, dtype=dtype, with_h0=True, with_dhT=True)
+    x = wl.make_inputs(w, seed=70 + K)
+    g, _ = gpu_bwd(x, scale=0.3, l2_eps=1e-3)
+    _check_status()
+    _compare(g, oracle_bwd(x, scale=0.3, eps=1e-3), x, TOL[dtype])
+
+
 def test_varlen_bf16_with_empty_sequence():
     w = wl.custom("v", H=2, K=128, V=128, dtype="bf16", with_h0=True, with_dhT=True,
                   varlen=(5, 1, 200))
