@@ -72,10 +72,10 @@ def launches_per_step(shape, cu, forward=False):
 # is measured again.
 NCU_TRAFFIC = {
     # ncu on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read 841.7 MB +
-    # write 244.8 MB (profiles/traffic_main_b1_bf16.md), scaled by 4 to the main
+    # write 245.1 MB (profiles/traffic_main_b1_bf16.md), scaled by 4 to the main
     # workload's 16384 chunk-heads (the kernel's traffic is proportional to them)
-    "kda_grads_tc_kernel": {"sha": "cf4ea4907ec74cd2", "workload": "main_bf16",
-                            "bytes_per_launch": 4345711616},
+    "kda_grads_tc_kernel": {"sha": "0b14a0a7e8ac1c1d", "workload": "main_bf16",
+                            "bytes_per_launch": 4347370496},
 }
 
 KERNEL_SOURCES = {

@@ -18,11 +18,26 @@
 // contraction and the 16-row reverse cumsum.)
 #pragma once
 
+#include <type_traits>
+
 #include "kda_device.cuh"
 #include "kda_params.h"
 
 namespace kda {
 
+// Gate arithmetic by input type.  fp32 inputs are held to 1e-4 relative
+// error, so their gate path takes the accurate softplus and exponential (the
+// fast exponential's error bound grows with |x|, and gate exponents reach
+// tens of nats); bf16 operands are rounded to 2^-9, far above either fast
+// form's error, and keep the fast ones.
+template <typename E> __device__ __forceinline__ float gate_exp(float x) {
+  if constexpr (std::is_same<E, float>::value) return expf(x);
+  else return __expf(x);
+}
+template <typename E> __device__ __forceinline__ float gate_softplus(float x) {
+  if constexpr (std::is_same<E, float>::value) return softplus_f(x);
+  else return softplus_gate(x);
+}
 
 
 // Bounds of sequence s.  Returns false (and flags the device status) on a
@@ -211,7 +226,7 @@ __device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, cons
   constexpr int ROWS = CHUNK / PARTS;        // rows per segment (16 or 8)
   static_assert(ROWS == 16 || ROWS == 8, "segment must tile the 16-row blocks");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float A = __expf(p.A_log[h]);
+  const float A = gate_exp<E>(p.A_log[h]);
   // 1. L2 norms: one warp per row, 4 (K = 128) or 2 (K = 64) channels per lane
   for (int i = warp; i < CHUNK; i += NWARPS) {
     float sk = 0.f, sq = 0.f;
@@ -248,8 +263,8 @@ __device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, cons
     const int i = r0 + r;
     const float2 gv = load2(Gr + i * K + c);
     const bool ok = i < len;
-    run0 += ok ? -A * softplus_gate(gv.x + bias0) : 0.f;
-    run1 += ok ? -A * softplus_gate(gv.y + bias1) : 0.f;
+    run0 += ok ? -A * gate_softplus<E>(gv.x + bias0) : 0.f;
+    run1 += ok ? -A * gate_softplus<E>(gv.y + bias1) : 0.f;
     g0[r] = run0;
     g1[r] = run1;
   }
@@ -294,8 +309,8 @@ __device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, cons
       float after = bb[L];
 #pragma unroll
       for (int L2 = L + 1; L2 < 4; ++L2) after += a[L2] + bb[L2];
-      sv.em[L * K + e] = __expf(before + a[L]);   // e^(m_L)
-      sv.egm[L * K + e] = __expf(after);          // e^(gT - m_L)
+      sv.em[L * K + e] = gate_exp<E>(before + a[L]);   // e^(m_L)
+      sv.egm[L * K + e] = gate_exp<E>(after);       // e^(gT - m_L)
       before += a[L] + bb[L];
     }
 #pragma unroll
@@ -305,7 +320,7 @@ __device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, cons
         float d = bb[J] + a[I2];
 #pragma unroll
         for (int L = J + 1; L < I2; ++L) d += a[L] + bb[L];
-        sv.F[pair_index(I2, J) * K + e] = __expf(d);  // e^(m_I - m_J)
+        sv.F[pair_index(I2, J) * K + e] = gate_exp<E>(d);  // e^(m_I - m_J)
       }
     sv.gT[e] = tot;
   }
@@ -325,8 +340,8 @@ __device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, cons
     const float rk = sv.rk[i];
     const float kh0 = kv.x * rk, kh1 = kv.y * rk;
     const float d0 = g0[r] - ref0, d1 = g1[r] - ref1;
-    const float e0 = __expf(d0), e1 = __expf(d1);
-    const float ei0 = __expf(-d0), ei1 = __expf(-d1);
+    const float e0 = gate_exp<E>(d0), e1 = gate_exp<E>(d1);
+    const float ei0 = gate_exp<E>(-d0), ei1 = gate_exp<E>(-d1);
     if (tiles.KM) store2(tiles.KM + i * LD + c, kh0 * e0, kh1 * e1);
     if (tiles.KP) store2(tiles.KP + i * LD + c, kh0 * ei0, kh1 * ei1);
     if (tiles.KD) store2(tiles.KD + i * LD + c, (kh0 * e0) * em0, (kh1 * e1) * em1);

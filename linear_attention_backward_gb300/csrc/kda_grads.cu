@@ -26,14 +26,29 @@
 
 namespace kda {
 
+// Accumulator of the gate gradient's carries.  The chunk-end term dgT (the
+// row dot e^gT dS_{n+1} . S_n plus the kr column sums) is large next to dgk
+// and cancels against the reverse cumulative sum of dgc, and dA_log = sum
+// dgk gk cancels once more over the rows; one fp32 rounding of dgT alone
+// moves dA_log by ~5e-5 relative on ordinary inputs.  fp32 inputs are held
+// to 1e-4, so their dgT, the cumulative sum and the dA_log partial are
+// accumulated in fp64 (exact products of the fp32 factors); bf16 inputs keep
+// fp32, far below their own 2e-2 bound.
+template <typename E>
+using GAcc = typename std::conditional<std::is_same<E, float>::value, double, float>::type;
+
 template <typename E, int D> struct GradSmem {
   static constexpr int LD = tile_ld<E>(D);
   static constexpr int LDS = tile_ld<E>(64);
   static constexpr int LDF = D + 4;
   static constexpr size_t sz_E = 64 * LDF * 4;
-  // the prep view, then dgT (D) and dA (8); the dbeta parts and row dots
-  // reuse the view's column-partial scratch between the prep and the cumsum
-  static constexpr size_t n_small = PrepView<E, D>::floats + D + 8;
+  // the prep view, then dgT (D) and dA (8) as GAcc; the dbeta parts and
+  // row dots reuse the view's column-partial scratch between the prep and the
+  // cumsum, and so do the cumsum's segment totals (GAcc)
+  static constexpr size_t n_small = PrepView<E, D>::floats + (D + 8) * (sizeof(GAcc<E>) / 4);
+  static_assert(PrepView<E, D>::floats % 2 == 0, "dgT must be 8-byte aligned");
+  static_assert((NTHREADS / D) * D * sizeof(GAcc<E>) <= 2 * NTHREADS * 4,
+                "segment totals must fit the column-partial scratch");
   static constexpr size_t sz_small = ((n_small * 4 + 127) / 128) * 128;
   static constexpr size_t sz_G = 64 * 68 * 4;
   static constexpr size_t sz_sq = 64 * LDS * sizeof(E);
@@ -81,11 +96,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
   float *Eg = reinterpret_cast<float *>(smem + SM::o_E);
   float *sm = reinterpret_cast<float *>(smem + SM::o_small);
   PrepView<E, D> sv = make_view<E, D>(sm);
-  float *dgT = sm + PrepView<E, D>::floats;  // [D]
-  float *dAred = dgT + D;           // [8]
+  using Acc = GAcc<E>;
+  Acc *dgT = reinterpret_cast<Acc *>(sm + PrepView<E, D>::floats);  // [D]
+  Acc *dAred = dgT + D;             // [8]
   float *dbp = sv.part;             // [4][64]: dbeta1 halves, dbeta2 halves
   float *rowdot = sv.part + 256;    // [2][64]
-  float *partsum = sv.part;         // [NTHREADS / D][D], reused by the gate cumsum
+  Acc *partsum = reinterpret_cast<Acc *>(sv.part);  // [NTHREADS / D][D], the gate cumsum
   E *INV = reinterpret_cast<E *>(smem + SM::o_INV);
   E *MQK = reinterpret_cast<E *>(smem + SM::o_MQK);
   E *DA = reinterpret_cast<E *>(smem + SM::o_DA);
@@ -107,7 +123,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
   const E *Sg = reinterpret_cast<const E *>(states) + ((size_t)slot * H + h) * DD;
   const E *dSg = reinterpret_cast<const E *>(p.dstates) + ((size_t)slot * H + h) * DD;
 
-  if (tid < D) dgT[tid] = 0.f;
+  if (tid < D) dgT[tid] = Acc(0);
 
   // ---- prep: norms, gates, operand tiles, pair matrices, inverse ----
   {
@@ -173,15 +189,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
   {
     constexpr int TPR = NTHREADS / D;
     const int r = tid / TPR, part = tid % TPR;
-    float acc_p = 0.f;
+    Acc acc_p = Acc(0);
     for (int d = part * (D / TPR); d < (part + 1) * (D / TPR); d += 2) {
       const float2 a = load2(BIG2 + r * LD + d);
       const float2 b = load2(BIG1 + r * LD + d);
-      acc_p = fmaf(a.x, b.x, fmaf(a.y, b.y, acc_p));
+      acc_p = fma(Acc(a.x), Acc(b.x), fma(Acc(a.y), Acc(b.y), acc_p));
     }
 #pragma unroll
     for (int o = 1; o < TPR; o <<= 1) acc_p += __shfl_xor_sync(0xffffffffu, acc_p, o);
-    if (part == 0) atomicAdd(&dgT[r], __expf(sv.gT[r]) * acc_p);
+    if (part == 0) atomicAdd(&dgT[r], Acc(gate_exp<E>(sv.gT[r])) * acc_p);
   }
   __syncthreads();  // all reads of KRt, MQK, BIG2 (dS) done
   store_acc(KRt + 16 * rb * LD + ch, LD, acc);  // dU
@@ -419,9 +435,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
         }
     }
     float rp[2] = {0.f, 0.f};
-    float colp[NF][2];
+    Acc colp[NF][2];
 #pragma unroll
-    for (int f = 0; f < NF; ++f) colp[f][0] = colp[f][1] = 0.f;
+    for (int f = 0; f < NF; ++f) colp[f][0] = colp[f][1] = Acc(0);
 #pragma unroll
     for (int f = 0; f < NF; ++f)
 #pragma unroll
@@ -437,14 +453,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
         tmp[f][e] = kh;
         dgc[i * LDF + c] += dks * kh;
         rp[e >> 1] = fmaf(dkh, kh, rp[e >> 1]);
-        colp[f][e & 1] = fmaf(dkr[f][e], kh, colp[f][e & 1]);
+        colp[f][e & 1] = fma(Acc(dkr[f][e]), Acc(kh), colp[f][e & 1]);
       }
     // dgT += sum over the chunk rows of dkr' k^ (same k^ as the cancelling term)
 #pragma unroll
     for (int f = 0; f < NF; ++f)
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
-        float v = colp[f][x];
+        Acc v = colp[f][x];
         v += __shfl_xor_sync(0xffffffffu, v, 4);
         v += __shfl_xor_sync(0xffffffffu, v, 8);
         v += __shfl_xor_sync(0xffffffffu, v, 16);
@@ -481,42 +497,44 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
     constexpr int SEG = 64 / PARTS;
     const int c = tid % D, part = tid / D;
     const int ra = part * SEG;
-    float tot = 0.f;
+    Acc tot = Acc(0);
     for (int i = ra; i < ra + SEG; ++i) tot += dgc[i * LDF + c];
     partsum[part * D + c] = tot;
     __syncthreads();
-    float run = dgT[c];
+    Acc run = dgT[c];
     for (int q2 = part + 1; q2 < PARTS; ++q2) run += partsum[q2 * D + c];
-    const float A = __expf(p.A_log[h]);
+    const float A = gate_exp<E>(p.A_log[h]);
     const float bias = gate_bias(p, h, c, D);
-    float dA = 0.f, ddt = 0.f;
+    Acc dA = Acc(0);
+    float ddt = 0.f;
     E *dgg = reinterpret_cast<E *>(p.dg);
     for (int i = ra + SEG - 1; i >= ra; --i) {
       run += dgc[i * LDF + c];
       if (i < len) {
         const float gv = to_f(Graw[i * D + c]) + bias;
         const float gk = -A * softplus_f(gv);
-        const float dgv = run * (-A) * sigmoid_f(gv);
+        const float dgv = (float)run * (-A) / (1.f + gate_exp<E>(-gv));
         dgg[((tok0 + i) * H + h) * D + c] = from_f<E>(dgv);
-        dA = fmaf(run, gk, dA);
+        dA = fma(run, Acc(gk), dA);
         ddt += dgv;
       }
     }
-    dA = warp_sum(dA);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dA += __shfl_xor_sync(0xffffffffu, dA, o);
     if (lane == 0) dAred[warp] = dA;
     __syncthreads();
     if (tid == 0) {
-      float t = 0.f;
+      Acc t = Acc(0);
       for (int w = 0; w < NWARPS; ++w) t += dAred[w];
-      p.dA_part[slot * H + h] = t;
+      p.dA_part[slot * H + h] = (float)t;
     }
     if (p.ddt_part != nullptr) {  // ddt_bias partial of the chunk: the dg column sums
       partsum[part * D + c] = ddt;  // (every thread has read partsum above)
       __syncthreads();
       if (part == 0) {
-        float t = 0.f;
+        Acc t = Acc(0);
         for (int q2 = 0; q2 < PARTS; ++q2) t += partsum[q2 * D + c];
-        p.ddt_part[(slot * H + h) * D + c] = t;
+        p.ddt_part[(slot * H + h) * D + c] = (float)t;
       }
     }
   }

@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
       store_acc(UB + 16 * rb * LDB + ch, LDB, acc);
       __syncthreads();
       // S <- diag(e^gT) S + kr^T U
-      for_acc(S, [&](int r, int c, float &x) { x *= __expf(sv.gT[srow0 + r]); });
+      for_acc(S, [&](int r, int c, float &x) { x *= gate_exp<E>(sv.gT[srow0 + r]); });
       warp_gemm<NFS, false, false>(S, KR + srow0, LD, UB + scol0, LDB, 64);
     } else {
       // dU = scale Mqk^T dO + kr dS
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_scan_kernel(KdaParams p) {
       });
       __syncthreads();
       // dS <- diag(e^gT) dS + scale qd^T dO - kd^T diag(beta) dvcorr
-      for_acc(S, [&](int r, int c, float &x) { x *= __expf(sv.gT[srow0 + r]); });
+      for_acc(S, [&](int r, int c, float &x) { x *= gate_exp<E>(sv.gT[srow0 + r]); });
       warp_gemm<NFS, false, false>(S, QD + srow0, LD, BAND + scol0, LDB, 64);
       warp_gemm<NFS, false, false>(S, KD + srow0, LD, W + scol0, LDB, 64);
     }
