@@ -154,8 +154,10 @@ size_t kda_workspace_dstates_offset(const kda_shape *shape);
  * (N sequences; 152 is the SM count) and at least 4 P chunks per sequence
  * (for varlen, on average: T / 64 / N, since the host never reads
  * cu_seqlens; shorter sequences get shorter or empty segments): the most
- * segments, 3 to 8, whose first-pass chains fit one per SM.  The workspace
- * then ends with (3 P - 4) fp32 K x V tiles per (sequence, head).
+ * segments, 3 to 8, whose first-pass chains ((3 P - 4) N H) fit one per SM;
+ * if not even 3 do and 4 N H <= 152, the most whose chains fit two per SM
+ * (the scan kernel's residency).  The workspace then ends with (3 P - 4)
+ * fp32 K x V tiles per (sequence, head).
  * The environment variable KDA_SCAN_CP=0 turns this off per call, and
  * KDA_SCAN_CP=n (3 <= n <= the value without it) takes n segments.
  * Returns 0 on a bad shape. */

@@ -111,11 +111,15 @@ kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR
 // Segments of the context-parallel tcgen05 scans (0: whole-sequence chains).
 // Used when the whole-sequence chains (two per sequence and head) leave most
 // SMs idle: the most segments (3..8, at least four chunks each) whose phase-1
-// chains, kda_cp_tiles(P) per sequence and head, still fit one per SM.  A
-// function of the shape, so that the workspace size is too: for varlen the
-// host does not read cu_seqlens, and the chunks per sequence are taken as
-// the average T / 64 / num_seqs (shorter sequences get shorter, possibly
-// empty, segments).
+// chains, kda_cp_tiles(P) per sequence and head, still fit one per SM.  When
+// even three segments do not fit so but the whole-sequence chains fill at
+// most half the SMs (up to 38 sequence-heads), the most whose chains fit two
+// per SM, the scan kernel's residency: at B = 1, T = 8192, H = 32 four
+// segments take the scans from 0.282 to 0.222 ms, where at H = 16 more than
+// the one-per-SM count (four) gained nothing.  A function of the shape, so
+// that the workspace size is too: for varlen the host does not read
+// cu_seqlens, and the chunks per sequence are taken as the average
+// T / 64 / num_seqs (shorter sequences get shorter, possibly empty, segments).
 int cp_segments(const kda_shape *s) {
   if (!tc_state_path(s)) return 0;
   const int64_t units = (int64_t)num_seqs_of(s) * s->H;
@@ -125,6 +129,9 @@ int cp_segments(const kda_shape *s) {
   int best = 0;
   for (int P = 3; P <= 8; ++P)
     if (kda::kda_cp_tiles(P) * units <= kTargetCtas && nck >= 4 * P) best = P;
+  if (best == 0 && 4 * units <= kTargetCtas)
+    for (int P = 3; P <= 8; ++P)
+      if (kda::kda_cp_tiles(P) * units <= 2 * kTargetCtas && nck >= 4 * P) best = P;
   return best;
 }
 

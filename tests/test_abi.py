@@ -172,8 +172,11 @@ def test_fwd_argument_checks(L):
     (1, 1024, 2, 4),      # 16 chunks: at least 4 per segment -> P = 4
     (1, 704, 2, 0),       # 11 chunks: fewer than 4 per segment for P = 3
     (4, 8192, 19, 0),     # 2 * 76 chains fill the 152 SMs
-    (1, 8192, 32, 0),     # 32 sequence-heads: (3 * 3 - 4) * 32 > 152
     (1, 8192, 30, 3),     # 30: (3 * 3 - 4) * 30 = 150 <= 152
+    (1, 8192, 32, 4),     # 32: (3 * 3 - 4) * 32 > 152, so two per SM: 8 * 32 = 256 <= 304
+    (1, 8192, 38, 4),     # 38: two per SM, (3 * 4 - 4) * 38 = 304 <= 304 -> P = 4
+    (1, 8192, 39, 0),     # 39: the whole-sequence chains fill more than half the SMs
+    (1, 768, 32, 3),      # two per SM, 12 chunks: at least 4 per segment -> P = 3
 ])
 def test_scan_segments_rule(L, B, T, H, expect):
     assert kda.scan_segments(_shape(B=B, T=T, H=H)) == expect

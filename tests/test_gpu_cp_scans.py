@@ -80,6 +80,24 @@ def test_cp_matches_whole_sequence_chains(monkeypatch):
     _compare(g_cp, oracle_bwd(x))
 
 
+def test_cp_two_chains_per_sm(monkeypatch):
+    # 32 sequence-heads: three segments would need 160 first-pass chains, more
+    # than one per SM, so the split takes two per SM: 4 segments, 256 chains
+    w = wl.custom("cp", B=1, T=64 * 16 + 37, H=32, K=128, V=128, dtype="bf16", with_h0=True,
+                  with_dhT=True)
+    x = wl.make_inputs(w, seed=38)
+    d = to_dev(x)
+    assert kda.scan_segments(kda.make_shape(d["q"], d["v"])) == 4
+    g_cp, _ = gpu_bwd(x)
+    assert kda.get_device_status() == 0
+    _compare(g_cp, oracle_bwd(x))
+    monkeypatch.setenv("KDA_SCAN_CP", "0")
+    g_one, _ = gpu_bwd(x)
+    assert kda.get_device_status() == 0
+    for k in GRADS:
+        assert rel_l2(g_cp[k].double().cpu().numpy(), g_one[k].double().cpu().numpy()) < 1e-2, k
+
+
 def test_cp_long_segments_eight_way():
     # 128 chunks, 2 chains: 8 segments of 16 chunks and 6 combine steps
     w = wl.custom("cp", B=1, T=8192, H=2, K=128, V=128, dtype="bf16", with_h0=True,
