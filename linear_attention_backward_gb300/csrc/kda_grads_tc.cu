@@ -101,6 +101,8 @@ struct Smem {
   static_assert(o_KPl + T64x128 <= o_stk + kStk, "KPl stays clear of slab 1");
   static_assert(total <= 232448, "shared memory budget");
   static_assert(16 * NT * 4 <= sz_C, "K1 row buffer must fit R_C");
+  static_assert(o_small % 16 == 0 && (19 * D * 4) % 16 == 0,
+                "the view's rq, rk and beta rows start on 16-byte boundaries (lds4)");
 };
 
 // TMEM address of this thread's lane (warp quarter) at column col
@@ -206,12 +208,17 @@ __device__ void prep_tc(const KdaParams &p, int h, int len, const bf16 *Qr, cons
   for (int q8 = 0; q8 < 2; ++q8) {
     float vkd[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int r = 8 * q8 + t, i = 16 * I + r;
-      const float e = __expf(d[r]);
-      E[r] = e;
-      const float kh = BF16_AT(k2, r) * sv.rk[i];
-      vkd[t] = (kh * e) * em;
+    for (int t4 = 0; t4 < 8; t4 += 4) {
+      float rk4[4];
+      lds4(sv.rk + 16 * I + 8 * q8 + t4, rk4);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = t4 + u, r = 8 * q8 + t;
+        const float e = __expf(d[r]);
+        E[r] = e;
+        const float kh = BF16_AT(k2, r) * rk4[u];
+        vkd[t] = (kh * e) * em;
+      }
     }
     pstore8(KDt, c, 16 * I + 8 * q8, 64, vkd);
   }
@@ -460,13 +467,18 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     for (int q = 0; q < 2; ++q) pload8(XrT, c, 16 * I + 8 * q, 64, xr + 8 * q);
     float pr[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const int i = 16 * I + r;
-      // dvcorr row i = row 64 + i of the stacked swizzled operand
-      *reinterpret_cast<bf16 *>(stk + umma::sw128_off(64 + i, c, SM::kStk)) =
-          __float2bfloat16_rn(acc[r]);
-      dvs[i * D + c] = __float2bfloat16_rn(sv.beta[i] * acc[r]);
-      pr[r] = acc[r] * xr[r];
+    for (int r4 = 0; r4 < 16; r4 += 4) {
+      float b4[4];
+      lds4(sv.beta + 16 * I + r4, b4);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = r4 + u, i = 16 * I + r;
+        // dvcorr row i = row 64 + i of the stacked swizzled operand
+        *reinterpret_cast<bf16 *>(stk + umma::sw128_off(64 + i, c, SM::kStk)) =
+            __float2bfloat16_rn(acc[r]);
+        dvs[i * D + c] = __float2bfloat16_rn(b4[u] * acc[r]);
+        pr[r] = acc[r] * xr[r];
+      }
     }
     // sums over this warp's 32 channels; lane l < 16 holds row 16 I + l
     const float t = rows16_sum(pr);
@@ -514,6 +526,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     tld16(tbase, 64, v16);  // columns j in [16 I, 16 I + 16)
     if (c >= 64) {
       const int i = c - 64;
+      const float bi = sv.beta[i];
       float db2 = 0.f;
       float o8[8];
 #pragma unroll
@@ -525,7 +538,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
           const int jj = 16 * I + 8 * q + t;
           const float dak = jj < i ? -v16[8 * q + t] : 0.f;
           db2 = fmaf(dak, g8[t], db2);
-          o8[t] = sv.beta[i] * dak;
+          o8[t] = bi * dak;
         }
         pstore8(dMA, dma_row(i, 1), 16 * I + 8 * q, 64, o8);
       }
@@ -562,26 +575,40 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   float qh[16], kh[16];
 #pragma unroll
   for (int q8 = 0; q8 < 2; ++q8) {
-    float hv[3][8], lv[3][8];
+    // two rows at a time: hi = bf16 pair (one conversion), lo = the pair of
+    // remainders x - hi (exact in fp32), rounded as a pair
+    uint32_t hp[3][4], lp[3][4];
+    float rq8[8], rk8[8];
+    lds4(sv.rq + 16 * I + 8 * q8, rq8);
+    lds4(sv.rq + 16 * I + 8 * q8 + 4, rq8 + 4);
+    lds4(sv.rk + 16 * I + 8 * q8, rk8);
+    lds4(sv.rk + 16 * I + 8 * q8 + 4, rk8 + 4);
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int r = 8 * q8 + t, i = 16 * I + r;
-      qh[r] = BF16_AT(q2, r) * sv.rq[i];
-      kh[r] = BF16_AT(k2, r) * sv.rk[i];
-      const float x[3] = {qh[r] * E[r], kh[r] * E[r], __fdividef(kh[r], E[r])};
+    for (int t2 = 0; t2 < 4; ++t2) {
+      float x[3][2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int r = 8 * q8 + 2 * t2 + e;
+        qh[r] = BF16_AT(q2, r) * rq8[2 * t2 + e];
+        kh[r] = BF16_AT(k2, r) * rk8[2 * t2 + e];
+        x[0][e] = qh[r] * E[r];
+        x[1][e] = kh[r] * E[r];
+        x[2][e] = __fdividef(kh[r], E[r]);
+      }
 #pragma unroll
       for (int u = 0; u < 3; ++u) {
-        hv[u][t] = __bfloat162float(__float2bfloat16_rn(x[u]));
-        lv[u][t] = x[u] - hv[u][t];
+        const uint32_t h2 = f2_to_bf2(x[u][0], x[u][1]);
+        hp[u][t2] = h2;
+        lp[u][t2] = f2_to_bf2(x[u][0] - bf_lo(h2), x[u][1] - bf_hi(h2));
       }
     }
-    const int i0 = 16 * I + 8 * q8;
+    const uint32_t off = pcore_off(c, 16 * I + 8 * q8, 64);  // rows i0 .. i0 + 7 of channel c
     char *hi[3] = {QMh, KMh, KPh};
     char *lo[3] = {QMl, KMl, KPl};
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
-      pstore8(hi[u], c, i0, 64, hv[u]);
-      pstore8(lo[u], c, i0, 64, lv[u]);
+      *reinterpret_cast<uint4 *>(hi[u] + off) = make_uint4(hp[u][0], hp[u][1], hp[u][2], hp[u][3]);
+      *reinterpret_cast<uint4 *>(lo[u] + off) = make_uint4(lp[u][0], lp[u][1], lp[u][2], lp[u][3]);
     }
   }
   umma::fence_async_smem();
@@ -643,9 +670,10 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       }
     }
     float dq[16], pr[16];
+    const float sem = scale * emI;
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      dq[r] = scale * E[r] * emI * bq[r] + E[r] * in[r];
+      dq[r] = E[r] * fmaf(sem, bq[r], in[r]);
       dgc[r] = dq[r] * qh[r];
       pr[r] = dgc[r];
     }
@@ -657,9 +685,15 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     const float tot = red[(4 * I) * 16 + (lane & 15)] + red[(4 * I + 1) * 16 + (lane & 15)] +
                       red[(4 * I + 2) * 16 + (lane & 15)] + red[(4 * I + 3) * 16 + (lane & 15)];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const float rd = __shfl_sync(0xffffffffu, tot, r);
-      dqs[(16 * I + r) * D + c] = __float2bfloat16_rn((dq[r] - qh[r] * rd) * sv.rq[16 * I + r]);
+    for (int r4 = 0; r4 < 16; r4 += 4) {
+      float rq4[4];
+      lds4(sv.rq + 16 * I + r4, rq4);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = r4 + u;
+        const float rd = __shfl_sync(0xffffffffu, tot, r);
+        dqs[(16 * I + r) * D + c] = __float2bfloat16_rn((dq[r] - qh[r] * rd) * rq4[u]);
+      }
     }
   }
 
@@ -684,9 +718,14 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       }
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const int i = 16 * I + r;
-      dkt[r] = -sv.beta[i] * E[r] * emI * bk[r] + E[r] * dkt[r];
+    for (int r4 = 0; r4 < 16; r4 += 4) {
+      float b4[4];
+      lds4(sv.beta + 16 * I + r4, b4);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = r4 + u;
+        dkt[r] = E[r] * fmaf(-b4[u] * emI, bk[r], dkt[r]);
+      }
     }
   }
   umma::fence_async_smem();  // the dq rows, for the TMA store
@@ -769,9 +808,15 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     const float tot = red[(4 * I) * 16 + (lane & 15)] + red[(4 * I + 1) * 16 + (lane & 15)] +
                       red[(4 * I + 2) * 16 + (lane & 15)] + red[(4 * I + 3) * 16 + (lane & 15)];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const float rd = __shfl_sync(0xffffffffu, tot, r);
-      dks[(16 * I + r) * D + c] = __float2bfloat16_rn((dk[r] - kh[r] * rd) * sv.rk[16 * I + r]);
+    for (int r4 = 0; r4 < 16; r4 += 4) {
+      float rk4[4];
+      lds4(sv.rk + 16 * I + r4, rk4);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = r4 + u;
+        const float rd = __shfl_sync(0xffffffffu, tot, r);
+        dks[(16 * I + r) * D + c] = __float2bfloat16_rn((dk[r] - kh[r] * rd) * rk4[u]);
+      }
     }
   }
 
@@ -812,21 +857,26 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     const float A = gsc[0], bias = gsc[D + c];
     float dA = 0.f, ddt = 0.f;
     bf16 *dgsm = dqs;  // dg rows, [64][128]
-#pragma unroll 4
-    for (int r = 15; r >= 0; --r) {
-      const int i = 16 * I + r;
-      run += dgs[r * NT + tid];
-      const float gv = __bfloat162float(gs[(r >> 1) * 2 * NT + 2 * tid + (r & 1)]) + bias;
-      // sigmoid and softplus from one exponential, t = e^-|g|
-      const float t = __expf(-fabsf(gv));
-      const float inv = __fdividef(1.f, 1.f + t);
-      const float sg = gv >= 0.f ? inv : t * inv;
-      const float sp = fmaxf(gv, 0.f) + log1p_unit_warp(t);
-      const float dgv = run * (-A) * sg;
-      dgsm[i * D + c] = __float2bfloat16_rn(dgv);
-      if (i < len) {
-        dA = fmaf(run, -A * sp, dA);
-        ddt += dgv;
+#pragma unroll 2
+    for (int r2 = 7; r2 >= 0; --r2) {
+      // the g rows 2 r2 (low half) and 2 r2 + 1 (high half), one load
+      const uint32_t gp = *reinterpret_cast<const uint32_t *>(gs + r2 * 2 * NT + 2 * tid);
+#pragma unroll
+      for (int e = 1; e >= 0; --e) {
+        const int r = 2 * r2 + e, i = 16 * I + r;
+        run += dgs[r * NT + tid];
+        const float gv = (e ? bf_hi(gp) : bf_lo(gp)) + bias;
+        // sigmoid and softplus from one exponential, t = e^-|g|
+        const float t = __expf(-fabsf(gv));
+        const float inv = __fdividef(1.f, 1.f + t);
+        const float sg = gv >= 0.f ? inv : t * inv;
+        const float sp = fmaxf(gv, 0.f) + log1p_unit_warp(t);
+        const float dgv = run * (-A) * sg;
+        dgsm[i * D + c] = __float2bfloat16_rn(dgv);
+        if (i < len) {
+          dA = fmaf(run, -A * sp, dA);
+          ddt += dgv;
+        }
       }
     }
     dA = warp_sum(dA);

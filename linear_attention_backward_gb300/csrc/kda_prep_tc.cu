@@ -51,6 +51,8 @@ struct Smem {
   static constexpr size_t o_INVb = o_G + 64 * kGfStride * 4;  // INV diag(beta) [i][j] padded
   static constexpr size_t total = o_INVb + T64x64;
   static_assert(total + 1024 <= 233472 / 2, "two CTAs per SM");
+  static_assert(o_G % 16 == 0 && (kGfStride * 4) % 16 == 0 && (19 * D * 4) % 16 == 0,
+                "16-byte loads (lds4) of the inverse's rows and the view's rq, rk, beta");
 };
 
 // Row sums of a 16-vector over the warp's 32 lanes: lane l returns the sum
@@ -249,10 +251,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
     for (int h8 = 0; h8 < 2; ++h8) {
       float kr0[8], kr1[8];
+      float rk8[8], rq8[8];  // the rows' norms, 16-byte loads
+      lds4(sv.rk + 16 * I + 8 * h8, rk8);
+      lds4(sv.rk + 16 * I + 8 * h8 + 4, rk8 + 4);
+      lds4(sv.rq + 16 * I + 8 * h8, rq8);
+      lds4(sv.rq + 16 * I + 8 * h8 + 4, rq8 + 4);
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const int r = 8 * h8 + t, i = 16 * I + r;
-        const float rk = sv.rk[i], rq = sv.rq[i];
+        const float rk = rk8[t], rq = rq8[t];
         const float2 kv = bf2_to_f2(kraw[r]), qv = bf2_to_f2(qraw[r]);
         const float kh0 = kv.x * rk, kh1 = kv.y * rk, qh0 = qv.x * rq, qh1 = qv.y * rq;
         const float d0 = g0[r] - g0[7], d1 = g1[r] - g1[7];
@@ -347,9 +354,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   // go to HBM while that product runs (it reads only the shared tile)
   for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
     const int i = e8 >> 3, j0 = (e8 & 7) * 8;
-    float x[8];
+    float x[8], b8[8];
+    lds4(Gf + i * kGfStride + j0, x);
+    lds4(Gf + i * kGfStride + j0 + 4, x + 4);
+    lds4(sv.beta + j0, b8);
+    lds4(sv.beta + j0 + 4, b8 + 4);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) x[u] = Gf[i * kGfStride + j0 + u] * sv.beta[j0 + u];
+    for (int u = 0; u < 8; ++u) x[u] *= b8[u];
     pstore8(INVb, i, j0, 64, x);
   }
   umma::fence_async_smem();
@@ -370,11 +381,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   }
   for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
     const int i = e8 >> 3, j0 = (e8 & 7) * 8;
-    float x[8];
+    float g8[8], x[8], b8[8];
+    lds4(Gf + i * kGfStride + j0, g8);
+    lds4(Gf + i * kGfStride + j0 + 4, g8 + 4);
+    lds4(sv.beta + j0, b8);
+    lds4(sv.beta + j0 + 4, b8 + 4);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) x[u] = Gf[i * kGfStride + j0 + u] * sv.beta[j0 + u];
+    for (int u = 0; u < 8; ++u) x[u] = g8[u] * b8[u];
     const uint32_t off = umma::core_off(i, j0, 64);
-    st16_bf(unit + kPrepINV + off, Gf + i * kGfStride + j0);
+    st16_bf(unit + kPrepINV + off, g8);
     st16_bf(unit + kPrepINVb + off, x);
   }
   mma_wait();

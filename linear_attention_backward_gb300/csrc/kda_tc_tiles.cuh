@@ -48,6 +48,17 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t *>(&h);
 }
+// Four consecutive fp32 values from shared memory, one 16-byte load (p must be
+// 16-byte aligned); used for per-row vectors such as the row norms and beta,
+// which every lane of a warp reads at the same address
+__device__ __forceinline__ void lds4(const float *p, float *v) {
+  const float4 t = *reinterpret_cast<const float4 *>(p);
+  v[0] = t.x;
+  v[1] = t.y;
+  v[2] = t.z;
+  v[3] = t.w;
+}
+
 // 8 fp32 -> one 16-byte row of a packed core tile (global or shared)
 __device__ __forceinline__ void st16_bf(void *dst, const float *v) {
   uint4 u;
@@ -159,12 +170,13 @@ __device__ __forceinline__ void wg_core(float (&acc)[NF][4], const void *A, int 
     if (k0 + 16 < kdim) load(k0 + 16, cur ^ 1);
     uint32_t a[4] = {af[cur][0], af[cur][1], af[cur][2], af[cur][3]};
     if (kscale != nullptr) {
-      const int c = k0 + 2 * (lane & 3);
-      const float s0 = kscale[c], s1 = kscale[c + 1], s8 = kscale[c + 8], s9 = kscale[c + 9];
-      a[0] = scale_pair(a[0], s0, s1);
-      a[1] = scale_pair(a[1], s0, s1);
-      a[2] = scale_pair(a[2], s8, s9);
-      a[3] = scale_pair(a[3], s8, s9);
+      const int c = k0 + 2 * (lane & 3);  // even: 8-byte pairs (kscale is 8-byte aligned)
+      const float2 s01 = *reinterpret_cast<const float2 *>(kscale + c);
+      const float2 s89 = *reinterpret_cast<const float2 *>(kscale + c + 8);
+      a[0] = scale_pair(a[0], s01.x, s01.y);
+      a[1] = scale_pair(a[1], s01.x, s01.y);
+      a[2] = scale_pair(a[2], s89.x, s89.y);
+      a[3] = scale_pair(a[3], s89.x, s89.y);
     }
 #pragma unroll
     for (int f = 0; f < NF; f += 2) {
@@ -211,17 +223,23 @@ __device__ inline void inverse_inplace(float *Gf, const float *beta, float *tbuf
     float x[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
+      // x_r = e_r - beta_r sum_{j < r} G_rj x_j, the row's G entries by
+      // 16-byte loads (rows are 16-byte aligned: kGfStride = 68)
       const float br = beta[o + r];
       const float *grow = Gf + (o + r) * LG + o;
-      float s0 = (r == col) ? 1.f : 0.f, s1 = 0.f;
+      float g16[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (4 * q < r) lds4(grow + 4 * q, g16 + 4 * q);
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
       for (int j = 0; j < r; ++j) {
         if (j & 1)
-          s1 = fmaf(-br * grow[j], x[j], s1);
+          s1 = fmaf(g16[j], x[j], s1);
         else
-          s0 = fmaf(-br * grow[j], x[j], s0);
+          s0 = fmaf(g16[j], x[j], s0);
       }
-      x[r] = s0 + s1;
+      x[r] = fmaf(-br, s0 + s1, (r == col) ? 1.f : 0.f);
     }
     __syncwarp();
     if (lane < 16) {
