@@ -564,8 +564,30 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / E
     e2e_ms = max_over_ranks(e2e_ms, pg, dev)
+    # the same copies without the backward, for the host link's own time per
+    # step on this machine (the link differs between boxes)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record(comp)
+    s_in.wait_event(c0)
+    s_out.wait_event(c0)
+    for i in range(E):
+        di, oi = dsets[i % 2], osets[i % 2]
+        with torch.cuda.stream(s_in):
+            for n in names_in:
+                di[n].copy_(pin[n], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for n, o in oi.items():
+                host_out[n].copy_(o, non_blocking=True)
+    comp.wait_stream(s_in)
+    comp.wait_stream(s_out)
+    c1.record(comp)
+    torch.cuda.synchronize()
+    copies_ms = max_over_ranks(c0.elapsed_time(c1) / E, pg, dev)
     e2e = {"value": job_rate(tokens, ws, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
+           "copies_only_ms_per_step": copies_ms,
            "steps": E, "pipeline": "H2D / backward / D2H on three streams, two device "
                                    "buffer sets, every step's inputs up and gradients down"}
 
