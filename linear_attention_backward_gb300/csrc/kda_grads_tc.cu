@@ -141,25 +141,6 @@ __device__ __forceinline__ int col_p9c(int X) { return X == 0 ? 0 : (X == 1 ? 16
 // row of the interleaved dMqk | dA tile holding row i of dMqk (side 0) or dA (side 1)
 __device__ __forceinline__ int dma_row(int i, int side) { return 32 * (i >> 4) + 16 * side + (i & 15); }
 
-// Row sums over the warp's 32 lanes for the thread's 16 rows: lanes l and
-// l + 16 return the sum of row l (31 shuffles); v is consumed.
-__device__ __forceinline__ float rows16_sum(float (&v)[16]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int r = 0; r < 16; ++r) v[r] += __shfl_xor_sync(0xffffffffu, v[r], 16);
-#pragma unroll
-  for (int s = 8; s >= 1; s >>= 1) {
-    const bool up = (lane & s) != 0;
-#pragma unroll
-    for (int k = 0; k < s; ++k) {
-      const float send = up ? v[k] : v[k + s];
-      const float keep = up ? v[k + s] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-    }
-  }
-  return v[0];
-}
-
 // prep in the (channel, 16-row block) mapping; E kept in registers.  The row
 // norms and the block factors (em, egm, F, gT) come with the prep kernel's
 // operand block; here only the thread's own gate running sum (for E) and the
@@ -383,13 +364,19 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   cp_async_wait_all();                 // row-major S / dS, if any
   ok = umma::mbar_wait(lbar, 0, lim_ld) && ok;  // v, dO, S, dS, kr^T
   if (len < CHUNK) {
-    // a sequence's partial last chunk: the dO boxes' rows past it hold the
-    // next sequence's rows; zero them (a row's 128 bytes stay within the row)
+    // a sequence's partial last chunk: the dO and v boxes' rows past it hold
+    // the next sequence's rows; zero them (a dO row's 128 bytes stay within
+    // the row; v rows are row-major, 256 bytes)
     for (int e = tid; e < 2 * 64 * 8; e += NT) {
       const int row = (e >> 3) & 63;
       if (row >= len)
         *reinterpret_cast<uint4 *>(stk + (e >> 9) * SM::kStk + row * 128 + (e & 7) * 16) =
             make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int e = tid; e < 64 * 16; e += NT) {
+      const int row = e >> 4;
+      if (row >= len)
+        *reinterpret_cast<uint4 *>(Ut + row * 256 + (e & 15) * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   umma::fence_async_smem();
@@ -405,9 +392,8 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   float acc[16];
   tld16(tbase, 0, acc);
 #pragma unroll
-  for (int r = 0; r < 16; ++r)  // v rows, row-major in U's slot (rows past the chunk: zero)
-    acc[r] = (16 * I + r < len ? __bfloat162float(reinterpret_cast<const bf16 *>(Ut)[(16 * I + r) * D + c])
-                               : 0.f) - acc[r];
+  for (int r = 0; r < 16; ++r)  // v rows, row-major in U's slot (rows past the chunk: zeroed)
+    acc[r] = __bfloat162float(reinterpret_cast<const bf16 *>(Ut)[(16 * I + r) * D + c]) - acc[r];
 #pragma unroll
   for (int q = 0; q < 2; ++q) pstore8(XrT, c, 16 * I + 8 * q, 64, acc + 8 * q);  // Xr^T[d][i]
   ok = umma::mbar_wait(pbar, 0, lim_ld) && ok;  // Mqk, INV, INVb, G
@@ -480,9 +466,9 @@ __global__ void __launch_bounds__(gtc::NT, 1)
         pr[r] = acc[r] * xr[r];
       }
     }
-    // sums over this warp's 32 channels; lane l < 16 holds row 16 I + l
+    // sums over this warp's 32 channels; lanes 2 l, 2 l + 1 hold row 16 I + l
     const float t = rows16_sum(pr);
-    if (lane < 16) red[warp * 16 + lane] = t;
+    if ((lane & 1) == 0) red[warp * 16 + (lane >> 1)] = t;
   }
   umma::fence_async_smem();
   umma::tc_fence_before();
@@ -678,7 +664,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
       pr[r] = dgc[r];
     }
     const float t = rows16_sum(pr);
-    if (lane < 16) red[warp * 16 + lane] = t;
+    if ((lane & 1) == 0) red[warp * 16 + (lane >> 1)] = t;
     umma::tc_fence_before();
     if (__syncthreads_or(!ok)) { ok = false; goto drain; }
     // lane l < 16: row 16 I + l summed over the block's 4 warps; broadcast below
@@ -792,17 +778,17 @@ __global__ void __launch_bounds__(gtc::NT, 1)
     const float egI = sv.egm[I * D + c];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
+      // dki' + dkr' = E^-1 (dki + e^(gT - m_I) dkr); dkr' alone enters dgT
       const float rE = __fdividef(1.f, E[r]);
-      const float dkip = dki[r] * rE;
-      const float dkrp = dkr[r] * egI * rE;
-      dk[r] = dkt[r] + dkip + dkrp;
-      const float dks = dkt[r] - dkip - dkrp;
-      dgc[r] = fmaf(dks, kh[r], dgc[r]);
-      colp = fmaf(dkrp, kh[r], colp);
+      const float w = dkr[r] * egI;
+      const float sk = (dki[r] + w) * rE;
+      dk[r] = dkt[r] + sk;
+      dgc[r] = fmaf(dkt[r] - sk, kh[r], dgc[r]);
+      colp = fmaf(w * rE, kh[r], colp);
       pr[r] = dk[r] * kh[r];
     }
     const float t = rows16_sum(pr);
-    if (lane < 16) red[warp * 16 + lane] = t;
+    if ((lane & 1) == 0) red[warp * 16 + (lane >> 1)] = t;
     dgT[I * D + c] += colp;
     if (__syncthreads_or(!ok)) { ok = false; goto drain; }
     const float tot = red[(4 * I) * 16 + (lane & 15)] + red[(4 * I + 1) * 16 + (lane & 15)] +

@@ -55,25 +55,6 @@ struct Smem {
                 "16-byte loads (lds4) of the inverse's rows and the view's rq, rk, beta");
 };
 
-// Row sums of a 16-vector over the warp's 32 lanes: lane l returns the sum
-// of v[l % 16] over all lanes (31 shuffles).
-__device__ __forceinline__ float half_transpose_sum(float (&v)[16]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int r = 0; r < 16; ++r) v[r] += __shfl_xor_sync(0xffffffffu, v[r], 16);
-#pragma unroll
-  for (int s = 8; s >= 1; s >>= 1) {
-    const bool up = (lane & s) != 0;
-#pragma unroll
-    for (int k = 0; k < s; ++k) {
-      const float send = up ? v[k] : v[k + s];
-      const float keep = up ? v[k + s] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-    }
-  }
-  return v[0];
-}
-
 }  // namespace ptc
 
 __global__ void __launch_bounds__(NTHREADS, 2)
@@ -173,11 +154,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       sk[r] = fmaf(kv.x, kv.x, kv.y * kv.y);
       sq[r] = fmaf(qv.x, qv.x, qv.y * qv.y);
     }
-    const float tk = half_transpose_sum(sk);
-    const float tq = half_transpose_sum(sq);
-    if (lane < 16) {
-      red[warp * 16 + lane] = tk;
-      red[128 + warp * 16 + lane] = tq;
+    const float tk = rows16_sum(sk);
+    const float tq = rows16_sum(sq);
+    if ((lane & 1) == 0) {  // lanes 2 r, 2 r + 1 hold row 16 I + r
+      red[warp * 16 + (lane >> 1)] = tk;
+      red[128 + warp * 16 + (lane >> 1)] = tq;
     }
     // gate: running sum over the block (sums local to the block)
     const float A = __expf(a_log);

@@ -59,6 +59,27 @@ __device__ __forceinline__ void lds4(const float *p, float *v) {
   v[3] = t.w;
 }
 
+// Sums over the warp's 32 lanes of each of 16 per-lane values (a row each):
+// lanes 2 r and 2 r + 1 return the sum of row r.  Four halving steps exchange
+// 8, 4, 2 and 1 values (a lane keeps the half of the rows that its bit 4, 3,
+// 2, 1 selects and sends the other), then lanes 2 r, 2 r + 1 add their two
+// partial sums: 16 shuffles in all.  v is consumed.
+__device__ __forceinline__ float rows16_sum(float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const int n = 8 >> st, s = 16 >> st;
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < n; ++k) {
+      const float send = up ? v[k] : v[k + n];
+      const float keep = up ? v[k + n] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
 // 8 fp32 -> one 16-byte row of a packed core tile (global or shared)
 __device__ __forceinline__ void st16_bf(void *dst, const float *v) {
   uint4 u;
