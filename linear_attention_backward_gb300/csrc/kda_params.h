@@ -99,13 +99,14 @@ constexpr size_t kPrepUnitBytes = kPrepSV + kPrepSVBytes;
 // the 64 rows x 128 channels of one chunk and head, row-major (256-byte rows)
 // in shared memory; rows past the tensor's end read as zero (and are not
 // written by a store).  Inputs q, k, g, v, dO; gradients dq, dk, dv, dg
-// (stored from shared memory for whole chunks).  dO_sw maps dO with boxes of
-// 64 rows x 64 channels in the 128-byte swizzled layout (umma::sw128_off),
-// which the tensor cores read as it lands.  A null tensor keeps an empty map.
+// (stored from shared memory for whole chunks).  dO_sw and v_sw map dO and v
+// with boxes of 64 rows x 64 channels in the 128-byte swizzled layout
+// (umma::sw128_off), which the tensor cores read as it lands.  A null tensor
+// keeps an empty map.
 struct TokenMaps {
   CUtensorMap q, k, g, v, dO;
   CUtensorMap dq, dk, dv, dg;
-  CUtensorMap dO_sw;
+  CUtensorMap dO_sw, v_sw;
 };
 // kda_tmap.cu: encodes the five maps; false if the driver refuses one.
 bool encode_token_maps(const KdaParams &p, TokenMaps &m);

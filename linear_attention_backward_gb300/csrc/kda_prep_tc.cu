@@ -42,15 +42,16 @@ struct Smem {
   static constexpr size_t n_view = PrepView<bf16, D>::floats;
   // extra floats: tbuf 768 (inverse), red 2 x 8 x 16 (row norms)
   static constexpr size_t n_extra = 768 + 256;
-  static constexpr size_t sz_small = (((n_view + n_extra) * 4 + 64 + 127) / 128) * 128;
+  static constexpr size_t sz_small = (((n_view + n_extra) * 4 + 64 + 1023) / 1024) * 1024;
   static constexpr size_t o_QM = sz_small;          // q^ e^(gc - m)  [i][c] padded
   static constexpr size_t o_KM = o_QM + T64x128;    // k^ e^(gc - m)  [i][c] padded
   static constexpr size_t o_KP = o_KM + T64x128;    // k^ e^(m - gc)  -> later Mqk [i][j]
-  static constexpr size_t o_V = o_KP + T64x128;     // v [j][v] packed
+  static constexpr size_t o_V = o_KP + T64x128;     // v: two 64-channel swizzled boxes [j][v]
   static constexpr size_t o_G = o_V + 16384;        // G / INV fp32 [64][68] -> later W^T
   static constexpr size_t o_INVb = o_G + 64 * kGfStride * 4;  // INV diag(beta) [i][j] padded
   static constexpr size_t total = o_INVb + T64x64;
   static_assert(total + 1024 <= 233472 / 2, "two CTAs per SM");
+  static_assert(o_V % 1024 == 0, "swizzled boxes start on 1024-byte atoms");
   static_assert(o_G % 16 == 0 && (kGfStride * 4) % 16 == 0 && (19 * D * 4) % 16 == 0,
                 "16-byte loads (lds4) of the inverse's rows and the view's rq, rk, beta");
 };
@@ -82,7 +83,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   float *red = tbuf + 768;  // [2 (k, q)][8 warps][16 rows]
   uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + (SM::n_view + SM::n_extra) * 4);
   uint64_t *rbar = mbar + 1;  // TMA boxes of the raw q, k, g rows
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 2);
+  uint64_t *vbar = mbar + 2;  // TMA boxes of the v rows
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 3);
   char *QM = smem + SM::o_QM, *KM = smem + SM::o_KM, *KP = smem + SM::o_KP;
   char *Mqk = KP;
   char *Vt = smem + SM::o_V;
@@ -93,32 +95,28 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 
   // raw q, k, g rows (row-major [64][128]) into the tile region, which the
   // tiles overwrite only after every thread has taken its rows; thread 0 issues
-  // them as soon as the barriers exist, warp 0 then allocates Tensor Memory
+  // them as soon as the barriers exist, and the v rows as two 64-channel boxes
+  // in the 128-byte swizzled layout, which the U0^T product reads MN-major as
+  // they land; warp 0 then allocates Tensor Memory
   const bf16 *Qraw = reinterpret_cast<const bf16 *>(QM);
   const bf16 *Kraw = Qraw + 64 * D, *Graw = Kraw + 64 * D;
   if (tid == 0) {
     umma::mbar_init(mbar, 1);
     umma::mbar_init(rbar, 1);
+    umma::mbar_init(vbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     umma::mbar_expect_tx(rbar, 3 * 16384u);
-    if ((p.starve & kStarvePrep) == 0u) {  // (a timeout test arms the barrier only)
+    umma::mbar_expect_tx(vbar, 16384u);
+    if ((p.starve & kStarvePrep) == 0u) {  // (a timeout test arms the barriers only)
       umma::tma_load_3d(QM, &tm.q, 0, h, (int)tok0, rbar);
       umma::tma_load_3d(QM + 16384, &tm.k, 0, h, (int)tok0, rbar);
       umma::tma_load_3d(QM + 32768, &tm.g, 0, h, (int)tok0, rbar);
+      umma::tma_load_3d(Vt, &tm.v_sw, 0, h, (int)tok0, vbar);
+      umma::tma_load_3d(Vt + 8192, &tm.v_sw, 64, h, (int)tok0, vbar);
     }
   }
   if (warp == 0) umma::tmem_alloc(tslot, 256);
   __syncthreads();
-  // v rows -> packed core tile [j][v] (the MN-major A operand of U0^T)
-  {
-    const bf16 *vg = reinterpret_cast<const bf16 *>(p.v);
-    for (int e = tid; e < 64 * (D / 8); e += NTHREADS) {
-      const int i = e >> 4, c8 = (e & 15) * 8;
-      const bool ok = i < len;
-      cp_async16(Vt + umma::core_off(i, c8, D), vg + ((tok0 + (ok ? i : 0)) * H + h) * D + c8, ok);
-    }
-    cp_async_commit();
-  }
   if (tid < CHUNK)
     sv.beta[tid] = tid < len ? __bfloat162float(reinterpret_cast<const bf16 *>(p.beta)[(tok0 + tid) * H + h])
                              : 0.f;
@@ -397,14 +395,24 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       st16_bf(unit + kPrepW + off, w + 8 * q);
     }
   }
-  cp_async_wait_all();  // v has landed
+  ok = umma::mbar_wait(vbar, 0, poll_cap(p, umma::kPollLoads)) && ok;  // v has landed
+  if (len < CHUNK) {
+    // a sequence's partial last chunk: the v boxes' rows past it hold the next
+    // sequence's rows; zero them (a row's 128 bytes stay within the row)
+    for (int e = tid; e < 2 * 64 * 8; e += NTHREADS) {
+      const int row = (e >> 3) & 63;
+      if (row >= len)
+        *reinterpret_cast<uint4 *>(Vt + (e >> 9) * 8192 + row * 128 + (e & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   umma::fence_async_smem();
   umma::tc_fence_before();
   if (__syncthreads_or(!ok)) { ok = false; goto drain; }
   // ---- U0^T = v^T (INV diag(beta))^T ;  (Mqk W)^T = W^T Mqk^T ----
   if (tid == 0) {
     umma::tc_fence_after();
-    gemm(tbase + 0, opmn(Vt, D, 0, CP), true, opk(INVb, 64), false, 64, 4, false);
+    gemm(tbase + 0, opsw_mn(Vt, 8192u), true, opk(INVb, 64), false, 64, 4, false);
     gemm(tbase + 64, opk(Wt, 64, 0, CP), false, opk(Mqk, 64), false, 64, 4, false);
     umma::mma_commit(mbar);
   }
@@ -443,9 +451,9 @@ drain:
     if (tid == 0) {
       const uint32_t lim = poll_cap(p, umma::kPollDrain);
       umma::mbar_wait(rbar, 0, lim);
+      umma::mbar_wait(vbar, 0, lim);
       if (phase > 0) umma::mbar_wait(mbar, (phase - 1) & 1, lim);
     }
-    cp_async_wait_all();
   }
   if (warp == 0) {
     __syncwarp();  // thread 0 may have drained alone: the release is warp-collective

@@ -55,7 +55,8 @@ bool encode_token_maps(const KdaParams &p, TokenMaps &m) {
   return enc(&m.q, p.q) && enc(&m.k, p.k) && enc(&m.g, p.g) && enc(&m.v, p.v) &&
          enc(&m.dO, p.dO) && enc(&m.dq, p.dq) && enc(&m.dk, p.dk) && enc(&m.dv, p.dv) &&
          enc(&m.dg, p.dg) &&
-         (p.dO == nullptr || encode(&m.dO_sw, p.dO, ntok, p.H, 64, true));
+         (p.dO == nullptr || encode(&m.dO_sw, p.dO, ntok, p.H, 64, true)) &&
+         (p.v == nullptr || encode(&m.v_sw, p.v, ntok, p.H, 64, true));
 }
 
 }  // namespace kda
