@@ -178,9 +178,10 @@ int kda_scan_segments(const kda_shape *shape);
  *            kda_workspace_bytes(shape) bytes, 256-byte aligned (the layout
  *            kda_bwd uses; the per-chunk operand blocks of the chunk-parallel
  *            prep live there).  Other shapes need none (ws may be NULL).
- * bf16 with K = V = 128 runs the chunk-parallel prep (which also forms the
- * read-out operands and so needs q) and the forward tcgen05 state scan,
- * context-parallel where kda_scan_segments() > 0; q is then required.  Other
+ * bf16 with K = V = 128 runs the chunk-parallel prep (its pair blocks read
+ * q; it writes only the scans' operands, not the read-out's or the gradient
+ * kernel's) and the forward tcgen05 state scan, context-parallel where
+ * kda_scan_segments() > 0; q is then required.  Other
  * shapes run the per-band scan and ignore q (bf16 K = V = 64 included: its
  * row-major 64 x 64 states are packed into the padded layout by kda_bwd). */
 kda_status kda_fwd_states(const kda_shape *shape, const void *q, const void *k,

@@ -347,6 +347,7 @@ kda_status kda_fwd_states(const kda_shape *shape, const void *q, const void *k, 
     p.dA_part = reinterpret_cast<float *>(w + dA_part_offset(shape));
     kda::TokenMaps tm{};  // left zero when there are no tokens (no kernel then reads it)
     if (!kda::encode_token_maps(p, tm)) return KDA_ERR_CUDA;
+    p.prep_mode = kda::kPrepStates;  // the scans' operands only
     return from_cuda(forward_states_tc(p, shape, w, tm, cs));
   }
   // other dtypes and head sizes: the per-band scan (row-major states; no
@@ -415,6 +416,7 @@ kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const v
   p.hT = hT;
   p.states = w;  // packed chunk states, as kda_bwd keeps them
   p.dA_part = reinterpret_cast<float *>(w + dA_part_offset(shape));
+  p.prep_mode = kda::kPrepReadout;  // the scans' operands and QE^T, scale * Mqk
   kda::TokenMaps tm{};  // left zero when there are no tokens (no kernel then reads it)
   if (!kda::encode_token_maps(p, tm)) return KDA_ERR_CUDA;
   // 1. per-chunk operands, 2. forward state scan (S_n of every chunk, hT),

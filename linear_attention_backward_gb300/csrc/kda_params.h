@@ -49,7 +49,14 @@ struct KdaParams {
   // load barrier but issue none of its copies, so that its bounded wait runs
   // out; `poll_limit` (0 = the kernels' defaults) caps every bounded wait.
   uint32_t starve, poll_limit;
+  // What the prep kernel writes beyond the scans' operands (W^T, kr^T, U0^T,
+  // gT): kPrepAll (0) everything, the gradient kernel's tiles and factors
+  // included; kPrepReadout (1) also QE^T and scale * Mqk, which the forward
+  // read-out needs; kPrepStates (2) nothing more (the chunk states alone).
+  uint32_t prep_mode;
 };
+
+constexpr uint32_t kPrepAll = 0, kPrepReadout = 1, kPrepStates = 2;
 
 constexpr uint32_t kStarvePrep = 1, kStarveScan = 2, kStarveGrads = 4, kStarveOut = 8;
 

@@ -58,6 +58,9 @@ struct Smem {
 
 }  // namespace ptc
 
+// kMode: what the kernel writes beyond the scans' operands (kPrepAll,
+// kPrepReadout, kPrepStates; kda_params.h), one instance each
+template <uint32_t kMode>
 __global__ void __launch_bounds__(NTHREADS, 2)
     kda_prep_tc_kernel(KdaParams p, const __grid_constant__ TokenMaps tm, char *prep) {
   using namespace ptc;
@@ -221,8 +224,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   // the block factors and the row norms for the gradient kernel (one 8 KB span
   // of the view: e^(m_I), e^(gT - m_I), e^(m_I - m_J), gT, 1/|q|, 1/|k|)
   static_assert(19 * D + 128 - 4 * D == kPrepSVBytes / 4, "factor span");
-  for (int e = tid; e < (int)(kPrepSVBytes / 16); e += NTHREADS)
-    reinterpret_cast<uint4 *>(unit + kPrepSV)[e] = reinterpret_cast<const uint4 *>(sv.em)[e];
+  constexpr bool grad_tiles = kMode == kPrepAll, readout = kMode != kPrepStates;
+  if constexpr (grad_tiles)
+    for (int e = tid; e < (int)(kPrepSVBytes / 16); e += NTHREADS)
+      reinterpret_cast<uint4 *>(unit + kPrepSV)[e] = reinterpret_cast<const uint4 *>(sv.em)[e];
   // ---- decay-scaled tiles; kr^T goes straight to HBM ----
   {
     const float eg0 = sv.egm[I * D + c], eg1 = sv.egm[I * D + c + 1];
@@ -315,18 +320,22 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   }
   __syncthreads();
   // G for the gradient kernel (packed 64 x 64 tile; the inverse overwrites Gf)
-  for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
-    const int i = e8 >> 3, j0 = (e8 & 7) * 8;
-    st16_bf(unit + kPrepG + umma::core_off(i, j0, 64), Gf + i * kGfStride + j0);
+  if constexpr (grad_tiles) {
+    for (int e8 = tid; e8 < 64 * 8; e8 += NTHREADS) {
+      const int i = e8 >> 3, j0 = (e8 & 7) * 8;
+      st16_bf(unit + kPrepG + umma::core_off(i, j0, 64), Gf + i * kGfStride + j0);
+    }
+    __syncthreads();
   }
-  __syncthreads();
   // scale * Mqk for the gradient kernel, stored by the warps the inverse's
   // diagonal phase leaves idle
   inverse_inplace(Gf, sv.beta, tbuf, [&](int w4) {
-    for (int e8 = 32 * w4 + lane; e8 < 64 * 8; e8 += 32 * (NWARPS - 4)) {
-      const int i = e8 >> 3, j0 = (e8 & 7) * 8;
-      *reinterpret_cast<uint4 *>(unit + kPrepMqk + umma::core_off(i, j0, 64)) =
-          *reinterpret_cast<const uint4 *>(Mqk + pcore_off(i, j0, 64));
+    if constexpr (readout) {
+      for (int e8 = 32 * w4 + lane; e8 < 64 * 8; e8 += 32 * (NWARPS - 4)) {
+        const int i = e8 >> 3, j0 = (e8 & 7) * 8;
+        *reinterpret_cast<uint4 *>(unit + kPrepMqk + umma::core_off(i, j0, 64)) =
+            *reinterpret_cast<const uint4 *>(Mqk + pcore_off(i, j0, 64));
+      }
     }
   });
   // INV diag(beta) as the W^T product's operand first; INV and INV diag(beta)
@@ -367,9 +376,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     lds4(sv.beta + j0 + 4, b8 + 4);
 #pragma unroll
     for (int u = 0; u < 8; ++u) x[u] = g8[u] * b8[u];
-    const uint32_t off = umma::core_off(i, j0, 64);
-    st16_bf(unit + kPrepINV + off, g8);
-    st16_bf(unit + kPrepINVb + off, x);
+    if constexpr (grad_tiles) {
+      const uint32_t off = umma::core_off(i, j0, 64);
+      st16_bf(unit + kPrepINV + off, g8);
+      st16_bf(unit + kPrepINVb + off, x);
+    }
   }
   mma_wait();
   const int ch = tid & 127, gq = tid >> 7;  // TMEM lane (channel) and 32-column group
@@ -413,7 +424,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   if (tid == 0) {
     umma::tc_fence_after();
     gemm(tbase + 0, opsw_mn(Vt, 8192u), true, opk(INVb, 64), false, 64, 4, false);
-    gemm(tbase + 64, opk(Wt, 64, 0, CP), false, opk(Mqk, 64), false, 64, 4, false);
+    if constexpr (readout)
+      gemm(tbase + 64, opk(Wt, 64, 0, CP), false, opk(Mqk, 64), false, 64, 4, false);
     umma::mma_commit(mbar);
   }
   mma_wait();
@@ -424,6 +436,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       st16_bf(unit + kPrepU0 + umma::core_off(ch, 32 * gq + 8 * q, 64), a + 8 * q);
+    if constexpr (!readout) goto drain;
     tld32(tbase, 64, a);
     const float em0 = sv.em[(2 * gq) * D + ch], em1 = sv.em[(2 * gq + 1) * D + ch];
 #pragma unroll
@@ -463,7 +476,9 @@ drain:
 }
 
 cudaError_t prep_tc_launch(const KdaParams &p, const TokenMaps &tm, void *prep, cudaStream_t st) {
-  auto kfn = kda_prep_tc_kernel;
+  auto kfn = p.prep_mode == kPrepStates    ? kda_prep_tc_kernel<kPrepStates>
+             : p.prep_mode == kPrepReadout ? kda_prep_tc_kernel<kPrepReadout>
+                                           : kda_prep_tc_kernel<kPrepAll>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)ptc::Smem::total);
   if (e != cudaSuccess) return e;
