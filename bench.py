@@ -71,11 +71,11 @@ def launches_per_step(shape, cu, forward=False):
 # kernel sources it was taken from; a changed kernel reports null until it
 # is measured again.
 NCU_TRAFFIC = {
-    # ncu on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read 841.6 MB +
-    # write 244.6 MB (profiles/traffic_main_b1_bf16.md), scaled by 4 to the main
+    # ncu on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read 841.4 MB +
+    # write 244.8 MB (profiles/traffic_main_b1_bf16.md), scaled by 4 to the main
     # workload's 16384 chunk-heads (the kernel's traffic is proportional to them)
-    "kda_grads_tc_kernel": {"sha": "06e25f80d14d9f5c", "workload": "main_bf16",
-                            "bytes_per_launch": 4344632320},
+    "kda_grads_tc_kernel": {"sha": "f90df49f7417aaf0", "workload": "main_bf16",
+                            "bytes_per_launch": 4344904704},
 }
 
 KERNEL_SOURCES = {
