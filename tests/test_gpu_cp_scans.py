@@ -98,6 +98,34 @@ def test_cp_two_chains_per_sm(monkeypatch):
         assert rel_l2(g_cp[k].double().cpu().numpy(), g_one[k].double().cpu().numpy()) < 1e-2, k
 
 
+def test_cp_fwd_states_two_chains_per_sm_match_the_backward():
+    # kda_fwd_states at the two-per-SM split (32 sequence-heads, 4 segments),
+    # with the prep kernel writing the scans' operands only: its packed states
+    # match the ones kda_bwd recomputes (the same scans on the full prep
+    # kernel's operands) and the oracle's
+    w = wl.custom("cp", B=1, T=64 * 16 + 37, H=32, K=128, V=128, dtype="bf16", with_h0=True,
+                  with_dhT=True)
+    x = wl.make_inputs(w, seed=39)
+    d = to_dev(x)
+    shape = kda.make_shape(d["q"], d["v"])
+    assert kda.scan_segments(shape) == 4
+    states, hT = kda.fwd_states(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"],
+                                want_hT=True)
+    torch.cuda.synchronize()
+    assert kda.get_device_status() == 0
+    g, _ = gpu_bwd(x)
+    assert kda.get_device_status() == 0
+    n = kda.num_chunk_slots(shape) * 32 * 128 * 128  # elements
+    internal = g["_workspace"][:2 * n].view(torch.bfloat16)
+    assert rel_l2(states.reshape(-1).double().cpu().numpy(),
+                  internal.double().cpu().numpy()) < 1e-3
+    cs, hT_ref = oracle_states(x)
+    slots = np.concatenate(slot_index(x))
+    got = unpack_core_tiles(states).double().cpu().numpy()[slots]
+    assert rel_l2(got, cs) < 1e-2
+    assert rel_l2(hT.double().cpu().numpy(), hT_ref) < 1e-2
+
+
 def test_cp_long_segments_eight_way():
     # 128 chunks, 2 chains: 8 segments of 16 chunks and 6 combine steps
     w = wl.custom("cp", B=1, T=8192, H=2, K=128, V=128, dtype="bf16", with_h0=True,
