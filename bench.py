@@ -57,13 +57,18 @@ KERNEL_NAMES = {"prep": "kda_prep_tc_kernel", "scan": "kda_scan_tc_kernel",
                 "grads": "kda_grads_tc_kernel", "reduce": "kda_dalog_reduce_kernel"}
 # kernels of one kda_bwd call: prep, scans, gradients, dA_log reduction; a
 # varlen call adds the sequence-order kernel, context-parallel scans (few
-# (sequence, head) chains) add their combine kernel and second scan pass
+# (sequence, head) chains) add their combine kernel and second scan pass, and
+# the tensor-core path (bf16, K = V = 128) its two exact kernels for gates
+# past the block range (one after the prep, one after the gradients; each
+# walks the chunk flags and works only on flagged chunks)
 LAUNCHES_PER_STEP = 4
 
 
 def launches_per_step(shape, cu, forward=False):
     import linear_attention_backward_gb300 as kda
     n = (3 if forward else LAUNCHES_PER_STEP) + (0 if cu is None else 1)
+    if shape.dtype == kda.KDA_BF16 and shape.K == 128:
+        n += 1 if forward else 2
     return n + (2 if kda.scan_segments(shape) > 0 else 0)
 
 # DRAM traffic per launch of the gradient kernel from ncu

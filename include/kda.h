@@ -59,9 +59,9 @@
  *    stream, except kda_get_device_status which synchronises its stream.
  *  - Errors: argument errors are returned before anything is launched.  A
  *    failed launch returns KDA_ERR_CUDA.  Errors found on the device (a bad
- *    cu_seqlens table, a gate beyond the block range, a bounded wait that
- *    gave up) are recorded in a device status word read by
- *    kda_get_device_status; the outputs of that call are then not valid.
+ *    cu_seqlens table, a gate beyond the block range on the fp32 kernels, a
+ *    bounded wait that gave up) are recorded in a device status word read
+ *    by kda_get_device_status; the outputs of that call are then not valid.
  *  - Bounded waits.  Every wait of a kernel on a copy or a tensor-core
  *    product polls a bounded number of times (2^24 polls for copies, 2^20
  *    for products).  A CTA whose wait gives up records KDA_ERR_TIMEOUT,
@@ -96,10 +96,16 @@ typedef enum {
   KDA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
   KDA_ERR_DEVICE_ARG = 6,  /* the device found a bad cu_seqlens table */
   KDA_ERR_TOO_LARGE = 7,   /* kda_bwd_noalloc: problem needs more than its fixed scratch */
-  KDA_ERR_GATE_RANGE = 8   /* the device found a channel whose gate log-decay over the
-                              7 or 8 tokens on either side of a 16-row block's reference
-                              row exceeds 88 nats: the block factors e^x leave the fp32
-                              range, and the outputs of that call are not valid */
+  KDA_ERR_GATE_RANGE = 8   /* fp32 inputs (and the comparison switches of the README)
+                              only: the device found a channel whose gate log-decay over
+                              the 7 or 8 tokens on either side of a 16-row block's
+                              reference row exceeds 88 nats, where the block factors e^x
+                              leave the fp32 range, or a chunk in which every channel
+                              decays by more than 5 nats per token (6 for bf16), where
+                              the block-factored dg misses the tolerance; the outputs of
+                              that call are not valid.  bf16 inputs take such chunks
+                              through exact kernels (one exponential per row pair)
+                              instead */
 } kda_status;
 
 typedef enum { KDA_FP32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -122,8 +128,10 @@ int64_t kda_num_chunk_slots(const kda_shape *shape);
  * state gradients dS (same size), per-chunk dA_log and ddt_bias partials
  * ([slots, H] and [slots, H, K] fp32) and, for bf16
  * with K = V = 128, the per-chunk operand blocks of the tensor-core scans
- * (107008 bytes per slot and head) and, where kda_scan_segments() > 0, the
- * segment boundary tiles of the context-parallel scans.  For bf16 with
+ * (107008 bytes per slot and head), where kda_scan_segments() > 0 the
+ * segment boundary tiles of the context-parallel scans, and a 4-byte flag
+ * per slot and head (the chunks whose gate passes the block factors' range,
+ * which exact kernels then redo).  For bf16 with
  * K = V = 64 it is the workspace of the 128-channel shape plus the padded
  * copies of the inputs, gradients, h0 / dh_T / dh0, the gate bias and given
  * states.  Returns 0 on a bad shape. */
@@ -174,16 +182,19 @@ int kda_scan_segments(const kda_shape *shape);
  *            them in the same layout.
  *   h0     : nullable (zero initial state), fp32 [N, H, K, V].
  *   hT     : nullable OUT fp32 [N, H, K, V]: the final state of each sequence.
- *   ws     : bf16 with K = V = 128: DEVICE workspace of at least
- *            kda_workspace_bytes(shape) bytes, 256-byte aligned (the layout
- *            kda_bwd uses; the per-chunk operand blocks of the chunk-parallel
- *            prep live there).  Other shapes need none (ws may be NULL).
+ *   ws     : bf16: DEVICE workspace of at least kda_workspace_bytes(shape)
+ *            bytes, 256-byte aligned (the layout kda_bwd uses; the per-chunk
+ *            operand blocks of the chunk-parallel prep live there).
+ *            Required for K = V = 128; for K = V = 64 it selects the
+ *            tensor-core path below.  fp32 needs none (ws may be NULL).
  * bf16 with K = V = 128 runs the chunk-parallel prep (its pair blocks read
  * q; it writes only the scans' operands, not the read-out's or the gradient
  * kernel's) and the forward tcgen05 state scan, context-parallel where
- * kda_scan_segments() > 0; q is then required.  Other
- * shapes run the per-band scan and ignore q (bf16 K = V = 64 included: its
- * row-major 64 x 64 states are packed into the padded layout by kda_bwd). */
+ * kda_scan_segments() > 0; q is then required.  bf16 K = V = 64 with a
+ * workspace and q runs the same kernels on zero-padded 128-channel copies and
+ * returns the states' 64 x 64 corners row-major (kda_bwd packs them back into
+ * the padded layout).  fp32, and bf16 K = V = 64 without a workspace, run the
+ * per-band scan and ignore q. */
 kda_status kda_fwd_states(const kda_shape *shape, const void *q, const void *k,
                           const void *v, const void *g, const void *beta,
                           const float *A_log, const float *dt_bias, const float *h0,
@@ -310,7 +321,7 @@ kda_status kda_check_cu_seqlens_host(const int32_t *cu_seqlens, int num_seqs,
 /* Static description of a status code. */
 const char *kda_status_str(kda_status status);
 
-/* Version of this ABI (increments on any signature change). */
+/* Version of this ABI (increments on any signature or workspace-layout change). */
 int kda_abi_version(void);
 
 #ifdef __cplusplus

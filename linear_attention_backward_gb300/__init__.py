@@ -157,9 +157,9 @@ def fwd_states(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None,
     For bf16 with K = V = 128 every K x V tile is in packed core-matrix order
     (see ``kda_fwd_states`` in include/kda.h; ``unpack_core_tiles`` in the
     tests turns it row-major), the layout :func:`bwd` takes back as
-    ``states``; ``workspace`` (uint8 CUDA tensor of at least
-    ``workspace_bytes``) is allocated when not given.  Other shapes return
-    row-major tiles and use no workspace."""
+    ``states``.  For bf16 (K = V = 128 or 64) ``workspace`` (uint8 CUDA
+    tensor of at least ``workspace_bytes``) is allocated when not given.
+    Other shapes return row-major tiles and use no workspace."""
     shape = make_shape(k, v, cu_seqlens=cu_seqlens, scale=scale, l2_eps=l2_eps)
     B, T, H, K = k.shape
     V = v.shape[-1]
@@ -167,7 +167,7 @@ def fwd_states(q, k, v, g, beta, A_log, h0=None, *, cu_seqlens=None, scale=None,
         states = torch.empty((num_chunk_slots(shape), H, K, V), dtype=k.dtype, device=k.device)
     if want_hT and hT is None:
         hT = torch.empty((_nseq(B, cu_seqlens), H, K, V), dtype=torch.float32, device=k.device)
-    tc = k.dtype == torch.bfloat16 and K == 128 and V == 128
+    tc = k.dtype == torch.bfloat16 and K == V and K in (64, 128)
     if workspace is None and tc:
         workspace = torch.empty((workspace_bytes(shape),), dtype=torch.uint8, device=k.device)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -153,7 +153,8 @@ size_t cp_bytes(const kda_shape *s) {
 
 // Workspace layout: states | dS | dA_log partials [slots, H] | ddt_bias
 // partials [slots, H, K] | per-chunk operand blocks (tcgen05 path) |
-// boundary tiles of the context-parallel scans.
+// boundary tiles of the context-parallel scans | range flags [slots, H]
+// (tcgen05 path: the chunks whose gate the exact kernels of kda_range.cu take).
 size_t dA_part_offset(const kda_shape *s) { return 2 * states_bytes(s); }
 size_t ddt_part_offset(const kda_shape *s) {
   return dA_part_offset(s) + round_up((size_t)slots_of(s) * s->H * sizeof(float));
@@ -162,6 +163,10 @@ size_t prep_offset(const kda_shape *s) {
   return ddt_part_offset(s) + round_up((size_t)slots_of(s) * s->H * s->K * sizeof(float));
 }
 size_t cp_offset(const kda_shape *s) { return prep_offset(s) + prep_bytes(s); }
+size_t flags_offset(const kda_shape *s) { return cp_offset(s) + cp_bytes(s); }
+size_t flags_bytes(const kda_shape *s) {
+  return tc_state_path(s) ? round_up((size_t)slots_of(s) * s->H * sizeof(int32_t)) : 0;
+}
 
 // The forward half shared by kda_fwd and kda_fwd_states on the tcgen05 path:
 // per-chunk operands into the workspace, then the forward state scan (whole
@@ -173,7 +178,9 @@ cudaError_t forward_states_tc(kda::KdaParams &p, const kda_shape *shape, char *w
                               const kda::TokenMaps &tm, cudaStream_t cs) {
   void *prep = w + prep_offset(shape);
   p.prep = static_cast<const char *>(prep);
+  p.range_flags = reinterpret_cast<int32_t *>(w + flags_offset(shape));
   cudaError_t e = kda::prep_tc_launch(p, tm, prep, cs);
+  if (e == cudaSuccess) e = kda::range_prep_launch(p, prep, cs);
   p.role_base = 0;
   p.states_packed = 1;
   const int cp = cp_segments_used(shape);
@@ -221,7 +228,7 @@ struct Pad64 {
 Pad64 pad64_layout(const kda_shape *s) {
   const kda_shape ps = padded_shape(s);
   Pad64 L;
-  size_t o = round_up(cp_offset(&ps) + cp_bytes(&ps));
+  size_t o = round_up(flags_offset(&ps) + flags_bytes(&ps));
   L.inner = o;
   const size_t tok = round_up((size_t)s->B * s->T * s->H * 128 * 2);
   size_t *toks[] = {&L.q, &L.k, &L.v, &L.g, &L.dO, &L.dq, &L.dk, &L.dv, &L.dg};
@@ -258,7 +265,7 @@ kda_status check_ws(const kda_shape *shape, const void *ws, size_t ws_bytes) {
 
 extern "C" {
 
-int kda_abi_version(void) { return 6; }
+int kda_abi_version(void) { return 7; }
 
 const char *kda_status_str(kda_status st) {
   switch (st) {
@@ -301,7 +308,7 @@ int kda_scan_segments(const kda_shape *shape) {
 size_t kda_workspace_bytes(const kda_shape *shape) {
   if (check_shape(shape) != KDA_OK) return 0;
   if (pad64_shape(shape)) return pad64_layout(shape).total;  // also covers the mma.sync path
-  return cp_offset(shape) + cp_bytes(shape);
+  return flags_offset(shape) + flags_bytes(shape);
 }
 
 kda_status kda_check_cu_seqlens_host(const int32_t *cu, int num_seqs, int total_T) {
@@ -338,6 +345,36 @@ kda_status kda_fwd_states(const kda_shape *shape, const void *q, const void *k, 
   p.h0 = h0;
   p.states = states;
   p.hT = hT;
+  if (pad64_path(shape) && ws != nullptr && (q != nullptr || !tokens)) {
+    // bf16 K = V = 64 with a workspace: the 128-channel prep and forward scan
+    // on padded copies, then the states' 64 x 64 corners (row-major) and hT
+    // cut back out
+    st = check_ws(shape, ws, ws_bytes);
+    if (st != KDA_OK) return st;
+    const kda_shape ps = padded_shape(shape);
+    const Pad64 L = pad64_layout(shape);
+    char *w = static_cast<char *>(ws);
+    const int64_t rows = (int64_t)shape->B * shape->T * shape->H;
+    const int64_t nst = (int64_t)num_seqs_of(shape) * shape->H;
+    cudaError_t e = cudaSuccess;
+    const void *src[] = {q, k, v, g};
+    const size_t dst[] = {L.q, L.k, L.v, L.g};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      if (src[i]) e = kda::pad_rows_launch(src[i], w + dst[i], rows, i == 3 ? -30.f : 0.f, cs);
+    float *h0p = h0 ? reinterpret_cast<float *>(w + L.h0) : nullptr;
+    float *dtp = dt_bias ? reinterpret_cast<float *>(w + L.dt) : nullptr;
+    float *hTp = hT ? reinterpret_cast<float *>(w + L.dh0) : nullptr;
+    if (e == cudaSuccess && h0) e = kda::pad_tiles_f32_launch(h0, h0p, nst, 64, 64, 128, 128, false, cs);
+    if (e == cudaSuccess && dt_bias)
+      e = kda::pad_tiles_f32_launch(dt_bias, dtp, shape->H, 1, 64, 1, 128, false, cs);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    st = kda_fwd_states(&ps, w + L.q, w + L.k, w + L.v, w + L.g, beta, A_log, dtp, h0p,
+                        w + L.states, hTp, w, L.inner, stream);
+    if (st != KDA_OK) return st;
+    if (tokens) e = kda::unpack_states64_launch(w + L.states, states, slots_of(shape) * shape->H, cs);
+    if (e == cudaSuccess && hT) e = kda::pad_tiles_f32_launch(hTp, hT, nst, 64, 64, 128, 128, true, cs);
+    return from_cuda(e);
+  }
   if (tc) {
     // the tcgen05 path: the chunk-parallel prep and the forward scan, with
     // the operand blocks in the caller's workspace
@@ -350,8 +387,8 @@ kda_status kda_fwd_states(const kda_shape *shape, const void *q, const void *k, 
     p.prep_mode = kda::kPrepStates;  // the scans' operands only
     return from_cuda(forward_states_tc(p, shape, w, tm, cs));
   }
-  // other dtypes and head sizes: the per-band scan (row-major states; no
-  // workspace)
+  // other dtypes and head sizes (and bf16 K = V = 64 without a workspace):
+  // the per-band scan (row-major states; no workspace)
   p.role_base = 0;
   const int bv = pick_band(shape, 1);
   p.nb = shape->V / bv;
@@ -540,7 +577,11 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
     if (!kda::encode_token_maps(p, tm)) return KDA_ERR_CUDA;
     void *prep = w + prep_offset(shape);
     p.prep = static_cast<const char *>(prep);
+    // chunks whose gate passes the block factors' range are redone exactly
+    // (kda_range.cu) on the tcgen05 scans' path; the per-band scans report them
+    if (!legacy_scan()) p.range_flags = reinterpret_cast<int32_t *>(w + flags_offset(shape));
     e = kda::prep_tc_launch(p, tm, prep, cs);
+    if (e == cudaSuccess) e = kda::range_prep_launch(p, prep, cs);
   }
   mark(1);
   if (e == cudaSuccess && tc_state_path(shape) && !legacy_scan()) {
@@ -585,9 +626,10 @@ kda_status kda_bwd_timed(const kda_shape *shape, const void *q, const void *k, c
 kda_status kda_get_device_status(kda_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KDA_ERR_CUDA;
-  const int words[] = {kda::scan_status_take(), kda::prep_tc_status_take(),
-                       kda::scan_tc_status_take(), kda::grads_status_take(),
-                       kda::grads_tc_status_take(), kda::out_tc_status_take()};
+  const int words[] = {kda::scan_status_take(),     kda::prep_tc_status_take(),
+                       kda::scan_tc_status_take(),  kda::grads_status_take(),
+                       kda::grads_tc_status_take(), kda::out_tc_status_take(),
+                       kda::range_status_take()};
   for (int v : words)
     if (v < 0) return KDA_ERR_CUDA;
   for (int v : words)

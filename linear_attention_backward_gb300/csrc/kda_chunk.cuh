@@ -40,6 +40,14 @@ template <typename E> __device__ __forceinline__ float gate_softplus(float x) {
 }
 
 
+// Mean log-decay per token, on every channel of a chunk, past which the
+// block-factored dg leaves the input type's tolerance (kda_device.cuh): fp32
+// inputs are held to 1e-4 (dg's error measured 1.2e-5 at 4 nats per token,
+// 1.1e-4 at 6), bf16 to 2e-2 (3.5e-3 at 6, 3.1e-2 at 8 on the tcgen05 kernels).
+template <typename E> __host__ __device__ constexpr float sustained_decay_limit() {
+  return std::is_same<E, float>::value ? 5.f : kStrongTokenDecay;
+}
+
 // Bounds of sequence s.  Returns false (and flags the device status) on a
 // malformed cu_seqlens entry.
 __device__ __forceinline__ bool seq_bounds(const KdaParams &p, int s, int64_t &tok0, int &L,
@@ -279,6 +287,10 @@ __device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, cons
   } else {
     check_block_log_decay(fmaxf(-g0[ROWS - 1], -g1[ROWS - 1]));
   }
+  // a channel that decays by at most the sustained-decay limit over the chunk
+  // (below): set by step 3, read after its barrier
+  __shared__ int weak_any;
+  if (tid == 0) weak_any = 0;
   // block partials: Ablk = sum of rows 16I .. 16I+7 (through the reference
   // row), Bblk = rows 16I+8 .. 16I+15
   float *Ablk = sv.part, *Bblk = sv.m;  // [4][K] each (sv.m reused as scratch)
@@ -323,8 +335,14 @@ __device__ void chunk_prep(const KdaParams &p, int h, int len, bool need_q, cons
         sv.F[pair_index(I2, J) * K + e] = gate_exp<E>(d);  // e^(m_I - m_J)
       }
     sv.gT[e] = tot;
+    if (-tot <= sustained_decay_limit<E>() * (float)len) weak_any = 1;
   }
   __syncthreads();
+  // When every channel decays by more than the limit per token, the
+  // block-factored products leave dg (then tiny) outside the tolerance of the
+  // input type (measured on a GB300: fp32 dg error 1.1e-4 at 6 nats per token
+  // on every channel, 6e-2 at 8); these kernels report it as a range error.
+  if (tid == 0 && weak_any == 0 && len > 0) set_status(kStatusGateRange);
   // 4. operand tiles.  gc_i - m_I from the segment's local sums: the
   //    reference row 16I+7 lies in this segment (local index 7) unless the
   //    segment is the second half of its block, where it is the row just

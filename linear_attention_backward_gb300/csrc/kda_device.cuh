@@ -25,11 +25,20 @@ __device__ __forceinline__ void set_status(int code) { atomicCAS(&g_status, 0, c
 // The intra-chunk products carry the gate through 16-row block factors
 // e^(gc_i - m_I) and e^(m_I - gc_j) around each block's reference row (up to
 // 7 and 8 tokens of log-decay).  Past 88 nats such a factor is infinite in
-// fp32 and the gradients cannot be finite: the prep kernels then raise this
+// fp32 and the gradients cannot be finite: the tcgen05 prep flags the chunk
+// for the exact kernels (kda_range.cu), the other prep kernels raise this
 // status code (KDA_ERR_GATE_RANGE) instead of returning them silently.
 // (Below it the factors are finite; sums of them stay finite for ordinary
 // operands: a parity test reaches 85.6 nats.)
 constexpr float kMaxBlockLogDecay = 88.f;
+// The tcgen05 path also flags a chunk in which every channel decays by more
+// than this many nats per token on average over the chunk's rows.  There the
+// true dg is of order e^(-gk) while the block-factored products leave an
+// absolute error of about 1e-5 of the terms that cancel in it (measured on a
+// GB300 with uniform gates: dg's relative error 3.5e-3 at 6 nats per token,
+// 3.1e-2 at 8, 0.16 at 10); with one weaker channel the tensor's dg is
+// carried by that channel and stays accurate.
+constexpr float kStrongTokenDecay = 6.f;
 constexpr int kStatusGateRange = 8;
 __device__ __forceinline__ void check_block_log_decay(float span) {
   if (span > kMaxBlockLogDecay) set_status(kStatusGateRange);

@@ -592,6 +592,7 @@ static cudaError_t launch_grads(const KdaParams &p, const void *states, cudaStre
   if (sizeof(E) == 2 && D == 128 && tm != nullptr &&
       (use_tc_kernel() || p.states_packed || p.dstates_packed)) {
     e = grads_tc_launch(p, *tm, states, st);
+    if (e == cudaSuccess) e = range_grads_launch(p, states, st);  // flagged chunks, exactly
     if (e != cudaSuccess) return e;
   } else {
     auto kfn = kda_grads_kernel<E, D>;

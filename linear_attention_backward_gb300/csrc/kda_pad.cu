@@ -73,6 +73,17 @@ __global__ void kda_pack_states64_kernel(const bf16 *src, uint4 *dst, int64_t n)
   dst[e] = v;
 }
 
+// the reverse: n packed [128][128] states -> their 64 x 64 corners,
+// row-major, one 16-byte piece (8 columns of a row) per thread
+__global__ void kda_unpack_states64_kernel(const uint4 *src, uint4 *dst, int64_t n) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // piece of the output
+  if (e >= n * 512) return;
+  const int64_t t = e >> 9;
+  const int q = (int)(e & 511);
+  const int r = q >> 3, c0 = (q & 7) * 8;
+  dst[e] = src[t * 2048 + ((r >> 3) * 16 + (c0 >> 3)) * 8 + (r & 7)];
+}
+
 unsigned blocks_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
 
 }  // namespace
@@ -107,6 +118,13 @@ cudaError_t pack_states64_launch(const void *src, void *dst, int64_t n, cudaStre
   if (n <= 0) return cudaSuccess;
   kda_pack_states64_kernel<<<blocks_for(n * 2048, 256), 256, 0, st>>>(
       static_cast<const bf16 *>(src), static_cast<uint4 *>(dst), n);
+  return cudaGetLastError();
+}
+
+cudaError_t unpack_states64_launch(const void *src, void *dst, int64_t n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  kda_unpack_states64_kernel<<<blocks_for(n * 512, 256), 256, 0, st>>>(
+      static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n);
   return cudaGetLastError();
 }
 

@@ -54,6 +54,10 @@ struct KdaParams {
   // included; kPrepReadout (1) also QE^T and scale * Mqk, which the forward
   // read-out needs; kPrepStates (2) nothing more (the chunk states alone).
   uint32_t prep_mode;
+  // [slots, H] flags of the chunks whose gate passes the 16-row block
+  // factors' range (kda_range.cu), written by the tcgen05 prep kernel for
+  // every (chunk slot, head); null: such chunks raise KDA_ERR_GATE_RANGE.
+  int32_t *range_flags;
 };
 
 constexpr uint32_t kPrepAll = 0, kPrepReadout = 1, kPrepStates = 2;
@@ -135,6 +139,15 @@ cudaError_t scan_tc_cp_launch(KdaParams p, const TokenMaps &tm, const void *prep
 cudaError_t seq_order_launch(const int32_t *cu, int num_seqs, int32_t *order, cudaStream_t st);
 int scan_tc_status_take();
 
+// kda_range.cu: exact fp32 arithmetic for the chunks p.range_flags marks
+// (no-ops without flags).  range_prep_launch after prep_tc_launch (the scans'
+// operands, and the read-out's by p.prep_mode), range_grads_launch after
+// grads_tc_launch (the chunk's gradient rows and partials; the prep block
+// serves as its scratch).
+cudaError_t range_prep_launch(const KdaParams &p, void *prep, cudaStream_t st);
+cudaError_t range_grads_launch(const KdaParams &p, const void *states, cudaStream_t st);
+int range_status_take();
+
 // kda_out_tc.cu: forward outputs o = QE S_n + Mqk U0 per chunk (bf16, K = V =
 // 128) from the prep blocks and the packed chunk states.
 cudaError_t out_tc_launch(const KdaParams &p, const void *states, void *o, cudaStream_t st);
@@ -157,13 +170,14 @@ int grads_status_take();
 
 // kda_pad.cu: bf16 K = V = 64 on the 128-channel path.  rows x 64 bf16 <->
 // rows x 128 bf16 (padded channels = fill), n fp32 tiles a x b <-> A x B
-// (zero outside), and n row-major 64 x 64 bf16 states -> packed 128 x 128.
+// (zero outside), and n row-major 64 x 64 bf16 states <-> packed 128 x 128.
 cudaError_t pad_rows_launch(const void *src, void *dst, int64_t rows, float fill,
                             cudaStream_t st);
 cudaError_t unpad_rows_launch(const void *src, void *dst, int64_t rows, cudaStream_t st);
 cudaError_t pad_tiles_f32_launch(const float *src, float *dst, int64_t n, int a, int b, int A,
                                  int B, bool unpad, cudaStream_t st);
 cudaError_t pack_states64_launch(const void *src, void *dst, int64_t n, cudaStream_t st);
+cudaError_t unpack_states64_launch(const void *src, void *dst, int64_t n, cudaStream_t st);
 
 // kda_grads_tc.cu: the same per-chunk gradients on tcgen05 (bf16, K = V = 128).
 cudaError_t grads_tc_launch(const KdaParams &p, const TokenMaps &tm, const void *states,

@@ -72,7 +72,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int s_, j_, len;
   int64_t tok0;
-  if (!slot_owner(p, slot, s_, j_, tok0, len)) return;  // padding slot: never read
+  if (!slot_owner(p, slot, s_, j_, tok0, len)) {  // padding slot: never read
+    if (tid == 0 && p.range_flags != nullptr) p.range_flags[slot * H + h] = 0;
+    return;
+  }
   char *unit = prep + ((size_t)slot * H + h) * kPrepUnitBytes;
   // the gate's per-head scale and per-channel bias, loaded now (first used
   // after the raw rows have landed, so their latency hides behind that wait)
@@ -88,6 +91,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   uint64_t *rbar = mbar + 1;  // TMA boxes of the raw q, k, g rows
   uint64_t *vbar = mbar + 2;  // TMA boxes of the v rows
   uint32_t *tslot = reinterpret_cast<uint32_t *>(mbar + 3);
+  int *far_s = reinterpret_cast<int *>(tslot + 1);  // a channel passes the block range
+  int *weak_s = far_s + 1;  // a live channel decays by at most kStrongTokenDecay per token
+  // live channels (a nonzero key row in the chunk; a zero-padded channel is not):
+  // word 2 q + o, bit l = channel 64 q + 2 l + o
+  uint32_t *live_s = reinterpret_cast<uint32_t *>(weak_s + 1);
   char *QM = smem + SM::o_QM, *KM = smem + SM::o_KM, *KP = smem + SM::o_KP;
   char *Mqk = KP;
   char *Vt = smem + SM::o_V;
@@ -107,6 +115,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     umma::mbar_init(mbar, 1);
     umma::mbar_init(rbar, 1);
     umma::mbar_init(vbar, 1);
+    *far_s = 0;
+    *weak_s = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) live_s[w] = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     umma::mbar_expect_tx(rbar, 3 * 16384u);
     umma::mbar_expect_tx(vbar, 16384u);
@@ -173,16 +185,36 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       g0[r] = run0;
       g1[r] = run1;
     }
-    // log-decay around the block's reference row (row 7): rows 0..7 and 8..15
-    check_block_log_decay(fmaxf(fmaxf(g0[0] - g0[7], g0[7] - g0[15]),
-                                fmaxf(g1[0] - g1[7], g1[7] - g1[15])));
+    // log-decay around the block's reference row (row 7): rows 0..7 and 8..15.
+    // Past the range the chunk is flagged for the exact kernels of
+    // kda_range.cu (or, without a flag array, reported)
+    const float span = fmaxf(fmaxf(g0[0] - g0[7], g0[7] - g0[15]),
+                             fmaxf(g1[0] - g1[7], g1[7] - g1[15]));
+    if (p.range_flags == nullptr) check_block_log_decay(span);
+    else if (span > kMaxBlockLogDecay) atomicOr(far_s, 1);
+    {
+      uint32_t any = 0u;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) any |= kraw[r];
+      // this warp's lanes hold channels 64 (warp & 1) + 2 lane (+ 1)
+      const uint32_t m0 = __ballot_sync(0xffffffffu, (any & 0xffffu) != 0u);
+      const uint32_t m1 = __ballot_sync(0xffffffffu, (any >> 16) != 0u);
+      if (lane == 0) {
+        atomicOr(live_s + 2 * (warp & 1), m0);
+        atomicOr(live_s + 2 * (warp & 1) + 1, m1);
+      }
+    }
     float *Ablk = sv.part, *Bblk = sv.m;
     Ablk[I * D + c] = g0[7];
     Ablk[I * D + c + 1] = g1[7];
     Bblk[I * D + c] = g0[15] - g0[7];
     Bblk[I * D + c + 1] = g1[15] - g1[7];
   }
-  if (__syncthreads_or(!ok)) { ok = false; goto drain; }
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0 && p.range_flags != nullptr) p.range_flags[slot * H + h] = *far_s;
+    ok = false;
+    goto drain;
+  }
   {
   if (tid < CHUNK) {  // row norms: block I's rows live in warps 2I, 2I + 1
     const int ib = tid >> 4, r = tid & 15;
@@ -219,8 +251,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
     reinterpret_cast<float *>(unit + kPrepGT)[e] = tot;
     sv.gT[e] = tot;
+    const bool live = (live_s[2 * (e >> 6) + (e & 1)] >> ((e & 63) >> 1)) & 1u;
+    if (live && -tot <= kStrongTokenDecay * (float)len) atomicOr(weak_s, 1);
   }
   __syncthreads();
+  // the chunk goes to the exact kernels if a channel passes the block range,
+  // or if every live channel decays strongly (kda_device.cuh)
+  if (tid == 0 && p.range_flags != nullptr)
+    p.range_flags[slot * H + h] = (*far_s != 0 || *weak_s == 0) ? 1 : 0;
   // the block factors and the row norms for the gradient kernel (one 8 KB span
   // of the view: e^(m_I), e^(gT - m_I), e^(m_I - m_J), gT, 1/|q|, 1/|k|)
   static_assert(19 * D + 128 - 4 * D == kPrepSVBytes / 4, "factor span");

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_strings(L):
-    assert L.kda_abi_version() == 6
+    assert L.kda_abi_version() == 7
     for st in range(9):
         assert len(L.kda_status_str(st)) > 0
 
@@ -58,10 +58,13 @@ def test_slots_and_workspace(L):
     sb = (sb + 255) // 256 * 256
     assert kda.workspace_dstates_offset(s) == sb
     # states, dS, dA_log and ddt_bias partials and (bf16, K = V = 128) the
-    # per-chunk operand blocks of the tcgen05 path: 107008 bytes per (slot, head)
+    # per-chunk operand blocks of the tcgen05 path, 107008 bytes per (slot,
+    # head), and its range flags, 4 bytes per (slot, head)
     prep = (6 * 3 * 107008 + 255) // 256 * 256
     ddt = (6 * 3 * 128 * 4 + 255) // 256 * 256
-    assert kda.workspace_bytes(s) == 2 * sb + ((6 * 3 * 4 + 255) // 256) * 256 + ddt + prep
+    flags = (6 * 3 * 4 + 255) // 256 * 256
+    assert kda.workspace_bytes(s) == (2 * sb + ((6 * 3 * 4 + 255) // 256) * 256 + ddt + prep
+                                      + flags)
     v = _shape(B=1, T=300, num_seqs=4, cu_seqlens=0x1000)
     assert kda.num_chunk_slots(v) == 300 // 64 + 4
     assert kda.scan_segments(v) == 0 and kda.scan_segments(s) == 0
@@ -71,7 +74,8 @@ def test_slots_and_workspace(L):
     r = lambda x: (x + 255) // 256 * 256
     n = (5507 // 64 + 5) * 3
     assert kda.workspace_bytes(v) == (2 * r(n * 128 * 128 * 2) + r(n * 4) + r(n * 128 * 4)
-                                      + r(n * 107008) + r(5 * 3 * 8 * 128 * 128 * 4))
+                                      + r(n * 107008) + r(5 * 3 * 8 * 128 * 128 * 4)
+                                      + r(n * 4))
     f = _shape(K=64, V=64, dtype=kda.KDA_FP32, T=64, B=1)
     assert kda.workspace_dstates_offset(f) == 1 * 3 * 64 * 64 * 4
     sf = 1 * 3 * 64 * 64 * 4
@@ -85,13 +89,13 @@ def test_slots_and_workspace(L):
     assert kda.scan_segments(c) == 4
     n = 16 * 3
     base = 2 * r(n * 128 * 128 * 2) + r(n * 4) + r(n * 128 * 4) + r(n * 107008)
-    assert kda.workspace_bytes(c) == base + r(3 * 8 * 128 * 128 * 4)
+    assert kda.workspace_bytes(c) == base + r(3 * 8 * 128 * 128 * 4) + r(n * 4)
     # 15 chunks allow 3 segments (5 tiles); varlen shapes use whole-sequence chains
     c = _shape(B=1, T=960)
     assert kda.scan_segments(c) == 3
     n = 15 * 3
     base = 2 * r(n * 128 * 128 * 2) + r(n * 4) + r(n * 128 * 4) + r(n * 107008)
-    assert kda.workspace_bytes(c) == base + r(3 * 5 * 128 * 128 * 4)
+    assert kda.workspace_bytes(c) == base + r(3 * 5 * 128 * 128 * 4) + r(n * 4)
 
 
 @pytest.mark.parametrize("kw,code", [

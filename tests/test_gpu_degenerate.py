@@ -2,10 +2,13 @@
 no tokens at all, beta = 0 (no writes: the state only decays), all-zero
 query / key rows (the L2 norm's epsilon carries them), no decay (the gate
 saturates at zero: the plain delta rule), heavy decay inside the range the
-16-row block factors cover, and a gate beyond it (reported by the status
-word).  Tolerances as for the other bf16 parity tests: 2e-2 per-tensor
+16-row block factors cover, and, for fp32 inputs, a gate beyond it
+(reported by the status word; bf16 takes it exactly, test_gpu_gate_range.py).
+Tolerances as for the other bf16 parity tests: 2e-2 per-tensor
 relative L2 against the fp64 oracle (absolute L2 where the oracle's tensor
 is exactly zero)."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -121,23 +124,40 @@ def test_heavy_decay_inside_the_block_range():
     _compare(g, ref, GRADS)
 
 
-@pytest.mark.parametrize("dtype,K", [("bf16", 128), ("bf16", 64), ("fp32", 64)])
-def test_gate_beyond_block_range_is_reported(dtype, K):
+def test_gate_beyond_block_range_is_reported_fp32():
     # g = +20 on a run of tokens of one sequence, e^A_log >= 1: over 20 nats of
     # log-decay per token, far beyond the 88 nats around a 16-row block's
-    # reference row that the block factors hold in fp32.  The call is flagged (KDA_ERR_GATE_RANGE)
-    # instead of returning non-finite values silently; the next valid call is
-    # clean.
-    w = wl.custom("gr", B=2, T=130, H=2, K=K, V=K, dtype=dtype)
+    # reference row that the block factors hold in fp32.  fp32 inputs run the
+    # mma.sync / SIMT kernels, which have no exact counterpart: the call is
+    # flagged (KDA_ERR_GATE_RANGE) instead of returning non-finite values
+    # silently, and the next valid call is clean.
+    w = wl.custom("gr", B=2, T=130, H=2, K=64, V=64, dtype="fp32")
     x = wl.make_inputs(w, seed=45)
     x["g"][1, 20:40] = 20.0
     gpu_bwd(x)
     assert kda.get_device_status() == 8
-    if dtype == "bf16" and K == 128:
-        d = {n: (t.cuda() if t is not None else None) for n, t in x.items()}
-        kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["h0"])
-        assert kda.get_device_status() == 8
     g, _ = gpu_bwd(wl.make_inputs(w, seed=46))
     assert kda.get_device_status() == 0
     for k in GRADS:
         assert torch.isfinite(g[k]).all(), k
+
+
+def test_sustained_strong_decay_is_reported_fp32():
+    # every channel decays by 8 nats per token (A_log = 0, dt_bias =
+    # softplus^-1(8)): inside the 88-nat block range, but the block-factored
+    # dg (of order e^-8) would miss the fp32 bound, so the fp32 kernels report
+    # the range error; at 3 nats per token the same call is clean
+    w = wl.custom("sd", B=1, T=130, H=2, K=64, V=64, dtype="fp32", with_h0=True, with_dhT=True)
+    for d, status in ((8.0, 8), (3.0, 0)):
+        x = wl.make_inputs(w, seed=47)
+        x["A_log"] = torch.zeros(2)
+        x["dt_bias"] = torch.full((2, 64), d + math.log1p(-math.exp(-d)))
+        g, _ = gpu_bwd(x)
+        assert kda.get_device_status() == status, d
+        if status == 0:  # the fp32 bound, 1e-4
+            ref = oracle_bwd(x)
+            for k in GRADS:
+                if k != "dA_log":
+                    got = g[k].double().cpu().numpy().reshape(ref[k].shape)
+                    assert rel_l2(got, ref[k]) <= 1e-4, k
+
