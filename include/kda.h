@@ -100,10 +100,10 @@ typedef enum {
                               only: the device found a channel whose gate log-decay over
                               the 7 or 8 tokens on either side of a 16-row block's
                               reference row exceeds 88 nats, where the block factors e^x
-                              leave the fp32 range, or a chunk in which every channel
-                              decays by more than 5 nats per token (6 for bf16), where
-                              the block-factored dg misses the tolerance; the outputs of
-                              that call are not valid.  bf16 inputs take such chunks
+                              leave the fp32 range, or (kda_bwd) a chunk in which every
+                              channel decays by more than 5 nats per token (6 for bf16),
+                              where the block-factored dg misses the tolerance; the
+                              outputs of that call are not valid.  bf16 inputs take such chunks
                               through exact kernels (one exponential per row pair)
                               instead */
 } kda_status;

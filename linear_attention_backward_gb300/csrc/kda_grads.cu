@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
     tl.KD = BIG2 + 64 * LD;
     tl.KR = KRt;
     tl.Et = Eg;
-    chunk_prep<E, D>(p, h, len, true, Qr, Kr, Gr, sv, tl);
+    chunk_prep<E, D>(p, h, len, true, Qr, Kr, Gr, sv, tl, true);
   }
   intra_pairs<E, D>(BIG1, BIG1 + 64 * LD, BIG2, sv.F, G, 68, MQK, LDS, scale);
   __syncthreads();

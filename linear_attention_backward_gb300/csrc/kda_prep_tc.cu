@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const float span = fmaxf(fmaxf(g0[0] - g0[7], g0[7] - g0[15]),
                              fmaxf(g1[0] - g1[7], g1[7] - g1[15]));
     if (p.range_flags == nullptr) check_block_log_decay(span);
-    else if (span > kMaxBlockLogDecay) atomicOr(far_s, 1);
+    else if (span > kMaxBlockLogDecay) *far_s = 1;
     {
       uint32_t any = 0u;
 #pragma unroll
@@ -252,13 +252,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     reinterpret_cast<float *>(unit + kPrepGT)[e] = tot;
     sv.gT[e] = tot;
     const bool live = (live_s[2 * (e >> 6) + (e & 1)] >> ((e & 63) >> 1)) & 1u;
-    if (live && -tot <= kStrongTokenDecay * (float)len) atomicOr(weak_s, 1);
+    if (live && -tot <= kStrongTokenDecay * (float)len) *weak_s = 1;  // (same value from all)
   }
   __syncthreads();
   // the chunk goes to the exact kernels if a channel passes the block range,
   // or if every live channel decays strongly (kda_device.cuh)
-  if (tid == 0 && p.range_flags != nullptr)
-    p.range_flags[slot * H + h] = (*far_s != 0 || *weak_s == 0) ? 1 : 0;
+  if (tid == 0) {
+    if (p.range_flags != nullptr)
+      p.range_flags[slot * H + h] = (*far_s != 0 || *weak_s == 0) ? 1 : 0;
+    else if (*weak_s == 0)  // (only the backward runs without flags)
+      set_status(kStatusGateRange);
+  }
   // the block factors and the row norms for the gradient kernel (one 8 KB span
   // of the view: e^(m_I), e^(gT - m_I), e^(m_I - m_J), gT, 1/|q|, 1/|k|)
   static_assert(19 * D + 128 - 4 * D == kPrepSVBytes / 4, "factor span");

@@ -16,7 +16,7 @@ import torch
 import __graft_entry__
 import linear_attention_backward_gb300 as kda
 from linear_attention_backward_gb300 import workloads as wl
-from kda_testutil import GRADS, gpu_bwd, oracle_bwd, rel_l2
+from kda_testutil import GRADS, gpu_bwd, oracle_bwd, oracle_states, rel_l2, slot_index
 
 pytestmark = pytest.mark.gpu
 
@@ -152,8 +152,16 @@ def test_sustained_strong_decay_is_reported_fp32():
         x = wl.make_inputs(w, seed=47)
         x["A_log"] = torch.zeros(2)
         x["dt_bias"] = torch.full((2, 64), d + math.log1p(-math.exp(-d)))
-        g, _ = gpu_bwd(x)
+        g, dev = gpu_bwd(x)
         assert kda.get_device_status() == status, d
+        # the chunk states alone stay accurate: kda_fwd_states reports nothing
+        states = kda.fwd_states(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                                dev["A_log"], dev["h0"], dt_bias=dev["dt_bias"])
+        torch.cuda.synchronize()
+        assert kda.get_device_status() == 0, d
+        cs, _ = oracle_states(x)
+        slots = np.concatenate(slot_index(x))
+        assert rel_l2(states.double().cpu().numpy()[slots], cs) <= 1e-4, d
         if status == 0:  # the fp32 bound, 1e-4
             ref = oracle_bwd(x)
             for k in GRADS:
