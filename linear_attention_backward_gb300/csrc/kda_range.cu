@@ -51,12 +51,15 @@ namespace rng {
 using namespace tct;
 
 constexpr int D = 128;
-constexpr int NT = 256;
+constexpr int NT = 512;
 constexpr int RS = D + 1;          // row stride of the [64][128] fp32 tiles
 constexpr int PS = CHUNK + 1;      // row stride of the [64][64] fp32 tiles
 constexpr int kRow = CHUNK * RS;   // floats of a [64][128] tile
 constexpr int kPair = CHUNK * PS;  // floats of a [64][64] tile
-static_assert(NT == 4 * CHUNK, "the inverse takes four lanes per column");
+constexpr int RB = CHUNK * D / NT;      // rows per thread, (channel, row block) mappings
+constexpr int CG = CHUNK * D / NT;      // columns per thread, (row, column group) mappings
+constexpr int PB = CHUNK * CHUNK / NT;  // rows per thread, (pair column, row block) mapping
+static_assert(NT == 8 * CHUNK && RB % 8 == 0 && CG % 8 == 0, "the mappings below");
 
 // Shared-memory views common to both kernels.
 struct Basics {
@@ -204,16 +207,17 @@ __device__ void pair_matrices(const Basics &b) {
 }
 
 // T = (I + diag(beta) G)^-1 (unit lower triangular) by forward substitution:
-// column j by lanes 4 (j % 8) .. + 3 of warp j / 8, each dot product split
-// over the four lanes.  Ends with a barrier.
+// column j by lanes 8 (j % 4) .. + 7 of warp j / 4, each dot product split
+// over the eight lanes.  Ends with a barrier.
 __device__ void wy_inverse_exact(const Basics &b) {
-  const int j = threadIdx.x >> 2, part = threadIdx.x & 3;
+  const int j = threadIdx.x >> 3, part = threadIdx.x & 7;
   for (int i = 0; i < CHUNK; ++i) {
     float t = 0.f;
     if (i > j)
-      for (int l = j + part; l < i; l += 4) t = fmaf(b.G[i * PS + l], b.T[l * PS + j], t);
+      for (int l = j + part; l < i; l += 8) t = fmaf(b.G[i * PS + l], b.T[l * PS + j], t);
     t += __shfl_xor_sync(0xffffffffu, t, 1);
     t += __shfl_xor_sync(0xffffffffu, t, 2);
+    t += __shfl_xor_sync(0xffffffffu, t, 4);
     if (part == 0) b.T[i * PS + j] = i < j ? 0.f : (i == j ? 1.f : -b.beta[i] * t);
     __syncwarp();
   }
@@ -256,13 +260,13 @@ __global__ void __launch_bounds__(rng::NT, 1) kda_range_prep_kernel(KdaParams p,
     int64_t tok0;
     if (!slot_owner(p, slot, s_, j_, tok0, len)) return;  // (the prep kernel writes 0 there)
     char *unit = prep + (size_t)u * kPrepUnitBytes;
-    const int tid = threadIdx.x, c = tid & 127, i0 = 32 * (tid >> 7);
+    const int tid = threadIdx.x, c = tid & 127, i0 = RB * (tid >> 7);
     chunk_basics<readout>(p, h, tok0, len, b);
     pair_matrices<readout>(b);
     wy_inverse_exact(b);
     // kr^T [c][i] and gT
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < RB / 8; ++q) {
       float v[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
@@ -290,43 +294,43 @@ __global__ void __launch_bounds__(rng::NT, 1) kda_range_prep_kernel(KdaParams p,
       for (int t = 0; t < 8; ++t) b.gc[i * RS + c8 + t] = i < len ? b.beta[i] * x[t] : 0.f;
     }
     __syncthreads();
-    // W = T diag(beta) kd, U0 = T diag(beta) v: thread (channel c, rows i0 .. + 31)
+    // W = T diag(beta) kd, U0 = T diag(beta) v: thread (channel c, rows i0 .. + 15)
     {
-      float w[32], u0[32];
+      float w[RB], u0[RB];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) w[r] = u0[r] = 0.f;
-      for (int j = 0; j < i0 + 32; ++j) {
+      for (int r = 0; r < RB; ++r) w[r] = u0[r] = 0.f;
+      for (int j = 0; j < i0 + RB; ++j) {
         const float kj = b.kh[j * RS + c], vj = b.gc[j * RS + c];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
+        for (int r = 0; r < RB; ++r) {
           const float t = b.T[(i0 + r) * PS + j];  // zero for j > i0 + r
           w[r] = fmaf(t, kj, w[r]);
           u0[r] = fmaf(t, vj, u0[r]);
         }
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < RB / 8; ++q) {
         const uint32_t off = umma::core_off(c, i0 + 8 * q, 64);
         st16_bf(unit + kPrepW + off, w + 8 * q);
         st16_bf(unit + kPrepU0 + off, u0 + 8 * q);
       }
       if (readout)
 #pragma unroll
-        for (int r = 0; r < 32; ++r) Wf[(i0 + r) * RS + c] = w[r];
+        for (int r = 0; r < RB; ++r) Wf[(i0 + r) * RS + c] = w[r];
     }
     if (readout) {
       __syncthreads();
       // QE = scale (qd - Mq W), and scale * Mq as the packed 64 x 64 tile
-      float qe[32];
+      float qe[RB];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) qe[r] = b.qh[(i0 + r) * RS + c];
-      for (int j = 0; j < i0 + 32; ++j) {
+      for (int r = 0; r < RB; ++r) qe[r] = b.qh[(i0 + r) * RS + c];
+      for (int j = 0; j < i0 + RB; ++j) {
         const float wj = -p.scale * Wf[j * RS + c];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) qe[r] = fmaf(b.Mq[(i0 + r) * PS + j], wj, qe[r]);
+        for (int r = 0; r < RB; ++r) qe[r] = fmaf(b.Mq[(i0 + r) * PS + j], wj, qe[r]);
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < RB / 8; ++q)
         st16_bf(unit + kPrepQE + umma::core_off(c, i0 + 8 * q, 64), qe + 8 * q);
       for (int e8 = tid; e8 < CHUNK * 8; e8 += NT) {
         const int i = e8 >> 3, j0 = (e8 & 7) * 8;
@@ -388,22 +392,22 @@ __global__ void __launch_bounds__(rng::NT, 1)
     chunk_basics<true>(p, h, tok0, len, b);
     pair_matrices<true>(b);
     wy_inverse_exact(b);
-    // ---- X = v - kd S_n: thread (row i, columns v0 .. + 31) ----
+    // ---- X = v - kd S_n: thread (row i, columns v0 .. + 15) ----
     {
-      const int i = tid >> 2, v0 = 32 * (tid & 3);
-      float x[32];
+      const int i = tid >> 3, v0 = CG * (tid & 7);
+      float x[CG];
       if (i < len) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < CG / 8; ++q)
           ld16_bf(static_cast<const bf16 *>(p.v) + (tok0 + i) * rowH + h * D + v0 + 8 * q, x + 8 * q);
       } else {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) x[r] = 0.f;
+        for (int r = 0; r < CG; ++r) x[r] = 0.f;
       }
       for (int c = 0; c < D; ++c) {
         const float kd = b.kh[i * RS + c] * __expf(b.gc[i * RS + c]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < CG / 8; ++q) {
           float s8[8];
           state_row8(Sb, c, v0 + 8 * q, s8);
 #pragma unroll
@@ -411,39 +415,39 @@ __global__ void __launch_bounds__(rng::NT, 1)
         }
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
+      for (int q = 0; q < CG / 4; ++q)
         reinterpret_cast<float4 *>(X + i * D + v0)[q] =
             make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     }
     if (tid < D) dgTs[tid] *= __expf(b.gT[tid]);
     __syncthreads();
-    // ---- U = T diag(beta) X: thread (column v, rows i0 .. + 31) ----
+    // ---- U = T diag(beta) X: thread (column v, rows i0 .. + 15) ----
     {
-      const int v = tid & 127, i0 = 32 * (tid >> 7);
-      float uu[32];
+      const int v = tid & 127, i0 = RB * (tid >> 7);
+      float uu[RB];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) uu[r] = 0.f;
-      for (int j = 0; j < i0 + 32; ++j) {
+      for (int r = 0; r < RB; ++r) uu[r] = 0.f;
+      for (int j = 0; j < i0 + RB; ++j) {
         const float xj = b.beta[j] * X[j * D + v];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) uu[r] = fmaf(b.T[(i0 + r) * PS + j], xj, uu[r]);
+        for (int r = 0; r < RB; ++r) uu[r] = fmaf(b.T[(i0 + r) * PS + j], xj, uu[r]);
       }
 #pragma unroll
-      for (int r = 0; r < 32; ++r) U[(i0 + r) * D + v] = uu[r];
+      for (int r = 0; r < RB; ++r) U[(i0 + r) * D + v] = uu[r];
     }
     __syncthreads();
     copy16(Sb, dSg, D * D / 8);  // S_n is no longer read until it is copied back
     __syncthreads();
     // ---- dU = s Mq^T dO + kr dS_{n+1} (into dY's tile): thread (row i, columns v0 ..) ----
     {
-      const int i = tid >> 2, v0 = 32 * (tid & 3);
-      float d[32];
+      const int i = tid >> 3, v0 = CG * (tid & 7);
+      float d[CG];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) d[r] = 0.f;
+      for (int r = 0; r < CG; ++r) d[r] = 0.f;
       for (int l = i; l < CHUNK; ++l) {
         const float m = p.scale * b.Mq[l * PS + i];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < CG / 8; ++q) {
           float o8[8];
           ld16_bf(dOs + l * D + v0 + 8 * q, o8);
 #pragma unroll
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(rng::NT, 1)
       for (int c = 0; c < D; ++c) {
         const float kr = b.kh[i * RS + c] * __expf(b.gT[c] - b.gc[i * RS + c]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < CG / 8; ++q) {
           float s8[8];
           state_row8(Sb, c, v0 + 8 * q, s8);
 #pragma unroll
@@ -461,25 +465,25 @@ __global__ void __launch_bounds__(rng::NT, 1)
         }
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
+      for (int q = 0; q < CG / 4; ++q)
         reinterpret_cast<float4 *>(dY + i * D + v0)[q] =
             make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
     }
     __syncthreads();
-    // ---- dY = T^T dU in place: thread (column v, rows i0 .. + 31) ----
+    // ---- dY = T^T dU in place: thread (column v, rows i0 .. + 15) ----
     {
-      const int v = tid & 127, i0 = 32 * (tid >> 7);
-      float y[32];
+      const int v = tid & 127, i0 = RB * (tid >> 7);
+      float y[RB];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) y[r] = 0.f;
+      for (int r = 0; r < RB; ++r) y[r] = 0.f;
       for (int i = i0; i < CHUNK; ++i) {
         const float du = dY[i * D + v];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) y[r] = fmaf(b.T[i * PS + i0 + r], du, y[r]);  // T_ij = 0, j > i
+        for (int r = 0; r < RB; ++r) y[r] = fmaf(b.T[i * PS + i0 + r], du, y[r]);  // T_ij = 0, j > i
       }
       __syncthreads();
 #pragma unroll
-      for (int r = 0; r < 32; ++r) dY[(i0 + r) * D + v] = y[r];
+      for (int r = 0; r < RB; ++r) dY[(i0 + r) * D + v] = y[r];
     }
     __syncthreads();
     // ---- dv; U^T into shared memory (over dS_{n+1}, copied back below) ----
@@ -502,19 +506,19 @@ __global__ void __launch_bounds__(rng::NT, 1)
     }
     __syncthreads();
     // ---- the pair gradients: dG over G, dMq over Mq, dA o G over T.  Thread
-    //      (column j, rows 16 iq .. + 15): dA_ij = -dY_i . U_j, dMq_ij = s dO_i . U_j ----
+    //      (column j, rows 8 iq .. + 7): dA_ij = -dY_i . U_j, dMq_ij = s dO_i . U_j ----
     {
       const float *UT = reinterpret_cast<const float *>(Sb);
-      const int j = tid & 63, ib = 16 * (tid >> 6);
-      float a[16], m[16];
+      const int j = tid & 63, ib = PB * (tid >> 6);
+      float a[PB], m[PB];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) a[r] = m[r] = 0.f;
+      for (int r = 0; r < PB; ++r) a[r] = m[r] = 0.f;
       for (int v8 = 0; v8 < D; v8 += 8) {
         float u8[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) u8[t] = UT[(v8 + t) * CHUNK + j];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
+        for (int r = 0; r < PB; ++r) {
           float o8[8];
           ld16_bf(dOs + (ib + r) * D + v8, o8);
           const float4 ya = reinterpret_cast<const float4 *>(dY + (ib + r) * D + v8)[0];
@@ -531,7 +535,7 @@ __global__ void __launch_bounds__(rng::NT, 1)
         }
       }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
+      for (int r = 0; r < PB; ++r) {
         const int i = ib + r;
         if (j <= i) {
           const float dA = j < i ? -a[r] : 0.f;
@@ -555,17 +559,17 @@ __global__ void __launch_bounds__(rng::NT, 1)
     }
     __syncthreads();  // dS_{n+1} has landed
     // ---- dkr = U dS_{n+1}^T (over X), then dqd = s dO S_n^T (over U) and
-    //      dkd = -diag(beta) dY S_n^T (over dY): thread (channel c, rows i0 .. + 31) ----
-    const int c = tid & 127, i0 = 32 * (tid >> 7);
+    //      dkd = -diag(beta) dY S_n^T (over dY): thread (channel c, rows i0 .. + 15) ----
+    const int c = tid & 127, i0 = RB * (tid >> 7);
     {
-      float dkr[32];
+      float dkr[RB];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) dkr[r] = 0.f;
+      for (int r = 0; r < RB; ++r) dkr[r] = 0.f;
       for (int v8 = 0; v8 < D; v8 += 8) {
         float s8[8];
         state_row8(Sb, c, v8, s8);
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
+        for (int r = 0; r < RB; ++r) {
           const float4 ua = reinterpret_cast<const float4 *>(U + (i0 + r) * D + v8)[0];
           const float4 ub = reinterpret_cast<const float4 *>(U + (i0 + r) * D + v8)[1];
           float t = dkr[r];
@@ -582,21 +586,21 @@ __global__ void __launch_bounds__(rng::NT, 1)
       }
       __syncthreads();  // X (read by dbeta) and S's place in shared memory are free
 #pragma unroll
-      for (int r = 0; r < 32; ++r) X[(i0 + r) * D + c] = dkr[r];
+      for (int r = 0; r < RB; ++r) X[(i0 + r) * D + c] = dkr[r];
     }
     copy16(Sb, Sg, D * D / 8);
     __syncthreads();
     // dqd, then dkd (one 32-row accumulator set at a time)
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
-      float acc[32];
+      float acc[RB];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) acc[r] = 0.f;
+      for (int r = 0; r < RB; ++r) acc[r] = 0.f;
       for (int v8 = 0; v8 < D; v8 += 8) {
         float s8[8];
         state_row8(Sb, c, v8, s8);
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
+        for (int r = 0; r < RB; ++r) {
           float x8[8];
           if (pass == 0) {
             ld16_bf(dOs + (i0 + r) * D + v8, x8);
@@ -614,7 +618,7 @@ __global__ void __launch_bounds__(rng::NT, 1)
       }
       __syncthreads();  // pass 0: U is read no more; pass 1: dY is read no more
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
+      for (int r = 0; r < RB; ++r) {
         if (pass == 0) U[(i0 + r) * D + c] = p.scale * acc[r];
         else dY[(i0 + r) * D + c] = -b.beta[i0 + r] * acc[r];
       }
