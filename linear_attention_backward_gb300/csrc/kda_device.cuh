@@ -22,6 +22,12 @@ static __device__ int g_status = 0;
 
 __device__ __forceinline__ void set_status(int code) { atomicCAS(&g_status, 0, code); }
 
+// Programmatic dependent launch: a kernel launched by pdl_launch (kda_params.h)
+// may start while the kernel before it on the stream finishes its last CTAs;
+// it waits here, before it touches anything that kernel writes (a no-op for a
+// kernel launched the ordinary way).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // The intra-chunk products carry the gate through 16-row block factors
 // e^(gc_i - m_I) and e^(m_I - gc_j) around each block's reference row (up to
 // 7 and 8 tokens of log-decay).  Past 88 nats such a factor is infinite in

@@ -544,6 +544,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_grads_kernel(KdaParams p, con
 // fixed order.
 __global__ void kda_dalog_reduce_kernel(const float *part, int64_t nslots, int H, float *dA) {
   __shared__ float red[NWARPS];
+  pdl_wait();  // the gradient kernels' partials
   const int h = blockIdx.x;
   float t = 0.f;
   for (int64_t s = threadIdx.x; s < nslots; s += NTHREADS) t += part[s * H + h];
@@ -605,11 +606,12 @@ static cudaError_t launch_grads(const KdaParams &p, const void *states, cudaStre
     }
   }
   if (after != nullptr) cudaEventRecord(reinterpret_cast<cudaEvent_t>(after), st);
-  kda_dalog_reduce_kernel<<<p.H, NTHREADS, 0, st>>>(p.dA_part, p.nslots, p.H, p.dA_log);
-  if (p.ddt_bias != nullptr && p.H > 0)
+  cudaError_t er = pdl_launch(kda_dalog_reduce_kernel, dim3(p.H), dim3(NTHREADS), 0, st, p.dA_part,
+                              p.nslots, p.H, p.dA_log);
+  if (er == cudaSuccess && p.ddt_bias != nullptr && p.H > 0)
     kda_ddt_reduce_kernel<<<p.H, dim3(D, 1024 / D), 0, st>>>(p.ddt_part, p.nslots, p.H, D,
                                                              p.ddt_bias);
-  return cudaGetLastError();
+  return er != cudaSuccess ? er : cudaGetLastError();
 }
 
 cudaError_t grads_dispatch(const KdaParams &p, int K, bool is_bf16, const void *states,

@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(gtc::NT, 1)
   using namespace gtc;
   using SM = Smem;
   extern __shared__ __align__(1024) char smem[];
+  pdl_wait();  // the scans' states and state gradients
   const int64_t slot = blockIdx.x;
   const int h = blockIdx.y;
   const int H = p.H;
@@ -926,8 +927,8 @@ cudaError_t grads_tc_launch(const KdaParams &p, const TokenMaps &tm, const void 
                                        (int)gtc::Smem::total);
   if (e != cudaSuccess) return e;
   if (p.nslots > 0) {
-    kfn<<<dim3((unsigned)p.nslots, p.H), gtc::NT, gtc::Smem::total, st>>>(p, tm, states);
-    e = cudaGetLastError();
+    e = pdl_launch(kfn, dim3((unsigned)p.nslots, p.H), dim3(gtc::NT), gtc::Smem::total, st, p, tm,
+                   states);
   }
   return e;
 }

@@ -9,6 +9,26 @@
 
 namespace kda {
 
+// Launches kernel(args...) allowed to start while the previous kernel on the
+// stream finishes (programmatic dependent launch); the kernel calls pdl_wait()
+// (kda_device.cuh) before reading anything the previous kernels wrote.  It
+// hides the gap between two dependent launches.
+template <typename... K, typename... A>
+inline cudaError_t pdl_launch(void (*kernel)(K...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 struct KdaParams {
   int B, T, H, num_seqs;
   const int32_t *cu;          // device, nullable

@@ -247,6 +247,7 @@ static_assert((size_t)(kBasicFloats + D + 8) * 4 % 16 == 0, "16-byte aligned sta
 template <uint32_t kMode>
 __global__ void __launch_bounds__(rng::NT, 1) kda_range_prep_kernel(KdaParams p, char *prep) {
   using namespace rng;
+  pdl_wait();  // the prep kernel's flags and operand blocks
   constexpr bool readout = kMode != kPrepStates;
   extern __shared__ __align__(16) float rsm[];
   const Basics b = basics_view(rsm);
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(rng::NT, 1) kda_range_prep_kernel(KdaParams p,
 __global__ void __launch_bounds__(rng::NT, 1)
     kda_range_grads_kernel(KdaParams p, const void *states) {
   using namespace rng;
+  pdl_wait();  // the gradient kernel's rows and partials
   extern __shared__ __align__(16) float rsm[];
   const Basics b = basics_view(rsm);
   float *dgTs = rsm + kBasicFloats;  // [128] e^gT sum_v S dS
@@ -742,8 +744,8 @@ cudaError_t range_prep_launch(const KdaParams &p, void *prep, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)rng::kPrepBytes);
   if (e != cudaSuccess) return e;
-  kfn<<<range_grid(p), rng::NT, rng::kPrepBytes, st>>>(p, static_cast<char *>(prep));
-  return cudaGetLastError();
+  return pdl_launch(kfn, dim3(range_grid(p)), dim3(rng::NT), rng::kPrepBytes, st, p,
+                    static_cast<char *>(prep));
 }
 
 cudaError_t range_grads_launch(const KdaParams &p, const void *states, cudaStream_t st) {
@@ -753,8 +755,8 @@ cudaError_t range_grads_launch(const KdaParams &p, const void *states, cudaStrea
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)rng::kGradBytes);
   if (e != cudaSuccess) return e;
-  kda_range_grads_kernel<<<range_grid(p), rng::NT, rng::kGradBytes, st>>>(p, states);
-  return cudaGetLastError();
+  return pdl_launch(kda_range_grads_kernel, dim3(range_grid(p)), dim3(rng::NT), rng::kGradBytes,
+                    st, p, states);
 }
 
 int range_status_take() {

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   using namespace stc;
   using SM = stc::Smem;
   extern __shared__ __align__(1024) char smem[];
+  pdl_wait();  // the prep kernels' operand blocks
   // the swizzled dO boxes need 1024-byte aligned atoms; the dynamic window of
   // a kernel without static shared memory is, and a launch where it were not
   // records KDA_ERR_CUDA and does nothing rather than issue a misaligned copy
@@ -466,9 +467,8 @@ cudaError_t scan_tc_launch(const KdaParams &p, const TokenMaps &tm, const void *
   const int64_t nunits = (int64_t)(p.cu ? p.num_seqs : p.B) * p.H;
   if (nunits == 0 || nroles == 0) return cudaSuccess;
   if (nroles < 1 || p.role_base + nroles > 2) return cudaErrorInvalidValue;
-  kfn<<<(unsigned)(nunits * nroles), NTHREADS, stc::Smem::total, st>>>(
-      p, tm, static_cast<const char *>(prep));
-  return cudaGetLastError();
+  return pdl_launch(kfn, dim3((unsigned)(nunits * nroles)), dim3(NTHREADS), stc::Smem::total, st,
+                    p, tm, static_cast<const char *>(prep));
 }
 
 // ---------------------------------------------------------------------------
