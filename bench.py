@@ -76,11 +76,11 @@ def launches_per_step(shape, cu, forward=False):
 # kernel sources it was taken from; a changed kernel reports null until it
 # is measured again.
 NCU_TRAFFIC = {
-    # ncu on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read 841.6 MB +
+    # ncu on main_b1_bf16 (B=1: 4096 chunk-heads per launch), DRAM read 841.4 MB +
     # write 244.7 MB (profiles/traffic_main_b1_bf16.md), scaled by 4 to the main
     # workload's 16384 chunk-heads (the kernel's traffic is proportional to them)
-    "kda_grads_tc_kernel": {"sha": "490ae7c8c8a2a3c3", "workload": "main_bf16",
-                            "bytes_per_launch": 4345072640},
+    "kda_grads_tc_kernel": {"sha": "523e956effe5a3d3", "workload": "main_bf16",
+                            "bytes_per_launch": 4344210432},
 }
 
 KERNEL_SOURCES = {
