@@ -96,16 +96,16 @@ typedef enum {
   KDA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
   KDA_ERR_DEVICE_ARG = 6,  /* the device found a bad cu_seqlens table */
   KDA_ERR_TOO_LARGE = 7,   /* kda_bwd_noalloc: problem needs more than its fixed scratch */
-  KDA_ERR_GATE_RANGE = 8   /* fp32 inputs (and the comparison switches of the README)
-                              only: the device found a channel whose gate log-decay over
-                              the 7 or 8 tokens on either side of a 16-row block's
-                              reference row exceeds 88 nats, where the block factors e^x
-                              leave the fp32 range, or (kda_bwd) a chunk in which every
-                              channel decays by more than 5 nats per token (6 for bf16),
-                              where the block-factored dg misses the tolerance; the
-                              outputs of that call are not valid.  bf16 inputs take such chunks
-                              through exact kernels (one exponential per row pair)
-                              instead */
+  KDA_ERR_GATE_RANGE = 8   /* fp32 inputs and the comparison switches (KDA_SCAN_LEGACY,
+                              KDA_GRADS_MMA_SYNC, KDA_PAD64=0) only: the device found a
+                              channel whose gate log-decay over the 7 or 8 tokens on either
+                              side of a 16-row block's reference row exceeds 88 nats, where
+                              the block factors e^x leave the fp32 range, or (kda_bwd) a
+                              chunk in which every channel decays by more than 5 nats per
+                              token (6 for bf16), where the block-factored dg misses the
+                              tolerance; the outputs of that call are not valid.  bf16
+                              inputs take such chunks through exact kernels (one
+                              exponential per row pair) instead */
 } kda_status;
 
 typedef enum { KDA_FP32 = 0, KDA_BF16 = 1 } kda_dtype;
