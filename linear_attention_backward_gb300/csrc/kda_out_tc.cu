@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(otc::NT) kda_out_tc_kernel(KdaParams p, const 
   using namespace otc;
   using SM = otc::Smem;
   extern __shared__ __align__(1024) char smem[];
+  pdl_wait();  // the scan's chunk states
   const int64_t slot = blockIdx.x;
   const int h = blockIdx.y;
   const int H = p.H;
@@ -137,8 +138,8 @@ cudaError_t out_tc_launch(const KdaParams &p, const void *states, void *o, cudaS
                                        (int)otc::Smem::total);
   if (e != cudaSuccess) return e;
   if (p.nslots > 0 && p.H > 0) {
-    kfn<<<dim3((unsigned)p.nslots, p.H), otc::NT, otc::Smem::total, st>>>(p, states, o);
-    e = cudaGetLastError();
+    e = pdl_launch(kfn, dim3((unsigned)p.nslots, p.H), dim3(otc::NT), otc::Smem::total, st, p,
+                   states, o);
   }
   return e;
 }

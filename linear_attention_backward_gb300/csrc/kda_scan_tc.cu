@@ -505,6 +505,7 @@ constexpr int kSinLd = 40;     // row stride (floats) of the staged columns: B f
 __global__ void __launch_bounds__(NTHREADS) kda_cp_combine_kernel(KdaParams p) {
   using namespace stc;
   __shared__ __align__(16) float Sin[D * kSinLd];
+  pdl_wait();  // the first pass's segment boundaries and transfer matrices
   const int P = p.cp_segs;
   const int dir = p.role_base + (int)blockIdx.z;
   const int j0 = (int)blockIdx.y * kCombCols;
@@ -610,21 +611,18 @@ cudaError_t scan_tc_cp_launch(KdaParams p, const TokenMaps &tm, const void *prep
   p.seq_order = nullptr;
   // 1. local segment scans and the inner transfer matrices
   p.cp_phase = 1;
-  kfn<<<(unsigned)(nunits * (roles * (P - 1) + (P - 2))), NTHREADS, stc::Smem::total, st>>>(
-      p, tm, static_cast<const char *>(prep));
-  e = cudaGetLastError();
+  e = pdl_launch(kfn, dim3((unsigned)(nunits * (roles * (P - 1) + (P - 2)))), dim3(NTHREADS),
+                 stc::Smem::total, st, p, tm, static_cast<const char *>(prep));
   if (e != cudaSuccess) return e;
   // 2. the segment boundaries
   p.cp_phase = 2;
-  kda_cp_combine_kernel<<<dim3((unsigned)nunits, stc::D / stc::kCombCols, (unsigned)roles),
-                          NTHREADS, 0, st>>>(p);
-  e = cudaGetLastError();
+  e = pdl_launch(kda_cp_combine_kernel, dim3((unsigned)nunits, stc::D / stc::kCombCols, (unsigned)roles),
+                 dim3(NTHREADS), 0, st, p);
   if (e != cudaSuccess) return e;
   // 3. the remaining segments from their true boundaries
   p.cp_phase = 3;
-  kfn<<<(unsigned)(nunits * roles * (P - 1)), NTHREADS, stc::Smem::total, st>>>(
-      p, tm, static_cast<const char *>(prep));
-  return cudaGetLastError();
+  return pdl_launch(kfn, dim3((unsigned)(nunits * roles * (P - 1))), dim3(NTHREADS),
+                    stc::Smem::total, st, p, tm, static_cast<const char *>(prep));
 }
 
 // rank of sequence s = the number of sequences longer than s, or as long and
