@@ -98,6 +98,25 @@ def test_slots_and_workspace(L):
     assert kda.workspace_bytes(c) == base + r(3 * 5 * 128 * 128 * 4) + r(n * 4)
 
 
+def test_pad64_workspace_layout(L):
+    # bf16 K = V = 64 runs on zero-padded 128-channel copies: the workspace is
+    # the 128-channel shape's own (states, dS, partials, operand blocks, range
+    # flags), then the padded q, k, v, g, dO and dq, dk, dv, dg, h0 / dh_T / dh0
+    # tiles, the gate bias and its gradient, and the padded given states
+    r = lambda x: (x + 255) // 256 * 256
+    B, T, H = 2, 150, 3
+    s = _shape(B=B, T=T, H=H, K=64, V=64)
+    slots = B * ((T + 63) // 64)
+    n = slots * H
+    assert kda.scan_segments(s) == 0  # 3 chunks per sequence: too few to split
+    inner = r(2 * r(n * 128 * 128 * 2) + r(n * 4) + r(n * 128 * 4) + r(n * 107008) + r(n * 4))
+    pads = (9 * r(B * T * H * 128 * 2) + 3 * r(B * H * 128 * 128 * 4) + 2 * r(H * 128 * 4)
+            + r(n * 128 * 128 * 2))
+    assert kda.workspace_bytes(s) == inner + pads
+    # the state gradients sit after the padded shape's states
+    assert kda.workspace_dstates_offset(s) == r(n * 128 * 128 * 2)
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(K=96, V=96), 2), (dict(K=128, V=64), 2), (dict(chunk=32), 2),
     (dict(B=0), 1), (dict(H=0), 1), (dict(T=-1), 1), (dict(dtype=7), 1),
