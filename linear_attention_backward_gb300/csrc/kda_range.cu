@@ -86,7 +86,8 @@ __device__ __forceinline__ Basics basics_view(float *s) {
 
 // Calls f(u) for every flagged unit u = slot * H + h of this CTA's contiguous
 // share of the flag array, taken NT flags at a time.  Every thread calls f
-// the same number of times.
+// the same number of times.  The order within a piece follows the shared
+// atomic and may vary; each unit's results depend on that unit alone.
 template <typename F>
 __device__ __forceinline__ void for_each_flagged(const int32_t *flags, int64_t nunits, int *list,
                                                  int *count, F &&f) {
